@@ -1,0 +1,257 @@
+/*
+ * tq_oracle.c -- plain CPU oracle for the ternary FWHT-128 linear layers.
+ *
+ * TEST INFRASTRUCTURE ONLY: used by the tests, the smoke check and the CPU
+ * baseline leg of the benchmark; never by the product path.  It shares no
+ * code, header, table or constant generator with the CUDA library.
+ *
+ * Every function is the literal definition, one element at a time, in the
+ * order the pages give.  Build with -O2 -ffp-contract=off so that no
+ * multiply-add is fused behind our back (the fp32 results are compared bit
+ * for bit).  Page names are explained in tq_oracle.h.
+ */
+#include "tq_oracle.h"
+
+#include <math.h>
+#include <string.h>
+
+static float bits_to_f32(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t f32_to_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+/* ---------------------------------------------------------------- Hadamard */
+
+/* [dpshk] sec. 2.1: entry (i, j) is -1 to the number of common set bits. */
+int tqo_hadamard_entry(int i, int j) {
+  unsigned v = (unsigned)(i & j);
+  int ones = 0;
+  while (v) { ones += (int)(v & 1u); v >>= 1; }
+  return (ones & 1) ? -1 : 1;
+}
+
+/* [dpshk] sec. 2.1 / [mhpq] sec. 2.2: H_2n = [[H_n, H_n], [H_n, -H_n]]. */
+void tqo_sylvester(int n, int8_t *h) {
+  h[0] = 1;
+  for (int m = 1; m < n; m *= 2) {
+    /* h currently holds H_m in its top-left m x m corner (row stride n). */
+    for (int i = 0; i < m; ++i)
+      for (int j = 0; j < m; ++j) {
+        int8_t v = h[i * n + j];
+        h[i * n + (j + m)] = v;
+        h[(i + m) * n + j] = v;
+        h[(i + m) * n + (j + m)] = (int8_t)(-v);
+      }
+  }
+}
+
+/* The normalisation 1/sqrt(n) for n = 128 ([dpshk] sec. 2.3; [zwxr] sec. 2,
+ * normalised transform), rounded once to fp32. */
+uint32_t tqo_norm_const_bits(void) {
+  float c = (float)(1.0 / sqrt(128.0));
+  return f32_to_bits(c);
+}
+
+/* [xxqk] sec. 2: log2(n) rounds of (a + b, a - b); the round with pair
+ * distance h = 1 comes first and h = 64 last. */
+void tqo_fwht128_f32(const float *in, float *out) {
+  float v[128];
+  for (int i = 0; i < 128; ++i) v[i] = in[i];
+  for (int h = 1; h < 128; h *= 2) {
+    for (int i = 0; i < 128; ++i) {
+      if ((i & h) == 0) {
+        float a = v[i];
+        float b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+    }
+  }
+  float c = bits_to_f32(tqo_norm_const_bits());
+  for (int i = 0; i < 128; ++i) out[i] = v[i] * c;
+}
+
+/* Dense matrix-vector form of the same rotation in fp64. */
+void tqo_fwht128_f64(const double *in, double *out) {
+  double tmp[128];
+  double c = 1.0 / sqrt(128.0);
+  for (int i = 0; i < 128; ++i) {
+    double acc = 0.0;
+    for (int j = 0; j < 128; ++j) acc += (double)tqo_hadamard_entry(i, j) * in[j];
+    tmp[i] = acc * c;
+  }
+  for (int i = 0; i < 128; ++i) out[i] = tmp[i];
+}
+
+/* ------------------------------------------------------------ fp16 / bf16 */
+
+/* IEEE 754 binary32 -> binary16, round to nearest, ties to even. */
+uint16_t tqo_f32_to_f16(float f) {
+  uint32_t x = f32_to_bits(f);
+  uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+  uint32_t bexp = (x >> 23) & 0xffu;
+  uint32_t frac = x & 0x7fffffu;
+  if (bexp == 0xffu) return (uint16_t)(sign | (frac ? 0x7e00u : 0x7c00u));
+  if (bexp == 0) return sign; /* fp32 subnormals are far below half of 2^-24 */
+  int e = (int)bexp - 127;    /* value = m * 2^(e - 23), m has 24 bits */
+  uint32_t m = frac | 0x800000u;
+  if (e >= -14) {
+    /* normal binary16: keep 11 significant bits */
+    uint32_t q = m >> 13, rem = m & 0x1fffu, half = 0x1000u;
+    if (rem > half || (rem == half && (q & 1u))) q += 1;
+    if (q == 0x800u) { q = 0x400u; e += 1; }
+    if (e > 15) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (uint32_t)((e + 15) << 10) | (q & 0x3ffu));
+  }
+  /* subnormal binary16: value in units of 2^-24 is m * 2^(e + 1) */
+  int s = -(e + 1);
+  if (s > 25) return sign;
+  uint32_t q = m >> s, rem = m & ((1u << s) - 1u), half = 1u << (s - 1);
+  if (rem > half || (rem == half && (q & 1u))) q += 1;
+  return (uint16_t)(sign | q); /* q == 0x400 becomes the smallest normal */
+}
+
+float tqo_f16_to_f32(uint16_t h) {
+  uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+  uint32_t e = (h >> 10) & 0x1fu;
+  uint32_t frac = h & 0x3ffu;
+  if (e == 0x1fu) return bits_to_f32(sign | 0x7f800000u | (frac << 13));
+  if (e == 0) {
+    /* zero or subnormal: frac * 2^-24, exact in fp32 */
+    float v = (float)frac * 5.9604644775390625e-08f;
+    return sign ? -v : v;
+  }
+  return bits_to_f32(sign | ((e - 15 + 127) << 23) | (frac << 13));
+}
+
+float tqo_bf16_to_f32(uint16_t b) { return bits_to_f32((uint32_t)b << 16); }
+
+/* ------------------------------------------------------------ quantiser */
+
+/* [mhpq] sec. 1.1: scale = group mean of |w|; divide; round; clip to
+ * {-1, 0, 1}.  [mhpq] sec. 1.3: one fp16 scale per 128 weights. */
+uint16_t tqo_quantize_group(const float *wrot, int8_t *t) {
+  float s[128];
+  for (int i = 0; i < 128; ++i) s[i] = fabsf(wrot[i]);
+  for (int h = 64; h >= 1; h /= 2)
+    for (int i = 0; i < h; ++i) s[i] = s[i] + s[i + h];
+  float mean = s[0] * 0.0078125f; /* * 2^-7 */
+  uint16_t sbits = tqo_f32_to_f16(mean);
+  float sc = tqo_f16_to_f32(sbits);
+  for (int i = 0; i < 128; ++i) {
+    if (sc == 0.0f) { t[i] = 0; continue; }
+    float q = wrot[i] / sc;
+    float r = nearbyintf(q); /* default rounding mode: ties to even */
+    t[i] = (int8_t)(r > 1.0f ? 1 : (r < -1.0f ? -1 : (int)r));
+  }
+  return sbits;
+}
+
+static void load_group(const void *W, int wt, int64_t row, int64_t ldw, int64_t k0, float *dst) {
+  if (wt == 0) {
+    const float *w = (const float *)W + row * ldw + k0;
+    for (int i = 0; i < 128; ++i) dst[i] = w[i];
+  } else {
+    const uint16_t *w = (const uint16_t *)W + row * ldw + k0;
+    for (int i = 0; i < 128; ++i) dst[i] = tqo_bf16_to_f32(w[i]);
+  }
+}
+
+void tqo_quantize_rows(const void *W, int wt, int64_t K, int64_t ldw,
+                       const int64_t *rows, int64_t nrows, int8_t *T, uint16_t *S) {
+  int64_t G = K / 128;
+  float grp[128], rot[128];
+  for (int64_t r = 0; r < nrows; ++r) {
+    int64_t n = rows ? rows[r] : r;
+    for (int64_t g = 0; g < G; ++g) {
+      load_group(W, wt, n, ldw, g * 128, grp);
+      tqo_fwht128_f32(grp, rot);
+      S[r * G + g] = tqo_quantize_group(rot, T + r * K + g * 128);
+    }
+  }
+}
+
+void tqo_quantize_matrix(const void *W, int wt, int64_t N, int64_t K, int64_t ldw,
+                         int8_t *T, uint16_t *S) {
+  tqo_quantize_rows(W, wt, K, ldw, 0, N, T, S);
+}
+
+/* ------------------------------------------------------------ packing */
+
+/* [mhpq] sec. 3.1: two bits per weight, aligned and quick to decode. */
+void tqo_pack2(const int8_t *T, int64_t N, int64_t K, uint8_t *codes, int64_t ld2) {
+  for (int64_t n = 0; n < N; ++n) {
+    uint8_t *row = codes + n * ld2;
+    for (int64_t j = 0; j < ld2; ++j) row[j] = 0;
+    for (int64_t k = 0; k < K; ++k) {
+      unsigned code = (unsigned)(T[n * K + k] + 1);
+      row[k / 4] = (uint8_t)(row[k / 4] | (code << (2 * (k % 4))));
+    }
+  }
+}
+
+void tqo_unpack2(const uint8_t *codes, int64_t ld2, int64_t N, int64_t K, int8_t *T) {
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k) {
+      unsigned code = (codes[n * ld2 + k / 4] >> (2 * (k % 4))) & 3u;
+      T[n * K + k] = (int8_t)((int)code - 1);
+    }
+}
+
+int64_t tqo_ld3(int64_t K) {
+  int64_t nb = (K + 4) / 5;
+  return (nb + 15) / 16 * 16;
+}
+
+/* five base-3 digits per byte (3^5 = 243 <= 256), lowest K first */
+void tqo_pack3(const int8_t *T, int64_t N, int64_t K, uint8_t *codes, int64_t ld3) {
+  int64_t nb = (K + 4) / 5;
+  for (int64_t n = 0; n < N; ++n) {
+    uint8_t *row = codes + n * ld3;
+    for (int64_t j = 0; j < ld3; ++j) row[j] = 0;
+    for (int64_t j = 0; j < nb; ++j) {
+      unsigned v = 0, p = 1;
+      for (int i = 0; i < 5; ++i) {
+        int64_t k = 5 * j + i;
+        unsigned d = (k < K) ? (unsigned)(T[n * K + k] + 1) : 1u;
+        v += d * p;
+        p *= 3;
+      }
+      row[j] = (uint8_t)v;
+    }
+  }
+}
+
+void tqo_unpack3(const uint8_t *codes, int64_t ld3, int64_t N, int64_t K, int8_t *T) {
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k) {
+      unsigned v = codes[n * ld3 + k / 5];
+      for (int i = 0; i < (int)(k % 5); ++i) v /= 3;
+      T[n * K + k] = (int8_t)((int)(v % 3) - 1);
+    }
+}
+
+/* ------------------------------------------------------------ GEMV */
+
+/* y = sum over groups of scale * (sum of t * x'), in fp64, where x' is the
+ * activation rotated by the same block transform ([mhpq] sec. 2.3, rotation
+ * absorbed on the activation side; [zwxr] activation-side Hadamard). */
+void tqo_gemv_f64(const int8_t *T, const uint16_t *S, int64_t N, int64_t K,
+                  const float *x, int64_t M, const int64_t *rows, int64_t nrows,
+                  double *y) {
+  int64_t G = K / 128;
+  int64_t nout = rows ? nrows : N;
+  double blk[128], rot[128];
+  (void)N;
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t r = 0; r < nout; ++r) y[m * nout + r] = 0.0;
+    for (int64_t g = 0; g < G; ++g) {
+      for (int i = 0; i < 128; ++i) blk[i] = (double)x[m * K + g * 128 + i];
+      tqo_fwht128_f64(blk, rot);
+      for (int64_t r = 0; r < nout; ++r) {
+        const int8_t *t = T + r * K + g * 128;
+        double part = 0.0;
+        for (int i = 0; i < 128; ++i) part += (double)t[i] * rot[i];
+        y[m * nout + r] += (double)tqo_f16_to_f32(S[r * G + g]) * part;
+      }
+    }
+  }
+}

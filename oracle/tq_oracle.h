@@ -1,0 +1,97 @@
+/*
+ * tq_oracle.h -- plain, slow, single-threaded CPU oracle for the ternary
+ * FWHT-128 linear-layer path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this code; only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark do.  It shares no code with the CUDA library.
+ *
+ * Pages cited (no page carries a title, so each is named by its address):
+ *   [mhpq]  mhpq.cn/news/1159370  -- "Ternary Bonsai 2 27B" seen from TensorSharp
+ *   [dpshk] dpshk.com/news/5289456
+ *   [xxqk]  xxqk.cn/news/652513
+ *   [zwxr]  zwxr.cn/news/303439
+ *
+ * Conventions: a weight matrix W is row-major [N][K] (out x in), an
+ * activation matrix x is row-major [M][K], y is [M][N].  A "group" is 128
+ * consecutive K indices of one row; G = K/128.  K must be a multiple of 128.
+ */
+#ifndef TQ_ORACLE_H
+#define TQ_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* H[i][j] = (-1)^popcount(i & j)   ([dpshk] sec. 2.1). Returns +1 or -1. */
+int tqo_hadamard_entry(int i, int j);
+
+/* Sylvester construction H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]]
+ * ([dpshk] sec. 2.1; [mhpq] sec. 2.2), written into h[n*n] (n a power of 2,
+ * n <= 128).  Independent of tqo_hadamard_entry; used to cross-check it. */
+void tqo_sylvester(int n, int8_t *h);
+
+/* fp32 constant c = RN_fp32(1/sqrt(128)); the bits are returned. */
+uint32_t tqo_norm_const_bits(void);
+
+/* 128-point FWHT in fp32, staged butterflies h = 1, 2, 4, ..., 64, each
+ * stage mapping (a, b) -> (a + b, a - b) for every pair (i, i + h) with
+ * (i & h) == 0, then one multiply of every element by c
+ * ([xxqk] sec. 2, butterfly rounds; [mhpq] sec. 2.2).  in and out may alias. */
+void tqo_fwht128_f32(const float *in, float *out);
+
+/* Dense 128-point transform in fp64: out[i] = sum_j H[i][j] in[j] / sqrt(128),
+ * H from the popcount definition.  Reference-quality rotation for y. */
+void tqo_fwht128_f64(const double *in, double *out);
+
+/* binary16 <-> binary32, round-to-nearest-even, written from the IEEE 754
+ * formats (no tables, no hardware conversion). */
+uint16_t tqo_f32_to_f16(float f);
+float tqo_f16_to_f32(uint16_t h);
+
+/* bfloat16 bits -> fp32 (exact widening). */
+float tqo_bf16_to_f32(uint16_t b);
+
+/* absmean ternarisation of one rotated group of 128 values ([mhpq] sec. 1.1,
+ * 1.3):  sum |w'| by the halving tree (s[i] += s[i + h] for h = 64 .. 1, in
+ * fp32), mean = sum * 2^-7, scale = fp16_RN(mean),
+ * t = clamp(rint(w' / fp32(scale)), -1, 1) with IEEE fp32 division and
+ * round-half-even; t = 0 throughout when scale == 0.  Returns the fp16 scale
+ * bits; writes 128 trits. */
+uint16_t tqo_quantize_group(const float *wrot, int8_t *t);
+
+/* Whole matrix: for each row and each group, FWHT-128 in fp32, then
+ * tqo_quantize_group.  W is fp32 (wt == 0) or bf16 bits (wt == 1), leading
+ * dimension ldw elements.  T is [N][K] trits, S is [N][G] fp16 bits. */
+void tqo_quantize_matrix(const void *W, int wt, int64_t N, int64_t K, int64_t ldw,
+                         int8_t *T, uint16_t *S);
+
+/* Same, for a list of rows only (T and S hold nrows rows). */
+void tqo_quantize_rows(const void *W, int wt, int64_t K, int64_t ldw,
+                       const int64_t *rows, int64_t nrows, int8_t *T, uint16_t *S);
+
+/* 2-bit packing: code = t + 1 in bits 2*(k % 4) of byte k / 4 of the row;
+ * rows ld2 bytes apart (ld2 >= K/4). */
+void tqo_pack2(const int8_t *T, int64_t N, int64_t K, uint8_t *codes, int64_t ld2);
+void tqo_unpack2(const uint8_t *codes, int64_t ld2, int64_t N, int64_t K, int8_t *T);
+
+/* base-3 packing, five trits per byte: byte j of a row is
+ * sum_{i=0..4} (t[5j+i] + 1) * 3^i; trits past K count as t = 0 (digit 1);
+ * bytes from ceil(K/5) up to ld3 are 0. */
+int64_t tqo_ld3(int64_t K);  /* ceil(K/5) rounded up to a multiple of 16 */
+void tqo_pack3(const int8_t *T, int64_t N, int64_t K, uint8_t *codes, int64_t ld3);
+void tqo_unpack3(const uint8_t *codes, int64_t ld3, int64_t N, int64_t K, int8_t *T);
+
+/* y[m][n] = sum_g s[n][g] * sum_{k in g} t[n][k] * x'[m][k]  in fp64, where
+ * x' is the fp64 dense rotation of the fp32 (bf16-exact) activations x.
+ * rows == NULL means all N rows; else y is [M][nrows] for those rows and
+ * T, S hold those rows only. */
+void tqo_gemv_f64(const int8_t *T, const uint16_t *S, int64_t N, int64_t K,
+                  const float *x, int64_t M, const int64_t *rows, int64_t nrows,
+                  double *y);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

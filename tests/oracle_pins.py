@@ -1,0 +1,433 @@
+"""Pins for the CPU oracle: facts fixed by the pages or by mathematics.
+
+Every ``check_*`` function takes a loaded oracle and raises AssertionError on a
+mismatch.  ``test_oracle.py`` runs them against the real oracle;
+``test_oracle_mutants.py`` runs them against deliberately broken copies of the
+oracle source to show that each plausible mistake is caught by at least one.
+
+Sources of truth used here (never the oracle itself):
+  * scipy.linalg.hadamard (Sylvester-built) and numpy Kronecker products;
+  * numpy's IEEE float16 conversion and fp32 division/rint;
+  * exact rational arithmetic (fractions.Fraction);
+  * hand-worked byte values in tests/golden/pack_cases.txt;
+  * closed forms derived in the comments next to each check.
+Page names: [mhpq] mhpq.cn/news/1159370, [dpshk] dpshk.com/news/5289456,
+[xxqk] xxqk.cn/news/652513, [zwxr] zwxr.cn/news/303439.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import scipy.linalg
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+C_BITS = 0x3DB504F3  # RN_fp32(1/sqrt(128)), derived exactly in check_norm_const
+
+
+def _f32(bits: int) -> np.float32:
+    return np.array([bits], dtype=np.uint32).view(np.float32)[0]
+
+
+def _block_h(K: int) -> np.ndarray:
+    """blockdiag(H_128, ..., H_128) / sqrt(128) in fp64, H from scipy."""
+    H = scipy.linalg.hadamard(128).astype(np.float64) / math.sqrt(128.0)
+    return scipy.linalg.block_diag(*([H] * (K // 128)))
+
+
+# --------------------------------------------------------------- Hadamard
+
+def check_hadamard_definitions(orc):
+    """[dpshk] sec. 2.1: the popcount entry rule equals the Sylvester recursion
+    H_2n = [[H, H], [H, -H]] ([mhpq] sec. 2.2 writes it as H_n (x) H_2)."""
+    h2 = np.array([[1, 1], [1, -1]], dtype=np.int64)
+    kron = np.array([[1]], dtype=np.int64)
+    n = 1
+    while n <= 128:
+        pop = orc.hadamard(n)
+        assert np.array_equal(pop, kron), f"popcount H_{n} != Kronecker H_{n}"
+        assert np.array_equal(orc.sylvester(n), kron), f"Sylvester H_{n} wrong"
+        assert np.array_equal(pop, scipy.linalg.hadamard(n)), f"H_{n} != scipy"
+        kron = np.kron(kron, h2)
+        n *= 2
+
+
+def check_hadamard_orthogonal(orc):
+    """[mhpq] sec. 2.2 / [xxqk] sec. 2: H H^T = n I (and H = H^T, H^2 = n I)."""
+    H = orc.hadamard(128)
+    assert np.array_equal(H @ H.T, 128 * np.eye(128, dtype=np.int64))
+    assert np.array_equal(H, H.T)
+
+
+def check_norm_const(orc):
+    """c = RN_fp32(1/sqrt(128)) = 0x3DB504F3, decided with exact rationals:
+    among fp32 neighbours a < b around r = 2^-3.5, r is nearer to a iff
+    r^2 = 1/128 < ((a + b) / 2)^2."""
+    assert orc.norm_const_bits() == C_BITS, hex(orc.norm_const_bits())
+    a = Fraction(float(_f32(C_BITS - 1)))
+    c = Fraction(float(_f32(C_BITS)))
+    b = Fraction(float(_f32(C_BITS + 1)))
+    target = Fraction(1, 128)
+    assert ((a + c) / 2) ** 2 < target < ((c + b) / 2) ** 2
+
+
+def check_fwht_dense_f64(orc):
+    """fp64 rotation = H_128 v / sqrt(128) with scipy's Sylvester H."""
+    rng = np.random.default_rng(11)
+    v = rng.standard_normal((6, 256))
+    ref = v @ _block_h(256).T
+    out = orc.fwht128_f64(v)
+    assert np.max(np.abs(out - ref)) <= 1e-13 * max(1.0, np.max(np.abs(ref)))
+
+
+def check_fwht_f32_close(orc):
+    """The fp32 staged transform equals the exact rotation within fp32
+    rounding: 7 add stages and one multiply, |err| <= 8 u ||v||_2 per entry."""
+    rng = np.random.default_rng(12)
+    v = (rng.standard_normal((32, 128)) * rng.uniform(0.01, 100, size=(32, 1))).astype(np.float32)
+    ref = v.astype(np.float64) @ _block_h(128).T
+    out = orc.fwht128_f32(v).astype(np.float64)
+    bound = 8 * 2.0 ** -24 * np.linalg.norm(v.astype(np.float64), axis=1, keepdims=True) * 2
+    assert np.all(np.abs(out - ref) <= bound)
+
+
+def check_fwht_delta(orc):
+    """A unit input e_j is rotated to c * (column j of H) exactly: every
+    butterfly of a delta is an exact +-1, and one multiply by c is exact."""
+    H = scipy.linalg.hadamard(128)
+    c = _f32(C_BITS)
+    for j in (0, 1, 5, 64, 127):
+        e = np.zeros(128, dtype=np.float32)
+        e[j] = 1.0
+        out = orc.fwht128_f32(e)
+        assert np.array_equal(out, (H[:, j] * c).astype(np.float32)), j
+
+
+def check_fwht_stage_order(orc):
+    """The butterfly rounds run h = 1, 2, ..., 64 in fp32 (the fixed order that
+    makes codes bit-reproducible).  Written here in tensor form: view the 128
+    entries as a 2x2x...x2 array whose axis s is index bit s; round s
+    combines the two slices along bit s."""
+    rng = np.random.default_rng(13)
+    v = (rng.standard_normal((64, 128)) * 3).astype(np.float32)
+    w = v.copy()
+    for s in range(7):
+        h = 1 << s
+        t = w.reshape(64, 128 // (2 * h), 2, h)
+        a, b = t[:, :, 0, :].copy(), t[:, :, 1, :].copy()
+        t[:, :, 0, :] = a + b
+        t[:, :, 1, :] = a - b
+        w = t.reshape(64, 128)
+    w = (w * _f32(C_BITS)).astype(np.float32)
+    assert np.array_equal(orc.fwht128_f32(v), w)
+
+
+def check_fwht_involution_energy(orc):
+    """The normalised rotation is its own inverse ([zwxr] sec. 2: the inverse
+    is the same transform up to 1/n) and keeps the 2-norm ([mhpq] sec. 2.2)."""
+    rng = np.random.default_rng(14)
+    v = rng.standard_normal((8, 128))
+    r = orc.fwht128_f64(v)
+    assert np.allclose(np.linalg.norm(r, axis=1), np.linalg.norm(v, axis=1), rtol=1e-13, atol=0)
+    assert np.max(np.abs(orc.fwht128_f64(r) - v)) <= 1e-13
+    v32 = v.astype(np.float32)
+    rr = orc.fwht128_f32(orc.fwht128_f32(v32)).astype(np.float64)
+    assert np.all(np.abs(rr - v32) <= 1e-6 * np.linalg.norm(v32, axis=1, keepdims=True))
+
+
+# ------------------------------------------------------------------ fp16
+
+def _f16_cases() -> np.ndarray:
+    """Every finite fp16 value, its fp32 neighbours, every midpoint between
+    adjacent fp16 values and the midpoints' neighbours, plus edge values."""
+    h = np.arange(0, 0x7C00, dtype=np.uint16)
+    f = h.view(np.float16).astype(np.float32)
+    nxt = np.append(f[1:], np.float32(65520.0))
+    mid = ((f.astype(np.float64) + nxt.astype(np.float64)) / 2).astype(np.float32)  # exact in fp32
+    up = np.nextafter(f, np.float32(np.inf))
+    dn = np.nextafter(f, np.float32(0))
+    mu = np.nextafter(mid, np.float32(np.inf))
+    md = np.nextafter(mid, np.float32(0))
+    extra = np.array([2.0 ** -25, 2.0 ** -26, 3 * 2.0 ** -26, 1e-30, 65504.0, 65519.996, 65520.0,
+                      1e5, 3.4e38, np.inf], dtype=np.float32)
+    allv = np.concatenate([f, up, dn, mid, mu, md, extra])
+    return np.concatenate([allv, -allv])
+
+
+def check_f16_conversion(orc):
+    """fp32 -> binary16 round-to-nearest-even equals numpy's IEEE conversion
+    on every rounding boundary; binary16 -> fp32 is exact for all patterns."""
+    vals = _f16_cases()
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([orc.f32_to_f16(float(v)) for v in vals], dtype=np.uint16)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first {vals[bad[0]]!r}: {got[bad[0]]:#x} vs {ref[bad[0]]:#x}"
+    pats = np.arange(0, 0x10000, 7, dtype=np.uint32).astype(np.uint16)
+    pats = pats[(pats & 0x7C00) != 0x7C00]
+    back = np.array([orc.f16_to_f32(int(p)) for p in pats], dtype=np.float32)
+    assert np.array_equal(back.view(np.uint32), pats.view(np.float16).astype(np.float32).view(np.uint32))
+
+
+# ------------------------------------------------------------- quantiser
+
+def _fp16(x: float) -> int:
+    return int(np.array([x], dtype=np.float32).astype(np.float16).view(np.uint16)[0])
+
+
+def _fp16_val(bits: int) -> np.float32:
+    return np.array([bits], dtype=np.uint16).view(np.float16).astype(np.float32)[0]
+
+
+def check_quantize_constant_magnitude(orc):
+    """[mhpq] sec. 1.1: a group whose |w'| all equal a has mean a, so the
+    scale is fp16(a) and every weight maps to its sign (a / fp16(a) is within
+    2^-11 of 1)."""
+    rng = np.random.default_rng(21)
+    for a in (0.02, 1.0, 0.0883883476, 3.7e-3, 1234.5):
+        sign = np.where(rng.random(128) < 0.5, -1.0, 1.0).astype(np.float32)
+        w = (sign * np.float32(a)).astype(np.float32)
+        s, t = orc.quantize_group(w)
+        assert s == _fp16(np.float32(a)), (a, hex(s))
+        assert np.array_equal(t, sign.astype(np.int8))
+
+
+def check_quantize_zero_and_extremes(orc):
+    """All-zero group: scale 0, trits 0.  A group whose mean underflows fp16
+    (< 2^-25) also gets scale 0 and trits 0.  A group whose mean reaches
+    65520 rounds to an infinite scale and w'/inf = 0 gives trits 0."""
+    s, t = orc.quantize_group(np.zeros(128, dtype=np.float32))
+    assert s == 0 and not t.any()
+    w = np.full(128, 2.0 ** -27, dtype=np.float32)
+    w[::3] *= -1
+    s, t = orc.quantize_group(w)
+    assert s == 0 and not t.any()
+    w = np.full(128, 70000.0, dtype=np.float32)
+    s, t = orc.quantize_group(w)
+    assert s == 0x7C00 and not t.any()
+
+
+def _tie_group(s0: float):
+    """A group whose mean rounds to the fp16 value s0, holding probe values at
+    chosen multiples of s0.  The mean is about s0 * 1.0003, which still rounds
+    to s0 in fp16 but differs from it in fp32."""
+    s0 = np.float32(s0)
+    probes = np.array([0.5, -0.5, 1.5, -1.5, 2.5, -2.5, 0.0, 1.0, -1.0, 0.25], dtype=np.float32) * s0
+    up = np.nextafter(np.float32(0.5) * s0, np.float32(np.inf))
+    dn = np.nextafter(np.float32(0.5) * s0, np.float32(0))
+    probes = np.concatenate([probes, [up, dn, -up, -dn]]).astype(np.float32)
+    expect = np.array([0, 0, 1, -1, 1, -1, 0, 1, -1, 0, 1, 0, -1, 0], dtype=np.int8)
+    nfill = 128 - probes.size
+    fill_total = 128 * float(s0) * 1.0003 - float(np.sum(np.abs(probes.astype(np.float64))))
+    fill = np.full(nfill, fill_total / nfill, dtype=np.float32)
+    fill[1::2] *= -1
+    return np.concatenate([probes, fill]).astype(np.float32), expect, probes.size
+
+
+def check_quantize_ties(orc):
+    """[mhpq] sec. 1.1 with round-half-even: w'/s = +-0.5 -> 0, +-1.5 -> +-2
+    clipped to +-1, +-2.5 -> +-1; the fp32 neighbours of s/2 fall on either
+    side.  The divisor is the stored fp16 scale, not the fp32 mean."""
+    for s0 in (1.0, 0.01171875, 0.0234375, 6.103515625e-05):
+        w, expect, n = _tie_group(s0)
+        s, t = orc.quantize_group(w)
+        assert s == _fp16(np.float32(s0)), (s0, hex(s))
+        assert np.array_equal(t[:n], expect), (s0, t[:n], expect)
+
+
+def check_quantize_rule_identity(orc):
+    """For a finite scale s > 0, clamp(rint(fl(w/s)), -1, 1) equals
+    sign(w) * [|w| > s/2] (exact fp32 reasoning: the quotient rounds above
+    0.5 iff |w| exceeds s/2).  Checked on random groups with numpy's IEEE
+    fp32 division and rint as the independent side."""
+    rng = np.random.default_rng(23)
+    for _ in range(200):
+        w = (rng.standard_normal(128) * rng.uniform(1e-4, 10)).astype(np.float32)
+        s, t = orc.quantize_group(w)
+        sv = _fp16_val(s)
+        q = np.rint(w / sv)
+        ref = np.clip(q, -1, 1).astype(np.int8)
+        assert np.array_equal(t, ref)
+        rule = (np.sign(w) * (np.abs(w) > sv / np.float32(2))).astype(np.int8)
+        assert np.array_equal(t, rule)
+
+
+def check_quantize_mean_exact(orc):
+    """When every partial sum is exact (small integers / 2^k), the scale is
+    fp16 of the exact mean of |w'|."""
+    rng = np.random.default_rng(24)
+    for _ in range(20):
+        ints = rng.integers(-64, 65, size=128)
+        w = (ints / 16.0).astype(np.float32)
+        s, _ = orc.quantize_group(w)
+        mean = Fraction(int(np.sum(np.abs(ints))), 16 * 128)
+        assert s == _fp16(np.float32(float(mean)))
+
+
+def check_quantize_delta_rows(orc):
+    """A weight row that is a unit vector in one group rotates to c * (column
+    of H): all |w'| = c, mean = c exactly, scale = fp16(c), trits = that
+    column of H; groups left at zero get scale 0."""
+    H = scipy.linalg.hadamard(128)
+    K = 256
+    W = np.zeros((3, K), dtype=np.float32)
+    W[0, 7] = 1.0
+    W[1, 128 + 100] = 1.0
+    W[2, 0] = 1.0
+    W[2, 255] = 1.0
+    T, S = orc.quantize(W)
+    sc = _fp16(_f32(C_BITS))
+    assert list(S[0]) == [sc, 0] and list(S[1]) == [0, sc] and list(S[2]) == [sc, sc]
+    assert np.array_equal(T[0, :128], H[:, 7]) and not T[0, 128:].any()
+    assert np.array_equal(T[1, 128:], H[:, 100]) and not T[1, :128].any()
+    assert np.array_equal(T[2, :128], H[:, 0]) and np.array_equal(T[2, 128:], H[:, 127])
+
+
+def check_quantize_bf16_input(orc):
+    """bf16 weights are widened exactly: quantising bf16 bits equals
+    quantising the same values given as fp32."""
+    rng = np.random.default_rng(25)
+    w = (rng.standard_normal((4, 256)) * 0.02).astype(np.float32)
+    bits = (w.view(np.uint32) >> 16).astype(np.uint16)
+    wv = (bits.astype(np.uint32) << 16).view(np.float32)
+    T1, S1 = orc.quantize(bits)
+    T2, S2 = orc.quantize(wv)
+    assert np.array_equal(T1, T2) and np.array_equal(S1, S2)
+
+
+# --------------------------------------------------------------- packing
+
+def _read_pack_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "pack_cases.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            fmt, K, trits, bytes_ = line.split("|")
+            cases.append((fmt.strip(), int(K), [int(v) for v in trits.split()],
+                          [int(v) for v in bytes_.split()]))
+    return cases
+
+
+def check_pack_golden(orc):
+    """Hand-worked bytes (tests/golden/pack_cases.txt) for both layouts."""
+    for fmt, K, trits, expect in _read_pack_cases():
+        T = np.array([trits], dtype=np.int8)
+        assert T.shape[1] == K
+        if fmt == "2bit":
+            got = orc.pack2(T)[0]
+            back = orc.unpack2(got[None, :], K)
+        else:
+            got = orc.pack3(T)[0]
+            back = orc.unpack3(got[None, :], K)
+        assert list(got) == expect, (fmt, trits, list(got), expect)
+        assert np.array_equal(back, T)
+
+
+def check_pack_roundtrip(orc):
+    """unpack(pack(t)) = t for both layouts; base-3 bytes never exceed
+    3^5 - 1 = 242; padding bytes are zero; the 2-bit layout never emits
+    code 3."""
+    rng = np.random.default_rng(31)
+    for K in (128, 256, 640, 27648 // 8):
+        T = rng.integers(-1, 2, size=(5, K)).astype(np.int8)
+        c2 = orc.pack2(T)
+        assert c2.shape == (5, K // 4)
+        assert np.array_equal(orc.unpack2(c2, K), T)
+        codes = np.stack([(c2 >> (2 * i)) & 3 for i in range(4)])
+        assert codes.max() <= 2
+        c3 = orc.pack3(T)
+        ld = orc.ld3(K)
+        assert c3.shape == (5, ld) and ld % 16 == 0 and ld >= -(-K // 5)
+        assert c3.max() <= 242
+        assert not c3[:, -(-K // 5):].any()
+        assert np.array_equal(orc.unpack3(c3, K), T)
+
+
+def check_bit_accounting(orc):
+    """[mhpq] sec. 1.1: log2(3) = 1.585 bit per ternary weight; sec. 1.3: one
+    fp16 scale per 128 weights adds 16/128 = 0.125 bit, 1.585 + 0.125 = 1.71.
+    The layouts built here store 8/5 + 0.125 = 1.725 (base-3) and
+    2 + 0.125 = 2.125 (2-bit) bits per weight at K = 5120."""
+    assert round(math.log2(3), 3) == 1.585
+    assert 16 / 128 == 0.125
+    assert round(math.log2(3) + 0.125, 2) == 1.71
+    K = 5120
+    T = np.zeros((1, K), dtype=np.int8)
+    assert orc.pack3(T).shape[1] * 8 / K + 16 / 128 == 1.725
+    assert orc.pack2(T).shape[1] * 8 / K + 16 / 128 == 2.125
+
+
+# ------------------------------------------------------------------ GEMV
+
+def _dequant(T: np.ndarray, S: np.ndarray) -> np.ndarray:
+    s = S.view(np.float16).astype(np.float64)
+    return T.astype(np.float64) * np.repeat(s, 128, axis=1)
+
+
+def check_gemv_dense(orc):
+    """y equals the dense fp64 product of the dequantised weights
+    (t * s per group) with the block-rotated activations (scipy H)."""
+    rng = np.random.default_rng(41)
+    for (N, K, M) in ((7, 128, 1), (33, 384, 3), (64, 512, 2)):
+        T = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+        S = (rng.uniform(0.001, 0.1, size=(N, K // 128))).astype(np.float16).view(np.uint16)
+        x = rng.standard_normal((M, K)).astype(np.float32)
+        ref = (x.astype(np.float64) @ _block_h(K).T) @ _dequant(T, S).T
+        got = orc.gemv(T, S, x)
+        assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+def check_gemv_delta_activation(orc):
+    """x = e_k gives y[n] = (W_deq . blockdiag(H)/sqrt(128))[n, k]: the
+    weight column k mapped back to the unrotated basis."""
+    rng = np.random.default_rng(42)
+    N, K = 9, 256
+    T = rng.integers(-1, 2, size=(N, K)).astype(np.int8)
+    S = rng.uniform(0.01, 0.05, size=(N, 2)).astype(np.float16).view(np.uint16)
+    back = _dequant(T, S) @ _block_h(K)
+    for k in (0, 77, 128, 255):
+        x = np.zeros((1, K), dtype=np.float32)
+        x[0, k] = 1.0
+        assert np.max(np.abs(orc.gemv(T, S, x)[0] - back[:, k])) <= 1e-14
+
+
+def check_rotation_invariance(orc):
+    """[mhpq] sec. 2.3 (rotation absorbed): rotating the weight rows and the
+    activations by the same normalised block transform leaves W x unchanged
+    (fp64, before quantisation)."""
+    rng = np.random.default_rng(43)
+    W = rng.standard_normal((16, 384))
+    x = rng.standard_normal(384)
+    Wr = orc.fwht128_f64(W)
+    xr = orc.fwht128_f64(x)
+    assert np.max(np.abs(Wr @ xr - W @ x)) <= 1e-12 * np.max(np.abs(W @ x))
+
+
+ALL_CHECKS = [
+    check_hadamard_definitions,
+    check_hadamard_orthogonal,
+    check_norm_const,
+    check_fwht_dense_f64,
+    check_fwht_f32_close,
+    check_fwht_delta,
+    check_fwht_stage_order,
+    check_fwht_involution_energy,
+    check_f16_conversion,
+    check_quantize_constant_magnitude,
+    check_quantize_zero_and_extremes,
+    check_quantize_ties,
+    check_quantize_rule_identity,
+    check_quantize_mean_exact,
+    check_quantize_delta_rows,
+    check_quantize_bf16_input,
+    check_pack_golden,
+    check_pack_roundtrip,
+    check_bit_accounting,
+    check_gemv_dense,
+    check_gemv_delta_activation,
+    check_rotation_invariance,
+]

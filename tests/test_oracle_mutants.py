@@ -1,0 +1,60 @@
+"""Each plausible mistake planted in a copy of the oracle source must make at
+least one pin fail.  The mutants are built on the CPU from a temporary copy of
+oracle/tq_oracle.c; the committed oracle is never changed."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "tq_oracle.c")
+
+# (name, text in tq_oracle.c, replacement): one planted mistake each
+MUTANTS = [
+    ("butterfly_sign", "v[i + h] = a - b;", "v[i + h] = b - a;"),
+    ("stage_order", "for (int h = 1; h < 128; h *= 2) {", "for (int h = 64; h >= 1; h /= 2) {"),
+    ("no_normalisation", "out[i] = v[i] * c;", "out[i] = v[i];"),
+    ("popcount_bit", "return (ones & 1) ? -1 : 1;", "return (ones & 2) ? -1 : 1;"),
+    ("sylvester_block", "h[(i + m) * n + (j + m)] = (int8_t)(-v);", "h[(i + m) * n + (j + m)] = v;"),
+    ("f16_round_ties_down", "if (rem > half || (rem == half && (q & 1u))) q += 1;\n    if (q == 0x800u)",
+     "if (rem > half) q += 1;\n    if (q == 0x800u)"),
+    ("f16_subnormal_scale", "5.9604644775390625e-08f", "1.1920928955078125e-07f"),
+    ("mean_factor", "s[0] * 0.0078125f", "s[0] * 0.00390625f"),
+    ("signed_sum", "s[i] = fabsf(wrot[i]);", "s[i] = wrot[i];"),
+    ("divide_by_mean", "float q = wrot[i] / sc;", "float q = wrot[i] / mean;"),
+    ("round_half_away", "float r = nearbyintf(q);", "float r = roundf(q);"),
+    ("no_clamp", "t[i] = (int8_t)(r > 1.0f ? 1 : (r < -1.0f ? -1 : (int)r));",
+     "t[i] = (int8_t)(r > 2.0f ? 1 : (r < -2.0f ? -1 : (int)r));"),
+    ("skip_weight_rotation", "tqo_fwht128_f32(grp, rot);", "for (int i = 0; i < 128; ++i) rot[i] = grp[i];"),
+    ("pack2_code_map", "unsigned code = (unsigned)(T[n * K + k] + 1);", "unsigned code = (unsigned)(1 - T[n * K + k]);"),
+    ("pack2_bit_order", "(code << (2 * (k % 4)))", "(code << (6 - 2 * (k % 4)))"),
+    ("pack3_digit_order", "v += d * p;", "v = v * 3 + d;"),
+    ("pack3_pad_digit", ": 1u;", ": 0u;"),
+    ("gemv_drops_scale", "y[m * nout + r] += (double)tqo_f16_to_f32(S[r * G + g]) * part;",
+     "y[m * nout + r] += part;"),
+    ("gemv_reversed_x", "blk[i] = (double)x[m * K + g * 128 + i];", "blk[i] = (double)x[m * K + g * 128 + (127 - i)];"),
+    ("gemv_no_x_rotation", "tqo_fwht128_f64(blk, rot);\n      for (int64_t r",
+     "for (int i = 0; i < 128; ++i) rot[i] = blk[i];\n      for (int64_t r"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mut = tmp_path / "tq_oracle.c"
+    mut.write_text(src.replace(old, new))
+    shutil.copy(os.path.join(os.path.dirname(SRC), "tq_oracle.h"), tmp_path / "tq_oracle.h")
+    lib = str(tmp_path / f"lib_{name}.so")
+    subprocess.run(["gcc", *oracle.CFLAGS, "-I", str(tmp_path), "-o", lib, str(mut), "-lm"], check=True)
+    orc = oracle.Oracle(lib)
+    failed = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(orc)
+        except AssertionError:
+            failed.append(check.__name__)
+    assert failed, f"mutant {name} passed every pin"
