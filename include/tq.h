@@ -1,0 +1,153 @@
+/*
+ * tq.h -- C ABI of libtq: ternary weights after a 128-point block
+ * Walsh-Hadamard rotation, on one GB300 GPU (sm_103a).
+ *
+ * The method (pages are named by address; none carries a title):
+ *   offline   w' = W . blockdiag(H_128)/sqrt(128) along K, then per group of
+ *             128 weights s = fp16(mean |w'|), t = clamp(rint(w'/s), -1, 1),
+ *             packed as 2-bit codes or as five base-3 digits per byte
+ *             (mhpq.cn/news/1159370 sec. 1.1, 1.3, 2.2, 3.1);
+ *   run time  x' = blockdiag(H_128)/sqrt(128) . x along K (the rotation is
+ *             absorbed on the activation side, mhpq.cn/news/1159370 sec. 2.3;
+ *             zwxr.cn/news/303439, activation-side Hadamard), and
+ *             y[m][n] = sum_g s[n][g] * sum_{k in g} t[n][k] * x'[m][k]
+ *             accumulated in fp32 (fusion of transform and ternary matmul:
+ *             mhpq.cn/news/1159370 sec. 3.3; dpshk.com/news/5289456 sec. 4).
+ *
+ * H[i][j] = (-1)^popcount(i & j) (dpshk.com/news/5289456 sec. 2.1).  The
+ * transform runs butterfly stages h = 1, 2, 4, ..., 64 in fp32 and then
+ * multiplies by c = RN_fp32(1/sqrt(128)) (xxqk.cn/news/652513 sec. 2).
+ *
+ * Layouts (row-major, leading dimensions in ELEMENTS of the pointed-to type):
+ *   W      [N][ldw]   weights, fp32 or bf16          (N outputs, K inputs)
+ *   x      [M][ldx]   activations, bf16 (fp32 also accepted by tq_fwht128)
+ *   y      [M][ldy]   fp32 outputs
+ *   scales [N][lds]   fp16 bit patterns, one per group of 128 (G = K/128)
+ *   codes2 [N][ld2]   2-bit codes: code = t + 1 in bits 2*(k%4) of byte k/4
+ *   codes3 [N][ld3]   base-3 bytes: byte j = sum_{i<5} (t[5j+i] + 1) * 3^i;
+ *                     trits past K count as t = 0; bytes from ceil(K/5)
+ *                     to ld3 are written as 0
+ *
+ * Every call:
+ *   - takes DEVICE pointers owned by the caller (except where noted) and
+ *     allocates no memory;
+ *   - is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream); results are valid once the stream reaches that point;
+ *   - validates its arguments on the host first and returns a status; a
+ *     non-OK status means nothing was launched;
+ *   - is thread-safe; the library keeps only per-device read-only setup.
+ * Pointers must be 16-byte aligned and every row must start 16-byte aligned
+ * (ld * element size % 16 == 0), else TQ_ERR_ALIGN.  K must be a positive
+ * multiple of 128, else TQ_ERR_SHAPE.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TQ_API __attribute__((visibility("default")))
+#else
+#define TQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1, /* NULL pointer, bad enum, negative size         */
+  TQ_ERR_SHAPE = 2,       /* K % 128 != 0, M out of range, ld too small    */
+  TQ_ERR_ALIGN = 3,       /* pointer or row not 16-byte aligned            */
+  TQ_ERR_UNSUPPORTED = 4, /* dtype/format combination not provided         */
+  TQ_ERR_CUDA = 5,        /* a CUDA launch or query failed                 */
+  TQ_ERR_RANGE = 6,       /* fp16 overflow recorded by tq_gemm             */
+  TQ_ERR_TIMEOUT = 7      /* a kernel gave up a bounded wait (see below)   */
+} tq_status;
+
+typedef enum { TQ_F32 = 0, TQ_BF16 = 1, TQ_F16 = 2 } tq_dtype;
+
+typedef enum { TQ_PACK_2BIT = 1, TQ_PACK_BASE3 = 2, TQ_PACK_BOTH = 3 } tq_pack;
+
+/* cudaStream_t, passed through untouched. */
+typedef void *tq_stream;
+
+/* Human-readable name of a status code (static storage). */
+TQ_API const char *tq_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+TQ_API int tq_version(void);
+
+/* Minimum leading dimension in bytes of one packed layout for K inputs:
+ * K/4 for TQ_PACK_2BIT; ceil(K/5) rounded up to 16 for TQ_PACK_BASE3.
+ * Returns -1 for a bad K or format. */
+TQ_API int64_t tq_packed_ld(int64_t K, int fmt);
+
+/* Block FWHT-128 along K of `rows` rows:
+ *   y[r][128g + i] = c * sum_j H[i][j] x[r][128g + j]
+ * computed in fp32 (stages h = 1..64, then * c) and rounded once to yt.
+ * xt in {TQ_F32, TQ_BF16}; yt in {TQ_F32, TQ_BF16, TQ_F16}.  With an fp32
+ * output the result is bit-identical to the staged fp32 definition.
+ * x == y is allowed when xt == yt and ldx == ldy (in place); other
+ * overlaps are undefined.  rows == 0 is a no-op. */
+TQ_API tq_status tq_fwht128(const void *x, int xt, int64_t ldx, void *y, int yt, int64_t ldy,
+                     int64_t rows, int64_t K, tq_stream stream);
+
+/* Offline quantise + pack (mhpq.cn/news/1159370 sec. 1.1 absmean
+ * ternarisation, sec. 1.3 fp16 scale per 128, sec. 3.1 packing):
+ * for every row n and group g, w' = FWHT-128 of W[n][128g .. 128g+127]
+ * (fp32, as tq_fwht128), sum |w'| by the halving tree (h = 64 .. 1),
+ * s = fp16_RN(sum * 2^-7), t = clamp(rint(w' / s), -1, 1) with IEEE
+ * division and ties to even (t = 0 when s == 0).  Codes and scales are
+ * bit-exact with that definition.  wt in {TQ_F32, TQ_BF16}.  fmt selects
+ * which of codes2 / codes3 are written (the other may be NULL); scales is
+ * always written.  ld2 >= K/4, ld3 >= tq_packed_ld(K, TQ_PACK_BASE3),
+ * lds >= K/128 (fp16 elements, lds * 2 % 16 == 0 not required). */
+TQ_API tq_status tq_quantize_pack(const void *W, int wt, int64_t N, int64_t K, int64_t ldw, int fmt,
+                           uint8_t *codes2, int64_t ld2, uint8_t *codes3, int64_t ld3,
+                           uint16_t *scales, int64_t lds, tq_stream stream);
+
+/* Decode GEMV / skinny GEMM, 1 <= M <= 16, FWHT of x fused into the kernel
+ * (no workspace):  y[m][n] = sum_g s[n][g] sum_{k in g} t[n][k] x'[m][k]
+ * with x' = FWHT-128(x) rounded to fp16, products and sums in fp32.
+ * fmt is TQ_PACK_2BIT or TQ_PACK_BASE3 (codes laid out as above); x is
+ * bf16.  Accuracy against the fp64 definition: relative L2 error <= 2e-3.
+ * N == 0 is a no-op.  y must not overlap the inputs. */
+TQ_API tq_status tq_gemv(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
+                  int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
+                  tq_stream stream);
+
+/* Bytes of caller-provided workspace tq_gemm needs for M x K activations:
+ * the rotated activations in fp16 plus a status word. */
+TQ_API size_t tq_gemm_workspace_bytes(int64_t M, int64_t K);
+
+/* Prefill GEMM, M >= 1 (tensor cores: tcgen05 MMA with fp16 operands and
+ * fp32 accumulation in tensor memory):  same formula as tq_gemv.  Runs the
+ * FWHT-128 of x into the workspace (fp16, overflow recorded in the status
+ * word), then the GEMM, on `stream`.  fmt is TQ_PACK_2BIT.  ws_bytes must
+ * be >= tq_gemm_workspace_bytes(M, K).  y must not overlap the inputs. */
+TQ_API tq_status tq_gemm(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
+                  int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
+                  void *workspace, size_t ws_bytes, tq_stream stream);
+
+/* Synchronises `stream`, then reads the status word the last tq_gemm left in
+ * `workspace`: TQ_ERR_RANGE if a rotated activation overflowed fp16 (the
+ * output is then not meaningful), else TQ_OK. */
+TQ_API tq_status tq_gemm_check_range(const void *workspace, tq_stream stream);
+
+/* Failure detection.  Every wait inside a kernel (pipeline barriers between
+ * the warps that copy weights and the warps that compute) is bounded by a
+ * wall-clock limit of about 2 s.  A kernel whose wait runs out stops early,
+ * lets its in-flight copies land, records the event in a device status word
+ * and exits, so the CUDA context stays usable; its outputs are then not
+ * meaningful.  This call synchronises the device, returns TQ_ERR_TIMEOUT if
+ * any kernel recorded such an event since the previous call (and clears the
+ * record), else TQ_OK; TQ_ERR_CUDA if the device could not be queried. */
+TQ_API tq_status tq_device_fault(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */

@@ -1,0 +1,192 @@
+"""Python binding of libtq (ternary weights after a block FWHT-128, on GB300).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/tq.h``.  PyTorch provides the
+device memory and the current CUDA stream.  There is no CPU fallback: if the
+library is not built, every call raises.
+
+Functions (names follow the C ABI):
+  fwht128(x, out_dtype)                 x' = blockdiag(H_128)/sqrt(128) x along K
+  quantize_pack(W, fmt)                 (codes2, codes3, scales)
+  gemv(codes, scales, x, K, fmt)        y fp32 [M][N], M = 1..16
+  gemm(codes, scales, x, K, fmt, ws)    y fp32 [M][N] on tcgen05 tensor cores
+  gemm_workspace_bytes(M, K), gemm_check_range(ws)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+(TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_SHAPE, TQ_ERR_ALIGN, TQ_ERR_UNSUPPORTED, TQ_ERR_CUDA, TQ_ERR_RANGE,
+ TQ_ERR_TIMEOUT) = range(8)
+TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
+TQ_PACK_2BIT, TQ_PACK_BASE3, TQ_PACK_BOTH = 1, 2, 3
+
+EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_quantize_pack", "tq_gemv",
+            "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_check_range", "tq_device_fault")
+
+_lib = None
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_int = ctypes.c_int
+
+
+class TQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libtq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libtq.so is not built ({_LIB_PATH}); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(_LIB_PATH)
+        L.tq_status_string.restype = ctypes.c_char_p
+        L.tq_status_string.argtypes = [_int]
+        L.tq_version.restype = _int
+        L.tq_packed_ld.restype = _i64
+        L.tq_packed_ld.argtypes = [_i64, _int]
+        L.tq_fwht128.restype = _int
+        L.tq_fwht128.argtypes = [_vp, _int, _i64, _vp, _int, _i64, _i64, _i64, _vp]
+        L.tq_quantize_pack.restype = _int
+        L.tq_quantize_pack.argtypes = [_vp, _int, _i64, _i64, _i64, _int, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
+        L.tq_gemv.restype = _int
+        L.tq_gemv.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp]
+        L.tq_gemm_workspace_bytes.restype = ctypes.c_size_t
+        L.tq_gemm_workspace_bytes.argtypes = [_i64, _i64]
+        L.tq_gemm.restype = _int
+        L.tq_gemm.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
+                              ctypes.c_size_t, _vp]
+        L.tq_gemm_check_range.restype = _int
+        L.tq_gemm_check_range.argtypes = [_vp, _vp]
+        L.tq_device_fault.restype = _int
+        L.tq_device_fault.argtypes = []
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().tq_status_string(status).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != TQ_OK:
+        raise TQError(status, where)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return TQ_F32
+    if t.dtype == torch.bfloat16:
+        return TQ_BF16
+    if t.dtype == torch.float16:
+        return TQ_F16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _cuda2d(t: torch.Tensor, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with unit stride along its last dimension")
+
+
+def packed_ld(K: int, fmt: int) -> int:
+    return int(lib().tq_packed_ld(K, fmt))
+
+
+def fwht128(x: torch.Tensor, out_dtype: torch.dtype = torch.float32, out: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    """Block FWHT-128 of every row of x (fp32 or bf16) along its last dimension."""
+    _cuda2d(x, "x")
+    rows, K = x.shape
+    if out is None:
+        out = torch.empty((rows, K), dtype=out_dtype, device=x.device)
+    _cuda2d(out, "out")
+    st = lib().tq_fwht128(x.data_ptr(), _dt(x), x.stride(0), out.data_ptr(), _dt(out), out.stride(0), rows, K,
+                          _stream(stream))
+    _check(st, "tq_fwht128")
+    return out
+
+
+def quantize_pack(W: torch.Tensor, fmt: int = TQ_PACK_BOTH, stream=None):
+    """Rotate, ternarise and pack W [N][K] (fp32 or bf16).
+
+    Returns (codes2 uint8 [N][K/4] or None, codes3 uint8 [N][ld3] or None,
+    scales int16 [N][K/128] holding fp16 bit patterns)."""
+    _cuda2d(W, "W")
+    N, K = W.shape
+    dev = W.device
+    codes2 = torch.empty((N, K // 4), dtype=torch.uint8, device=dev) if fmt & TQ_PACK_2BIT else None
+    ld3 = packed_ld(K, TQ_PACK_BASE3) if K > 0 else 0
+    codes3 = torch.empty((N, max(ld3, 0)), dtype=torch.uint8, device=dev) if fmt & TQ_PACK_BASE3 else None
+    scales = torch.empty((N, K // 128), dtype=torch.int16, device=dev)
+    st = lib().tq_quantize_pack(W.data_ptr(), _dt(W), N, K, W.stride(0), fmt,
+                                codes2.data_ptr() if codes2 is not None else None, K // 4,
+                                codes3.data_ptr() if codes3 is not None else None, max(ld3, 0),
+                                scales.data_ptr(), scales.stride(0), _stream(stream))
+    _check(st, "tq_quantize_pack")
+    return codes2, codes3, scales
+
+
+def gemv(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, fmt: int = TQ_PACK_2BIT,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y [M][N] fp32 = ternary GEMV/skinny GEMM of bf16 x [M][K] (M <= 16)."""
+    _cuda2d(codes, "codes")
+    _cuda2d(scales, "scales")
+    _cuda2d(x, "x")
+    N = codes.shape[0]
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    st = lib().tq_gemv(codes.data_ptr(), codes.stride(0), fmt, scales.data_ptr(), scales.stride(0), N, K,
+                       x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), _stream(stream))
+    _check(st, "tq_gemv")
+    return out
+
+
+def gemm_workspace_bytes(M: int, K: int) -> int:
+    return int(lib().tq_gemm_workspace_bytes(M, K))
+
+
+def gemm(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, fmt: int = TQ_PACK_2BIT,
+         workspace: torch.Tensor | None = None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y [M][N] fp32 = prefill GEMM of bf16 x [M][K] on tcgen05 tensor cores."""
+    _cuda2d(codes, "codes")
+    _cuda2d(scales, "scales")
+    _cuda2d(x, "x")
+    N = codes.shape[0]
+    M = x.shape[0]
+    if workspace is None:
+        workspace = torch.empty(gemm_workspace_bytes(M, K), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    st = lib().tq_gemm(codes.data_ptr(), codes.stride(0), fmt, scales.data_ptr(), scales.stride(0), N, K,
+                       x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), workspace.data_ptr(),
+                       workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "tq_gemm")
+    return out
+
+
+def device_fault() -> None:
+    """Raises TQError(TQ_ERR_TIMEOUT) if a kernel gave up a bounded wait since
+    the last call (synchronises the device)."""
+    _check(lib().tq_device_fault(), "tq_device_fault")
+
+
+def gemm_check_range(workspace: torch.Tensor, stream=None) -> None:
+    """Raises TQError(TQ_ERR_RANGE) if the last tq_gemm saw an fp16 overflow."""
+    _check(lib().tq_gemm_check_range(workspace.data_ptr(), _stream(stream)), "tq_gemm_check_range")

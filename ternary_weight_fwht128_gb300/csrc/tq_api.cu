@@ -1,0 +1,169 @@
+// tq_api.cu -- the C ABI of libtq: host-side validation, then one launch (or
+// two for tq_gemm) on the caller's stream.  No entry point allocates memory,
+// throws, aborts or synchronises (except tq_gemm_check_range, which must).
+#include <atomic>
+#include <cstring>
+
+#include "tq_internal.h"
+
+namespace tq {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_smem[kMaxDevices];
+
+int cached_attr(std::atomic<int>* cache, cudaDeviceAttr attr, int fallback) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fallback;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess || v <= 0) return fallback;
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+
+int dtype_size(int t) { return t == TQ_F32 ? 4 : 2; }
+
+bool k_ok(int64_t K) { return K > 0 && K % 128 == 0; }
+
+tq_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return TQ_OK;
+  if (e == cudaErrorNotSupported) {
+    (void)cudaGetLastError();  // clear a sticky launch-config error, if any
+    return TQ_ERR_UNSUPPORTED;
+  }
+  return TQ_ERR_CUDA;
+}
+
+int64_t ld3_min(int64_t K) { return ((K + 4) / 5 + 15) / 16 * 16; }
+
+}  // namespace
+
+int device_sm_count() { return cached_attr(g_sms, cudaDevAttrMultiProcessorCount, 148); }
+int device_max_smem_optin() { return cached_attr(g_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, 227 * 1024); }
+
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" {
+
+const char* tq_status_string(int status) {
+  switch (status) {
+    case TQ_OK: return "TQ_OK";
+    case TQ_ERR_INVALID_ARG: return "TQ_ERR_INVALID_ARG: null pointer, bad enum or negative size";
+    case TQ_ERR_SHAPE: return "TQ_ERR_SHAPE: K must be a positive multiple of 128; M or a leading dimension out of range";
+    case TQ_ERR_ALIGN: return "TQ_ERR_ALIGN: pointer or row start not 16-byte aligned";
+    case TQ_ERR_UNSUPPORTED: return "TQ_ERR_UNSUPPORTED: format/dtype/shape combination not provided";
+    case TQ_ERR_CUDA: return "TQ_ERR_CUDA: a CUDA call failed";
+    case TQ_ERR_RANGE: return "TQ_ERR_RANGE: a rotated activation overflowed fp16";
+    case TQ_ERR_TIMEOUT: return "TQ_ERR_TIMEOUT: a kernel gave up a bounded wait; its outputs are not meaningful";
+    default: return "unknown tq_status";
+  }
+}
+
+int tq_version(void) { return 100; }
+
+int64_t tq_packed_ld(int64_t K, int fmt) {
+  if (K <= 0) return -1;
+  if (fmt == TQ_PACK_2BIT) return K % 4 == 0 ? K / 4 : -1;
+  if (fmt == TQ_PACK_BASE3) return ld3_min(K);
+  return -1;
+}
+
+tq_status tq_fwht128(const void* x, int xt, int64_t ldx, void* y, int yt, int64_t ldy, int64_t rows, int64_t K,
+                     tq_stream stream) {
+  if (xt != TQ_F32 && xt != TQ_BF16) return TQ_ERR_INVALID_ARG;
+  if (yt != TQ_F32 && yt != TQ_BF16 && yt != TQ_F16) return TQ_ERR_INVALID_ARG;
+  if (rows < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_ok(K)) return TQ_ERR_SHAPE;
+  if (rows == 0) return TQ_OK;
+  if (x == nullptr || y == nullptr) return TQ_ERR_INVALID_ARG;
+  if (ldx < K || ldy < K) return TQ_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(y) || (ldx * dtype_size(xt)) % 16 || (ldy * dtype_size(yt)) % 16)
+    return TQ_ERR_ALIGN;
+  if (x == y && (xt != yt || ldx != ldy)) return TQ_ERR_INVALID_ARG;
+  return from_cuda(launch_fwht128(x, xt, ldx, y, yt, ldy, rows, K, false, nullptr, (cudaStream_t)stream));
+}
+
+tq_status tq_quantize_pack(const void* W, int wt, int64_t N, int64_t K, int64_t ldw, int fmt, uint8_t* codes2,
+                           int64_t ld2, uint8_t* codes3, int64_t ld3, uint16_t* scales, int64_t lds,
+                           tq_stream stream) {
+  if (wt != TQ_F32 && wt != TQ_BF16) return TQ_ERR_INVALID_ARG;
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3 && fmt != TQ_PACK_BOTH) return TQ_ERR_INVALID_ARG;
+  if (N < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_ok(K)) return TQ_ERR_SHAPE;
+  if (N == 0) return TQ_OK;
+  const bool do2 = (fmt & TQ_PACK_2BIT) != 0, do3 = (fmt & TQ_PACK_BASE3) != 0;
+  if (W == nullptr || scales == nullptr || (do2 && codes2 == nullptr) || (do3 && codes3 == nullptr))
+    return TQ_ERR_INVALID_ARG;
+  if (ldw < K || lds < K / 128 || (do2 && ld2 < K / 4) || (do3 && ld3 < ld3_min(K))) return TQ_ERR_SHAPE;
+  if (!aligned16(W) || (ldw * dtype_size(wt)) % 16 || !aligned2(scales)) return TQ_ERR_ALIGN;
+  return from_cuda(launch_quantize_pack(W, wt, N, K, ldw, fmt, do2 ? codes2 : nullptr, ld2, do3 ? codes3 : nullptr,
+                                        ld3, scales, lds, (cudaStream_t)stream));
+}
+
+tq_status tq_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
+                  int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, tq_stream stream) {
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return TQ_ERR_INVALID_ARG;
+  if (N < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_ok(K) || M < 1 || M > 16) return TQ_ERR_SHAPE;
+  if (N == 0) return TQ_OK;
+  if (codes == nullptr || scales == nullptr || x == nullptr || y == nullptr) return TQ_ERR_INVALID_ARG;
+  if (ldc < tq_packed_ld(K, fmt) || lds < K / 128 || ldx < K || ldy < N) return TQ_ERR_SHAPE;
+  if (!aligned16(codes) || ldc % 16 || !aligned2(scales) || !aligned16(x) || (ldx * 2) % 16 ||
+      (reinterpret_cast<uintptr_t>(y) & 3u))
+    return TQ_ERR_ALIGN;
+  return from_cuda(launch_gemv(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy, (cudaStream_t)stream));
+}
+
+size_t tq_gemm_workspace_bytes(int64_t M, int64_t K) {
+  if (M < 0 || K < 0) return 0;
+  return 256 + (size_t)M * (size_t)K * 2;
+}
+
+tq_status tq_gemm(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
+                  int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, void* workspace,
+                  size_t ws_bytes, tq_stream stream) {
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return TQ_ERR_INVALID_ARG;
+  if (N < 0 || M < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_ok(K)) return TQ_ERR_SHAPE;
+  if (N == 0 || M == 0) return TQ_OK;
+  if (fmt != TQ_PACK_2BIT) return TQ_ERR_UNSUPPORTED;
+  if (codes == nullptr || scales == nullptr || x == nullptr || y == nullptr || workspace == nullptr)
+    return TQ_ERR_INVALID_ARG;
+  if (ldc < K / 4 || lds < K / 128 || ldx < K || ldy < N) return TQ_ERR_SHAPE;
+  if (ws_bytes < tq_gemm_workspace_bytes(M, K)) return TQ_ERR_SHAPE;
+  if (!aligned16(codes) || ldc % 16 || !aligned2(scales) || !aligned16(x) || (ldx * 2) % 16 ||
+      !aligned16(workspace) || !aligned16(y) || ldy % 4)
+    return TQ_ERR_ALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t* flag = static_cast<uint32_t*>(workspace);
+  uint16_t* xrot = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(workspace) + 256);
+  cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return TQ_ERR_CUDA;
+  e = launch_fwht128(x, TQ_BF16, ldx, xrot, TQ_F16, K, M, K, true, flag, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, s));
+}
+
+tq_status tq_gemm_check_range(const void* workspace, tq_stream stream) {
+  if (workspace == nullptr) return TQ_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return TQ_ERR_ALIGN;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return TQ_ERR_CUDA;
+  uint32_t flag = 0;
+  if (cudaMemcpy(&flag, workspace, sizeof(flag), cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ERR_CUDA;
+  return (flag & 1u) ? TQ_ERR_RANGE : TQ_OK;
+}
+
+tq_status tq_device_fault(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
+  return take_fault_gemv() ? TQ_ERR_TIMEOUT : TQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,36 @@
+// tq_internal.h -- declarations shared by the libtq translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/tq.h"
+#include "tq_device.cuh"
+
+namespace tq {
+
+// Device properties of the current device, cached per device (read-only
+// after the first query).
+int device_sm_count();
+int device_max_smem_optin();
+
+cudaError_t launch_fwht128(const void* x, int xt, int64_t ldx, void* y, int yt, int64_t ldy, int64_t rows,
+                           int64_t K, bool perm16, uint32_t* flag, cudaStream_t s);
+
+cudaError_t launch_quantize_pack(const void* W, int wt, int64_t N, int64_t K, int64_t ldw, int fmt,
+                                 uint8_t* codes2, int64_t ld2, uint8_t* codes3, int64_t ld3, uint16_t* scales,
+                                 int64_t lds, cudaStream_t s);
+
+cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
+                        int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, cudaStream_t s);
+
+// Returns cudaErrorNotSupported when the shape needs more shared memory than
+// one CTA can have.
+cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
+                        const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, cudaStream_t s);
+
+// Reads and clears the device status word of the GEMV kernels (non-zero:
+// a bounded wait ran out).
+unsigned int take_fault_gemv();
+
+}  // namespace tq

@@ -1,0 +1,153 @@
+"""The C ABI on the host: the library loads without a GPU, exports every
+symbol include/tq.h declares, and rejects bad arguments before any launch.
+
+Every call below fails host-side validation (or is an empty no-op), so the
+fake device pointers are never dereferenced and no CUDA work is issued."""
+from __future__ import annotations
+
+import os
+import re
+
+import pytest
+
+import ternary_weight_fwht128_gb300 as tq
+from ternary_weight_fwht128_gb300 import build as tqbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "tq.h")
+A = 0x10000   # 16-byte aligned fake device address (never dereferenced)
+B = 0x20000
+MIS = 0x10008  # 8-byte aligned only
+
+
+@pytest.fixture(scope="module")
+def L():
+    tqbuild.build()
+    return tq.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"TQ_API[^;(]*?\b(tq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    syms = declared_symbols()
+    assert len(syms) >= 9
+    for s in syms:
+        assert hasattr(L, s), f"{s} not exported"
+    assert sorted(tq.EXPORTED) == syms
+
+
+def test_status_strings_and_version(L):
+    names = ["TQ_OK", "TQ_ERR_INVALID_ARG", "TQ_ERR_SHAPE", "TQ_ERR_ALIGN", "TQ_ERR_UNSUPPORTED", "TQ_ERR_CUDA",
+             "TQ_ERR_RANGE", "TQ_ERR_TIMEOUT"]
+    for st, name in enumerate(names):
+        assert tq.status_string(st).startswith(name)
+    assert tq.status_string(99) == "unknown tq_status"
+    assert L.tq_version() == 100
+
+
+def test_packed_ld(L):
+    assert tq.packed_ld(5120, tq.TQ_PACK_2BIT) == 1280
+    assert tq.packed_ld(5120, tq.TQ_PACK_BASE3) == 1024
+    assert tq.packed_ld(27648, tq.TQ_PACK_BASE3) == 5536   # ceil(27648/5) = 5530 -> 5536
+    assert tq.packed_ld(128, tq.TQ_PACK_BASE3) == 32       # 26 -> 32
+    assert tq.packed_ld(0, tq.TQ_PACK_2BIT) == -1
+    assert tq.packed_ld(128, 7) == -1
+
+
+def test_gemm_workspace_bytes(L):
+    assert tq.gemm_workspace_bytes(2048, 5120) == 256 + 2048 * 5120 * 2
+    assert tq.gemm_workspace_bytes(-1, 5) == 0
+
+
+def test_fwht_validation(L):
+    f = L.tq_fwht128
+    assert f(A, tq.TQ_F32, 256, B, tq.TQ_F32, 256, 0, 256, None) == tq.TQ_OK          # empty
+    assert f(A, 7, 256, B, tq.TQ_F32, 256, 4, 256, None) == tq.TQ_ERR_INVALID_ARG
+    assert f(A, tq.TQ_F16, 256, B, tq.TQ_F32, 256, 4, 256, None) == tq.TQ_ERR_INVALID_ARG
+    assert f(A, tq.TQ_F32, 256, B, 9, 256, 4, 256, None) == tq.TQ_ERR_INVALID_ARG
+    assert f(A, tq.TQ_F32, 256, B, tq.TQ_F32, 256, -1, 256, None) == tq.TQ_ERR_INVALID_ARG
+    assert f(A, tq.TQ_F32, 256, B, tq.TQ_F32, 256, 4, 200, None) == tq.TQ_ERR_SHAPE
+    assert f(A, tq.TQ_F32, 256, B, tq.TQ_F32, 256, 4, 0, None) == tq.TQ_ERR_SHAPE
+    assert f(None, tq.TQ_F32, 256, B, tq.TQ_F32, 256, 4, 256, None) == tq.TQ_ERR_INVALID_ARG
+    assert f(A, tq.TQ_F32, 128, B, tq.TQ_F32, 256, 4, 256, None) == tq.TQ_ERR_SHAPE
+    assert f(MIS, tq.TQ_F32, 256, B, tq.TQ_F32, 256, 4, 256, None) == tq.TQ_ERR_ALIGN
+    assert f(A, tq.TQ_F32, 258, B, tq.TQ_F32, 256, 4, 256, None) == tq.TQ_ERR_ALIGN   # row stride not 16 B
+    assert f(A, tq.TQ_F32, 256, A, tq.TQ_F16, 256, 4, 256, None) == tq.TQ_ERR_INVALID_ARG  # in place, dtypes differ
+
+
+def test_quantize_validation(L):
+    f = L.tq_quantize_pack
+    ok = dict(W=A, wt=tq.TQ_BF16, N=4, K=256, ldw=256, fmt=tq.TQ_PACK_BOTH, c2=B, ld2=64, c3=B + 4096, ld3=64,
+              s=B + 8192, lds=2)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["W"], a["wt"], a["N"], a["K"], a["ldw"], a["fmt"], a["c2"], a["ld2"], a["c3"], a["ld3"], a["s"],
+                 a["lds"], None)
+
+    assert call(N=0) == tq.TQ_OK
+    assert call(wt=tq.TQ_F16) == tq.TQ_ERR_INVALID_ARG
+    assert call(fmt=0) == tq.TQ_ERR_INVALID_ARG
+    assert call(N=-2) == tq.TQ_ERR_INVALID_ARG
+    assert call(K=100) == tq.TQ_ERR_SHAPE
+    assert call(c2=None) == tq.TQ_ERR_INVALID_ARG
+    assert call(c3=None) == tq.TQ_ERR_INVALID_ARG
+    assert call(s=None) == tq.TQ_ERR_INVALID_ARG
+    assert call(ld2=63) == tq.TQ_ERR_SHAPE
+    assert call(ld3=52) == tq.TQ_ERR_SHAPE           # ceil(256/5) = 52, padded minimum is 64
+    assert call(lds=1) == tq.TQ_ERR_SHAPE
+    assert call(ldw=255) == tq.TQ_ERR_SHAPE
+    assert call(W=MIS) == tq.TQ_ERR_ALIGN
+    assert call(s=B + 8193) == tq.TQ_ERR_ALIGN
+    # a format that does not write a layout does not need its pointer
+    assert call(fmt=tq.TQ_PACK_2BIT, c3=None, N=0) == tq.TQ_OK
+
+
+def test_gemv_validation(L):
+    f = L.tq_gemv
+    ok = dict(c=A, ldc=64, fmt=tq.TQ_PACK_2BIT, s=B, lds=2, N=8, K=256, x=B + 4096, ldx=256, M=1, y=B + 8192, ldy=8)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["c"], a["ldc"], a["fmt"], a["s"], a["lds"], a["N"], a["K"], a["x"], a["ldx"], a["M"], a["y"],
+                 a["ldy"], None)
+
+    assert call(N=0) == tq.TQ_OK
+    assert call(fmt=3) == tq.TQ_ERR_INVALID_ARG
+    assert call(M=0) == tq.TQ_ERR_SHAPE
+    assert call(M=17) == tq.TQ_ERR_SHAPE
+    assert call(K=384 + 1) == tq.TQ_ERR_SHAPE
+    assert call(ldc=48) == tq.TQ_ERR_SHAPE
+    assert call(fmt=tq.TQ_PACK_BASE3, ldc=48) == tq.TQ_ERR_SHAPE   # base-3 needs 64 for K = 256
+    assert call(ldy=7) == tq.TQ_ERR_SHAPE
+    assert call(ldx=128) == tq.TQ_ERR_SHAPE
+    assert call(x=None) == tq.TQ_ERR_INVALID_ARG
+    assert call(c=MIS) == tq.TQ_ERR_ALIGN
+    assert call(ldc=72) == tq.TQ_ERR_ALIGN
+    assert call(x=MIS) == tq.TQ_ERR_ALIGN
+    assert call(y=B + 8194) == tq.TQ_ERR_ALIGN
+
+
+def test_gemm_validation(L):
+    f = L.tq_gemm
+    ws = tq.gemm_workspace_bytes(4, 256)
+    ok = dict(c=A, ldc=64, fmt=tq.TQ_PACK_2BIT, s=B, lds=2, N=8, K=256, x=B + 4096, ldx=256, M=4, y=B + 8192, ldy=8,
+              w=B + 65536, wsb=ws)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["c"], a["ldc"], a["fmt"], a["s"], a["lds"], a["N"], a["K"], a["x"], a["ldx"], a["M"], a["y"],
+                 a["ldy"], a["w"], a["wsb"], None)
+
+    assert call(M=0) == tq.TQ_OK
+    assert call(N=0) == tq.TQ_OK
+    assert call(fmt=tq.TQ_PACK_BASE3) == tq.TQ_ERR_UNSUPPORTED
+    assert call(wsb=ws - 1) == tq.TQ_ERR_SHAPE
+    assert call(w=None) == tq.TQ_ERR_INVALID_ARG
+    assert call(w=B + 65544) == tq.TQ_ERR_ALIGN
+    assert call(ldy=10) == tq.TQ_ERR_ALIGN
+    assert call(K=0) == tq.TQ_ERR_SHAPE
+    assert L.tq_gemm_check_range(None, None) == tq.TQ_ERR_INVALID_ARG
+    assert L.tq_gemm_check_range(MIS, None) == tq.TQ_ERR_ALIGN

@@ -1,0 +1,188 @@
+"""CUDA path against the CPU oracle, through the C ABI (needs a GB300)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import ternary_weight_fwht128_gb300 as tq
+from ternary_weight_fwht128_gb300 import synth
+from tq_testutil import check_y, guarded, to_dev_bf16, to_dev_f32, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tq.lib()
+    torch.cuda.set_device(0)
+
+
+# ------------------------------------------------------------------ FWHT
+
+@pytest.mark.parametrize("rows,K", [(1, 128), (37, 384), (5, 5120), (3, 27648)])
+def test_fwht_f32_bitexact(orc, rows, K):
+    rng = np.random.default_rng(rows * 1000 + K)
+    x = (rng.standard_normal((rows, K)) * rng.uniform(0.01, 30, size=(rows, 1))).astype(np.float32)
+    ref = orc.fwht128_f32(x)
+    out, check = guarded((rows, K), torch.float32)
+    tq.fwht128(to_dev_f32(x), out=out)
+    torch.cuda.synchronize()
+    check()
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_fwht_bf16_input_all_outputs(orc, out_dtype):
+    xb = synth.activations(19, 1024, 7)
+    ref = orc.fwht128_f32(synth.bf16_bits_to_f32(xb))
+    got = tq.fwht128(to_dev_bf16(xb), out_dtype=out_dtype)
+    if out_dtype == torch.float32:
+        assert np.array_equal(got.cpu().numpy(), ref)
+    elif out_dtype == torch.bfloat16:
+        assert np.array_equal(u16(got), synth.f32_to_bf16_bits(ref))
+    else:
+        assert np.array_equal(u16(got), ref.astype(np.float16).view(np.uint16))
+
+
+def test_fwht_in_place_and_strided(orc):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((9, 640)).astype(np.float32)
+    ref = orc.fwht128_f32(x[:, :512])
+    t = to_dev_f32(x)
+    sub = t[:, :512]  # ld 640, K 512
+    tq.fwht128(sub, out=sub)
+    got = t.cpu().numpy()
+    assert np.array_equal(got[:, :512], ref)
+    assert np.array_equal(got[:, 512:], x[:, 512:])  # untouched tail of each row
+
+
+def test_fwht_delta_rows(orc):
+    x = np.zeros((128, 128), dtype=np.float32)
+    x[np.arange(128), np.arange(128)] = 1.0
+    got = tq.fwht128(to_dev_f32(x)).cpu().numpy()
+    assert np.array_equal(got, orc.fwht128_f32(x))
+
+
+# ------------------------------------------------------------- quantise
+
+def _quant_check(orc, W, fmt=tq.TQ_PACK_BOTH, rows=None):
+    dev = to_dev_f32(W) if W.dtype == np.float32 else to_dev_bf16(W)
+    c2, c3, s = tq.quantize_pack(dev, fmt)
+    T, S = orc.quantize(W, rows)
+    sel = slice(None) if rows is None else torch.as_tensor(rows, device="cuda")
+    assert np.array_equal(u16(s[sel]), S), "scales differ"
+    K = W.shape[1]
+    if c2 is not None:
+        assert np.array_equal(c2[sel].cpu().numpy(), orc.pack2(T)), "2-bit codes differ"
+    if c3 is not None:
+        assert np.array_equal(c3[sel].cpu().numpy(), orc.pack3(T)), "base-3 codes differ"
+    return c2, c3, s, T, S
+
+
+def test_quantize_tiny_config(orc):
+    W, _ = synth.tiny_config()
+    _quant_check(orc, W)
+
+
+@pytest.mark.parametrize("N,K,dtype,fmt", [
+    (37, 384, "f32", tq.TQ_PACK_BOTH),
+    (1, 128, "bf16", tq.TQ_PACK_2BIT),
+    (3, 768, "bf16", tq.TQ_PACK_BASE3),   # six groups: a segment of five plus one
+    (65, 5120, "bf16", tq.TQ_PACK_BOTH),
+    (7, 27648, "bf16", tq.TQ_PACK_BOTH),  # 216 groups, last base-3 byte padded
+])
+def test_quantize_shapes(orc, N, K, dtype, fmt):
+    W = synth.weights(N, K, N + K, dtype=dtype)
+    _quant_check(orc, W, fmt)
+
+
+def test_quantize_special_groups(orc):
+    """All-zero groups (scale 0), tiny groups (fp16 underflow -> scale 0),
+    huge groups (scale inf -> trits 0), delta rows (rows of H)."""
+    K = 512
+    W = np.zeros((6, K), dtype=np.float32)
+    W[1, :128] = 1e-9
+    W[2, 128:256] = 3e6
+    W[3, 5] = 1.0
+    W[3, 300] = -2.0
+    W[4] = np.linspace(-1, 1, K, dtype=np.float32)
+    W[5, ::2] = 0.25
+    _quant_check(orc, W)
+
+
+def test_quantize_guard_bytes(orc):
+    N, K = 33, 640
+    W = synth.weights(N, K, 5, dtype="bf16")
+    c2, ck2 = guarded((N, K // 4), torch.uint8)
+    ld3 = tq.packed_ld(K, tq.TQ_PACK_BASE3)
+    c3, ck3 = guarded((N, ld3), torch.uint8)
+    s, cks = guarded((N, K // 128), torch.int16)
+    st = tq.lib().tq_quantize_pack(to_dev_bf16(W).data_ptr(), tq.TQ_BF16, N, K, K, tq.TQ_PACK_BOTH,
+                                   c2.data_ptr(), K // 4, c3.data_ptr(), ld3, s.data_ptr(), K // 128,
+                                   torch.cuda.current_stream().cuda_stream)
+    assert st == tq.TQ_OK
+    torch.cuda.synchronize()
+    ck2(); ck3(); cks()
+    T, S = orc.quantize(W)
+    assert np.array_equal(c2.cpu().numpy(), orc.pack2(T))
+    assert np.array_equal(c3.cpu().numpy(), orc.pack3(T))
+
+
+# ----------------------------------------------------------------- GEMV
+
+def _gemv_case(orc, N, K, M, seed, fmt=tq.TQ_PACK_2BIT, rows=None):
+    W = synth.weights(N, K, seed, dtype="bf16")
+    xb = synth.activations(M, K, seed + 1)
+    c2, c3, s = tq.quantize_pack(to_dev_bf16(W), fmt)
+    codes = c2 if fmt == tq.TQ_PACK_2BIT else c3
+    out, check = guarded((M, N), torch.float32)
+    tq.gemv(codes, s, to_dev_bf16(xb), K, fmt, out=out)
+    torch.cuda.synchronize()
+    check()
+    T, S = orc.quantize(W, rows)
+    ref = orc.gemv(T, S, synth.bf16_bits_to_f32(xb))
+    got = out.cpu().numpy()
+    if rows is not None:
+        got = got[:, rows]
+    return check_y(got, ref)
+
+
+def test_gemv_tiny_config(orc):
+    W, xb = synth.tiny_config()
+    c2, _, s = tq.quantize_pack(to_dev_f32(W), tq.TQ_PACK_2BIT)
+    y = tq.gemv(c2, s, to_dev_bf16(xb), 256)
+    T, S = orc.quantize(W)
+    check_y(y.cpu().numpy(), orc.gemv(T, S, synth.bf16_bits_to_f32(xb)))
+
+
+@pytest.mark.parametrize("N,K,M", [
+    (256, 256, 1), (37, 384, 3), (15, 128, 1), (1, 128, 16), (300, 1280, 2),
+    (1000, 1280, 4), (513, 2560, 8), (200, 640, 16), (64, 27648 // 4, 5),
+])
+def test_gemv_shapes(orc, N, K, M):
+    _gemv_case(orc, N, K, M, seed=N * 31 + K + M)
+
+
+@pytest.mark.parametrize("N,K", [(5120, 5120), (27648, 5120), (5120, 27648)])
+@pytest.mark.parametrize("M", [1, 16])
+def test_gemv_full_size_sampled(orc, N, K, M):
+    """The benchmark's shapes and launch configuration; the oracle checks a
+    seeded sample of 48 output rows (it cannot do all of them quickly)."""
+    rows = np.sort(np.random.default_rng(N + K + M).choice(N, size=48, replace=False))
+    rows[-1] = N - 1
+    _gemv_case(orc, N, K, M, seed=N + K + M, rows=rows)
+
+
+def test_gemv_zero_and_delta_activations(orc):
+    N, K = 96, 512
+    W = synth.weights(N, K, 9, dtype="bf16")
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    x = np.zeros((2, K), dtype=np.uint16)
+    x[1, 77] = synth.f32_to_bf16_bits(np.array([1.0], dtype=np.float32))[0]
+    y = tq.gemv(c2, s, to_dev_bf16(x), K).cpu().numpy()
+    assert np.all(y[0] == 0.0)
+    T, S = orc.quantize(W)
+    check_y(y[1:], orc.gemv(T, S, synth.bf16_bits_to_f32(x[1:])))
