@@ -1,0 +1,441 @@
+#!/usr/bin/env python3
+"""Benchmark of the ternary FWHT-128 linear-layer hot path on GB300.
+
+Headline (the `value` of the JSON line): decode GEMV throughput on packed
+weight bytes (codes + fp16 scales), GB/s, for one decode step = one token
+(M = 1) through the linear layers of a 64-layer stack of 27B-class shapes
+(per layer 5120x5120 x2, 27648x5120 x2, 5120x27648; 2-bit codes): 320 GEMV
+launches and 8.1 GB of packed weights per step, far larger than L2, so every
+step streams its weights from HBM.  The activation FWHT-128 runs inside every
+GEMV launch.  Extra keys report the other hot-path rows: skinny M = 2..16
+(2-bit and base-3), the tensor-core prefill GEMM (M = 2048), and the offline
+quantise + pack sweep.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+`--impl reference` times the CPU oracle (single core) on a bounded sample of
+the same workload and prints the same JSON line with "impl": "reference".
+Multi-GPU runs are independent replicas (the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HIDDEN, FFN, LAYERS = 5120, 27648, 64
+# (name, N, K, count per layer): two 5120x5120, two 27648x5120, one 5120x27648
+LAYER_SHAPES = [("h2h_a", HIDDEN, HIDDEN), ("h2h_b", HIDDEN, HIDDEN), ("gate", FFN, HIDDEN), ("up", FFN, HIDDEN),
+                ("down", HIDDEN, FFN)]
+METRIC = "ternary GEMV packed-weight HBM GB/s (% of peak); prefill GEMM TFLOP/s"
+WORKLOAD = ("decode GEMV M=1, 2-bit codes, 64-layer stack of 27B-class shapes "
+            "{5120x5120 x2, 27648x5120 x2, 5120x27648} per layer (320 launches, FWHT-128 fused)")
+
+
+def packed_bytes(N: int, K: int, fmt: str = "2bit") -> int:
+    """Algorithmic bytes a GEMV must read: packed codes + fp16 scales."""
+    codes = N * (K // 4) if fmt == "2bit" else N * (((K + 4) // 5 + 15) // 16 * 16)
+    return codes + N * (K // 128) * 2
+
+
+def step_bytes() -> int:
+    return LAYERS * sum(packed_bytes(N, K) for _, N, K in LAYER_SHAPES)
+
+
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- ranks
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (x itself when running alone)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while active."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def build_stack(tq, torch, dev, seed: int):
+    """64 layers of packed weights, quantised on the GPU from seeded synthetic
+    bf16 weights ~N(0, 0.02) with 0.1% of entries x20."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    stack = []
+    for layer in range(LAYERS):
+        mats = []
+        for name, N, K in LAYER_SHAPES:
+            W = torch.randn(N, K, device=dev, generator=gen, dtype=torch.float32).mul_(0.02)
+            n_out = max(1, (N * K) // 1000)
+            idx = torch.randint(0, N * K, (n_out,), device=dev, generator=gen)
+            W.view(-1)[idx] *= 20.0
+            Wb = W.to(torch.bfloat16)
+            del W
+            c2, _, s = tq.quantize_pack(Wb, tq.TQ_PACK_2BIT)
+            del Wb
+            mats.append((name, N, K, c2, s))
+        stack.append(mats)
+    return stack
+
+
+def activations(torch, dev, K: int, M: int, seed: int):
+    """x [M][K] bf16 ~N(0, 1) with 4 channels x30 (seeded)."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    x = torch.randn(M, K, device=dev, generator=gen)
+    ch = torch.randperm(K, device=dev, generator=gen)[:4]
+    x[:, ch] *= 30.0
+    return x.to(torch.bfloat16)
+
+
+def gpu_arm(args, world, rank, local):
+    import torch
+    import ternary_weight_fwht128_gb300 as tq
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+
+    stack = build_stack(tq, torch, dev, seed=1000 + rank)
+    xs = {K: activations(torch, dev, K, 1, seed=K) for K in (HIDDEN, FFN)}
+    ys = {N: torch.empty(1, N, device=dev) for N in (HIDDEN, FFN)}
+    launches_per_step = LAYERS * len(LAYER_SHAPES)
+
+    def step():
+        for mats in stack:
+            for _, N, K, c2, s in mats:
+                tq.gemv(c2, s, xs[K], K, tq.TQ_PACK_2BIT, out=ys[N])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world, dev)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world, dev)
+    ms_local = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms_local, world, dev)
+    bytes_step = step_bytes()
+    gbs = world * bytes_step / (ms * 1e-3) / 1e9
+    gbs_rank = bytes_step / (ms_local * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers: every step
+    # copies its activations in from pinned host memory (one token row per
+    # input width), runs the 320 GEMVs, and reads its outputs back.
+    hx = {K: xs[K].cpu().pin_memory() for K in xs}
+    hy = {N: torch.empty(1, N, dtype=torch.float32).pin_memory() for N in ys}
+    dx = {K: torch.empty_like(xs[K]) for K in xs}
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = sum(t.numel() * t.element_size() for t in hy.values())
+
+    def e2e_step():
+        for K in dx:
+            dx[K].copy_(hx[K], non_blocking=True)
+        for mats in stack:
+            for _, N, K, c2, s in mats:
+                tq.gemv(c2, s, dx[K], K, tq.TQ_PACK_2BIT, out=ys[N])
+        for N in hy:
+            hy[N].copy_(ys[N], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier(world, dev)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world, dev)
+    e2e_gbs = world * bytes_step / e2e_s / 1e9
+
+    extras = {}
+    if not args.quick:
+        extras = gpu_extras(args, tq, torch, dev, stack, pk)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u8 2-bit codes x fp16 scales, fp16 x' on mma.sync, fp32 accumulate",
+        "data": "synthetic (seeded; weights N(0,0.02)+0.1% x20 outliers, x N(0,1)+4 channels x30)",
+        "config": {"workload": WORKLOAD, "M": 1, "layers": LAYERS, "packed_bytes_per_step": bytes_step,
+                   "launches_per_step": launches_per_step,
+                   "l2": "inputs larger than L2 (8.1 GB of packed weights streamed per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "frac_of_peak": round(gbs_rank / pk["hbm_gbs"], 4),
+        "roofline": {"bound": "hbm", "achieved": round(gbs_rank, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs_rank / pk["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "k_gemv<1> (tq_gemv, M=1)",
+                     "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    line.update(extras)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def time_events(fn, reps: int, torch) -> float:
+    """Average ms of fn() over reps, CUDA events on the current stream."""
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fn()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
+    """Skinny decode (2-bit vs base-3), prefill GEMM and the quantise sweep."""
+    out = {}
+    # --- skinny M in {2,4,8,16} on 27648x5120 and 5120x27648: cycle over the
+    # stack's layers so that every launch streams from HBM
+    skinny = []
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    for (name, N, K) in (("gate", FFN, HIDDEN), ("down", HIDDEN, FFN)):
+        mats = [[m for m in layer if m[0] == name][0] for layer in stack]
+        for M in (2, 4, 8, 16):
+            x = activations(torch, dev, K, M, seed=K + M)
+            y = torch.empty(M, N, device=dev)
+            it = [0]
+
+            def run():
+                _, _, _, c2, s = mats[it[0] % len(mats)]
+                it[0] += 1
+                tq.gemv(c2, s, x, K, tq.TQ_PACK_2BIT, out=y)
+
+            ms = time_events(run, 3 * len(mats), torch)
+            gb = packed_bytes(N, K) / (ms * 1e-3) / 1e9
+            skinny.append({"shape": f"{N}x{K}", "M": M, "fmt": "2bit", "us": round(ms * 1e3, 2),
+                           "GB/s": round(gb, 1), "frac_of_peak": round(gb / pk["hbm_gbs"], 4),
+                           "TFLOP/s": round(2 * M * N * K / (ms * 1e-3) / 1e12, 2)})
+    out["skinny"] = skinny
+    # --- prefill GEMM, M = 2048 on the three shapes
+    prefill = []
+    for name, N, K in (("h2h_a", HIDDEN, HIDDEN), ("gate", FFN, HIDDEN), ("down", HIDDEN, FFN)):
+        _, _, _, c2, s = [m for m in stack[0] if m[0] == name][0]
+        M = 2048
+        x = activations(torch, dev, K, M, seed=11 + K)
+        ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+        y = torch.empty(M, N, device=dev)
+        try:
+            ms = time_events(lambda: tq.gemm(c2, s, x, K, tq.TQ_PACK_2BIT, workspace=ws, out=y), 10, torch)
+        except tq.TQError as e:
+            prefill.append({"shape": f"{N}x{K}", "M": M, "unavailable": str(e)})
+            continue
+        tf = 2 * M * N * K / (ms * 1e-3) / 1e12
+        prefill.append({"shape": f"{N}x{K}", "M": M, "us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                        "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4)})
+    out["prefill"] = prefill
+    # --- offline quantise + pack of one layer group, weights resident (bf16)
+    sweep = []
+    for name, N, K in (("h2h_a", HIDDEN, HIDDEN), ("gate", FFN, HIDDEN), ("down", HIDDEN, FFN)):
+        W = (torch.randn(N, K, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+        ms = time_events(lambda: tq.quantize_pack(W, tq.TQ_PACK_BOTH), 5, torch)
+        nbytes = N * K * 2 + N * (K // 4) + N * tq.packed_ld(K, tq.TQ_PACK_BASE3) + N * (K // 128) * 2
+        sweep.append({"shape": f"{N}x{K}", "fmt": "2bit+base3", "us": round(ms * 1e3, 1),
+                      "Gparams/s": round(N * K / (ms * 1e-3) / 1e9, 1),
+                      "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)})
+        del W
+    out["quantize_pack"] = sweep
+    return out
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(budget_s: float = 12.0) -> dict:
+    """The CPU oracle, as it stands, on a bounded sample of the decode
+    workload: fp64 GEMV of oracle-quantised 5120x5120 and 27648x5120 layers
+    (single core), repeated until the time budget is spent.  Reported in the
+    same unit: packed weight bytes consumed per second."""
+    import numpy as np
+
+    import oracle
+    from ternary_weight_fwht128_gb300 import synth
+
+    orc = oracle.load()
+    shapes = [(HIDDEN, HIDDEN), (1024, FFN), (FFN // 8, HIDDEN)]
+    prepared = []
+    for (N, K) in shapes:
+        W = synth.weights(N, K, N + K, dtype="bf16")
+        T, S = orc.quantize(W)
+        x = synth.bf16_bits_to_f32(synth.activations(1, K, K))
+        prepared.append((N, K, T, S, x))
+    done_bytes, spent, calls = 0, 0.0, 0
+    while spent < budget_s:
+        for (N, K, T, S, x) in prepared:
+            t0 = time.perf_counter()
+            orc.gemv(T, S, x)
+            spent += time.perf_counter() - t0
+            done_bytes += packed_bytes(N, K)
+            calls += 1
+    return {"value": round(done_bytes / spent / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{calls} oracle fp64 GEMVs (M=1) over 5120x5120, 1024x27648, 3456x5120 rows of "
+                      f"oracle-quantised synthetic weights, {spent:.1f} s of one host core"}
+
+
+def reference_arm(args, world, rank):
+    """The oracle as the reference implementation (single host core)."""
+    if rank != 0:
+        return
+    t_total = 0.0
+    base = None
+    for _ in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        base = cpu_baseline(budget_s=args.ref_budget)
+        t_total += time.perf_counter() - t0
+    line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": WORKLOAD, "M": 1, "sample": "bounded oracle sample per step"},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": base["sample"], "value": base["value"],
+                             "unit": "GB/s"},
+            "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--quick", action="store_true", help="headline decode step only (no extra sections)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-budget", type=float, default=4.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+        return
+    gpu_arm(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

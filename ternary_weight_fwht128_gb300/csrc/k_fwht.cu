@@ -1,11 +1,11 @@
 // k_fwht.cu -- block FWHT-128 of activation rows (tq_fwht128, and the
 // rotation pre-pass of tq_gemm).
 //
-// One warp rotates one 128-block (row r, group g) at a time; every lane loads
-// four consecutive elements (16 B for fp32, 8 B for bf16), so a warp moves
-// 256-512 contiguous bytes per block.  Each warp keeps kUnroll blocks' loads
-// in flight before it computes, which is what keeps HBM busy in this purely
-// bandwidth-bound pass.  The grid is a whole number of waves over the SMs.
+// A half-warp rotates one 128-block (row r, group g): lane p holds elements
+// 8p .. 8p+7, loaded with one 16-byte load (bf16) or two (fp32), so a warp
+// moves two blocks per load instruction.  Each warp keeps kUnroll block pairs
+// in flight before it computes; with four CTAs of eight warps per SM that is
+// 64-128 KB in flight per SM, which is what this bandwidth-bound pass needs.
 #include "tq_internal.h"
 
 namespace tq {
@@ -16,85 +16,132 @@ constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
 template <int XT>
-__device__ __forceinline__ void load4(const void* x, int64_t off, float v[4]) {
+struct Raw {
+  uint4 w[XT == TQ_F32 ? 2 : 1];
+};
+
+template <int XT>
+__device__ __forceinline__ void unpack8(const Raw<XT>& r, float v[8]) {
   if constexpr (XT == TQ_F32) {
-    const uint4 w = ldg_nc_u4(static_cast<const float*>(x) + off);
-    v[0] = __uint_as_float(w.x);
-    v[1] = __uint_as_float(w.y);
-    v[2] = __uint_as_float(w.z);
-    v[3] = __uint_as_float(w.w);
+    v[0] = __uint_as_float(r.w[0].x);
+    v[1] = __uint_as_float(r.w[0].y);
+    v[2] = __uint_as_float(r.w[0].z);
+    v[3] = __uint_as_float(r.w[0].w);
+    v[4] = __uint_as_float(r.w[1].x);
+    v[5] = __uint_as_float(r.w[1].y);
+    v[6] = __uint_as_float(r.w[1].z);
+    v[7] = __uint_as_float(r.w[1].w);
   } else {
-    bf16x4_to_f32(ldg_nc_u2(static_cast<const uint16_t*>(x) + off), v);
+    bf16x8_to_f32(r.w[0], v);
   }
 }
 
-// PERM16: inside every 16-element chunk store element order
-// 0,8,1,9,...,7,15 (the order in which the tensor-core GEMM unpacks its
-// weight codes, see k_gemm.cu).  FLAG: record fp16 overflow in *flag.
+// PERM16: inside every 16-element chunk store element order 0,8,1,9,...,7,15
+// (the order in which the tensor-core GEMM unpacks its weight codes, see
+// k_gemm.cu).  Lane p holds elements 8(p&1) .. 8(p&1)+7 of chunk p/2; the two
+// lanes of a chunk swap four values so each writes 8 interleaved slots.
+// FLAG: record fp16 overflow in *flag.
 template <int YT, bool PERM16>
-__device__ __forceinline__ void store4(void* y, int64_t row_off, int lane, const float v[4], uint32_t* flag) {
+__device__ __forceinline__ void store8(void* y, int64_t off, int p, const float v[8], uint32_t* flag, bool valid) {
   if constexpr (YT == TQ_F32) {
-    float4 o = make_float4(v[0], v[1], v[2], v[3]);
-    *reinterpret_cast<float4*>(static_cast<float*>(y) + row_off + 4 * lane) = o;
+    if (!valid) return;
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(y) + off + 8 * p);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
   } else if constexpr (YT == TQ_BF16) {
-    uint2 o = make_uint2(pack_bf162(v[0], v[1]), pack_bf162(v[2], v[3]));
-    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + row_off + 4 * lane) = o;
+    if (!valid) return;
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + off + 8 * p) =
+        make_uint4(pack_bf162(v[0], v[1]), pack_bf162(v[2], v[3]), pack_bf162(v[4], v[5]), pack_bf162(v[6], v[7]));
   } else {
-    __half h[4];
+    uint32_t h[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) h[j] = __float2half_rn(v[j]);
-    if (flag != nullptr) {
+    for (int j = 0; j < 4; ++j) h[j] = pack_half2(v[2 * j], v[2 * j + 1]);
+    if (flag != nullptr && valid) {
       bool bad = false;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) bad |= __hisinf(h[j]) != 0;
+      for (int j = 0; j < 4; ++j) {
+        const __half2 hh = *reinterpret_cast<const __half2*>(&h[j]);
+        bad |= (__hisinf(__low2half(hh)) != 0) | (__hisinf(__high2half(hh)) != 0);
+      }
       if (bad) atomicOr(flag, 1u);
     }
-    uint16_t* yp = static_cast<uint16_t*>(y) + row_off;
+    uint16_t* yp = static_cast<uint16_t*>(y) + off;
     if constexpr (PERM16) {
-      // element p of the 16-chunk goes to slot 2p (p < 8) or 2(p-8)+1
-      const int chunk = lane >> 2;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int p = 4 * (lane & 3) + j;
-        const int slot = p < 8 ? 2 * p : 2 * (p - 8) + 1;
-        yp[16 * chunk + slot] = __half_as_ushort(h[j]);
-      }
+      // even lane (elements a0..a7 of the chunk) writes slots 0..7 =
+      // a0 b0 a1 b1 a2 b2 a3 b3; odd lane (b0..b7) writes slots 8..15 =
+      // a4 b4 .. a7 b7.  Odd sends b0..b3, even sends a4..a7.
+      const bool odd = p & 1;
+      const uint32_t s0 = odd ? h[0] : h[2], s1 = odd ? h[1] : h[3];
+      const uint32_t r0 = __shfl_xor_sync(kFull, s0, 1), r1 = __shfl_xor_sync(kFull, s1, 1);
+      const uint32_t a01 = odd ? r0 : h[0], a23 = odd ? r1 : h[1];  // a(0..3) or a(4..7)
+      const uint32_t b01 = odd ? h[2] : r0, b23 = odd ? h[3] : r1;  // b(0..3) or b(4..7)
+      uint4 o;
+      o.x = __byte_perm(a01, b01, 0x5410);  // a_lo b_lo
+      o.y = __byte_perm(a01, b01, 0x7632);  // a_hi b_hi
+      o.z = __byte_perm(a23, b23, 0x5410);
+      o.w = __byte_perm(a23, b23, 0x7632);
+      if (valid) *reinterpret_cast<uint4*>(yp + 16 * (p >> 1) + 8 * (p & 1)) = o;
     } else {
-      uint2 o;
-      o.x = (uint32_t)__half_as_ushort(h[0]) | ((uint32_t)__half_as_ushort(h[1]) << 16);
-      o.y = (uint32_t)__half_as_ushort(h[2]) | ((uint32_t)__half_as_ushort(h[3]) << 16);
-      *reinterpret_cast<uint2*>(yp + 4 * lane) = o;
+      if (valid) *reinterpret_cast<uint4*>(yp + 8 * p) = make_uint4(h[0], h[1], h[2], h[3]);
     }
   }
 }
 
 template <int XT, int YT, bool PERM16>
-__global__ void __launch_bounds__(kThreads) k_fwht128(const void* __restrict__ x, int64_t ldx, void* y,
-                                                      int64_t ldy, int64_t rows, int64_t G, uint32_t* flag) {
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kThreads, 4) k_fwht128(const void* __restrict__ x, int64_t ldx, void* y,
+                                                         int64_t ldy, int64_t rows, int64_t G, uint32_t* flag) {
+  constexpr int esize = XT == TQ_F32 ? 4 : 2;
+  const int lane = threadIdx.x & 31, p = lane & 15, half = lane >> 4;
   const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
   const int64_t nblk = rows * G;
-  for (int64_t b0 = warp; b0 < nblk; b0 += nwarps * kUnroll) {
-    float v[kUnroll][4];
-    int64_t yo[kUnroll];
+  pdl_wait();
+  // Warp-iteration u covers block pair b0 + u * nwarps, i.e. blocks
+  // 2 * (b0 + u * nwarps) + {0, 1}.  Each lane walks its block sequence with
+  // a constant stride of 2 * nwarps blocks, advancing (row, group) and the
+  // element offsets incrementally (no division inside the loop).
+  const int64_t step = 2 * nwarps, dr = step / G, dg = step - (step / G) * G;
+  const int64_t b_first = 2 * warp + half;
+  int64_t g = b_first % G, r = b_first / G;
+  int64_t xo = r * ldx + g * 128, yo = r * ldy + g * 128;
+  const int64_t xadv = dr * ldx + dg * 128, yadv = dr * ldy + dg * 128;
+  const int64_t xwrap = ldx - G * 128, ywrap = ldy - G * 128;
+  for (int64_t b0 = warp; 2 * b0 < nblk; b0 += nwarps * kUnroll) {
+    Raw<XT> raw[kUnroll];
+    int64_t yof[kUnroll];
+    bool ok[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const int64_t b = b0 + (int64_t)u * nwarps;
-      yo[u] = -1;
-      if (b < nblk) {
-        const int64_t r = b / G, g = b - r * G;
-        load4<XT>(x, r * ldx + g * 128 + 4 * lane, v[u]);
-        yo[u] = r * ldy + g * 128;
+      ok[u] = r < rows;
+      yof[u] = yo;
+      raw[u].w[0] = make_uint4(0, 0, 0, 0);
+      if constexpr (XT == TQ_F32) raw[u].w[1] = raw[u].w[0];
+      if (ok[u]) {
+        const unsigned char* src = static_cast<const unsigned char*>(x) + (xo + 8 * p) * esize;
+        raw[u].w[0] = ldg_nc_u4(src);
+        if constexpr (XT == TQ_F32) raw[u].w[1] = ldg_nc_u4(src + 16);
+      }
+      g += dg;
+      r += dr;
+      xo += xadv;
+      yo += yadv;
+      if (g >= G) {
+        g -= G;
+        r += 1;
+        xo += xwrap;
+        yo += ywrap;
       }
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (yo[u] < 0) continue;  // warp-uniform
-      fwht128_lane(v[u], lane);
-      store4<YT, PERM16>(y, yo[u], lane, v[u], flag);
+      if (2 * (b0 + (int64_t)u * nwarps) >= nblk) break;  // warp-uniform
+      float v[8];
+      unpack8<XT>(raw[u], v);
+      fwht128_x8(v, lane);
+      store8<YT, PERM16>(y, yof[u], p, v, flag, ok[u]);
     }
   }
+  pdl_launch_dependents();
 }
 
 template <int XT, int YT, bool PERM16>
@@ -102,12 +149,20 @@ cudaError_t launch_t(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t r
                      cudaStream_t s) {
   const int64_t nblk = rows * G;
   const int sms = device_sm_count();
-  const int64_t want = (nblk + (kThreads / 32) - 1) / (kThreads / 32);
-  const int64_t cap = (int64_t)sms * 8;  // 8 CTAs of 256 threads per SM = full occupancy
+  const int64_t want = (nblk + 2 * (kThreads / 32) - 1) / (2 * (kThreads / 32));
+  const int64_t cap = (int64_t)sms * 4;  // 4 resident CTAs of 256 threads per SM
   int64_t grid = want < cap ? want : cap;
   if (grid < 1) grid = 1;
-  k_fwht128<XT, YT, PERM16><<<(unsigned)grid, kThreads, 0, s>>>(x, ldx, y, ldy, rows, G, flag);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_fwht128<XT, YT, PERM16>, x, ldx, y, ldy, rows, G, flag);
 }
 
 }  // namespace

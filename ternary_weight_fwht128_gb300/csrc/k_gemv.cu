@@ -3,26 +3,28 @@
 //   y[m][n] = sum_g s[n][g] * sum_{k in g} t[n][k] * x'[m][k],  x' = FWHT-128(x)
 //
 // Decode is bound by the HBM stream of packed weights (mhpq.cn/news/1159370
-// sec. 4.2), so the kernel is built around reading the codes once, with many
-// bytes in flight and few instructions per weight:
+// sec. 4.2), so the kernel reads the codes exactly once, in 16-byte loads
+// with enough of them in flight, and spends few instructions per weight:
 //
 // * Work split.  A thread-block cluster of kCl CTAs owns a range of 16-row
 //   tiles; CTA rank r of the cluster owns the r-th slice of the K groups.
 //   Each CTA rotates only its own slice of x (no CTA repeats another's
 //   transform) and keeps it in shared memory as fp16; the kCl partial sums of
 //   every output are added through distributed shared memory at the end
-//   (fixed order, no global atomics, no workspace).
-// * Weight stream.  One producer warp copies "stages" (16 rows x up to
-//   kStageGroups groups of codes) from global into a ring of kSlots shared
-//   buffers with cp.async.bulk, completing on mbarriers; about 100 KB are in
-//   flight per SM, which is what HBM needs to run near its peak.  Sixteen
-//   consumer warps take the stages round-robin.
+//   (fixed order, no global atomics, no workspace).  Inside a CTA, (tile,
+//   group pair) units are dealt to the warps in contiguous ranges.
+// * Loads.  Lane (gid, tq) reads 8 bytes (32 codes) of each of the unit's two
+//   groups, for row gid and for row gid + 8; a warp instruction therefore
+//   moves 8 rows x 32 contiguous bytes (whole sectors).  Each warp keeps
+//   kDepth units in flight in registers (64 KB per SM), which is what HBM
+//   needs to run near its peak.
 // * Inner product on tensor cores (mma.sync m16n8k16, fp16 x fp16 -> fp32):
 //   A = 16 weight rows x 16 k as fp16 trits, B = 16 k x 8 activation columns.
-//   Lane (gid, tq) reads 8 bytes (32 codes) of row gid and of row gid + 8 per
-//   group; those codes feed the lane's four k-slots of each of the group's
-//   eight MMAs.  The dot product does not depend on which physical k sits in
-//   which slot as long as A and B agree, so x' is stored already permuted.
+//   The four lanes of a quad feed one MMA from a single group (its scale is
+//   applied afterwards): lane tq's 32 codes fill its four k-slots of each of
+//   the group's eight MMAs.  Which physical k sits in which MMA slot does not
+//   change the dot product as long as A and B agree, so x' is stored in
+//   shared memory already permuted to match.
 // * Trit decode: code c (= t + 1) sits at bits 2j..2j+1 of a 16-bit half;
 //   OR-ing the exponent of 2^(10-2j) over it gives the fp16 value
 //   2^(10-2j) + c, and subtracting 2^(10-2j) + 1 leaves t exactly (one LOP3
@@ -35,20 +37,20 @@ namespace tq {
 
 namespace {
 
-constexpr int kCl = 2;            // CTAs per cluster (split of K)
-constexpr int kConsumers = 16;    // consumer warps per CTA
-constexpr int kThreads = 32 * (kConsumers + 1);
-constexpr int kStageGroups = 8;   // groups per stage and row (256 bytes)
-constexpr int kPitch = kStageGroups * 32 + 32;  // padded row: 2 wavefronts per 64-bit lane read
-constexpr int kStageBytes = 16 * kPitch;
-constexpr int kSlots = 24;
-static_assert(2 * kSlots * 8 + 16 <= 1024, "barrier area");
+constexpr int kCl = 2;       // CTAs per cluster (split of K)
+constexpr int kWarps = 16;   // warps per CTA
+constexpr int kThreads = 32 * kWarps;
+constexpr int kDepth = 4;    // units of codes in flight per warp
 
-__device__ unsigned int g_fault;  // set when a bounded wait ran out
+struct Unit {
+  uint2 a0, a1, b0, b1;        // 32 codes of groups g, g + 1 for rows gid (a) and gid + 8 (b)
+  uint32_t sa, sb;             // fp16 scales of the two groups (low = first)
+};
 
 __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
-  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 // Trits of codes j (low half) and j + 8 (high half) of a 16-code word as an
@@ -67,7 +69,7 @@ __device__ __forceinline__ uint32_t trit_pair(uint32_t w, uint32_t w10) {
 
 __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -117,30 +119,127 @@ struct Params {
   int64_t ldy;
   int clusters;      // tile ranges: cluster c owns [c*T/clusters, (c+1)*T/clusters)
   int chunk_groups;  // K groups whose rotated activations are in shared memory at once
-  int xs_bytes;      // shared bytes for those activations
+  int xs_bytes;      // shared bytes for those activations (permuted x', then per-group sums)
+  int sum_off;       // byte offset of the per-group sums of x' inside that region
   int ms;            // activation rows stored per (group, quad): 1 for M == 1, else M
 };
 
-// Rotated activations in shared memory (fp16), per chunk-local group gl:
-//   entry (gl, tq, m, i) = 4 fp16 at byte offset
-//     gl*XG + tq*XQ + m*64 + i*8,  XQ = ms*64 + 16 (pad), XG = 4*XQ
-//   holding x'[m][128 g + 32 tq + {0, 8, 16, 24} + i] -- the four activations
-//   lane quad tq multiplies with the codes feeding MMA i.
+// Rotated activations in shared memory (fp16).  Lane tq of a quad holds the
+// codes of k = 128 g + 32 tq + 0..31.  Entry (gl, tq, m, i) = 4 fp16 at byte
+// offset gl*XG + tq*XQ + m*64 + i*8, XQ = ms*64 + 16 (pad), XG = 4*XQ, holds
+// x'[m][128 g + 32 tq + {0, 8, 16, 24} + i]: the activations MMA i multiplies
+// with the lane's codes.
 __host__ __device__ constexpr int xs_quad_bytes(int ms) { return ms * 64 + 16; }
 __host__ __device__ constexpr int xs_group_bytes(int ms) { return 4 * xs_quad_bytes(ms); }
 
-// Shared memory: [barriers][stage ring][x' chunk][partial y]
+template <int MB>
+__device__ __forceinline__ void group_mma(uint32_t wa0, uint32_t wa1, uint32_t wb0, uint32_t wb1, uint32_t xq,
+                                          int dm1, float c0v[4], float c1v[4]) {
+  const uint32_t a_lo10 = wa0 >> 10, a_hi10 = wa1 >> 10;
+  const uint32_t b_lo10 = wb0 >> 10, b_hi10 = wb1 >> 10;
+#define TQ_MMA_ONE(I, B0, B1)                                                              \
+  {                                                                                        \
+    const uint32_t a0 = trit_pair<I>(wa0, a_lo10), a2 = trit_pair<I>(wa1, a_hi10);         \
+    const uint32_t a1 = trit_pair<I>(wb0, b_lo10), a3 = trit_pair<I>(wb1, b_hi10);         \
+    mma16816(c0v, a0, a1, a2, a3, B0, B1);                                                 \
+    if (MB == 16) {                                                                        \
+      const uint2 bc = lds_u2(xq + dm1 + (I)*8);                                           \
+      mma16816(c1v, a0, a1, a2, a3, bc.x, bc.y);                                           \
+    }                                                                                      \
+  }
+#define TQ_MMA_PAIR(I)                   \
+  {                                      \
+    const uint4 bq = lds_u4(xq + (I)*8); \
+    TQ_MMA_ONE(I, bq.x, bq.y)            \
+    TQ_MMA_ONE((I) + 1, bq.z, bq.w)      \
+  }
+  TQ_MMA_PAIR(0)
+  TQ_MMA_PAIR(2)
+  TQ_MMA_PAIR(4)
+  TQ_MMA_PAIR(6)
+#undef TQ_MMA_PAIR
+#undef TQ_MMA_ONE
+}
+
+// Codes j and j + 8 of a 16-code word, masked in place: as fp16 subnormals
+// they are exactly c * 2^(2jj - 24) (c = t + 1 in {0, 1, 2}).  One LOP3 per
+// two weights and no fp16 arithmetic; the tensor cores take fp16 subnormals
+// exactly and the products c * x' are exact in fp32.
+template <int J>
+__device__ __forceinline__ uint32_t code_pair_sub(uint32_t w, uint32_t w10) {
+  constexpr int jj = J < 5 ? J : J - 5;
+  constexpr uint32_t mask = 0x00030003u << (2 * jj);
+  return (J < 5 ? w : w10) & mask;
+}
+
+// One group with the subnormal decode (M <= 8): MMA i lands in the
+// accumulator of its bit position jj (codes 0..4 and 5..7 share positions
+// 0..2), so accumulator jj holds 2^(2jj - 24) * (sum of c x' over its slots).
+// Returns, per C fragment entry, 2^-24 * sum_k c_k x'_k = sum_jj 4^-jj acc_jj
+// (powers of two: the weights are exact).
+__device__ __forceinline__ void group_sub(uint32_t wa0, uint32_t wa1, uint32_t wb0, uint32_t wb1, uint32_t xq,
+                                          float v[4]) {
+  const uint32_t a_lo10 = wa0 >> 10, a_hi10 = wa1 >> 10;
+  const uint32_t b_lo10 = wb0 >> 10, b_hi10 = wb1 >> 10;
+  float c[5][4];
+#pragma unroll
+  for (int q = 0; q < 5; ++q) c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.0f;
+#define TQ_SUB_ONE(I, B0, B1)                                                              \
+  {                                                                                        \
+    const uint32_t a0 = code_pair_sub<I>(wa0, a_lo10), a2 = code_pair_sub<I>(wa1, a_hi10); \
+    const uint32_t a1 = code_pair_sub<I>(wb0, b_lo10), a3 = code_pair_sub<I>(wb1, b_hi10); \
+    mma16816(c[(I) < 5 ? (I) : (I)-5], a0, a1, a2, a3, B0, B1);                            \
+  }
+#define TQ_SUB_PAIR(I)                   \
+  {                                      \
+    const uint4 bq = lds_u4(xq + (I)*8); \
+    TQ_SUB_ONE(I, bq.x, bq.y)            \
+    TQ_SUB_ONE((I) + 1, bq.z, bq.w)      \
+  }
+  TQ_SUB_PAIR(0)
+  TQ_SUB_PAIR(2)
+  TQ_SUB_PAIR(4)
+  TQ_SUB_PAIR(6)
+#undef TQ_SUB_PAIR
+#undef TQ_SUB_ONE
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float t = fmaf(0.25f, c[1][e], c[0][e]);
+    t = fmaf(0.0625f, c[2][e], t);
+    t = fmaf(0.015625f, c[3][e], t);
+    v[e] = fmaf(0.00390625f, c[4][e], t);
+  }
+}
+
+template <int MB>
+__device__ __forceinline__ void scale_add(float acc[8], const float c0v[4], const float c1v[4], float sa, float sb) {
+  acc[0] = fmaf(sa, c0v[0], acc[0]);
+  acc[1] = fmaf(sa, c0v[1], acc[1]);
+  acc[2] = fmaf(sb, c0v[2], acc[2]);
+  acc[3] = fmaf(sb, c0v[3], acc[3]);
+  if (MB == 16) {
+    acc[4] = fmaf(sa, c1v[0], acc[4]);
+    acc[5] = fmaf(sa, c1v[1], acc[5]);
+    acc[6] = fmaf(sb, c1v[2], acc[6]);
+    acc[7] = fmaf(sb, c1v[3], acc[7]);
+  }
+}
+
+// Per-(group, activation row) sums of the fp16-rounded x', used by the
+// subnormal decode: sum_k t_k x'_k = sum_k c_k x'_k - sum_k x'_k.  Stride 1
+// (M == 1) or 8 floats per group.
+__host__ __device__ constexpr int xsum_stride(int mb) { return mb == 1 ? 1 : 8; }
+
+// Shared memory: [x' chunk][x' group sums][partial y]
 template <int MB>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kSlots;
-  volatile int* abort = reinterpret_cast<volatile int*>(empty + kSlots);
-  unsigned char* ring = smem + 1024;
-  unsigned char* xs = ring + kSlots * kStageBytes;
-  float* ypart = reinterpret_cast<float*>(xs + p.xs_bytes);
+  unsigned char* xs = smem;
+  float* xsum = reinterpret_cast<float*>(smem + p.sum_off);
+  float* ypart = reinterpret_cast<float*>(smem + p.xs_bytes);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tq = lane & 3;
   const int M = p.M;
   const uint32_t rank = cluster_rank();
   const int64_t cluster = blockIdx.x / kCl;
@@ -150,177 +249,160 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
   const int64_t t0 = ntiles_all * cluster / p.clusters;
   const int ntiles = (int)(ntiles_all * (cluster + 1) / p.clusters - t0);
   const int nchunks = (int)((g1 - g0 + p.chunk_groups - 1) / p.chunk_groups);
+  const int ms = p.ms;
+  const int mB0 = MB == 1 ? 0 : (gid < M ? gid : M - 1);  // B column of this lane
+  const int mB1 = (8 + gid) < M ? 8 + gid : M - 1;        // second MMA (M > 8)
+  const int dm1 = (mB1 - mB0) * 64;
+  const uint32_t xs_base = smem_u32(xs);
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    *abort = 0;
-    fence_mbar_init();
-  }
   for (int i = threadIdx.x; i < ntiles * 16 * M; i += kThreads) ypart[i] = 0.0f;
-  __syncthreads();
   // Inputs (codes, scales, x) may come from the preceding kernel on the stream.
   pdl_wait();
 
-  // Stage numbering: chunk-major, then tile, then group block inside the chunk.
-  auto chunk_range = [&](int c, int64_t& cg0, int& ng, int& nsub) {
-    cg0 = g0 + (int64_t)c * p.chunk_groups;
-    const int64_t rest = g1 - cg0;
-    ng = (int)(rest < p.chunk_groups ? rest : p.chunk_groups);
-    nsub = (ng + kStageGroups - 1) / kStageGroups;
-  };
+  for (int c = 0; c < nchunks; ++c) {
+    const int64_t cg0 = g0 + (int64_t)c * p.chunk_groups;
+    const int ng = (int)((g1 - cg0) < p.chunk_groups ? (g1 - cg0) : p.chunk_groups);
+    const int npairs = (ng + 1) >> 1;
+    const int U = ntiles * npairs;
+    const int u0 = (int)((int64_t)U * warp / kWarps), u1 = (int)((int64_t)U * (warp + 1) / kWarps);
 
-  if (warp == kConsumers) {
-    // ------------------------------------------------------------ producer
-    bool ok = true;
-    int s = 0;
-    for (int c = 0; c < nchunks && ok; ++c) {
-      int64_t cg0;
-      int ng, nsub;
-      chunk_range(c, cg0, ng, nsub);
-      for (int tl = 0; tl < ntiles && ok; ++tl) {
-        int64_t row = (t0 + tl) * 16 + (lane & 15);
-        if (row >= p.N) row = p.N - 1;
-        for (int sb = 0; sb < nsub; ++sb, ++s) {
-          const int slot = s % kSlots, use = s / kSlots;
-          if (use > 0 && !mbar_wait_abortable(&empty[slot], (use - 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          const int gs = sb * kStageGroups;
-          const int ngs = (ng - gs) < kStageGroups ? (ng - gs) : kStageGroups;
-          if (lane == 0) mbar_arrive_expect_tx(&full[slot], 16u * 32u * ngs);
-          __syncwarp();
-          if (lane < 16)
-            bulk_g2s(ring + slot * kStageBytes + lane * kPitch, p.codes + row * p.ldc + (cg0 + gs) * 32,
-                     32u * ngs, &full[slot]);
-        }
+    // loader iterator: unit (lt, lp); pointers at pair 0 of tile lt
+    int lt = npairs ? u0 / npairs : 0, lp = u0 - lt * npairs;
+    const uint8_t *pa = nullptr, *pb = nullptr;
+    const uint16_t *qa = nullptr, *qb = nullptr;
+    auto set_tile = [&]() {
+      int64_t ra = (t0 + lt) * 16 + gid, rb = ra + 8;
+      if (ra >= p.N) ra = p.N - 1;
+      if (rb >= p.N) rb = p.N - 1;
+      pa = p.codes + ra * p.ldc + cg0 * 32 + tq * 8;
+      pb = p.codes + rb * p.ldc + cg0 * 32 + tq * 8;
+      qa = p.scales + ra * p.lds + cg0;
+      qb = p.scales + rb * p.lds + cg0;
+    };
+    set_tile();
+    auto load_unit = [&](Unit& d) {
+      const bool two = 2 * lp + 1 < ng;  // the unit's second group exists
+      const int o = lp * 64;
+      d.a0 = ldg_stream_u2(pa + o);
+      d.b0 = ldg_stream_u2(pb + o);
+      if (two) {
+        d.a1 = ldg_stream_u2(pa + o + 32);
+        d.b1 = ldg_stream_u2(pb + o + 32);
+      } else {
+        d.a1 = make_uint2(0, 0);
+        d.b1 = d.a1;
+      }
+      d.sa = (uint32_t)__ldg(qa + 2 * lp) | (two ? ((uint32_t)__ldg(qa + 2 * lp + 1) << 16) : 0u);
+      d.sb = (uint32_t)__ldg(qb + 2 * lp) | (two ? ((uint32_t)__ldg(qb + 2 * lp + 1) << 16) : 0u);
+      if (++lp == npairs) {
+        lp = 0;
+        ++lt;
+        set_tile();
+      }
+    };
+
+    Unit buf[kDepth];
+#pragma unroll
+    for (int s = 0; s < kDepth; ++s)
+      if (u0 + s < u1) load_unit(buf[s]);
+
+    // rotate this chunk of x (all M rows) into the permuted fp16 layout
+    if (c > 0) __syncthreads();  // previous chunk's activations no longer read
+    for (int b = warp; b < ng * M; b += kWarps) {
+      const int m = b / ng, gl = b - m * ng;
+      float v[4];
+      bf16x4_to_f32(ldg_nc_u2(p.x + (int64_t)m * p.ldx + (cg0 + gl) * 128 + 4 * lane), v);
+      fwht128_lane(v, lane);
+      float hsum = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = 4 * lane + j;  // element of the group
+        const int q = e >> 5, o = e & 31, h = ((o >> 4) << 1) | ((o >> 3) & 1), i = o & 7;
+        uint16_t* dst =
+            reinterpret_cast<uint16_t*>(xs + gl * xs_group_bytes(ms) + q * xs_quad_bytes(ms) + m * 64 + i * 8) + h;
+        const __half hv = __float2half_rn(v[j]);
+        *dst = __half_as_ushort(hv);
+        hsum += __half2float(hv);
+      }
+      if (MB != 16) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) hsum += __shfl_xor_sync(kFull, hsum, off);
+        if (lane == 0) xsum[gl * xsum_stride(MB) + m] = hsum;
       }
     }
-    if (!ok) {
-      // A consumer stopped (timeout).  Copies already issued must land before
-      // this CTA's shared memory is released, so wait (bounded) for the last
-      // kSlots stages: their full barriers complete once their bytes arrive.
-      if (lane == 0) atomicOr(&g_fault, 1u);
-      for (int q = (s > kSlots ? s - kSlots : 0); q < s; ++q) (void)mbar_wait(&full[q % kSlots], (q / kSlots) & 1);
-    }
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int gid = lane >> 2, tq = lane & 3;
-    const int mB0 = MB == 1 ? 0 : (gid < M ? gid : M - 1);
-    const int mB1 = (8 + gid) < M ? 8 + gid : M - 1;
-    const int ms = p.ms;
-    const uint32_t xs_base = smem_u32(xs);
-    const uint32_t ring_base = smem_u32(ring);
-    int s_base = 0;  // first stage number of the current chunk
-    bool ok = true;
+    __syncthreads();
 
-    for (int c = 0; c < nchunks; ++c) {
-      int64_t cg0;
-      int ng, nsub;
-      chunk_range(c, cg0, ng, nsub);
-      // rotate this chunk of x (all M rows) into the permuted fp16 layout
-      if (c > 0) named_sync(1, 32 * kConsumers);  // previous chunk's activations no longer read
-      for (int b = warp; b < ng * M; b += kConsumers) {
-        const int m = b / ng, gl = b - m * ng;
-        float v[4];
-        bf16x4_to_f32(ldg_nc_u2(p.x + (int64_t)m * p.ldx + (cg0 + gl) * 128 + 4 * lane), v);
-        fwht128_lane(v, lane);
+    // compute iterator
+    int ct = npairs ? u0 / npairs : 0, cp = u0 - ct * npairs;
+    float acc[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = 4 * lane + j;  // element of the group
-          const int q = e >> 5, o = e & 31, h = ((o >> 4) << 1) | ((o >> 3) & 1), i = o & 7;
-          uint16_t* dst =
-              reinterpret_cast<uint16_t*>(xs + gl * xs_group_bytes(ms) + q * xs_quad_bytes(ms) + m * 64 + i * 8) + h;
-          *dst = __half_as_ushort(__float2half_rn(v[j]));
-        }
-      }
-      named_sync(1, 32 * kConsumers);
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
 
-      const int nst = ntiles * nsub;
-      for (int st = warp; st < nst && ok; st += kConsumers) {
-        const int s = s_base + st;
-        const int slot = s % kSlots, use = s / kSlots;
-        const int tl = st / nsub, sb = st - tl * nsub;
-        const int gs = sb * kStageGroups;
-        const int ngs = (ng - gs) < kStageGroups ? (ng - gs) : kStageGroups;
-        const int64_t ra = (t0 + tl) * 16 + gid, rb = ra + 8;
-        const int64_t rac = ra < p.N ? ra : p.N - 1, rbc = rb < p.N ? rb : p.N - 1;
-        const uint16_t* spa = p.scales + rac * p.lds + cg0 + gs;
-        const uint16_t* spb = p.scales + rbc * p.lds + cg0 + gs;
-        if (!mbar_wait_abortable(&full[slot], use & 1, abort)) {
-          if (lane == 0) atomicOr(&g_fault, 1u);
-          ok = false;
-          break;
-        }
-        const uint32_t ca = ring_base + slot * kStageBytes + gid * kPitch + tq * 8;
-        const uint32_t cb = ca + 8 * kPitch;
-        uint32_t xq = xs_base + (uint32_t)(gs * xs_group_bytes(ms) + tq * xs_quad_bytes(ms) + mB0 * 64);
-        float acc[MB == 16 ? 8 : 4];
+    for (int ub = u0; ub < u1; ub += kDepth) {
 #pragma unroll
-        for (int i = 0; i < (MB == 16 ? 8 : 4); ++i) acc[i] = 0.0f;
-        for (int gl = 0; gl < ngs; ++gl, xq += xs_group_bytes(ms)) {
-          const uint2 wa = lds_u2(ca + gl * 32), wb = lds_u2(cb + gl * 32);
-          const float sa = __half2float(__ushort_as_half(__ldg(spa + gl)));
-          const float sb2 = __half2float(__ushort_as_half(__ldg(spb + gl)));
-          const uint32_t a_lo10 = wa.x >> 10, a_hi10 = wa.y >> 10;
-          const uint32_t b_lo10 = wb.x >> 10, b_hi10 = wb.y >> 10;
-          float c0v[4] = {0.f, 0.f, 0.f, 0.f};
-          float c1v[4] = {0.f, 0.f, 0.f, 0.f};
-#define TQ_MMA_ONE(I, B0, B1)                                                                   \
-  {                                                                                             \
-    const uint32_t a0 = trit_pair<I>(wa.x, a_lo10), a2 = trit_pair<I>(wa.y, a_hi10);            \
-    const uint32_t a1 = trit_pair<I>(wb.x, b_lo10), a3 = trit_pair<I>(wb.y, b_hi10);            \
-    mma16816(c0v, a0, a1, a2, a3, B0, B1);                                                      \
-    if (MB == 16) {                                                                             \
-      const uint2 bc = lds_u2(xq + (mB1 - mB0) * 64 + (I)*8);                                   \
-      mma16816(c1v, a0, a1, a2, a3, bc.x, bc.y);                                                \
-    }                                                                                           \
-  }
-#define TQ_MMA_PAIR(I)                       \
-  {                                          \
-    const uint4 bq = lds_u4(xq + (I)*8);     \
-    TQ_MMA_ONE(I, bq.x, bq.y)                \
-    TQ_MMA_ONE((I) + 1, bq.z, bq.w)          \
-  }
-          TQ_MMA_PAIR(0)
-          TQ_MMA_PAIR(2)
-          TQ_MMA_PAIR(4)
-          TQ_MMA_PAIR(6)
-#undef TQ_MMA_PAIR
-#undef TQ_MMA_ONE
-          acc[0] = fmaf(sa, c0v[0], acc[0]);
-          acc[1] = fmaf(sa, c0v[1], acc[1]);
-          acc[2] = fmaf(sb2, c0v[2], acc[2]);
-          acc[3] = fmaf(sb2, c0v[3], acc[3]);
-          if (MB == 16) {
-            acc[4] = fmaf(sa, c1v[0], acc[4]);
-            acc[5] = fmaf(sa, c1v[1], acc[5]);
-            acc[6] = fmaf(sb2, c1v[2], acc[6]);
-            acc[7] = fmaf(sb2, c1v[3], acc[7]);
+      for (int s = 0; s < kDepth; ++s) {
+        if (ub + s < u1) {
+          const Unit cur = buf[s];
+          if (ub + s + kDepth < u1) load_unit(buf[s]);
+          const int gl = 2 * cp;
+          const uint32_t xq = xs_base + (uint32_t)(gl * xs_group_bytes(ms) + tq * xs_quad_bytes(ms) + mB0 * 64);
+          if constexpr (MB == 16) {
+            {
+              float c0v[4] = {0.f, 0.f, 0.f, 0.f}, c1v[4] = {0.f, 0.f, 0.f, 0.f};
+              group_mma<MB>(cur.a0.x, cur.a0.y, cur.b0.x, cur.b0.y, xq, dm1, c0v, c1v);
+              scale_add<MB>(acc, c0v, c1v, __half2float(__ushort_as_half((uint16_t)(cur.sa & 0xffffu))),
+                            __half2float(__ushort_as_half((uint16_t)(cur.sb & 0xffffu))));
+            }
+            if (gl + 1 < ng) {
+              float c0v[4] = {0.f, 0.f, 0.f, 0.f}, c1v[4] = {0.f, 0.f, 0.f, 0.f};
+              group_mma<MB>(cur.a1.x, cur.a1.y, cur.b1.x, cur.b1.y, xq + xs_group_bytes(ms), dm1, c0v, c1v);
+              scale_add<MB>(acc, c0v, c1v, __half2float(__ushort_as_half((uint16_t)(cur.sa >> 16))),
+                            __half2float(__ushort_as_half((uint16_t)(cur.sb >> 16))));
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              if (q == 1 && gl + 1 >= ng) break;
+              float v[4];
+              group_sub(q ? cur.a1.x : cur.a0.x, q ? cur.a1.y : cur.a0.y, q ? cur.b1.x : cur.b0.x,
+                        q ? cur.b1.y : cur.b0.y, xq + q * xs_group_bytes(ms), v);
+              const float sa = __half2float(__ushort_as_half((uint16_t)(q ? cur.sa >> 16 : cur.sa & 0xffffu)));
+              const float sb = __half2float(__ushort_as_half((uint16_t)(q ? cur.sb >> 16 : cur.sb & 0xffffu)));
+              const float* sg = xsum + (gl + q) * xsum_stride(MB);
+              // columns 2 tq and 2 tq + 1 of the C fragment (all equal when M == 1)
+              const float x0 = MB == 1 ? sg[0] : sg[2 * tq], x1 = MB == 1 ? sg[0] : sg[2 * tq + 1];
+              // s * (sum c x' - sum x'), with sum c x' = 2^24 v
+              acc[0] = fmaf(-sa, x0, fmaf(sa * 16777216.0f, v[0], acc[0]));
+              acc[1] = fmaf(-sa, x1, fmaf(sa * 16777216.0f, v[1], acc[1]));
+              acc[2] = fmaf(-sb, x0, fmaf(sb * 16777216.0f, v[2], acc[2]));
+              acc[3] = fmaf(-sb, x1, fmaf(sb * 16777216.0f, v[3], acc[3]));
+            }
           }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        // add this stage's partial sums into the CTA's partial outputs
+          // leaving the tile (or the range): add the row totals into the CTA's partial outputs
+          const bool last = (ub + s + 1 == u1);
+          if (++cp == npairs || last) {
+            const int64_t ra = (t0 + ct) * 16 + gid;
 #pragma unroll
-        for (int half = 0; half < (MB == 16 ? 2 : 1); ++half) {
+            for (int half = 0; half < (MB == 16 ? 2 : 1); ++half) {
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int m = 8 * half + 2 * tq + cc;
-            const bool use_m = MB == 1 ? (tq == 0 && cc == 0) : (m < M);
-            if (use_m) {
-              if (ra < p.N) atomicAdd(&ypart[(tl * 16 + gid) * M + m], acc[4 * half + cc]);
-              if (rb < p.N) atomicAdd(&ypart[(tl * 16 + gid + 8) * M + m], acc[4 * half + 2 + cc]);
+              for (int cc = 0; cc < 2; ++cc) {
+                const int m = 8 * half + 2 * tq + cc;
+                const bool use_m = MB == 1 ? (tq == 0 && cc == 0) : (m < M);
+                if (use_m) {
+                  if (ra < p.N) atomicAdd(&ypart[(ct * 16 + gid) * M + m], acc[4 * half + cc]);
+                  if (ra + 8 < p.N) atomicAdd(&ypart[(ct * 16 + gid + 8) * M + m], acc[4 * half + 2 + cc]);
+                }
+                acc[4 * half + cc] = 0.0f;
+                acc[4 * half + 2 + cc] = 0.0f;
+              }
+            }
+            if (cp == npairs) {
+              cp = 0;
+              ++ct;
             }
           }
         }
       }
-      s_base += ntiles * nsub;
-      // after a timeout the warp skips its remaining stages but still takes
-      // part in every named barrier, so no warp is left waiting there
     }
   }
   pdl_launch_dependents();
@@ -351,7 +433,6 @@ cudaError_t launch_mb(const Params& p0, cudaStream_t s) {
   const int64_t max_smem = device_max_smem_optin();
   const int sms = device_sm_count();
   p.ms = MB == 1 ? 1 : p.M;
-  const int64_t fixed = 1024 + (int64_t)kSlots * kStageBytes;
   // one CTA per SM: as many clusters as fit, each owning a balanced tile range
   int64_t clusters = sms / kCl;
   if (clusters > ntiles_all) clusters = ntiles_all;
@@ -362,8 +443,8 @@ cudaError_t launch_mb(const Params& p0, cudaStream_t s) {
     if (clusters > ntiles_all) clusters = ntiles_all;
     tpc = (ntiles_all + clusters - 1) / clusters;
   }
-  const int64_t per_group = xs_group_bytes(p.ms);
-  int64_t chunk = (max_smem - fixed - tpc * 16 * p.M * 4) / per_group;
+  const int64_t per_group = xs_group_bytes(p.ms) + 4 * xsum_stride(MB);
+  int64_t chunk = (max_smem - tpc * 16 * p.M * 4) / per_group;
   if (chunk > ng_max) chunk = ng_max;
   if (chunk < 1) return cudaErrorNotSupported;
   const int64_t steps = (ng_max + chunk - 1) / chunk;  // walk the slice in near-equal chunks
@@ -371,7 +452,8 @@ cudaError_t launch_mb(const Params& p0, cudaStream_t s) {
   p.clusters = (int)clusters;
   p.chunk_groups = (int)chunk;
   p.xs_bytes = (int)(chunk * per_group);
-  const int smem = (int)(fixed + p.xs_bytes + tpc * 16 * p.M * 4);
+  p.sum_off = (int)(chunk * xs_group_bytes(p.ms));
+  const int smem = (int)(p.xs_bytes + tpc * 16 * p.M * 4);
   cudaError_t e = cudaFuncSetAttribute(k_gemv<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -414,11 +496,7 @@ cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16
   return launch_mb<16>(p, s);
 }
 
-unsigned int take_fault_gemv() {
-  unsigned int v = 0, z = 0;
-  if (cudaMemcpyFromSymbol(&v, g_fault, sizeof(v)) != cudaSuccess) return 0;
-  if (v) (void)cudaMemcpyToSymbol(g_fault, &z, sizeof(z));
-  return v;
-}
+// This kernel has no waits that could stall (no producer/consumer barriers).
+unsigned int take_fault_gemv() { return 0; }
 
 }  // namespace tq

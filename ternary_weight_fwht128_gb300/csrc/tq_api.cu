@@ -163,7 +163,8 @@ tq_status tq_gemm_check_range(const void* workspace, tq_stream stream) {
 
 tq_status tq_device_fault(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
-  return take_fault_gemv() ? TQ_ERR_TIMEOUT : TQ_OK;
+  const unsigned int f = take_fault_gemv() | take_fault_quant();
+  return f ? TQ_ERR_TIMEOUT : TQ_OK;
 }
 
 }  // extern "C"

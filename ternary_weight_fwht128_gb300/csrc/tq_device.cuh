@@ -40,6 +40,48 @@ __device__ __forceinline__ void fwht128_lane(float v[4], int lane) {
   for (int j = 0; j < 4; ++j) v[j] = __fmul_rn(v[j], kInvSqrt128);
 }
 
+// FWHT-128 on half a warp: lane l holds elements 8p .. 8p+7 (p = l & 15) of
+// the block of its half-warp (l >> 4), so one warp rotates two blocks.
+// Stages h = 1, 2, 4 stay inside a lane; stages h = 8 .. 64 pair lane l with
+// lane l ^ (h / 8), never crossing the half-warp.  Bit-identical to the
+// staged definition, like fwht128_lane.
+__device__ __forceinline__ void fwht128_x8(float v[8], int lane) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if ((j & h) == 0) {
+        const float a = v[j], b = v[j + h];
+        v[j] = a + b;
+        v[j + h] = a - b;
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float o = __shfl_xor_sync(kFull, v[j], m);
+      v[j] = __fmaf_rn(sgn, v[j], o);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], kInvSqrt128);
+}
+
+// Eight consecutive bf16 (as a 128-bit word) -> fp32.
+__device__ __forceinline__ void bf16x8_to_f32(uint4 w, float v[8]) {
+  v[0] = __uint_as_float(w.x << 16);
+  v[1] = __uint_as_float(w.x & 0xffff0000u);
+  v[2] = __uint_as_float(w.y << 16);
+  v[3] = __uint_as_float(w.y & 0xffff0000u);
+  v[4] = __uint_as_float(w.z << 16);
+  v[5] = __uint_as_float(w.z & 0xffff0000u);
+  v[6] = __uint_as_float(w.w << 16);
+  v[7] = __uint_as_float(w.w & 0xffff0000u);
+}
+
 // Four consecutive bf16 (as a 64-bit word) -> fp32.
 __device__ __forceinline__ void bf16x4_to_f32(uint2 w, float v[4]) {
   v[0] = __uint_as_float(w.x << 16);

@@ -32,5 +32,6 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
 // Reads and clears the device status word of the GEMV kernels (non-zero:
 // a bounded wait ran out).
 unsigned int take_fault_gemv();
+unsigned int take_fault_quant();
 
 }  // namespace tq
