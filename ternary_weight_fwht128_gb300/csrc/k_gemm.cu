@@ -1,13 +1,366 @@
-// k_gemm.cu -- prefill GEMM (tq_gemm) on tcgen05 tensor cores.
+// k_gemm.cu -- prefill GEMM (tq_gemm) on the 5th-generation tensor cores.
+//
+//   y[m][n] = sum_k x'[m][k] * (t[n][k] * s[n][k/128]),  fp32 accumulation
+//
+// Prefill (M = 2048 tokens) is the one dense contraction of the path, so it
+// runs on tcgen05 MMA with accumulators in tensor memory.  The operands are
+// fp16: x' comes from the rotation pre-pass (fp16, with an overflow flag) and
+// the weight operand is t * s, which is exact in fp16 because s is an fp16
+// number and t is -1, 0 or +1.  Folding the per-group scale into the operand
+// applies it exactly where the group structure needs it, so one K-long
+// accumulation covers all groups (equivalent to scaling each group's partial
+// sum in an epilogue, without per-group accumulator traffic).
+//
+// One CTA computes a 256 (tokens) x 256 (weight rows) tile, K in stages of 64:
+//   warp 8     (one lane) TMA-loads the 256 x 64 fp16 tile of x' (128-byte
+//              swizzle, K-major) into the stage ring;
+//   warps 0-7  decode the 256 x 64 weight tile from 2-bit codes straight into
+//              the same swizzled K-major layout (lane = weight row), then,
+//              after the last stage, drain tensor memory to y;
+//   warp 9     allocates tensor memory and (one lane) issues the MMAs: per
+//              stage 2 (token halves) x 4 (K steps of 16) tcgen05.mma of
+//              128 x 256 x 16 into two 256-column fp32 accumulators.
+// Stages are handed over with mbarriers (TMA bytes, decoder arrivals, MMA
+// completion via tcgen05.commit).  Every wait is bounded in time; a wait that
+// runs out records bit 1 of the status word and the CTA winds down.
+//
+// The k order inside each 16-element chunk is 0,8,1,9,...,7,15 on both
+// operands: the decoder produces (c_j, c_{j+8}) fp16 pairs from one 32-bit
+// word of codes without shuffling, and the pre-pass stores x' in that order.
+#include <cuda.h>
+
 #include "tq_internal.h"
 
 namespace tq {
 
+namespace {
+
+constexpr int BM = 256;  // tokens per CTA (two 128-row MMA tiles)
+constexpr int BN = 256;  // weight rows per CTA (MMA N)
+constexpr int BK = 64;   // k per stage: 128 bytes of fp16 = one swizzle row
+constexpr int kStages = 3;
+constexpr int kDecoders = 8;  // warps
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 32 * 10;
+constexpr int kAStage = BM * BK * 2;  // 32 KB
+constexpr int kBStage = BN * BK * 2;  // 32 KB
+constexpr int kTmemCols = 512;
+constexpr uint32_t kFaultTimeout = 2u;  // status word bit
+
+struct SmemCtl {
+  uint64_t full_a[kStages];
+  uint64_t full_b[kStages];
+  uint64_t empty[kStages];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms of
+// 1024 bytes (stride byte offset 1024), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);            // start address
+  d |= (uint64_t)1 << 16;                              // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;                    // stride byte offset
+  d |= (uint64_t)1 << 46;                              // version
+  d |= (uint64_t)2 << 61;                              // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
+// K-major, N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%"
+      "20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// (c_j, c_{j+8}) of a 16-code word -> fp16x2 (t_j * s, t_{j+8} * s), exact:
+// OR the exponent of 2^(10-2jj) over the code bits, subtract 2^(10-2jj) + 1
+// (gives t), multiply by s (exact: t is -1, 0 or +1).
+template <int J>
+__device__ __forceinline__ uint32_t ts_pair(uint32_t w, uint32_t w10, uint32_t s2) {
+  constexpr int jj = J < 5 ? J : J - 5;
+  constexpr uint32_t mask = 0x00030003u << (2 * jj);
+  constexpr uint32_t magic = (uint32_t)(25 - 2 * jj) << 10;
+  constexpr uint32_t magic2 = magic | (magic << 16);
+  constexpr uint32_t bias = magic | (1u << (2 * jj));
+  constexpr uint32_t bias2 = bias | (bias << 16);
+  const uint32_t src = J < 5 ? w : w10;
+  return hmul2_bits(hsub2_bits((src & mask) | magic2, bias2), s2);
+}
+
+struct Params {
+  const uint8_t* codes;
+  int64_t ldc;
+  const uint16_t* scales;
+  int64_t lds;
+  int64_t N, K, M;
+  float* y;
+  int64_t ldy;
+  uint32_t* flag;
+  int n_tiles_m;
+  int vec_store;  // y 16-byte aligned and ldy % 4 == 0: rows can take 16-byte stores
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SmemCtl* ctl, uint32_t* flag) {
+  if (mbar_wait_abortable(bar, parity, &ctl->abort)) return true;
+  atomicOr(flag, kFaultTimeout);
+  return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const Params p) {
+  extern __shared__ unsigned char smem_raw[];
+  // 1024-byte alignment (of the shared-window address) for the swizzled tiles
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  unsigned char* a_ring = smem;
+  unsigned char* b_ring = smem + kStages * kAStage;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(b_ring + kStages * kBStage);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_m = blockIdx.x % p.n_tiles_m, tile_n = blockIdx.x / p.n_tiles_m;
+  const int64_t m0 = (int64_t)tile_m * BM, n0 = (int64_t)tile_n * BN;
+  const int nk = (int)(p.K / BK);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&ctl->full_a[i], 1);
+      mbar_init(&ctl->full_b[i], kDecoders);
+      mbar_init(&ctl->empty[i], 1);
+    }
+    mbar_init(&ctl->done, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&ctl->tmem_base)),
+                 "n"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  pdl_wait();  // x' and the status word come from the pre-pass
+
+  if (warp == kTmaWarp) {
+    // ---------------------------------------------------------------- TMA (x')
+    if (lane == 0) {
+      int s = 0;
+      for (; s < nk; ++s) {
+        const int slot = s % kStages, use = s / kStages;
+        if (use > 0 && !wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl, p.flag)) break;
+        mbar_arrive_expect_tx(&ctl->full_a[slot], kAStage);
+        tma_load_2d(smem_u32(a_ring + slot * kAStage), &xmap, s * BK, (int)m0, &ctl->full_a[slot]);
+      }
+      // loads issued but possibly not consumed: let them land before exit
+      for (int q = (s > kStages ? s - kStages : 0); q < s; ++q)
+        (void)mbar_wait(&ctl->full_a[q % kStages], (q / kStages) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      for (int s = 0; s < nk; ++s) {
+        const int slot = s % kStages, par = (s / kStages) & 1;
+        if (!wait_or_abort(&ctl->full_a[slot], par, ctl, p.flag)) break;
+        if (!wait_or_abort(&ctl->full_b[slot], par, ctl, p.flag)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(a_ring + slot * kAStage), b0 = smem_u32(b_ring + slot * kBStage);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            mma_f16(tmem + h * BN, smem_desc_sw128(a0 + h * (kAStage / 2) + kk * 32), smem_desc_sw128(b0 + kk * 32),
+                    (s > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&ctl->empty[slot]);  // stage free once these MMAs have read it
+      }
+      mma_commit(&ctl->done);  // accumulators complete (or, after an abort, all issued MMAs done)
+    }
+  } else {
+    // ---------------------------------------------------------------- decoders
+    const int r = warp * 32 + lane;  // weight row inside the tile
+    int64_t n = n0 + r;
+    const bool row_ok = n < p.N;
+    if (!row_ok) n = p.N - 1;
+    const uint8_t* crow = p.codes + n * p.ldc;
+    const uint16_t* srow = p.scales + n * p.lds;
+    const uint32_t row_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+    const int rx = r & 7;
+    uint4 cur = ldg_nc_u4(crow);
+    for (int s = 0; s < nk; ++s) {
+      const int slot = s % kStages, use = s / kStages;
+      const uint4 nxt = (s + 1 < nk) ? ldg_nc_u4(crow + (s + 1) * (BK / 4)) : make_uint4(0, 0, 0, 0);
+      const uint16_t sbits = row_ok ? __ldg(srow + (s * BK) / 128) : (uint16_t)0;
+      if (use > 0 && !wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl, p.flag)) break;
+      const uint32_t s2 = (uint32_t)sbits | ((uint32_t)sbits << 16);
+      unsigned char* dst = b_ring + slot * kBStage + row_off;
+      const uint32_t w[4] = {cur.x, cur.y, cur.z, cur.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // 16 codes -> two 16-byte chunks
+        const uint32_t wq = w[q], w10 = wq >> 10;
+        const uint4 lo = make_uint4(ts_pair<0>(wq, w10, s2), ts_pair<1>(wq, w10, s2), ts_pair<2>(wq, w10, s2),
+                                    ts_pair<3>(wq, w10, s2));
+        const uint4 hi = make_uint4(ts_pair<4>(wq, w10, s2), ts_pair<5>(wq, w10, s2), ts_pair<6>(wq, w10, s2),
+                                    ts_pair<7>(wq, w10, s2));
+        *reinterpret_cast<uint4*>(dst + (((2 * q) ^ rx) << 4)) = lo;
+        *reinterpret_cast<uint4*>(dst + (((2 * q + 1) ^ rx) << 4)) = hi;
+      }
+      fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->full_b[slot]);
+      cur = nxt;
+    }
+    // ---------------------------------------------------------------- epilogue
+    (void)wait_or_abort(&ctl->done, 0, ctl, p.flag);
+    tc_fence_after();
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lanes 32*quad.., accumulator half
+    const int64_t m = m0 + half * 128 + quad * 32 + lane;
+    const bool m_ok = m < p.M;
+    float* yrow = p.y + (m_ok ? m : 0) * p.ldy + n0;
+    const int ncols = (int)((p.N - n0) < BN ? (p.N - n0) : BN);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      float v[32];
+      tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * BN + c0), v);
+      if (m_ok && !ctl->abort) {
+        if (p.vec_store && c0 + 32 <= ncols) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(yrow + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+          for (int i = 0; i < 32 && c0 + i < ncols; ++i) yrow[c0 + i] = v[i];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+  }
+  pdl_launch_dependents();
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once (no link to libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    tried = true;
+  }
+  return fn;
+}
+
+}  // namespace
+
+constexpr size_t kGemmSmem = (size_t)kStages * (kAStage + kBStage) + sizeof(SmemCtl) + 1024;
+
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
                         const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, cudaStream_t s) {
-  (void)codes; (void)ldc; (void)scales; (void)lds; (void)N; (void)K; (void)xrot; (void)M; (void)y; (void)ldy;
-  (void)flag; (void)s;
-  return cudaErrorNotSupported;
+  if (N == 0 || M == 0) return cudaSuccess;
+  if ((int64_t)device_max_smem_optin() < (int64_t)kGemmSmem) return cudaErrorNotSupported;
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t estride[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(xrot), gdim, gstride, box, estride,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.codes = codes;
+  p.ldc = ldc;
+  p.scales = scales;
+  p.lds = lds;
+  p.N = N;
+  p.K = K;
+  p.M = M;
+  p.y = y;
+  p.ldy = ldy;
+  p.flag = flag;
+  p.n_tiles_m = (int)((M + BM - 1) / BM);
+  p.vec_store = ((reinterpret_cast<uintptr_t>(y) & 15u) == 0 && ldy % 4 == 0) ? 1 : 0;
+  const int64_t tiles = (int64_t)p.n_tiles_m * ((N + BN - 1) / BN);
+  cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gemm_tc, map, p);
 }
 
 }  // namespace tq

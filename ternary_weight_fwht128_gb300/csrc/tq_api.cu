@@ -140,7 +140,7 @@ tq_status tq_gemm(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* sc
   if (ldc < K / 4 || lds < K / 128 || ldx < K || ldy < N) return TQ_ERR_SHAPE;
   if (ws_bytes < tq_gemm_workspace_bytes(M, K)) return TQ_ERR_SHAPE;
   if (!aligned16(codes) || ldc % 16 || !aligned2(scales) || !aligned16(x) || (ldx * 2) % 16 ||
-      !aligned16(workspace) || !aligned16(y) || ldy % 4)
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(y) & 3u))
     return TQ_ERR_ALIGN;
   cudaStream_t s = (cudaStream_t)stream;
   uint32_t* flag = static_cast<uint32_t*>(workspace);
@@ -158,6 +158,7 @@ tq_status tq_gemm_check_range(const void* workspace, tq_stream stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return TQ_ERR_CUDA;
   uint32_t flag = 0;
   if (cudaMemcpy(&flag, workspace, sizeof(flag), cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ERR_CUDA;
+  if (flag & 2u) return TQ_ERR_TIMEOUT;
   return (flag & 1u) ? TQ_ERR_RANGE : TQ_OK;
 }
 

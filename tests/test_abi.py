@@ -147,7 +147,7 @@ def test_gemm_validation(L):
     assert call(wsb=ws - 1) == tq.TQ_ERR_SHAPE
     assert call(w=None) == tq.TQ_ERR_INVALID_ARG
     assert call(w=B + 65544) == tq.TQ_ERR_ALIGN
-    assert call(ldy=10) == tq.TQ_ERR_ALIGN
+    assert call(y=B + 8194) == tq.TQ_ERR_ALIGN
     assert call(K=0) == tq.TQ_ERR_SHAPE
     assert L.tq_gemm_check_range(None, None) == tq.TQ_ERR_INVALID_ARG
     assert L.tq_gemm_check_range(MIS, None) == tq.TQ_ERR_ALIGN

@@ -186,3 +186,64 @@ def test_gemv_zero_and_delta_activations(orc):
     assert np.all(y[0] == 0.0)
     T, S = orc.quantize(W)
     check_y(y[1:], orc.gemv(T, S, synth.bf16_bits_to_f32(x[1:])))
+
+
+# ----------------------------------------------------------- prefill GEMM
+
+def _gemm_case(orc, N, K, M, seed, rows=None, out_cols=None):
+    W = synth.weights(N, K, seed, dtype="bf16")
+    xb = synth.activations(M, K, seed + 1)
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    out, check = guarded((M, N), torch.float32)
+    ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    tq.gemm(c2, s, to_dev_bf16(xb), K, tq.TQ_PACK_2BIT, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    check()
+    tq.gemm_check_range(ws)
+    T, S = orc.quantize(W, rows)
+    xs = synth.bf16_bits_to_f32(xb)
+    if out_cols is not None:
+        xs = xs[out_cols]
+    ref = orc.gemv(T, S, xs)
+    got = out.cpu().numpy()
+    if out_cols is not None:
+        got = got[out_cols]
+    if rows is not None:
+        got = got[:, rows]
+    return check_y(got, ref, "gemm y")
+
+
+@pytest.mark.parametrize("N,K,M", [(256, 128, 256), (256, 256, 256), (300, 384, 300), (513, 640, 77),
+                                   (1024, 1280, 512), (64, 128, 1)])
+def test_gemm_shapes(orc, N, K, M):
+    _gemm_case(orc, N, K, M, seed=N + 3 * K + 7 * M)
+
+
+@pytest.mark.parametrize("N,K", [(5120, 5120), (27648, 5120), (5120, 27648)])
+def test_gemm_full_size_sampled(orc, N, K):
+    """M = 2048 tokens at the benchmark's shapes; the oracle checks a seeded
+    sample of output rows (weights) and tokens."""
+    rng = np.random.default_rng(N + K)
+    rows = np.sort(rng.choice(N, size=24, replace=False))
+    rows[-1] = N - 1
+    toks = np.sort(rng.choice(2048, size=12, replace=False))
+    toks[-1] = 2047
+    _gemm_case(orc, N, K, 2048, seed=N * 7 + K, rows=rows, out_cols=toks)
+
+
+def test_gemm_range_flag():
+    """An activation block whose rotation exceeds the fp16 range is reported
+    through the status word (tq_gemm_check_range -> TQ_ERR_RANGE)."""
+    N, K, M = 256, 256, 256
+    W = synth.weights(N, K, 1, dtype="bf16")
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    x = torch.zeros(M, K, device="cuda", dtype=torch.bfloat16)
+    x[3, :128] = 30000.0  # ||block||_2 = 30000 * sqrt(128) -> x'[0] far above 65504
+    ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    tq.gemm(c2, s, x, K, workspace=ws)
+    with pytest.raises(tq.TQError) as ei:
+        tq.gemm_check_range(ws)
+    assert ei.value.status == tq.TQ_ERR_RANGE
+    x[3].zero_()
+    tq.gemm(c2, s, x, K, workspace=ws)
+    tq.gemm_check_range(ws)  # cleared on the next call
