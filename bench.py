@@ -36,6 +36,10 @@ HIDDEN, FFN, LAYERS = 5120, 27648, 64
 LAYER_SHAPES = [("h2h_a", HIDDEN, HIDDEN), ("h2h_b", HIDDEN, HIDDEN), ("gate", FFN, HIDDEN), ("up", FFN, HIDDEN),
                 ("down", HIDDEN, FFN)]
 METRIC = "ternary GEMV packed-weight HBM GB/s (% of peak); prefill GEMM TFLOP/s"
+# DRAM bytes per algorithmic byte of k_gemv<1>, measured with ncu on one
+# 27648x5120 launch (37,657,600 read for 37,601,280 packed bytes); every weight
+# byte is read once, so the ratio carries over to the step's other shapes.
+GEMV_TRAFFIC_RATIO = 37657600 / 37601280
 WORKLOAD = ("decode GEMV M=1, 2-bit codes, 64-layer stack of 27B-class shapes "
             "{5120x5120 x2, 27648x5120 x2, 5120x27648} per layer (320 launches, FWHT-128 fused)")
 
@@ -110,7 +114,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -280,7 +284,10 @@ def gpu_arm(args, world, rank, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "frac_of_peak": round(gbs_rank / pk["hbm_gbs"], 4),
         "roofline": {"bound": "hbm", "achieved": round(gbs_rank, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(gbs_rank / pk["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(gbs_rank / pk["hbm_gbs"], 4),
+                     "traffic": int(GEMV_TRAFFIC_RATIO * bytes_step / launches_per_step),
+                     "traffic_note": "DRAM bytes per launch, ncu capture of one 27648x5120 launch scaled by "
+                                     "the algorithmic bytes of the average launch of the step",
                      "kernel": "k_gemv<1> (tq_gemv, M=1)",
                      "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -417,20 +424,71 @@ def reference_arm(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def only_arm(args):
+    """One operation on one shape, `warmup` + `steps` launches, timed with
+    CUDA events: the small, self-contained command the ncu captures use."""
+    import torch
+    import ternary_weight_fwht128_gb300 as tq
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    N, K = (int(v) for v in args.shape.lower().split("x"))
+    M = args.M
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    W = (torch.randn(N, K, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+    fmt = tq.TQ_PACK_BASE3 if args.fmt == "base3" else tq.TQ_PACK_2BIT
+    x = activations(torch, dev, K, M, seed=K + M)
+    if args.only == "quantize":
+        run = lambda: tq.quantize_pack(W, tq.TQ_PACK_BOTH)
+        work, unit = N * K * 2 + N * (K // 4) + N * tq.packed_ld(K, tq.TQ_PACK_BASE3) + N * (K // 128) * 2, "GB/s"
+    elif args.only == "fwht":
+        out = torch.empty(M, K, device=dev, dtype=torch.float16)
+        run = lambda: tq.fwht128(x, out=out)
+        work, unit = M * K * 4, "GB/s"
+    else:
+        c2, c3, s = tq.quantize_pack(W, fmt | tq.TQ_PACK_2BIT)
+        codes = c3 if fmt == tq.TQ_PACK_BASE3 else c2
+        del W
+        if args.only == "gemv":
+            y = torch.empty(M, N, device=dev)
+            run = lambda: tq.gemv(codes, s, x, K, fmt, out=y)
+            work, unit = packed_bytes(N, K, "base3" if fmt == tq.TQ_PACK_BASE3 else "2bit"), "GB/s"
+        else:
+            ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+            y = torch.empty(M, N, device=dev)
+            run = lambda: tq.gemm(codes, s, x, K, fmt, workspace=ws, out=y)
+            work, unit = 2 * M * N * K, "TFLOP/s"
+    for _ in range(args.warmup):
+        run()
+    ms = time_events(run, args.steps, torch)
+    rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(json.dumps({"only": args.only, "shape": f"{N}x{K}", "M": M, "fmt": args.fmt, "us": round(ms * 1e3, 2),
+                      unit: round(rate, 1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--quick", action="store_true", help="headline decode step only (no extra sections)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=4.0)
+    ap.add_argument("--only", choices=["gemv", "gemm", "quantize", "fwht"],
+                    help="time one operation on one shape (for profiler captures)")
+    ap.add_argument("--shape", default="27648x5120", help="NxK for --only")
+    ap.add_argument("--M", type=int, default=1, help="activation rows for --only")
+    ap.add_argument("--fmt", choices=["2bit", "base3"], default="2bit")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()
+    if args.only:
+        only_arm(args)
+        return
     if args.impl == "reference":
         reference_arm(args, world, rank)
         return

@@ -12,7 +12,7 @@
  *             zwxr.cn/news/303439, activation-side Hadamard), and
  *             y[m][n] = sum_g s[n][g] * sum_{k in g} t[n][k] * x'[m][k]
  *             accumulated in fp32 (fusion of transform and ternary matmul:
- *             mhpq.cn/news/1159370 sec. 3.3; dpshk.com/news/5289456 sec. 4).
+ *             mhpq.cn/news/1159370 sec. 3.3; dpshk.com/news/5289456 sec. 4.2).
  *
  * H[i][j] = (-1)^popcount(i & j) (dpshk.com/news/5289456 sec. 2.1).  The
  * transform runs butterfly stages h = 1, 2, 4, ..., 64 in fp32 and then

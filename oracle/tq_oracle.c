@@ -43,7 +43,7 @@ void tqo_sylvester(int n, int8_t *h) {
   }
 }
 
-/* The normalisation 1/sqrt(n) for n = 128 ([dpshk] sec. 2.3; [zwxr] sec. 2,
+/* The normalisation 1/sqrt(n) for n = 128 ([dpshk] sec. 2.3; [zwxr] sec. 2.1,
  * normalised transform), rounded once to fp32. */
 uint32_t tqo_norm_const_bits(void) {
   float c = (float)(1.0 / sqrt(128.0));

@@ -125,7 +125,7 @@ def check_fwht_stage_order(orc):
 
 
 def check_fwht_involution_energy(orc):
-    """The normalised rotation is its own inverse ([zwxr] sec. 2: the inverse
+    """The normalised rotation is its own inverse ([zwxr] sec. 2.1: the inverse
     is the same transform up to 1/n) and keeps the 2-norm ([mhpq] sec. 2.2)."""
     rng = np.random.default_rng(14)
     v = rng.standard_normal((8, 128))
