@@ -137,6 +137,31 @@ TQ_API tq_status tq_gemm(const uint8_t *codes, int64_t ldc, int fmt, const uint1
  * output is then not meaningful), else TQ_OK. */
 TQ_API tq_status tq_gemm_check_range(const void *workspace, tq_stream stream);
 
+/* Prefill GEMM that allocates nothing and needs no workspace argument.  The
+ * paper has no counterpart; this entry exists for callers that cannot
+ * allocate device memory themselves (code that runs inside a fixed memory
+ * pool or arena, or plugins that may only use the buffers their host hands
+ * them).  It computes exactly what tq_gemm computes, with the same kernels,
+ * but takes the workspace from a fixed scratch array inside the library:
+ *   - the array holds the rotated activations for M * K <= 16,777,216
+ *     (e.g. 2048 x 8192); larger M * K returns TQ_ERR_SHAPE;
+ *   - it lives in device memory of every GPU that loads the library, until
+ *     the process exits (about 32 MiB per GPU);
+ *   - the first call on a device looks up the array's device address with
+ *     that device current (set-up); make that first call before any stream
+ *     capture;
+ *   - every call shares the one array and it keeps the last call's contents;
+ *     calls whose work overlaps on the GPU (different streams, or different
+ *     host threads on the same device) race on it and must be serialised by
+ *     the caller;
+ *   - the fp16-overflow status word of tq_gemm is kept in the array and is
+ *     not reported here; callers that need that check use tq_gemm.
+ * No cudaMalloc, cudaFree or other allocating call is made.  Arguments,
+ * layouts and other errors as for tq_gemm. */
+TQ_API tq_status tq_gemm_noalloc(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
+                                 int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
+                                 tq_stream stream);
+
 /* Failure detection.  Every wait inside a kernel (pipeline barriers between
  * the warps that copy weights and the warps that compute) is bounded by a
  * wall-clock limit of about 2 s.  A kernel whose wait runs out stops early,

@@ -27,7 +27,7 @@ TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
 TQ_PACK_2BIT, TQ_PACK_BASE3, TQ_PACK_BOTH = 1, 2, 3
 
 EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_quantize_pack", "tq_gemv",
-            "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_check_range", "tq_device_fault")
+            "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_check_range", "tq_device_fault", "tq_gemm_noalloc")
 
 _lib = None
 _i64 = ctypes.c_int64
@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
         L.tq_gemm_check_range.argtypes = [_vp, _vp]
         L.tq_device_fault.restype = _int
         L.tq_device_fault.argtypes = []
+        L.tq_gemm_noalloc.restype = _int
+        L.tq_gemm_noalloc.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp]
         _lib = L
     return _lib
 
