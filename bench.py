@@ -173,9 +173,11 @@ def build_stack(tq, torch, dev, seed: int):
             W.view(-1)[idx] *= 20.0
             Wb = W.to(torch.bfloat16)
             del W
-            c2, _, s = tq.quantize_pack(Wb, tq.TQ_PACK_2BIT)
+            # base-3 codes as well for the shapes the skinny comparison uses
+            fmt = tq.TQ_PACK_BOTH if name in ("gate", "down") else tq.TQ_PACK_2BIT
+            c2, c3, s = tq.quantize_pack(Wb, fmt)
             del Wb
-            mats.append((name, N, K, c2, s))
+            mats.append((name, N, K, c2, s, c3))
         stack.append(mats)
     return stack
 
@@ -209,7 +211,7 @@ def gpu_arm(args, world, rank, local):
 
     def step():
         for mats in stack:
-            for _, N, K, c2, s in mats:
+            for _, N, K, c2, s, _ in mats:
                 tq.gemv(c2, s, xs[K], K, tq.TQ_PACK_2BIT, out=ys[N])
 
     for _ in range(args.warmup):
@@ -244,7 +246,7 @@ def gpu_arm(args, world, rank, local):
         for K in dx:
             dx[K].copy_(hx[K], non_blocking=True)
         for mats in stack:
-            for _, N, K, c2, s in mats:
+            for _, N, K, c2, s, _ in mats:
                 tq.gemv(c2, s, dx[K], K, tq.TQ_PACK_2BIT, out=ys[N])
         for N in hy:
             hy[N].copy_(ys[N], non_blocking=True)
@@ -324,26 +326,27 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
     gen.manual_seed(7)
     for (name, N, K) in (("gate", FFN, HIDDEN), ("down", HIDDEN, FFN)):
         mats = [[m for m in layer if m[0] == name][0] for layer in stack]
-        for M in (2, 4, 8, 16):
-            x = activations(torch, dev, K, M, seed=K + M)
-            y = torch.empty(M, N, device=dev)
-            it = [0]
+        for fmt_name, fmt in (("2bit", tq.TQ_PACK_2BIT), ("base3", tq.TQ_PACK_BASE3)):
+            for M in (1, 2, 4, 8, 16):
+                x = activations(torch, dev, K, M, seed=K + M)
+                y = torch.empty(M, N, device=dev)
+                it = [0]
 
-            def run():
-                _, _, _, c2, s = mats[it[0] % len(mats)]
-                it[0] += 1
-                tq.gemv(c2, s, x, K, tq.TQ_PACK_2BIT, out=y)
+                def run():
+                    _, _, _, c2, s, c3 = mats[it[0] % len(mats)]
+                    it[0] += 1
+                    tq.gemv(c2 if fmt == tq.TQ_PACK_2BIT else c3, s, x, K, fmt, out=y)
 
-            ms = time_events(run, 3 * len(mats), torch)
-            gb = packed_bytes(N, K) / (ms * 1e-3) / 1e9
-            skinny.append({"shape": f"{N}x{K}", "M": M, "fmt": "2bit", "us": round(ms * 1e3, 2),
-                           "GB/s": round(gb, 1), "frac_of_peak": round(gb / pk["hbm_gbs"], 4),
-                           "TFLOP/s": round(2 * M * N * K / (ms * 1e-3) / 1e12, 2)})
+                ms = time_events(run, 3 * len(mats), torch)
+                gb = packed_bytes(N, K, fmt_name) / (ms * 1e-3) / 1e9
+                skinny.append({"shape": f"{N}x{K}", "M": M, "fmt": fmt_name, "us": round(ms * 1e3, 2),
+                               "GB/s": round(gb, 1), "frac_of_peak": round(gb / pk["hbm_gbs"], 4),
+                               "TFLOP/s": round(2 * M * N * K / (ms * 1e-3) / 1e12, 2)})
     out["skinny"] = skinny
     # --- prefill GEMM, M = 2048 on the three shapes
     prefill = []
     for name, N, K in (("h2h_a", HIDDEN, HIDDEN), ("gate", FFN, HIDDEN), ("down", HIDDEN, FFN)):
-        _, _, _, c2, s = [m for m in stack[0] if m[0] == name][0]
+        _, _, _, c2, s, _ = [m for m in stack[0] if m[0] == name][0]
         M = 2048
         x = activations(torch, dev, K, M, seed=11 + K)
         ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device=dev)

@@ -239,11 +239,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const uint16_t* srow = p.scales + n * p.lds;
     const uint32_t row_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
     const int rx = r & 7;
-    uint4 cur = ldg_nc_u4(crow);
+    // codes and scales run two stages ahead of the decode, so their latency
+    // hides behind two stages of MMA
+    auto ld_codes = [&](int st) { return st < nk ? ldg_nc_u4(crow + st * (BK / 4)) : make_uint4(0, 0, 0, 0); };
+    auto ld_scale = [&](int st) { return (row_ok && st < nk) ? __ldg(srow + (st * BK) / 128) : (uint16_t)0; };
+    uint4 cur = ld_codes(0), nx1 = ld_codes(1);
+    uint16_t scur = ld_scale(0), snx1 = ld_scale(1);
     for (int s = 0; s < nk; ++s) {
       const int slot = s % kStages, use = s / kStages;
-      const uint4 nxt = (s + 1 < nk) ? ldg_nc_u4(crow + (s + 1) * (BK / 4)) : make_uint4(0, 0, 0, 0);
-      const uint16_t sbits = row_ok ? __ldg(srow + (s * BK) / 128) : (uint16_t)0;
+      const uint4 nx2 = ld_codes(s + 2);
+      const uint16_t snx2 = ld_scale(s + 2);
+      const uint16_t sbits = scur;
       if (use > 0 && !wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl, p.flag)) break;
       const uint32_t s2 = (uint32_t)sbits | ((uint32_t)sbits << 16);
       unsigned char* dst = b_ring + slot * kBStage + row_off;
@@ -261,7 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
       fence_async_smem();  // generic-proxy writes -> visible to the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->full_b[slot]);
-      cur = nxt;
+      cur = nx1;
+      nx1 = nx2;
+      scur = snx1;
+      snx1 = snx2;
     }
     // ---------------------------------------------------------------- epilogue
     (void)wait_or_abort(&ctl->done, 0, ctl, p.flag);

@@ -31,6 +31,8 @@
 //   and one HADD2 per two weights).
 // * Scales: each group's MMA result is scaled by its fp16 scale and added to
 //   fp32 row totals, so the group structure of the sum is kept exactly.
+#include <type_traits>
+
 #include "tq_internal.h"
 
 namespace tq {
@@ -46,6 +48,27 @@ struct Unit {
   uint2 a0, a1, b0, b1;        // 32 codes of groups g, g + 1 for rows gid (a) and gid + 8 (b)
   uint32_t sa, sb;             // fp16 scales of the two groups (low = first)
 };
+
+// Base-3 codes: the lane's 32 trits of a group start at trit 128 g + 32 tq,
+// inside byte b0 = k0 / 5 at digit r0 = k0 % 5; they span at most 8 bytes,
+// which lie in the 16-byte window starting at a8 = b0 & ~7 (two 8-byte loads).
+struct Unit3 {
+  uint2 w[8];                  // windows: (group 0, group 1) x (row gid, row gid + 8) x (lo, hi)
+  uint32_t sa, sb;
+};
+
+// 32 trits -> the 2-bit code words of the same 32 k (code = digit = t + 1):
+// every byte goes through a 256-entry table (five 2-bit codes per byte).
+__device__ __forceinline__ uint2 trits_to_codes(uint2 lo, uint2 hi, int o, int r0, const uint16_t* lut) {
+  const uint64_t L = ((uint64_t)lo.y << 32) | lo.x, H = ((uint64_t)hi.y << 32) | hi.x;
+  const uint64_t v = o ? ((L >> (8 * o)) | (H << (64 - 8 * o))) : L;  // bytes b0 .. b0 + 7
+  uint64_t a0 = 0, a1 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a0 |= (uint64_t)lut[(v >> (8 * i)) & 255u] << (10 * i);      // trits 0..19
+#pragma unroll
+  for (int i = 3; i < 8; ++i) a1 |= (uint64_t)lut[(v >> (8 * i)) & 255u] << (10 * (i - 3));  // trits 15..39
+  return make_uint2((uint32_t)(a0 >> (2 * r0)), (uint32_t)(a1 >> (2 * (r0 + 1))));
+}
 
 __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -231,8 +254,10 @@ __device__ __forceinline__ void scale_add(float acc[8], const float c0v[4], cons
 __host__ __device__ constexpr int xsum_stride(int mb) { return mb == 1 ? 1 : 8; }
 
 // Shared memory: [x' chunk][x' group sums][partial y]
-template <int MB>
+template <int MB, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
+  constexpr bool B3 = FMT == TQ_PACK_BASE3;
+  __shared__ uint16_t lut3[256];  // base-3 byte -> five 2-bit codes
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* xs = smem;
   float* xsum = reinterpret_cast<float*>(smem + p.sum_off);
@@ -256,6 +281,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
   const uint32_t xs_base = smem_u32(xs);
 
   for (int i = threadIdx.x; i < ntiles * 16 * M; i += kThreads) ypart[i] = 0.0f;
+  if (B3) {
+    for (int b = threadIdx.x; b < 256; b += kThreads) {
+      uint32_t v = 0x155u, q = (uint32_t)b;  // bytes >= 243 never occur; read as all zero trits
+      if (b < 243) {
+        v = 0;
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+          v |= (q % 3u) << (2 * i);
+          q /= 3u;
+        }
+      }
+      lut3[b] = (uint16_t)v;
+    }
+  }
   // Inputs (codes, scales, x) may come from the preceding kernel on the stream.
   pdl_wait();
 
@@ -274,12 +313,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
       int64_t ra = (t0 + lt) * 16 + gid, rb = ra + 8;
       if (ra >= p.N) ra = p.N - 1;
       if (rb >= p.N) rb = p.N - 1;
-      pa = p.codes + ra * p.ldc + cg0 * 32 + tq * 8;
-      pb = p.codes + rb * p.ldc + cg0 * 32 + tq * 8;
+      pa = p.codes + ra * p.ldc + (B3 ? 0 : cg0 * 32 + tq * 8);
+      pb = p.codes + rb * p.ldc + (B3 ? 0 : cg0 * 32 + tq * 8);
       qa = p.scales + ra * p.lds + cg0;
       qb = p.scales + rb * p.lds + cg0;
     };
     set_tile();
+    auto load_unit3 = [&](Unit3& d) {
+      const bool two = 2 * lp + 1 < ng;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int64_t k0 = (cg0 + 2 * lp + q) * 128 + 32 * tq;
+        const int64_t a8 = (k0 / 5) & ~(int64_t)7;
+        const bool has = q == 0 || two, hi = a8 + 16 <= p.ldc;
+        d.w[4 * q + 0] = has ? ldg_stream_u2(pa + a8) : make_uint2(0, 0);
+        d.w[4 * q + 1] = (has && hi) ? ldg_stream_u2(pa + a8 + 8) : make_uint2(0, 0);
+        d.w[4 * q + 2] = has ? ldg_stream_u2(pb + a8) : make_uint2(0, 0);
+        d.w[4 * q + 3] = (has && hi) ? ldg_stream_u2(pb + a8 + 8) : make_uint2(0, 0);
+      }
+      d.sa = (uint32_t)__ldg(qa + 2 * lp) | (two ? ((uint32_t)__ldg(qa + 2 * lp + 1) << 16) : 0u);
+      d.sb = (uint32_t)__ldg(qb + 2 * lp) | (two ? ((uint32_t)__ldg(qb + 2 * lp + 1) << 16) : 0u);
+      if (++lp == npairs) {
+        lp = 0;
+        ++lt;
+        set_tile();
+      }
+    };
     auto load_unit = [&](Unit& d) {
       const bool two = 2 * lp + 1 < ng;  // the unit's second group exists
       const int o = lp * 64;
@@ -301,10 +360,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
       }
     };
 
-    Unit buf[kDepth];
+    using Raw = typename std::conditional<B3, Unit3, Unit>::type;
+    constexpr int D = B3 ? 2 : kDepth;  // units in flight (base-3 units hold twice the registers)
+    Raw buf[D];
+    auto load_raw = [&](Raw& d) {
+      if constexpr (B3)
+        load_unit3(d);
+      else
+        load_unit(d);
+    };
 #pragma unroll
-    for (int s = 0; s < kDepth; ++s)
-      if (u0 + s < u1) load_unit(buf[s]);
+    for (int s = 0; s < D; ++s)
+      if (u0 + s < u1) load_raw(buf[s]);
 
     // rotate this chunk of x (all M rows) into the permuted fp16 layout
     if (c > 0) __syncthreads();  // previous chunk's activations no longer read
@@ -338,12 +405,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
 
-    for (int ub = u0; ub < u1; ub += kDepth) {
+    for (int ub = u0; ub < u1; ub += D) {
 #pragma unroll
-      for (int s = 0; s < kDepth; ++s) {
+      for (int s = 0; s < D; ++s) {
         if (ub + s < u1) {
-          const Unit cur = buf[s];
-          if (ub + s + kDepth < u1) load_unit(buf[s]);
+          Unit cur;
+          if constexpr (B3) {
+            const Unit3 raw = buf[s];
+            if (ub + s + D < u1) load_raw(buf[s]);
+            uint2 cw[4];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const int64_t k0 = (cg0 + 2 * cp + q) * 128 + 32 * tq;
+              const int64_t b0 = k0 / 5;
+              const int r0 = (int)(k0 - 5 * b0), o = (int)(b0 & 7);
+              cw[2 * q] = trits_to_codes(raw.w[4 * q], raw.w[4 * q + 1], o, r0, lut3);
+              cw[2 * q + 1] = trits_to_codes(raw.w[4 * q + 2], raw.w[4 * q + 3], o, r0, lut3);
+            }
+            cur.a0 = cw[0];
+            cur.b0 = cw[1];
+            cur.a1 = cw[2];
+            cur.b1 = cw[3];
+            cur.sa = raw.sa;
+            cur.sb = raw.sb;
+          } else {
+            cur = buf[s];
+            if (ub + s + D < u1) load_raw(buf[s]);
+          }
           const int gl = 2 * cp;
           const uint32_t xq = xs_base + (uint32_t)(gl * xs_group_bytes(ms) + tq * xs_quad_bytes(ms) + mB0 * 64);
           if constexpr (MB == 16) {
@@ -424,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
   cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
 }
 
-template <int MB>
+template <int MB, int FMT>
 cudaError_t launch_mb(const Params& p0, cudaStream_t s) {
   Params p = p0;
   const int64_t G = p.K / 128;
@@ -454,7 +542,7 @@ cudaError_t launch_mb(const Params& p0, cudaStream_t s) {
   p.xs_bytes = (int)(chunk * per_group);
   p.sum_off = (int)(chunk * xs_group_bytes(p.ms));
   const int smem = (int)(p.xs_bytes + tpc * 16 * p.M * 4);
-  cudaError_t e = cudaFuncSetAttribute(k_gemv<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(k_gemv<MB, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(clusters * kCl));
@@ -470,7 +558,7 @@ cudaError_t launch_mb(const Params& p0, cudaStream_t s) {
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemv<MB>, p);
+  return cudaLaunchKernelEx(&cfg, k_gemv<MB, FMT>, p);
 }
 
 }  // namespace
@@ -478,7 +566,7 @@ cudaError_t launch_mb(const Params& p0, cudaStream_t s) {
 cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
                         int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
-  if (fmt != TQ_PACK_2BIT) return cudaErrorNotSupported;
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return cudaErrorNotSupported;
   Params p{};
   p.codes = codes;
   p.ldc = ldc;
@@ -491,9 +579,14 @@ cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16
   p.M = (int)M;
   p.y = y;
   p.ldy = ldy;
-  if (M == 1) return launch_mb<1>(p, s);
-  if (M <= 8) return launch_mb<8>(p, s);
-  return launch_mb<16>(p, s);
+  if (fmt == TQ_PACK_BASE3) {
+    if (M == 1) return launch_mb<1, TQ_PACK_BASE3>(p, s);
+    if (M <= 8) return launch_mb<8, TQ_PACK_BASE3>(p, s);
+    return launch_mb<16, TQ_PACK_BASE3>(p, s);
+  }
+  if (M == 1) return launch_mb<1, TQ_PACK_2BIT>(p, s);
+  if (M <= 8) return launch_mb<8, TQ_PACK_2BIT>(p, s);
+  return launch_mb<16, TQ_PACK_2BIT>(p, s);
 }
 
 // This kernel has no waits that could stall (no producer/consumer barriers).

@@ -176,6 +176,24 @@ def test_gemv_full_size_sampled(orc, N, K, M):
     _gemv_case(orc, N, K, M, seed=N + K + M, rows=rows)
 
 
+@pytest.mark.parametrize("N,K,M", [
+    (256, 256, 1), (37, 384, 3), (15, 128, 1), (100, 640, 16), (300, 1280, 2), (513, 2560, 8),
+    (64, 27648 // 4, 5), (20, 27648, 1),
+])
+def test_gemv_base3_shapes(orc, N, K, M):
+    """Base-3 codes (five trits per byte; a lane's 32 trits start anywhere in
+    a byte and the last byte of a row is padded)."""
+    _gemv_case(orc, N, K, M, seed=N * 17 + K + M, fmt=tq.TQ_PACK_BASE3)
+
+
+@pytest.mark.parametrize("N,K", [(27648, 5120), (5120, 27648)])
+@pytest.mark.parametrize("M", [1, 16])
+def test_gemv_base3_full_size_sampled(orc, N, K, M):
+    rows = np.sort(np.random.default_rng(N + K + M + 3).choice(N, size=32, replace=False))
+    rows[-1] = N - 1
+    _gemv_case(orc, N, K, M, seed=N + K + M + 3, fmt=tq.TQ_PACK_BASE3, rows=rows)
+
+
 def test_gemv_zero_and_delta_activations(orc):
     N, K = 96, 512
     W = synth.weights(N, K, 9, dtype="bf16")
