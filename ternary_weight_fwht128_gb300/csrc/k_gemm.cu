@@ -29,6 +29,8 @@
 // word of codes without shuffling, and the pre-pass stores x' in that order.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "tq_internal.h"
 
 namespace tq {
@@ -357,8 +359,14 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   p.n_tiles_m = (int)((M + BM - 1) / BM);
   p.vec_store = ((reinterpret_cast<uintptr_t>(y) & 15u) == 0 && ldy % 4 == 0) ? 1 : 0;
   const int64_t tiles = (int64_t)p.n_tiles_m * ((N + BN - 1) / BN);
-  cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-  if (e != cudaSuccess) return e;
+  static std::atomic<bool> smem_set[64];  // the kernel's shared-memory limit, raised once per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!smem_set[dev].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    if (e != cudaSuccess) return e;
+    smem_set[dev].store(true, std::memory_order_release);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)tiles);
   cfg.blockDim = dim3(kThreads);

@@ -31,6 +31,7 @@
 //   and one HADD2 per two weights).
 // * Scales: each group's MMA result is scaled by its fp16 scale and added to
 //   fp32 row totals, so the group structure of the sum is kept exactly.
+#include <atomic>
 #include <type_traits>
 
 #include "tq_internal.h"
@@ -542,8 +543,17 @@ cudaError_t launch_mb(const Params& p0, cudaStream_t s) {
   p.xs_bytes = (int)(chunk * per_group);
   p.sum_off = (int)(chunk * xs_group_bytes(p.ms));
   const int smem = (int)(p.xs_bytes + tpc * 16 * p.M * 4);
-  cudaError_t e = cudaFuncSetAttribute(k_gemv<MB, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+  // raise the kernel's shared-memory limit only when a launch needs more
+  static std::atomic<int> smem_set[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem_set[dev].load(std::memory_order_acquire) < smem) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemv<MB, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int cur = smem_set[dev].load(std::memory_order_acquire);
+    while (cur < smem && !smem_set[dev].compare_exchange_weak(cur, smem)) {
+    }
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(clusters * kCl));
   cfg.blockDim = dim3(kThreads);
@@ -584,12 +594,14 @@ cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16
     if (M <= 8) return launch_mb<8, TQ_PACK_BASE3>(p, s);
     return launch_mb<16, TQ_PACK_BASE3>(p, s);
   }
-  if (M == 1) return launch_mb<1, TQ_PACK_2BIT>(p, s);
+  if (M == 1) {
+    const cudaError_t e = launch_gemv_tc(codes, ldc, scales, lds, N, K, x, y, s);
+    if (e != cudaErrorNotSupported) return e;
+    return launch_mb<1, TQ_PACK_2BIT>(p, s);
+  }
   if (M <= 8) return launch_mb<8, TQ_PACK_2BIT>(p, s);
   return launch_mb<16, TQ_PACK_2BIT>(p, s);
 }
 
-// This kernel has no waits that could stall (no producer/consumer barriers).
-unsigned int take_fault_gemv() { return 0; }
 
 }  // namespace tq

@@ -194,6 +194,30 @@ def test_gemv_base3_full_size_sampled(orc, N, K, M):
     _gemv_case(orc, N, K, M, seed=N + K + M + 3, fmt=tq.TQ_PACK_BASE3, rows=rows)
 
 
+@pytest.mark.parametrize("N,K", [(19457, 128), (20000, 384), (19456, 1280), (19500, 4480)])
+def test_gemv_tc_shapes(orc, N, K):
+    """M = 1 with at least one 128-row tile per SM takes the tensor-memory
+    kernel: a ragged last tile (down to one row), one group per row, odd group
+    counts (padded four-group stages), sampled rows including the tail."""
+    rng = np.random.default_rng(N + K)
+    rows = np.unique(np.concatenate([rng.choice(N, size=40, replace=False), np.arange(N - 130, N)]))
+    _gemv_case(orc, N, K, 1, seed=N * 7 + K, rows=rows)
+
+
+def test_gemv_tc_zero_and_delta_activations(orc):
+    N, K = 19456, 512
+    W = synth.weights(N, K, 11, dtype="bf16")
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    x = np.zeros((1, K), dtype=np.uint16)
+    y0 = tq.gemv(c2, s, to_dev_bf16(x), K).cpu().numpy()
+    assert np.all(y0 == 0.0)
+    x[0, 300] = synth.f32_to_bf16_bits(np.array([-2.5], dtype=np.float32))[0]
+    y1 = tq.gemv(c2, s, to_dev_bf16(x), K).cpu().numpy()
+    rows = np.arange(0, N, 97)
+    T, S = orc.quantize(W, rows)
+    check_y(y1[:, rows], orc.gemv(T, S, synth.bf16_bits_to_f32(x)))
+
+
 def test_gemv_zero_and_delta_activations(orc):
     N, K = 96, 512
     W = synth.weights(N, K, 9, dtype="bf16")
