@@ -538,6 +538,36 @@ size_t smem_bytes(int groups_cap, int tiles_cap) {
          (size_t)groups_cap * sizeof(float2) + (size_t)tiles_cap * 128 * sizeof(float) + sizeof(Ctl);
 }
 
+// Clusters of kcl CTAs that can be resident at once (a cluster lives on one
+// GPC, so large clusters do not tile all SMs); queried once per device.
+int max_active_clusters(int kcl) {
+  static std::atomic<int> cache[64][4];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int slot = kcl == 1 ? 0 : kcl == 2 ? 1 : kcl == 4 ? 2 : 3;
+  int v = cache[dev][slot].load(std::memory_order_acquire);
+  if (v > 0) return v;
+  const int smem = device_max_smem_optin();
+  if (cudaFuncSetAttribute(k_gemv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(device_sm_count() * kcl));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)kcl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&v, k_gemv_tc, &cfg) != cudaSuccess || v < 1) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cache[dev][slot].store(v, std::memory_order_release);
+  return v;
+}
+
 }  // namespace
 
 unsigned int take_fault_gemv() {
@@ -551,36 +581,36 @@ unsigned int take_fault_gemv() {
 }
 
 // Work split: kcl in {1, 2, 4, 8} CTAs per cluster share a tile range and
-// split its K groups; the choice minimises the largest per-CTA work, with a
-// small allowance for grids a little larger than the SM count.
+// split its K groups; at most as many clusters as can be resident at once
+// (one wave).  The choice minimises the stages of the busiest CTA (a stage
+// is four groups of one 128-row tile); ties go to fewer CTAs.
 cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,
                            int64_t K, const void* x, float* y, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   const int64_t G = K / 128, T = (N + 127) / 128;
   const int sms = device_sm_count();
   const int64_t smem_max = device_max_smem_optin();
-  double best = 0.0;
-  int64_t best_kcl = 0, best_c = 0;
+  int64_t best = 0, best_kcl = 0, best_c = 0;
   for (int64_t kcl = 1; kcl <= 8; kcl *= 2) {
     if (kcl > G) break;
+    int64_t c = max_active_clusters((int)kcl);
+    if (c > sms / kcl) c = sms / kcl;
+    if (c > T) c = T;
+    if (c < 1) continue;
     const int64_t gcap = 4 * (((G + kcl - 1) / kcl + 3) / 4);
-    for (int64_t c : {T < sms / kcl ? T : sms / kcl}) {
-      if (c < 1) continue;
-      const int64_t tcap = (T + c - 1) / c;
-      if ((int64_t)smem_bytes((int)gcap, (int)tcap) > smem_max) continue;
-      double cost = (double)tcap * (double)((G + kcl - 1) / kcl);
-      if (c * kcl > sms) cost *= 1.25;
-      if (best_kcl == 0 || cost < best - 1e-9) {
-        best = cost;
-        best_kcl = kcl;
-        best_c = c;
-      }
+    const int64_t tcap = (T + c - 1) / c;
+    if ((int64_t)smem_bytes((int)gcap, (int)tcap) > smem_max) continue;
+    const int64_t cost = tcap * (gcap / 4);
+    if (best_kcl == 0 || cost < best || (cost == best && c * kcl < best_c * best_kcl)) {
+      best = cost;
+      best_kcl = kcl;
+      best_c = c;
     }
   }
   if (best_kcl == 0) return cudaErrorNotSupported;
-  // 128-row tiles need at least one tile per SM to keep the GPU busy; below
-  // that the 16-row-tile kernel balances better
-  if (T < sms) return cudaErrorNotSupported;
+  // small matrices (under about four stages per SM) are dominated by fixed
+  // latencies, where the 16-row-tile kernel does as well or better
+  if (T * ((G + 3) / 4) < 4 * (int64_t)sms) return cudaErrorNotSupported;
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   CUtensorMap map;

@@ -194,18 +194,19 @@ def test_gemv_base3_full_size_sampled(orc, N, K, M):
     _gemv_case(orc, N, K, M, seed=N + K + M + 3, fmt=tq.TQ_PACK_BASE3, rows=rows)
 
 
-@pytest.mark.parametrize("N,K", [(19457, 128), (20000, 384), (19456, 1280), (19500, 4480)])
+@pytest.mark.parametrize("N,K", [(19457, 2560), (20000, 2944), (4999, 27648), (19500, 4480)])
 def test_gemv_tc_shapes(orc, N, K):
-    """M = 1 with at least one 128-row tile per SM takes the tensor-memory
-    kernel: a ragged last tile (down to one row), one group per row, odd group
-    counts (padded four-group stages), sampled rows including the tail."""
+    """M = 1 GEMVs of more than about ten megabytes take the tensor-memory
+    kernel: ragged last tiles (down to one row), group counts that leave
+    padded four-group stages and odd K slices, few tiles with a deep K
+    split, sampled rows including the tail."""
     rng = np.random.default_rng(N + K)
     rows = np.unique(np.concatenate([rng.choice(N, size=40, replace=False), np.arange(N - 130, N)]))
     _gemv_case(orc, N, K, 1, seed=N * 7 + K, rows=rows)
 
 
 def test_gemv_tc_zero_and_delta_activations(orc):
-    N, K = 19456, 512
+    N, K = 19456, 2560
     W = synth.weights(N, K, 11, dtype="bf16")
     c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
     x = np.zeros((1, K), dtype=np.uint16)
