@@ -36,10 +36,11 @@ HIDDEN, FFN, LAYERS = 5120, 27648, 64
 LAYER_SHAPES = [("h2h_a", HIDDEN, HIDDEN), ("h2h_b", HIDDEN, HIDDEN), ("gate", FFN, HIDDEN), ("up", FFN, HIDDEN),
                 ("down", HIDDEN, FFN)]
 METRIC = "ternary GEMV packed-weight HBM GB/s (% of peak); prefill GEMM TFLOP/s"
-# DRAM bytes per algorithmic byte of k_gemv<1>, measured with ncu on one
-# 27648x5120 launch (37,657,600 read for 37,601,280 packed bytes); every weight
-# byte is read once, so the ratio carries over to the step's other shapes.
-GEMV_TRAFFIC_RATIO = 37657600 / 37601280
+# DRAM bytes per algorithmic byte of k_gemv_tc, from an ncu capture of one
+# 27648x5120 launch (dram__bytes_read.sum + dram__bytes_write.sum over the
+# 37,601,280 packed bytes); None until such a capture exists for the kernel as
+# it stands.
+GEMV_TC_TRAFFIC_RATIO = None
 WORKLOAD = ("decode GEMV M=1, 2-bit codes, 64-layer stack of 27B-class shapes "
             "{5120x5120 x2, 27648x5120 x2, 5120x27648} per layer (320 launches, FWHT-128 fused)")
 
@@ -192,6 +193,54 @@ def activations(torch, dev, K: int, M: int, seed: int):
     return x.to(torch.bfloat16)
 
 
+def capture(torch, fn):
+    """fn's launches captured once into a CUDA graph (replayed per step)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def timing_event(torch):
+    """A timing event that, inside a graph capture, becomes an event-record
+    node of its own (needs torch's `external` events; None without them)."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
+def launch_times(args, tq, torch, launches, path_of) -> dict:
+    """Per-kernel launch durations in the step: a copy of the step graph with
+    a timing event before and after every launch, replayed `steps` times (the
+    events cut the programmatic overlap between neighbours, so each duration
+    is one launch on its own in the stream).  Without graph-capturable events
+    the same launches run eagerly between events."""
+    ev = [(timing_event(torch), timing_event(torch)) for _ in launches]
+    graphed = all(a is not None for a, _ in ev)
+    if not graphed:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in launches]
+
+    def body():
+        for (e0, e1), fn in zip(ev, launches):
+            e0.record()
+            fn()
+            e1.record()
+
+    g = capture(torch, body) if graphed else None
+    reps = max(3, min(args.steps, 10))
+    sums: dict[int, list[float]] = {}
+    for _ in range(reps):
+        if graphed:
+            g.replay()
+        else:
+            body()
+        torch.cuda.synchronize()
+        for i, (e0, e1) in enumerate(ev):
+            sums.setdefault(path_of[i], []).append(e0.elapsed_time(e1))
+    return {"graphed": graphed, "reps": reps, "ms": sums}
+
+
 def gpu_arm(args, world, rank, local):
     import torch
     import ternary_weight_fwht128_gb300 as tq
@@ -209,13 +258,27 @@ def gpu_arm(args, world, rank, local):
     ys = {N: torch.empty(1, N, device=dev) for N in (HIDDEN, FFN)}
     launches_per_step = LAYERS * len(LAYER_SHAPES)
 
-    def step():
-        for mats in stack:
-            for _, N, K, c2, s, _ in mats:
-                tq.gemv(c2, s, xs[K], K, tq.TQ_PACK_2BIT, out=ys[N])
+    # the weights are written once, before any timing: every GEMV may start
+    # streaming them while the one before it finishes (TQ_GEMV_WEIGHTS_READY)
+    def gemv_calls(xsrc):
+        return [(lambda c2=c2, s=s, N=N, K=K: tq.gemv(c2, s, xsrc[K], K, tq.TQ_PACK_2BIT, out=ys[N],
+                                                      weights_ready=True))
+                for mats in stack for _, N, K, c2, s, _ in mats]
 
+    calls = gemv_calls(xs)
+
+    def step():
+        for fn in calls:
+            fn()
+
+    # eager steps first: one-time set-up (attributes, occupancy queries) runs
+    # before the capture; then the step's 320 launches become one CUDA graph
     for _ in range(args.warmup):
         step()
+    torch.cuda.synchronize()
+    graph = capture(torch, step)
+    for _ in range(args.warmup):
+        graph.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
@@ -223,7 +286,7 @@ def gpu_arm(args, world, rank, local):
         torch.cuda.synchronize()
         e0.record(stream)
         for _ in range(args.steps):
-            step()
+            graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(world, dev)
@@ -231,23 +294,51 @@ def gpu_arm(args, world, rank, local):
     ms = max_over_ranks(ms_local, world, dev)
     bytes_step = step_bytes()
     gbs = world * bytes_step / (ms * 1e-3) / 1e9
-    gbs_rank = bytes_step / (ms_local * 1e-3) / 1e9
+
+    # ---- per-kernel launch durations (roofline of the dominant kernel)
+    shapes = [(N, K) for mats in stack for _, N, K, _, _, _ in mats]
+    path_of = [tq.gemv_path(N, K, 1, tq.TQ_PACK_2BIT) for N, K in shapes]
+    lt = launch_times(args, tq, torch, calls, path_of)
+    names = {tq.TQ_GEMV_TENSOR_MEMORY: "k_gemv_tc (tcgen05, weights in tensor memory)",
+             tq.TQ_GEMV_MMA_SYNC: "k_gemv<1> (mma.sync)"}
+    kernels = []
+    for pth, times in lt["ms"].items():
+        idx = [i for i, q in enumerate(path_of) if q == pth]
+        nbytes = sum(packed_bytes(*shapes[i]) for i in idx)
+        per_launch_ms = sum(times) / len(times)
+        step_ms = per_launch_ms * len(idx)
+        kernels.append({"kernel": names[pth], "launches_per_step": len(idx),
+                        "us_per_launch": round(per_launch_ms * 1e3, 3),
+                        "bytes_per_launch": nbytes // len(idx),
+                        "GB/s": round(nbytes / len(idx) / (per_launch_ms * 1e-3) / 1e9, 1),
+                        "ms_per_step_alone": round(step_ms, 4)})
+    kernels.sort(key=lambda k: -k["ms_per_step_alone"])
+    total_alone = sum(k["ms_per_step_alone"] for k in kernels)
+    for k in kernels:
+        k["share"] = round(k["ms_per_step_alone"] / total_alone, 4)
+    dom = kernels[0]
+    dom_is_tc = dom["kernel"].startswith("k_gemv_tc")
 
     # ---- end to end through the public API with host buffers: every step
     # copies its activations in from pinned host memory (one token row per
-    # input width), runs the 320 GEMVs, and reads its outputs back.
+    # input width), replays the step's 320 GEMVs, and reads its outputs back.
     hx = {K: xs[K].cpu().pin_memory() for K in xs}
     hy = {N: torch.empty(1, N, dtype=torch.float32).pin_memory() for N in ys}
     dx = {K: torch.empty_like(xs[K]) for K in xs}
     h2d = sum(t.numel() * t.element_size() for t in hx.values())
     d2h = sum(t.numel() * t.element_size() for t in hy.values())
+    e2e_calls = gemv_calls(dx)
+
+    def e2e_compute():
+        for fn in e2e_calls:
+            fn()
+
+    e2e_graph = capture(torch, e2e_compute)
 
     def e2e_step():
         for K in dx:
             dx[K].copy_(hx[K], non_blocking=True)
-        for mats in stack:
-            for _, N, K, c2, s, _ in mats:
-                tq.gemv(c2, s, dx[K], K, tq.TQ_PACK_2BIT, out=ys[N])
+        e2e_graph.replay()
         for N in hy:
             hy[N].copy_(ys[N], non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -267,6 +358,7 @@ def gpu_arm(args, world, rank, local):
 
     if rank != 0:
         return
+    dom_gbs = dom["GB/s"]
     line = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -278,20 +370,26 @@ def gpu_arm(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "u8 2-bit codes x fp16 scales, fp16 x' on mma.sync, fp32 accumulate",
+        "dtype": "u8 codes; e4m3 x e4m3 (tcgen05) and f16 x f16 (mma.sync) MMAs; f32 accumulate",
         "data": "synthetic (seeded; weights N(0,0.02)+0.1% x20 outliers, x N(0,1)+4 channels x30)",
         "config": {"workload": WORKLOAD, "M": 1, "layers": LAYERS, "packed_bytes_per_step": bytes_step,
                    "launches_per_step": launches_per_step,
+                   "launch": "one CUDA graph per step (320 launches, programmatic dependent launch edges; "
+                             "tq_gemv_ex with TQ_GEMV_WEIGHTS_READY: weights stream while the previous GEMV ends)",
                    "l2": "inputs larger than L2 (8.1 GB of packed weights streamed per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "frac_of_peak": round(gbs_rank / pk["hbm_gbs"], 4),
-        "roofline": {"bound": "hbm", "achieved": round(gbs_rank, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(gbs_rank / pk["hbm_gbs"], 4),
-                     "traffic": int(GEMV_TRAFFIC_RATIO * bytes_step / launches_per_step),
-                     "traffic_note": "DRAM bytes per launch, ncu capture of one 27648x5120 launch scaled by "
-                                     "the algorithmic bytes of the average launch of the step",
-                     "kernel": "k_gemv<1> (tq_gemv, M=1)",
+        "frac_of_peak": round(gbs / world / pk["hbm_gbs"], 4),
+        "roofline": {"bound": "hbm", "achieved": dom_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(dom_gbs / pk["hbm_gbs"], 4),
+                     "traffic": (int(GEMV_TC_TRAFFIC_RATIO * dom["bytes_per_launch"])
+                                 if dom_is_tc and GEMV_TC_TRAFFIC_RATIO else None),
+                     "traffic_note": "DRAM bytes per launch of the dominant kernel, ncu capture of one "
+                                     "27648x5120 launch (same algorithmic bytes as every launch of it here)",
+                     "kernel": dom["kernel"],
+                     "kernel_timing": ("timing-event nodes around each launch in a replay of the step graph"
+                                       if lt["graphed"] else "CUDA events around each eager launch of the step"),
                      "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
+        "kernels": kernels,
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),

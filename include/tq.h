@@ -119,6 +119,32 @@ TQ_API tq_status tq_gemv(const uint8_t *codes, int64_t ldc, int fmt, const uint1
                   int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
                   tq_stream stream);
 
+/* tq_gemv with flags (0 = exactly tq_gemv).
+ *   TQ_GEMV_WEIGHTS_READY  codes and scales were completely written before
+ *       the work that precedes this call on `stream` started (inference
+ *       weights written once, long before).  The kernel may then start
+ *       streaming them while that preceding work is still finishing
+ *       (programmatic dependent launch); x is still read only after it has
+ *       finished.  Without the flag every input waits for it.
+ * Unknown flag bits: TQ_ERR_INVALID_ARG.  Everything else as tq_gemv. */
+enum { TQ_GEMV_WEIGHTS_READY = 1 };
+TQ_API tq_status tq_gemv_ex(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
+                            int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
+                            unsigned int flags, tq_stream stream);
+
+/* Which kernel tq_gemv runs for a shape (introspection; launches nothing):
+ *   TQ_GEMV_TENSOR_MEMORY  M == 1, 2-bit codes, more than about 4 x (SM
+ *                          count) stages of 128 rows x 512 k: weights
+ *                          unpacked to fp8 in tensor memory, activations as
+ *                          three e4m3 pieces, tcgen05 MMAs;
+ *   TQ_GEMV_MMA_SYNC       everything else: fp16 x' in shared memory, weights
+ *                          as fp16 on mma.sync (16-row tiles).
+ * Queries device properties of the current device on first use.  Returns
+ * -TQ_ERR_INVALID_ARG / -TQ_ERR_SHAPE for arguments tq_gemv would reject
+ * with those codes. */
+enum { TQ_GEMV_TENSOR_MEMORY = 1, TQ_GEMV_MMA_SYNC = 2 };
+TQ_API int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt);
+
 /* Bytes of caller-provided workspace tq_gemm needs for M x K activations:
  * the rotated activations in fp16 plus a status word. */
 TQ_API size_t tq_gemm_workspace_bytes(int64_t M, int64_t K);

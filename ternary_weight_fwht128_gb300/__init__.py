@@ -27,7 +27,10 @@ TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
 TQ_PACK_2BIT, TQ_PACK_BASE3, TQ_PACK_BOTH = 1, 2, 3
 
 EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_quantize_pack", "tq_gemv",
-            "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_check_range", "tq_device_fault", "tq_gemm_noalloc")
+            "tq_gemv_ex", "tq_gemv_path", "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_check_range", "tq_device_fault",
+            "tq_gemm_noalloc")
+TQ_GEMV_TENSOR_MEMORY, TQ_GEMV_MMA_SYNC = 1, 2
+TQ_GEMV_WEIGHTS_READY = 1
 
 _lib = None
 _i64 = ctypes.c_int64
@@ -60,6 +63,11 @@ def lib() -> ctypes.CDLL:
         L.tq_quantize_pack.argtypes = [_vp, _int, _i64, _i64, _i64, _int, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
         L.tq_gemv.restype = _int
         L.tq_gemv.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp]
+        L.tq_gemv_ex.restype = _int
+        L.tq_gemv_ex.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, ctypes.c_uint,
+                                 _vp]
+        L.tq_gemv_path.restype = _int
+        L.tq_gemv_path.argtypes = [_i64, _i64, _i64, _int]
         L.tq_gemm_workspace_bytes.restype = ctypes.c_size_t
         L.tq_gemm_workspace_bytes.argtypes = [_i64, _i64]
         L.tq_gemm.restype = _int
@@ -145,8 +153,10 @@ def quantize_pack(W: torch.Tensor, fmt: int = TQ_PACK_BOTH, stream=None):
 
 
 def gemv(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, fmt: int = TQ_PACK_2BIT,
-         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y [M][N] fp32 = ternary GEMV/skinny GEMM of bf16 x [M][K] (M <= 16)."""
+         out: torch.Tensor | None = None, stream=None, weights_ready: bool = False) -> torch.Tensor:
+    """y [M][N] fp32 = ternary GEMV/skinny GEMM of bf16 x [M][K] (M <= 16).
+    weights_ready: codes and scales were complete before the work preceding
+    this call on the stream started (tq_gemv_ex, TQ_GEMV_WEIGHTS_READY)."""
     _cuda2d(codes, "codes")
     _cuda2d(scales, "scales")
     _cuda2d(x, "x")
@@ -154,10 +164,20 @@ def gemv(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, fmt
     M = x.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    st = lib().tq_gemv(codes.data_ptr(), codes.stride(0), fmt, scales.data_ptr(), scales.stride(0), N, K,
-                       x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), _stream(stream))
-    _check(st, "tq_gemv")
+    flags = TQ_GEMV_WEIGHTS_READY if weights_ready else 0
+    st = lib().tq_gemv_ex(codes.data_ptr(), codes.stride(0), fmt, scales.data_ptr(), scales.stride(0), N, K,
+                          x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), flags, _stream(stream))
+    _check(st, "tq_gemv_ex")
     return out
+
+
+def gemv_path(N: int, K: int, M: int = 1, fmt: int = TQ_PACK_2BIT) -> int:
+    """Which kernel tq_gemv runs for the shape: TQ_GEMV_TENSOR_MEMORY or
+    TQ_GEMV_MMA_SYNC (queries the current CUDA device; launches nothing)."""
+    r = int(lib().tq_gemv_path(N, K, M, fmt))
+    if r < 0:
+        raise TQError(-r, "tq_gemv_path")
+    return r
 
 
 def gemm_workspace_bytes(M: int, K: int) -> int:

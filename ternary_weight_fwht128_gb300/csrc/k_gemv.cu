@@ -146,6 +146,7 @@ struct Params {
   int xs_bytes;      // shared bytes for those activations (permuted x', then per-group sums)
   int sum_off;       // byte offset of the per-group sums of x' inside that region
   int ms;            // activation rows stored per (group, quad): 1 for M == 1, else M
+  int prefetch;      // codes and scales are ready before the preceding kernel ends
 };
 
 // Rotated activations in shared memory (fp16).  Lane tq of a quad holds the
@@ -296,8 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
       lut3[b] = (uint16_t)v;
     }
   }
-  // Inputs (codes, scales, x) may come from the preceding kernel on the stream.
-  pdl_wait();
+  // Inputs may come from the preceding kernel on the stream: x always waits
+  // for it; codes and scales too unless the caller declared them ready, in
+  // which case the first units of codes are in flight while it finishes.
+  if (!p.prefetch) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   for (int c = 0; c < nchunks; ++c) {
     const int64_t cg0 = g0 + (int64_t)c * p.chunk_groups;
@@ -373,6 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
 #pragma unroll
     for (int s = 0; s < D; ++s)
       if (u0 + s < u1) load_raw(buf[s]);
+    if (c == 0 && p.prefetch) {
+      pdl_wait();
+      pdl_launch_dependents();
+    }
 
     // rotate this chunk of x (all M rows) into the permuted fp16 layout
     if (c > 0) __syncthreads();  // previous chunk's activations no longer read
@@ -494,8 +504,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
       }
     }
   }
-  pdl_launch_dependents();
-
   // ---- reduce the kCl partial sums through distributed shared memory
   __syncthreads();
   cluster_sync();
@@ -574,7 +582,8 @@ cudaError_t launch_mb(const Params& p0, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
-                        int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, cudaStream_t s) {
+                        int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, bool prefetch,
+                        cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return cudaErrorNotSupported;
   Params p{};
@@ -589,13 +598,14 @@ cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16
   p.M = (int)M;
   p.y = y;
   p.ldy = ldy;
+  p.prefetch = prefetch ? 1 : 0;
   if (fmt == TQ_PACK_BASE3) {
     if (M == 1) return launch_mb<1, TQ_PACK_BASE3>(p, s);
     if (M <= 8) return launch_mb<8, TQ_PACK_BASE3>(p, s);
     return launch_mb<16, TQ_PACK_BASE3>(p, s);
   }
   if (M == 1) {
-    const cudaError_t e = launch_gemv_tc(codes, ldc, scales, lds, N, K, x, y, s);
+    const cudaError_t e = launch_gemv_tc(codes, ldc, scales, lds, N, K, x, y, prefetch, s);
     if (e != cudaErrorNotSupported) return e;
     return launch_mb<1, TQ_PACK_2BIT>(p, s);
   }

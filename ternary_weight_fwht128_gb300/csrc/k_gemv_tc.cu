@@ -48,11 +48,12 @@
 //                sixteen MMAs of each stage of team t into accumulator
 //                buffer t;
 //   warps 19-22  read the accumulators of their 32 rows and apply the scales.
-// The kcl partial sums of every output are added through distributed shared
-// memory in a fixed order.  Every wait is bounded in time; a wait that runs
-// out sets the library's GEMV status word and the CTA winds down (pending
-// copies and MMAs are waited for, tensor memory is freed, the cluster
-// barriers are still met).
+// Ranks 1 .. kcl-1 push each finished row sum into rank 0's shared memory
+// (st.async, counted on an mbarrier there) and exit; rank 0 adds the kcl
+// partial sums in a fixed order and writes y.  Every wait is bounded in time;
+// a wait that runs out sets the library's GEMV status word and the CTA winds
+// down (pending copies and MMAs are waited for, tensor memory is freed, the
+// cluster barrier is still met).
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -70,6 +71,7 @@ constexpr int kDecWarps = 16;                 // two teams of 8: even and odd de
 constexpr int kTeamWarps = 8;
 constexpr int kTmaWarp = 16;
 constexpr int kMmaWarp = 17;                  // warps 17, 18 issue the MMAs of team 0, 1
+constexpr int kEpiWarp0 = 19;                 // warps 19-22: epilogue
 constexpr int kThreads = 32 * 23;             // + 4 epilogue warps (19-22)
 constexpr int kRing = 4;                      // code slots in flight (four groups each)
 constexpr int kAbuf = 3;                      // weight (A) buffers in tensor memory, one stage each
@@ -93,6 +95,7 @@ struct Ctl {
   uint64_t a_free[kAbuf]; // MMA -> decoders
   uint64_t d_full[kDbuf]; // MMA -> epilogue
   uint64_t d_free[kDbuf]; // epilogue -> MMA
+  uint64_t red_bar;       // rank 0: the other ranks' partial outputs have landed
   uint32_t tmem_base;
   int abort;
 };
@@ -107,6 +110,7 @@ struct Params {
   int clusters;    // tile ranges: cluster c owns [c*T/clusters, (c+1)*T/clusters)
   int groups_cap;  // groups per CTA the shared layout holds (multiple of 4)
   int tiles_cap;   // tiles per cluster the partial outputs hold
+  int prefetch;    // codes and scales are ready before the preceding kernel ends
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -184,16 +188,24 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ float ld_dsmem_f32(const float* p, uint32_t rank) {
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(const void* p, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  return remote;
+}
+
+// 4-byte store into another CTA's shared memory that counts as 4 bytes of
+// transaction on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr), "f"(v),
+               "r"(remote_bar)
+               : "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -224,7 +236,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ct
 }
 
 // Shared memory (1024-aligned): [code ring][B: groups_cap x 1 KB][zeros 256]
-// [ztab: groups_cap x {Zt, pw}][partial y: tiles_cap x 128][Ctl]
+// [ztab: groups_cap x {Zt, pw}][partial y: kcl slots x tiles_cap x 128][Ctl]
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__ CUtensorMap cmap, const Params p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -233,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   unsigned char* zero = bsm + p.groups_cap * kGroupBBytes;
   float2* ztab = reinterpret_cast<float2*>(zero + kZeroBytes);
   float* ypart = reinterpret_cast<float*>(ztab + p.groups_cap);
-  Ctl* ctl = reinterpret_cast<Ctl*>(ypart + p.tiles_cap * 128);
+  Ctl* ctl = reinterpret_cast<Ctl*>(ypart + p.kcl * p.tiles_cap * 128);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -260,6 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       mbar_init(&ctl->d_full[i], 1);
       mbar_init(&ctl->d_free[i], 4);
     }
+    mbar_init(&ctl->red_bar, 1);
+    // rank 0 receives every other rank's partial outputs: ntiles x 128 floats each
+    if (rank == 0 && p.kcl > 1) mbar_arrive_expect_tx(&ctl->red_bar, (uint32_t)((p.kcl - 1) * ntiles * 128 * 4));
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -275,26 +290,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     const int n16 = (p.groups_cap * kGroupBBytes + kZeroBytes) / 16;
     for (int i = threadIdx.x; i < n16; i += kThreads) z4[i] = make_uint4(0, 0, 0, 0);
     for (int i = threadIdx.x; i < p.groups_cap; i += kThreads) ztab[i] = make_float2(0.0f, 0.0f);
-    for (int i = threadIdx.x; i < p.tiles_cap * 128; i += kThreads) ypart[i] = 0.0f;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  // Rank 0's reduction barrier is armed: the other ranks may push once they
+  // pass the matching wait (epilogue warps before their first push, every
+  // other warp before it exits -- each thread waits exactly once).
+  cluster_arrive();
 
-  // Every input (codes, scales, x) may come from the preceding kernel.
-  pdl_wait();
-  pdl_launch_dependents();
-
+  // Inputs may come from the preceding kernel on the stream: x always waits
+  // for it; codes and scales too unless the caller declared them ready, in
+  // which case the ring fills while that kernel finishes.
   int issued_loads = 0;
-  if (warp == kTmaWarp && lane == 0) {  // fill the ring while the others rotate x
+  auto fill_ring = [&]() {
     for (; issued_loads < L && issued_loads < kRing; ++issued_loads) {
       const int l = issued_loads, tile = l / nlc, lc = l - tile * nlc;
       mbar_arrive_expect_tx(&ctl->full[l], kSlotBytes);
       tma_load_2d(smem_u32(ring + l * kSlotBytes), &cmap, (int)((g0 + 4 * lc) * 32), (int)((t0 + tile) * 128),
                   &ctl->full[l]);
     }
-  }
+  };
+  if (p.prefetch && warp == kTmaWarp && lane == 0) fill_ring();
+  pdl_wait();
+  pdl_launch_dependents();
+  if (!p.prefetch && warp == kTmaWarp && lane == 0) fill_ring();  // while the others rotate x
 
   // ---- rotate this CTA's slice of x and split it into three e4m3 pieces
   for (int gl = warp; gl < ng; gl += kThreads / 32) {
@@ -463,6 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     };
     uint32_t sc[2];
     ld_scales(0, 0, sc);
+    cluster_wait();
+    const uint32_t push_base = rank == 0 ? 0u : map_rank(ypart + rank * p.tiles_cap * 128 + r, 0);
+    const uint32_t push_bar = rank == 0 ? 0u : map_rank(&ctl->red_bar, 0);
     for (int s = 0; s < S; ++s) {
       // scales of the next stage, loaded one stage ahead
       const int ntl = (ch + 1 == nch) ? tile + 1 : tile, nc = (ch + 1 == nch) ? 0 : ch + 1;
@@ -483,8 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
         const float sh = __half2float(__ushort_as_half((uint16_t)(sc[h >> 1] >> (16 * (h & 1)))));
         acc = fmaf(sh * z.y, (d[h][0] + d[h][1]) + d[h][2] + z.x, acc);
       }
-      if (ch + 1 == nch) {
-        ypart[tile * 128 + r] = acc;
+      if (ch + 1 == nch) {  // this row of the tile is complete: into rank 0's slot of this rank
+        if (rank == 0)
+          ypart[tile * 128 + r] = acc;
+        else
+          st_async_f32(push_base + (uint32_t)(tile * 128 * 4), acc, push_bar);
         acc = 0.0f;
       }
       sc[0] = sc_next[0];
@@ -495,20 +522,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     }
   }
 
-  // ---- add the kcl CTAs' partial sums through distributed shared memory
+  // ---- rank 0 adds the kcl partial sums (fixed order) once the others' have landed
   tc_fence_before();
   __syncthreads();
-  cluster_sync();
-  const int nout = ntiles * 128;
-  const int r0 = (int)((int64_t)nout * rank / p.kcl), r1 = (int)((int64_t)nout * (rank + 1) / p.kcl);
-  for (int i = r0 + threadIdx.x; i < r1; i += kThreads) {
-    const int64_t n = t0 * 128 + i;
-    if (n >= p.N) continue;
-    float sum = 0.0f;
-    for (int q = 0; q < p.kcl; ++q) sum += ld_dsmem_f32(ypart + i, (uint32_t)q);
-    p.y[n] = sum;
+  if (warp < kEpiWarp0) cluster_wait();
+  if (rank == 0) {
+    bool ok = true;
+    if (p.kcl > 1) {
+      ok = mbar_wait(&ctl->red_bar, 0);
+      if (!ok && threadIdx.x == 0) atomicOr(&g_gemv_fault, kFaultTimeout);
+    }
+    if (ok && !ctl->abort) {
+      for (int i = threadIdx.x; i < ntiles * 128; i += kThreads) {
+        const int64_t n = t0 * 128 + i;
+        if (n >= p.N) continue;
+        float sum = ypart[i];
+        for (int q = 1; q < p.kcl; ++q) sum += ypart[q * p.tiles_cap * 128 + i];
+        p.y[n] = sum;
+      }
+    }
   }
-  cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
   if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
@@ -533,9 +566,9 @@ EncodeTiledFn encode_fn() {
   return f;
 }
 
-size_t smem_bytes(int groups_cap, int tiles_cap) {
+size_t smem_bytes(int groups_cap, int tiles_cap, int kcl) {
   return 1024 + (size_t)kRing * kSlotBytes + (size_t)groups_cap * kGroupBBytes + kZeroBytes +
-         (size_t)groups_cap * sizeof(float2) + (size_t)tiles_cap * 128 * sizeof(float) + sizeof(Ctl);
+         (size_t)groups_cap * sizeof(float2) + (size_t)kcl * tiles_cap * 128 * sizeof(float) + sizeof(Ctl);
 }
 
 // Clusters of kcl CTAs that can be resident at once (a cluster lives on one
@@ -583,12 +616,16 @@ unsigned int take_fault_gemv() {
 // Work split: kcl in {1, 2, 4, 8} CTAs per cluster share a tile range and
 // split its K groups; at most as many clusters as can be resident at once
 // (one wave).  The choice minimises the stages of the busiest CTA (a stage
-// is four groups of one 128-row tile); ties go to fewer CTAs.
-cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,
-                           int64_t K, const void* x, float* y, cudaStream_t s) {
-  if (N == 0) return cudaSuccess;
+// is four groups of one 128-row tile); ties go to fewer CTAs.  Returns false
+// when this kernel does not suit the shape.
+bool plan_gemv_tc(int64_t N, int64_t K, int* kcl_out, int* clusters_out) {
+  if (N <= 0 || K <= 0 || K % 128 != 0) return false;
   const int64_t G = K / 128, T = (N + 127) / 128;
   const int sms = device_sm_count();
+  if (sms <= 0) return false;
+  // small matrices (under about four stages per SM) are dominated by fixed
+  // latencies, where the 16-row-tile kernel does as well or better
+  if (T * ((G + 3) / 4) < 4 * (int64_t)sms) return false;
   const int64_t smem_max = device_max_smem_optin();
   int64_t best = 0, best_kcl = 0, best_c = 0;
   for (int64_t kcl = 1; kcl <= 8; kcl *= 2) {
@@ -599,7 +636,7 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* sc
     if (c < 1) continue;
     const int64_t gcap = 4 * (((G + kcl - 1) / kcl + 3) / 4);
     const int64_t tcap = (T + c - 1) / c;
-    if ((int64_t)smem_bytes((int)gcap, (int)tcap) > smem_max) continue;
+    if ((int64_t)smem_bytes((int)gcap, (int)tcap, (int)kcl) > smem_max) continue;
     const int64_t cost = tcap * (gcap / 4);
     if (best_kcl == 0 || cost < best || (cost == best && c * kcl < best_c * best_kcl)) {
       best = cost;
@@ -607,10 +644,19 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* sc
       best_c = c;
     }
   }
-  if (best_kcl == 0) return cudaErrorNotSupported;
-  // small matrices (under about four stages per SM) are dominated by fixed
-  // latencies, where the 16-row-tile kernel does as well or better
-  if (T * ((G + 3) / 4) < 4 * (int64_t)sms) return cudaErrorNotSupported;
+  if (best_kcl == 0) return false;
+  *kcl_out = (int)best_kcl;
+  *clusters_out = (int)best_c;
+  return true;
+}
+
+cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,
+                           int64_t K, const void* x, float* y, bool prefetch, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  const int64_t G = K / 128, T = (N + 127) / 128;
+  int kcl_i = 0, c_i = 0;
+  if (!plan_gemv_tc(N, K, &kcl_i, &c_i)) return cudaErrorNotSupported;
+  const int64_t best_kcl = kcl_i, best_c = c_i;
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -633,7 +679,8 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* sc
   p.clusters = (int)best_c;
   p.groups_cap = (int)(4 * (((G + best_kcl - 1) / best_kcl + 3) / 4));
   p.tiles_cap = (int)((T + best_c - 1) / best_c);
-  const size_t smem = smem_bytes(p.groups_cap, p.tiles_cap);
+  p.prefetch = prefetch ? 1 : 0;
+  const size_t smem = smem_bytes(p.groups_cap, p.tiles_cap, p.kcl);
   // raise the kernel's shared-memory limit only when a launch needs more
   static std::atomic<int> smem_set[64];
   int dev = 0;

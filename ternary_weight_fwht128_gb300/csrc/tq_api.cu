@@ -108,9 +108,11 @@ tq_status tq_quantize_pack(const void* W, int wt, int64_t N, int64_t K, int64_t 
                                         ld3, scales, lds, (cudaStream_t)stream));
 }
 
-tq_status tq_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
-                  int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, tq_stream stream) {
+tq_status tq_gemv_ex(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
+                     int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, unsigned int flags,
+                     tq_stream stream) {
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return TQ_ERR_INVALID_ARG;
+  if (flags & ~(unsigned int)TQ_GEMV_WEIGHTS_READY) return TQ_ERR_INVALID_ARG;
   if (N < 0) return TQ_ERR_INVALID_ARG;
   if (!k_ok(K) || M < 1 || M > 16) return TQ_ERR_SHAPE;
   if (N == 0) return TQ_OK;
@@ -119,7 +121,22 @@ tq_status tq_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* sc
   if (!aligned16(codes) || ldc % 16 || !aligned2(scales) || !aligned16(x) || (ldx * 2) % 16 ||
       (reinterpret_cast<uintptr_t>(y) & 3u))
     return TQ_ERR_ALIGN;
-  return from_cuda(launch_gemv(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy, (cudaStream_t)stream));
+  return from_cuda(launch_gemv(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy,
+                               (flags & TQ_GEMV_WEIGHTS_READY) != 0, (cudaStream_t)stream));
+}
+
+tq_status tq_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
+                  int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, tq_stream stream) {
+  return tq_gemv_ex(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy, 0u, stream);
+}
+
+int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt) {
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return -(int)TQ_ERR_INVALID_ARG;
+  if (N < 0) return -(int)TQ_ERR_INVALID_ARG;
+  if (!k_ok(K) || M < 1 || M > 16) return -(int)TQ_ERR_SHAPE;
+  int kcl = 0, clusters = 0;
+  if (M == 1 && fmt == TQ_PACK_2BIT && tq::plan_gemv_tc(N, K, &kcl, &clusters)) return TQ_GEMV_TENSOR_MEMORY;
+  return TQ_GEMV_MMA_SYNC;
 }
 
 size_t tq_gemm_workspace_bytes(int64_t M, int64_t K) {

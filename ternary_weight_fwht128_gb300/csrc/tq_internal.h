@@ -21,14 +21,18 @@ cudaError_t launch_quantize_pack(const void* W, int wt, int64_t N, int64_t K, in
                                  uint8_t* codes2, int64_t ld2, uint8_t* codes3, int64_t ld3, uint16_t* scales,
                                  int64_t lds, cudaStream_t s);
 
+// prefetch: codes and scales may be read before the preceding kernel on the
+// stream has finished (they were complete before it started).
 cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
-                        int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, cudaStream_t s);
+                        int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, bool prefetch,
+                        cudaStream_t s);
 
 // M = 1, 2-bit codes, on tcgen05 fp8 MMAs with the weights in tensor memory;
 // cudaErrorNotSupported when the shape does not suit it (the caller then
 // uses launch_gemv's kernel).
+bool plan_gemv_tc(int64_t N, int64_t K, int* kcl, int* clusters);
 cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,
-                           int64_t K, const void* x, float* y, cudaStream_t s);
+                           int64_t K, const void* x, float* y, bool prefetch, cudaStream_t s);
 
 // Returns cudaErrorNotSupported when the shape needs more shared memory than
 // one CTA can have.

@@ -105,6 +105,26 @@ def test_quantize_validation(L):
     assert call(fmt=tq.TQ_PACK_2BIT, c3=None, N=0) == tq.TQ_OK
 
 
+def test_gemv_ex_validation(L):
+    f = L.tq_gemv_ex
+    args = (A, 64, tq.TQ_PACK_2BIT, B, 2, 8, 256, B + 4096, 256, 1, B + 8192, 8)
+    assert f(*args, 2, None) == tq.TQ_ERR_INVALID_ARG            # unknown flag bit
+    assert f(*args[:5], 0, *args[6:], tq.TQ_GEMV_WEIGHTS_READY, None) == tq.TQ_OK   # N == 0
+    assert f(*args[:9], 0, *args[10:], tq.TQ_GEMV_WEIGHTS_READY, None) == tq.TQ_ERR_SHAPE  # M == 0
+
+
+def test_gemv_path_validation(L):
+    f = L.tq_gemv_path
+    assert f(8, 256, 1, 3) == -tq.TQ_ERR_INVALID_ARG
+    assert f(-1, 256, 1, tq.TQ_PACK_2BIT) == -tq.TQ_ERR_INVALID_ARG
+    assert f(8, 200, 1, tq.TQ_PACK_2BIT) == -tq.TQ_ERR_SHAPE
+    assert f(8, 256, 0, tq.TQ_PACK_2BIT) == -tq.TQ_ERR_SHAPE
+    assert f(8, 256, 17, tq.TQ_PACK_2BIT) == -tq.TQ_ERR_SHAPE
+    # skinny M and base-3 codes always take the mma.sync kernel (no device query needed)
+    assert f(27648, 5120, 2, tq.TQ_PACK_2BIT) == tq.TQ_GEMV_MMA_SYNC
+    assert f(27648, 5120, 1, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
+
+
 def test_gemv_validation(L):
     f = L.tq_gemv
     ok = dict(c=A, ldc=64, fmt=tq.TQ_PACK_2BIT, s=B, lds=2, N=8, K=256, x=B + 4096, ldx=256, M=1, y=B + 8192, ldy=8)

@@ -205,6 +205,62 @@ def test_gemv_tc_shapes(orc, N, K):
     _gemv_case(orc, N, K, 1, seed=N * 7 + K, rows=rows)
 
 
+def test_gemv_path_of_benchmark_shapes():
+    """On a GB300 (152 SMs) the large decode shapes use the tensor-memory
+    kernel and 5120 x 5120 the mma.sync kernel."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the size rule is stated for 152 SMs")
+    assert tq.gemv_path(27648, 5120) == tq.TQ_GEMV_TENSOR_MEMORY
+    assert tq.gemv_path(5120, 27648) == tq.TQ_GEMV_TENSOR_MEMORY
+    assert tq.gemv_path(5120, 5120) == tq.TQ_GEMV_MMA_SYNC
+    assert tq.gemv_path(27648, 5120, 2) == tq.TQ_GEMV_MMA_SYNC
+
+
+@pytest.mark.parametrize("N,K", [(27648, 5120), (512, 1280)])
+def test_gemv_weights_ready_matches(orc, N, K):
+    """TQ_GEMV_WEIGHTS_READY only moves when codes are first read.  The
+    tensor-memory kernel sums in a fixed order, so its result is
+    bit-identical to the plain call; the mma.sync kernel adds partial tiles
+    with shared-memory atomics (order varies), so both calls are checked
+    against the oracle instead."""
+    W = synth.weights(N, K, 21, dtype="bf16")
+    xb = synth.activations(1, K, 22)
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(xb)
+    torch.cuda.synchronize()
+    y0 = tq.gemv(c2, s, x, K)
+    y1 = tq.gemv(c2, s, x, K, weights_ready=True)
+    if tq.gemv_path(N, K) == tq.TQ_GEMV_TENSOR_MEMORY:
+        assert torch.equal(y0, y1)
+    else:
+        rows = np.arange(0, N, max(1, N // 64))
+        T, S = orc.quantize(W, rows)
+        ref = orc.gemv(T, S, synth.bf16_bits_to_f32(xb))
+        check_y(y0.cpu().numpy()[:, rows], ref)
+        check_y(y1.cpu().numpy()[:, rows], ref)
+
+
+def test_gemv_weights_ready_chain(orc):
+    """Back-to-back GEMVs whose x is the previous GEMV's output (converted to
+    bf16 in between): with the flag, each kernel streams its fixed weights
+    while the one before it finishes, and still reads x only afterwards."""
+    K = 5120
+    W1 = synth.weights(27648, K, 31, dtype="bf16")
+    W2 = synth.weights(K, 27648, 32, dtype="bf16")
+    c1, _, s1 = tq.quantize_pack(to_dev_bf16(W1), tq.TQ_PACK_2BIT)
+    c2, _, s2 = tq.quantize_pack(to_dev_bf16(W2), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(synth.activations(1, K, 33))
+    torch.cuda.synchronize()
+    assert tq.gemv_path(27648, K) == tq.gemv_path(K, 27648) == tq.TQ_GEMV_TENSOR_MEMORY
+    outs = []
+    for flag in (False, True):
+        h = tq.gemv(c1, s1, x, K, weights_ready=flag)
+        h16 = (h * 0.05).to(torch.bfloat16)
+        outs.append(tq.gemv(c2, s2, h16, 27648, weights_ready=flag))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_gemv_tc_zero_and_delta_activations(orc):
     N, K = 19456, 2560
     W = synth.weights(N, K, 11, dtype="bf16")
