@@ -77,8 +77,13 @@ constexpr int kRing = 4;                      // code slots in flight (four grou
 constexpr int kAbuf = 3;                      // weight (A) buffers in tensor memory, one stage each
 constexpr int kDbuf = 2;                      // accumulator buffers: buffer t belongs to team t's stages
 constexpr int kSlotBytes = 128 * 128;         // 128 rows x 128 bytes (four groups): one stage
-constexpr int kGroupBBytes = 4 * 256;         // B of one group: 4 MMAs x (8 rows x 32 bytes)
-constexpr int kZeroBytes = 256;               // B rows 8..15 of every MMA
+// B of one MMA: two core matrices (8 rows x 16 bytes: k 0-15 and k 16-31)
+// 144 bytes apart (16 bytes of padding spread the prologue's stores over all
+// banks); rows 8..15 come from a shared zero block.
+constexpr int kBLbo = 144;
+constexpr int kMmaBBytes = 2 * kBLbo;         // 288
+constexpr int kGroupBBytes = 4 * kMmaBBytes;  // B of one group: 4 MMAs
+constexpr int kZeroBytes = kMmaBBytes;        // B rows 8..15 of every MMA
 constexpr int kTmemCols = 512;                // one CTA per SM
 constexpr uint32_t kAcol = 0;                 // A buffer b: columns 128 b .. 128 b + 127 (4 groups x 32)
 constexpr uint32_t kDcol = 128 * kAbuf;       // D buffer b: columns kDcol + 64 b .. + 63 (4 groups x 16)
@@ -208,6 +213,42 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint
                : "memory");
 }
 
+__device__ __forceinline__ uint16_t ldg_nc_u16(const uint16_t* p) {
+  uint16_t r;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+
+// FWHT-128 with lane 4i + j holding elements 16i + j + 4b (b = 0..3): stages
+// h = 1, 2 pair lanes l ^ 1, l ^ 2; h = 4, 8 stay in the lane (b ^ 1, b ^ 2);
+// h = 16, 32, 64 pair lanes l ^ 4, l ^ 8, l ^ 16.  The stages run in the
+// order h = 1, 2, 4, ..., 64 with the lower index keeping a + b, then * c,
+// so the result equals the staged fp32 definition bit for bit.
+__device__ __forceinline__ void fwht128_strided(float v[4], int lane) {
+  auto shfl_stage = [&](int m) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float o = __shfl_xor_sync(kFull, v[b], m);
+      v[b] = __fmaf_rn(sgn, v[b], o);  // lower lane: o + v; upper lane: o - v
+    }
+  };
+  shfl_stage(1);
+  shfl_stage(2);
+  {
+    const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+    v[0] = a0 + a2;
+    v[2] = a0 - a2;
+    v[1] = a1 + a3;
+    v[3] = a1 - a3;
+  }
+  shfl_stage(4);
+  shfl_stage(8);
+  shfl_stage(16);
+#pragma unroll
+  for (int b = 0; b < 4; ++b) v[b] = __fmul_rn(v[b], kInvSqrt128);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
@@ -235,7 +276,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ct
   return false;
 }
 
-// Shared memory (1024-aligned): [code ring][B: groups_cap x 1 KB][zeros 256]
+// Shared memory (1024-aligned): [code ring][B: groups_cap x kGroupBBytes][zeros kZeroBytes]
 // [ztab: groups_cap x {Zt, pw}][partial y: kcl slots x tiles_cap x 128][Ctl]
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__ CUtensorMap cmap, const Params p) {
   extern __shared__ unsigned char smem_raw[];
@@ -317,11 +358,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   pdl_launch_dependents();
   if (!p.prefetch && warp == kTmaWarp && lane == 0) fill_ring();  // while the others rotate x
 
-  // ---- rotate this CTA's slice of x and split it into three e4m3 pieces
+  // ---- rotate this CTA's slice of x and split it into three e4m3 pieces.
+  // Lane 4i + j holds elements k = 16i + j + 4b (b = 0..3) of its group: these
+  // are the four B bytes that meet one code class j of one code word i, so
+  // the lane writes each piece as one 32-bit word.
   for (int gl = warp; gl < ng; gl += kThreads / 32) {
+    const int i8 = lane >> 2, jc = lane & 3;
+    const uint16_t* xg = p.x + (g0 + gl) * 128 + 16 * i8 + jc;
     float v[4];
-    bf16x4_to_f32(ldg_nc_u2(p.x + (g0 + gl) * 128 + 4 * lane), v);
-    fwht128_lane(v, lane);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ldg_nc_u16(xg + 4 * b) << 16);
+    fwht128_strided(v, lane);
     float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
@@ -329,34 +376,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     E = E < -100 ? -100 : (E > 100 ? 100 : E);
     const float up = __uint_as_float((uint32_t)(127 + E) << 23);
     const float pw = __uint_as_float((uint32_t)(127 + 9 - E) << 23);
-    // element jj of this lane is k = 4 lane + jj; odd jj meet the 4c weights
+    // odd classes j meet the 4c weights: their values are stored divided by 4
+    const float cls = (jc & 1) ? 0.25f : 1.0f, acls = (jc & 1) ? 4.0f : 1.0f;
     float u[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) u[j] = v[j] * up * ((j & 1) ? 0.25f : 1.0f);
+    for (int b = 0; b < 4; ++b) u[b] = v[b] * up * cls;
     float zs = 0.0f;
-    uint32_t pk[3][2];
+    // MMA m = i / 2 of the group; k'' = 16 (i % 2) + 4 j + b inside it, at byte
+    // (k'' / 16) * kBLbo + piece * 16 + k'' % 16 of the MMA's B
+    uint32_t* dst = reinterpret_cast<uint32_t*>(bsm + gl * kGroupBBytes + (i8 >> 1) * kMmaBBytes + (i8 & 1) * kBLbo +
+                                                4 * jc);
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
       float r0, r1, r2, r3;
-      pk[q][0] = to_e4m3x2(u[0], u[1], r0, r1);
-      pk[q][1] = to_e4m3x2(u[2], u[3], r2, r3);
-      zs += (r0 + r2) + 4.0f * (r1 + r3);
+      const uint32_t lo = to_e4m3x2(u[0], u[1], r0, r1), hi = to_e4m3x2(u[2], u[3], r2, r3);
+      dst[q * 4] = (lo & 0xffffu) | (hi << 16);
+      zs += (r0 + r1) + (r2 + r3);
       u[0] -= r0;
       u[1] -= r1;
       u[2] -= r2;
       u[3] -= r3;
     }
-    // MMA m = k / 32 of the group; inside it k' = 16 ((k / 16) % 2) + 4 (k % 4) + (k / 4) % 4,
-    // at byte (k' / 16) * 128 + piece * 16 + k' % 16 of the MMA's 256 bytes
-    unsigned char* dst = bsm + gl * kGroupBBytes + (lane >> 3) * 256 + ((lane >> 2) & 1) * 128 + (lane & 3);
-#pragma unroll
-    for (int q = 0; q < 3; ++q) {
-      dst[q * 16 + 0] = (unsigned char)(pk[q][0] & 0xffu);
-      dst[q * 16 + 4] = (unsigned char)((pk[q][0] >> 8) & 0xffu);
-      dst[q * 16 + 8] = (unsigned char)(pk[q][1] & 0xffu);
-      dst[q * 16 + 12] = (unsigned char)((pk[q][1] >> 8) & 0xffu);
-    }
-    zs = warp_sum(zs);
+    zs = warp_sum(zs * acls);
     if (lane == 0) ztab[gl] = make_float2(zs * -0.001953125f, pw);  // -2^-9 sum
   }
   fence_async_smem();  // B written by ordinary stores, read by the tensor cores
@@ -426,10 +467,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     // The whole warp walks the stages (its loop state stays warp-uniform);
     // lane 0 waits; one elected lane issues the MMAs and the commits.
     const uint32_t bsm_u32 = smem_u32(bsm), zero_u32 = smem_u32(zero);
-    // B descriptor of MMA m of local group gl: start = bsm + 1024 gl + 256 m,
-    // sbo = zero - start; consecutive MMAs step start by +256 and sbo by -256
-    const uint64_t desc_g0 = smem_desc_plain(bsm_u32, 128, zero_u32 - bsm_u32);
-    constexpr uint64_t kStepM = (uint64_t)(256 >> 4) - ((uint64_t)(256 >> 4) << 32);
+    // B descriptor of MMA m of local group gl: start = bsm + kGroupBBytes gl +
+    // kMmaBBytes m, sbo = zero - start; consecutive MMAs step start up and sbo
+    // down by kMmaBBytes
+    const uint64_t desc_g0 = smem_desc_plain(bsm_u32, kBLbo, zero_u32 - bsm_u32);
+    constexpr uint64_t kStepM = (uint64_t)(kMmaBBytes >> 4) - ((uint64_t)(kMmaBBytes >> 4) << 32);
+    constexpr uint64_t kStepG = (uint64_t)(kGroupBBytes >> 4) - ((uint64_t)(kGroupBBytes >> 4) << 32);
     // warp kMmaWarp + t takes the stages of parity t (team t), accumulating
     // into D buffer t
     const int t = warp - kMmaWarp;
@@ -446,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       tc_fence_after();
       if (elect_one()) {
         const uint32_t d0 = tmem + kDcol + (uint32_t)(t * 64), a0 = tmem + kAcol + (uint32_t)(ab * 128);
-        uint64_t bd = desc_g0 + (uint64_t)(4 * ch) * ((uint64_t)(1024 >> 4) - ((uint64_t)(1024 >> 4) << 32));
+        uint64_t bd = desc_g0 + (uint64_t)(4 * ch) * kStepG;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
 #pragma unroll
