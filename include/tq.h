@@ -133,10 +133,11 @@ TQ_API tq_status tq_gemv_ex(const uint8_t *codes, int64_t ldc, int fmt, const ui
                             unsigned int flags, tq_stream stream);
 
 /* Which kernel tq_gemv runs for a shape (introspection; launches nothing):
- *   TQ_GEMV_TENSOR_MEMORY  M == 1, 2-bit codes, more than about 4 x (SM
- *                          count) stages of 128 rows x 512 k: weights
- *                          unpacked to fp8 in tensor memory, activations as
- *                          three e4m3 pieces, tcgen05 MMAs;
+ *   TQ_GEMV_TENSOR_MEMORY  M == 1 with 2-bit codes (when one CTA's share of
+ *                          K fits in shared memory: K up to several hundred
+ *                          thousand): weights unpacked to fp8 in tensor
+ *                          memory, activations as three e4m3 pieces,
+ *                          tcgen05 MMAs;
  *   TQ_GEMV_MMA_SYNC       everything else: fp16 x' in shared memory, weights
  *                          as fp16 on mma.sync (16-row tiles).
  * Queries device properties of the current device on first use.  Returns

@@ -666,9 +666,6 @@ bool plan_gemv_tc(int64_t N, int64_t K, int* kcl_out, int* clusters_out) {
   const int64_t G = K / 128, T = (N + 127) / 128;
   const int sms = device_sm_count();
   if (sms <= 0) return false;
-  // small matrices (under about four stages per SM) are dominated by fixed
-  // latencies, where the 16-row-tile kernel does as well or better
-  if (T * ((G + 3) / 4) < 4 * (int64_t)sms) return false;
   const int64_t smem_max = device_max_smem_optin();
   int64_t best = 0, best_kcl = 0, best_c = 0;
   for (int64_t kcl = 1; kcl <= 8; kcl *= 2) {

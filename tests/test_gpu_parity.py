@@ -206,31 +206,29 @@ def test_gemv_tc_shapes(orc, N, K):
 
 
 def test_gemv_path_of_benchmark_shapes():
-    """On a GB300 (152 SMs) the large decode shapes use the tensor-memory
-    kernel and 5120 x 5120 the mma.sync kernel."""
-    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
-        pytest.skip("the size rule is stated for 152 SMs")
-    assert tq.gemv_path(27648, 5120) == tq.TQ_GEMV_TENSOR_MEMORY
-    assert tq.gemv_path(5120, 27648) == tq.TQ_GEMV_TENSOR_MEMORY
-    assert tq.gemv_path(5120, 5120) == tq.TQ_GEMV_MMA_SYNC
+    """M = 1 with 2-bit codes uses the tensor-memory kernel; skinny M and
+    base-3 codes the mma.sync kernel."""
+    for N, K in [(27648, 5120), (5120, 27648), (5120, 5120), (1, 128)]:
+        assert tq.gemv_path(N, K) == tq.TQ_GEMV_TENSOR_MEMORY
     assert tq.gemv_path(27648, 5120, 2) == tq.TQ_GEMV_MMA_SYNC
+    assert tq.gemv_path(27648, 5120, 1, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
 
 
-@pytest.mark.parametrize("N,K", [(27648, 5120), (512, 1280)])
-def test_gemv_weights_ready_matches(orc, N, K):
+@pytest.mark.parametrize("N,K,M", [(27648, 5120, 1), (512, 1280, 1), (512, 1280, 4)])
+def test_gemv_weights_ready_matches(orc, N, K, M):
     """TQ_GEMV_WEIGHTS_READY only moves when codes are first read.  The
     tensor-memory kernel sums in a fixed order, so its result is
     bit-identical to the plain call; the mma.sync kernel adds partial tiles
     with shared-memory atomics (order varies), so both calls are checked
     against the oracle instead."""
     W = synth.weights(N, K, 21, dtype="bf16")
-    xb = synth.activations(1, K, 22)
+    xb = synth.activations(M, K, 22)
     c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
     x = to_dev_bf16(xb)
     torch.cuda.synchronize()
     y0 = tq.gemv(c2, s, x, K)
     y1 = tq.gemv(c2, s, x, K, weights_ready=True)
-    if tq.gemv_path(N, K) == tq.TQ_GEMV_TENSOR_MEMORY:
+    if tq.gemv_path(N, K, M) == tq.TQ_GEMV_TENSOR_MEMORY:
         assert torch.equal(y0, y1)
     else:
         rows = np.arange(0, N, max(1, N // 64))
