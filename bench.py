@@ -448,7 +448,10 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
 
                 ms = time_events(run, 3 * len(mats), torch)
                 gb = packed_bytes(N, K, fmt_name) / (ms * 1e-3) / 1e9
-                skinny.append({"shape": f"{N}x{K}", "M": M, "fmt": fmt_name, "us": round(ms * 1e3, 2),
+                path = tq.gemv_path(N, K, M, fmt)
+                skinny.append({"shape": f"{N}x{K}", "M": M, "fmt": fmt_name,
+                               "kernel": "k_gemv_tc" if path == tq.TQ_GEMV_TENSOR_MEMORY else "k_gemv (mma.sync)",
+                               "us": round(ms * 1e3, 2),
                                "GB/s": round(gb, 1), "frac_of_peak": round(gb / pk["hbm_gbs"], 4),
                                "TFLOP/s": round(2 * M * N * K / (ms * 1e-3) / 1e12, 2)})
     out["skinny"] = skinny

@@ -1,7 +1,7 @@
-// k_gemv_tc.cu -- decode GEMV (tq_gemv, M = 1, 2-bit codes) on tcgen05 tensor
-// cores with the weight operand in tensor memory.
+// k_gemv_tc.cu -- decode GEMV / skinny GEMM (tq_gemv, 2-bit codes, M = 1..16)
+// on tcgen05 tensor cores with the weight operand in tensor memory.
 //
-//   y[n] = sum_g s[n][g] * sum_{k in g} t[n][k] * x'[k],  x' = FWHT-128(x)
+//   y[m][n] = sum_g s[n][g] * sum_{k in g} t[n][k] * x'[m][k],  x' = FWHT-128(x)
 //
 // Decode streams every packed weight once and should run at the HBM rate
 // (mhpq.cn/news/1159370 sec. 4.2).  On this GPU the limit of a GEMV over
@@ -18,42 +18,47 @@
 // * Weights in tensor memory.  Lane r of tensor memory holds weight row r of
 //   a 128-row tile; each thread unpacks its own row into 32 columns per group
 //   (tcgen05.st), and the MMA reads A from there, so the unpacked bytes never
-//   pass through shared memory (whose bandwidth would not cover them).
-// * Activations as three e4m3 pieces (the B operand, N = 16 columns, three
-//   used).  Per group of 128 the rotated activations are scaled by a power
-//   of two 2^E with max |x' 2^E| in [128, 256), and each scaled value v is
-//   written as p1 + p2 + p3, p1 = e4m3(v), p2 = e4m3(v - p1),
+//   pass through shared memory (whose bandwidth would not cover them).  The
+//   weights are unpacked once whatever M is.
+// * Activations as three e4m3 pieces (the B operand, N = 16 columns).  Per
+//   group of 128 and row m of x the rotated activations are scaled by a
+//   power of two 2^E with max |x' 2^E| in [128, 256), and each scaled value
+//   v is written as p1 + p2 + p3, p1 = e4m3(v), p2 = e4m3(v - p1),
 //   p3 = e4m3(v - p1 - p2) (nearest even; the residuals are exact in fp32):
 //   within max(2^-12 |v|, 2^-8) of v, finer than an fp16 rounding of x' for
 //   all but the smallest elements.  Values that meet the 4c weights are
-//   stored divided by 4 (exact).
-// * Groups.  Each group's four MMAs (K = 32 each) write their own 16-column
-//   accumulator, so C[row][p] = 2^-9 sum_k c_k a_k piece_p(k) for one group;
-//   the thread of that row adds the pieces and the correction term
-//   -2^-9 sum_k a_k (p1 + p2 + p3)(k), and multiplies by s[row][g] 2^(9 - E)
-//   in fp32 -- the scale is applied to each group's inner product.
+//   stored divided by 4 (exact).  The 3M pieces go to the 16 B columns in
+//   kP passes per 32-wide K step, each pass one MMA accumulating into the
+//   same 16 accumulator columns: M <= 5 (one pass, column 3m + piece),
+//   M <= 8 (two passes; columns m and 8 + m), M <= 16 (three passes, one
+//   piece each, column m).  For M <= 2 only B rows 0..7 are stored; rows
+//   8..15 come from a shared zero block.
+// * Groups.  Each group's MMAs write their own 16 accumulator columns, so
+//   the thread of row n reads one group's inner products with x'[m] (after
+//   adding the columns that share an m), adds the correction term
+//   -2^-9 sum_k (p1 + p2 + p3)(k) and multiplies by s[n][g] 2^(9 - E) in fp32
+//   -- the scale is applied to each group's inner product.
 //
 // Work split: a cluster of kcl CTAs owns a range of 128-row tiles; CTA rank r
 // owns the r-th slice of the K groups and rotates only that slice of x.  A
-// CTA walks (tile, two-group) decode stages with four warp roles that hand
-// buffers to one another through mbarriers, so each runs ahead on its own:
+// CTA walks (tile, four-group) stages with four warp roles that hand buffers
+// to one another through mbarriers, so each runs ahead on its own:
 //   warp 16      (one lane) TMA-loads 128 x 128-byte code tiles (four groups,
-//                128-byte swizzle) into a ring of kRing slots; each slot feeds
-//                two decode stages of two groups;
-//   warps 0-15   two teams of eight take the even and the odd decode stages
-//                (the two halves of each slot); warp w unpacks group
-//                (w / 4) % 2 of its stage for rows 32 (w % 4) .. +31 into one
-//                of kAbuf A buffers in tensor memory;
+//                128-byte swizzle) into a ring of kRing slots, one per stage;
+//   warps 0-15   two teams of eight take the even and the odd stages; warp w
+//                unpacks groups 2 ((w / 4) % 2) .. +1 of its stage for rows
+//                32 (w % 4) .. +31 into one of kAbuf A buffers in tensor
+//                memory;
 //   warps 17-18  warp 17 allocates tensor memory; warp 17 + t issues the
-//                sixteen MMAs of each stage of team t into accumulator
-//                buffer t;
+//                MMAs of each stage of team t into accumulator buffer t;
 //   warps 19-22  read the accumulators of their 32 rows and apply the scales.
-// Ranks 1 .. kcl-1 push each finished row sum into rank 0's shared memory
-// (st.async, counted on an mbarrier there) and exit; rank 0 adds the kcl
-// partial sums in a fixed order and writes y.  Every wait is bounded in time;
-// a wait that runs out sets the library's GEMV status word and the CTA winds
-// down (pending copies and MMAs are waited for, tensor memory is freed, the
-// cluster barrier is still met).
+// The partial sums of the K slices are reduced across the cluster by rows:
+// rank q owns rows 128 q / kcl .. of every tile, the others push their
+// partial sums of those rows into its shared memory (st.async, counted on an
+// mbarrier there), and rank q adds the kcl partials in rank order and writes
+// y.  Every wait is bounded in time; a wait that runs out sets the library's
+// GEMV status word and the CTA winds down (pending copies and MMAs are
+// waited for, tensor memory is freed, the cluster barrier is still met).
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -75,15 +80,11 @@ constexpr int kEpiWarp0 = 19;                 // warps 19-22: epilogue
 constexpr int kThreads = 32 * 23;             // + 4 epilogue warps (19-22)
 constexpr int kRing = 4;                      // code slots in flight (four groups each)
 constexpr int kAbuf = 3;                      // weight (A) buffers in tensor memory, one stage each
+constexpr int kAPeriod = 2 * kAbuf;           // stages between two uses of one A buffer by one team
+static_assert(kAbuf % 2 == 1, "A buffers alternate between the two teams");
 constexpr int kDbuf = 2;                      // accumulator buffers: buffer t belongs to team t's stages
 constexpr int kSlotBytes = 128 * 128;         // 128 rows x 128 bytes (four groups): one stage
-// B of one MMA: two core matrices (8 rows x 16 bytes: k 0-15 and k 16-31)
-// 144 bytes apart (16 bytes of padding spread the prologue's stores over all
-// banks); rows 8..15 come from a shared zero block.
-constexpr int kBLbo = 144;
-constexpr int kMmaBBytes = 2 * kBLbo;         // 288
-constexpr int kGroupBBytes = 4 * kMmaBBytes;  // B of one group: 4 MMAs
-constexpr int kZeroBytes = kMmaBBytes;        // B rows 8..15 of every MMA
+constexpr int kZeroBytes = 288;               // B rows 8..15 of the 8-row layout (two core matrices 144 apart)
 constexpr int kTmemCols = 512;                // one CTA per SM
 constexpr uint32_t kAcol = 0;                 // A buffer b: columns 128 b .. 128 b + 127 (4 groups x 32)
 constexpr uint32_t kDcol = 128 * kAbuf;       // D buffer b: columns kDcol + 64 b .. + 63 (4 groups x 16)
@@ -93,14 +94,67 @@ constexpr uint32_t kFaultTimeout = 2u;
 // kind::f8f6f4: fp32 accumulator, A = B = e4m3, both K-major, N = 16, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 
+// B layouts by how many rows of x they hold (kMM): kP MMA passes per 32-wide
+// K step, kRows B rows stored per pass (8: rows 8..15 are read from the zero
+// block).  One pass of one K step (a "unit") holds kRows / 8 core matrices
+// (8 rows x 16 bytes) for k 0..15 and the same for k 16..31 at kLbo; the 16
+// bytes of padding after each make the prologue's stores conflict-free
+// (kLbo / 4 = 4 and kUnit / 4 = 8 banks, mod 32).  A group's units are
+// stored pass-major: unit (pass, K step i) at (4 pass + i) kUnit.
+template <int V> struct Lay;
+template <> struct Lay<1> { static constexpr int kP = 1, kRows = 8, kMM = 2; };
+template <> struct Lay<2> { static constexpr int kP = 1, kRows = 16, kMM = 5; };
+template <> struct Lay<3> { static constexpr int kP = 2, kRows = 16, kMM = 8; };
+template <> struct Lay<4> { static constexpr int kP = 3, kRows = 16, kMM = 16; };
+
+template <int V>
+struct Geo {
+  static constexpr int kP = Lay<V>::kP, kRows = Lay<V>::kRows, kMM = Lay<V>::kMM;
+  static constexpr int kLbo = 16 * kRows + 16;
+  static constexpr int kUnit = 2 * kLbo;
+  static constexpr int kGroupB = 4 * kP * kUnit;
+  static constexpr int kZs = (kMM + 1) & ~1;       // ztab entries per group (even: read in pairs)
+  static constexpr int kCw = kRows == 8 ? 8 : 16;  // accumulator columns read per group
+  static constexpr int kGw = kMM > 5 ? 1 : 2;      // groups read per tensor-memory wait
+  static constexpr int kScAhead = kMM > 5 ? 3 : 4; // stages the epilogue loads scales ahead
+  static_assert(kLbo % 128 == 16 && kUnit % 128 == 32, "bank-spreading padding");
+  static_assert(3 * kMM <= kP * (kRows == 8 ? 8 : 16), "pieces fit the B columns");
+};
+
+// B column (pass, row) that carries piece q (0..2) of row m of x.  The
+// epilogue adds the accumulator columns of one m: 3m .. 3m + 2 (one pass),
+// m and 8 + m (two passes), m (three passes).
+template <int V>
+__device__ __forceinline__ void piece_slot(int m, int q, int& pass, int& row) {
+  if constexpr (Lay<V>::kP == 1) {
+    pass = 0;
+    row = 3 * m + q;
+  } else if constexpr (Lay<V>::kP == 2) {
+    pass = q >> 1;
+    row = q == 1 ? 8 + m : m;
+  } else {
+    pass = q;
+    row = m;
+  }
+}
+
+int variant_of(int64_t M) { return M <= 2 ? 1 : M <= 5 ? 2 : M <= 8 ? 3 : 4; }
+
+// A buffer b holds the stages s with s % kAbuf == b, so its stages alternate
+// between the teams (and MMA warps).  Its barriers are kept per team, which
+// gives every barrier one sequential producer and one sequential consumer and
+// so keeps each waiter within one phase of the barrier (a parity wait cannot
+// pass on an older phase):
+//   a_full[b][t]  team t's decode of a stage in b -> MMA warp t (every 6th stage);
+//   a_free[b][t]  MMA warp 1 - t's reads of b done -> team t, which writes b next.
 struct Ctl {
-  uint64_t full[kRing];   // TMA -> decoders
-  uint64_t empty[kRing];  // decoders -> TMA
-  uint64_t a_full[kAbuf]; // decoders -> MMA
-  uint64_t a_free[kAbuf]; // MMA -> decoders
+  uint64_t full[kRing];      // TMA -> decoders (slot s % kRing: always team s % 2)
+  uint64_t empty[kRing];     // decoders -> TMA
+  uint64_t a_full[kAbuf][2]; // decoders -> MMA
+  uint64_t a_free[kAbuf][2]; // MMA -> decoders
   uint64_t d_full[kDbuf]; // MMA -> epilogue
   uint64_t d_free[kDbuf]; // epilogue -> MMA
-  uint64_t red_bar;       // rank 0: the other ranks' partial outputs have landed
+  uint64_t red_bar;       // this rank's rows: the other ranks' partial sums have landed
   uint32_t tmem_base;
   int abort;
 };
@@ -109,15 +163,17 @@ struct Params {
   const uint16_t* scales;
   int64_t lds;
   int64_t N, K;
-  const uint16_t* x;  // bf16
-  float* y;
+  const uint16_t* x;  // bf16, M rows of ldx
+  int64_t ldx;
+  float* y;           // M rows of ldy
+  int64_t ldy;
+  int M;
   int kcl;         // CTAs per cluster (K split)
   int clusters;    // tile ranges: cluster c owns [c*T/clusters, (c+1)*T/clusters)
   int groups_cap;  // groups per CTA the shared layout holds (multiple of 4)
-  int tiles_cap;   // tiles per cluster the partial outputs hold
+  int tiles_cap;   // tiles per cluster the partial sums hold
   int prefetch;    // codes and scales are ready before the preceding kernel ends
 };
-
 // ---------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -169,16 +225,31 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t r[32]) 
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float v[4]) {
-  uint32_t r0, r1, r2, r3;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+// tcgen05.ld of 8 / 16 consecutive columns of this warp's 32 lanes; the
+// registers are valid after tmem_ld_wait on them.
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// Waits for this thread's tensor-memory loads; the registers pass through an
+// empty asm after the wait so that no use of them is scheduled before it.
+template <int G, int N>
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&a)[G][N]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-  v[0] = __uint_as_float(r0);
-  v[1] = __uint_as_float(r1);
-  v[2] = __uint_as_float(r2);
-  v[3] = __uint_as_float(r3);
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(a[g][i]));
 }
 
 __device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
@@ -276,29 +347,33 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ct
   return false;
 }
 
-// Shared memory (1024-aligned): [code ring][B: groups_cap x kGroupBBytes][zeros kZeroBytes]
-// [ztab: groups_cap x {Zt, pw}][partial y: kcl slots x tiles_cap x 128][Ctl]
+// Shared memory (1024-aligned): [code ring][B: groups_cap x kGroupB][zeros kZeroBytes]
+// [ztab: groups_cap x kZs x {pw Zt, pw}][partial sums: tiles_cap x kcl x M x 128 / kcl][Ctl]
+template <int V>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__ CUtensorMap cmap, const Params p) {
+  using Gm = Geo<V>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* ring = smem;
   unsigned char* bsm = ring + kRing * kSlotBytes;
-  unsigned char* zero = bsm + p.groups_cap * kGroupBBytes;
+  unsigned char* zero = bsm + p.groups_cap * Gm::kGroupB;
   float2* ztab = reinterpret_cast<float2*>(zero + kZeroBytes);
-  float* ypart = reinterpret_cast<float*>(ztab + p.groups_cap);
-  Ctl* ctl = reinterpret_cast<Ctl*>(ypart + p.kcl * p.tiles_cap * 128);
+  float* ypart = reinterpret_cast<float*>(ztab + p.groups_cap * Gm::kZs);
+  Ctl* ctl = reinterpret_cast<Ctl*>(ypart + p.tiles_cap * 128 * p.M);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const int64_t cluster = blockIdx.x / p.kcl;
   const int64_t G = p.K / 128;
   const int64_t g0 = G * rank / p.kcl, g1 = G * (rank + 1) / p.kcl;
-  const int ng = (int)(g1 - g0), nch = (ng + 3) >> 2, nlc = nch;  // four-group stages per tile
+  const int ng = (int)(g1 - g0), nch = (ng + 3) >> 2;  // four-group stages per tile
   const int64_t T = (p.N + 127) / 128;
   const int64_t t0 = T * cluster / p.clusters;
   const int ntiles = (int)(T * (cluster + 1) / p.clusters - t0);
   const int S = ntiles * nch;  // stages (ring loads) of this CTA
-  const int L = S;
+  const int M = p.M;
+  // rank q reduces rows R q .. R q + R - 1 of every tile
+  const int lgR = 7 - (31 - __clz(p.kcl)), R = 1 << lgR;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
@@ -306,16 +381,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       mbar_init(&ctl->empty[i], kTeamWarps);
     }
     for (int i = 0; i < kAbuf; ++i) {
-      mbar_init(&ctl->a_full[i], kTeamWarps);
-      mbar_init(&ctl->a_free[i], 1);
+      for (int t = 0; t < 2; ++t) {
+        mbar_init(&ctl->a_full[i][t], kTeamWarps);
+        mbar_init(&ctl->a_free[i][t], 1);
+      }
     }
     for (int i = 0; i < kDbuf; ++i) {
       mbar_init(&ctl->d_full[i], 1);
       mbar_init(&ctl->d_free[i], 4);
     }
     mbar_init(&ctl->red_bar, 1);
-    // rank 0 receives every other rank's partial outputs: ntiles x 128 floats each
-    if (rank == 0 && p.kcl > 1) mbar_arrive_expect_tx(&ctl->red_bar, (uint32_t)((p.kcl - 1) * ntiles * 128 * 4));
+    // every other rank sends its partial sums of this rank's rows: ntiles x M x R floats each
+    if (p.kcl > 1) mbar_arrive_expect_tx(&ctl->red_bar, (uint32_t)((p.kcl - 1) * ntiles * M * R * 4));
     ctl->abort = 0;
     fence_mbar_init();
   }
@@ -325,18 +402,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // zero B (unused rows and groups), the zero block, ztab and the partial outputs
+  // zero B (unused rows and groups), the zero block and ztab
   {
     uint4* z4 = reinterpret_cast<uint4*>(bsm);
-    const int n16 = (p.groups_cap * kGroupBBytes + kZeroBytes) / 16;
+    const int n16 = (p.groups_cap * Gm::kGroupB + kZeroBytes) / 16;
     for (int i = threadIdx.x; i < n16; i += kThreads) z4[i] = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < p.groups_cap; i += kThreads) ztab[i] = make_float2(0.0f, 0.0f);
+    for (int i = threadIdx.x; i < p.groups_cap * Gm::kZs; i += kThreads) ztab[i] = make_float2(0.0f, 0.0f);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  // Rank 0's reduction barrier is armed: the other ranks may push once they
+  // This CTA's reduction barrier is armed: the other ranks may push once they
   // pass the matching wait (epilogue warps before their first push, every
   // other warp before it exits -- each thread waits exactly once).
   cluster_arrive();
@@ -346,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   // which case the ring fills while that kernel finishes.
   int issued_loads = 0;
   auto fill_ring = [&]() {
-    for (; issued_loads < L && issued_loads < kRing; ++issued_loads) {
-      const int l = issued_loads, tile = l / nlc, lc = l - tile * nlc;
+    for (; issued_loads < S && issued_loads < kRing; ++issued_loads) {
+      const int l = issued_loads, tile = l / nch, lc = l - tile * nch;
       mbar_arrive_expect_tx(&ctl->full[l], kSlotBytes);
       tma_load_2d(smem_u32(ring + l * kSlotBytes), &cmap, (int)((g0 + 4 * lc) * 32), (int)((t0 + tile) * 128),
                   &ctl->full[l]);
@@ -358,13 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   pdl_launch_dependents();
   if (!p.prefetch && warp == kTmaWarp && lane == 0) fill_ring();  // while the others rotate x
 
-  // ---- rotate this CTA's slice of x and split it into three e4m3 pieces.
-  // Lane 4i + j holds elements k = 16i + j + 4b (b = 0..3) of its group: these
-  // are the four B bytes that meet one code class j of one code word i, so
-  // the lane writes each piece as one 32-bit word.
-  for (int gl = warp; gl < ng; gl += kThreads / 32) {
+  // ---- rotate this CTA's slice of each row of x and split it into three
+  // e4m3 pieces.  Lane 4i + j holds elements k = 16i + j + 4b (b = 0..3) of
+  // its group: these are the four B bytes that meet one code class j of one
+  // code word i, so the lane writes each piece as one 32-bit word.
+  for (int it = warp; it < ng * M; it += kThreads / 32) {
+    const int gl = it / M, m = it - gl * M;
     const int i8 = lane >> 2, jc = lane & 3;
-    const uint16_t* xg = p.x + (g0 + gl) * 128 + 16 * i8 + jc;
+    const uint16_t* xg = p.x + m * p.ldx + (g0 + gl) * 128 + 16 * i8 + jc;
     float v[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ldg_nc_u16(xg + 4 * b) << 16);
@@ -382,15 +460,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
 #pragma unroll
     for (int b = 0; b < 4; ++b) u[b] = v[b] * up * cls;
     float zs = 0.0f;
-    // MMA m = i / 2 of the group; k'' = 16 (i % 2) + 4 j + b inside it, at byte
-    // (k'' / 16) * kBLbo + piece * 16 + k'' % 16 of the MMA's B
-    uint32_t* dst = reinterpret_cast<uint32_t*>(bsm + gl * kGroupBBytes + (i8 >> 1) * kMmaBBytes + (i8 & 1) * kBLbo +
-                                                4 * jc);
+    // K step i / 2 of the group; k'' = 16 (i % 2) + 4 j + b inside it, at byte
+    // (k'' / 16) kLbo + 16 row + k'' % 16 of the unit of the piece's pass
+    unsigned char* gdst = bsm + gl * Gm::kGroupB + (i8 >> 1) * Gm::kUnit + (i8 & 1) * Gm::kLbo + 4 * jc;
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
       float r0, r1, r2, r3;
       const uint32_t lo = to_e4m3x2(u[0], u[1], r0, r1), hi = to_e4m3x2(u[2], u[3], r2, r3);
-      dst[q * 4] = (lo & 0xffffu) | (hi << 16);
+      int pass, row;
+      piece_slot<V>(m, q, pass, row);
+      *reinterpret_cast<uint32_t*>(gdst + pass * 4 * Gm::kUnit + (row >> 3) * 128 + (row & 7) * 16) =
+          (lo & 0xffffu) | (hi << 16);
       zs += (r0 + r1) + (r2 + r3);
       u[0] -= r0;
       u[1] -= r1;
@@ -398,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       u[3] -= r3;
     }
     zs = warp_sum(zs * acls);
-    if (lane == 0) ztab[gl] = make_float2(zs * -0.001953125f, pw);  // -2^-9 sum
+    if (lane == 0) ztab[gl * Gm::kZs + m] = make_float2(pw * (zs * -0.001953125f), pw);  // pw * (-2^-9 sum), pw
   }
   fence_async_smem();  // B written by ordinary stores, read by the tensor cores
   __syncthreads();
@@ -406,14 +486,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int l = issued_loads, slot = l % kRing, use = l / kRing, tile = l / (nlc > 0 ? nlc : 1), lc = l - tile * nlc;
-      for (; l < L; ++l) {
+      int l = issued_loads, slot = l % kRing, use = l / kRing, tile = l / (nch > 0 ? nch : 1), lc = l - tile * nch;
+      for (; l < S; ++l) {
         if (!wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(&ctl->full[slot], kSlotBytes);
         tma_load_2d(smem_u32(ring + slot * kSlotBytes), &cmap, (int)((g0 + 4 * lc) * 32), (int)((t0 + tile) * 128),
                     &ctl->full[slot]);
         if (++slot == kRing) { slot = 0; ++use; }
-        if (++lc == nlc) { lc = 0; ++tile; }
+        if (++lc == nch) { lc = 0; ++tile; }
       }
       // loads issued but possibly never consumed: let them land before exit
       for (int q = (l > kRing ? l - kRing : 0); q < l; ++q) (void)mbar_wait(&ctl->full[q % kRing], (q / kRing) & 1);
@@ -433,14 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
 #pragma unroll
     for (int q = 0; q < 4; ++q) off[q] = rbase + ((((uint32_t)(4 * gh + q)) ^ rx) << 4);
     for (int s = team; s < S; s += 2) {
-      const int slot = s % kRing, use = s / kRing, ab = s % kAbuf, ause = s / kAbuf;
+      // A buffer ab last held stage s - kAbuf (the other team's), whose MMAs
+      // are the ((s - kAbuf) / kAPeriod)-th completion a_free[ab][team] counts
+      const int slot = s % kRing, use = s / kRing, ab = s % kAbuf;
       bool ok = wait_or_abort(&ctl->full[slot], use & 1, ctl);
       uint4 c[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) c[q] = ok ? lds_u4(ring_u32 + slot * kSlotBytes + off[q]) : make_uint4(0, 0, 0, 0);
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->empty[slot]);
-      if (ause > 0) ok = wait_or_abort(&ctl->a_free[ab], (ause - 1) & 1, ctl) && ok;
+      if (s >= kAbuf) ok = wait_or_abort(&ctl->a_free[ab][team], ((s - kAbuf) / kAPeriod) & 1, ctl) && ok;
       if (!__all_sync(kFull, ok)) break;  // the tensor-memory stores below are warp-collective
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -460,45 +542,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->a_full[ab]);
+      if (lane == 0) mbar_arrive(&ctl->a_full[ab][team]);
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------ MMA issue
     // The whole warp walks the stages (its loop state stays warp-uniform);
     // lane 0 waits; one elected lane issues the MMAs and the commits.
     const uint32_t bsm_u32 = smem_u32(bsm), zero_u32 = smem_u32(zero);
-    // B descriptor of MMA m of local group gl: start = bsm + kGroupBBytes gl +
-    // kMmaBBytes m, sbo = zero - start; consecutive MMAs step start up and sbo
-    // down by kMmaBBytes
-    const uint64_t desc_g0 = smem_desc_plain(bsm_u32, kBLbo, zero_u32 - bsm_u32);
-    constexpr uint64_t kStepM = (uint64_t)(kMmaBBytes >> 4) - ((uint64_t)(kMmaBBytes >> 4) << 32);
-    constexpr uint64_t kStepG = (uint64_t)(kGroupBBytes >> 4) - ((uint64_t)(kGroupBBytes >> 4) << 32);
+    // B descriptor of unit (pass, K step i) of local group gl: start = bsm +
+    // kGroupB gl + kUnit (4 pass + i).  In the 8-row layout the stride to the
+    // next 8 rows points at the zero block, so moving the start up by d moves
+    // that stride down by d; in the 16-row layout it is 128.
+    constexpr bool k8 = Gm::kRows == 8;
+    const uint64_t desc_g0 = smem_desc_plain(bsm_u32, Gm::kLbo, k8 ? zero_u32 - bsm_u32 : 128u);
+    constexpr uint64_t kStepU = (uint64_t)(Gm::kUnit >> 4) - (k8 ? ((uint64_t)(Gm::kUnit >> 4) << 32) : 0);
+    constexpr uint64_t kStepG = (uint64_t)(Gm::kGroupB >> 4) - (k8 ? ((uint64_t)(Gm::kGroupB >> 4) << 32) : 0);
     // warp kMmaWarp + t takes the stages of parity t (team t), accumulating
     // into D buffer t
     const int t = warp - kMmaWarp;
     int s = t, ch = t % (nch > 0 ? nch : 1), duse = 0;  // ch: stage inside the tile
     for (; s < S; s += 2) {
-      const int ab = s % kAbuf, ause = s / kAbuf;
+      // stage s is the (s / kAPeriod)-th that a_full[ab][t] counts
+      const int ab = s % kAbuf;
       // only lane 0 waits; one elected lane issues the tensor-core work
       bool ok = true;
       if (lane == 0) {
-        ok = wait_or_abort(&ctl->a_full[ab], ause & 1, ctl);
+        ok = wait_or_abort(&ctl->a_full[ab][t], (s / kAPeriod) & 1, ctl);
         if (ok && duse > 0) ok = wait_or_abort(&ctl->d_free[t], (duse - 1) & 1, ctl);
       }
       if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
       tc_fence_after();
       if (elect_one()) {
         const uint32_t d0 = tmem + kDcol + (uint32_t)(t * 64), a0 = tmem + kAcol + (uint32_t)(ab * 128);
-        uint64_t bd = desc_g0 + (uint64_t)(4 * ch) * kStepG;
+        uint64_t bg = desc_g0 + (uint64_t)(4 * ch) * kStepG;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            mma_f8_tmem_a(d0 + h * 16, a0 + h * 32 + m * 8, bd, m > 0 ? 1u : 0u);
-            bd += kStepM;
+          for (int pass = 0; pass < Gm::kP; ++pass) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              mma_f8_tmem_a(d0 + h * 16, a0 + h * 32 + i * 8, bg + (uint64_t)(4 * pass + i) * kStepU,
+                            (pass | i) != 0 ? 1u : 0u);
           }
+          bg += kStepG;
         }
-        mma_commit(&ctl->a_free[ab]);
+        mma_commit(&ctl->a_free[ab][t ^ 1]);  // team 1 - t writes buffer ab next (stage s + 3)
         mma_commit(&ctl->d_full[t]);
       }
       __syncwarp();
@@ -510,79 +598,144 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     if (s - 2 >= 0 && lane == 0) (void)mbar_wait(&ctl->d_full[t], ((s - 2) >> 1) & 1);
   } else {
     // ------------------------------------------------------------ epilogue
+    constexpr int kMM = Gm::kMM, kCw = Gm::kCw;
     const int quad = warp & 3;  // warps 19..22 reach tensor-memory lanes 32 (warp % 4) ..
     const int r = quad * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    float acc = 0.0f;
+    float acc[kMM];
+#pragma unroll
+    for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
     int tile = 0, ch = 0, db = 0, duse = 0;
-    // scales of the stage's four groups for this row (groups past the slice: 0)
-    auto ld_scales = [&](int tl, int c, uint32_t sc[2]) {
-      sc[0] = sc[1] = 0u;
+    // Raw fp16 scales of the stage's four groups for this row (groups past
+    // the slice: 0).  Each stays in its own register until it is used, so
+    // the loads remain in flight meanwhile.
+    auto ld_scales = [&](int tl, int c, uint32_t (&sc)[4]) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) sc[h] = 0u;
       const int64_t n = (t0 + tl) * 128 + r;
       if (tl >= ntiles || n >= p.N) return;
       const uint16_t* q = p.scales + n * p.lds + g0 + 4 * c;
 #pragma unroll
       for (int h = 0; h < 4; ++h)
-        if (4 * c + h < ng) sc[h >> 1] |= (uint32_t)__ldg(q + h) << (16 * (h & 1));
+        if (4 * c + h < ng) sc[h] = __ldg(q + h);
     };
-    uint32_t sc[2];
-    ld_scales(0, 0, sc);
+    // The scales are loaded kAhead stages before they are used (a DRAM miss
+    // takes longer than a stage).  The stage loop is unrolled by kAhead so
+    // that slot j of the ring is always the same registers: a slot is read
+    // (converted) at the start of its stage, then reloaded for the stage
+    // kAhead later; (ltl, lc) is the next stage to load.
+    constexpr int kAhead = Gm::kScAhead;
+    uint32_t scq[kAhead][4];
+    int ltl = 0, lc = 0;
+#pragma unroll
+    for (int i = 0; i < kAhead; ++i) {
+      ld_scales(ltl, lc, scq[i]);
+      if (++lc == nch) { lc = 0; ++ltl; }
+    }
     cluster_wait();
-    const uint32_t push_base = rank == 0 ? 0u : map_rank(ypart + rank * p.tiles_cap * 128 + r, 0);
-    const uint32_t push_bar = rank == 0 ? 0u : map_rank(&ctl->red_bar, 0);
-    for (int s = 0; s < S; ++s) {
-      // scales of the next stage, loaded one stage ahead
+    // this row's partial sums go to the rank that reduces it
+    const uint32_t owner = (uint32_t)(r >> lgR);
+    const int rr = r & (R - 1);
+    const bool local = owner == rank;
+    const uint32_t push_base = local ? 0u : map_rank(ypart, owner);
+    const uint32_t push_bar = local ? 0u : map_rank(&ctl->red_bar, owner);
+    const float4* ztab4 = reinterpret_cast<const float4*>(ztab);
+    // one stage; false when a wait gave up
+    auto stage = [&](uint32_t (&slot)[4]) -> bool {
+      float sh[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) sh[h] = __half2float(__ushort_as_half((uint16_t)slot[h]));
+      ld_scales(ltl, lc, slot);
+      if (++lc == nch) { lc = 0; ++ltl; }
       const int ntl = (ch + 1 == nch) ? tile + 1 : tile, nc = (ch + 1 == nch) ? 0 : ch + 1;
-      uint32_t sc_next[2];
-      ld_scales(ntl, nc, sc_next);
       const bool ok = wait_or_abort(&ctl->d_full[db], duse & 1, ctl);
-      if (!__all_sync(kFull, ok)) break;  // the tensor-memory loads below are warp-collective
+      if (!__all_sync(kFull, ok)) return false;  // the tensor-memory loads below are warp-collective
       tc_fence_after();
-      float d[4][4];
+      // kGw groups per tensor-memory wait (fewer registers for the wide layouts)
 #pragma unroll
-      for (int h = 0; h < 4; ++h) tmem_ld4(tmem + lane_addr + kDcol + (uint32_t)(db * 64 + h * 16), d[h]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->d_free[db]);
+      for (int hp = 0; hp < 4 / Gm::kGw; ++hp) {
+        uint32_t d[Gm::kGw][kCw];
+        const uint32_t dcol = tmem + lane_addr + kDcol + (uint32_t)(db * 64 + hp * 16 * Gm::kGw);
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const float2 z = ztab[4 * ch + h];  // zero for a group past the slice
-        const float sh = __half2float(__ushort_as_half((uint16_t)(sc[h >> 1] >> (16 * (h & 1)))));
-        acc = fmaf(sh * z.y, (d[h][0] + d[h][1]) + d[h][2] + z.x, acc);
+        for (int u = 0; u < Gm::kGw; ++u) tmem_ld(dcol + 16 * u, d[u]);
+        tmem_ld_wait(d);
+        if (hp == 4 / Gm::kGw - 1) {  // the whole accumulator buffer has been read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->d_free[db]);
+        }
+#pragma unroll
+        for (int u = 0; u < Gm::kGw; ++u) {
+          const int h = Gm::kGw * hp + u;
+          float vs[kMM];
+#pragma unroll
+          for (int m = 0; m < kMM; ++m) {
+            if constexpr (Gm::kP == 1)
+              vs[m] = (__uint_as_float(d[u][3 * m]) + __uint_as_float(d[u][3 * m + 1])) + __uint_as_float(d[u][3 * m + 2]);
+            else if constexpr (Gm::kP == 2)
+              vs[m] = __uint_as_float(d[u][m]) + __uint_as_float(d[u][m + 8]);
+            else
+              vs[m] = __uint_as_float(d[u][m]);
+          }
+          // {pw Zt, pw} of (group, m) and (group, m + 1); zero past the slice and for m >= M
+          const float4* z = ztab4 + (((4 * ch + h) * Gm::kZs) >> 1);
+#pragma unroll
+          for (int m = 0; m < kMM; m += 2) {
+            if (m < M) {
+              const float4 zz = z[m >> 1];
+              acc[m] = fmaf(sh[h], fmaf(zz.y, vs[m], zz.x), acc[m]);
+              if (m + 1 < kMM) acc[m + 1] = fmaf(sh[h], fmaf(zz.w, vs[m + 1], zz.z), acc[m + 1]);
+            }
+          }
+        }
       }
-      if (ch + 1 == nch) {  // this row of the tile is complete: into rank 0's slot of this rank
-        if (rank == 0)
-          ypart[tile * 128 + r] = acc;
-        else
-          st_async_f32(push_base + (uint32_t)(tile * 128 * 4), acc, push_bar);
-        acc = 0.0f;
+      if (ch + 1 == nch) {  // this row of the tile is complete: to the rank that reduces it
+        const int base = (tile * p.kcl + (int)rank) * M * R + rr;
+        if (local) {
+#pragma unroll
+          for (int m = 0; m < kMM; ++m)
+            if (m < M) ypart[base + m * R] = acc[m];
+        } else {
+#pragma unroll
+          for (int m = 0; m < kMM; ++m)
+            if (m < M) st_async_f32(push_base + (uint32_t)((base + m * R) * 4), acc[m], push_bar);
+        }
+#pragma unroll
+        for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
       }
-      sc[0] = sc_next[0];
-      sc[1] = sc_next[1];
       tile = ntl;
       ch = nc;
       if (++db == kDbuf) { db = 0; ++duse; }
+      return true;
+    };
+    bool go = true;
+    for (int s0 = 0; go && s0 < S; s0 += kAhead) {
+#pragma unroll
+      for (int j = 0; j < kAhead; ++j)
+        if (go && s0 + j < S) go = stage(scq[j]);
     }
   }
 
-  // ---- rank 0 adds the kcl partial sums (fixed order) once the others' have landed
+  // ---- each rank adds the kcl partial sums of its rows (in rank order) once
+  // the others' have landed
   tc_fence_before();
   __syncthreads();
   if (warp < kEpiWarp0) cluster_wait();
-  if (rank == 0) {
-    bool ok = true;
-    if (p.kcl > 1) {
-      ok = mbar_wait(&ctl->red_bar, 0);
-      if (!ok && threadIdx.x == 0) atomicOr(&g_gemv_fault, kFaultTimeout);
-    }
-    if (ok && !ctl->abort) {
-      for (int i = threadIdx.x; i < ntiles * 128; i += kThreads) {
-        const int64_t n = t0 * 128 + i;
-        if (n >= p.N) continue;
-        float sum = ypart[i];
-        for (int q = 1; q < p.kcl; ++q) sum += ypart[q * p.tiles_cap * 128 + i];
-        p.y[n] = sum;
-      }
+  bool ok = true;
+  if (p.kcl > 1) {
+    ok = mbar_wait(&ctl->red_bar, 0);
+    if (!ok && threadIdx.x == 0) atomicOr(&g_gemv_fault, kFaultTimeout);
+  }
+  if (ok && !ctl->abort) {
+    const int total = ntiles * M * R;
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+      const int rr = i & (R - 1), j = i >> lgR, tl = j / M, m = j - tl * M;
+      const int64_t n = (t0 + tl) * 128 + (int64_t)rank * R + rr;
+      if (n >= p.N) continue;
+      const float* src = ypart + (tl * p.kcl * M + m) * R + rr;
+      float sum = src[0];
+      for (int q = 1; q < p.kcl; ++q) sum += src[q * M * R];
+      p.y[m * p.ldy + n] = sum;
     }
   }
   if (warp == kMmaWarp) {
@@ -609,13 +762,25 @@ EncodeTiledFn encode_fn() {
   return f;
 }
 
-size_t smem_bytes(int groups_cap, int tiles_cap, int kcl) {
-  return 1024 + (size_t)kRing * kSlotBytes + (size_t)groups_cap * kGroupBBytes + kZeroBytes +
-         (size_t)groups_cap * sizeof(float2) + (size_t)kcl * tiles_cap * 128 * sizeof(float) + sizeof(Ctl);
+template <int V>
+size_t smem_bytes_v(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
+  return 1024 + (size_t)kRing * kSlotBytes + (size_t)groups_cap * Geo<V>::kGroupB + kZeroBytes +
+         (size_t)groups_cap * Geo<V>::kZs * sizeof(float2) + (size_t)tiles_cap * 128 * M * sizeof(float) +
+         sizeof(Ctl);
+}
+
+size_t smem_bytes(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
+  switch (variant_of(M)) {
+    case 1: return smem_bytes_v<1>(groups_cap, tiles_cap, M);
+    case 2: return smem_bytes_v<2>(groups_cap, tiles_cap, M);
+    case 3: return smem_bytes_v<3>(groups_cap, tiles_cap, M);
+    default: return smem_bytes_v<4>(groups_cap, tiles_cap, M);
+  }
 }
 
 // Clusters of kcl CTAs that can be resident at once (a cluster lives on one
-// GPC, so large clusters do not tile all SMs); queried once per device.
+// GPC, so large clusters do not tile all SMs); queried once per device.  The
+// layouts share block size and shared-memory limit, so one query serves all.
 int max_active_clusters(int kcl) {
   static std::atomic<int> cache[64][4];
   int dev = 0;
@@ -624,7 +789,7 @@ int max_active_clusters(int kcl) {
   int v = cache[dev][slot].load(std::memory_order_acquire);
   if (v > 0) return v;
   const int smem = device_max_smem_optin();
-  if (cudaFuncSetAttribute(k_gemv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+  if (cudaFuncSetAttribute(k_gemv_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(device_sm_count() * kcl));
   cfg.blockDim = dim3(kThreads);
@@ -636,13 +801,48 @@ int max_active_clusters(int kcl) {
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&v, k_gemv_tc, &cfg) != cudaSuccess || v < 1) {
+  if (cudaOccupancyMaxActiveClusters(&v, k_gemv_tc<1>, &cfg) != cudaSuccess || v < 1) {
     (void)cudaGetLastError();
     return 0;
   }
   cache[dev][slot].store(v, std::memory_order_release);
   return v;
 }
+
+template <int V>
+cudaError_t launch_v(const CUtensorMap& map, const Params& p, size_t smem, cudaStream_t s) {
+  // raise the kernel's shared-memory limit only when a launch needs more
+  static std::atomic<int> smem_set[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem_set[dev].load(std::memory_order_acquire) < (int)smem) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemv_tc<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int cur = smem_set[dev].load(std::memory_order_acquire);
+    while (cur < (int)smem && !smem_set[dev].compare_exchange_weak(cur, (int)smem)) {
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.clusters * p.kcl));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)p.kcl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_gemv_tc<V>, map, p);
+}
+
+// Cost model of the busiest CTA, in units of 1/24 stage: a stage streams
+// 16 KB of codes (about 0.4 us per SM at the HBM rate), and rotating and
+// splitting one (group, row of x) in the prologue costs about 1/24 of that.
+constexpr int64_t kItemsPerStage = 24;
 
 }  // namespace
 
@@ -656,13 +856,14 @@ unsigned int take_fault_gemv() {
   return f;
 }
 
-// Work split: kcl in {1, 2, 4, 8} CTAs per cluster share a tile range and
-// split its K groups; at most as many clusters as can be resident at once
-// (one wave).  The choice minimises the stages of the busiest CTA (a stage
-// is four groups of one 128-row tile); ties go to fewer CTAs.  Returns false
-// when this kernel does not suit the shape.
-bool plan_gemv_tc(int64_t N, int64_t K, int* kcl_out, int* clusters_out) {
-  if (N <= 0 || K <= 0 || K % 128 != 0) return false;
+// Work split for M rows of x: kcl in {1, 2, 4, 8} CTAs per cluster share a
+// tile range and split its K groups; at most as many clusters as can be
+// resident at once (one wave).  The choice minimises the cost model of the
+// busiest CTA (its stages -- four groups of one 128-row tile -- and its
+// prologue items); ties go to fewer CTAs.  Returns false when no split fits
+// in shared memory.
+bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int* kcl_out, int* clusters_out) {
+  if (N <= 0 || K <= 0 || K % 128 != 0 || M < 1 || M > 16) return false;
   const int64_t G = K / 128, T = (N + 127) / 128;
   const int sms = device_sm_count();
   if (sms <= 0) return false;
@@ -674,10 +875,11 @@ bool plan_gemv_tc(int64_t N, int64_t K, int* kcl_out, int* clusters_out) {
     if (c > sms / kcl) c = sms / kcl;
     if (c > T) c = T;
     if (c < 1) continue;
-    const int64_t gcap = 4 * (((G + kcl - 1) / kcl + 3) / 4);
+    const int64_t gslice = (G + kcl - 1) / kcl;
+    const int64_t gcap = 4 * ((gslice + 3) / 4);
     const int64_t tcap = (T + c - 1) / c;
-    if ((int64_t)smem_bytes((int)gcap, (int)tcap, (int)kcl) > smem_max) continue;
-    const int64_t cost = tcap * (gcap / 4);
+    if ((int64_t)smem_bytes(gcap, tcap, M) > smem_max) continue;
+    const int64_t cost = tcap * (gcap / 4) * kItemsPerStage + gslice * M;
     if (best_kcl == 0 || cost < best || (cost == best && c * kcl < best_c * best_kcl)) {
       best = cost;
       best_kcl = kcl;
@@ -690,13 +892,29 @@ bool plan_gemv_tc(int64_t N, int64_t K, int* kcl_out, int* clusters_out) {
   return true;
 }
 
+// 1: one launch takes all M rows; 2: two launches of ceil(M / 2) and
+// floor(M / 2) rows (the B layout of all M rows does not fit); 0: neither.
+int gemv_tc_launches(int64_t N, int64_t K, int64_t M) {
+  int kcl = 0, c = 0;
+  if (plan_gemv_tc(N, K, M, &kcl, &c)) return 1;
+  if (M > 1 && plan_gemv_tc(N, K, (M + 1) / 2, &kcl, &c) && plan_gemv_tc(N, K, M / 2, &kcl, &c)) return 2;
+  return 0;
+}
+
 cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,
-                           int64_t K, const void* x, float* y, bool prefetch, cudaStream_t s) {
+                           int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, bool prefetch,
+                           cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   const int64_t G = K / 128, T = (N + 127) / 128;
-  int kcl_i = 0, c_i = 0;
-  if (!plan_gemv_tc(N, K, &kcl_i, &c_i)) return cudaErrorNotSupported;
-  const int64_t best_kcl = kcl_i, best_c = c_i;
+  int kcl = 0, clusters = 0;
+  if (!plan_gemv_tc(N, K, M, &kcl, &clusters)) {
+    if (gemv_tc_launches(N, K, M) != 2) return cudaErrorNotSupported;
+    const int64_t m1 = (M + 1) / 2;
+    cudaError_t e = launch_gemv_tc(codes, ldc, scales, lds, N, K, x, ldx, m1, y, ldy, prefetch, s);
+    if (e != cudaSuccess) return e;
+    return launch_gemv_tc(codes, ldc, scales, lds, N, K, static_cast<const uint16_t*>(x) + m1 * ldx, ldx, M - m1,
+                          y + m1 * ldy, ldy, prefetch, s);
+  }
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -714,39 +932,22 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* sc
   p.N = N;
   p.K = K;
   p.x = static_cast<const uint16_t*>(x);
+  p.ldx = ldx;
   p.y = y;
-  p.kcl = (int)best_kcl;
-  p.clusters = (int)best_c;
-  p.groups_cap = (int)(4 * (((G + best_kcl - 1) / best_kcl + 3) / 4));
-  p.tiles_cap = (int)((T + best_c - 1) / best_c);
+  p.ldy = ldy;
+  p.M = (int)M;
+  p.kcl = kcl;
+  p.clusters = clusters;
+  p.groups_cap = (int)(4 * (((G + kcl - 1) / kcl + 3) / 4));
+  p.tiles_cap = (int)((T + clusters - 1) / clusters);
   p.prefetch = prefetch ? 1 : 0;
-  const size_t smem = smem_bytes(p.groups_cap, p.tiles_cap, p.kcl);
-  // raise the kernel's shared-memory limit only when a launch needs more
-  static std::atomic<int> smem_set[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (smem_set[dev].load(std::memory_order_acquire) < (int)smem) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    int cur = smem_set[dev].load(std::memory_order_acquire);
-    while (cur < (int)smem && !smem_set[dev].compare_exchange_weak(cur, (int)smem)) {
-    }
+  const size_t smem = smem_bytes(p.groups_cap, p.tiles_cap, M);
+  switch (variant_of(M)) {
+    case 1: return launch_v<1>(map, p, smem, s);
+    case 2: return launch_v<2>(map, p, smem, s);
+    case 3: return launch_v<3>(map, p, smem, s);
+    default: return launch_v<4>(map, p, smem, s);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(best_c * best_kcl));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = (unsigned)best_kcl;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemv_tc, map, p);
 }
 
 }  // namespace tq

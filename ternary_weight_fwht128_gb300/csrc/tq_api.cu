@@ -134,8 +134,7 @@ int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt) {
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return -(int)TQ_ERR_INVALID_ARG;
   if (N < 0) return -(int)TQ_ERR_INVALID_ARG;
   if (!k_ok(K) || M < 1 || M > 16) return -(int)TQ_ERR_SHAPE;
-  int kcl = 0, clusters = 0;
-  if (M == 1 && fmt == TQ_PACK_2BIT && tq::plan_gemv_tc(N, K, &kcl, &clusters)) return TQ_GEMV_TENSOR_MEMORY;
+  if (fmt == TQ_PACK_2BIT && tq::gemv_tc_launches(N, K, M) > 0) return TQ_GEMV_TENSOR_MEMORY;
   return TQ_GEMV_MMA_SYNC;
 }
 

@@ -120,9 +120,9 @@ def test_gemv_path_validation(L):
     assert f(8, 200, 1, tq.TQ_PACK_2BIT) == -tq.TQ_ERR_SHAPE
     assert f(8, 256, 0, tq.TQ_PACK_2BIT) == -tq.TQ_ERR_SHAPE
     assert f(8, 256, 17, tq.TQ_PACK_2BIT) == -tq.TQ_ERR_SHAPE
-    # skinny M and base-3 codes always take the mma.sync kernel (no device query needed)
-    assert f(27648, 5120, 2, tq.TQ_PACK_2BIT) == tq.TQ_GEMV_MMA_SYNC
+    # base-3 codes always take the mma.sync kernel (no device query needed)
     assert f(27648, 5120, 1, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
+    assert f(5120, 27648, 16, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
 
 
 def test_gemv_validation(L):

@@ -205,16 +205,58 @@ def test_gemv_tc_shapes(orc, N, K):
     _gemv_case(orc, N, K, 1, seed=N * 7 + K, rows=rows)
 
 
+@pytest.mark.parametrize("N,K,M", [
+    (27648, 5120, 2), (19457, 2560, 3), (20000, 2944, 5), (27648, 5120, 6), (4999, 27648, 8),
+    (19500, 4480, 11), (5120, 27648, 13), (2049, 1152, 16),
+])
+def test_gemv_tc_skinny(orc, N, K, M):
+    """Skinny M on the tensor-memory kernel: each B layout (M <= 2, 5, 8, 16
+    rows of x: one, one, two and three MMA passes), ragged tiles and K
+    slices, and a shape whose B for all M rows does not fit one CTA's share
+    of shared memory (two launches of half the rows)."""
+    assert tq.gemv_path(N, K, M) == tq.TQ_GEMV_TENSOR_MEMORY
+    rng = np.random.default_rng(N + K + M)
+    rows = np.unique(np.concatenate([rng.choice(N, size=24, replace=False), np.arange(N - 130, N)]))
+    _gemv_case(orc, N, K, M, seed=N * 5 + K + M, rows=rows)
+
+
+@pytest.mark.parametrize("N,K,M", [(27648, 5120, 1), (5120, 27648, 1), (5120, 5120, 4), (27648, 5120, 16)])
+def test_gemv_tc_repeatable(N, K, M):
+    """The tensor-memory kernel sums in a fixed order and its barriers admit
+    one schedule of results: 200 back-to-back launches (each streaming its
+    weights while the previous one finishes) give the same bits as the
+    first, and no bounded wait ran out."""
+    W = synth.weights(N, K, 41, dtype="bf16")
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(synth.activations(M, K, 42))
+    outs = [torch.empty(M, N, device="cuda") for _ in range(200)]
+    torch.cuda.synchronize()
+    for y in outs:
+        tq.gemv(c2, s, x, K, out=y, weights_ready=True)
+    tq.device_fault()
+    for y in outs[1:]:
+        assert torch.equal(y, outs[0])
+
+
+def test_gemv_mma_sync_fallback_2bit(orc):
+    """2-bit codes whose K slice of B does not fit shared memory even for half
+    the rows of x take the mma.sync kernel."""
+    N, K, M = 96, 65536, 16
+    assert tq.gemv_path(N, K, M) == tq.TQ_GEMV_MMA_SYNC
+    _gemv_case(orc, N, K, M, seed=77)
+
+
 def test_gemv_path_of_benchmark_shapes():
-    """M = 1 with 2-bit codes uses the tensor-memory kernel; skinny M and
+    """2-bit codes take the tensor-memory kernel for every M of the benchmark;
     base-3 codes the mma.sync kernel."""
     for N, K in [(27648, 5120), (5120, 27648), (5120, 5120), (1, 128)]:
-        assert tq.gemv_path(N, K) == tq.TQ_GEMV_TENSOR_MEMORY
-    assert tq.gemv_path(27648, 5120, 2) == tq.TQ_GEMV_MMA_SYNC
+        for M in (1, 2, 4, 8, 16):
+            assert tq.gemv_path(N, K, M) == tq.TQ_GEMV_TENSOR_MEMORY
     assert tq.gemv_path(27648, 5120, 1, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
+    assert tq.gemv_path(5120, 27648, 16, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
 
 
-@pytest.mark.parametrize("N,K,M", [(27648, 5120, 1), (512, 1280, 1), (512, 1280, 4)])
+@pytest.mark.parametrize("N,K,M", [(27648, 5120, 1), (512, 1280, 1), (512, 1280, 4), (5120, 27648, 16)])
 def test_gemv_weights_ready_matches(orc, N, K, M):
     """TQ_GEMV_WEIGHTS_READY only moves when codes are first read.  The
     tensor-memory kernel sums in a fixed order, so its result is
