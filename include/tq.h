@@ -113,13 +113,14 @@ TQ_API tq_status tq_quantize_pack(const void *W, int wt, int64_t N, int64_t K, i
  * (no workspace):  y[m][n] = sum_g s[n][g] sum_{k in g} t[n][k] x'[m][k]
  * with x' = FWHT-128(x) in fp32, then carried at reduced precision: on the
  * tensor-memory kernel (tq_gemv_path) as three e4m3 pieces per element under
- * a power-of-two scale per group and row of x (within max(2^-12 |x'|,
- * 2^-15 max|x'|) of it, the maximum over the element's group), on the mma.sync kernel rounded to fp16; products and
- * sums in fp32.  fmt is TQ_PACK_2BIT or TQ_PACK_BASE3 (codes laid out as
- * above); x is bf16.  Accuracy against the fp64 definition: relative L2
- * error <= 2e-3.  N == 0 is a no-op.  y must not overlap the inputs.  The
- * tensor-memory kernel adds its partial sums in a fixed order (repeated calls
- * give identical bits); the mma.sync kernel does not. */
+ * a power-of-two scale per group and row of x (within max(2^-12 |x'|, 2^-15
+ * max|x'|) of it, the maximum over the element's group), on the mma.sync
+ * kernel rounded to fp16; products and sums in fp32.  fmt is TQ_PACK_2BIT or
+ * TQ_PACK_BASE3 (codes laid out as above); x is bf16.  Accuracy against the
+ * fp64 definition: relative L2 error <= 2e-3.  N == 0 is a no-op.  y must
+ * not overlap the inputs.  The tensor-memory kernel adds its partial sums in
+ * a fixed order (repeated calls give identical bits); the mma.sync kernel
+ * does not. */
 TQ_API tq_status tq_gemv(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
                   int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
                   tq_stream stream);
