@@ -11,15 +11,18 @@
 // accumulation covers all groups (equivalent to scaling each group's partial
 // sum in an epilogue, without per-group accumulator traffic).
 //
-// One CTA computes a 256 (tokens) x 256 (weight rows) tile, K in stages of 64:
+// One CTA computes a 256 (tokens) x bn (weight rows) tile, K in stages of 64;
+// bn (a multiple of 16, at most 256) is chosen per shape so that the tiles
+// fill the SMs in whole waves (two 256-row tiles of a 5120-row matrix would
+// otherwise leave a second wave of 8 tiles on 152 SMs):
 //   warp 8     (one lane) TMA-loads the 256 x 64 fp16 tile of x' (128-byte
 //              swizzle, K-major) into the stage ring;
-//   warps 0-7  decode the 256 x 64 weight tile from 2-bit codes straight into
+//   warps 0-7  decode the bn x 64 weight tile from 2-bit codes straight into
 //              the same swizzled K-major layout (lane = weight row), then,
 //              after the last stage, drain tensor memory to y;
 //   warp 9     allocates tensor memory and (one lane) issues the MMAs: per
 //              stage 2 (token halves) x 4 (K steps of 16) tcgen05.mma of
-//              128 x 256 x 16 into two 256-column fp32 accumulators.
+//              128 x bn x 16 into two fp32 accumulators (256 columns apart).
 // Stages are handed over with mbarriers (TMA bytes, decoder arrivals, MMA
 // completion via tcgen05.commit).  Every wait is bounded in time; a wait that
 // runs out records bit 1 of the status word and the CTA winds down.
@@ -38,7 +41,7 @@ namespace tq {
 namespace {
 
 constexpr int BM = 256;  // tokens per CTA (two 128-row MMA tiles)
-constexpr int BN = 256;  // weight rows per CTA (MMA N)
+constexpr int BN = 256;  // most weight rows per CTA (MMA N); a launch uses bn <= BN
 constexpr int BK = 64;   // k per stage: 128 bytes of fp16 = one swizzle row
 constexpr int kStages = 3;
 constexpr int kDecoders = 8;  // warps
@@ -81,14 +84,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
-// K-major, N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+// K-major, N = bn, M = 128.
+constexpr uint32_t idesc_f16(int bn) { return (1u << 4) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(128 >> 4) << 24); }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -152,6 +156,8 @@ struct Params {
   int64_t ldy;
   uint32_t* flag;
   int n_tiles_m;
+  int bn;          // weight rows per tile (multiple of 16, <= BN)
+  uint32_t idesc;  // idesc_f16(bn)
   int vec_store;  // y 16-byte aligned and ldy % 4 == 0: rows can take 16-byte stores
 };
 
@@ -171,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_m = blockIdx.x % p.n_tiles_m, tile_n = blockIdx.x / p.n_tiles_m;
-  const int64_t m0 = (int64_t)tile_m * BM, n0 = (int64_t)tile_n * BN;
+  const int bn = p.bn;
+  const int64_t m0 = (int64_t)tile_m * BM, n0 = (int64_t)tile_n * bn;
   const int nk = (int)(p.K / BK);
 
   if (threadIdx.x == 0) {
@@ -224,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             mma_f16(tmem + h * BN, smem_desc_sw128(a0 + h * (kAStage / 2) + kk * 32), smem_desc_sw128(b0 + kk * 32),
-                    (s > 0 || kk > 0) ? 1u : 0u);
+                    p.idesc, (s > 0 || kk > 0) ? 1u : 0u);
           }
         }
         mma_commit(&ctl->empty[slot]);  // stage free once these MMAs have read it
@@ -233,9 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     }
   } else {
     // ---------------------------------------------------------------- decoders
-    const int r = warp * 32 + lane;  // weight row inside the tile
+    const int r = warp * 32 + lane;  // weight row inside the tile (rows >= bn only arrive)
+    const bool in_tile = r < bn;
     int64_t n = n0 + r;
-    const bool row_ok = n < p.N;
+    const bool row_ok = in_tile && n < p.N;
     if (!row_ok) n = p.N - 1;
     const uint8_t* crow = p.codes + n * p.ldc;
     const uint16_t* srow = p.scales + n * p.lds;
@@ -243,7 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const int rx = r & 7;
     // codes and scales run two stages ahead of the decode, so their latency
     // hides behind two stages of MMA
-    auto ld_codes = [&](int st) { return st < nk ? ldg_nc_u4(crow + st * (BK / 4)) : make_uint4(0, 0, 0, 0); };
+    auto ld_codes = [&](int st) {
+      return (in_tile && st < nk) ? ldg_nc_u4(crow + st * (BK / 4)) : make_uint4(0, 0, 0, 0);
+    };
     auto ld_scale = [&](int st) { return (row_ok && st < nk) ? __ldg(srow + (st * BK) / 128) : (uint16_t)0; };
     uint4 cur = ld_codes(0), nx1 = ld_codes(1);
     uint16_t scur = ld_scale(0), snx1 = ld_scale(1);
@@ -257,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
       unsigned char* dst = b_ring + slot * kBStage + row_off;
       const uint32_t w[4] = {cur.x, cur.y, cur.z, cur.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {  // 16 codes -> two 16-byte chunks
+      for (int q = 0; q < 4; ++q) {  // 16 codes -> two 16-byte chunks (rows past the tile: none)
+        if (!in_tile) break;
         const uint32_t wq = w[q], w10 = wq >> 10;
         const uint4 lo = make_uint4(ts_pair<0>(wq, w10, s2), ts_pair<1>(wq, w10, s2), ts_pair<2>(wq, w10, s2),
                                     ts_pair<3>(wq, w10, s2));
@@ -281,9 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const int64_t m = m0 + half * 128 + quad * 32 + lane;
     const bool m_ok = m < p.M;
     float* yrow = p.y + (m_ok ? m : 0) * p.ldy + n0;
-    const int ncols = (int)((p.N - n0) < BN ? (p.N - n0) : BN);
+    const int ncols = (int)((p.N - n0) < bn ? (p.N - n0) : bn);
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
+    for (int c0 = 0; c0 < ncols; c0 += 32) {
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * BN + c0), v);
       if (m_ok && !ctl->abort) {
@@ -292,7 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(yrow + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
         } else {
-          for (int i = 0; i < 32 && c0 + i < ncols; ++i) yrow[c0 + i] = v[i];
+#pragma unroll
+          for (int i = 0; i < 32; ++i)  // constant indices keep v in registers
+            if (c0 + i < ncols) yrow[c0 + i] = v[i];
         }
       }
     }
@@ -330,6 +343,29 @@ EncodeTiledFn encode_fn() {
 
 constexpr size_t kGemmSmem = (size_t)kStages * (kAStage + kBStage) + sizeof(SmemCtl) + 1024;
 
+// Weight rows per tile: the multiple of 16 in [64, 256] that minimises the
+// busiest SM's work, (waves of tiles over the SMs) x (bn + 96).  The 96 rows'
+// worth stands for what a stage costs whatever bn is -- streaming the
+// 256 x 64 x' tile from L2, which narrow tiles repeat more often -- and the
+// per-tile fill and drain; it is fitted to timings of the 27B shapes (256-row
+// tiles for 27648 x 5120, 144 for 5120-row matrices).  Ties go to the larger
+// tile.
+static int gemm_tile_rows(int64_t N, int64_t M) {
+  const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 1;
+  const int64_t tm = (M + BM - 1) / BM;
+  int best = BN;
+  int64_t best_cost = -1;
+  for (int bn = BN; bn >= 64; bn -= 16) {
+    const int64_t tiles = tm * ((N + bn - 1) / bn);
+    const int64_t cost = ((tiles + sms - 1) / sms) * (bn + 96);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
                         const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, cudaStream_t s) {
   if (N == 0 || M == 0) return cudaSuccess;
@@ -357,8 +393,10 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   p.ldy = ldy;
   p.flag = flag;
   p.n_tiles_m = (int)((M + BM - 1) / BM);
+  p.bn = gemm_tile_rows(N, M);
+  p.idesc = idesc_f16(p.bn);
   p.vec_store = ((reinterpret_cast<uintptr_t>(y) & 15u) == 0 && ldy % 4 == 0) ? 1 : 0;
-  const int64_t tiles = (int64_t)p.n_tiles_m * ((N + BN - 1) / BN);
+  const int64_t tiles = (int64_t)p.n_tiles_m * ((N + p.bn - 1) / p.bn);
   static std::atomic<bool> smem_set[64];  // the kernel's shared-memory limit, raised once per device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
