@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
+  __syncwarp();  // a warp reaches the block barrier whole (lanes may have diverged)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
       for (int q = (s > kStages ? s - kStages : 0); q < s; ++q)
         (void)mbar_wait(&ctl->full_a[q % kStages], (q / kStages) & 1);
     }
+    __syncwarp();  // block-wide barriers must not be reached by part of a warp
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
@@ -238,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
       }
       mma_commit(&ctl->done);  // accumulators complete (or, after an abort, all issued MMAs done)
     }
+    __syncwarp();
   } else {
     // ---------------------------------------------------------------- decoders
     const int r = warp * 32 + lane;  // weight row inside the tile (rows >= bn only arrive)
@@ -295,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const int ncols = (int)((p.N - n0) < bn ? (p.N - n0) : bn);
 #pragma unroll 1
     for (int c0 = 0; c0 < ncols; c0 += 32) {
+      __syncwarp();  // tcgen05.ld is warp-collective; the stores below diverge
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * BN + c0), v);
       if (m_ok && !ctl->abort) {
@@ -311,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     }
   }
   tc_fence_before();
+  __syncwarp();  // a warp reaches the block barrier whole (lanes may have diverged)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();

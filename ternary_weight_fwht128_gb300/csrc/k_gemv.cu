@@ -385,6 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
     }
 
     // rotate this chunk of x (all M rows) into the permuted fp16 layout
+    __syncwarp();  // warps reach block barriers whole
     if (c > 0) __syncthreads();  // previous chunk's activations no longer read
     for (int b = warp; b < ng * M; b += kWarps) {
       const int m = b / ng, gl = b - m * ng;
@@ -408,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
         if (lane == 0) xsum[gl * xsum_stride(MB) + m] = hsum;
       }
     }
+    __syncwarp();
     __syncthreads();
 
     // compute iterator
@@ -505,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
     }
   }
   // ---- reduce the kCl partial sums through distributed shared memory
+  __syncwarp();
   __syncthreads();
   cluster_sync();
   const int nout = ntiles * 16 * M;

@@ -62,6 +62,7 @@
 #include <cuda.h>
 #include <cuda_fp8.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "tq_internal.h"
@@ -78,7 +79,7 @@ constexpr int kTmaWarp = 16;
 constexpr int kMmaWarp = 17;                  // warps 17, 18 issue the MMAs of team 0, 1
 constexpr int kEpiWarp0 = 19;                 // warps 19-22: epilogue
 constexpr int kThreads = 32 * 23;             // + 4 epilogue warps (19-22)
-constexpr int kRing = 4;                      // code slots in flight (four groups each)
+constexpr int kRing = 4;                      // code slots in flight (four groups each; even: slot s % kRing is always team s % 2)
 constexpr int kAbuf = 3;                      // weight (A) buffers in tensor memory, one stage each
 constexpr int kAPeriod = 2 * kAbuf;           // stages between two uses of one A buffer by one team
 static_assert(kAbuf % 2 == 1, "A buffers alternate between the two teams");
@@ -355,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* ring = smem;
-  unsigned char* bsm = ring + kRing * kSlotBytes;
+  constexpr int nring = kRing;
+  unsigned char* bsm = ring + nring * kSlotBytes;
   unsigned char* zero = bsm + p.groups_cap * Gm::kGroupB;
   float2* ztab = reinterpret_cast<float2*>(zero + kZeroBytes);
   float* ypart = reinterpret_cast<float*>(ztab + p.groups_cap * Gm::kZs);
@@ -363,20 +365,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
-  const int64_t cluster = blockIdx.x / p.kcl;
+  // kcl is a power of two; the tile ranges use 32-bit division when it cannot
+  // overflow (64-bit division is a long instruction sequence)
+  const int lgk = __ffs(p.kcl) - 1;
+  const int64_t cluster = blockIdx.x >> lgk;
   const int64_t G = p.K / 128;
-  const int64_t g0 = G * rank / p.kcl, g1 = G * (rank + 1) / p.kcl;
+  const int64_t g0 = (G * rank) >> lgk, g1 = (G * (rank + 1)) >> lgk;
   const int ng = (int)(g1 - g0), nch = (ng + 3) >> 2;  // four-group stages per tile
   const int64_t T = (p.N + 127) / 128;
-  const int64_t t0 = T * cluster / p.clusters;
-  const int ntiles = (int)(T * (cluster + 1) / p.clusters - t0);
+  int64_t t0, t1;
+  if (T * p.clusters <= 0xffffffffll) {
+    t0 = (uint32_t)(T * cluster) / (uint32_t)p.clusters;
+    t1 = (uint32_t)(T * (cluster + 1)) / (uint32_t)p.clusters;
+  } else {
+    t0 = T * cluster / p.clusters;
+    t1 = T * (cluster + 1) / p.clusters;
+  }
+  const int ntiles = (int)(t1 - t0);
   const int S = ntiles * nch;  // stages (ring loads) of this CTA
   const int M = p.M;
   // rank q reduces rows R q .. R q + R - 1 of every tile
-  const int lgR = 7 - (31 - __clz(p.kcl)), R = 1 << lgR;
+  const int lgR = 7 - lgk, R = 1 << lgR;
 
+  int issued_loads = 0;
+  auto fill_ring = [&]() {
+    for (; issued_loads < S && issued_loads < nring; ++issued_loads) {
+      const int l = issued_loads, tile = l / nch, lc = l - tile * nch;
+      mbar_arrive_expect_tx(&ctl->full[l], kSlotBytes);
+      tma_load_2d(smem_u32(ring + l * kSlotBytes), &cmap, (int)((g0 + 4 * lc) * 32), (int)((t0 + tile) * 128),
+                  &ctl->full[l]);
+    }
+  };
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < nring; ++i) {
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->empty[i], kTeamWarps);
     }
@@ -410,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     for (int i = threadIdx.x; i < p.groups_cap * Gm::kZs; i += kThreads) ztab[i] = make_float2(0.0f, 0.0f);
   }
   tc_fence_before();
+  __syncwarp();  // a warp reaches the block barrier whole (lanes may have diverged)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
@@ -420,26 +442,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
 
   // Inputs may come from the preceding kernel on the stream: x always waits
   // for it; codes and scales too unless the caller declared them ready, in
-  // which case the ring fills while that kernel finishes.
-  int issued_loads = 0;
-  auto fill_ring = [&]() {
-    for (; issued_loads < S && issued_loads < kRing; ++issued_loads) {
-      const int l = issued_loads, tile = l / nch, lc = l - tile * nch;
-      mbar_arrive_expect_tx(&ctl->full[l], kSlotBytes);
-      tma_load_2d(smem_u32(ring + l * kSlotBytes), &cmap, (int)((g0 + 4 * lc) * 32), (int)((t0 + tile) * 128),
-                  &ctl->full[l]);
-    }
-  };
+  // which case the ring fills while that kernel finishes.  The TMA warp fills
+  // the ring while the other warps rotate x; block-wide barriers must not be
+  // reached by part of a warp, hence the __syncwarp.
   if (p.prefetch && warp == kTmaWarp && lane == 0) fill_ring();
   pdl_wait();
   pdl_launch_dependents();
-  if (!p.prefetch && warp == kTmaWarp && lane == 0) fill_ring();  // while the others rotate x
+  if (!p.prefetch && warp == kTmaWarp && lane == 0) fill_ring();
+  if (warp == kTmaWarp) __syncwarp();
 
   // ---- rotate this CTA's slice of each row of x and split it into three
   // e4m3 pieces.  Lane 4i + j holds elements k = 16i + j + 4b (b = 0..3) of
   // its group: these are the four B bytes that meet one code class j of one
   // code word i, so the lane writes each piece as one 32-bit word.
-  for (int it = warp; it < ng * M; it += kThreads / 32) {
+  const int pwarp = warp < kTmaWarp ? warp : warp - 1;  // rotation warps: all but the TMA warp
+  for (int it = pwarp; it < ng * M && warp != kTmaWarp; it += kThreads / 32 - 1) {
     const int gl = it / M, m = it - gl * M;
     const int i8 = lane >> 2, jc = lane & 3;
     const uint16_t* xg = p.x + m * p.ldx + (g0 + gl) * 128 + 16 * i8 + jc;
@@ -481,23 +498,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     if (lane == 0) ztab[gl * Gm::kZs + m] = make_float2(pw * (zs * -0.001953125f), pw);  // pw * (-2^-9 sum), pw
   }
   fence_async_smem();  // B written by ordinary stores, read by the tensor cores
+  __syncwarp();  // a warp reaches the block barrier whole (lanes may have diverged)
   __syncthreads();
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int l = issued_loads, slot = l % kRing, use = l / kRing, tile = l / (nch > 0 ? nch : 1), lc = l - tile * nch;
+      int l = issued_loads, slot = l % nring, use = l / nring, tile = l / (nch > 0 ? nch : 1), lc = l - tile * nch;
       for (; l < S; ++l) {
         if (!wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(&ctl->full[slot], kSlotBytes);
         tma_load_2d(smem_u32(ring + slot * kSlotBytes), &cmap, (int)((g0 + 4 * lc) * 32), (int)((t0 + tile) * 128),
                     &ctl->full[slot]);
-        if (++slot == kRing) { slot = 0; ++use; }
+        if (++slot == nring) { slot = 0; ++use; }
         if (++lc == nch) { lc = 0; ++tile; }
       }
       // loads issued but possibly never consumed: let them land before exit
-      for (int q = (l > kRing ? l - kRing : 0); q < l; ++q) (void)mbar_wait(&ctl->full[q % kRing], (q / kRing) & 1);
+      for (int q = (l > nring ? l - nring : 0); q < l; ++q) (void)mbar_wait(&ctl->full[q % nring], (q / nring) & 1);
     }
+    __syncwarp();
   } else if (warp < kDecWarps) {
     // ------------------------------------------------------------ decoders
     // team (warp / 8) takes the stages of its parity, so two stages are
@@ -512,10 +531,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     uint32_t off[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) off[q] = rbase + ((((uint32_t)(4 * gh + q)) ^ rx) << 4);
+    int slot = team, use = 0;  // ring slot of stage s and its use count (s % nring, s / nring)
     for (int s = team; s < S; s += 2) {
       // A buffer ab last held stage s - kAbuf (the other team's), whose MMAs
       // are the ((s - kAbuf) / kAPeriod)-th completion a_free[ab][team] counts
-      const int slot = s % kRing, use = s / kRing, ab = s % kAbuf;
+      const int ab = s % kAbuf;
       bool ok = wait_or_abort(&ctl->full[slot], use & 1, ctl);
       uint4 c[4];
 #pragma unroll
@@ -543,6 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->a_full[ab][team]);
+      slot += 2;
+      if (slot >= nring) { slot -= nring; ++use; }
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------ MMA issue
@@ -596,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     }
     // every MMA this warp issued must be complete before tensor memory is freed
     if (s - 2 >= 0 && lane == 0) (void)mbar_wait(&ctl->d_full[t], ((s - 2) >> 1) & 1);
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     constexpr int kMM = Gm::kMM, kCw = Gm::kCw;
@@ -719,6 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   // ---- each rank adds the kcl partial sums of its rows (in rank order) once
   // the others' have landed
   tc_fence_before();
+  __syncwarp();  // a warp reaches the block barrier whole (lanes may have diverged)
   __syncthreads();
   if (warp < kEpiWarp0) cluster_wait();
   bool ok = true;
@@ -739,6 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     }
   }
   if (warp == kMmaWarp) {
+    __syncwarp();  // the reduction loop above may leave the warp diverged
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
   }
@@ -763,18 +788,18 @@ EncodeTiledFn encode_fn() {
 }
 
 template <int V>
-size_t smem_bytes_v(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
-  return 1024 + (size_t)kRing * kSlotBytes + (size_t)groups_cap * Geo<V>::kGroupB + kZeroBytes +
+size_t smem_bytes_v(int64_t groups_cap, int64_t tiles_cap, int64_t M, int ring) {
+  return 1024 + (size_t)ring * kSlotBytes + (size_t)groups_cap * Geo<V>::kGroupB + kZeroBytes +
          (size_t)groups_cap * Geo<V>::kZs * sizeof(float2) + (size_t)tiles_cap * 128 * M * sizeof(float) +
          sizeof(Ctl);
 }
 
-size_t smem_bytes(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
+size_t smem_bytes(int64_t groups_cap, int64_t tiles_cap, int64_t M, int ring = kRing) {
   switch (variant_of(M)) {
-    case 1: return smem_bytes_v<1>(groups_cap, tiles_cap, M);
-    case 2: return smem_bytes_v<2>(groups_cap, tiles_cap, M);
-    case 3: return smem_bytes_v<3>(groups_cap, tiles_cap, M);
-    default: return smem_bytes_v<4>(groups_cap, tiles_cap, M);
+    case 1: return smem_bytes_v<1>(groups_cap, tiles_cap, M, ring);
+    case 2: return smem_bytes_v<2>(groups_cap, tiles_cap, M, ring);
+    case 3: return smem_bytes_v<3>(groups_cap, tiles_cap, M, ring);
+    default: return smem_bytes_v<4>(groups_cap, tiles_cap, M, ring);
   }
 }
 
@@ -941,7 +966,11 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* sc
   p.groups_cap = (int)(4 * (((G + kcl - 1) / kcl + 3) / 4));
   p.tiles_cap = (int)((T + clusters - 1) / clusters);
   p.prefetch = prefetch ? 1 : 0;
-  const size_t smem = smem_bytes(p.groups_cap, p.tiles_cap, M);
+  const int64_t smem_max = device_max_smem_optin();
+  // More than half an SM's shared memory, so no two CTAs share an SM whatever
+  // the register count: each allocates all of tensor memory, and a second
+  // one would block in tcgen05.alloc while its cluster peers wait for it.
+  const size_t smem = std::max(smem_bytes(p.groups_cap, p.tiles_cap, M), (size_t)(smem_max / 2 + 1024));
   switch (variant_of(M)) {
     case 1: return launch_v<1>(map, p, smem, s);
     case 2: return launch_v<2>(map, p, smem, s);

@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_quantize_pack(const void* __res
         // ten groups' trits -> 256 base-3 bytes (plus the zero padding after
         // the row's last byte); trits[] is double-buffered, so one barrier per
         // unit suffices.
+        __syncwarp();
         __syncthreads();
         const int64_t k0 = d * 1280;
         const int64_t unit_trits = (K - k0) < 1280 ? (K - k0) : 1280;

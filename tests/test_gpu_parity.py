@@ -238,6 +238,27 @@ def test_gemv_tc_repeatable(N, K, M):
         assert torch.equal(y, outs[0])
 
 
+@pytest.mark.parametrize("N,K,M", [(5120, 27648, 1), (27648, 5120, 2), (2049, 1152, 16)])
+def test_gemv_tc_reads_no_stale_shared_memory(N, K, M):
+    """Between launches a cuBLAS matmul of changing random operands leaves
+    different data in every SM's shared memory; a kernel that read any of it
+    before writing it would not reproduce its first result."""
+    W = synth.weights(N, K, 51, dtype="bf16")
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(synth.activations(M, K, 52))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(53)
+    scrib = [torch.randn(2048, 2048, device="cuda", generator=gen, dtype=torch.bfloat16) for _ in range(4)]
+    outs = [torch.empty(M, N, device="cuda") for _ in range(40)]
+    torch.cuda.synchronize()
+    for i, y in enumerate(outs):
+        _ = scrib[i % 4] @ scrib[(i + 1) % 4]
+        tq.gemv(c2, s, x, K, out=y)
+    tq.device_fault()
+    for y in outs[1:]:
+        assert torch.equal(y, outs[0])
+
+
 def test_gemv_mma_sync_fallback_2bit(orc):
     """2-bit codes whose K slice of B does not fit shared memory even for half
     the rows of x take the mma.sync kernel."""
