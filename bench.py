@@ -38,8 +38,8 @@ LAYER_SHAPES = [("h2h_a", HIDDEN, HIDDEN), ("h2h_b", HIDDEN, HIDDEN), ("gate", F
 METRIC = "ternary GEMV packed-weight HBM GB/s (% of peak); prefill GEMM TFLOP/s"
 # DRAM bytes per algorithmic byte of k_gemv_tc, from an ncu capture of one
 # 27648x5120 launch: dram__bytes_read.sum + dram__bytes_write.sum =
-# 37,657,856 + 256 for 37,601,280 packed bytes (every weight byte read once).
-GEMV_TC_TRAFFIC_RATIO = (37657856 + 256) / 37601280
+# 37,668,096 + 256 for 37,601,280 packed bytes (every weight byte read once).
+GEMV_TC_TRAFFIC_RATIO = (37668096 + 256) / 37601280
 WORKLOAD = ("decode GEMV M=1, 2-bit codes, 64-layer stack of 27B-class shapes "
             "{5120x5120 x2, 27648x5120 x2, 5120x27648} per layer (320 launches, FWHT-128 fused)")
 
