@@ -1,182 +1,276 @@
 // k_quant.cu -- offline quantise + pack (tq_quantize_pack).
 //
-// Per (row n, group g) of 128 weights, one half-warp:
-//   1. loads the group with 16-byte loads (lane p: elements 8p .. 8p+7),
-//   2. rotates it with the staged FWHT-128 in fp32 (fwht128_x8),
-//   3. sums |w'| in the halving-tree order h = 64, 32, ..., 1: h >= 8 pairs
-//      lane p with lane p ^ (h/8) through shuffles, h = 4, 2, 1 stay in-lane
-//      (IEEE addition commutes, so every lane ends with the same bits),
+// Per (row n, group g) of 128 weights, one lane pair; lane h (0, 1) of the
+// pair holds elements 64h .. 64h + 63 of the group in registers:
+//   1. 16-byte loads (8 for bf16, 16 for fp32);
+//   2. the staged FWHT-128 in fp32: stages h = 1 .. 32 inside the lane, stage
+//      64 across the pair (one shuffle per element), then * c;
+//   3. sum |w'| in the halving-tree order h = 64, 32, ..., 1.  At each level
+//      the pair holds the 2P partial sums of the level before (P per lane)
+//      and splits the P new sums between its lanes, so each sum is one
+//      shuffle and one addition; an IEEE sum does not depend on the order of
+//      its two operands, so the tree is the oracle's bit for bit;
 //   4. mean = sum * 2^-7, scale = fp16_RN(mean) (absmean, mhpq.cn/news/1159370
-//      sec. 1.1; one fp16 scale per 128 weights, sec. 1.3),
+//      sec. 1.1; one fp16 scale per 128 weights, sec. 1.3);
 //   5. t = sign(w') * [|w'| > s/2] for a finite s > 0, t = 0 when s == 0.
 //      This equals clamp(rint(w'/s), -1, 1) with IEEE division and ties to
 //      even: the quotient rounds above 0.5 exactly when |w'| > (s/2)(1 + 2^-24),
 //      and no fp32 value lies strictly between s/2 and that bound.  For
 //      s = +inf both forms give 0.
-//   6. packs: 2-bit codes straight from registers (lane p owns bytes 2p,
-//      2p + 1 of the group); base-3 bytes from the trits of ten consecutive
-//      groups (1280 trits = 256 bytes, so such units never share a byte),
-//      staged in shared memory.
+//   6. packs: the lane's 64 codes c = t + 1 form four 32-bit words that are
+//      its 16 bytes of the 2-bit layout (one store).  The same words are the
+//      base-3 digits: a warp takes three units of five groups (640 trits =
+//      128 bytes each, so units never share a byte; lanes 30, 31 idle), puts
+//      its code words in shared memory, and each lane forms 12 of the warp's
+//      384 base-3 bytes from 10-bit windows of them.
 //
-// This pass reads 2 or 4 bytes per weight and is bound by HBM.  A CTA of five
-// warps handles units of (row, ten groups); every warp keeps kDepth units of
-// 16-byte loads in flight in registers.
+// The pass reads 2 or 4 bytes per weight and should be bound by HBM: each warp
+// copies the next unit triple's weights into shared memory (cp.async, no
+// registers held) while it works on the current one.
+#include <atomic>
+
 #include "tq_internal.h"
 
 namespace tq {
 
 namespace {
 
-constexpr int kWarps = 5;
+constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kDepth = 4;
 
 template <int WT>
 struct Raw {
-  uint4 w[WT == TQ_F32 ? 2 : 1];
+  uint4 w[WT == TQ_F32 ? 16 : 8];  // this lane's 64 weights
 };
 
+// Staging of the weights: per warp and buffer, 32 lanes x (the lane's 64
+// weights + 16 bytes, so that lanes 16-byte reads spread over all banks).
+template <int WT>
+constexpr int kLaneStage = (WT == TQ_F32 ? 256 : 128) + 16;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 template <int WT, bool DO2, bool DO3>
-__global__ void __launch_bounds__(kThreads, 4) k_quantize_pack(const void* __restrict__ W, int64_t N, int64_t K,
+__global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __restrict__ W, int64_t N, int64_t K,
                                                             int64_t ldw, uint8_t* __restrict__ codes2, int64_t ld2,
                                                             uint8_t* __restrict__ codes3, int64_t ld3,
-                                                            uint16_t* __restrict__ scales, int64_t lds) {
+                                                            uint16_t* __restrict__ scales, int64_t lds, int vec2) {
   constexpr int esize = WT == TQ_F32 ? 4 : 2;
-  __shared__ __align__(16) int8_t trits[2][1280];
+  __shared__ __align__(16) uint32_t cw[kWarps][32 * 4 + 4];  // code words of the warp's lanes (+ one spare word)
+  // weights of two triples (dynamic: 72 KB for fp32 weights)
+  extern __shared__ __align__(16) unsigned char qstage[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int p = lane & 15, half = lane >> 4;
+  auto stage_at = [&](int buf) { return qstage + ((size_t)buf * kWarps + warp) * (32 * kLaneStage<WT>); };
+  const int h = lane & 1;            // half of the group
+  const int ul = lane / 10;          // unit of the triple (3: idle lanes 30, 31)
+  const int kq = (lane % 10) >> 1;   // group inside the unit
   const int64_t G = K / 128;
-  const int64_t ndec = (G + 9) / 10;
-  const int64_t total = N * ndec;
+  const int64_t nu = (G + 4) / 5;    // units per row
+  const int64_t nunits = N * nu;
+  const int64_t niters = (nunits + 2) / 3;
   const int64_t nbytes3 = (K + 4) / 5;
   const int64_t ld3min = (nbytes3 + 15) / 16 * 16;
-  const int64_t mine = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  const int gw = 2 * warp + half;  // this half-warp's group inside a unit
+  const int64_t stride = (int64_t)gridDim.x * kWarps;
+  uint32_t* const wbuf = cw[warp];
 
   pdl_wait();
 
-  // Units of this CTA: u = blockIdx.x + i * gridDim.x, i = 0, 1, ...  Two
-  // iterators (loads run kDepth units ahead of the arithmetic) walk them with
-  // a constant stride, advancing (row n, unit-in-row d) without division.
-  const int64_t dn = (int64_t)gridDim.x / ndec, dd = (int64_t)gridDim.x - dn * ndec;
-  struct It {
-    int64_t n, d;
+  // rows and units-in-row of the three units of triple `it` (one division)
+  struct Tri {
+    int64_t n[3], u[3];
   };
-  auto advance = [&](It& it) {
-    it.d += dd;
-    it.n += dn;
-    if (it.d >= ndec) {
-      it.d -= ndec;
-      it.n += 1;
+  auto triple = [&](int64_t it) {
+    Tri t;
+    const int64_t U0 = 3 * it;
+    t.n[0] = U0 / nu;
+    t.u[0] = U0 - t.n[0] * nu;
+#pragma unroll
+    for (int q = 1; q < 3; ++q) {
+      t.n[q] = t.n[q - 1];
+      t.u[q] = t.u[q - 1] + 1;
+      if (t.u[q] == nu) {
+        t.u[q] = 0;
+        ++t.n[q];
+      }
     }
+    return t;
   };
-  It li{(int64_t)blockIdx.x / ndec, (int64_t)blockIdx.x % ndec};
-  It ci = li;
-  auto load = [&](Raw<WT>& r) {
-    const int64_t g = li.d * 10 + gw;
-    r.w[0] = make_uint4(0, 0, 0, 0);
-    if constexpr (WT == TQ_F32) r.w[1] = r.w[0];
-    if (g < G) {
-      const unsigned char* src = static_cast<const unsigned char*>(W) + ((li.n * ldw) + g * 128 + 8 * p) * esize;
-      r.w[0] = ldg_nc_u4(src);
-      if constexpr (WT == TQ_F32) r.w[1] = ldg_nc_u4(src + 16);
+  // group of this lane in triple `it`: row n, group g (valid: inside the matrix)
+  auto locate = [&](int64_t it, const Tri& t, int64_t& n, int64_t& g) -> bool {
+    const int q = ul < 3 ? ul : 0;
+    n = q == 0 ? t.n[0] : (q == 1 ? t.n[1] : t.n[2]);
+    g = 5 * (q == 0 ? t.u[0] : (q == 1 ? t.u[1] : t.u[2])) + kq;
+    return ul < 3 && 3 * it + ul < nunits && g < G;
+  };
+  // starts the copy of triple `it`'s weights into staging buffer `buf`
+  auto load = [&](int buf, int64_t it) {
+    int64_t n, g;
+    if (it < niters && locate(it, triple(it), n, g)) {
+      const unsigned char* src = static_cast<const unsigned char*>(W) + (n * ldw + g * 128 + 64 * h) * esize;
+      const uint32_t dst = smem_u32(stage_at(buf) + lane * kLaneStage<WT>);
+#pragma unroll
+      for (int i = 0; i < (WT == TQ_F32 ? 16 : 8); ++i) cp_async16(dst + 16 * i, src + 16 * i);
     }
-    advance(li);
+    cp_async_commit();
+  };
+  auto fetch = [&](Raw<WT>& r, int buf, bool ok) {
+    const uint4* src = reinterpret_cast<const uint4*>(stage_at(buf) + lane * kLaneStage<WT>);
+#pragma unroll
+    for (int i = 0; i < (WT == TQ_F32 ? 16 : 8); ++i) r.w[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
   };
 
-  Raw<WT> buf[kDepth];
+  auto process = [&](int buf, int64_t it) {
+    int64_t n, g;
+    const Tri tri = triple(it);
+    const bool ok = locate(it, tri, n, g);
+    Raw<WT> r;
+    fetch(r, buf, ok);
+    float v[64];
 #pragma unroll
-  for (int s = 0; s < kDepth; ++s)
-    if (s < mine) load(buf[s]);
-
-  for (int64_t ib = 0; ib < mine; ib += kDepth) {
+    for (int i = 0; i < (WT == TQ_F32 ? 16 : 8); ++i) {
+      if constexpr (WT == TQ_F32) {
+        v[4 * i + 0] = __uint_as_float(r.w[i].x);
+        v[4 * i + 1] = __uint_as_float(r.w[i].y);
+        v[4 * i + 2] = __uint_as_float(r.w[i].z);
+        v[4 * i + 3] = __uint_as_float(r.w[i].w);
+      } else {
+        bf16x8_to_f32(r.w[i], &v[8 * i]);
+      }
+    }
+    // ---- FWHT-128: stages 1 .. 32 in the lane, 64 across the pair, then * c
 #pragma unroll
-    for (int s = 0; s < kDepth; ++s) {
-      const int64_t i = ib + s;
-      if (i >= mine) break;  // CTA-uniform
-      const Raw<WT> cur = buf[s];
-      if (i + kDepth < mine) load(buf[s]);
-      const int64_t n = ci.n, d = ci.d;
-      advance(ci);
-      const int64_t g = d * 10 + gw;
-      int8_t* tr = trits[i & 1];
-      // A half-warp whose group lies past the row end still runs the
-      // arithmetic (its shuffles stay inside the half-warp) and discards it.
-      {
-        float v[8];
-        if constexpr (WT == TQ_F32) {
-          v[0] = __uint_as_float(cur.w[0].x);
-          v[1] = __uint_as_float(cur.w[0].y);
-          v[2] = __uint_as_float(cur.w[0].z);
-          v[3] = __uint_as_float(cur.w[0].w);
-          v[4] = __uint_as_float(cur.w[1].x);
-          v[5] = __uint_as_float(cur.w[1].y);
-          v[6] = __uint_as_float(cur.w[1].z);
-          v[7] = __uint_as_float(cur.w[1].w);
+    for (int hs = 1; hs < 64; hs <<= 1) {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        if (j & hs) continue;
+        const float a = v[j], b = v[j + hs];
+        v[j] = __fadd_rn(a, b);
+        v[j + hs] = __fsub_rn(a, b);
+      }
+    }
+    {
+      const float sgn = h ? -1.0f : 1.0f;  // lower half: own + other; upper half: other - own
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        const float o = __shfl_xor_sync(kFull, v[j], 1);
+        v[j] = __fmaf_rn(sgn, v[j], o);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 64; ++j) v[j] = __fmul_rn(v[j], kInvSqrt128);
+    // ---- sum |w'|: halving tree h = 64 .. 1, each level's sums split over the pair
+    float t32[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const float lo = fabsf(v[jj]), hi = fabsf(v[32 + jj]);
+      const float mine = h ? hi : lo, send = h ? lo : hi;
+      t32[jj] = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
+    }
+    float t16[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const float mine = h ? t32[16 + jj] : t32[jj], send = h ? t32[jj] : t32[16 + jj];
+      t16[jj] = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
+    }
+    float t8[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const float mine = h ? t16[8 + jj] : t16[jj], send = h ? t16[jj] : t16[8 + jj];
+      t8[jj] = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
+    }
+    float t4[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const float mine = h ? t8[4 + jj] : t8[jj], send = h ? t8[jj] : t8[4 + jj];
+      t4[jj] = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
+    }
+    float t2[2];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      const float mine = h ? t4[2 + jj] : t4[jj], send = h ? t4[jj] : t4[2 + jj];
+      t2[jj] = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
+    }
+    float t1;
+    {
+      const float mine = h ? t2[1] : t2[0], send = h ? t2[0] : t2[1];
+      t1 = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
+    }
+    const float sum = __fadd_rn(t1, __shfl_xor_sync(kFull, t1, 1));  // h = 1: the same bits in both lanes
+    const float mean = __fmul_rn(sum, 0.0078125f);
+    const __half sh = __float2half_rn(mean);
+    const float sc = __half2float(sh);
+    const float half_s = sc * 0.5f;  // exact
+    // ---- ternarise: code c = t + 1 at bits 2 (j % 16) of word j / 16
+    uint32_t cwd[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      const float w = v[j];
+      const uint32_t c = (sc != 0.0f && fabsf(w) > half_s) ? (w > 0.0f ? 2u : 0u) : 1u;
+      cwd[j >> 4] |= c << (2 * (j & 15));
+    }
+    if (ok) {
+      if constexpr (DO2) {
+        uint8_t* dst = codes2 + n * ld2 + g * 32 + 16 * h;
+        if (vec2) {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(cwd[0], cwd[1], cwd[2], cwd[3]);
         } else {
-          bf16x8_to_f32(cur.w[0], v);
-        }
-        fwht128_x8(v, lane);
-        float a[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) a[j] = fabsf(v[j]);
-#pragma unroll
-        for (int m = 8; m >= 1; m >>= 1) {  // h = 64, 32, 16, 8
-#pragma unroll
-          for (int j = 0; j < 8; ++j) a[j] = __fadd_rn(a[j], __shfl_xor_sync(kFull, a[j], m));
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) a[j] = __fadd_rn(a[j], a[j + 4]);  // h = 4
-        a[0] = __fadd_rn(a[0], a[2]);                                  // h = 2
-        a[1] = __fadd_rn(a[1], a[3]);
-        a[0] = __fadd_rn(a[0], a[1]);  // h = 1
-        const float mean = __fmul_rn(a[0], 0.0078125f);
-        const __half sh = __float2half_rn(mean);
-        const float sc = __half2float(sh);
-        const float half_s = sc * 0.5f;  // exact
-        uint32_t codes = 0;
-        uint32_t tw[2] = {0u, 0u};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float w = v[j];
-          const int t = (sc != 0.0f && fabsf(w) > half_s) ? (w > 0.0f ? 1 : -1) : 0;
-          codes |= (uint32_t)(t + 1) << (2 * j);
-          tw[j >> 2] |= ((uint32_t)t & 0xffu) << (8 * (j & 3));
-        }
-        if (g < G) {
-          if constexpr (DO2) *reinterpret_cast<uint16_t*>(codes2 + n * ld2 + g * 32 + 2 * p) = (uint16_t)codes;
-          if constexpr (DO3) *reinterpret_cast<uint2*>(&tr[gw * 128 + 8 * p]) = make_uint2(tw[0], tw[1]);
-          if (p == 0) scales[n * lds + g] = __half_as_ushort(sh);
+          for (int i = 0; i < 16; ++i) dst[i] = (uint8_t)(cwd[i >> 2] >> (8 * (i & 3)));
         }
       }
-      if constexpr (DO3) {
-        // ten groups' trits -> 256 base-3 bytes (plus the zero padding after
-        // the row's last byte); trits[] is double-buffered, so one barrier per
-        // unit suffices.
-        __syncwarp();
-        __syncthreads();
-        const int64_t k0 = d * 1280;
-        const int64_t unit_trits = (K - k0) < 1280 ? (K - k0) : 1280;
-        const int64_t b0 = d * 256;
-        const int64_t bend = (d == ndec - 1) ? ld3min : b0 + 256;
-        for (int64_t b = b0 + threadIdx.x; b < bend; b += kThreads) {
-          const int64_t lb = b - b0;
-          uint32_t val = 0;
-          if (b < nbytes3) {
-            uint32_t pw = 1;
+      if (h == 0) scales[n * lds + g] = __half_as_ushort(sh);
+    }
+    if constexpr (DO3) {
+      // ---- base-3: trit T of unit q of the triple is bits 2T .. 2T + 1 of
+      // the unit's 1280-bit run in wbuf (lanes 10q .. 10q + 9, 128 bits each);
+      // groups past the matrix read as code 1 (t = 0).
+      __syncwarp();  // the previous triple's reads of wbuf are done
+      if (ok) {
+        reinterpret_cast<uint4*>(wbuf)[lane] = make_uint4(cwd[0], cwd[1], cwd[2], cwd[3]);
+      } else {
+        reinterpret_cast<uint4*>(wbuf)[lane] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
+      }
+      __syncwarp();
+      const int64_t U0 = 3 * it;
 #pragma unroll
-            for (int q = 0; q < 5; ++q) {
-              const int64_t lk = 5 * lb + q;
-              const uint32_t dg = lk < unit_trits ? (uint32_t)(tr[lk] + 1) : 1u;
-              val += dg * pw;
-              pw *= 3;
-            }
-          }
-          codes3[n * ld3 + b] = (uint8_t)val;
+      for (int m = 0; m < 12; ++m) {
+        const int B = 12 * lane + m;  // byte of the triple's 384
+        const int q = B >> 7, b = B & 127;
+        const int64_t U = U0 + q;
+        if (U >= nunits) continue;
+        const int64_t un = q == 0 ? tri.n[0] : (q == 1 ? tri.n[1] : tri.n[2]);
+        const int64_t uu = q == 0 ? tri.u[0] : (q == 1 ? tri.u[1] : tri.u[2]);
+        const int64_t pos = uu * 128 + b;  // byte of the row
+        if (pos >= ld3min) continue;        // past the row's zero padding
+        uint32_t val = 0;
+        if (pos < nbytes3) {
+          const int bit = 1280 * q + 10 * b;
+          const uint32_t lo = wbuf[bit >> 5], hi = wbuf[(bit >> 5) + 1];
+          const uint32_t win = __funnelshift_r(lo, hi, bit & 31);
+          val = (win & 3u) + 3u * ((win >> 2) & 3u) + 9u * ((win >> 4) & 3u) + 27u * ((win >> 6) & 3u) +
+                81u * ((win >> 8) & 3u);
         }
+        codes3[un * ld3 + pos] = (uint8_t)val;
       }
     }
+  };
+
+  int64_t it = (int64_t)blockIdx.x * kWarps + warp;
+  int buf = 0;
+  load(buf, it);
+  for (; it < niters; it += stride) {
+    load(buf ^ 1, it + stride);  // the next triple streams in meanwhile
+    cp_async_wait<1>();          // this lane's copies of triple `it` have landed
+    process(buf, it);
+    __syncwarp();                // every lane has read `buf` before it is refilled
+    buf ^= 1;
   }
+  cp_async_wait<0>();
   pdl_launch_dependents();
 }
 
@@ -184,25 +278,38 @@ template <int WT, bool DO2, bool DO3>
 cudaError_t launch_t(const void* W, int64_t N, int64_t K, int64_t ldw, uint8_t* c2, int64_t ld2, uint8_t* c3,
                      int64_t ld3, uint16_t* sc, int64_t lds, cudaStream_t s) {
   const int64_t G = K / 128;
-  const int64_t total = N * ((G + 9) / 10);
-  // exactly the resident CTAs: units are dealt out statically, so a CTA
+  const int64_t niters = (N * ((G + 4) / 5) + 2) / 3;  // unit triples, one per warp iteration
+  // exactly the resident CTAs: triples are dealt out statically, so a CTA
   // waiting for a second wave would leave the tail to few SMs
+  const size_t smem = (size_t)2 * kWarps * 32 * kLaneStage<WT>;
+  static std::atomic<bool> smem_set[64];  // the kernel's dynamic shared-memory limit, raised once per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!smem_set[dev].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(k_quantize_pack<WT, DO2, DO3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set[dev].store(true, std::memory_order_release);
+  }
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quantize_pack<WT, DO2, DO3>, kThreads, 0);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quantize_pack<WT, DO2, DO3>, kThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const int64_t cap = (int64_t)device_sm_count() * per_sm;
-  const int64_t grid = total < cap ? total : cap;
+  const int64_t want = (niters + kWarps - 1) / kWarps;
+  const int64_t grid = want < cap ? want : cap;
+  const int vec2 = (c2 != nullptr && (reinterpret_cast<uintptr_t>(c2) & 15u) == 0 && ld2 % 16 == 0) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
+  cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
   cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_quantize_pack<WT, DO2, DO3>, W, N, K, ldw, c2, ld2, c3, ld3, sc, lds);
+  return cudaLaunchKernelEx(&cfg, k_quantize_pack<WT, DO2, DO3>, W, N, K, ldw, c2, ld2, c3, ld3, sc, lds, vec2);
 }
 
 template <int WT>
