@@ -62,6 +62,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
                                                             uint16_t* __restrict__ scales, int64_t lds, int vec2) {
   constexpr int esize = WT == TQ_F32 ? 4 : 2;
   __shared__ __align__(16) uint32_t cw[kWarps][32 * 4 + 4];  // code words of the warp's lanes (+ one spare word)
+  // base-3 byte of every 10-bit window of five 2-bit codes c0 + 3 c1 + ... + 81 c4
+  // (windows holding a code 3 never occur)
+  __shared__ uint8_t b3[1024];
   // weights of two triples (dynamic: 72 KB for fp32 weights)
   extern __shared__ __align__(16) unsigned char qstage[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -78,6 +81,12 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
   const int64_t stride = (int64_t)gridDim.x * kWarps;
   uint32_t* const wbuf = cw[warp];
 
+  if constexpr (DO3) {
+    for (int i = threadIdx.x; i < 1024; i += kThreads)
+      b3[i] = (uint8_t)((i & 3) + 3 * ((i >> 2) & 3) + 9 * ((i >> 4) & 3) + 27 * ((i >> 6) & 3) + 81 * ((i >> 8) & 3));
+    __syncwarp();
+    __syncthreads();
+  }
   pdl_wait();
 
   // rows and units-in-row of the three units of triple `it` (one division)
@@ -205,12 +214,16 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
     const __half sh = __float2half_rn(mean);
     const float sc = __half2float(sh);
     const float half_s = sc * 0.5f;  // exact
-    // ---- ternarise: code c = t + 1 at bits 2 (j % 16) of word j / 16
+    // ---- ternarise: code c = t + 1 at bits 2 (j % 16) of word j / 16.
+    // c = [w > thr] + [not (w < -thr)] with thr = s/2 for a finite s > 0 and
+    // +inf otherwise: 2 above s/2, 0 below -s/2, 1 in between, at +-s/2
+    // exactly, for NaN and for every weight of a zero, infinite or NaN scale
+    // -- the compare rule above.
+    const float thr = (sc != 0.0f) ? half_s : __int_as_float(0x7f800000);
     uint32_t cwd[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int j = 0; j < 64; ++j) {
-      const float w = v[j];
-      const uint32_t c = (sc != 0.0f && fabsf(w) > half_s) ? (w > 0.0f ? 2u : 0u) : 1u;
+      const uint32_t c = (uint32_t)(v[j] > thr) + (uint32_t)!(v[j] < -thr);
       cwd[j >> 4] |= c << (2 * (j & 15));
     }
     if (ok) {
@@ -251,9 +264,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
         if (pos < nbytes3) {
           const int bit = 1280 * q + 10 * b;
           const uint32_t lo = wbuf[bit >> 5], hi = wbuf[(bit >> 5) + 1];
-          const uint32_t win = __funnelshift_r(lo, hi, bit & 31);
-          val = (win & 3u) + 3u * ((win >> 2) & 3u) + 9u * ((win >> 4) & 3u) + 27u * ((win >> 6) & 3u) +
-                81u * ((win >> 8) & 3u);
+          val = b3[__funnelshift_r(lo, hi, bit & 31) & 0x3ffu];
         }
         codes3[un * ld3 + pos] = (uint8_t)val;
       }
