@@ -173,7 +173,7 @@ TQ_API tq_status tq_gemm(const uint8_t *codes, int64_t ldc, int fmt, const uint1
 TQ_API tq_status tq_gemm_check_range(const void *workspace, tq_stream stream);
 
 /* Prefill GEMM that allocates nothing and needs no workspace argument.  The
- * paper has no counterpart; this entry exists for callers that cannot
+ * published method has no counterpart; this entry exists for callers that cannot
  * allocate device memory themselves (code that runs inside a fixed memory
  * pool or arena, or plugins that may only use the buffers their host hands
  * them).  It computes exactly what tq_gemm computes, with the same kernels,

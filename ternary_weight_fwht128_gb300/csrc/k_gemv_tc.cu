@@ -79,7 +79,9 @@ constexpr int kTmaWarp = 16;
 constexpr int kMmaWarp = 17;                  // warps 17, 18 issue the MMAs of team 0, 1
 constexpr int kEpiWarp0 = 19;                 // warps 19-22: epilogue
 constexpr int kThreads = 32 * 23;             // + 4 epilogue warps (19-22)
-constexpr int kRing = 4;                      // code slots in flight (four groups each; even: slot s % kRing is always team s % 2)
+// code slots in flight (four groups each); an even count, so that slot
+// s % kRing always belongs to team s % 2
+constexpr int kRing = 4;
 constexpr int kAbuf = 3;                      // weight (A) buffers in tensor memory, one stage each
 constexpr int kAPeriod = 2 * kAbuf;           // stages between two uses of one A buffer by one team
 static_assert(kAbuf % 2 == 1, "A buffers alternate between the two teams");
@@ -356,8 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* ring = smem;
-  constexpr int nring = kRing;
-  unsigned char* bsm = ring + nring * kSlotBytes;
+  unsigned char* bsm = ring + kRing * kSlotBytes;
   unsigned char* zero = bsm + p.groups_cap * Gm::kGroupB;
   float2* ztab = reinterpret_cast<float2*>(zero + kZeroBytes);
   float* ypart = reinterpret_cast<float*>(ztab + p.groups_cap * Gm::kZs);
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
 
   int issued_loads = 0;
   auto fill_ring = [&]() {
-    for (; issued_loads < S && issued_loads < nring; ++issued_loads) {
+    for (; issued_loads < S && issued_loads < kRing; ++issued_loads) {
       const int l = issued_loads, tile = l / nch, lc = l - tile * nch;
       mbar_arrive_expect_tx(&ctl->full[l], kSlotBytes);
       tma_load_2d(smem_u32(ring + l * kSlotBytes), &cmap, (int)((g0 + 4 * lc) * 32), (int)((t0 + tile) * 128),
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     }
   };
   if (threadIdx.x == 0) {
-    for (int i = 0; i < nring; ++i) {
+    for (int i = 0; i < kRing; ++i) {
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->empty[i], kTeamWarps);
     }
@@ -504,17 +505,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int l = issued_loads, slot = l % nring, use = l / nring, tile = l / (nch > 0 ? nch : 1), lc = l - tile * nch;
+      int l = issued_loads, slot = l % kRing, use = l / kRing, tile = l / (nch > 0 ? nch : 1), lc = l - tile * nch;
       for (; l < S; ++l) {
         if (!wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(&ctl->full[slot], kSlotBytes);
         tma_load_2d(smem_u32(ring + slot * kSlotBytes), &cmap, (int)((g0 + 4 * lc) * 32), (int)((t0 + tile) * 128),
                     &ctl->full[slot]);
-        if (++slot == nring) { slot = 0; ++use; }
+        if (++slot == kRing) { slot = 0; ++use; }
         if (++lc == nch) { lc = 0; ++tile; }
       }
       // loads issued but possibly never consumed: let them land before exit
-      for (int q = (l > nring ? l - nring : 0); q < l; ++q) (void)mbar_wait(&ctl->full[q % nring], (q / nring) & 1);
+      for (int q = (l > kRing ? l - kRing : 0); q < l; ++q) (void)mbar_wait(&ctl->full[q % kRing], (q / kRing) & 1);
     }
     __syncwarp();
   } else if (warp < kDecWarps) {
@@ -531,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     uint32_t off[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) off[q] = rbase + ((((uint32_t)(4 * gh + q)) ^ rx) << 4);
-    int slot = team, use = 0;  // ring slot of stage s and its use count (s % nring, s / nring)
+    int slot = team, use = 0;  // ring slot of stage s and its use count (s % kRing, s / kRing)
     for (int s = team; s < S; s += 2) {
       // A buffer ab last held stage s - kAbuf (the other team's), whose MMAs
       // are the ((s - kAbuf) / kAPeriod)-th completion a_free[ab][team] counts
@@ -564,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->a_full[ab][team]);
       slot += 2;
-      if (slot >= nring) { slot -= nring; ++use; }
+      if (slot >= kRing) { slot -= kRing; ++use; }
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------ MMA issue
@@ -788,18 +789,18 @@ EncodeTiledFn encode_fn() {
 }
 
 template <int V>
-size_t smem_bytes_v(int64_t groups_cap, int64_t tiles_cap, int64_t M, int ring) {
-  return 1024 + (size_t)ring * kSlotBytes + (size_t)groups_cap * Geo<V>::kGroupB + kZeroBytes +
+size_t smem_bytes_v(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
+  return 1024 + (size_t)kRing * kSlotBytes + (size_t)groups_cap * Geo<V>::kGroupB + kZeroBytes +
          (size_t)groups_cap * Geo<V>::kZs * sizeof(float2) + (size_t)tiles_cap * 128 * M * sizeof(float) +
          sizeof(Ctl);
 }
 
-size_t smem_bytes(int64_t groups_cap, int64_t tiles_cap, int64_t M, int ring = kRing) {
+size_t smem_bytes(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
   switch (variant_of(M)) {
-    case 1: return smem_bytes_v<1>(groups_cap, tiles_cap, M, ring);
-    case 2: return smem_bytes_v<2>(groups_cap, tiles_cap, M, ring);
-    case 3: return smem_bytes_v<3>(groups_cap, tiles_cap, M, ring);
-    default: return smem_bytes_v<4>(groups_cap, tiles_cap, M, ring);
+    case 1: return smem_bytes_v<1>(groups_cap, tiles_cap, M);
+    case 2: return smem_bytes_v<2>(groups_cap, tiles_cap, M);
+    case 3: return smem_bytes_v<3>(groups_cap, tiles_cap, M);
+    default: return smem_bytes_v<4>(groups_cap, tiles_cap, M);
   }
 }
 
