@@ -155,14 +155,20 @@ enum { TQ_GEMV_TENSOR_MEMORY = 1, TQ_GEMV_MMA_SYNC = 2 };
 TQ_API int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt);
 
 /* Bytes of caller-provided workspace tq_gemm needs for M x K activations:
- * the rotated activations in fp16 plus a status word. */
+ * a status word and the rotated activations in fp16 (256 + 2 M K bytes,
+ * rounded up to 256), then 16 MiB for the fp32 partial tiles of a last wave
+ * of tiles that the GEMM splits along K (see tq_gemm). */
 TQ_API size_t tq_gemm_workspace_bytes(int64_t M, int64_t K);
 
 /* Prefill GEMM, M >= 1 (tensor cores: tcgen05 MMA with fp16 operands and
  * fp32 accumulation in tensor memory):  same formula as tq_gemv.  Runs the
  * FWHT-128 of x into the workspace (fp16, overflow recorded in the status
- * word), then the GEMM, on `stream`.  fmt is TQ_PACK_2BIT.  ws_bytes must
- * be >= tq_gemm_workspace_bytes(M, K).  y must not overlap the inputs. */
+ * word), then the GEMM, on `stream`.  When the output tiles leave a short
+ * last wave on the GPU's SMs, those tiles are computed in K segments whose
+ * partial sums go to the workspace and are added in a fixed order by a second
+ * kernel (results are identical from call to call).  fmt is TQ_PACK_2BIT.
+ * ws_bytes must be >= tq_gemm_workspace_bytes(M, K).  y must not overlap the
+ * inputs. */
 TQ_API tq_status tq_gemm(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
                   int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
                   void *workspace, size_t ws_bytes, tq_stream stream);

@@ -23,6 +23,11 @@
 //   warp 9     allocates tensor memory and (one lane) issues the MMAs: per
 //              stage 2 (token halves) x 4 (K steps of 16) tcgen05.mma of
 //              128 x bn x 16 into two fp32 accumulators (256 columns apart).
+// When the tiles leave a last wave of few tiles (2048 x 5120 in 256-row tiles:
+// 160 tiles on 152 SMs), those tiles are split along K instead: each of their
+// K segments runs as a CTA of its own and writes its fp32 partial tile to the
+// workspace, and k_gemm_fixup adds the segments of every output in segment
+// order and writes y (deterministic; no atomics, no CTA waits for another).
 // Stages are handed over with mbarriers (TMA bytes, decoder arrivals, MMA
 // completion via tcgen05.commit).  Every wait is bounded in time; a wait that
 // runs out records bit 1 of the status word and the CTA winds down.
@@ -156,6 +161,9 @@ struct Params {
   int64_t ldy;
   uint32_t* flag;
   int n_tiles_m;
+  int n_main;      // blocks below n_main compute whole tiles 0 .. n_main - 1
+  int splits;      // K segments of each later tile (blocks n_main + u: tile n_main + u / splits)
+  float* part;     // their partial tiles, [unit][BM][bn] fp32
   int bn;          // weight rows per tile (multiple of 16, <= BN)
   uint32_t idesc;  // idesc_f16(bn)
   int vec_store;  // y 16-byte aligned and ldy % 4 == 0: rows can take 16-byte stores
@@ -176,10 +184,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(b_ring + kStages * kBStage);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_m = blockIdx.x % p.n_tiles_m, tile_n = blockIdx.x / p.n_tiles_m;
+  const int nk_all = (int)(p.K / BK);
+  // whole tile, or K segment [s0, s1) of a split tile (unit >= 0)
+  int tile = (int)blockIdx.x, s0 = 0, s1 = nk_all, unit = -1;
+  if (tile >= p.n_main) {
+    unit = tile - p.n_main;
+    tile = p.n_main + unit / p.splits;
+    const int seg = unit % p.splits;
+    s0 = nk_all * seg / p.splits;
+    s1 = nk_all * (seg + 1) / p.splits;
+  }
+  const int tile_m = tile % p.n_tiles_m, tile_n = tile / p.n_tiles_m;
   const int bn = p.bn;
   const int64_t m0 = (int64_t)tile_m * BM, n0 = (int64_t)tile_n * bn;
-  const int nk = (int)(p.K / BK);
+  const int nk = s1 - s0;  // stages of this CTA
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -212,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         const int slot = s % kStages, use = s / kStages;
         if (use > 0 && !wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl, p.flag)) break;
         mbar_arrive_expect_tx(&ctl->full_a[slot], kAStage);
-        tma_load_2d(smem_u32(a_ring + slot * kAStage), &xmap, s * BK, (int)m0, &ctl->full_a[slot]);
+        tma_load_2d(smem_u32(a_ring + slot * kAStage), &xmap, (s0 + s) * BK, (int)m0, &ctl->full_a[slot]);
       }
       // loads issued but possibly not consumed: let them land before exit
       for (int q = (s > kStages ? s - kStages : 0); q < s; ++q)
@@ -255,9 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     // codes and scales run two stages ahead of the decode, so their latency
     // hides behind two stages of MMA
     auto ld_codes = [&](int st) {
-      return (in_tile && st < nk) ? ldg_nc_u4(crow + st * (BK / 4)) : make_uint4(0, 0, 0, 0);
+      return (in_tile && st < nk) ? ldg_nc_u4(crow + (s0 + st) * (BK / 4)) : make_uint4(0, 0, 0, 0);
     };
-    auto ld_scale = [&](int st) { return (row_ok && st < nk) ? __ldg(srow + (st * BK) / 128) : (uint16_t)0; };
+    auto ld_scale = [&](int st) {
+      return (row_ok && st < nk) ? __ldg(srow + ((s0 + st) * BK) / 128) : (uint16_t)0;
+    };
     uint4 cur = ld_codes(0), nx1 = ld_codes(1);
     uint16_t scur = ld_scale(0), snx1 = ld_scale(1);
     for (int s = 0; s < nk; ++s) {
@@ -292,17 +312,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     (void)wait_or_abort(&ctl->done, 0, ctl, p.flag);
     tc_fence_after();
     const int quad = warp & 3, half = warp >> 2;  // TMEM lanes 32*quad.., accumulator half
-    const int64_t m = m0 + half * 128 + quad * 32 + lane;
-    const bool m_ok = m < p.M;
-    float* yrow = p.y + (m_ok ? m : 0) * p.ldy + n0;
-    const int ncols = (int)((p.N - n0) < bn ? (p.N - n0) : bn);
+    const int row = half * 128 + quad * 32 + lane;
+    const int64_t m = m0 + row;
+    // a K segment writes its whole partial tile; a whole tile writes y
+    const bool m_ok = unit >= 0 || m < p.M;
+    float* yrow = unit >= 0 ? p.part + ((int64_t)unit * BM + row) * bn : p.y + (m < p.M ? m : 0) * p.ldy + n0;
+    const bool vec = unit >= 0 || p.vec_store;
+    const int ncols = unit >= 0 ? bn : (int)((p.N - n0) < bn ? (p.N - n0) : bn);
 #pragma unroll 1
     for (int c0 = 0; c0 < ncols; c0 += 32) {
       __syncwarp();  // tcgen05.ld is warp-collective; the stores below diverge
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * BN + c0), v);
       if (m_ok && !ctl->abort) {
-        if (p.vec_store && c0 + 32 <= ncols) {
+        if (vec && c0 + 32 <= ncols) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(yrow + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
@@ -320,6 +343,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
   if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+  }
+  pdl_launch_dependents();
+}
+
+// y of the split tiles: output (tile, row, 4 columns) per thread, the sum of
+// its splits partials in segment order.
+__global__ void __launch_bounds__(256) k_gemm_fixup(const float* __restrict__ part, int n_main, int n_split_tiles,
+                                                   int splits, int n_tiles_m, int bn, int64_t M, int64_t N,
+                                                   float* __restrict__ y, int64_t ldy) {
+  pdl_wait();
+  const int c4 = bn / 4;
+  const int64_t total = (int64_t)n_split_tiles * BM * c4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int lt = (int)(i / ((int64_t)BM * c4));
+    const int rem = (int)(i - (int64_t)lt * BM * c4);
+    const int row = rem / c4, c = 4 * (rem - row * c4);
+    const int tile = n_main + lt;
+    const int64_t m = (int64_t)(tile % n_tiles_m) * BM + row, n = (int64_t)(tile / n_tiles_m) * bn + c;
+    if (m >= M || n >= N) continue;
+    const float* src = part + ((int64_t)lt * splits * BM + row) * bn + c;
+    float4 acc = *reinterpret_cast<const float4*>(src);
+    for (int q = 1; q < splits; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(src + (int64_t)q * BM * bn);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    float* dst = y + m * ldy + n;
+    dst[0] = acc.x;
+    if (n + 1 < N) dst[1] = acc.y;
+    if (n + 2 < N) dst[2] = acc.z;
+    if (n + 3 < N) dst[3] = acc.w;
   }
   pdl_launch_dependents();
 }
@@ -348,31 +404,54 @@ EncodeTiledFn encode_fn() {
 
 constexpr size_t kGemmSmem = (size_t)kStages * (kAStage + kBStage) + sizeof(SmemCtl) + 1024;
 
-// Weight rows per tile: the multiple of 16 in [64, 256] that minimises the
-// busiest SM's work, (waves of tiles over the SMs) x (bn + 96).  The 96 rows'
-// worth stands for what a stage costs whatever bn is -- streaming the
-// 256 x 64 x' tile from L2, which narrow tiles repeat more often -- and the
-// per-tile fill and drain; it is fitted to timings of the 27B shapes (256-row
-// tiles for 27648 x 5120, 144 for 5120-row matrices).  Ties go to the larger
-// tile.
-static int gemm_tile_rows(int64_t N, int64_t M) {
+// The launch shape: weight rows per tile (bn, a multiple of 16 in [64, 256])
+// and the K split of a short last wave.  Cost model of the busiest SM, in
+// units of one weight row's share of a tile: a tile costs bn + 96 (the 96
+// stand for what a stage costs whatever bn is -- streaming the 256 x 64 x'
+// tile, the hand-overs -- and the per-tile fill and drain; fitted to the 27B
+// shapes).  A last wave of L <= SMs / 2 tiles can instead run as L x S
+// K segments (S = SMs / L, at most kMaxSplitUnits units and what the
+// workspace holds), costing (bn + 96) / S plus an eighth of a tile for the
+// fix-up.  Ties go to the larger tile.
+struct GemmPlan {
+  int bn, n_main, splits;
+  int64_t tiles;
+};
+
+static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes) {
   const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 1;
-  const int64_t tm = (M + BM - 1) / BM;
-  int best = BN;
+  const int64_t tm = (M + BM - 1) / BM, nk = K / BK;
+  GemmPlan best{BN, 0, 0, 0};
   int64_t best_cost = -1;
   for (int bn = BN; bn >= 64; bn -= 16) {
-    const int64_t tiles = tm * ((N + bn - 1) / bn);
-    const int64_t cost = ((tiles + sms - 1) / sms) * (bn + 96);
+    const int64_t tiles = tm * ((N + bn - 1) / bn), c = 8 * (bn + 96);
+    const int64_t full = tiles / sms, L = tiles - full * sms;
+    int64_t cost = (full + (L > 0 ? 1 : 0)) * c, n_main = tiles, S = 0;
+    if (full >= 1 && L > 0 && 2 * L <= sms) {
+      int64_t sp = sms / L;
+      if (sp > nk) sp = nk;
+      if (sp > kMaxSplitUnits / L) sp = kMaxSplitUnits / L;
+      while (sp >= 2 && (size_t)(L * sp * BM * bn) * sizeof(float) > split_bytes) --sp;
+      if (sp >= 2) {
+        const int64_t split_cost = full * c + c / sp + c / 8;
+        if (split_cost < cost) {
+          cost = split_cost;
+          n_main = tiles - L;
+          S = sp;
+        }
+      }
+    }
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
-      best = bn;
+      best = GemmPlan{bn, (int)n_main, (int)S, tiles};
     }
   }
   return best;
 }
 
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
-                        const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, cudaStream_t s) {
+                        const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, void* split_ws,
+                        size_t split_bytes, cudaStream_t s) {
   if (N == 0 || M == 0) return cudaSuccess;
   if ((int64_t)device_max_smem_optin() < (int64_t)kGemmSmem) return cudaErrorNotSupported;
   EncodeTiledFn enc = encode_fn();
@@ -398,10 +477,15 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   p.ldy = ldy;
   p.flag = flag;
   p.n_tiles_m = (int)((M + BM - 1) / BM);
-  p.bn = gemm_tile_rows(N, M);
+  const GemmPlan g = gemm_plan(N, M, K, split_ws != nullptr ? split_bytes : 0);
+  p.bn = g.bn;
   p.idesc = idesc_f16(p.bn);
   p.vec_store = ((reinterpret_cast<uintptr_t>(y) & 15u) == 0 && ldy % 4 == 0) ? 1 : 0;
-  const int64_t tiles = (int64_t)p.n_tiles_m * ((N + p.bn - 1) / p.bn);
+  p.n_main = g.n_main;
+  p.splits = g.splits > 0 ? g.splits : 1;
+  p.part = static_cast<float*>(split_ws);
+  const int64_t n_split_tiles = g.tiles - g.n_main;
+  const int64_t tiles = g.n_main + n_split_tiles * g.splits;  // CTAs
   static std::atomic<bool> smem_set[64];  // the kernel's shared-memory limit, raised once per device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -420,7 +504,21 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_gemm_tc, map, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, map, p);
+  if (e != cudaSuccess || n_split_tiles == 0) return e;
+  // y of the split tiles: the partials added in segment order
+  const int64_t work = n_split_tiles * BM * (p.bn / 4);
+  const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 1;
+  int64_t blocks = (work + 255) / 256;
+  if (blocks > 4 * sms) blocks = 4 * sms;
+  cudaLaunchConfig_t fc = {};
+  fc.gridDim = dim3((unsigned)blocks);
+  fc.blockDim = dim3(256);
+  fc.stream = s;
+  fc.attrs = at;
+  fc.numAttrs = 1;  // programmatic serialisation: waits for the GEMM in pdl_wait
+  return cudaLaunchKernelEx(&fc, k_gemm_fixup, static_cast<const float*>(split_ws), g.n_main, (int)n_split_tiles,
+                            g.splits, p.n_tiles_m, p.bn, M, N, y, ldy);
 }
 
 }  // namespace tq

@@ -138,9 +138,15 @@ int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt) {
   return TQ_GEMV_MMA_SYNC;
 }
 
+namespace {
+// start of the split-partial area of a tq_gemm workspace (256-byte aligned)
+size_t gemm_split_offset(int64_t M, int64_t K) { return (256 + (size_t)M * (size_t)K * 2 + 255) / 256 * 256; }
+}  // namespace
+
 size_t tq_gemm_workspace_bytes(int64_t M, int64_t K) {
   if (M < 0 || K < 0) return 0;
-  return 256 + (size_t)M * (size_t)K * 2;
+  // status word, rotated activations (fp16), then the partial tiles of a K-split last wave
+  return gemm_split_offset(M, K) + tq::kGemmSplitBytes;
 }
 
 tq_status tq_gemm(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
@@ -165,7 +171,9 @@ tq_status tq_gemm(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* sc
   if (e != cudaSuccess) return TQ_ERR_CUDA;
   e = launch_fwht128(x, TQ_BF16, ldx, xrot, TQ_F16, K, M, K, true, flag, s);
   if (e != cudaSuccess) return from_cuda(e);
-  return from_cuda(launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, s));
+  unsigned char* split = static_cast<unsigned char*>(workspace) + gemm_split_offset(M, K);
+  return from_cuda(launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, split,
+                               ws_bytes - gemm_split_offset(M, K), s));
 }
 
 tq_status tq_gemm_check_range(const void* workspace, tq_stream stream) {

@@ -74,7 +74,8 @@ extern "C" TQ_API tq_status tq_gemm_noalloc(const uint8_t* codes, int64_t ldc, i
   // the array keeps the previous call's contents: clear the status word
   if (cudaMemsetAsync(flag, 0, sizeof(uint32_t), s) != cudaSuccess) return TQ_ERR_CUDA;
   cudaError_t e = launch_fwht128(x, TQ_BF16, ldx, xrot, TQ_F16, K, M, K, true, flag, s);
-  if (e == cudaSuccess) e = launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, s);
+  // no room for the partial tiles of a K-split last wave: whole tiles only
+  if (e == cudaSuccess) e = launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, nullptr, 0, s);
   if (e == cudaSuccess) return TQ_OK;
   if (e == cudaErrorNotSupported) {
     (void)cudaGetLastError();

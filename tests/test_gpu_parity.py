@@ -391,6 +391,29 @@ def test_gemm_full_size_sampled(orc, N, K):
     _gemm_case(orc, N, K, 2048, seed=N * 7 + K, rows=rows, out_cols=toks)
 
 
+def test_gemm_split_last_wave(orc):
+    """5120 weight rows in 256-row tiles x 8 token blocks make 160 tiles on
+    152 SMs; the last 8 (weight rows 4864..5119, every token) are computed
+    as K segments whose partial sums a second kernel adds in a fixed order.
+    Every output of those tiles is checked, plus rows of whole tiles, and a
+    second call gives the same bits."""
+    N, K, M = 5120, 1024, 2048
+    W = synth.weights(N, K, 61, dtype="bf16")
+    xb = synth.activations(M, K, 62)
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(xb)
+    ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    y0 = tq.gemm(c2, s, x, K, tq.TQ_PACK_2BIT, workspace=ws)
+    y1 = tq.gemm(c2, s, x, K, tq.TQ_PACK_2BIT, workspace=ws)
+    torch.cuda.synchronize()
+    tq.gemm_check_range(ws)
+    assert torch.equal(y0, y1)
+    rows = np.concatenate([np.arange(4864, 5120), np.array([0, 255, 256, 2500, 4863])])
+    T, S = orc.quantize(W, rows)
+    ref = orc.gemv(T, S, synth.bf16_bits_to_f32(xb))
+    check_y(y0.cpu().numpy()[:, rows], ref, "gemm y (split tiles)")
+
+
 def test_gemm_range_flag():
     """An activation block whose rotation exceeds the fp16 range is reported
     through the status word (tq_gemm_check_range -> TQ_ERR_RANGE)."""
