@@ -19,7 +19,10 @@
 //              swizzle, K-major) into the stage ring;
 //   warps 0-7  decode the bn x 64 weight tile from 2-bit codes straight into
 //              the same swizzled K-major layout (lane = weight row), then,
-//              after the last stage, drain tensor memory to y;
+//              after the last stage, drain tensor memory to y: 32 x 32 fp32
+//              blocks staged in the freed stage ring (128-byte swizzle) and
+//              written by TMA stores, so y leaves as whole 128-byte lines and
+//              the CTA does not wait for the writes to land;
 //   warp 9     allocates tensor memory and (one lane) issues the MMAs: per
 //              stage 2 (token halves) x 4 (K steps of 16) tcgen05.mma of
 //              128 x bn x 16 into two fp32 accumulators (256 columns apart).
@@ -55,6 +58,9 @@ constexpr int kThreads = 32 * 10;
 constexpr int kAStage = BM * BK * 2;  // 32 KB
 constexpr int kBStage = BN * BK * 2;  // 32 KB
 constexpr int kTmemCols = 512;
+constexpr int kOutBox = 32;                         // output block: 32 rows x 32 fp32 (128-byte rows)
+constexpr int kOutBlock = kOutBox * kOutBox * 4;    // 4 KB
+constexpr int kOutSlots = 4;                        // staged blocks in flight per warp
 constexpr uint32_t kFaultTimeout = 2u;  // status word bit
 
 struct SmemCtl {
@@ -67,6 +73,20 @@ struct SmemCtl {
 };
 
 // ---------------------------------------------------------------- PTX helpers
+
+// Bulk tensor store of a staged shared-memory block, and the waits on the
+// issuing thread's bulk groups (.read: the source may be reused).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -167,6 +187,8 @@ struct Params {
   int bn;          // weight rows per tile (multiple of 16, <= BN)
   uint32_t idesc;  // idesc_f16(bn)
   int vec_store;  // y 16-byte aligned and ldy % 4 == 0: rows can take 16-byte stores
+  int tma_y;      // ymap describes y (M x N fp32, row pitch ldy): blocks leave by TMA store
+  int tma_part;   // pmap describes the partial tiles ([unit * BM + row][bn] fp32)
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SmemCtl* ctl, uint32_t* flag) {
@@ -175,7 +197,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sm
   return false;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const Params p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
+              const __grid_constant__ CUtensorMap pmap, const Params p) {
   extern __shared__ unsigned char smem_raw[];
   // 1024-byte alignment (of the shared-window address) for the swizzled tiles
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -319,12 +343,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     float* yrow = unit >= 0 ? p.part + ((int64_t)unit * BM + row) * bn : p.y + (m < p.M ? m : 0) * p.ldy + n0;
     const bool vec = unit >= 0 || p.vec_store;
     const int ncols = unit >= 0 ? bn : (int)((p.N - n0) < bn ? (p.N - n0) : bn);
+    // TMA path: this warp's 32 rows leave as 32 x 32 blocks staged in its own
+    // 16 KB of the (now idle) stage ring; a block is written only where all 32
+    // of its columns belong to this tile (TMA clips rows >= M and columns >= N)
+    const bool tma = unit >= 0 ? p.tma_part != 0 : p.tma_y != 0;
+    const CUtensorMap* omap = unit >= 0 ? &pmap : &ymap;
+    const int64_t oy64 = unit >= 0 ? (int64_t)unit * BM + half * 128 + quad * 32 : m0 + half * 128 + quad * 32;
+    const bool rows_any = unit >= 0 || oy64 < p.M;  // warp-uniform
+    const int ox = unit >= 0 ? 0 : (int)n0, oy = (int)oy64;
+    unsigned char* stage = smem + warp * (kOutSlots * kOutBlock);
+    int issued = 0;
 #pragma unroll 1
     for (int c0 = 0; c0 < ncols; c0 += 32) {
       __syncwarp();  // tcgen05.ld is warp-collective; the stores below diverge
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * BN + c0), v);
-      if (m_ok && !ctl->abort) {
+      const bool aborted = __any_sync(0xffffffffu, ctl->abort != 0);
+      if (aborted) continue;
+      if (tma && c0 + kOutBox <= bn) {
+        if (!rows_any) continue;
+        unsigned char* buf = stage + (issued % kOutSlots) * kOutBlock;
+        if (issued >= kOutSlots) {  // the block staged kOutSlots ago has been read
+          if (lane == 0) bulk_wait_read<kOutSlots - 1>();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)  // row = lane, 16-byte chunk i at position i ^ (row % 8)
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+              make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+                         __float_as_uint(v[4 * i + 3]));
+        fence_async_smem();  // generic-proxy writes -> visible to the bulk copy
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(omap, ox + c0, oy, smem_u32(buf));
+          bulk_commit();
+        }
+        ++issued;
+      } else if (m_ok) {
         if (vec && c0 + 32 <= ncols) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
@@ -336,6 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         }
       }
     }
+    // staged blocks must be read out before the CTA's shared memory is released
+    if (lane == 0 && issued > 0) bulk_wait_read<0>();
+    __syncwarp();
   }
   tc_fence_before();
   __syncwarp();  // a warp reaches the block barrier whole (lanes may have diverged)
@@ -486,6 +544,19 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   p.part = static_cast<float*>(split_ws);
   const int64_t n_split_tiles = g.tiles - g.n_main;
   const int64_t tiles = g.n_main + n_split_tiles * g.splits;  // CTAs
+  // output maps: 32 x 32 fp32 boxes, 128-byte swizzle (the staging layout);
+  // where one cannot be made the kernel stores from registers instead
+  auto out_map = [&](CUtensorMap* m, void* base, int64_t cols, int64_t rows, int64_t pitch) {
+    const cuuint64_t od[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t os[1] = {(cuuint64_t)pitch * 4};
+    const cuuint32_t ob[2] = {kOutBox, kOutBox};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, od, os, ob, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  CUtensorMap ymap = map, pmap = map;
+  p.tma_y = (p.vec_store && M < (int64_t)1 << 31 && N < (int64_t)1 << 31 && out_map(&ymap, y, N, M, ldy)) ? 1 : 0;
+  p.tma_part = (n_split_tiles > 0 && out_map(&pmap, split_ws, p.bn, n_split_tiles * g.splits * BM, p.bn)) ? 1 : 0;
   static std::atomic<bool> smem_set[64];  // the kernel's shared-memory limit, raised once per device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -504,7 +575,7 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, map, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, map, ymap, pmap, p);
   if (e != cudaSuccess || n_split_tiles == 0) return e;
   // y of the split tiles: the partials added in segment order
   const int64_t work = n_split_tiles * BM * (p.bn / 4);

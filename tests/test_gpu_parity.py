@@ -391,6 +391,38 @@ def test_gemm_full_size_sampled(orc, N, K):
     _gemm_case(orc, N, K, 2048, seed=N * 7 + K, rows=rows, out_cols=toks)
 
 
+def test_gemm_row_pitch_and_ragged_edges(orc):
+    """y with a row pitch wider than N (the output blocks leave by TMA store):
+    the last weight tile and the last token block are ragged (N = 300 and
+    M = 300 against 64-column and 256-token tiles), and the pitch's padding
+    columns keep their poison bytes."""
+    N, K, M, pad = 300, 384, 300, 12
+    W = synth.weights(N, K, 71, dtype="bf16")
+    xb = synth.activations(M, K, 72)
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    raw = torch.empty((M, N + pad), dtype=torch.float32, device="cuda")
+    raw.view(torch.uint8).fill_(0x5A)
+    out = raw[:, :N]
+    ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    tq.gemm(c2, s, to_dev_bf16(xb), K, tq.TQ_PACK_2BIT, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    tail = raw[:, N:].contiguous().view(torch.uint8).cpu().numpy()
+    assert np.all(tail == 0x5A), "write into the row pitch's padding"
+    T, S = orc.quantize(W)
+    check_y(out.cpu().numpy(), orc.gemv(T, S, synth.bf16_bits_to_f32(xb)), "gemm y (row pitch)")
+
+
+def test_gemm_tile_width_not_multiple_of_32(orc):
+    """N = 152 x 208 weight rows at M = 256 fill 152 SMs with 208-row tiles:
+    the last 16 columns of every tile's output leave by plain stores, the
+    rest by TMA store.  Rows from both parts of every few tiles are checked."""
+    N, K, M = 152 * 208, 256, 256
+    rng = np.random.default_rng(83)
+    tiles = rng.choice(152, size=6, replace=False)
+    rows = np.sort(np.concatenate([t * 208 + np.array([0, 31, 191, 192, 200, 207]) for t in tiles]))
+    _gemm_case(orc, N, K, M, seed=81, rows=rows)
+
+
 def test_gemm_split_last_wave(orc):
     """5120 weight rows in 256-row tiles x 8 token blocks make 160 tiles on
     152 SMs; the last 8 (weight rows 4864..5119, every token) are computed
