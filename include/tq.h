@@ -156,7 +156,7 @@ TQ_API int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt);
 
 /* Bytes of caller-provided workspace tq_gemm needs for M x K activations:
  * a status word and the rotated activations in fp16 (256 + 2 M K bytes,
- * rounded up to 256), then 16 MiB for the fp32 partial tiles of a last wave
+ * rounded up to 256), then 40 MiB for the fp32 partial tiles of a last wave
  * of tiles that the GEMM splits along K (see tq_gemm). */
 TQ_API size_t tq_gemm_workspace_bytes(int64_t M, int64_t K);
 

@@ -27,7 +27,8 @@
 //              stage 2 (token halves) x 4 (K steps of 16) tcgen05.mma of
 //              128 x bn x 16 into two fp32 accumulators (256 columns apart).
 // When the tiles leave a last wave of few tiles (2048 x 5120 in 256-row tiles:
-// 160 tiles on 152 SMs), those tiles are split along K instead: each of their
+// 160 tiles on 152 SMs), those tiles are split along K instead (up to one
+// segment per SM): each of their
 // K segments runs as a CTA of its own and writes its fp32 partial tile to the
 // workspace, and k_gemm_fixup adds the segments of every output in segment
 // order and writes y (deterministic; no atomics, no CTA waits for another).
@@ -421,13 +422,22 @@ __global__ void __launch_bounds__(256) k_gemm_fixup(const float* __restrict__ pa
     const int64_t m = (int64_t)(tile % n_tiles_m) * BM + row, n = (int64_t)(tile / n_tiles_m) * bn + c;
     if (m >= M || n >= N) continue;
     const float* src = part + ((int64_t)lt * splits * BM + row) * bn + c;
+    const int64_t seg = (int64_t)BM * bn;
     float4 acc = *reinterpret_cast<const float4*>(src);
-    for (int q = 1; q < splits; ++q) {
-      const float4 v = *reinterpret_cast<const float4*>(src + (int64_t)q * BM * bn);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+    for (int q0 = 1; q0 < splits; q0 += 8) {  // loads of 8 segments in flight, added in segment order
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (q0 + j < splits) v[j] = *reinterpret_cast<const float4*>(src + (q0 + j) * seg);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (q0 + j < splits) {
+          acc.x += v[j].x;
+          acc.y += v[j].y;
+          acc.z += v[j].z;
+          acc.w += v[j].w;
+        }
+      }
     }
     float* dst = y + m * ldy + n;
     dst[0] = acc.x;
@@ -464,17 +474,22 @@ constexpr size_t kGemmSmem = (size_t)kStages * (kAStage + kBStage) + sizeof(Smem
 
 // The launch shape: weight rows per tile (bn, a multiple of 16 in [64, 256])
 // and the K split of a short last wave.  Cost model of the busiest SM, in
-// units of one weight row's share of a tile: a tile costs bn + 96 (the 96
-// stand for what a stage costs whatever bn is -- streaming the 256 x 64 x'
-// tile, the hand-overs -- and the per-tile fill and drain; fitted to the 27B
-// shapes).  A last wave of L <= SMs / 2 tiles can instead run as L x S
-// K segments (S = SMs / L, at most kMaxSplitUnits units and what the
-// workspace holds), costing (bn + 96) / S plus an eighth of a tile for the
-// fix-up.  Ties go to the larger tile.
+// 1/352 of one 64-k stage of a 256-row tile: a stage of a bn-row tile costs
+// bn + 96 (the 96 stand for what a stage costs whatever bn is -- streaming
+// the 256 x 64 x' tile, the hand-overs; fitted to the 27B shapes) and a tile
+// adds kFillStages stages' worth of pipeline fill and output drain.  A last
+// wave of L <= SMs / 2 tiles can instead run as L x S K segments (S <= SMs /
+// L, at most kMaxSplitUnits units and what the workspace holds), costing
+// ceil(nk / S) + kFillStages stages plus the fix-up: a launch (2.5 stages'
+// worth) and reading the L x S partial tiles (a 256 x 256 partial tile: 1/32
+// of a stage's worth).  A narrower tile replaces a wider one only when it is
+// more than 1 % cheaper.
 struct GemmPlan {
   int bn, n_main, splits;
   int64_t tiles;
 };
+
+constexpr int64_t kFillStages = 4;
 
 static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes) {
   const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 1;
@@ -482,16 +497,16 @@ static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes) {
   GemmPlan best{BN, 0, 0, 0};
   int64_t best_cost = -1;
   for (int bn = BN; bn >= 64; bn -= 16) {
-    const int64_t tiles = tm * ((N + bn - 1) / bn), c = 8 * (bn + 96);
+    const int64_t tiles = tm * ((N + bn - 1) / bn), w = bn + 96, c = (nk + kFillStages) * w;
     const int64_t full = tiles / sms, L = tiles - full * sms;
     int64_t cost = (full + (L > 0 ? 1 : 0)) * c, n_main = tiles, S = 0;
     if (full >= 1 && L > 0 && 2 * L <= sms) {
-      int64_t sp = sms / L;
-      if (sp > nk) sp = nk;
-      if (sp > kMaxSplitUnits / L) sp = kMaxSplitUnits / L;
-      while (sp >= 2 && (size_t)(L * sp * BM * bn) * sizeof(float) > split_bytes) --sp;
-      if (sp >= 2) {
-        const int64_t split_cost = full * c + c / sp + c / 8;
+      int64_t sp_max = sms / L;
+      if (sp_max > nk) sp_max = nk;
+      if (sp_max > kMaxSplitUnits / L) sp_max = kMaxSplitUnits / L;
+      for (int64_t sp = 2; sp <= sp_max; ++sp) {
+        if ((size_t)(L * sp * BM * bn) * sizeof(float) > split_bytes) break;
+        const int64_t split_cost = full * c + ((nk + sp - 1) / sp + kFillStages) * w + 880 + 11 * L * sp * bn / 256;
         if (split_cost < cost) {
           cost = split_cost;
           n_main = tiles - L;
@@ -499,7 +514,7 @@ static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes) {
         }
       }
     }
-    if (best_cost < 0 || cost < best_cost) {
+    if (best_cost < 0 || cost * 100 < best_cost * 99) {
       best_cost = cost;
       best = GemmPlan{bn, (int)n_main, (int)S, tiles};
     }

@@ -42,8 +42,8 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* sc
 // one CTA can have.
 // split_ws (may be null): room for the fp32 partial tiles of a K-split last
 // wave (up to kMaxSplitUnits tiles of 256 x 256), split_bytes long.
-constexpr int64_t kMaxSplitUnits = 64;
-constexpr size_t kGemmSplitBytes = (size_t)kMaxSplitUnits * 256 * 256 * sizeof(float);  // 16 MiB
+constexpr int64_t kMaxSplitUnits = 160;  // one segment per SM on up to 160 SMs
+constexpr size_t kGemmSplitBytes = (size_t)kMaxSplitUnits * 256 * 256 * sizeof(float);  // 40 MiB
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
                         const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, void* split_ws,
                         size_t split_bytes, cudaStream_t s);

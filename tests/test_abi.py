@@ -57,9 +57,9 @@ def test_packed_ld(L):
 
 
 def test_gemm_workspace_bytes(L):
-    # status word + fp16 rotated activations (rounded to 256 B) + 16 MiB of split partial tiles
-    assert tq.gemm_workspace_bytes(2048, 5120) == 256 + 2048 * 5120 * 2 + 64 * 256 * 256 * 4
-    assert tq.gemm_workspace_bytes(3, 128) == 1024 + 64 * 256 * 256 * 4
+    # status word + fp16 rotated activations (rounded to 256 B) + 40 MiB of split partial tiles
+    assert tq.gemm_workspace_bytes(2048, 5120) == 256 + 2048 * 5120 * 2 + 160 * 256 * 256 * 4
+    assert tq.gemm_workspace_bytes(3, 128) == 1024 + 160 * 256 * 256 * 4
     assert tq.gemm_workspace_bytes(-1, 5) == 0
 
 

@@ -426,10 +426,11 @@ def test_gemm_tile_width_not_multiple_of_32(orc):
 def test_gemm_split_last_wave(orc):
     """5120 weight rows in 256-row tiles x 8 token blocks make 160 tiles on
     152 SMs; the last 8 (weight rows 4864..5119, every token) are computed
-    as K segments whose partial sums a second kernel adds in a fixed order.
-    Every output of those tiles is checked, plus rows of whole tiles, and a
-    second call gives the same bits."""
-    N, K, M = 5120, 1024, 2048
+    as K segments (at K = 2048: 11 segments of 2 or 3 stages on 152 SMs)
+    whose partial sums a second kernel adds in a fixed order.  Every output
+    of those tiles is checked, plus rows of whole tiles, and a second call
+    gives the same bits."""
+    N, K, M = 5120, 2048, 2048
     W = synth.weights(N, K, 61, dtype="bf16")
     xb = synth.activations(M, K, 62)
     c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
