@@ -40,7 +40,7 @@ __device__ __forceinline__ void unpack8(const Raw<XT>& r, float v[8]) {
 // (the order in which the tensor-core GEMM unpacks its weight codes, see
 // k_gemm.cu).  Lane p holds elements 8(p&1) .. 8(p&1)+7 of chunk p/2; the two
 // lanes of a chunk swap four values so each writes 8 interleaved slots.
-// FLAG: record fp16 overflow in *flag.
+// With PERM16 (the GEMM pre-pass), fp16 overflow is recorded in *flag.
 template <int YT, bool PERM16>
 __device__ __forceinline__ void store8(void* y, int64_t off, int p, const float v[8], uint32_t* flag, bool valid) {
   if constexpr (YT == TQ_F32) {
@@ -56,14 +56,13 @@ __device__ __forceinline__ void store8(void* y, int64_t off, int p, const float 
     uint32_t h[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) h[j] = pack_half2(v[2 * j], v[2 * j + 1]);
-    if (flag != nullptr && valid) {
-      bool bad = false;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __half2 hh = *reinterpret_cast<const __half2*>(&h[j]);
-        bad |= (__hisinf(__low2half(hh)) != 0) | (__hisinf(__high2half(hh)) != 0);
-      }
-      if (bad) atomicOr(flag, 1u);
+    if (PERM16 && flag != nullptr && valid) {
+      // round-to-nearest-even gives an fp16 infinity exactly from |v| >= 65520
+      // (the midpoint between 65504 and 2^16 rounds to the even 2^16); NaN
+      // is not an overflow, and fmaxf passes over it
+      const float amax = fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+                               fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+      if (amax >= 65520.0f) atomicOr(flag, 1u);
     }
     uint16_t* yp = static_cast<uint16_t*>(y) + off;
     if constexpr (PERM16) {
@@ -172,6 +171,7 @@ cudaError_t launch_fwht128(const void* x, int xt, int64_t ldx, void* y, int yt, 
   const int64_t G = K / 128;
   if (rows == 0 || G == 0) return cudaSuccess;
   if (perm16) return launch_t<TQ_BF16, TQ_F16, true>(x, ldx, y, ldy, rows, G, flag, s);
+  flag = nullptr;  // overflow is recorded by the pre-pass form only
   if (xt == TQ_F32) {
     if (yt == TQ_F32) return launch_t<TQ_F32, TQ_F32, false>(x, ldx, y, ldy, rows, G, flag, s);
     if (yt == TQ_BF16) return launch_t<TQ_F32, TQ_BF16, false>(x, ldx, y, ldy, rows, G, flag, s);

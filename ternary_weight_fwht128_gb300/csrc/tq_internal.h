@@ -14,6 +14,9 @@ namespace tq {
 int device_sm_count();
 int device_max_smem_optin();
 
+// Block FWHT-128 of `rows` rows of x into y.  perm16: the GEMM pre-pass form
+// (bf16 -> fp16 in the GEMM's k order inside each 16-element chunk), which
+// ORs 1 into *flag when an output overflows fp16; the other forms ignore flag.
 cudaError_t launch_fwht128(const void* x, int xt, int64_t ldx, void* y, int yt, int64_t ldy, int64_t rows,
                            int64_t K, bool perm16, uint32_t* flag, cudaStream_t s);
 
