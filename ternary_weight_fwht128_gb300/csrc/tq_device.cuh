@@ -40,34 +40,84 @@ __device__ __forceinline__ void fwht128_lane(float v[4], int lane) {
   for (int j = 0; j < 4; ++j) v[j] = __fmul_rn(v[j], kInvSqrt128);
 }
 
+// Two fp32 lanes in one 64-bit register pair, and the paired (f32x2)
+// arithmetic on them: each half is rounded as the scalar operation would be.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t p, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // FWHT-128 on half a warp: lane l holds elements 8p .. 8p+7 (p = l & 15) of
 // the block of its half-warp (l >> 4), so one warp rotates two blocks.
 // Stages h = 1, 2, 4 stay inside a lane; stages h = 8 .. 64 pair lane l with
 // lane l ^ (h / 8), never crossing the half-warp.  Bit-identical to the
-// staged definition, like fwht128_lane.
+// staged definition, like fwht128_lane.  Elements 2i and 2i + 1 travel as one
+// f32x2 pair, so every stage but h = 1 takes one paired instruction per two
+// elements.
 __device__ __forceinline__ void fwht128_x8(float v[8], int lane) {
+  // h = 1: inside each pair
 #pragma unroll
-  for (int h = 1; h < 8; h <<= 1) {
+  for (int j = 0; j < 8; j += 2) {
+    const float a = v[j], b = v[j + 1];
+    v[j] = a + b;
+    v[j + 1] = a - b;
+  }
+  uint64_t q[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if ((j & h) == 0) {
-        const float a = v[j], b = v[j + h];
-        v[j] = a + b;
-        v[j + h] = a - b;
+  for (int i = 0; i < 4; ++i) q[i] = f2_pack(v[2 * i], v[2 * i + 1]);
+  // h = 2, 4: pair i with pair i ^ (h / 2)
+#pragma unroll
+  for (int hp = 1; hp < 4; hp <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if ((i & hp) == 0) {
+        const uint64_t a = q[i], b = q[i + hp];
+        q[i] = f2_add(a, b);
+        q[i + hp] = f2_sub(a, b);
       }
     }
   }
+  // h = 8 .. 64 across lanes: the upper lane of a butterfly keeps o - v, the
+  // lower v + o (one fma with a +-1 multiplier, exact like the add)
 #pragma unroll
   for (int m = 1; m < 16; m <<= 1) {
     const float sgn = (lane & m) ? -1.0f : 1.0f;
+    const uint64_t sg = f2_pack(sgn, sgn);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float o = __shfl_xor_sync(kFull, v[j], m);
-      v[j] = __fmaf_rn(sgn, v[j], o);
+    for (int i = 0; i < 4; ++i) {
+      float lo, hi;
+      f2_unpack(q[i], lo, hi);
+      const float olo = __shfl_xor_sync(kFull, lo, m), ohi = __shfl_xor_sync(kFull, hi, m);
+      q[i] = f2_fma(sg, q[i], f2_pack(olo, ohi));
     }
   }
+  const uint64_t sc = f2_pack(kInvSqrt128, kInvSqrt128);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], kInvSqrt128);
+  for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(q[i], sc), v[2 * i], v[2 * i + 1]);
 }
 
 // Eight consecutive bf16 (as a 128-bit word) -> fp32.
