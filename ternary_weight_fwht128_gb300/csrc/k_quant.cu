@@ -4,7 +4,8 @@
 // pair holds elements 64h .. 64h + 63 of the group in registers:
 //   1. 16-byte loads (8 for bf16, 16 for fp32);
 //   2. the staged FWHT-128 in fp32: stages h = 1 .. 32 inside the lane, stage
-//      64 across the pair (one shuffle per element), then * c;
+//      64 across the pair (one shuffle per element), then * c -- from stage 2
+//      on in f32x2 pairs;
 //   3. sum |w'| in the halving-tree order h = 64, 32, ..., 1.  At each level
 //      the pair holds the 2P partial sums of the level before (P per lane)
 //      and splits the P new sums between its lanes, so each sum is one
@@ -151,27 +152,40 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
         bf16x8_to_f32(r.w[i], &v[8 * i]);
       }
     }
-    // ---- FWHT-128: stages 1 .. 32 in the lane, 64 across the pair, then * c
+    // ---- FWHT-128: stages 1 .. 32 in the lane, 64 across the pair, then * c.
+    // Elements 2i and 2i + 1 travel as one f32x2 pair from stage 2 on (each
+    // half rounds as the scalar operation, so the stages are unchanged).
 #pragma unroll
-    for (int hs = 1; hs < 64; hs <<= 1) {
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        if (j & hs) continue;
-        const float a = v[j], b = v[j + hs];
-        v[j] = __fadd_rn(a, b);
-        v[j + hs] = __fsub_rn(a, b);
-      }
+    for (int j = 0; j < 64; j += 2) {
+      const float a = v[j], b = v[j + 1];
+      v[j] = __fadd_rn(a, b);
+      v[j + 1] = __fsub_rn(a, b);
     }
     {
-      const float sgn = h ? -1.0f : 1.0f;  // lower half: own + other; upper half: other - own
+      uint64_t q[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float o = __shfl_xor_sync(kFull, v[j], 1);
-        v[j] = __fmaf_rn(sgn, v[j], o);
+      for (int i = 0; i < 32; ++i) q[i] = f2_pack(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+      for (int hp = 1; hp < 32; hp <<= 1) {  // element stride 2 hp = 2 .. 32
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i & hp) continue;
+          const uint64_t a = q[i], b = q[i + hp];
+          q[i] = f2_add(a, b);
+          q[i + hp] = f2_sub(a, b);
+        }
+      }
+      // lower half: own + other; upper half: other - own
+      const float sgn = h ? -1.0f : 1.0f;
+      const uint64_t sg = f2_pack(sgn, sgn), c2 = f2_pack(kInvSqrt128, kInvSqrt128);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float lo, hi;
+        f2_unpack(q[i], lo, hi);
+        const float olo = __shfl_xor_sync(kFull, lo, 1), ohi = __shfl_xor_sync(kFull, hi, 1);
+        f2_unpack(f2_mul(f2_fma(sg, q[i], f2_pack(olo, ohi)), c2), v[2 * i], v[2 * i + 1]);
       }
     }
-#pragma unroll
-    for (int j = 0; j < 64; ++j) v[j] = __fmul_rn(v[j], kInvSqrt128);
     // ---- sum |w'|: halving tree h = 64 .. 1, each level's sums split over the pair
     float t32[32];
 #pragma unroll
