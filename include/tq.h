@@ -26,7 +26,8 @@
  *   codes2 [N][ld2]   2-bit codes: code = t + 1 in bits 2*(k%4) of byte k/4
  *   codes3 [N][ld3]   base-3 bytes: byte j = sum_{i<5} (t[5j+i] + 1) * 3^i;
  *                     trits past K count as t = 0; bytes from ceil(K/5)
- *                     to ld3 are written as 0
+ *                     to tq_packed_ld(K, TQ_PACK_BASE3) are written as 0,
+ *                     bytes past that (up to ld3) are not touched
  *
  * Every call:
  *   - takes DEVICE pointers owned by the caller (except where noted) and

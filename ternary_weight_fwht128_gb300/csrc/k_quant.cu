@@ -23,7 +23,7 @@
 //      base-3 digits: a warp takes three units of five groups (640 trits =
 //      128 bytes each, so units never share a byte; lanes 30, 31 idle), puts
 //      its code words in shared memory, and each lane forms 12 of the warp's
-//      384 base-3 bytes from 10-bit windows of them.
+//      384 base-3 bytes (three 32-bit words) from 10-bit windows of them.
 //
 // The pass reads 2 or 4 bytes per weight and should be bound by HBM: each warp
 // copies the next unit triple's weights into shared memory (cp.async, no
@@ -60,7 +60,8 @@ template <int WT, bool DO2, bool DO3>
 __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __restrict__ W, int64_t N, int64_t K,
                                                             int64_t ldw, uint8_t* __restrict__ codes2, int64_t ld2,
                                                             uint8_t* __restrict__ codes3, int64_t ld3,
-                                                            uint16_t* __restrict__ scales, int64_t lds, int vec2) {
+                                                            uint16_t* __restrict__ scales, int64_t lds, int vec2,
+                                                            int vec3) {
   constexpr int esize = WT == TQ_F32 ? 4 : 2;
   __shared__ __align__(16) uint32_t cw[kWarps][32 * 4 + 4];  // code words of the warp's lanes (+ one spare word)
   // base-3 byte of every 10-bit window of five 2-bit codes c0 + 3 c1 + ... + 81 c4
@@ -263,24 +264,38 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
         reinterpret_cast<uint4*>(wbuf)[lane] = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
       }
       __syncwarp();
+      // Each lane forms three 32-bit words of the triple's 384 bytes (bytes
+      // 12 lane .. 12 lane + 11): a word never straddles two units (128 bytes
+      // each), and its four bytes take their 10-bit windows from three
+      // consecutive code words.
       const int64_t U0 = 3 * it;
 #pragma unroll
-      for (int m = 0; m < 12; ++m) {
-        const int B = 12 * lane + m;  // byte of the triple's 384
+      for (int m4 = 0; m4 < 3; ++m4) {
+        const int B = 12 * lane + 4 * m4;  // first byte of the word, of the triple's 384
         const int q = B >> 7, b = B & 127;
-        const int64_t U = U0 + q;
-        if (U >= nunits) continue;
+        if (U0 + q >= nunits) continue;
         const int64_t un = q == 0 ? tri.n[0] : (q == 1 ? tri.n[1] : tri.n[2]);
         const int64_t uu = q == 0 ? tri.u[0] : (q == 1 ? tri.u[1] : tri.u[2]);
-        const int64_t pos = uu * 128 + b;  // byte of the row
-        if (pos >= ld3min) continue;        // past the row's zero padding
-        uint32_t val = 0;
-        if (pos < nbytes3) {
-          const int bit = 1280 * q + 10 * b;
-          const uint32_t lo = wbuf[bit >> 5], hi = wbuf[(bit >> 5) + 1];
-          val = b3[__funnelshift_r(lo, hi, bit & 31) & 0x3ffu];
+        const int64_t pos = uu * 128 + b;  // byte of the row (a multiple of 4)
+        if (pos >= ld3min) continue;        // past the row's zero padding (ld3min % 16 == 0)
+        const int bit0 = 1280 * q + 10 * b;
+        const uint32_t w0 = wbuf[bit0 >> 5], w1 = wbuf[(bit0 >> 5) + 1], w2 = wbuf[(bit0 >> 5) + 2];
+        uint32_t word = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (pos + k < nbytes3) {
+            const int sh = (bit0 & 31) + 10 * k;  // 0 .. 61
+            const uint32_t win = sh < 32 ? __funnelshift_r(w0, w1, sh) : __funnelshift_r(w1, w2, sh - 32);
+            word |= (uint32_t)b3[win & 0x3ffu] << (8 * k);
+          }
         }
-        codes3[un * ld3 + pos] = (uint8_t)val;
+        uint8_t* dst = codes3 + un * ld3 + pos;
+        if (vec3) {
+          *reinterpret_cast<uint32_t*>(dst) = word;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[k] = (uint8_t)(word >> (8 * k));
+        }
       }
     }
   };
@@ -324,6 +339,7 @@ cudaError_t launch_t(const void* W, int64_t N, int64_t K, int64_t ldw, uint8_t* 
   const int64_t want = (niters + kWarps - 1) / kWarps;
   const int64_t grid = want < cap ? want : cap;
   const int vec2 = (c2 != nullptr && (reinterpret_cast<uintptr_t>(c2) & 15u) == 0 && ld2 % 16 == 0) ? 1 : 0;
+  const int vec3 = (c3 != nullptr && (reinterpret_cast<uintptr_t>(c3) & 3u) == 0 && ld3 % 4 == 0) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(grid > 0 ? grid : 1));
   cfg.blockDim = dim3(kThreads);
@@ -334,7 +350,8 @@ cudaError_t launch_t(const void* W, int64_t N, int64_t K, int64_t ldw, uint8_t* 
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_quantize_pack<WT, DO2, DO3>, W, N, K, ldw, c2, ld2, c3, ld3, sc, lds, vec2);
+  return cudaLaunchKernelEx(&cfg, k_quantize_pack<WT, DO2, DO3>, W, N, K, ldw, c2, ld2, c3, ld3, sc, lds, vec2,
+                            vec3);
 }
 
 template <int WT>

@@ -131,6 +131,30 @@ def test_quantize_guard_bytes(orc):
     assert np.array_equal(c3.cpu().numpy(), orc.pack3(T))
 
 
+@pytest.mark.parametrize("extra", [3, 16])
+def test_quantize_base3_row_pitch(orc, extra):
+    """Base-3 rows with a pitch past the padded length: 4-byte stores where
+    the pitch allows them (extra = 16), byte stores otherwise (extra = 3).
+    Bytes up to the padded length match the oracle; the rest of each row
+    keeps its poison."""
+    N, K = 37, 1920  # 384 base-3 bytes per row: three units of 128
+    W = synth.weights(N, K, 91, dtype="bf16")
+    ld3min = tq.packed_ld(K, tq.TQ_PACK_BASE3)
+    ld3 = ld3min + extra
+    c3, ck3 = guarded((N, ld3), torch.uint8)
+    s = torch.empty(N, K // 128, dtype=torch.int16, device="cuda")
+    st = tq.lib().tq_quantize_pack(to_dev_bf16(W).data_ptr(), tq.TQ_BF16, N, K, K, tq.TQ_PACK_BASE3,
+                                   None, 0, c3.data_ptr(), ld3, s.data_ptr(), K // 128,
+                                   torch.cuda.current_stream().cuda_stream)
+    assert st == tq.TQ_OK
+    torch.cuda.synchronize()
+    ck3()
+    got = c3.cpu().numpy()
+    T, _ = orc.quantize(W)
+    assert np.array_equal(got[:, :ld3min], orc.pack3(T))
+    assert np.all(got[:, ld3min:] == 0x5A), "write past the padded row"
+
+
 # ----------------------------------------------------------------- GEMV
 
 def _gemv_case(orc, N, K, M, seed, fmt=tq.TQ_PACK_2BIT, rows=None):
