@@ -6,11 +6,11 @@
 //   2. the staged FWHT-128 in fp32: stages h = 1 .. 32 inside the lane, stage
 //      64 across the pair (one shuffle per element), then * c -- from stage 2
 //      on in f32x2 pairs;
-//   3. sum |w'| in the halving-tree order h = 64, 32, ..., 1.  At each level
-//      the pair holds the 2P partial sums of the level before (P per lane)
-//      and splits the P new sums between its lanes, so each sum is one
-//      shuffle and one addition; an IEEE sum does not depend on the order of
-//      its two operands, so the tree is the oracle's bit for bit;
+//   3. sum |w'| in the halving-tree order h = 64, 32, ..., 1.  Level 64
+//      adds each element to the partner lane's (one shuffle per element);
+//      both lanes form every sum, which gives both the same bits since an
+//      IEEE sum does not depend on the order of its two operands; levels
+//      32 .. 1 run inside the lane.  The tree is the oracle's bit for bit;
 //   4. mean = sum * 2^-7, scale = fp16_RN(mean) (absmean, mhpq.cn/news/1159370
 //      sec. 1.1; one fp16 scale per 128 weights, sec. 1.3);
 //   5. t = sign(w') * [|w'| > s/2] for a finite s > 0, t = 0 when s == 0.
@@ -187,44 +187,31 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
         f2_unpack(f2_mul(f2_fma(sg, q[i], f2_pack(olo, ohi)), c2), v[2 * i], v[2 * i + 1]);
       }
     }
-    // ---- sum |w'|: halving tree h = 64 .. 1, each level's sums split over the pair
-    float t32[32];
+    // ---- sum |w'|: halving tree h = 64 .. 1.  Both lanes of the pair form
+    // every sum (an IEEE sum does not depend on the order of its two
+    // operands, so the lanes hold the same bits): h = 64 pairs each element
+    // with the partner lane's, h = 32 .. 1 run inside the lane, from h = 32
+    // on in f32x2 pairs (sums 2i, 2i + 1).
+    uint64_t t16[16];  // the 32 sums of level h = 32
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-      const float lo = fabsf(v[jj]), hi = fabsf(v[32 + jj]);
-      const float mine = h ? hi : lo, send = h ? lo : hi;
-      t32[jj] = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
-    }
-    float t16[16];
+    for (int i = 0; i < 16; ++i) {
+      float a[2], b[2];
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
-      const float mine = h ? t32[16 + jj] : t32[jj], send = h ? t32[jj] : t32[16 + jj];
-      t16[jj] = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
+      for (int e = 0; e < 2; ++e) {
+        const int j = 2 * i + e;
+        a[e] = __fadd_rn(fabsf(v[j]), fabsf(__shfl_xor_sync(kFull, v[j], 1)));            // level 64, sum j
+        b[e] = __fadd_rn(fabsf(v[32 + j]), fabsf(__shfl_xor_sync(kFull, v[32 + j], 1)));  // level 64, sum 32 + j
+      }
+      t16[i] = f2_add(f2_pack(a[0], a[1]), f2_pack(b[0], b[1]));
     }
-    float t8[8];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const float mine = h ? t16[8 + jj] : t16[jj], send = h ? t16[jj] : t16[8 + jj];
-      t8[jj] = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
-    }
-    float t4[4];
+    for (int hp = 8; hp >= 1; hp >>= 1) {  // levels 16, 8, 4, 2
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const float mine = h ? t8[4 + jj] : t8[jj], send = h ? t8[jj] : t8[4 + jj];
-      t4[jj] = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
+      for (int i = 0; i < hp; ++i) t16[i] = f2_add(t16[i], t16[i + hp]);
     }
-    float t2[2];
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-      const float mine = h ? t4[2 + jj] : t4[jj], send = h ? t4[jj] : t4[2 + jj];
-      t2[jj] = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
-    }
-    float t1;
-    {
-      const float mine = h ? t2[1] : t2[0], send = h ? t2[0] : t2[1];
-      t1 = __fadd_rn(mine, __shfl_xor_sync(kFull, send, 1));
-    }
-    const float sum = __fadd_rn(t1, __shfl_xor_sync(kFull, t1, 1));  // h = 1: the same bits in both lanes
+    float s0, s1;
+    f2_unpack(t16[0], s0, s1);
+    const float sum = __fadd_rn(s0, s1);  // level 1
     const float mean = __fmul_rn(sum, 0.0078125f);
     const __half sh = __float2half_rn(mean);
     const float sc = __half2float(sh);
