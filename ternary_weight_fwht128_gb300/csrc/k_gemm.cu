@@ -12,9 +12,8 @@
 // sum in an epilogue, without per-group accumulator traffic).
 //
 // One CTA computes a 256 (tokens) x bn (weight rows) tile, K in stages of 64;
-// bn (a multiple of 16, at most 256) is chosen per shape so that the tiles
-// fill the SMs in whole waves (two 256-row tiles of a 5120-row matrix would
-// otherwise leave a second wave of 8 tiles on 152 SMs):
+// bn (a multiple of 16, at most 256) and the K split of a short last wave
+// come from a cost model of the busiest SM (gemm_plan):
 //   warp 8     (one lane) TMA-loads the 256 x 64 fp16 tile of x' (128-byte
 //              swizzle, K-major) into the stage ring;
 //   warps 0-7  decode the bn x 64 weight tile from 2-bit codes straight into
@@ -28,10 +27,10 @@
 //              128 x bn x 16 into two fp32 accumulators (256 columns apart).
 // When the tiles leave a last wave of few tiles (2048 x 5120 in 256-row tiles:
 // 160 tiles on 152 SMs), those tiles are split along K instead (up to one
-// segment per SM): each of their
-// K segments runs as a CTA of its own and writes its fp32 partial tile to the
-// workspace, and k_gemm_fixup adds the segments of every output in segment
-// order and writes y (deterministic; no atomics, no CTA waits for another).
+// segment per SM): each K segment runs as a CTA of its own and writes its
+// fp32 partial tile to the workspace, and k_gemm_fixup adds the segments of
+// every output in segment order and writes y (deterministic; no atomics, no
+// CTA waits for another).
 // Stages are handed over with mbarriers (TMA bytes, decoder arrivals, MMA
 // completion via tcgen05.commit).  Every wait is bounded in time; a wait that
 // runs out records bit 1 of the status word and the CTA winds down.
