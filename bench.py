@@ -471,6 +471,25 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
         tf = 2 * M * N * K / (ms * 1e-3) / 1e12
         prefill.append({"shape": f"{N}x{K}", "M": M, "us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
                         "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4)})
+    # gate and up of one layer read the same x: the second call reuses the
+    # rotated x' in the workspace (TQ_GEMM_REUSE_ROTATED), one pre-pass per pair
+    mats = {m[0]: m for m in stack[0]}
+    N, K, M = FFN, HIDDEN, 2048
+    x = activations(torch, dev, K, M, seed=11 + K)
+    ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+    yg, yu = torch.empty(M, N, device=dev), torch.empty(M, N, device=dev)
+
+    def pair():
+        tq.gemm(mats["gate"][3], mats["gate"][4], x, K, tq.TQ_PACK_2BIT, workspace=ws, out=yg)
+        tq.gemm(mats["up"][3], mats["up"][4], x, K, tq.TQ_PACK_2BIT, workspace=ws, out=yu, reuse_rotated=True)
+
+    try:
+        ms = time_events(pair, 10, torch)
+        tf = 2 * 2 * M * N * K / (ms * 1e-3) / 1e12
+        prefill.append({"shape": f"2x{N}x{K} (gate, up: one x' pre-pass)", "M": M, "us": round(ms * 1e3, 1),
+                        "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4)})
+    except tq.TQError as e:
+        prefill.append({"shape": f"2x{N}x{K} (gate, up: one x' pre-pass)", "M": M, "unavailable": str(e)})
     out["prefill"] = prefill
     # --- offline quantise + pack of one layer group, weights resident (bf16)
     sweep = []

@@ -174,6 +174,19 @@ TQ_API tq_status tq_gemm(const uint8_t *codes, int64_t ldc, int fmt, const uint1
                   int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
                   void *workspace, size_t ws_bytes, tq_stream stream);
 
+/* tq_gemm with flags.  TQ_GEMM_REUSE_ROTATED: the workspace already holds the
+ * rotated activations of this same x (same M, K and values), left there by
+ * the previous tq_gemm / tq_gemm_ex call on `workspace` -- e.g. the gate
+ * projection before the up projection of a feed-forward block, which read
+ * the same x.  The FWHT pre-pass is skipped and x is not read; the status
+ * word keeps what the earlier call recorded (its fp16-overflow bit describes
+ * the same x').  Whether x matches is the caller's contract: it is not
+ * checked.  Unknown flag bits return TQ_ERR_INVALID_ARG. */
+enum { TQ_GEMM_REUSE_ROTATED = 1 };
+TQ_API tq_status tq_gemm_ex(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
+                  int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
+                  void *workspace, size_t ws_bytes, unsigned int flags, tq_stream stream);
+
 /* Synchronises `stream`, then reads the status word the last tq_gemm left in
  * `workspace`: TQ_ERR_RANGE if a rotated activation overflowed fp16 (the
  * output is then not meaningful), else TQ_OK. */

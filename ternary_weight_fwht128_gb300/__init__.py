@@ -27,10 +27,11 @@ TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
 TQ_PACK_2BIT, TQ_PACK_BASE3, TQ_PACK_BOTH = 1, 2, 3
 
 EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_quantize_pack", "tq_gemv",
-            "tq_gemv_ex", "tq_gemv_path", "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_check_range", "tq_device_fault",
-            "tq_gemm_noalloc")
+            "tq_gemv_ex", "tq_gemv_path", "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_ex", "tq_gemm_check_range",
+            "tq_device_fault", "tq_gemm_noalloc")
 TQ_GEMV_TENSOR_MEMORY, TQ_GEMV_MMA_SYNC = 1, 2
 TQ_GEMV_WEIGHTS_READY = 1
+TQ_GEMM_REUSE_ROTATED = 1
 
 _lib = None
 _i64 = ctypes.c_int64
@@ -73,6 +74,9 @@ def lib() -> ctypes.CDLL:
         L.tq_gemm.restype = _int
         L.tq_gemm.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
                               ctypes.c_size_t, _vp]
+        L.tq_gemm_ex.restype = _int
+        L.tq_gemm_ex.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
+                                 ctypes.c_size_t, ctypes.c_uint, _vp]
         L.tq_gemm_check_range.restype = _int
         L.tq_gemm_check_range.argtypes = [_vp, _vp]
         L.tq_device_fault.restype = _int
@@ -185,8 +189,13 @@ def gemm_workspace_bytes(M: int, K: int) -> int:
 
 
 def gemm(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, fmt: int = TQ_PACK_2BIT,
-         workspace: torch.Tensor | None = None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y [M][N] fp32 = prefill GEMM of bf16 x [M][K] on tcgen05 tensor cores."""
+         workspace: torch.Tensor | None = None, out: torch.Tensor | None = None, stream=None,
+         reuse_rotated: bool = False) -> torch.Tensor:
+    """y [M][N] fp32 = prefill GEMM of bf16 x [M][K] on tcgen05 tensor cores.
+    reuse_rotated: `workspace` already holds the rotated x of the previous
+    gemm call on it with this same x (tq_gemm_ex, TQ_GEMM_REUSE_ROTATED)."""
+    if reuse_rotated and workspace is None:
+        raise ValueError("reuse_rotated needs the workspace of the previous call")
     _cuda2d(codes, "codes")
     _cuda2d(scales, "scales")
     _cuda2d(x, "x")
@@ -196,10 +205,11 @@ def gemm(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, fmt
         workspace = torch.empty(gemm_workspace_bytes(M, K), dtype=torch.uint8, device=x.device)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    st = lib().tq_gemm(codes.data_ptr(), codes.stride(0), fmt, scales.data_ptr(), scales.stride(0), N, K,
-                       x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), workspace.data_ptr(),
-                       workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(st, "tq_gemm")
+    flags = TQ_GEMM_REUSE_ROTATED if reuse_rotated else 0
+    st = lib().tq_gemm_ex(codes.data_ptr(), codes.stride(0), fmt, scales.data_ptr(), scales.stride(0), N, K,
+                          x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), workspace.data_ptr(),
+                          workspace.numel() * workspace.element_size(), flags, _stream(stream))
+    _check(st, "tq_gemm_ex")
     return out
 
 

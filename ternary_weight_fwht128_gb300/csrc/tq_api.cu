@@ -152,6 +152,13 @@ size_t tq_gemm_workspace_bytes(int64_t M, int64_t K) {
 tq_status tq_gemm(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
                   int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, void* workspace,
                   size_t ws_bytes, tq_stream stream) {
+  return tq_gemm_ex(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy, workspace, ws_bytes, 0u, stream);
+}
+
+tq_status tq_gemm_ex(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
+                     int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, void* workspace,
+                     size_t ws_bytes, unsigned int flags, tq_stream stream) {
+  if (flags & ~(unsigned int)TQ_GEMM_REUSE_ROTATED) return TQ_ERR_INVALID_ARG;
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return TQ_ERR_INVALID_ARG;
   if (N < 0 || M < 0) return TQ_ERR_INVALID_ARG;
   if (!k_ok(K)) return TQ_ERR_SHAPE;
@@ -167,10 +174,12 @@ tq_status tq_gemm(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* sc
   cudaStream_t s = (cudaStream_t)stream;
   uint32_t* flag = static_cast<uint32_t*>(workspace);
   uint16_t* xrot = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(workspace) + 256);
-  cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), s);
-  if (e != cudaSuccess) return TQ_ERR_CUDA;
-  e = launch_fwht128(x, TQ_BF16, ldx, xrot, TQ_F16, K, M, K, true, flag, s);
-  if (e != cudaSuccess) return from_cuda(e);
+  if (!(flags & TQ_GEMM_REUSE_ROTATED)) {  // else x' (and its status) are the previous call's
+    cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return TQ_ERR_CUDA;
+    e = launch_fwht128(x, TQ_BF16, ldx, xrot, TQ_F16, K, M, K, true, flag, s);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
   unsigned char* split = static_cast<unsigned char*>(workspace) + gemm_split_offset(M, K);
   return from_cuda(launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, split,
                                ws_bytes - gemm_split_offset(M, K), s));

@@ -171,5 +171,18 @@ def test_gemm_validation(L):
     assert call(w=B + 65544) == tq.TQ_ERR_ALIGN
     assert call(y=B + 8194) == tq.TQ_ERR_ALIGN
     assert call(K=0) == tq.TQ_ERR_SHAPE
+    # tq_gemm_ex: the same validation, plus its flags
+    fe = L.tq_gemm_ex
+
+    def call_ex(flags, **kw):
+        a = dict(ok, **kw)
+        return fe(a["c"], a["ldc"], a["fmt"], a["s"], a["lds"], a["N"], a["K"], a["x"], a["ldx"], a["M"], a["y"],
+                  a["ldy"], a["w"], a["wsb"], flags, None)
+
+    assert call_ex(2, M=0) == tq.TQ_ERR_INVALID_ARG  # unknown flag bit, before anything else
+    assert call_ex(tq.TQ_GEMM_REUSE_ROTATED, M=0) == tq.TQ_OK
+    assert call_ex(tq.TQ_GEMM_REUSE_ROTATED, wsb=ws - 1) == tq.TQ_ERR_SHAPE
+    assert call_ex(tq.TQ_GEMM_REUSE_ROTATED, w=B + 65544) == tq.TQ_ERR_ALIGN
+    assert call_ex(0, fmt=tq.TQ_PACK_BASE3) == tq.TQ_ERR_UNSUPPORTED
     assert L.tq_gemm_check_range(None, None) == tq.TQ_ERR_INVALID_ARG
     assert L.tq_gemm_check_range(MIS, None) == tq.TQ_ERR_ALIGN

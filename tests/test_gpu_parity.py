@@ -471,6 +471,30 @@ def test_gemm_split_last_wave(orc):
     check_y(y0.cpu().numpy()[:, rows], ref, "gemm y (split tiles)")
 
 
+def test_gemm_reuse_rotated(orc):
+    """Two projections of the same x (gate and up of a feed-forward block):
+    the second call reuses the rotated x' in the workspace and skips the
+    pre-pass.  Its output is bit-identical to a plain call (the GEMM is
+    deterministic), and matches the oracle."""
+    N, K, M = 768, 640, 300
+    W1 = synth.weights(N, K, 101, dtype="bf16")
+    W2 = synth.weights(N, K, 102, dtype="bf16")
+    xb = synth.activations(M, K, 103)
+    c1, _, s1 = tq.quantize_pack(to_dev_bf16(W1), tq.TQ_PACK_2BIT)
+    c2, _, s2 = tq.quantize_pack(to_dev_bf16(W2), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(xb)
+    ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    ref2 = tq.gemm(c2, s2, x, K, workspace=torch.empty_like(ws))
+    tq.gemm(c1, s1, x, K, workspace=ws)
+    junk = torch.zeros_like(x)  # not read when the rotation is reused
+    y2 = tq.gemm(c2, s2, junk, K, workspace=ws, reuse_rotated=True)
+    torch.cuda.synchronize()
+    tq.gemm_check_range(ws)
+    assert torch.equal(y2, ref2)
+    T, S = orc.quantize(W2)
+    check_y(y2.cpu().numpy(), orc.gemv(T, S, synth.bf16_bits_to_f32(xb)), "gemm y (reused x')")
+
+
 def test_gemm_range_flag():
     """An activation block whose rotation exceeds the fp16 range is reported
     through the status word (tq_gemm_check_range -> TQ_ERR_RANGE)."""
