@@ -181,7 +181,10 @@ TQ_API tq_status tq_gemm(const uint8_t *codes, int64_t ldc, int fmt, const uint1
  * the same x.  The FWHT pre-pass is skipped and x is not read; the status
  * word keeps what the earlier call recorded (its fp16-overflow bit describes
  * the same x').  Whether x matches is the caller's contract: it is not
- * checked.  Unknown flag bits return TQ_ERR_INVALID_ARG. */
+ * checked; with a workspace that holds no x' of this M and K the output is
+ * meaningless, but every access stays inside the workspace.  x is still
+ * validated like any argument, though not read.  Unknown flag bits return
+ * TQ_ERR_INVALID_ARG. */
 enum { TQ_GEMM_REUSE_ROTATED = 1 };
 TQ_API tq_status tq_gemm_ex(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
                   int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
