@@ -266,6 +266,81 @@ def check_quantize_mean_exact(orc):
         assert s == _fp16(np.float32(float(mean)))
 
 
+def _sum_halving_tree_f32(a: np.ndarray) -> np.float32:
+    """fp32 sum of 128 values in the order the scale's reduction fixes:
+    for h = 64, 32, ..., 1 the first h partial sums take in the next h
+    (element-wise, each addition rounded to fp32)."""
+    s = a.astype(np.float32).copy()
+    h = 64
+    while h >= 1:
+        s[:h] = s[:h] + s[h:2 * h]
+        h //= 2
+    return s[0]
+
+
+def _sum_sequential_f32(a: np.ndarray) -> np.float32:
+    acc = np.float32(0.0)
+    for v in a.astype(np.float32):
+        acc = np.float32(acc + v)
+    return acc
+
+
+def _sum_adjacent_tree_f32(a: np.ndarray) -> np.float32:
+    s = a.astype(np.float32).copy()
+    h = 1
+    while h < 128:
+        for i in range(0, 128, 2 * h):
+            s[i] = np.float32(s[i] + s[i + h])
+        h *= 2
+    return s[0]
+
+
+def _order_sensitive_groups(count: int = 4):
+    """Groups whose exact sum of |w'| sits on an fp16 rounding midpoint of
+    128 * scale, so that the fp32 rounding of the partial sums decides the
+    scale; kept only where the halving tree lands on the other side from
+    both a left-to-right sum and an adjacent-pair tree.  Magnitudes span
+    e^-6 .. e^3 (a wide dynamic range makes the orders round differently)."""
+    found = []
+    for seed in range(4000):
+        rng = np.random.default_rng(5000 + seed)
+        mag = np.exp(rng.uniform(-6.0, 3.0, size=128)).astype(np.float32)
+        sign = np.where(rng.random(128) < 0.5, -1.0, 1.0).astype(np.float32)
+        others = sum(Fraction(float(v)) for v in mag[:-1])
+        guess = np.float16(float(others + Fraction(float(mag[-1]))) / 128)
+        lo = Fraction(float(guess))
+        hi = Fraction(float(np.nextafter(guess, np.float16(np.inf))))
+        need = 128 * (lo + hi) / 2 - others
+        if need <= 0:
+            continue
+        mag[-1] = np.float32(float(need))
+        f16 = [_fp16(np.float32(fn(mag) * np.float32(0.0078125)))
+               for fn in (_sum_halving_tree_f32, _sum_sequential_f32, _sum_adjacent_tree_f32)]
+        if f16[0] != f16[1] and f16[0] != f16[2]:
+            found.append(((sign * mag).astype(np.float32), f16[0]))
+            if len(found) == count:
+                break
+    assert len(found) == count, "too few order-sensitive groups"
+    return found
+
+
+def check_quantize_sum_order(orc):
+    """The reduction order of mean |w'| (the pages are silent; the reading is
+    the fixed halving tree, s[i] += s[i + h] for h = 64 .. 1, in fp32).  On
+    groups whose exact sum lies on an fp16 rounding midpoint, the scale
+    depends on the order of the fp32 additions; the expected scale is
+    fp16_RN(tree sum * 2^-7) with the tree written out here, and the groups
+    are chosen so that a left-to-right sum or an adjacent-pair tree gives a
+    different scale.  The tree sum is also checked against the exact sum
+    (fractions) within the error bound of 7 levels of fp32 additions."""
+    for w, expect in _order_sensitive_groups():
+        exact = sum(Fraction(abs(float(v))) for v in w)
+        tree = _sum_halving_tree_f32(np.abs(w))
+        assert abs(Fraction(float(tree)) - exact) <= Fraction(7, 2 ** 24) * exact
+        s, _ = orc.quantize_group(w)
+        assert s == expect, (hex(s), hex(expect))
+
+
 def check_quantize_delta_rows(orc):
     """A weight row that is a unit vector in one group rotates to c * (column
     of H): all |w'| = c, mean = c exactly, scale = fp16(c), trits = that
@@ -422,6 +497,7 @@ ALL_CHECKS = [
     check_quantize_ties,
     check_quantize_rule_identity,
     check_quantize_mean_exact,
+    check_quantize_sum_order,
     check_quantize_delta_rows,
     check_quantize_bf16_input,
     check_pack_golden,

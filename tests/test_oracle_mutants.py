@@ -22,6 +22,10 @@ MUTANTS = [
     ("f16_round_ties_down", "if (rem > half || (rem == half && (q & 1u))) q += 1;\n    if (q == 0x800u)",
      "if (rem > half) q += 1;\n    if (q == 0x800u)"),
     ("f16_subnormal_scale", "5.9604644775390625e-08f", "1.1920928955078125e-07f"),
+    ("sequential_sum", "for (int h = 64; h >= 1; h /= 2)\n    for (int i = 0; i < h; ++i) s[i] = s[i] + s[i + h];",
+     "for (int i = 1; i < 128; ++i) s[0] = s[0] + s[i];"),
+    ("adjacent_tree", "for (int h = 64; h >= 1; h /= 2)\n    for (int i = 0; i < h; ++i) s[i] = s[i] + s[i + h];",
+     "for (int h = 1; h < 128; h *= 2)\n    for (int i = 0; i + h < 128; i += 2 * h) s[i] = s[i] + s[i + h];"),
     ("mean_factor", "s[0] * 0.0078125f", "s[0] * 0.00390625f"),
     ("signed_sum", "s[i] = fabsf(wrot[i]);", "s[i] = wrot[i];"),
     ("divide_by_mean", "float q = wrot[i] / sc;", "float q = wrot[i] / mean;"),
