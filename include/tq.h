@@ -36,7 +36,12 @@
  *     stream); results are valid once the stream reaches that point;
  *   - validates its arguments on the host first and returns a status; a
  *     non-OK status means nothing was launched;
- *   - is thread-safe; the library keeps only per-device read-only setup.
+ *   - is thread-safe.  The library keeps per-device read-only setup and
+ *     a few process-wide device status words (see tq_device_fault): a
+ *     kernel that gives up a bounded wait sets a bit there, and
+ *     tq_device_fault reads and clears them for every caller at once, so
+ *     in a process with several host threads one thread's call may report
+ *     (and clear) another thread's event.
  * Pointers must be 16-byte aligned and every row must start 16-byte aligned
  * (ld * element size % 16 == 0), else TQ_ERR_ALIGN.  K must be a positive
  * multiple of 128, else TQ_ERR_SHAPE.
@@ -205,15 +210,20 @@ TQ_API tq_status tq_gemm_check_range(const void *workspace, tq_stream stream);
  *     (e.g. 2048 x 8192); larger M * K returns TQ_ERR_SHAPE;
  *   - it lives in device memory of every GPU that loads the library, until
  *     the process exits (about 32 MiB per GPU);
- *   - the first call on a device looks up the array's device address with
- *     that device current (set-up); make that first call before any stream
- *     capture;
- *   - every call shares the one array and it keeps the last call's contents;
- *     calls whose work overlaps on the GPU (different streams, or different
- *     host threads on the same device) race on it and must be serialised by
- *     the caller;
- *   - the fp16-overflow status word of tq_gemm is kept in the array and is
- *     not reported here; callers that need that check use tq_gemm.
+ *   - every call looks up the array's device address with the device
+ *     current (a host-side query); the first call on a device also loads the
+ *     library's module there (set-up), so make that first call before any
+ *     stream capture;
+ *   - every call shares the one array and it keeps the last call's contents
+ *     (the call clears the status word it uses); calls whose work overlaps
+ *     on the GPU (different streams, or different host threads on the same
+ *     device) race on it and must be serialised by the caller;
+ *   - a bounded wait of the GEMM that ran out is recorded in the array's
+ *     status word and reported by tq_device_fault (TQ_ERR_TIMEOUT);
+ *   - an fp16 overflow of the rotated activations is NOT reported on this
+ *     path (tq_gemm reports it through tq_gemm_check_range): the output may
+ *     then hold inf or NaN.  With bf16 inputs this needs a 128-block of x
+ *     whose 2-norm exceeds 65504.
  * No cudaMalloc, cudaFree or other allocating call is made.  Arguments,
  * layouts and other errors as for tq_gemm. */
 TQ_API tq_status tq_gemm_noalloc(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,

@@ -197,7 +197,7 @@ tq_status tq_gemm_check_range(const void* workspace, tq_stream stream) {
 
 tq_status tq_device_fault(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
-  const unsigned int f = take_fault_gemv() | take_fault_quant();
+  const unsigned int f = take_fault_gemv() | take_fault_quant() | take_fault_noalloc();
   return f ? TQ_ERR_TIMEOUT : TQ_OK;
 }
 

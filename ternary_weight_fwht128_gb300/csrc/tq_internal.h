@@ -55,5 +55,8 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
 // a bounded wait ran out).
 unsigned int take_fault_gemv();
 unsigned int take_fault_quant();
+// Same for the status word of tq_gemm_noalloc's scratch array (its timeout
+// bit only; the word is left as it is otherwise).
+unsigned int take_fault_noalloc();
 
 }  // namespace tq

@@ -13,8 +13,14 @@
 // The array is a file-scope __device__ object of kScratchBytes, so every GPU
 // that loads the library holds it until the process exits.  In host code the
 // array's name is only a host-side stand-in, not a device address; its device
-// address is looked up with cudaGetSymbolAddress, once per device, with that
-// device current, on the first call made there.
+// address is looked up with cudaGetSymbolAddress, with the device current, on
+// every call (a host-side query that allocates nothing; looking it up each
+// time keeps a stale address from outliving a reset of the device).  The
+// first call on a device also loads the library's module there (set-up).
+//
+// The GEMM records a bounded wait that ran out in the status word at the
+// start of the array; tq_device_fault reads that word on every device where
+// this entry point has been used.
 #include <atomic>
 
 #include "tq_internal.h"
@@ -29,23 +35,38 @@ constexpr size_t kScratchBytes = 256 + ((size_t)1 << 24) * 2;
 __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+std::atomic<int> g_used[kMaxDevices];  // tq_gemm_noalloc has launched on this device
 
 // Device address of g_scratch on the current device (nullptr on failure).
 void* scratch_on_current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p != nullptr) return p;
+  void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) {
     (void)cudaGetLastError();
     return nullptr;
   }
-  g_scratch_addr[dev].store(p, std::memory_order_release);
   return p;
 }
 
 }  // namespace
+
+// Reads the status word of the scratch array on the current device when this
+// entry point has run there; returns kFaultTimeout-style bit 1 when a bounded
+// wait of the GEMM ran out, and clears that bit.  Called after a device-wide
+// synchronisation.
+unsigned int take_fault_noalloc() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (g_used[dev].load(std::memory_order_acquire) == 0) return 0;
+  uint32_t w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_scratch, sizeof(w)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  if (!(w & 2u)) return 0;
+  w &= ~2u;
+  (void)cudaMemcpyToSymbol(g_scratch, &w, sizeof(w));
+  return 2u;
+}
 
 }  // namespace tq
 
@@ -68,6 +89,9 @@ extern "C" TQ_API tq_status tq_gemm_noalloc(const uint8_t* codes, int64_t ldc, i
     return TQ_ERR_ALIGN;
   unsigned char* ws = static_cast<unsigned char*>(scratch_on_current_device());
   if (ws == nullptr) return TQ_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxDevices) g_used[dev].store(1, std::memory_order_release);
   cudaStream_t s = (cudaStream_t)stream;
   uint32_t* flag = reinterpret_cast<uint32_t*>(ws);
   uint16_t* xrot = reinterpret_cast<uint16_t*>(ws + 256);

@@ -186,3 +186,41 @@ def test_gemm_validation(L):
     assert call_ex(0, fmt=tq.TQ_PACK_BASE3) == tq.TQ_ERR_UNSUPPORTED
     assert L.tq_gemm_check_range(None, None) == tq.TQ_ERR_INVALID_ARG
     assert L.tq_gemm_check_range(MIS, None) == tq.TQ_ERR_ALIGN
+
+
+def test_gemm_noalloc_validation(L):
+    """tq_gemm_noalloc rejects bad arguments on the host, before it looks up
+    its scratch array or launches anything (fake pointers, no GPU needed)."""
+    f = L.tq_gemm_noalloc
+    ok = dict(c=A, ldc=64, fmt=tq.TQ_PACK_2BIT, s=B, lds=2, N=8, K=256, x=B + 4096, ldx=256, M=4, y=B + 8192,
+              ldy=8)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["c"], a["ldc"], a["fmt"], a["s"], a["lds"], a["N"], a["K"], a["x"], a["ldx"], a["M"], a["y"],
+                 a["ldy"], None)
+
+    assert call(M=0) == tq.TQ_OK
+    assert call(N=0) == tq.TQ_OK
+    assert call(fmt=7) == tq.TQ_ERR_INVALID_ARG
+    assert call(fmt=tq.TQ_PACK_BOTH) == tq.TQ_ERR_INVALID_ARG
+    assert call(fmt=tq.TQ_PACK_BASE3) == tq.TQ_ERR_UNSUPPORTED
+    assert call(N=-1) == tq.TQ_ERR_INVALID_ARG
+    assert call(M=-1) == tq.TQ_ERR_INVALID_ARG
+    assert call(K=0) == tq.TQ_ERR_SHAPE
+    assert call(K=200) == tq.TQ_ERR_SHAPE
+    for name in ("c", "s", "x", "y"):
+        assert call(**{name: None}) == tq.TQ_ERR_INVALID_ARG, name
+    assert call(ldc=63) == tq.TQ_ERR_SHAPE
+    assert call(lds=1) == tq.TQ_ERR_SHAPE
+    assert call(ldx=255) == tq.TQ_ERR_SHAPE
+    assert call(ldy=7) == tq.TQ_ERR_SHAPE
+    assert call(c=A + 8) == tq.TQ_ERR_ALIGN
+    assert call(ldc=72) == tq.TQ_ERR_ALIGN
+    assert call(s=B + 1) == tq.TQ_ERR_ALIGN
+    assert call(x=B + 4104) == tq.TQ_ERR_ALIGN
+    assert call(ldx=260) == tq.TQ_ERR_ALIGN
+    assert call(y=B + 8194) == tq.TQ_ERR_ALIGN
+    # M * K above the fixed scratch array (2^24 rotated activations)
+    assert call(M=2048, K=27648, ldx=27648, ldc=6912, lds=216) == tq.TQ_ERR_SHAPE
+    assert call(M=(1 << 24) // 256 + 1) == tq.TQ_ERR_SHAPE

@@ -38,13 +38,3 @@ def test_gemm_noalloc_matches_gemm_twice():
         torch.cuda.synchronize()
         check_y(y.cpu().numpy(), ref.cpu().numpy().astype(np.float64), f"no-alloc call {call}")
 
-
-def test_gemm_noalloc_rejects_oversize():
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
-    L = tq.lib()
-    # 2048 x 27648 activations need 113 MB of fp16 scratch: beyond the fixed array
-    dummy = torch.empty(16, dtype=torch.uint8, device="cuda")
-    p = dummy.data_ptr()
-    st = L.tq_gemm_noalloc(p, 6912, tq.TQ_PACK_2BIT, p, 216, 5120, 27648, p, 27648, 2048, p, 5120, None)
-    assert st == tq.TQ_ERR_SHAPE
