@@ -158,28 +158,38 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
-def build_stack(tq, torch, dev, seed: int):
+def synth_weight(torch, gen, dev, N: int, K: int):
+    """W [N][K] bf16 ~N(0, 0.02) with 0.1% of the entries (chosen without
+    replacement) x20, drawn on the device from a seeded generator."""
+    W = torch.randn(N, K, device=dev, generator=gen, dtype=torch.float32).mul_(0.02)
+    n_out = max(1, (N * K) // 1000)
+    idx = torch.randperm(N * K, device=dev, generator=gen)[:n_out]
+    W.view(-1)[idx] *= 20.0
+    del idx
+    return W.to(torch.bfloat16)
+
+
+def build_stack(tq, torch, dev, seed: int, keep_weights: bool = False):
     """64 layers of packed weights, quantised on the GPU from seeded synthetic
-    bf16 weights ~N(0, 0.02) with 0.1% of entries x20."""
+    bf16 weights ~N(0, 0.02) with 0.1% of entries x20.  keep_weights: also
+    return the bf16 weights (the offline sweep re-quantises them)."""
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
-    stack = []
+    stack, weights = [], []
     for layer in range(LAYERS):
-        mats = []
+        mats, wl = [], []
         for name, N, K in LAYER_SHAPES:
-            W = torch.randn(N, K, device=dev, generator=gen, dtype=torch.float32).mul_(0.02)
-            n_out = max(1, (N * K) // 1000)
-            idx = torch.randint(0, N * K, (n_out,), device=dev, generator=gen)
-            W.view(-1)[idx] *= 20.0
-            Wb = W.to(torch.bfloat16)
-            del W
+            Wb = synth_weight(torch, gen, dev, N, K)
             # base-3 codes as well for the shapes the skinny comparison uses
             fmt = tq.TQ_PACK_BOTH if name in ("gate", "down") else tq.TQ_PACK_2BIT
             c2, c3, s = tq.quantize_pack(Wb, fmt)
-            del Wb
             mats.append((name, N, K, c2, s, c3))
+            if keep_weights:
+                wl.append(Wb)
+            del Wb
         stack.append(mats)
-    return stack
+        weights.append(wl)
+    return (stack, weights) if keep_weights else stack
 
 
 def activations(torch, dev, K: int, M: int, seed: int):
@@ -252,7 +262,7 @@ def gpu_arm(args, world, rank, local):
     pk = peaks()
     stream = torch.cuda.current_stream()
 
-    stack = build_stack(tq, torch, dev, seed=1000 + rank)
+    stack, sweep_w = build_stack(tq, torch, dev, seed=1000 + rank, keep_weights=not args.quick)
     xs = {K: activations(torch, dev, K, 1, seed=K) for K in (HIDDEN, FFN)}
     ys = {N: torch.empty(1, N, device=dev) for N in (HIDDEN, FFN)}
     launches_per_step = LAYERS * len(LAYER_SHAPES)
@@ -354,6 +364,8 @@ def gpu_arm(args, world, rank, local):
     extras = {}
     if not args.quick:
         extras = gpu_extras(args, tq, torch, dev, stack, pk)
+        extras["sweep"] = sweep_bench(tq, torch, sweep_w, pk, world)
+    del sweep_w
 
     if rank != 0:
         return
@@ -505,56 +517,173 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
     return out
 
 
+def sweep_bench(tq, torch, weights, pk, world: int) -> dict:
+    """The offline quantise + pack sweep: all 64 layers x {5120x5120 x2,
+    27648x5120 x2, 5120x27648} of resident bf16 weights (30.5 G parameters,
+    61 GB, far larger than L2), 2-bit and base-3 codes plus scales in one pass
+    per matrix, into per-matrix outputs; CUDA events around whole sweeps."""
+    outs = []
+    params, nbytes = 0, 0
+    for wl in weights:
+        for Wb in wl:
+            N, K = Wb.shape
+            ld3 = tq.packed_ld(K, tq.TQ_PACK_BASE3)
+            o = (torch.empty(N, K // 4, dtype=torch.uint8, device=Wb.device),
+                 torch.empty(N, ld3, dtype=torch.uint8, device=Wb.device),
+                 torch.empty(N, K // 128, dtype=torch.int16, device=Wb.device))
+            outs.append((Wb, o))
+            params += N * K
+            nbytes += N * K * 2 + N * (K // 4) + N * ld3 + N * (K // 128) * 2
+
+    def sweep():
+        for Wb, o in outs:
+            tq.quantize_pack(Wb, tq.TQ_PACK_BOTH, out=o)
+
+    reps = 3
+    ms = time_events(sweep, reps, torch)
+    line = {"workload": "64 layers x {5120x5120 x2, 27648x5120 x2, 5120x27648}, bf16 N(0,0.02)+0.1% x20, "
+                        "2-bit + base-3 + fp16 scales in one pass per matrix",
+            "matrices": len(outs), "params": params, "bytes": nbytes, "ms": round(ms, 3),
+            "Gparams/s": round(world * params / (ms * 1e-3) / 1e9, 1),
+            "GB/s": round(world * nbytes / (ms * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "timing": f"CUDA events around {reps} whole sweeps after one warm-up sweep; inputs larger than L2",
+            "launches": len(outs) * (reps + 1)}
+    del outs
+    return line
+
+
 # ---------------------------------------------------------------- CPU oracle
+
+def host_cpu() -> dict:
+    """Host core count and CPU model (the oracle runs on one of the cores)."""
+    import platform
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    if key == "cpu part":
+                        model = f"{platform.machine()} (CPU part {model})"
+                    break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+class OracleGemv:
+    """The oracle's fp64 GEMV (M = 1) over oracle-quantised synthetic layers
+    of the decode shapes (5120x5120, 1024 rows of 27648 inputs, 3456 rows of
+    5120 inputs), prepared once; run() times it on one core for a budget."""
+
+    def __init__(self, orc):
+        from ternary_weight_fwht128_gb300 import synth
+        self.orc = orc
+        self.prepared = []
+        for (N, K) in [(HIDDEN, HIDDEN), (1024, FFN), (FFN // 8, HIDDEN)]:
+            W = synth.weights(N, K, N + K, dtype="bf16")
+            T, S = orc.quantize(W)
+            x = synth.bf16_bits_to_f32(synth.activations(1, K, K))
+            self.prepared.append((N, K, T, S, x))
+
+    def run(self, budget_s: float) -> dict:
+        done_bytes, spent, calls = 0, 0.0, 0
+        while spent < budget_s:
+            for (N, K, T, S, x) in self.prepared:
+                t0 = time.perf_counter()
+                self.orc.gemv(T, S, x)
+                spent += time.perf_counter() - t0
+                done_bytes += packed_bytes(N, K)
+                calls += 1
+        return {"value": round(done_bytes / spent / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"{calls} oracle fp64 GEMVs (M=1) over 5120x5120, 1024x27648, 3456x5120 rows of "
+                          f"oracle-quantised synthetic weights, {spent:.1f} s of one host core"}
+
 
 def cpu_baseline(budget_s: float = 12.0) -> dict:
     """The CPU oracle, as it stands, on a bounded sample of the decode
     workload: fp64 GEMV of oracle-quantised 5120x5120 and 27648x5120 layers
     (single core), repeated until the time budget is spent.  Reported in the
-    same unit: packed weight bytes consumed per second."""
+    same unit: packed weight bytes consumed per second.  Beside it: the small
+    end-to-end case (256x256: quantise, pack, GEMV) in ms, and the offline
+    sweep's quantise + pack rate on sampled rows, extrapolated to the 64-layer
+    sweep."""
     import numpy as np
 
     import oracle
     from ternary_weight_fwht128_gb300 import synth
 
     orc = oracle.load()
-    shapes = [(HIDDEN, HIDDEN), (1024, FFN), (FFN // 8, HIDDEN)]
-    prepared = []
-    for (N, K) in shapes:
-        W = synth.weights(N, K, N + K, dtype="bf16")
+    # small end-to-end case, whole
+    W, xb = synth.tiny_config()
+    xt = synth.bf16_bits_to_f32(xb)
+    t0 = time.perf_counter()
+    reps = 0
+    while reps < 5 or time.perf_counter() - t0 < 0.5:
         T, S = orc.quantize(W)
-        x = synth.bf16_bits_to_f32(synth.activations(1, K, K))
-        prepared.append((N, K, T, S, x))
-    done_bytes, spent, calls = 0, 0.0, 0
-    while spent < budget_s:
-        for (N, K, T, S, x) in prepared:
+        orc.pack2(T)
+        orc.gemv(T, S, xt)
+        reps += 1
+    tiny_ms = (time.perf_counter() - t0) / reps * 1e3
+    # offline sweep: 1% of the rows of each of the five shapes of a layer
+    sweep_rows, sweep_s, sweep_params = 0, 0.0, 0
+    sample = []
+    for i, (_, N, K) in enumerate(LAYER_SHAPES):
+        sample.append(synth.weights(max(1, N // 100), K, 700 + i, dtype="bf16"))
+    while sweep_s < min(3.0, budget_s / 4):
+        for Ws in sample:
             t0 = time.perf_counter()
-            orc.gemv(T, S, x)
-            spent += time.perf_counter() - t0
-            done_bytes += packed_bytes(N, K)
-            calls += 1
-    return {"value": round(done_bytes / spent / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{calls} oracle fp64 GEMVs (M=1) over 5120x5120, 1024x27648, 3456x5120 rows of "
-                      f"oracle-quantised synthetic weights, {spent:.1f} s of one host core"}
+            T, S = orc.quantize(Ws)
+            orc.pack2(T)
+            orc.pack3(T)
+            sweep_s += time.perf_counter() - t0
+            sweep_params += Ws.size
+            sweep_rows += Ws.shape[0]
+    sweep_pps = sweep_params / sweep_s
+    total_params = LAYERS * sum(N * K for _, N, K in LAYER_SHAPES)
+    # decode GEMV, the unit of the headline metric
+    gemv = OracleGemv(orc)
+    out = gemv.run(budget_s)
+    out.update({"tiny_ms": round(tiny_ms, 3),
+                "tiny_sample": "256x256 layer: oracle quantise + 2-bit pack + fp64 GEMV (M=1), whole, one core",
+                "sweep_params_per_s": round(sweep_pps, 1),
+                "sweep_s_extrapolated": round(total_params / sweep_pps, 1),
+                "sweep_sample": f"oracle quantise + 2-bit + base-3 pack of 1% of the rows of each layer shape "
+                                f"({sweep_rows} rows, {sweep_s:.1f} s, one core), extrapolated to the 64-layer "
+                                f"sweep ({total_params / 1e9:.2f} G params)"})
+    out.update(host_cpu())
+    return out
 
 
 def reference_arm(args, world, rank):
-    """The oracle as the reference implementation (single host core)."""
+    """The oracle as the reference implementation (single host core): each
+    step is a bounded sample of the decode workload (fp64 GEMVs of the
+    decode shapes), sized so the whole run takes about two minutes."""
     if rank != 0:
         return
-    t_total = 0.0
-    base = None
-    for _ in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        base = cpu_baseline(budget_s=args.ref_budget)
-        t_total += time.perf_counter() - t0
-    line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "GB/s", "n_gpus": world,
+    import oracle
+    orc = oracle.load()
+    gemv = OracleGemv(orc)
+    per_step = max(0.3, min(args.ref_budget, 120.0 / (args.warmup + args.steps)))
+    for _ in range(args.warmup):
+        gemv.run(per_step)
+    vals, samples = [], []
+    for _ in range(args.steps):
+        r = gemv.run(per_step)
+        vals.append(r["value"])
+        samples.append(r["sample"])
+    value = round(statistics.median(vals), 4)
+    base = {"kind": "oracle", "cores": 1, "value": value, "unit": "GB/s",
+            "sample": f"median of {args.steps} steps, each: {samples[-1]}"}
+    base.update(host_cpu())
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": WORKLOAD, "M": 1, "sample": "bounded oracle sample per step"},
-            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": base["sample"], "value": base["value"],
-                             "unit": "GB/s"},
-            "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": base,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 

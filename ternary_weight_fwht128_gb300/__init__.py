@@ -136,21 +136,30 @@ def fwht128(x: torch.Tensor, out_dtype: torch.dtype = torch.float32, out: torch.
     return out
 
 
-def quantize_pack(W: torch.Tensor, fmt: int = TQ_PACK_BOTH, stream=None):
+def quantize_pack(W: torch.Tensor, fmt: int = TQ_PACK_BOTH, stream=None, out=None):
     """Rotate, ternarise and pack W [N][K] (fp32 or bf16).
 
     Returns (codes2 uint8 [N][K/4] or None, codes3 uint8 [N][ld3] or None,
-    scales int16 [N][K/128] holding fp16 bit patterns)."""
+    scales int16 [N][K/128] holding fp16 bit patterns).  out: an earlier
+    (codes2, codes3, scales) triple of this shape and format to write into."""
     _cuda2d(W, "W")
     N, K = W.shape
     dev = W.device
-    codes2 = torch.empty((N, K // 4), dtype=torch.uint8, device=dev) if fmt & TQ_PACK_2BIT else None
     ld3 = packed_ld(K, TQ_PACK_BASE3) if K > 0 else 0
-    codes3 = torch.empty((N, max(ld3, 0)), dtype=torch.uint8, device=dev) if fmt & TQ_PACK_BASE3 else None
-    scales = torch.empty((N, K // 128), dtype=torch.int16, device=dev)
+    if out is None:
+        codes2 = torch.empty((N, K // 4), dtype=torch.uint8, device=dev) if fmt & TQ_PACK_2BIT else None
+        codes3 = torch.empty((N, max(ld3, 0)), dtype=torch.uint8, device=dev) if fmt & TQ_PACK_BASE3 else None
+        scales = torch.empty((N, K // 128), dtype=torch.int16, device=dev)
+    else:
+        codes2, codes3, scales = out
+        for t, name in ((codes2, "codes2"), (codes3, "codes3"), (scales, "scales")):
+            if t is not None:
+                _cuda2d(t, name)
     st = lib().tq_quantize_pack(W.data_ptr(), _dt(W), N, K, W.stride(0), fmt,
-                                codes2.data_ptr() if codes2 is not None else None, K // 4,
-                                codes3.data_ptr() if codes3 is not None else None, max(ld3, 0),
+                                codes2.data_ptr() if codes2 is not None else None,
+                                codes2.stride(0) if codes2 is not None else 0,
+                                codes3.data_ptr() if codes3 is not None else None,
+                                codes3.stride(0) if codes3 is not None else 0,
                                 scales.data_ptr(), scales.stride(0), _stream(stream))
     _check(st, "tq_quantize_pack")
     return codes2, codes3, scales

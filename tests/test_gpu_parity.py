@@ -99,6 +99,25 @@ def test_quantize_shapes(orc, N, K, dtype, fmt):
     _quant_check(orc, W, fmt)
 
 
+@pytest.mark.parametrize("N,K", [(27648, 5120), (5120, 27648)])
+def test_quantize_full_layer_sweep_shapes(orc, N, K):
+    """The offline sweep's two large shapes at full size, in the launch
+    configuration the sweep uses (2-bit and base-3 in one pass), with bf16
+    weights ~N(0, 0.02) and 0.1 % of the entries (chosen without
+    replacement) x20: one whole layer is compared bit for bit with the
+    oracle, then 1 % of the rows of two further seeded layers."""
+    W = synth.weights(N, K, 9000 + N + K, dtype="bf16")
+    _quant_check(orc, W)
+    del W
+    for layer in (1, 2):
+        W = synth.weights(N, K, 9000 + N + K + layer, dtype="bf16")
+        rng = np.random.default_rng(layer * 7 + N)
+        rows = np.sort(rng.choice(N, size=N // 100, replace=False))
+        rows[-1] = N - 1
+        _quant_check(orc, W, rows=rows)
+        del W
+
+
 def test_quantize_special_groups(orc):
     """All-zero groups (scale 0), tiny groups (fp16 underflow -> scale 0),
     huge groups (scale inf -> trits 0), delta rows (rows of H)."""
