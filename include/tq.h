@@ -145,15 +145,17 @@ TQ_API tq_status tq_gemv_ex(const uint8_t *codes, int64_t ldc, int fmt, const ui
                             unsigned int flags, tq_stream stream);
 
 /* Which kernel tq_gemv runs for a shape (introspection; launches nothing):
- *   TQ_GEMV_TENSOR_MEMORY  2-bit codes, any M, when one CTA's share of the
- *                          rotated activations fits in shared memory (K up to
- *                          about 140 thousand at M <= 2, 35 thousand at
- *                          M = 16; M > 8 may take two launches of half the
- *                          rows): weights unpacked to fp8 in tensor memory,
+ *   TQ_GEMV_TENSOR_MEMORY  2-bit or base-3 codes, any M, when one CTA's share
+ *                          of the rotated activations fits in shared memory
+ *                          (2-bit: K up to about 140 thousand at M <= 2, 35
+ *                          thousand at M = 16; base-3 about two thirds of
+ *                          that; when the rows of x do not fit one launch
+ *                          they are split evenly over up to four launches):
+ *                          weights unpacked to fp8 in tensor memory,
  *                          activations as three e4m3 pieces, tcgen05 MMAs;
- *   TQ_GEMV_MMA_SYNC       everything else (base-3 codes, larger K): fp16 x'
- *                          in shared memory, weights as fp16 on mma.sync
- *                          (16-row tiles).
+ *   TQ_GEMV_MMA_SYNC       everything else (larger K): fp16 x' in shared
+ *                          memory, weights as fp16 on mma.sync (16-row
+ *                          tiles).
  * Queries device properties of the current device on first use.  Returns
  * -TQ_ERR_INVALID_ARG / -TQ_ERR_SHAPE for arguments tq_gemv would reject
  * with those codes. */

@@ -602,14 +602,14 @@ cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16
   p.y = y;
   p.ldy = ldy;
   p.prefetch = prefetch ? 1 : 0;
+  {
+    const cudaError_t e = launch_gemv_tc(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy, prefetch, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (fmt == TQ_PACK_BASE3) {
     if (M == 1) return launch_mb<1, TQ_PACK_BASE3>(p, s);
     if (M <= 8) return launch_mb<8, TQ_PACK_BASE3>(p, s);
     return launch_mb<16, TQ_PACK_BASE3>(p, s);
-  }
-  {
-    const cudaError_t e = launch_gemv_tc(codes, ldc, scales, lds, N, K, x, ldx, M, y, ldy, prefetch, s);
-    if (e != cudaErrorNotSupported) return e;
   }
   if (M == 1) return launch_mb<1, TQ_PACK_2BIT>(p, s);
   if (M <= 8) return launch_mb<8, TQ_PACK_2BIT>(p, s);

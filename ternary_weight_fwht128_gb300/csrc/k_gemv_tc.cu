@@ -1,5 +1,5 @@
-// k_gemv_tc.cu -- decode GEMV / skinny GEMM (tq_gemv, 2-bit codes, M = 1..16)
-// on tcgen05 tensor cores with the weight operand in tensor memory.
+// k_gemv_tc.cu -- decode GEMV / skinny GEMM (tq_gemv, 2-bit or base-3 codes,
+// M = 1..16) on tcgen05 tensor cores with the weight operand in tensor memory.
 //
 //   y[m][n] = sum_g s[n][g] * sum_{k in g} t[n][k] * x'[m][k],  x' = FWHT-128(x)
 //
@@ -38,6 +38,23 @@
 //   adding the columns that share an m), adds the correction term
 //   -2^-9 sum_k (p1 + p2 + p3)(k) and multiplies by s[n][g] 2^(9 - E) in fp32
 //   -- the scale is applied to each group's inner product.
+//
+// Base-3 codes (five trits per byte, byte = sum_i d_i 3^i, d = t + 1;
+// mhpq.cn/news/1159370 sec. 3.1, tighter packing) take the same pipeline with
+// stages of five groups (640 trits = 128 bytes per row, so a stage starts on
+// a byte).  Digits come out of a 32-bit word of four code bytes with integer
+// arithmetic on two 16-bit lanes: p_k = floor(b / 3^k) from
+// floor(v / 3) = (85 v + 80) >> 8 (exact for v <= 242), the high bytes of
+// the lanes gathered by one byte permute, and digit i of every byte is
+// p_i - 3 p_(i+1) in one multiply-add on the whole word (no carry or borrow
+// crosses a byte).  Digit word i of code word q (digit i of its four bytes)
+// goes to tensor-memory column 5 q + i of the stage, so a group of 128 trits
+// no longer fills whole columns of its own: its MMAs run over a window of
+// 8-column K steps that covers its trits (5 or 6 steps), and the activations
+// of that group sit at the matching places of a B block of its own, zero
+// elsewhere, so the trits of the neighbouring groups that share the window
+// add nothing.  Digits are e4m3 bytes d * 2^-9 (no 4c class), and
+// sum_k t x = sum_k d x - sum_k x as before.
 //
 // Work split: a cluster of kcl CTAs owns a range of 128-row tiles; CTA rank r
 // owns the r-th slice of the K groups and rotates only that slice of x.  A
@@ -79,20 +96,42 @@ constexpr int kTmaWarp = 16;
 constexpr int kMmaWarp = 17;                  // warps 17, 18 issue the MMAs of team 0, 1
 constexpr int kEpiWarp0 = 19;                 // warps 19-22: epilogue
 constexpr int kThreads = 32 * 23;             // + 4 epilogue warps (19-22)
-// code slots in flight (four groups each); an even count, so that slot
+// code slots in flight (one stage each); an even count, so that slot
 // s % kRing always belongs to team s % 2
 constexpr int kRing = 4;
-constexpr int kAbuf = 3;                      // weight (A) buffers in tensor memory, one stage each
-constexpr int kAPeriod = 2 * kAbuf;           // stages between two uses of one A buffer by one team
-static_assert(kAbuf % 2 == 1, "A buffers alternate between the two teams");
 constexpr int kDbuf = 2;                      // accumulator buffers: buffer t belongs to team t's stages
-constexpr int kSlotBytes = 128 * 128;         // 128 rows x 128 bytes (four groups): one stage
+constexpr int kSlotBytes = 128 * 128;         // 128 rows x 128 bytes of codes: one stage
 constexpr int kZeroBytes = 288;               // B rows 8..15 of the 8-row layout (two core matrices 144 apart)
 constexpr int kTmemCols = 512;                // one CTA per SM
-constexpr uint32_t kAcol = 0;                 // A buffer b: columns 128 b .. 128 b + 127 (4 groups x 32)
-constexpr uint32_t kDcol = 128 * kAbuf;       // D buffer b: columns kDcol + 64 b .. + 63 (4 groups x 16)
-static_assert(kDcol + 64 * kDbuf <= kTmemCols, "tensor memory budget");
+constexpr int kAbufMax = 3;
 constexpr uint32_t kFaultTimeout = 2u;
+
+// Per code format: groups per stage (kGS), weight (A) buffers in tensor
+// memory (kAbuf, one stage each), A columns per stage (kACols) and K steps
+// of 32 per group in the B layout (kSteps).  2-bit: four groups of 32
+// columns; base-3: five groups in 160 columns, each group's MMAs over a
+// window of up to six K steps.  A buffer b of a stage: columns b kACols ..;
+// D buffer b: kDcol + b kDCols .. (16 accumulator columns per group).
+template <bool B3> struct Fmt;
+template <> struct Fmt<false> { static constexpr int kGS = 4, kAbuf = 3, kACols = 128, kSteps = 4; };
+template <> struct Fmt<true> { static constexpr int kGS = 5, kAbuf = 2, kACols = 160, kSteps = 6; };
+template <bool B3>
+struct FmtGeo : Fmt<B3> {
+  using F = Fmt<B3>;
+  // stages between two uses of one A buffer by one team (buffers alternate
+  // between the teams when their count is odd)
+  static constexpr int kAPeriod = (F::kAbuf % 2) ? 2 * F::kAbuf : F::kAbuf;
+  static constexpr uint32_t kDCols = 16 * F::kGS;
+  static constexpr uint32_t kDcol = (uint32_t)(F::kACols * F::kAbuf);
+  static_assert(kDcol + kDCols * kDbuf <= kTmemCols, "tensor memory budget");
+  static_assert(F::kAbuf <= kAbufMax, "barrier arrays");
+};
+
+// Base-3 group windows: group h of a stage (trits 128 h .. 128 h + 127, in
+// bytes 25.6 h ..) starts at A column kWin0[h] (a multiple of 8) and spans
+// kWinN[h] K steps of 8 columns.
+constexpr int win0(int h) { return h == 0 ? 0 : h == 1 ? 24 : h == 2 ? 56 : h == 3 ? 88 : 120; }
+constexpr int winn(int h) { return (h == 0 || h == 4) ? 5 : 6; }
 
 // kind::f8f6f4: fp32 accumulator, A = B = e4m3, both K-major, N = 16, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
@@ -110,12 +149,13 @@ template <> struct Lay<2> { static constexpr int kP = 1, kRows = 16, kMM = 5; };
 template <> struct Lay<3> { static constexpr int kP = 2, kRows = 16, kMM = 8; };
 template <> struct Lay<4> { static constexpr int kP = 3, kRows = 16, kMM = 16; };
 
-template <int V>
+template <int V, bool B3>
 struct Geo {
   static constexpr int kP = Lay<V>::kP, kRows = Lay<V>::kRows, kMM = Lay<V>::kMM;
+  static constexpr int kGS = Fmt<B3>::kGS, kSteps = Fmt<B3>::kSteps;
   static constexpr int kLbo = 16 * kRows + 16;
   static constexpr int kUnit = 2 * kLbo;
-  static constexpr int kGroupB = 4 * kP * kUnit;
+  static constexpr int kGroupB = kSteps * kP * kUnit;
   static constexpr int kZs = (kMM + 1) & ~1;       // ztab entries per group (even: read in pairs)
   static constexpr int kCw = kRows == 8 ? 8 : 16;  // accumulator columns read per group
   static constexpr int kGw = kMM > 5 ? 1 : 2;      // groups read per tensor-memory wait
@@ -148,13 +188,16 @@ int variant_of(int64_t M) { return M <= 2 ? 1 : M <= 5 ? 2 : M <= 8 ? 3 : 4; }
 // gives every barrier one sequential producer and one sequential consumer and
 // so keeps each waiter within one phase of the barrier (a parity wait cannot
 // pass on an older phase):
-//   a_full[b][t]  team t's decode of a stage in b -> MMA warp t (every 6th stage);
-//   a_free[b][t]  MMA warp 1 - t's reads of b done -> team t, which writes b next.
+//   a_full[b][t]  team t's decode of a stage in b -> MMA warp t;
+//   a_free[b][t]  the reads of b by the MMA warp of the stage before -> team t,
+//                 which writes b next.
+// With three buffers (2-bit) a buffer alternates between the teams (every
+// 6th stage is team t's in buffer b); with two (base-3) buffer t is team t's.
 struct Ctl {
   uint64_t full[kRing];      // TMA -> decoders (slot s % kRing: always team s % 2)
   uint64_t empty[kRing];     // decoders -> TMA
-  uint64_t a_full[kAbuf][2]; // decoders -> MMA
-  uint64_t a_free[kAbuf][2]; // MMA -> decoders
+  uint64_t a_full[kAbufMax][2]; // decoders -> MMA
+  uint64_t a_free[kAbufMax][2]; // MMA -> decoders
   uint64_t d_full[kDbuf]; // MMA -> epilogue
   uint64_t d_free[kDbuf]; // epilogue -> MMA
   uint64_t red_bar;       // this rank's rows: the other ranks' partial sums have landed
@@ -224,6 +267,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t r[32]) 
       "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t r[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -323,6 +372,31 @@ __device__ __forceinline__ void fwht128_strided(float v[4], int lane) {
   for (int b = 0; b < 4; ++b) v[b] = __fmul_rn(v[b], kInvSqrt128);
 }
 
+// The five base-3 digits of the four code bytes of w (byte b = sum_i d_i 3^i,
+// b <= 242): d[i] holds digit i of byte j in its byte j.  p_k = floor(b / 3^k)
+// comes from p_(k-1) with floor(v / 3) = (85 v + 80) >> 8 (exact for
+// v <= 242) on two 16-bit lanes per word (bytes 0, 2 and 1, 3), whose high
+// bytes one byte permute gathers; then digit i = p_i - 3 p_(i+1) for the
+// whole word at once (3 p_(i+1) <= p_i <= 242 in every byte: no carry or
+// borrow crosses a byte).
+__device__ __forceinline__ void trits5(uint32_t w, uint32_t d[5]) {
+  uint32_t lo = w & 0x00ff00ffu, hi = __byte_perm(w, 0u, 0x4341u);
+  uint32_t p[5];
+  p[0] = w;
+#pragma unroll
+  for (int k = 1; k < 5; ++k) {
+    const uint32_t vl = lo * 85u + 0x00500050u, vh = hi * 85u + 0x00500050u;
+    p[k] = __byte_perm(vl, vh, 0x7351u);
+    if (k < 4) {
+      lo = __byte_perm(vl, 0u, 0x4341u);
+      hi = __byte_perm(vh, 0u, 0x4341u);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = p[i] - 3u * p[i + 1];
+  d[4] = p[4];
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
@@ -352,9 +426,11 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ct
 
 // Shared memory (1024-aligned): [code ring][B: groups_cap x kGroupB][zeros kZeroBytes]
 // [ztab: groups_cap x kZs x {pw Zt, pw}][partial sums: tiles_cap x kcl x M x 128 / kcl][Ctl]
-template <int V>
+template <int V, bool B3>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__ CUtensorMap cmap, const Params p) {
-  using Gm = Geo<V>;
+  using Gm = Geo<V, B3>;
+  using Fg = FmtGeo<B3>;
+  constexpr int kGS = Fg::kGS, kAbuf = Fg::kAbuf, kAPeriod = Fg::kAPeriod;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* ring = smem;
@@ -371,8 +447,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   const int lgk = __ffs(p.kcl) - 1;
   const int64_t cluster = blockIdx.x >> lgk;
   const int64_t G = p.K / 128;
-  const int64_t g0 = (G * rank) >> lgk, g1 = (G * (rank + 1)) >> lgk;
-  const int ng = (int)(g1 - g0), nch = (ng + 3) >> 2;  // four-group stages per tile
+  // K slice of this rank: whole groups (2-bit), whole five-group stages (base-3,
+  // so that a slice starts on a code byte); nch stages per tile
+  int64_t g0, g1;
+  if constexpr (B3) {
+    const int64_t nst = (G + 4) / 5;
+    g0 = 5 * ((nst * rank) >> lgk);
+    g1 = std::min<int64_t>(5 * ((nst * (rank + 1)) >> lgk), G);
+  } else {
+    g0 = (G * rank) >> lgk;
+    g1 = (G * (rank + 1)) >> lgk;
+  }
+  const int ng = (int)(g1 - g0), nch = (ng + kGS - 1) / kGS;
+  // TMA x (bytes) of stage lc of the slice
+  auto stage_x = [&](int lc) -> int {
+    return B3 ? (int)((g0 / 5 + lc) * 128) : (int)((g0 + 4 * lc) * 32);
+  };
   const int64_t T = (p.N + 127) / 128;
   int64_t t0, t1;
   if (T * p.clusters <= 0xffffffffll) {
@@ -393,8 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     for (; issued_loads < S && issued_loads < kRing; ++issued_loads) {
       const int l = issued_loads, tile = l / nch, lc = l - tile * nch;
       mbar_arrive_expect_tx(&ctl->full[l], kSlotBytes);
-      tma_load_2d(smem_u32(ring + l * kSlotBytes), &cmap, (int)((g0 + 4 * lc) * 32), (int)((t0 + tile) * 128),
-                  &ctl->full[l]);
+      tma_load_2d(smem_u32(ring + l * kSlotBytes), &cmap, stage_x(lc), (int)((t0 + tile) * 128), &ctl->full[l]);
     }
   };
   if (threadIdx.x == 0) {
@@ -472,23 +561,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     E = E < -100 ? -100 : (E > 100 ? 100 : E);
     const float up = __uint_as_float((uint32_t)(127 + E) << 23);
     const float pw = __uint_as_float((uint32_t)(127 + 9 - E) << 23);
-    // odd classes j meet the 4c weights: their values are stored divided by 4
-    const float cls = (jc & 1) ? 0.25f : 1.0f, acls = (jc & 1) ? 4.0f : 1.0f;
+    // 2-bit: odd classes j meet the 4c weights, so their values are stored
+    // divided by 4; base-3 digits are all plain d * 2^-9
+    const float cls = (!B3 && (jc & 1)) ? 0.25f : 1.0f, acls = (!B3 && (jc & 1)) ? 4.0f : 1.0f;
     float u[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) u[b] = v[b] * up * cls;
     float zs = 0.0f;
-    // K step i / 2 of the group; k'' = 16 (i % 2) + 4 j + b inside it, at byte
-    // (k'' / 16) kLbo + 16 row + k'' % 16 of the unit of the piece's pass
-    unsigned char* gdst = bsm + gl * Gm::kGroupB + (i8 >> 1) * Gm::kUnit + (i8 & 1) * Gm::kLbo + 4 * jc;
+    unsigned char* gbase = bsm + gl * Gm::kGroupB;
+    // 2-bit: K step i / 2 of the group; k'' = 16 (i % 2) + 4 j + b inside it,
+    // at byte (k'' / 16) kLbo + 16 row + k'' % 16 of the unit of the piece's
+    // pass.  Base-3: element e of group h of its stage is trit 128 h + e, in
+    // code byte j = trit / 5 (digit trit % 5), which sits in byte j % 4 of
+    // A column 5 (j / 4) + digit; its place in the group's window of K steps
+    // is kappa = 4 (column - window start) + j % 4.
+    unsigned char* gdst = gbase + (i8 >> 1) * Gm::kUnit + (i8 & 1) * Gm::kLbo + 4 * jc;
+    int boff[4];
+    if constexpr (B3) {
+      const int h = (int)((g0 + gl) % 5);
+      const int w0 = win0(h);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int tr = 128 * h + 16 * i8 + jc + 4 * b, j = tr / 5, dg = tr - 5 * j;
+        const int kap = 4 * (5 * (j >> 2) + dg - w0) + (j & 3);
+        boff[b] = (kap >> 5) * Gm::kUnit + ((kap >> 4) & 1) * Gm::kLbo + (kap & 15);
+      }
+    }
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
       float r0, r1, r2, r3;
       const uint32_t lo = to_e4m3x2(u[0], u[1], r0, r1), hi = to_e4m3x2(u[2], u[3], r2, r3);
       int pass, row;
       piece_slot<V>(m, q, pass, row);
-      *reinterpret_cast<uint32_t*>(gdst + pass * 4 * Gm::kUnit + (row >> 3) * 128 + (row & 7) * 16) =
-          (lo & 0xffffu) | (hi << 16);
+      const uint32_t word = (lo & 0xffffu) | (hi << 16);
+      if constexpr (B3) {
+        unsigned char* rdst = gbase + pass * Gm::kSteps * Gm::kUnit + (row >> 3) * 128 + (row & 7) * 16;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) rdst[boff[b]] = (unsigned char)(word >> (8 * b));
+      } else {
+        *reinterpret_cast<uint32_t*>(gdst + pass * 4 * Gm::kUnit + (row >> 3) * 128 + (row & 7) * 16) = word;
+      }
       zs += (r0 + r1) + (r2 + r3);
       u[0] -= r0;
       u[1] -= r1;
@@ -509,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       for (; l < S; ++l) {
         if (!wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(&ctl->full[slot], kSlotBytes);
-        tma_load_2d(smem_u32(ring + slot * kSlotBytes), &cmap, (int)((g0 + 4 * lc) * 32), (int)((t0 + tile) * 128),
+        tma_load_2d(smem_u32(ring + slot * kSlotBytes), &cmap, stage_x(lc), (int)((t0 + tile) * 128),
                     &ctl->full[slot]);
         if (++slot == kRing) { slot = 0; ++use; }
         if (++lc == nch) { lc = 0; ++tile; }
@@ -521,8 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   } else if (warp < kDecWarps) {
     // ------------------------------------------------------------ decoders
     // team (warp / 8) takes the stages of its parity, so two stages are
-    // unpacked at once; warp w unpacks groups 2 ((w / 4) % 2) .. +1 of the
-    // stage for rows 32 (w % 4) .. +31
+    // unpacked at once; warp w unpacks half (w / 4) % 2 of the stage's code
+    // bytes (2-bit: groups 2 ((w / 4) % 2) .. +1) for rows 32 (w % 4) .. +31
     const int team = warp >> 3, quad = warp & 3, gh = (warp >> 2) & 1;
     const int r = quad * 32 + lane;  // row inside the tile = tensor-memory lane
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
@@ -534,8 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     for (int q = 0; q < 4; ++q) off[q] = rbase + ((((uint32_t)(4 * gh + q)) ^ rx) << 4);
     int slot = team, use = 0;  // ring slot of stage s and its use count (s % kRing, s / kRing)
     for (int s = team; s < S; s += 2) {
-      // A buffer ab last held stage s - kAbuf (the other team's), whose MMAs
-      // are the ((s - kAbuf) / kAPeriod)-th completion a_free[ab][team] counts
+      // A buffer ab last held stage s - kAbuf, whose MMAs are the
+      // ((s - kAbuf) / kAPeriod)-th completion a_free[ab][team] counts
       const int ab = s % kAbuf;
       bool ok = wait_or_abort(&ctl->full[slot], use & 1, ctl);
       uint4 c[4];
@@ -545,20 +657,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       if (lane == 0) mbar_arrive(&ctl->empty[slot]);
       if (s >= kAbuf) ok = wait_or_abort(&ctl->a_free[ab][team], ((s - kAbuf) / kAPeriod) & 1, ctl) && ok;
       if (!__all_sync(kFull, ok)) break;  // the tensor-memory stores below are warp-collective
+      const uint32_t acol = tmem + lane_addr + (uint32_t)(ab * Fg::kACols);
+      if constexpr (B3) {
+        // 16 code words: word q of this half -> columns 80 gh + 5 q .. + 4
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t w[8] = {c[2 * h].x, c[2 * h].y, c[2 * h].z, c[2 * h].w,
-                               c[2 * h + 1].x, c[2 * h + 1].y, c[2 * h + 1].z, c[2 * h + 1].w};
-        uint32_t a[32];
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t w[8] = {c[2 * h].x, c[2 * h].y, c[2 * h].z, c[2 * h].w,
+                                 c[2 * h + 1].x, c[2 * h + 1].y, c[2 * h + 1].z, c[2 * h + 1].w};
+          uint32_t a[40];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t w4 = w[i] >> 4;
-          a[4 * i + 0] = w[i] & 0x03030303u;
-          a[4 * i + 1] = w[i] & 0x0C0C0C0Cu;
-          a[4 * i + 2] = w4 & 0x03030303u;
-          a[4 * i + 3] = w4 & 0x0C0C0C0Cu;
+          for (int i = 0; i < 8; ++i) trits5(w[i], &a[5 * i]);
+          const uint32_t col = acol + (uint32_t)(80 * gh + 40 * h);
+          tmem_st32(col, a);
+          tmem_st8(col + 32, a + 32);
         }
-        tmem_st32(tmem + lane_addr + kAcol + (uint32_t)(ab * 128 + (2 * gh + h) * 32), a);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t w[8] = {c[2 * h].x, c[2 * h].y, c[2 * h].z, c[2 * h].w,
+                                 c[2 * h + 1].x, c[2 * h + 1].y, c[2 * h + 1].z, c[2 * h + 1].w};
+          uint32_t a[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t w4 = w[i] >> 4;
+            a[4 * i + 0] = w[i] & 0x03030303u;
+            a[4 * i + 1] = w[i] & 0x0C0C0C0Cu;
+            a[4 * i + 2] = w4 & 0x03030303u;
+            a[4 * i + 3] = w4 & 0x0C0C0C0Cu;
+          }
+          tmem_st32(acol + (uint32_t)((2 * gh + h) * 32), a);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -596,20 +724,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       if (!__shfl_sync(kFull, ok ? 1 : 0, 0)) break;
       tc_fence_after();
       if (elect_one()) {
-        const uint32_t d0 = tmem + kDcol + (uint32_t)(t * 64), a0 = tmem + kAcol + (uint32_t)(ab * 128);
-        uint64_t bg = desc_g0 + (uint64_t)(4 * ch) * kStepG;
+        const uint32_t d0 = tmem + Fg::kDcol + (uint32_t)t * Fg::kDCols, a0 = tmem + (uint32_t)(ab * Fg::kACols);
+        uint64_t bg = desc_g0 + (uint64_t)(kGS * ch) * kStepG;
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
+        for (int h = 0; h < kGS; ++h) {
+          // 2-bit: the group's own 32 columns; base-3: its window of K steps
+          constexpr int kNs = Gm::kSteps;
+          const int ns = B3 ? winn(h) : 4;
+          const uint32_t ah = a0 + (uint32_t)(B3 ? win0(h) : 32 * h);
 #pragma unroll
           for (int pass = 0; pass < Gm::kP; ++pass) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              mma_f8_tmem_a(d0 + h * 16, a0 + h * 32 + i * 8, bg + (uint64_t)(4 * pass + i) * kStepU,
-                            (pass | i) != 0 ? 1u : 0u);
+            for (int i = 0; i < kNs; ++i)
+              if (i < ns)
+                mma_f8_tmem_a(d0 + h * 16, ah + i * 8, bg + (uint64_t)(kNs * pass + i) * kStepU,
+                              (pass | i) != 0 ? 1u : 0u);
           }
           bg += kStepG;
         }
-        mma_commit(&ctl->a_free[ab][t ^ 1]);  // team 1 - t writes buffer ab next (stage s + 3)
+        // the team that writes buffer ab next (stage s + kAbuf)
+        mma_commit(&ctl->a_free[ab][(kAbuf & 1) ? t ^ 1 : t]);
         mma_commit(&ctl->d_full[t]);
       }
       __syncwarp();
@@ -630,18 +764,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
 #pragma unroll
     for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
     int tile = 0, ch = 0, db = 0, duse = 0;
-    // Raw fp16 scales of the stage's four groups for this row (groups past
+    // Raw fp16 scales of the stage's kGS groups for this row (groups past
     // the slice: 0).  Each stays in its own register until it is used, so
     // the loads remain in flight meanwhile.
-    auto ld_scales = [&](int tl, int c, uint32_t (&sc)[4]) {
+    auto ld_scales = [&](int tl, int c, uint32_t (&sc)[kGS]) {
 #pragma unroll
-      for (int h = 0; h < 4; ++h) sc[h] = 0u;
+      for (int h = 0; h < kGS; ++h) sc[h] = 0u;
       const int64_t n = (t0 + tl) * 128 + r;
       if (tl >= ntiles || n >= p.N) return;
-      const uint16_t* q = p.scales + n * p.lds + g0 + 4 * c;
+      const uint16_t* q = p.scales + n * p.lds + g0 + kGS * c;
 #pragma unroll
-      for (int h = 0; h < 4; ++h)
-        if (4 * c + h < ng) sc[h] = __ldg(q + h);
+      for (int h = 0; h < kGS; ++h)
+        if (kGS * c + h < ng) sc[h] = __ldg(q + h);
     };
     // The scales are loaded kAhead stages before they are used (a DRAM miss
     // takes longer than a stage).  The stage loop is unrolled by kAhead so
@@ -649,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     // (converted) at the start of its stage, then reloaded for the stage
     // kAhead later; (ltl, lc) is the next stage to load.
     constexpr int kAhead = Gm::kScAhead;
-    uint32_t scq[kAhead][4];
+    uint32_t scq[kAhead][kGS];
     int ltl = 0, lc = 0;
 #pragma unroll
     for (int i = 0; i < kAhead; ++i) {
@@ -665,10 +799,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     const uint32_t push_bar = local ? 0u : map_rank(&ctl->red_bar, owner);
     const float4* ztab4 = reinterpret_cast<const float4*>(ztab);
     // one stage; false when a wait gave up
-    auto stage = [&](uint32_t (&slot)[4]) -> bool {
-      float sh[4];
+    auto stage = [&](uint32_t (&slot)[kGS]) -> bool {
+      float sh[kGS];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) sh[h] = __half2float(__ushort_as_half((uint16_t)slot[h]));
+      for (int h = 0; h < kGS; ++h) sh[h] = __half2float(__ushort_as_half((uint16_t)slot[h]));
       ld_scales(ltl, lc, slot);
       if (++lc == nch) { lc = 0; ++ltl; }
       const int ntl = (ch + 1 == nch) ? tile + 1 : tile, nc = (ch + 1 == nch) ? 0 : ch + 1;
@@ -676,14 +810,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       if (!__all_sync(kFull, ok)) return false;  // the tensor-memory loads below are warp-collective
       tc_fence_after();
       // kGw groups per tensor-memory wait (fewer registers for the wide layouts)
+      constexpr int kHp = (kGS + Gm::kGw - 1) / Gm::kGw;
 #pragma unroll
-      for (int hp = 0; hp < 4 / Gm::kGw; ++hp) {
+      for (int hp = 0; hp < kHp; ++hp) {
         uint32_t d[Gm::kGw][kCw];
-        const uint32_t dcol = tmem + lane_addr + kDcol + (uint32_t)(db * 64 + hp * 16 * Gm::kGw);
+        const uint32_t dcol = tmem + lane_addr + Fg::kDcol + (uint32_t)db * Fg::kDCols + (uint32_t)(hp * 16 * Gm::kGw);
 #pragma unroll
-        for (int u = 0; u < Gm::kGw; ++u) tmem_ld(dcol + 16 * u, d[u]);
+        for (int u = 0; u < Gm::kGw; ++u) {
+          if (Gm::kGw * hp + u < kGS) {
+            tmem_ld(dcol + 16 * u, d[u]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < kCw; ++i) d[u][i] = 0u;
+          }
+        }
         tmem_ld_wait(d);
-        if (hp == 4 / Gm::kGw - 1) {  // the whole accumulator buffer has been read
+        if (hp == kHp - 1) {  // the whole accumulator buffer has been read
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl->d_free[db]);
@@ -691,6 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
 #pragma unroll
         for (int u = 0; u < Gm::kGw; ++u) {
           const int h = Gm::kGw * hp + u;
+          if (h >= kGS) continue;
           float vs[kMM];
 #pragma unroll
           for (int m = 0; m < kMM; ++m) {
@@ -702,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
               vs[m] = __uint_as_float(d[u][m]);
           }
           // {pw Zt, pw} of (group, m) and (group, m + 1); zero past the slice and for m >= M
-          const float4* z = ztab4 + (((4 * ch + h) * Gm::kZs) >> 1);
+          const float4* z = ztab4 + (((kGS * ch + h) * Gm::kZs) >> 1);
 #pragma unroll
           for (int m = 0; m < kMM; m += 2) {
             if (m < M) {
@@ -788,20 +931,33 @@ EncodeTiledFn encode_fn() {
   return f;
 }
 
-template <int V>
+template <int V, bool B3>
 size_t smem_bytes_v(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
-  return 1024 + (size_t)kRing * kSlotBytes + (size_t)groups_cap * Geo<V>::kGroupB + kZeroBytes +
-         (size_t)groups_cap * Geo<V>::kZs * sizeof(float2) + (size_t)tiles_cap * 128 * M * sizeof(float) +
+  return 1024 + (size_t)kRing * kSlotBytes + (size_t)groups_cap * Geo<V, B3>::kGroupB + kZeroBytes +
+         (size_t)groups_cap * Geo<V, B3>::kZs * sizeof(float2) + (size_t)tiles_cap * 128 * M * sizeof(float) +
          sizeof(Ctl);
 }
 
-size_t smem_bytes(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
+template <bool B3>
+size_t smem_bytes_f(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
   switch (variant_of(M)) {
-    case 1: return smem_bytes_v<1>(groups_cap, tiles_cap, M);
-    case 2: return smem_bytes_v<2>(groups_cap, tiles_cap, M);
-    case 3: return smem_bytes_v<3>(groups_cap, tiles_cap, M);
-    default: return smem_bytes_v<4>(groups_cap, tiles_cap, M);
+    case 1: return smem_bytes_v<1, B3>(groups_cap, tiles_cap, M);
+    case 2: return smem_bytes_v<2, B3>(groups_cap, tiles_cap, M);
+    case 3: return smem_bytes_v<3, B3>(groups_cap, tiles_cap, M);
+    default: return smem_bytes_v<4, B3>(groups_cap, tiles_cap, M);
   }
+}
+
+size_t smem_bytes(bool b3, int64_t groups_cap, int64_t tiles_cap, int64_t M) {
+  return b3 ? smem_bytes_f<true>(groups_cap, tiles_cap, M) : smem_bytes_f<false>(groups_cap, tiles_cap, M);
+}
+
+// Groups per CTA the shared layout holds: the largest K slice a rank gets,
+// in whole stages (2-bit: slices of whole groups; base-3: of five-group
+// stages).
+int64_t groups_cap_of(bool b3, int64_t G, int64_t kcl) {
+  if (b3) return 5 * (((G + 4) / 5 + kcl - 1) / kcl);
+  return 4 * (((G + kcl - 1) / kcl + 3) / 4);
 }
 
 // Clusters of kcl CTAs that can be resident at once (a cluster lives on one
@@ -815,7 +971,8 @@ int max_active_clusters(int kcl) {
   int v = cache[dev][slot].load(std::memory_order_acquire);
   if (v > 0) return v;
   const int smem = device_max_smem_optin();
-  if (cudaFuncSetAttribute(k_gemv_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+  if (cudaFuncSetAttribute(k_gemv_tc<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(device_sm_count() * kcl));
   cfg.blockDim = dim3(kThreads);
@@ -827,7 +984,7 @@ int max_active_clusters(int kcl) {
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&v, k_gemv_tc<1>, &cfg) != cudaSuccess || v < 1) {
+  if (cudaOccupancyMaxActiveClusters(&v, k_gemv_tc<1, false>, &cfg) != cudaSuccess || v < 1) {
     (void)cudaGetLastError();
     return 0;
   }
@@ -835,14 +992,14 @@ int max_active_clusters(int kcl) {
   return v;
 }
 
-template <int V>
+template <int V, bool B3>
 cudaError_t launch_v(const CUtensorMap& map, const Params& p, size_t smem, cudaStream_t s) {
   // raise the kernel's shared-memory limit only when a launch needs more
   static std::atomic<int> smem_set[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem_set[dev].load(std::memory_order_acquire) < (int)smem) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemv_tc<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_gemv_tc<V, B3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int cur = smem_set[dev].load(std::memory_order_acquire);
     while (cur < (int)smem && !smem_set[dev].compare_exchange_weak(cur, (int)smem)) {
@@ -862,7 +1019,7 @@ cudaError_t launch_v(const CUtensorMap& map, const Params& p, size_t smem, cudaS
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemv_tc<V>, map, p);
+  return cudaLaunchKernelEx(&cfg, k_gemv_tc<V, B3>, map, p);
 }
 
 // Cost model of the busiest CTA, in units of 1/24 stage: a stage streams
@@ -885,27 +1042,30 @@ unsigned int take_fault_gemv() {
 // Work split for M rows of x: kcl in {1, 2, 4, 8} CTAs per cluster share a
 // tile range and split its K groups; at most as many clusters as can be
 // resident at once (one wave).  The choice minimises the cost model of the
-// busiest CTA (its stages -- four groups of one 128-row tile -- and its
+// busiest CTA (its stages -- 128 code bytes of one 128-row tile -- and its
 // prologue items); ties go to fewer CTAs.  Returns false when no split fits
 // in shared memory.
-bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int* kcl_out, int* clusters_out) {
+bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* clusters_out) {
   if (N <= 0 || K <= 0 || K % 128 != 0 || M < 1 || M > 16) return false;
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return false;
+  const bool b3 = fmt == TQ_PACK_BASE3;
   const int64_t G = K / 128, T = (N + 127) / 128;
+  const int64_t gs = b3 ? 5 : 4;
   const int sms = device_sm_count();
   if (sms <= 0) return false;
   const int64_t smem_max = device_max_smem_optin();
   int64_t best = 0, best_kcl = 0, best_c = 0;
   for (int64_t kcl = 1; kcl <= 8; kcl *= 2) {
-    if (kcl > G) break;
+    if (kcl > (b3 ? (G + gs - 1) / gs : G)) break;  // at least one group (2-bit) / stage (base-3) per rank
     int64_t c = max_active_clusters((int)kcl);
     if (c > sms / kcl) c = sms / kcl;
     if (c > T) c = T;
     if (c < 1) continue;
-    const int64_t gslice = (G + kcl - 1) / kcl;
-    const int64_t gcap = 4 * ((gslice + 3) / 4);
+    const int64_t gcap = groups_cap_of(b3, G, kcl);
+    const int64_t gslice = b3 ? std::min(gcap, G) : (G + kcl - 1) / kcl;
     const int64_t tcap = (T + c - 1) / c;
-    if ((int64_t)smem_bytes(gcap, tcap, M) > smem_max) continue;
-    const int64_t cost = tcap * (gcap / 4) * kItemsPerStage + gslice * M;
+    if ((int64_t)smem_bytes(b3, gcap, tcap, M) > smem_max) continue;
+    const int64_t cost = tcap * (gcap / gs) * kItemsPerStage + gslice * M;
     if (best_kcl == 0 || cost < best || (cost == best && c * kcl < best_c * best_kcl)) {
       best = cost;
       best_kcl = kcl;
@@ -918,33 +1078,50 @@ bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int* kcl_out, int* clusters_o
   return true;
 }
 
-// 1: one launch takes all M rows; 2: two launches of ceil(M / 2) and
-// floor(M / 2) rows (the B layout of all M rows does not fit); 0: neither.
-int gemv_tc_launches(int64_t N, int64_t K, int64_t M) {
+// Launches that take M rows of x: the rows are split into the fewest
+// launches of at most m_fit rows each, m_fit the most rows one launch's
+// shared-memory layout holds (the B layout grows with M), at most
+// kMaxLaunches launches; 0 when the shape does not suit the kernel.
+constexpr int kMaxLaunches = 4;
+int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt) {
   int kcl = 0, c = 0;
-  if (plan_gemv_tc(N, K, M, &kcl, &c)) return 1;
-  if (M > 1 && plan_gemv_tc(N, K, (M + 1) / 2, &kcl, &c) && plan_gemv_tc(N, K, M / 2, &kcl, &c)) return 2;
+  for (int64_t m = M; m >= 1; --m) {
+    if (!plan_gemv_tc(N, K, m, fmt, &kcl, &c)) continue;
+    const int64_t l = (M + m - 1) / m;
+    return l <= kMaxLaunches ? (int)l : 0;
+  }
   return 0;
 }
 
-cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,
-                           int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, bool prefetch,
-                           cudaStream_t s) {
+cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds,
+                           int64_t N, int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
+                           bool prefetch, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
+  const bool b3 = fmt == TQ_PACK_BASE3;
   const int64_t G = K / 128, T = (N + 127) / 128;
   int kcl = 0, clusters = 0;
-  if (!plan_gemv_tc(N, K, M, &kcl, &clusters)) {
-    if (gemv_tc_launches(N, K, M) != 2) return cudaErrorNotSupported;
-    const int64_t m1 = (M + 1) / 2;
-    cudaError_t e = launch_gemv_tc(codes, ldc, scales, lds, N, K, x, ldx, m1, y, ldy, prefetch, s);
-    if (e != cudaSuccess) return e;
-    return launch_gemv_tc(codes, ldc, scales, lds, N, K, static_cast<const uint16_t*>(x) + m1 * ldx, ldx, M - m1,
-                          y + m1 * ldy, ldy, prefetch, s);
+  if (!plan_gemv_tc(N, K, M, fmt, &kcl, &clusters)) {
+    // several launches, the rows of x split as evenly as possible
+    const int l = gemv_tc_launches(N, K, M, fmt);
+    if (l < 2) return cudaErrorNotSupported;
+    int64_t m0 = 0;
+    for (int i = 0; i < l; ++i) {
+      const int64_t mi = (M - m0) / (l - i);
+      cudaError_t e = launch_gemv_tc(codes, ldc, fmt, scales, lds, N, K, static_cast<const uint16_t*>(x) + m0 * ldx,
+                                     ldx, mi, y + m0 * ldy, ldy, prefetch, s);
+      if (e != cudaSuccess) return e;
+      m0 += mi;
+    }
+    return cudaSuccess;
   }
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   CUtensorMap map;
-  const cuuint64_t gdim[2] = {(cuuint64_t)(K / 4), (cuuint64_t)N};
+  // 2-bit rows hold K / 4 code bytes; base-3 rows ceil(K / 5) rounded up to
+  // 16 (zero padding).  Boxes of 128 bytes past that read zeros, which meet
+  // zero activations.
+  const int64_t row_bytes = b3 ? ((K + 4) / 5 + 15) / 16 * 16 : K / 4;
+  const cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)N};
   const cuuint64_t gstride[1] = {(cuuint64_t)ldc};
   const cuuint32_t box[2] = {128, 128};
   const cuuint32_t estride[2] = {1, 1};
@@ -964,19 +1141,27 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* sc
   p.M = (int)M;
   p.kcl = kcl;
   p.clusters = clusters;
-  p.groups_cap = (int)(4 * (((G + kcl - 1) / kcl + 3) / 4));
+  p.groups_cap = (int)groups_cap_of(b3, G, kcl);
   p.tiles_cap = (int)((T + clusters - 1) / clusters);
   p.prefetch = prefetch ? 1 : 0;
   const int64_t smem_max = device_max_smem_optin();
   // More than half an SM's shared memory, so no two CTAs share an SM whatever
   // the register count: each allocates all of tensor memory, and a second
   // one would block in tcgen05.alloc while its cluster peers wait for it.
-  const size_t smem = std::max(smem_bytes(p.groups_cap, p.tiles_cap, M), (size_t)(smem_max / 2 + 1024));
+  const size_t smem = std::max(smem_bytes(b3, p.groups_cap, p.tiles_cap, M), (size_t)(smem_max / 2 + 1024));
+  if (b3) {
+    switch (variant_of(M)) {
+      case 1: return launch_v<1, true>(map, p, smem, s);
+      case 2: return launch_v<2, true>(map, p, smem, s);
+      case 3: return launch_v<3, true>(map, p, smem, s);
+      default: return launch_v<4, true>(map, p, smem, s);
+    }
+  }
   switch (variant_of(M)) {
-    case 1: return launch_v<1>(map, p, smem, s);
-    case 2: return launch_v<2>(map, p, smem, s);
-    case 3: return launch_v<3>(map, p, smem, s);
-    default: return launch_v<4>(map, p, smem, s);
+    case 1: return launch_v<1, false>(map, p, smem, s);
+    case 2: return launch_v<2, false>(map, p, smem, s);
+    case 3: return launch_v<3, false>(map, p, smem, s);
+    default: return launch_v<4, false>(map, p, smem, s);
   }
 }
 

@@ -134,7 +134,7 @@ int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt) {
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return -(int)TQ_ERR_INVALID_ARG;
   if (N < 0) return -(int)TQ_ERR_INVALID_ARG;
   if (!k_ok(K) || M < 1 || M > 16) return -(int)TQ_ERR_SHAPE;
-  if (fmt == TQ_PACK_2BIT && tq::gemv_tc_launches(N, K, M) > 0) return TQ_GEMV_TENSOR_MEMORY;
+  if (tq::gemv_tc_launches(N, K, M, fmt) > 0) return TQ_GEMV_TENSOR_MEMORY;
   return TQ_GEMV_MMA_SYNC;
 }
 

@@ -30,16 +30,16 @@ cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16
                         int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, bool prefetch,
                         cudaStream_t s);
 
-// 2-bit codes, M = 1..16, on tcgen05 fp8 MMAs with the weights in tensor
-// memory; cudaErrorNotSupported when the shape does not suit it (the caller
-// then uses launch_gemv's kernel).  gemv_tc_launches: 1 when one launch takes
-// all M rows of x, 2 when it takes two launches of half the rows each, 0 when
-// the shape does not suit it.
-bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int* kcl, int* clusters);
-int gemv_tc_launches(int64_t N, int64_t K, int64_t M);
-cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,
-                           int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, bool prefetch,
-                           cudaStream_t s);
+// 2-bit or base-3 codes, M = 1..16, on tcgen05 fp8 MMAs with the weights in
+// tensor memory; cudaErrorNotSupported when the shape does not suit it (the
+// caller then uses launch_gemv's mma.sync kernel).  gemv_tc_launches: 1 when
+// one launch takes all M rows of x, 2 when it takes two launches of half the
+// rows each, 0 when the shape does not suit it.
+bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl, int* clusters);
+int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt);
+cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds,
+                           int64_t N, int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
+                           bool prefetch, cudaStream_t s);
 
 // Returns cudaErrorNotSupported when the shape needs more shared memory than
 // one CTA can have.

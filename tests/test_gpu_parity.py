@@ -256,26 +256,57 @@ def test_gemv_tc_skinny(orc, N, K, M):
     """Skinny M on the tensor-memory kernel: each B layout (M <= 2, 5, 8, 16
     rows of x: one, one, two and three MMA passes), ragged tiles and K
     slices, and a shape whose B for all M rows does not fit one CTA's share
-    of shared memory (two launches of half the rows)."""
+    of shared memory (two launches of half the rows each)."""
     assert tq.gemv_path(N, K, M) == tq.TQ_GEMV_TENSOR_MEMORY
     rng = np.random.default_rng(N + K + M)
     rows = np.unique(np.concatenate([rng.choice(N, size=24, replace=False), np.arange(N - 130, N)]))
     _gemv_case(orc, N, K, M, seed=N * 5 + K + M, rows=rows)
 
 
-@pytest.mark.parametrize("N,K,M", [(27648, 5120, 1), (5120, 27648, 1), (5120, 5120, 4), (27648, 5120, 16)])
-def test_gemv_tc_repeatable(N, K, M):
+@pytest.mark.parametrize("N,K,M", [
+    (27648, 5120, 1), (19457, 2560, 3), (20000, 2944, 5), (27648, 5120, 6), (4999, 27648, 8),
+    (19500, 4480, 11), (5120, 27648, 13), (2049, 1152, 16), (300, 640, 1), (129, 768, 2), (1000, 27648, 16),
+])
+def test_gemv_tc_base3(orc, N, K, M):
+    """Base-3 codes on the tensor-memory kernel: five-group stages whose K
+    slices start on a code byte, group windows that share code bytes with
+    their neighbours, a last stage of fewer than five groups (K = 768:
+    six groups; K = 2944: 23; K = 27648: 216) reading the row's zero
+    padding, every B layout, ragged tiles, and rows of x split over two to
+    four launches (5120x27648 at M = 8, 13, 16)."""
+    assert tq.gemv_path(N, K, M, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_TENSOR_MEMORY
+    rng = np.random.default_rng(N + K + M + 1)
+    rows = np.unique(np.concatenate([rng.choice(N, size=min(N, 24), replace=False),
+                                     np.arange(max(0, N - 130), N)]))
+    _gemv_case(orc, N, K, M, seed=N * 3 + K + M, fmt=tq.TQ_PACK_BASE3, rows=rows)
+
+
+def test_gemv_mma_sync_fallback_base3(orc):
+    """Base-3 codes whose K slice of B does not fit shared memory even for
+    a quarter of the rows of x take the mma.sync kernel."""
+    N, K, M = 96, 131072, 16
+    assert tq.gemv_path(N, K, M, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
+    _gemv_case(orc, N, K, M, seed=78, fmt=tq.TQ_PACK_BASE3)
+
+
+@pytest.mark.parametrize("N,K,M,fmt", [
+    (27648, 5120, 1, tq.TQ_PACK_2BIT), (5120, 27648, 1, tq.TQ_PACK_2BIT), (5120, 5120, 4, tq.TQ_PACK_2BIT),
+    (27648, 5120, 16, tq.TQ_PACK_2BIT), (27648, 5120, 1, tq.TQ_PACK_BASE3), (5120, 27648, 1, tq.TQ_PACK_BASE3),
+    (5120, 27648, 16, tq.TQ_PACK_BASE3),
+])
+def test_gemv_tc_repeatable(N, K, M, fmt):
     """The tensor-memory kernel sums in a fixed order and its barriers admit
     one schedule of results: 200 back-to-back launches (each streaming its
     weights while the previous one finishes) give the same bits as the
     first, and no bounded wait ran out."""
     W = synth.weights(N, K, 41, dtype="bf16")
-    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    c2, c3, s = tq.quantize_pack(to_dev_bf16(W), fmt)
+    codes = c2 if fmt == tq.TQ_PACK_2BIT else c3
     x = to_dev_bf16(synth.activations(M, K, 42))
     outs = [torch.empty(M, N, device="cuda") for _ in range(200)]
     torch.cuda.synchronize()
     for y in outs:
-        tq.gemv(c2, s, x, K, out=y, weights_ready=True)
+        tq.gemv(codes, s, x, K, fmt, out=y, weights_ready=True)
     tq.device_fault()
     for y in outs[1:]:
         assert torch.equal(y, outs[0])
@@ -303,21 +334,20 @@ def test_gemv_tc_reads_no_stale_shared_memory(N, K, M):
 
 
 def test_gemv_mma_sync_fallback_2bit(orc):
-    """2-bit codes whose K slice of B does not fit shared memory even for half
-    the rows of x take the mma.sync kernel."""
-    N, K, M = 96, 65536, 16
+    """2-bit codes whose K slice of B does not fit shared memory even for a
+    quarter of the rows of x take the mma.sync kernel."""
+    N, K, M = 96, 131072, 16
     assert tq.gemv_path(N, K, M) == tq.TQ_GEMV_MMA_SYNC
     _gemv_case(orc, N, K, M, seed=77)
 
 
 def test_gemv_path_of_benchmark_shapes():
-    """2-bit codes take the tensor-memory kernel for every M of the benchmark;
-    base-3 codes the mma.sync kernel."""
+    """Both code formats take the tensor-memory kernel for every M of the
+    benchmark."""
     for N, K in [(27648, 5120), (5120, 27648), (5120, 5120), (1, 128)]:
         for M in (1, 2, 4, 8, 16):
             assert tq.gemv_path(N, K, M) == tq.TQ_GEMV_TENSOR_MEMORY
-    assert tq.gemv_path(27648, 5120, 1, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
-    assert tq.gemv_path(5120, 27648, 16, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
+            assert tq.gemv_path(N, K, M, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_TENSOR_MEMORY
 
 
 @pytest.mark.parametrize("N,K,M", [(27648, 5120, 1), (512, 1280, 1), (512, 1280, 4), (5120, 27648, 16)])
