@@ -189,7 +189,7 @@ def build_stack(tq, torch, dev, seed: int, keep_weights: bool = False):
             del Wb
         stack.append(mats)
         weights.append(wl)
-    return (stack, weights) if keep_weights else stack
+    return stack, weights
 
 
 def activations(torch, dev, K: int, M: int, seed: int):

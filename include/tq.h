@@ -138,8 +138,17 @@ TQ_API tq_status tq_gemv(const uint8_t *codes, int64_t ldc, int fmt, const uint1
  *       streaming them while that preceding work is still finishing
  *       (programmatic dependent launch); x is still read only after it has
  *       finished.  Without the flag every input waits for it.
+ *   TQ_GEMV_TEST_STALL (for testing the failure path, not for production
+ *       use): the first CTA of the tensor-memory kernel never issues the
+ *       copy of its first stage of codes, so its pipeline waits run out, and
+ *       every bounded wait of the launch gives up after about 20 ms instead
+ *       of about 2 s.  The launch winds down as after a real stall (no trap,
+ *       no fault, the context stays usable); tq_device_fault then returns
+ *       TQ_ERR_TIMEOUT and the rows of y of the stalled CTA's cluster are not
+ *       written.  TQ_ERR_UNSUPPORTED when the shape takes the mma.sync
+ *       kernel (which has no waits).
  * Unknown flag bits: TQ_ERR_INVALID_ARG.  Everything else as tq_gemv. */
-enum { TQ_GEMV_WEIGHTS_READY = 1 };
+enum { TQ_GEMV_WEIGHTS_READY = 1, TQ_GEMV_TEST_STALL = 0x100 };
 TQ_API tq_status tq_gemv_ex(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
                             int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
                             unsigned int flags, tq_stream stream);
@@ -190,9 +199,18 @@ TQ_API tq_status tq_gemm(const uint8_t *codes, int64_t ldc, int fmt, const uint1
  * the same x').  Whether x matches is the caller's contract: it is not
  * checked; with a workspace that holds no x' of this M and K the output is
  * meaningless, but every access stays inside the workspace.  x is still
- * validated like any argument, though not read.  Unknown flag bits return
- * TQ_ERR_INVALID_ARG. */
-enum { TQ_GEMM_REUSE_ROTATED = 1 };
+ * validated like any argument, though not read.
+ *
+ * TQ_GEMM_TEST_STALL (for testing the failure path, not for production
+ * use): the first CTA of the GEMM never issues the copy of its first stage
+ * of activations, so its pipeline waits run out, and every bounded wait of
+ * the launch gives up after about 20 ms instead of about 2 s.  The launch
+ * winds down as after a real stall (no trap, no fault, the context stays
+ * usable); tq_gemm_check_range then returns TQ_ERR_TIMEOUT and y is not
+ * meaningful.
+ *
+ * Unknown flag bits return TQ_ERR_INVALID_ARG. */
+enum { TQ_GEMM_REUSE_ROTATED = 1, TQ_GEMM_TEST_STALL = 0x100 };
 TQ_API tq_status tq_gemm_ex(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
                   int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
                   void *workspace, size_t ws_bytes, unsigned int flags, tq_stream stream);

@@ -68,6 +68,7 @@ struct SmemCtl {
   uint64_t full_b[kStages];
   uint64_t empty[kStages];
   uint64_t done;
+  unsigned long long wait_ns;  // limit of every bounded wait of this launch
   uint32_t tmem_base;
   int abort;
 };
@@ -189,10 +190,14 @@ struct Params {
   int vec_store;  // y 16-byte aligned and ldy % 4 == 0: rows can take 16-byte stores
   int tma_y;      // ymap describes y (M x N fp32, row pitch ldy): blocks leave by TMA store
   int tma_part;   // pmap describes the partial tiles ([unit * BM + row][bn] fp32)
+  // Failure-path test: CTA stall_cta (-1: none) never issues the copy of its
+  // first x' stage, so its waits run out; wait_ns bounds every wait.
+  int stall_cta;
+  unsigned long long wait_ns;
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SmemCtl* ctl, uint32_t* flag) {
-  if (mbar_wait_abortable(bar, parity, &ctl->abort)) return true;
+  if (mbar_wait_abortable(bar, parity, &ctl->abort, ctl->wait_ns)) return true;
   atomicOr(flag, kFaultTimeout);
   return false;
 }
@@ -231,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->done, 1);
     ctl->abort = 0;
+    ctl->wait_ns = p.wait_ns;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -253,12 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; s < nk; ++s) {
         const int slot = s % kStages, use = s / kStages;
         if (use > 0 && !wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl, p.flag)) break;
+        if (s == 0 && (int)blockIdx.x == p.stall_cta) continue;  // failure-path test: never arrives
         mbar_arrive_expect_tx(&ctl->full_a[slot], kAStage);
         tma_load_2d(smem_u32(a_ring + slot * kAStage), &xmap, (s0 + s) * BK, (int)m0, &ctl->full_a[slot]);
       }
       // loads issued but possibly not consumed: let them land before exit
       for (int q = (s > kStages ? s - kStages : 0); q < s; ++q)
-        (void)mbar_wait(&ctl->full_a[q % kStages], (q / kStages) & 1);
+        (void)mbar_wait(&ctl->full_a[q % kStages], (q / kStages) & 1, ctl->wait_ns);
     }
     __syncwarp();  // block-wide barriers must not be reached by part of a warp
   } else if (warp == kMmaWarp) {
@@ -523,7 +530,7 @@ static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes) {
 
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
                         const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, void* split_ws,
-                        size_t split_bytes, cudaStream_t s) {
+                        size_t split_bytes, cudaStream_t s, bool test_stall) {
   if (N == 0 || M == 0) return cudaSuccess;
   if ((int64_t)device_max_smem_optin() < (int64_t)kGemmSmem) return cudaErrorNotSupported;
   EncodeTiledFn enc = encode_fn();
@@ -548,6 +555,8 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   p.y = y;
   p.ldy = ldy;
   p.flag = flag;
+  p.stall_cta = test_stall ? 0 : -1;
+  p.wait_ns = test_stall ? kTestWaitLimitNs : kWaitLimitNs;
   p.n_tiles_m = (int)((M + BM - 1) / BM);
   const GemmPlan g = gemm_plan(N, M, K, split_ws != nullptr ? split_bytes : 0);
   p.bn = g.bn;

@@ -201,6 +201,7 @@ struct Ctl {
   uint64_t d_full[kDbuf]; // MMA -> epilogue
   uint64_t d_free[kDbuf]; // epilogue -> MMA
   uint64_t red_bar;       // this rank's rows: the other ranks' partial sums have landed
+  unsigned long long wait_ns;  // limit of every bounded wait of this launch
   uint32_t tmem_base;
   int abort;
 };
@@ -219,6 +220,10 @@ struct Params {
   int groups_cap;  // groups per CTA the shared layout holds (multiple of 4)
   int tiles_cap;   // tiles per cluster the partial sums hold
   int prefetch;    // codes and scales are ready before the preceding kernel ends
+  // Failure-path test: CTA stall_cta (-1: none) never issues the copy of its
+  // first stage of codes, so its waits run out; wait_ns bounds every wait.
+  int stall_cta;
+  unsigned long long wait_ns;
 };
 // ---------------------------------------------------------------- PTX helpers
 
@@ -419,7 +424,7 @@ __device__ __forceinline__ bool elect_one() {
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ctl* ctl) {
-  if (mbar_wait_abortable(bar, parity, &ctl->abort)) return true;
+  if (mbar_wait_abortable(bar, parity, &ctl->abort, ctl->wait_ns)) return true;
   atomicOr(&g_gemv_fault, kFaultTimeout);
   return false;
 }
@@ -482,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   auto fill_ring = [&]() {
     for (; issued_loads < S && issued_loads < kRing; ++issued_loads) {
       const int l = issued_loads, tile = l / nch, lc = l - tile * nch;
+      if (l == 0 && (int)blockIdx.x == p.stall_cta) continue;  // failure-path test: never arrives
       mbar_arrive_expect_tx(&ctl->full[l], kSlotBytes);
       tma_load_2d(smem_u32(ring + l * kSlotBytes), &cmap, stage_x(lc), (int)((t0 + tile) * 128), &ctl->full[l]);
     }
@@ -505,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     // every other rank sends its partial sums of this rank's rows: ntiles x M x R floats each
     if (p.kcl > 1) mbar_arrive_expect_tx(&ctl->red_bar, (uint32_t)((p.kcl - 1) * ntiles * M * R * 4));
     ctl->abort = 0;
+    ctl->wait_ns = p.wait_ns;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -627,7 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
         if (++lc == nch) { lc = 0; ++tile; }
       }
       // loads issued but possibly never consumed: let them land before exit
-      for (int q = (l > kRing ? l - kRing : 0); q < l; ++q) (void)mbar_wait(&ctl->full[q % kRing], (q / kRing) & 1);
+      for (int q = (l > kRing ? l - kRing : 0); q < l; ++q)
+        (void)mbar_wait(&ctl->full[q % kRing], (q / kRing) & 1, ctl->wait_ns);
     }
     __syncwarp();
   } else if (warp < kDecWarps) {
@@ -657,6 +665,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       if (lane == 0) mbar_arrive(&ctl->empty[slot]);
       if (s >= kAbuf) ok = wait_or_abort(&ctl->a_free[ab][team], ((s - kAbuf) / kAPeriod) & 1, ctl) && ok;
       if (!__all_sync(kFull, ok)) break;  // the tensor-memory stores below are warp-collective
+      // order the stores below after the MMAs that read this buffer (observed
+      // through the barrier): without this fence they may overtake those reads
+      tc_fence_after();
       const uint32_t acol = tmem + lane_addr + (uint32_t)(ab * Fg::kACols);
       if constexpr (B3) {
         // 16 code words: word q of this half -> columns 80 gh + 5 q .. + 4
@@ -752,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       while (ch >= nch) ch -= nch;
     }
     // every MMA this warp issued must be complete before tensor memory is freed
-    if (s - 2 >= 0 && lane == 0) (void)mbar_wait(&ctl->d_full[t], ((s - 2) >> 1) & 1);
+    if (s - 2 >= 0 && lane == 0) (void)mbar_wait(&ctl->d_full[t], ((s - 2) >> 1) & 1, ctl->wait_ns);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
@@ -891,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   if (warp < kEpiWarp0) cluster_wait();
   bool ok = true;
   if (p.kcl > 1) {
-    ok = mbar_wait(&ctl->red_bar, 0);
+    ok = mbar_wait(&ctl->red_bar, 0, ctl->wait_ns);
     if (!ok && threadIdx.x == 0) atomicOr(&g_gemv_fault, kFaultTimeout);
   }
   if (ok && !ctl->abort) {
@@ -1095,7 +1106,7 @@ int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt) {
 
 cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds,
                            int64_t N, int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
-                           bool prefetch, cudaStream_t s) {
+                           bool prefetch, cudaStream_t s, bool test_stall) {
   if (N == 0) return cudaSuccess;
   const bool b3 = fmt == TQ_PACK_BASE3;
   const int64_t G = K / 128, T = (N + 127) / 128;
@@ -1108,7 +1119,7 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
     for (int i = 0; i < l; ++i) {
       const int64_t mi = (M - m0) / (l - i);
       cudaError_t e = launch_gemv_tc(codes, ldc, fmt, scales, lds, N, K, static_cast<const uint16_t*>(x) + m0 * ldx,
-                                     ldx, mi, y + m0 * ldy, ldy, prefetch, s);
+                                     ldx, mi, y + m0 * ldy, ldy, prefetch, s, test_stall && i == 0);
       if (e != cudaSuccess) return e;
       m0 += mi;
     }
@@ -1144,6 +1155,8 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
   p.groups_cap = (int)groups_cap_of(b3, G, kcl);
   p.tiles_cap = (int)((T + clusters - 1) / clusters);
   p.prefetch = prefetch ? 1 : 0;
+  p.stall_cta = test_stall ? 0 : -1;
+  p.wait_ns = test_stall ? kTestWaitLimitNs : kWaitLimitNs;
   const int64_t smem_max = device_max_smem_optin();
   // More than half an SM's shared memory, so no two CTAs share an SM whatever
   // the register count: each allocates all of tensor memory, and a second

@@ -112,7 +112,7 @@ tq_status tq_gemv_ex(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t*
                      int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, unsigned int flags,
                      tq_stream stream) {
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return TQ_ERR_INVALID_ARG;
-  if (flags & ~(unsigned int)TQ_GEMV_WEIGHTS_READY) return TQ_ERR_INVALID_ARG;
+  if (flags & ~(unsigned int)(TQ_GEMV_WEIGHTS_READY | TQ_GEMV_TEST_STALL)) return TQ_ERR_INVALID_ARG;
   if (N < 0) return TQ_ERR_INVALID_ARG;
   if (!k_ok(K) || M < 1 || M > 16) return TQ_ERR_SHAPE;
   if (N == 0) return TQ_OK;
@@ -121,6 +121,11 @@ tq_status tq_gemv_ex(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t*
   if (!aligned16(codes) || ldc % 16 || !aligned2(scales) || !aligned16(x) || (ldx * 2) % 16 ||
       (reinterpret_cast<uintptr_t>(y) & 3u))
     return TQ_ERR_ALIGN;
+  if (flags & TQ_GEMV_TEST_STALL) {  // only the tensor-memory kernel has waits to stall
+    if (tq::gemv_tc_launches(N, K, M, fmt) == 0) return TQ_ERR_UNSUPPORTED;
+    return from_cuda(launch_gemv_tc(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy,
+                                    (flags & TQ_GEMV_WEIGHTS_READY) != 0, (cudaStream_t)stream, true));
+  }
   return from_cuda(launch_gemv(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy,
                                (flags & TQ_GEMV_WEIGHTS_READY) != 0, (cudaStream_t)stream));
 }
@@ -158,7 +163,7 @@ tq_status tq_gemm(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* sc
 tq_status tq_gemm_ex(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
                      int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, void* workspace,
                      size_t ws_bytes, unsigned int flags, tq_stream stream) {
-  if (flags & ~(unsigned int)TQ_GEMM_REUSE_ROTATED) return TQ_ERR_INVALID_ARG;
+  if (flags & ~(unsigned int)(TQ_GEMM_REUSE_ROTATED | TQ_GEMM_TEST_STALL)) return TQ_ERR_INVALID_ARG;
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return TQ_ERR_INVALID_ARG;
   if (N < 0 || M < 0) return TQ_ERR_INVALID_ARG;
   if (!k_ok(K)) return TQ_ERR_SHAPE;
@@ -182,7 +187,7 @@ tq_status tq_gemm_ex(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t*
   }
   unsigned char* split = static_cast<unsigned char*>(workspace) + gemm_split_offset(M, K);
   return from_cuda(launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, split,
-                               ws_bytes - gemm_split_offset(M, K), s));
+                               ws_bytes - gemm_split_offset(M, K), s, (flags & TQ_GEMM_TEST_STALL) != 0));
 }
 
 tq_status tq_gemm_check_range(const void* workspace, tq_stream stream) {

@@ -37,9 +37,11 @@ cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16
 // rows each, 0 when the shape does not suit it.
 bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl, int* clusters);
 int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt);
+// test_stall: failure-path test (CTA 0 withholds a copy; waits bounded by
+// milliseconds), see TQ_GEMV_TEST_STALL.
 cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds,
                            int64_t N, int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
-                           bool prefetch, cudaStream_t s);
+                           bool prefetch, cudaStream_t s, bool test_stall = false);
 
 // Returns cudaErrorNotSupported when the shape needs more shared memory than
 // one CTA can have.
@@ -47,9 +49,11 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
 // wave (up to kMaxSplitUnits tiles of 256 x 256), split_bytes long.
 constexpr int64_t kMaxSplitUnits = 160;  // one segment per SM on up to 160 SMs
 constexpr size_t kGemmSplitBytes = (size_t)kMaxSplitUnits * 256 * 256 * sizeof(float);  // 40 MiB
+// test_stall: failure-path test (CTA 0 withholds a copy; waits bounded by
+// milliseconds), see TQ_GEMM_TEST_STALL.
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
                         const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, void* split_ws,
-                        size_t split_bytes, cudaStream_t s);
+                        size_t split_bytes, cudaStream_t s, bool test_stall = false);
 
 // Reads and clears the device status word of the GEMV kernels (non-zero:
 // a bounded wait ran out).
