@@ -19,6 +19,11 @@ Parity status of each function (what pins it, see ``tests/test_oracle.py``):
                       byte range, bit accounting
   gemv_f64            pinned: dense dequantised fp64 matmul with a scipy-built
                       block rotation, rotation invariance, delta activations
+  LayoutOracle        block sizes 64/128/256, groups 128/256, residual pass:
+                      pinned by scipy's H_n, the n = 128 functions above (bit
+                      for bit), exact normalisation constants, order-sensitive
+                      sums over 256, a closed-form residual of a delta row, the
+                      residual's error reduction, and a dense fp64 GEMV
 """
 from __future__ import annotations
 
@@ -89,6 +94,16 @@ class Oracle:
         L.tqo_pack3.argtypes = [_vp, _i64, _i64, _vp, _i64]
         L.tqo_unpack3.argtypes = [_vp, _i64, _i64, _i64, _vp]
         L.tqo_gemv_f64.argtypes = [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
+        L.tqo_norm_const_bits_n.restype = ctypes.c_uint32
+        L.tqo_norm_const_bits_n.argtypes = [ctypes.c_int]
+        L.tqo_fwht_f32.argtypes = [ctypes.c_int, _vp, _vp]
+        L.tqo_fwht_f64.argtypes = [ctypes.c_int, _vp, _vp]
+        L.tqo_quantize_group_n.restype = ctypes.c_uint16
+        L.tqo_quantize_group_n.argtypes = [ctypes.c_int, _vp, _vp]
+        L.tqo_quantize_layout_rows.argtypes = [_vp, ctypes.c_int, _i64, _i64, _vp, _i64, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, _vp, _vp]
+        L.tqo_gemv_layout_f64.argtypes = [_vp, _vp, _i64, _vp, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          _vp]
 
     # -- Hadamard -------------------------------------------------------
     def hadamard_entry(self, i: int, j: int) -> int:
@@ -208,6 +223,71 @@ class Oracle:
         assert x.shape[1] == K and S.shape == (R, K // 128)
         y = np.zeros((M, R), dtype=np.float64)
         self._L.tqo_gemv_f64(_p(T), _p(S), R, K, _p(x), M, None, R, _p(y))
+        return y
+
+
+class LayoutOracle:
+    """The transform / group / residual variants of the oracle (see
+    tqo_quantize_layout_rows in tq_oracle.c), on a loaded Oracle."""
+
+    def __init__(self, orc: Oracle):
+        self._L = orc._L
+
+    def norm_const_bits(self, n: int) -> int:
+        return int(self._L.tqo_norm_const_bits_n(n))
+
+    def fwht_f32(self, n: int, v: np.ndarray) -> np.ndarray:
+        a = np.ascontiguousarray(v, dtype=np.float32)
+        flat = a.reshape(-1, n)
+        out = np.empty_like(flat)
+        for r in range(flat.shape[0]):
+            self._L.tqo_fwht_f32(n, _p(flat[r]), _p(out[r]))
+        return out.reshape(a.shape)
+
+    def fwht_f64(self, n: int, v: np.ndarray) -> np.ndarray:
+        a = np.ascontiguousarray(v, dtype=np.float64)
+        flat = a.reshape(-1, n)
+        out = np.empty_like(flat)
+        for r in range(flat.shape[0]):
+            self._L.tqo_fwht_f64(n, _p(flat[r]), _p(out[r]))
+        return out.reshape(a.shape)
+
+    def quantize_group(self, g: int, wrot: np.ndarray) -> tuple[int, np.ndarray]:
+        w = np.ascontiguousarray(wrot, dtype=np.float32)
+        assert w.shape == (g,)
+        t = np.zeros(g, dtype=np.int8)
+        s = self._L.tqo_quantize_group_n(g, _p(w), _p(t))
+        return int(s), t
+
+    def quantize(self, W: np.ndarray, block: int = 128, group: int = 128, residual: bool = False,
+                 rows: np.ndarray | None = None) -> tuple[np.ndarray, np.ndarray]:
+        """(T int8 [R][Keff], S uint16 [R][Geff]) of W (fp32, or uint16 bf16 bits)."""
+        W = np.ascontiguousarray(W)
+        wt = 0 if W.dtype == np.float32 else 1
+        if W.dtype not in (np.float32, np.uint16):
+            raise TypeError("W must be float32 or uint16 (bf16 bits)")
+        N, K = W.shape
+        if K % max(block, group):
+            raise ValueError("K must be a multiple of the block and the group size")
+        rp = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        R = N if rp is None else rp.shape[0]
+        f = 2 if residual else 1
+        T = np.zeros((R, f * K), dtype=np.int8)
+        S = np.zeros((R, f * (K // group)), dtype=np.uint16)
+        self._L.tqo_quantize_layout_rows(_p(W), wt, K, K, _p(rp), R, block, group, 1 if residual else 0, _p(T), _p(S))
+        return T, S
+
+    def gemv(self, T: np.ndarray, S: np.ndarray, x: np.ndarray, block: int = 128, group: int = 128,
+             residual: bool = False) -> np.ndarray:
+        T = np.ascontiguousarray(T, dtype=np.int8)
+        S = np.ascontiguousarray(S, dtype=np.uint16)
+        x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+        R = T.shape[0]
+        M, K = x.shape
+        f = 2 if residual else 1
+        assert T.shape == (R, f * K) and S.shape == (R, f * (K // group))
+        y = np.zeros((M, R), dtype=np.float64)
+        self._L.tqo_gemv_layout_f64(_p(T), _p(S), K, _p(x), M, R, block, group, 1 if residual else 0, _p(y))
         return y
 
 

@@ -13,6 +13,7 @@
 #include "tq_oracle.h"
 
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 static float bits_to_f32(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
@@ -254,4 +255,151 @@ void tqo_gemv_f64(const int8_t *T, const uint16_t *S, int64_t N, int64_t K,
       }
     }
   }
+}
+
+/* ------------------------------------------- transform and group variants */
+
+/* The block transform at sizes other than 128 (dpshk sec. 2.1 builds H for
+ * any power of two; xxqk sec. 2.1/2.2 weigh block sizes against caches).
+ * n-point staged butterflies in fp32, h = 1, 2, ..., n/2, then one multiply
+ * by RN_fp32(1/sqrt(n)); n in {64, 128, 256}.  in and out may alias. */
+uint32_t tqo_norm_const_bits_n(int n) {
+  float c = (float)(1.0 / sqrt((double)n));
+  return f32_to_bits(c);
+}
+
+void tqo_fwht_f32(int n, const float *in, float *out) {
+  float v[256];
+  for (int i = 0; i < n; ++i) v[i] = in[i];
+  for (int h = 1; h < n; h *= 2) {
+    for (int i = 0; i < n; ++i) {
+      if ((i & h) == 0) {
+        float a = v[i];
+        float b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+    }
+  }
+  float c = bits_to_f32(tqo_norm_const_bits_n(n));
+  for (int i = 0; i < n; ++i) out[i] = v[i] * c;
+}
+
+/* Dense fp64 form: out[i] = sum_j H[i][j] in[j] / sqrt(n). */
+void tqo_fwht_f64(int n, const double *in, double *out) {
+  double tmp[256];
+  double c = 1.0 / sqrt((double)n);
+  for (int i = 0; i < n; ++i) {
+    double acc = 0.0;
+    for (int j = 0; j < n; ++j) acc += (double)tqo_hadamard_entry(i, j) * in[j];
+    tmp[i] = acc * c;
+  }
+  for (int i = 0; i < n; ++i) out[i] = tmp[i];
+}
+
+/* absmean over a group of g in {128, 256} weights (mhpq sec. 1.4 tries group
+ * 256: 16/256 = 0.0625 bit of scale per weight): halving tree s[i] += s[i+h]
+ * for h = g/2 .. 1 in fp32, mean = sum * 2^-log2(g) (exact), fp16 RN scale,
+ * IEEE division by the stored scale, round half to even, clamp; t = 0 when
+ * the scale is 0. */
+uint16_t tqo_quantize_group_n(int g, const float *wrot, int8_t *t) {
+  float s[256] = {0.0f};
+  for (int i = 0; i < g; ++i) s[i] = fabsf(wrot[i]);
+  for (int h = g / 2; h >= 1; h /= 2)
+    for (int i = 0; i < h; ++i) s[i] = s[i] + s[i + h];
+  float inv = 1.0f / (float)g; /* 2^-7 or 2^-8, exact */
+  float mean = s[0] * inv;
+  uint16_t sbits = tqo_f32_to_f16(mean);
+  float sc = tqo_f16_to_f32(sbits);
+  for (int i = 0; i < g; ++i) {
+    if (sc == 0.0f) { t[i] = 0; continue; }
+    float q = wrot[i] / sc;
+    float r = nearbyintf(q);
+    t[i] = (int8_t)(r > 1.0f ? 1 : (r < -1.0f ? -1 : (int)r));
+  }
+  return sbits;
+}
+
+/* Quantise rows under a layout: FWHT block size `block` in {64, 128, 256},
+ * scale group `group` in {128, 256}, and, when `residual` is set, the
+ * residual two-pass form (xxqk sec. 3, residual calibrator: the difference
+ * between the rotated weight and its ternary approximation is rotated once
+ * more by the same block transform and ternarised with its own scale).
+ *
+ * Per row, in units of u = max(block, group) consecutive weights:
+ *   w'  = FWHT_block of every block of the unit (fp32, as tqo_fwht_f32);
+ *   s1, t1 per group of w' (tqo_quantize_group_n);
+ *   residual: r = w' - s1 t1 (fp32; a zero trit dequantises to 0 whatever
+ *   the scale), r' = FWHT_block of every block of r, s2, t2 per group of r'.
+ * T is [nrows][Keff], Keff = K (2 K with residual): t1 in columns 0 .. K-1,
+ * t2 in columns K .. 2K-1.  S is [nrows][Geff], Geff = K / group (twice that
+ * with residual): the s1 first, then the s2. */
+void tqo_quantize_layout_rows(const void *W, int wt, int64_t K, int64_t ldw, const int64_t *rows,
+                              int64_t nrows, int block, int group, int residual, int8_t *T,
+                              uint16_t *S) {
+  int u = block > group ? block : group;
+  int64_t G = K / group;
+  int64_t Keff = residual ? 2 * K : K, Geff = residual ? 2 * G : G;
+  float w[256], wr[256], r[256], rr[256];
+  int8_t t1[256], t2[256];
+  for (int64_t q = 0; q < nrows; ++q) {
+    int64_t n = rows ? rows[q] : q;
+    for (int64_t k0 = 0; k0 < K; k0 += u) {
+      for (int i = 0; i < u; ++i) {
+        if (wt == 0)
+          w[i] = ((const float *)W)[n * ldw + k0 + i];
+        else
+          w[i] = tqo_bf16_to_f32(((const uint16_t *)W)[n * ldw + k0 + i]);
+      }
+      for (int b = 0; b < u; b += block) tqo_fwht_f32(block, w + b, wr + b);
+      for (int g = 0; g < u; g += group) {
+        uint16_t s1 = tqo_quantize_group_n(group, wr + g, t1 + g);
+        S[q * Geff + (k0 + g) / group] = s1;
+        float s1f = tqo_f16_to_f32(s1);
+        for (int i = 0; i < group; ++i)
+          r[g + i] = (t1[g + i] == 0) ? wr[g + i] : wr[g + i] - s1f * (float)t1[g + i];
+      }
+      for (int i = 0; i < u; ++i) T[q * Keff + k0 + i] = t1[i];
+      if (!residual) continue;
+      for (int b = 0; b < u; b += block) tqo_fwht_f32(block, r + b, rr + b);
+      for (int g = 0; g < u; g += group)
+        S[q * Geff + G + (k0 + g) / group] = tqo_quantize_group_n(group, rr + g, t2 + g);
+      for (int i = 0; i < u; ++i) T[q * Keff + K + k0 + i] = t2[i];
+    }
+  }
+}
+
+/* y under a layout, fp64: the first pass meets x' = FWHT_block(x) (dense
+ * fp64 form), the residual pass meets x'' = FWHT_block(x') -- the residual's
+ * second rotation moved onto the activations (H is symmetric and, normalised,
+ * its own inverse).  T [nrows][Keff], S [nrows][Geff] as produced above. */
+void tqo_gemv_layout_f64(const int8_t *T, const uint16_t *S, int64_t K, const float *x, int64_t M,
+                         int64_t nrows, int block, int group, int residual, double *y) {
+  int64_t G = K / group;
+  int64_t Keff = residual ? 2 * K : K, Geff = residual ? 2 * G : G;
+  double *xr = (double *)malloc((size_t)K * sizeof(double));
+  double *xrr = (double *)malloc((size_t)K * sizeof(double));
+  double blk[256];
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t k0 = 0; k0 < K; k0 += block) {
+      for (int i = 0; i < block; ++i) blk[i] = (double)x[m * K + k0 + i];
+      tqo_fwht_f64(block, blk, xr + k0);
+      tqo_fwht_f64(block, xr + k0, xrr + k0);
+    }
+    for (int64_t q = 0; q < nrows; ++q) {
+      double acc = 0.0;
+      for (int pass = 0; pass < (residual ? 2 : 1); ++pass) {
+        const double *xa = pass == 0 ? xr : xrr;
+        for (int64_t g = 0; g < G; ++g) {
+          const int8_t *t = T + q * Keff + pass * K + g * group;
+          double part = 0.0;
+          for (int i = 0; i < group; ++i) part += (double)t[i] * xa[g * group + i];
+          acc += (double)tqo_f16_to_f32(S[q * Geff + pass * G + g]) * part;
+        }
+      }
+      y[m * nrows + q] = acc;
+    }
+  }
+  free(xr);
+  free(xrr);
 }

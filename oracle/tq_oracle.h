@@ -91,6 +91,21 @@ void tqo_gemv_f64(const int8_t *T, const uint16_t *S, int64_t N, int64_t K,
                   const float *x, int64_t M, const int64_t *rows, int64_t nrows,
                   double *y);
 
+/* Transform and group variants (see tq_oracle.c): n-point FWHT, n in
+ * {64, 128, 256}, fp32 staged and fp64 dense; absmean over groups of
+ * g in {128, 256}; quantisation under a (block, group, residual) layout and
+ * its fp64 GEMV.  T has Keff = K (2K with residual) columns, S has
+ * Geff = K/group (twice that with residual). */
+uint32_t tqo_norm_const_bits_n(int n);
+void tqo_fwht_f32(int n, const float *in, float *out);
+void tqo_fwht_f64(int n, const double *in, double *out);
+uint16_t tqo_quantize_group_n(int g, const float *wrot, int8_t *t);
+void tqo_quantize_layout_rows(const void *W, int wt, int64_t K, int64_t ldw, const int64_t *rows,
+                              int64_t nrows, int block, int group, int residual, int8_t *T,
+                              uint16_t *S);
+void tqo_gemv_layout_f64(const int8_t *T, const uint16_t *S, int64_t K, const float *x, int64_t M,
+                         int64_t nrows, int block, int group, int residual, double *y);
+
 #ifdef __cplusplus
 }
 #endif

@@ -482,6 +482,234 @@ def check_rotation_invariance(orc):
     assert np.max(np.abs(Wr @ xr - W @ x)) <= 1e-12 * np.max(np.abs(W @ x))
 
 
+# --------------------------------------------- transform / group / residual
+
+def _lay(orc):
+    import oracle
+    return oracle.LayoutOracle(orc)
+
+
+def _block_h_n(K: int, n: int) -> np.ndarray:
+    H = scipy.linalg.hadamard(n).astype(np.float64) / math.sqrt(float(n))
+    return scipy.linalg.block_diag(*([H] * (K // n)))
+
+
+def check_fwht_n_definitions(orc):
+    """[dpshk] sec. 2.1 (H for any power of two) / [xxqk] sec. 2.2 (block size
+    choices): the n-point transform for n = 64, 256 equals scipy's H_n / sqrt(n)
+    (fp64 dense form to 1e-13, fp32 staged form within fp32 rounding), its
+    normalisation constant is RN_fp32(1/sqrt(n)) -- exactly 1/8 and 1/16 --
+    and at n = 128 both forms equal the pinned 128-point functions bit for
+    bit."""
+    L = _lay(orc)
+    assert L.norm_const_bits(64) == 0x3E000000 and L.norm_const_bits(256) == 0x3D800000
+    assert L.norm_const_bits(128) == C_BITS
+    rng = np.random.default_rng(81)
+    for n in (64, 256):
+        v = rng.standard_normal((4, 2 * n))
+        ref = v @ _block_h_n(2 * n, n).T
+        assert np.max(np.abs(L.fwht_f64(n, v) - ref)) <= 1e-13 * max(1.0, np.max(np.abs(ref)))
+        v32 = v.astype(np.float32)
+        out = L.fwht_f32(n, v32).astype(np.float64)
+        bound = 10 * 2.0 ** -24 * np.linalg.norm(v32.astype(np.float64), axis=1, keepdims=True) * 2
+        assert np.all(np.abs(out - ref) <= bound)
+    v = (rng.standard_normal((5, 256)) * 3).astype(np.float32)
+    assert np.array_equal(L.fwht_f32(128, v), orc.fwht128_f32(v))
+    assert np.array_equal(L.fwht_f64(128, v.astype(np.float64)), orc.fwht128_f64(v.astype(np.float64)))
+
+
+def check_fwht_n_stage_order(orc):
+    """The n-point fp32 transform runs its butterfly rounds h = 1, ..., n/2 in
+    that order, then multiplies by the constant (tensor-form restatement, as
+    for n = 128)."""
+    L = _lay(orc)
+    rng = np.random.default_rng(82)
+    for n, cbits in ((64, 0x3E000000), (256, 0x3D800000)):
+        v = (rng.standard_normal((16, n)) * 3).astype(np.float32)
+        w = v.copy()
+        h = 1
+        while h < n:
+            t = w.reshape(16, n // (2 * h), 2, h)
+            a, b = t[:, :, 0, :].copy(), t[:, :, 1, :].copy()
+            t[:, :, 0, :] = a + b
+            t[:, :, 1, :] = a - b
+            w = t.reshape(16, n)
+            h *= 2
+        w = (w * _f32(cbits)).astype(np.float32)
+        assert np.array_equal(L.fwht_f32(n, v), w)
+
+
+def check_group256_quantiser(orc):
+    """[mhpq] sec. 1.4, a scale per 256 weights: constant-magnitude groups give
+    s = fp16(a), t = sign; exact integer sums give fp16 of the exact mean
+    (factor 2^-8); on groups whose exact sum of |w'| sits on an fp16 rounding
+    midpoint the scale follows the halving tree over 256 (h = 128 .. 1) and
+    not a left-to-right sum; at g = 128 the function equals the pinned
+    128-group quantiser bit for bit."""
+    L = _lay(orc)
+    rng = np.random.default_rng(83)
+    for a in (0.02, 1.0, 3.7e-3):
+        sign = np.where(rng.random(256) < 0.5, -1.0, 1.0).astype(np.float32)
+        s, t = L.quantize_group(256, (sign * np.float32(a)).astype(np.float32))
+        assert s == _fp16(np.float32(a)) and np.array_equal(t, sign.astype(np.int8))
+    for _ in range(10):
+        ints = rng.integers(-64, 65, size=256)
+        s, _ = L.quantize_group(256, (ints / 16.0).astype(np.float32))
+        assert s == _fp16(np.float32(float(Fraction(int(np.sum(np.abs(ints))), 16 * 256))))
+    # ties: probes at +-0.5 s, +-1.5 s, ... of the stored scale (round half to
+    # even, clamp), the mean filled up to about s * 1.0003 over 256 weights
+    for s0 in (1.0, 0.0234375):
+        g128, expect, n = _tie_group(s0)
+        probes = g128[:n]
+        fill_total = 256 * s0 * 1.0003 - float(np.sum(np.abs(probes.astype(np.float64))))
+        fill = np.full(256 - n, fill_total / (256 - n), dtype=np.float32)
+        fill[1::2] *= -1
+        s, t = L.quantize_group(256, np.concatenate([probes, fill]).astype(np.float32))
+        assert s == _fp16(np.float32(s0)) and np.array_equal(t[:n], expect)
+    for _ in range(20):
+        w = (rng.standard_normal(128) * rng.uniform(1e-3, 10)).astype(np.float32)
+        (sa, ta), (sb, tb) = L.quantize_group(128, w), orc.quantize_group(w)
+        assert sa == sb and np.array_equal(ta, tb)
+    found = 0
+    for seed in range(4000):
+        r = np.random.default_rng(9000 + seed)
+        mag = np.exp(r.uniform(-6.0, 3.0, size=256)).astype(np.float32)
+        others = sum(Fraction(float(v)) for v in mag[:-1])
+        guess = np.float16(float(others + Fraction(float(mag[-1]))) / 256)
+        lo = Fraction(float(guess))
+        hi = Fraction(float(np.nextafter(guess, np.float16(np.inf))))
+        need = 256 * (lo + hi) / 2 - others
+        if need <= 0:
+            continue
+        mag[-1] = np.float32(float(need))
+        sv = mag.astype(np.float32).copy()
+        h = 128
+        while h >= 1:
+            sv[:h] = sv[:h] + sv[h:2 * h]
+            h //= 2
+        tree = _fp16(np.float32(sv[0] * np.float32(0.00390625)))
+        acc = np.float32(0.0)
+        for v in mag:
+            acc = np.float32(acc + v)
+        if tree == _fp16(np.float32(acc * np.float32(0.00390625))):
+            continue
+        s, _ = L.quantize_group(256, mag)
+        assert s == tree, (hex(s), hex(tree))
+        found += 1
+        if found == 3:
+            break
+    assert found == 3
+
+
+def check_layout_default_is_the_method(orc):
+    """Block 128, group 128, no residual pass is the method itself: the layout
+    quantiser equals the pinned one bit for bit, and so does its GEMV."""
+    L = _lay(orc)
+    rng = np.random.default_rng(84)
+    W = (rng.standard_normal((9, 768)) * 0.02).astype(np.float32)
+    T, S = L.quantize(W)
+    T0, S0 = orc.quantize(W)
+    assert np.array_equal(T, T0) and np.array_equal(S, S0)
+    x = rng.standard_normal((2, 768)).astype(np.float32)
+    assert np.max(np.abs(L.gemv(T, S, x) - orc.gemv(T0, S0, x))) <= 1e-12 * np.max(np.abs(orc.gemv(T0, S0, x)))
+
+
+def check_residual_delta_row(orc):
+    """[xxqk] sec. 3 (residual calibrator), a closed form.  A unit row e_j of W
+    rotates to c * H[:, j] (all +-c), so pass 1 gives s1 = fp16(c) and
+    t1 = H[:, j]; the residual is r = H[:, j] * d with d = c - fp32(s1)
+    exactly; its rotation is 128 d c at position j (the sums of +-d are exact,
+    one rounding in the multiply by c) and 0 elsewhere, so s2 =
+    fp16(fp32(128 d c) / 128) and t2 = sign(d) at j, 0 elsewhere."""
+    L = _lay(orc)
+    H = scipy.linalg.hadamard(128)
+    c = _f32(C_BITS)
+    s1 = _fp16(c)
+    d = np.float32(c - _fp16_val(s1))
+    assert d != 0
+    rj = np.float32(np.float32(np.float32(128.0) * d) * c)
+    s2 = _fp16(np.float32(rj * np.float32(0.0078125)))
+    for j in (0, 5, 127):
+        W = np.zeros((1, 128), dtype=np.float32)
+        W[0, j] = 1.0
+        T, S = L.quantize(W, 128, 128, residual=True)
+        assert list(S[0]) == [s1, s2]
+        assert np.array_equal(T[0, :128], H[:, j])
+        t2 = np.zeros(128, dtype=np.int8)
+        t2[j] = 1 if d > 0 else -1
+        assert np.array_equal(T[0, 128:], t2)
+
+
+def check_residual_overflow_group(orc):
+    """A group whose mean |w'| rounds to an infinite fp16 scale gets t1 = 0
+    (w'/inf = 0); a zero trit dequantises to 0, so the residual is w' itself,
+    whose rotation (W again) also overflows: s2 = inf, t2 = 0 -- and nothing
+    becomes NaN."""
+    L = _lay(orc)
+    W = np.full((1, 128), 1.0e6, dtype=np.float32)
+    T, S = L.quantize(W, 128, 128, residual=True)
+    assert list(S[0]) == [0x7C00, 0x7C00]
+    assert not T.any()
+
+
+def check_residual_reduces_error(orc):
+    """The residual pass brings the dequantised rotated weights closer to w'
+    (what it is for): over random rows, ||w' - (s1 t1 + H_b s2 t2)|| is well
+    below ||w' - s1 t1|| for every block and group size."""
+    L = _lay(orc)
+    rng = np.random.default_rng(85)
+    W = (rng.standard_normal((6, 512)) * 0.02).astype(np.float32)
+    for b in (64, 128, 256):
+        for g in (128, 256):
+            T, S = L.quantize(W, b, g, residual=True)
+            K = 512
+            wr = W.astype(np.float64) @ _block_h_n(K, b).T
+            s = S.view(np.float16).astype(np.float64)
+            d1 = T[:, :K] * np.repeat(s[:, :K // g], g, axis=1)
+            d2 = T[:, K:] * np.repeat(s[:, K // g:], g, axis=1)
+            approx = d1 + d2 @ _block_h_n(K, b).T
+            e1 = np.linalg.norm(wr - d1)
+            e2 = np.linalg.norm(wr - approx)
+            assert e2 < 0.75 * e1, (b, g, e1, e2)
+
+
+def check_layout_gemv_dense(orc):
+    """The layout GEMV equals the dense fp64 product with scipy-built blocks:
+    y = (t1 s1) . (H_b x) + (t2 s2) . (H_b H_b x); the second term is the
+    residual against the unrotated x (H_b H_b = I)."""
+    L = _lay(orc)
+    rng = np.random.default_rng(86)
+    K, N, M = 512, 7, 2
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    for b in (64, 128, 256):
+        for g in (128, 256):
+            for res in (False, True):
+                f = 2 if res else 1
+                T = rng.integers(-1, 2, size=(N, f * K)).astype(np.int8)
+                S = rng.uniform(0.001, 0.1, size=(N, f * (K // g))).astype(np.float16).view(np.uint16)
+                s = S.view(np.float16).astype(np.float64)
+                Bh = _block_h_n(K, b)
+                xr = x.astype(np.float64) @ Bh.T
+                ref = xr @ (T[:, :K] * np.repeat(s[:, :K // g], g, axis=1)).T
+                if res:
+                    ref = ref + x.astype(np.float64) @ (T[:, K:] * np.repeat(s[:, K // g:], g, axis=1)).T
+                got = L.gemv(T, S, x, b, g, res)
+                assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref))), (b, g, res)
+
+
+def check_group256_bit_accounting(orc):
+    """[mhpq] sec. 1.4: one fp16 scale per 256 weights costs 16/256 = 0.0625
+    bit per weight; with the residual pass the layouts store twice the codes
+    and scales (2 x 2.125 = 4.25 bit per weight in 2-bit codes at group 128)."""
+    assert 16 / 256 == 0.0625
+    L = _lay(orc)
+    W = np.zeros((1, 512), dtype=np.float32)
+    T, S = L.quantize(W, 128, 256, residual=False)
+    assert S.shape[1] * 16 / 512 == 0.0625
+    T, S = L.quantize(W, 128, 128, residual=True)
+    assert (T.shape[1] * 2 + S.shape[1] * 16) / 512 == 4.25
+
+
 ALL_CHECKS = [
     check_hadamard_definitions,
     check_hadamard_orthogonal,
@@ -506,4 +734,13 @@ ALL_CHECKS = [
     check_gemv_dense,
     check_gemv_delta_activation,
     check_rotation_invariance,
+    check_fwht_n_definitions,
+    check_fwht_n_stage_order,
+    check_group256_quantiser,
+    check_layout_default_is_the_method,
+    check_residual_delta_row,
+    check_residual_overflow_group,
+    check_residual_reduces_error,
+    check_layout_gemv_dense,
+    check_group256_bit_accounting,
 ]

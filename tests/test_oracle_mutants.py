@@ -42,15 +42,49 @@ MUTANTS = [
     ("gemv_reversed_x", "blk[i] = (double)x[m * K + g * 128 + i];", "blk[i] = (double)x[m * K + g * 128 + (127 - i)];"),
     ("gemv_no_x_rotation", "tqo_fwht128_f64(blk, rot);\n      for (int64_t r",
      "for (int i = 0; i < 128; ++i) rot[i] = blk[i];\n      for (int64_t r"),
+    # transform / group / residual variants
+    ("fwhtn_stage_order", "for (int h = 1; h < n; h *= 2) {", "for (int h = n / 2; h >= 1; h /= 2) {"),
+    ("fwhtn_norm_1_over_n", "float c = (float)(1.0 / sqrt((double)n));", "float c = (float)(1.0 / (double)n);"),
+    ("group_n_mean_factor", "float inv = 1.0f / (float)g;", "float inv = 1.0f / 128.0f;"),
+    ("group_n_sequential_sum", "for (int h = g / 2; h >= 1; h /= 2)\n    for (int i = 0; i < h; ++i) s[i] = s[i] + s[i + h];",
+     "for (int i = 1; i < g; ++i) s[0] = s[0] + s[i];"),
+    ("residual_sign", "wr[g + i] - s1f * (float)t1[g + i]", "wr[g + i] + s1f * (float)t1[g + i]"),
+    ("residual_zero_trit_times_scale", "(t1[g + i] == 0) ? wr[g + i] : wr[g + i] - s1f * (float)t1[g + i]",
+     "wr[g + i] - s1f * (float)t1[g + i]"),
+    ("residual_no_second_rotation", "for (int b = 0; b < u; b += block) tqo_fwht_f32(block, r + b, rr + b);",
+     "for (int i = 0; i < u; ++i) rr[i] = r[i];"),
+    ("residual_x_not_rotated_twice", "tqo_fwht_f64(block, xr + k0, xrr + k0);",
+     "for (int i = 0; i < block; ++i) xrr[k0 + i] = xr[k0 + i];"),
+    ("layout_group_stride", "const int8_t *t = T + q * Keff + pass * K + g * group;",
+     "const int8_t *t = T + q * Keff + pass * K + g * 128;"),
 ]
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_mutant_is_caught(tmp_path, name, old, new):
+# sites that occur more than once: (name, text, replacement, which occurrence)
+# (the layout variants of the transform and the quantiser repeat lines of
+# the 128-point functions: occurrence 0 is the 128-point function, 1 the
+# variant)
+_REPEATED = ("butterfly_sign", "no_normalisation", "signed_sum", "divide_by_mean", "round_half_away", "no_clamp")
+MUTANTS_NTH = [(*m, 0) for m in MUTANTS if m[0] in _REPEATED] + \
+    [("n_" + m[0], m[1], m[2], 1) for m in MUTANTS if m[0] in _REPEATED]
+MUTANTS = [m for m in MUTANTS if m[0] not in _REPEATED]
+ALL_MUTANTS = [(*m, None) for m in MUTANTS] + MUTANTS_NTH
+
+
+def _replace(src: str, old: str, new: str, nth):
+    if nth is None:
+        assert src.count(old) == 1, "mutation site not unique"
+        return src.replace(old, new)
+    parts = src.split(old)
+    assert len(parts) > nth + 1, "mutation site missing"
+    return old.join(parts[:nth + 1]) + new + old.join(parts[nth + 1:])
+
+
+@pytest.mark.parametrize("name,old,new,nth", ALL_MUTANTS, ids=[m[0] for m in ALL_MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new, nth):
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation site for {name} not unique"
     mut = tmp_path / "tq_oracle.c"
-    mut.write_text(src.replace(old, new))
+    mut.write_text(_replace(src, old, new, nth))
     shutil.copy(os.path.join(os.path.dirname(SRC), "tq_oracle.h"), tmp_path / "tq_oracle.h")
     lib = str(tmp_path / f"lib_{name}.so")
     subprocess.run(["gcc", *oracle.CFLAGS, "-I", str(tmp_path), "-o", lib, str(mut), "-lm"], check=True)
