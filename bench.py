@@ -514,7 +514,65 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
                       "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)})
         del W
     out["quantize_pack"] = sweep
+    out["layouts"] = layout_bench(tq, torch, dev, pk, gen)
     return out
+
+
+def layout_bench(tq, torch, dev, pk, gen) -> list:
+    """The layout variants (FWHT block 64/256, a scale per 256 weights, the
+    residual two-pass form) on the benchmark's shapes: the decode GEMV (M = 1,
+    27648x5120, cycling over 8 copies of the codes so each launch streams from
+    HBM), the prefill GEMM (M = 2048, 5120x5120) and quantise + pack
+    (5120x5120, bf16).  Work is counted over both passes of a residual layout."""
+    rows = []
+    W = (torch.randn(FFN, HIDDEN, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+    Wh = (torch.randn(HIDDEN, HIDDEN, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+    for (b, g, res) in ((64, 128, False), (256, 128, False), (128, 256, False), (128, 128, True)):
+        lay = tq.layout(b, g, res)
+        name = f"block {b}, group {g}" + (", residual" if res else "")
+        r = {"layout": name}
+        try:
+            c2, _, s = tq.quantize_pack_layout(W, lay, tq.TQ_PACK_2BIT)
+            copies = [(c2.clone(), s.clone()) for _ in range(8)]
+            del c2, s
+            N, K = FFN, HIDDEN
+            x = activations(torch, dev, K, 1, seed=K + 1)
+            y = torch.empty(1, N, device=dev)
+            it = [0]
+
+            def run():
+                c, sc = copies[it[0] % len(copies)]
+                it[0] += 1
+                tq.gemv_layout(c, sc, x, K, lay, out=y)
+
+            ms = time_events(run, 3 * len(copies), torch)
+            nbytes = copies[0][0].numel() + copies[0][1].numel() * 2
+            gb = nbytes / (ms * 1e-3) / 1e9
+            r["gemv_M1_27648x5120"] = {"us": round(ms * 1e3, 2), "GB/s": round(gb, 1),
+                                       "frac_of_peak": round(gb / pk["hbm_gbs"], 4), "bytes": nbytes}
+            del copies
+            N = K = HIDDEN
+            c2, c3, s = tq.quantize_pack_layout(Wh, lay, tq.TQ_PACK_BOTH)
+            Keff = K * (2 if res else 1)
+            ms = time_events(lambda: tq.quantize_pack_layout(Wh, lay, tq.TQ_PACK_BOTH), 5, torch)
+            qbytes = N * K * 2 + c2.numel() + c3.numel() + s.numel() * 2
+            r["quantize_pack_5120x5120"] = {"us": round(ms * 1e3, 1), "Gparams/s": round(N * K / (ms * 1e-3) / 1e9, 1),
+                                            "GB/s": round(qbytes / (ms * 1e-3) / 1e9, 1),
+                                            "frac_of_peak": round(qbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+            M = 2048
+            xg = activations(torch, dev, K, M, seed=11 + K)
+            ws = torch.empty(tq.gemm_workspace_bytes_layout(M, K, lay), dtype=torch.uint8, device=dev)
+            yg = torch.empty(M, N, device=dev)
+            ms = time_events(lambda: tq.gemm_layout(c2, s, xg, K, lay, workspace=ws, out=yg), 10, torch)
+            tf = 2 * M * N * Keff / (ms * 1e-3) / 1e12
+            r["gemm_M2048_5120x5120"] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                                         "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                                         "flops": "2 M N Keff (both passes)"}
+            del c2, c3, s, ws, yg
+        except tq.TQError as e:
+            r["unavailable"] = str(e)
+        rows.append(r)
+    return rows
 
 
 def sweep_bench(tq, torch, weights, pk, world: int) -> dict:

@@ -250,6 +250,78 @@ TQ_API tq_status tq_gemm_noalloc(const uint8_t *codes, int64_t ldc, int fmt, con
                                  int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
                                  tq_stream stream);
 
+/* ------------------------------------------------------------------------
+ * Layout variants: the ranked follow-ons of the method, each a parameter of
+ * the same path.
+ *   block   FWHT block size along K: 64, 128 or 256 (H_n from the popcount
+ *           rule or the Sylvester recursion for any power of two,
+ *           dpshk.com/news/5289456 sec. 2.1; block size against caches,
+ *           xxqk.cn/news/652513 sec. 2.2).  The transform runs the stages
+ *           h = 1 .. block/2 in fp32 and multiplies by RN_fp32(1/sqrt(block))
+ *           (exactly 1/8 and 1/16 for 64 and 256).
+ *   group   weights per fp16 scale: 128 or 256 (mhpq.cn/news/1159370 sec.
+ *           1.4: 16/256 = 0.0625 bit of scale per weight); the absmean sum is
+ *           the halving tree over the group (h = group/2 .. 1), times
+ *           1/group.
+ *   flags   TQ_LAYOUT_RESIDUAL: the residual two-pass ternarisation
+ *           (xxqk.cn/news/652513 sec. 3, residual calibrator): after the
+ *           first pass (s1, t1) the residual r = w' - s1 t1 (a zero trit
+ *           dequantises to 0) is rotated by the same block transform and
+ *           ternarised with scales s2 of its own.  Since the normalised
+ *           transform is its own inverse, the residual pass meets the
+ *           unrotated activations:
+ *             y = sum s1 sum t1 x' + sum s2 sum t2 x.
+ * {128, 128, 0} is the method itself; a NULL layout means that.  K must be a
+ * multiple of max(block, group).  A layout's codes hold Keff = K trits per
+ * row (2K with TQ_LAYOUT_RESIDUAL: the first pass's, then the residual
+ * pass's), packed over all Keff as for the plain layout; its scales hold
+ * K/group per row (twice with the residual pass: the s1, then the s2). */
+typedef struct {
+  int32_t block;
+  int32_t group;
+  uint32_t flags;
+} tq_layout;
+enum { TQ_LAYOUT_RESIDUAL = 1 };
+
+/* Minimum leading dimensions of a layout's codes (bytes, fmt TQ_PACK_2BIT or
+ * TQ_PACK_BASE3) and scales (elements); -1 for bad arguments. */
+TQ_API int64_t tq_layout_codes_ld(int64_t K, int fmt, const tq_layout *lay);
+TQ_API int64_t tq_layout_scales_ld(int64_t K, const tq_layout *lay);
+
+/* tq_fwht128 at block size 64, 128 or 256 (K a multiple of block); same
+ * arguments, dtypes, exactness and in-place rule. */
+TQ_API tq_status tq_fwht(const void *x, int xt, int64_t ldx, void *y, int yt, int64_t ldy, int64_t rows,
+                         int64_t K, int block, tq_stream stream);
+
+/* tq_quantize_pack under a layout.  ld2 >= tq_layout_codes_ld(K, 2-bit),
+ * ld3 >= tq_layout_codes_ld(K, base-3), lds >= tq_layout_scales_ld(K).  Codes
+ * and scales are bit-exact with the definition.  A layout other than
+ * {128, 128, 0} runs a general kernel that keeps a row's trits in shared
+ * memory: TQ_ERR_UNSUPPORTED when Keff exceeds about 190 thousand. */
+TQ_API tq_status tq_quantize_pack_layout(const void *W, int wt, int64_t N, int64_t K, int64_t ldw, int fmt,
+                                         uint8_t *codes2, int64_t ld2, uint8_t *codes3, int64_t ld3,
+                                         uint16_t *scales, int64_t lds, const tq_layout *lay, tq_stream stream);
+
+/* tq_gemv_ex under a layout: K is the activations' K; codes hold Keff.  A
+ * layout other than {128, 128, 0} runs on the tensor-memory kernel only
+ * (TQ_ERR_UNSUPPORTED where that kernel does not take the shape).  Flags as
+ * tq_gemv_ex. */
+TQ_API tq_status tq_gemv_layout(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
+                                int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
+                                const tq_layout *lay, unsigned int flags, tq_stream stream);
+
+/* Workspace of tq_gemm_layout: as tq_gemm_workspace_bytes with the rotated
+ * activations of both passes (M x Keff fp16). */
+TQ_API size_t tq_gemm_workspace_bytes_layout(int64_t M, int64_t K, const tq_layout *lay);
+
+/* tq_gemm_ex under a layout: the pre-pass writes x' (block transform) and,
+ * with the residual pass, x itself beside it, both fp16 with the overflow
+ * check; the GEMM then runs over Keff.  Flags as tq_gemm_ex. */
+TQ_API tq_status tq_gemm_layout(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
+                                int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
+                                void *workspace, size_t ws_bytes, const tq_layout *lay, unsigned int flags,
+                                tq_stream stream);
+
 /* Failure detection.  Every wait inside a kernel (pipeline barriers between
  * the warps that copy weights and the warps that compute) is bounded by a
  * wall-clock limit of about 2 s.  A kernel whose wait runs out stops early,

@@ -11,6 +11,9 @@ Functions (names follow the C ABI):
   gemv(codes, scales, x, K, fmt)        y fp32 [M][N], M = 1..16
   gemm(codes, scales, x, K, fmt, ws)    y fp32 [M][N] on tcgen05 tensor cores
   gemm_workspace_bytes(M, K), gemm_check_range(ws)
+  Layout variants (FWHT block 64/128/256, scale group 128/256, residual
+  pass): fwht(x, block), quantize_pack_layout, gemv_layout, gemm_layout,
+  layout_codes_ld, layout_scales_ld, gemm_workspace_bytes_layout
 """
 from __future__ import annotations
 
@@ -28,10 +31,23 @@ TQ_PACK_2BIT, TQ_PACK_BASE3, TQ_PACK_BOTH = 1, 2, 3
 
 EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_quantize_pack", "tq_gemv",
             "tq_gemv_ex", "tq_gemv_path", "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_ex", "tq_gemm_check_range",
-            "tq_device_fault", "tq_gemm_noalloc")
+            "tq_device_fault", "tq_gemm_noalloc", "tq_layout_codes_ld", "tq_layout_scales_ld", "tq_fwht",
+            "tq_quantize_pack_layout", "tq_gemv_layout", "tq_gemm_workspace_bytes_layout", "tq_gemm_layout")
 TQ_GEMV_TENSOR_MEMORY, TQ_GEMV_MMA_SYNC = 1, 2
 TQ_GEMV_WEIGHTS_READY = 1
 TQ_GEMM_REUSE_ROTATED = 1
+TQ_GEMV_TEST_STALL = 0x100
+TQ_GEMM_TEST_STALL = 0x100
+TQ_LAYOUT_RESIDUAL = 1
+
+
+class Layout(ctypes.Structure):
+    """tq_layout: FWHT block size, weights per scale, flags (TQ_LAYOUT_RESIDUAL)."""
+    _fields_ = [("block", ctypes.c_int32), ("group", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+def layout(block: int = 128, group: int = 128, residual: bool = False) -> Layout:
+    return Layout(block, group, TQ_LAYOUT_RESIDUAL if residual else 0)
 
 _lib = None
 _i64 = ctypes.c_int64
@@ -83,6 +99,24 @@ def lib() -> ctypes.CDLL:
         L.tq_device_fault.argtypes = []
         L.tq_gemm_noalloc.restype = _int
         L.tq_gemm_noalloc.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp]
+        lp = ctypes.POINTER(Layout)
+        L.tq_layout_codes_ld.restype = _i64
+        L.tq_layout_codes_ld.argtypes = [_i64, _int, lp]
+        L.tq_layout_scales_ld.restype = _i64
+        L.tq_layout_scales_ld.argtypes = [_i64, lp]
+        L.tq_fwht.restype = _int
+        L.tq_fwht.argtypes = [_vp, _int, _i64, _vp, _int, _i64, _i64, _i64, _int, _vp]
+        L.tq_quantize_pack_layout.restype = _int
+        L.tq_quantize_pack_layout.argtypes = [_vp, _int, _i64, _i64, _i64, _int, _vp, _i64, _vp, _i64, _vp, _i64, lp,
+                                              _vp]
+        L.tq_gemv_layout.restype = _int
+        L.tq_gemv_layout.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, lp,
+                                     ctypes.c_uint, _vp]
+        L.tq_gemm_workspace_bytes_layout.restype = ctypes.c_size_t
+        L.tq_gemm_workspace_bytes_layout.argtypes = [_i64, _i64, lp]
+        L.tq_gemm_layout.restype = _int
+        L.tq_gemm_layout.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
+                                     ctypes.c_size_t, lp, ctypes.c_uint, _vp]
         _lib = L
     return _lib
 
@@ -231,3 +265,92 @@ def device_fault() -> None:
 def gemm_check_range(workspace: torch.Tensor, stream=None) -> None:
     """Raises TQError(TQ_ERR_RANGE) if the last tq_gemm saw an fp16 overflow."""
     _check(lib().tq_gemm_check_range(workspace.data_ptr(), _stream(stream)), "tq_gemm_check_range")
+
+
+# ------------------------------------------------------------ layout variants
+
+def _lp(lay: Layout | None):
+    return None if lay is None else ctypes.byref(lay)
+
+
+def layout_codes_ld(K: int, fmt: int, lay: Layout | None) -> int:
+    return int(lib().tq_layout_codes_ld(K, fmt, _lp(lay)))
+
+
+def layout_scales_ld(K: int, lay: Layout | None) -> int:
+    return int(lib().tq_layout_scales_ld(K, _lp(lay)))
+
+
+def fwht(x: torch.Tensor, block: int = 128, out_dtype: torch.dtype = torch.float32, out: torch.Tensor | None = None,
+         stream=None) -> torch.Tensor:
+    """Block FWHT (block 64, 128 or 256) of every row of x along its last dimension."""
+    _cuda2d(x, "x")
+    rows, K = x.shape
+    if out is None:
+        out = torch.empty((rows, K), dtype=out_dtype, device=x.device)
+    _cuda2d(out, "out")
+    st = lib().tq_fwht(x.data_ptr(), _dt(x), x.stride(0), out.data_ptr(), _dt(out), out.stride(0), rows, K, block,
+                       _stream(stream))
+    _check(st, "tq_fwht")
+    return out
+
+
+def quantize_pack_layout(W: torch.Tensor, lay: Layout, fmt: int = TQ_PACK_BOTH, stream=None):
+    """quantize_pack under a layout: (codes2 [N][ld2] or None, codes3 [N][ld3] or
+    None, scales int16 [N][Geff]); codes hold Keff = K (2K with the residual pass)."""
+    _cuda2d(W, "W")
+    N, K = W.shape
+    dev = W.device
+    ld2 = layout_codes_ld(K, TQ_PACK_2BIT, lay)
+    ld3 = layout_codes_ld(K, TQ_PACK_BASE3, lay)
+    lds = layout_scales_ld(K, lay)
+    if min(ld2, ld3, lds) < 0:
+        raise TQError(TQ_ERR_SHAPE, "tq_layout_codes_ld")
+    codes2 = torch.empty((N, ld2), dtype=torch.uint8, device=dev) if fmt & TQ_PACK_2BIT else None
+    codes3 = torch.empty((N, ld3), dtype=torch.uint8, device=dev) if fmt & TQ_PACK_BASE3 else None
+    scales = torch.empty((N, lds), dtype=torch.int16, device=dev)
+    st = lib().tq_quantize_pack_layout(W.data_ptr(), _dt(W), N, K, W.stride(0), fmt,
+                                       codes2.data_ptr() if codes2 is not None else None, ld2,
+                                       codes3.data_ptr() if codes3 is not None else None, ld3,
+                                       scales.data_ptr(), scales.stride(0), _lp(lay), _stream(stream))
+    _check(st, "tq_quantize_pack_layout")
+    return codes2, codes3, scales
+
+
+def gemv_layout(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, lay: Layout,
+                fmt: int = TQ_PACK_2BIT, out: torch.Tensor | None = None, stream=None, flags: int = 0) -> torch.Tensor:
+    _cuda2d(codes, "codes")
+    _cuda2d(scales, "scales")
+    _cuda2d(x, "x")
+    N = codes.shape[0]
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    st = lib().tq_gemv_layout(codes.data_ptr(), codes.stride(0), fmt, scales.data_ptr(), scales.stride(0), N, K,
+                              x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), _lp(lay), flags,
+                              _stream(stream))
+    _check(st, "tq_gemv_layout")
+    return out
+
+
+def gemm_workspace_bytes_layout(M: int, K: int, lay: Layout | None) -> int:
+    return int(lib().tq_gemm_workspace_bytes_layout(M, K, _lp(lay)))
+
+
+def gemm_layout(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, lay: Layout,
+                fmt: int = TQ_PACK_2BIT, workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                stream=None, flags: int = 0) -> torch.Tensor:
+    _cuda2d(codes, "codes")
+    _cuda2d(scales, "scales")
+    _cuda2d(x, "x")
+    N = codes.shape[0]
+    M = x.shape[0]
+    if workspace is None:
+        workspace = torch.empty(gemm_workspace_bytes_layout(M, K, lay), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    st = lib().tq_gemm_layout(codes.data_ptr(), codes.stride(0), fmt, scales.data_ptr(), scales.stride(0), N, K,
+                              x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _lp(lay), flags, _stream(stream))
+    _check(st, "tq_gemm_layout")
+    return out

@@ -1,5 +1,5 @@
-// k_fwht.cu -- block FWHT-128 of activation rows (tq_fwht128, and the
-// rotation pre-pass of tq_gemm).
+// k_fwht.cu -- block FWHT of activation rows (tq_fwht128 / tq_fwht, and the
+// rotation pre-pass of tq_gemm), block sizes 64, 128 and 256.
 //
 // A half-warp rotates one 128-block (row r, group g): lane p holds elements
 // 8p .. 8p+7, loaded with one 16-byte load (bf16) or two (fp32), so a warp
@@ -86,7 +86,59 @@ __device__ __forceinline__ void store8(void* y, int64_t off, int p, const float 
   }
 }
 
-template <int XT, int YT, bool PERM16>
+// The other block sizes on the same lane layout (lane p of a half-warp holds
+// elements 8p .. 8p + 7 of a 128-block; the two half-warps hold consecutive
+// 128-blocks of one row): 64 runs the stages h = 1 .. 32 (the last
+// cross-lane stage, lanes l ^ 8, would join the two 64-blocks of the half)
+// and multiplies by 1/8; 256 runs h = 1 .. 64 in each half and then h = 128
+// across the halves (lanes l ^ 16), and multiplies by 1/16.  The stages run
+// in the order h = 1, 2, 4, ..., the lower element of a pair keeping a + b,
+// so the result equals the staged fp32 definition bit for bit, as for 128.
+template <int BLK>
+__device__ __forceinline__ void fwht_blk_x8(float v[8], int lane) {
+  static_assert(BLK == 64 || BLK == 256, "block size");
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const float a = v[j], b = v[j + 1];
+    v[j] = a + b;
+    v[j + 1] = a - b;
+  }
+  uint64_t q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = f2_pack(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int hp = 1; hp < 4; hp <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if ((i & hp) == 0) {
+        const uint64_t a = q[i], b = q[i + hp];
+        q[i] = f2_add(a, b);
+        q[i + hp] = f2_sub(a, b);
+      }
+    }
+  }
+  constexpr int kLast = BLK == 64 ? 8 : 32;  // cross-lane stages m = 1 .. kLast / 2
+#pragma unroll
+  for (int m = 1; m < kLast; m <<= 1) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
+    const uint64_t sg = f2_pack(sgn, sgn);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float lo, hi;
+      f2_unpack(q[i], lo, hi);
+      const float olo = __shfl_xor_sync(kFull, lo, m), ohi = __shfl_xor_sync(kFull, hi, m);
+      q[i] = f2_fma(sg, q[i], f2_pack(olo, ohi));
+    }
+  }
+  const float c = BLK == 64 ? 0.125f : 0.0625f;
+  const uint64_t sc = f2_pack(c, c);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(q[i], sc), v[2 * i], v[2 * i + 1]);
+}
+
+// BLK: 64, 128 or 256, or 0 for no rotation (the residual half of the
+// pre-pass of a residual layout copies x, converted and permuted the same way).
+template <int XT, int YT, bool PERM16, int BLK>
 __global__ void __launch_bounds__(kThreads, 4) k_fwht128(const void* __restrict__ x, int64_t ldx, void* y,
                                                          int64_t ldy, int64_t rows, int64_t G, uint32_t* flag) {
   constexpr int esize = XT == TQ_F32 ? 4 : 2;
@@ -136,14 +188,18 @@ __global__ void __launch_bounds__(kThreads, 4) k_fwht128(const void* __restrict_
       if (2 * (b0 + (int64_t)u * nwarps) >= nblk) break;  // warp-uniform
       float v[8];
       unpack8<XT>(raw[u], v);
-      fwht128_x8(v, lane);
+      if constexpr (BLK == 128) {
+        fwht128_x8(v, lane);
+      } else if constexpr (BLK != 0) {
+        fwht_blk_x8<BLK>(v, lane);
+      }
       store8<YT, PERM16>(y, yof[u], p, v, flag, ok[u]);
     }
   }
   pdl_launch_dependents();
 }
 
-template <int XT, int YT, bool PERM16>
+template <int XT, int YT, bool PERM16, int BLK = 128>
 cudaError_t launch_t(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t rows, int64_t G, uint32_t* flag,
                      cudaStream_t s) {
   const int64_t nblk = rows * G;
@@ -161,7 +217,7 @@ cudaError_t launch_t(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t r
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_fwht128<XT, YT, PERM16>, x, ldx, y, ldy, rows, G, flag);
+  return cudaLaunchKernelEx(&cfg, k_fwht128<XT, YT, PERM16, BLK>, x, ldx, y, ldy, rows, G, flag);
 }
 
 }  // namespace
@@ -180,6 +236,36 @@ cudaError_t launch_fwht128(const void* x, int xt, int64_t ldx, void* y, int yt, 
   if (yt == TQ_F32) return launch_t<TQ_BF16, TQ_F32, false>(x, ldx, y, ldy, rows, G, flag, s);
   if (yt == TQ_BF16) return launch_t<TQ_BF16, TQ_BF16, false>(x, ldx, y, ldy, rows, G, flag, s);
   return launch_t<TQ_BF16, TQ_F16, false>(x, ldx, y, ldy, rows, G, flag, s);
+}
+
+namespace {
+template <int BLK>
+cudaError_t launch_blk(const void* x, int xt, int64_t ldx, void* y, int yt, int64_t ldy, int64_t rows, int64_t G,
+                       bool perm16, uint32_t* flag, cudaStream_t s) {
+  if (perm16) return launch_t<TQ_BF16, TQ_F16, true, BLK>(x, ldx, y, ldy, rows, G, flag, s);
+  flag = nullptr;
+  if (xt == TQ_F32) {
+    if (yt == TQ_F32) return launch_t<TQ_F32, TQ_F32, false, BLK>(x, ldx, y, ldy, rows, G, flag, s);
+    if (yt == TQ_BF16) return launch_t<TQ_F32, TQ_BF16, false, BLK>(x, ldx, y, ldy, rows, G, flag, s);
+    return launch_t<TQ_F32, TQ_F16, false, BLK>(x, ldx, y, ldy, rows, G, flag, s);
+  }
+  if (yt == TQ_F32) return launch_t<TQ_BF16, TQ_F32, false, BLK>(x, ldx, y, ldy, rows, G, flag, s);
+  if (yt == TQ_BF16) return launch_t<TQ_BF16, TQ_BF16, false, BLK>(x, ldx, y, ldy, rows, G, flag, s);
+  return launch_t<TQ_BF16, TQ_F16, false, BLK>(x, ldx, y, ldy, rows, G, flag, s);
+}
+}  // namespace
+
+cudaError_t launch_fwht(const void* x, int xt, int64_t ldx, void* y, int yt, int64_t ldy, int64_t rows, int64_t K,
+                        int block, bool perm16, uint32_t* flag, cudaStream_t s) {
+  const int64_t G = K / 128;
+  if (rows == 0 || G == 0) return cudaSuccess;
+  switch (block) {
+    case 128: return launch_fwht128(x, xt, ldx, y, yt, ldy, rows, K, perm16, flag, s);
+    case 64: return launch_blk<64>(x, xt, ldx, y, yt, ldy, rows, G, perm16, flag, s);
+    case 256: return launch_blk<256>(x, xt, ldx, y, yt, ldy, rows, G, perm16, flag, s);
+    case 0: return launch_t<TQ_BF16, TQ_F16, true, 0>(x, ldx, y, ldy, rows, G, perm16 ? flag : nullptr, s);
+    default: return cudaErrorNotSupported;
+  }
 }
 
 }  // namespace tq

@@ -194,6 +194,7 @@ struct Params {
   // first x' stage, so its waits run out; wait_ns bounds every wait.
   int stall_cta;
   unsigned long long wait_ns;
+  int lgs;  // one scale per 128 << lgs weights (layout variants: groups of 256)
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SmemCtl* ctl, uint32_t* flag) {
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return (in_tile && st < nk) ? ldg_nc_u4(crow + (s0 + st) * (BK / 4)) : make_uint4(0, 0, 0, 0);
     };
     auto ld_scale = [&](int st) {
-      return (row_ok && st < nk) ? __ldg(srow + ((s0 + st) * BK) / 128) : (uint16_t)0;
+      return (row_ok && st < nk) ? __ldg(srow + (((s0 + st) * BK) >> (7 + p.lgs))) : (uint16_t)0;
     };
     uint4 cur = ld_codes(0), nx1 = ld_codes(1);
     uint16_t scur = ld_scale(0), snx1 = ld_scale(1);
@@ -530,7 +531,7 @@ static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes) {
 
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
                         const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, void* split_ws,
-                        size_t split_bytes, cudaStream_t s, bool test_stall) {
+                        size_t split_bytes, cudaStream_t s, bool test_stall, int group) {
   if (N == 0 || M == 0) return cudaSuccess;
   if ((int64_t)device_max_smem_optin() < (int64_t)kGemmSmem) return cudaErrorNotSupported;
   EncodeTiledFn enc = encode_fn();
@@ -557,6 +558,7 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   p.flag = flag;
   p.stall_cta = test_stall ? 0 : -1;
   p.wait_ns = test_stall ? kTestWaitLimitNs : kWaitLimitNs;
+  p.lgs = group == 256 ? 1 : 0;
   p.n_tiles_m = (int)((M + BM - 1) / BM);
   const GemmPlan g = gemm_plan(N, M, K, split_ws != nullptr ? split_bytes : 0);
   p.bn = g.bn;

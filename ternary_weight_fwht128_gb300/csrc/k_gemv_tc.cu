@@ -224,6 +224,13 @@ struct Params {
   // first stage of codes, so its waits run out; wait_ns bounds every wait.
   int stall_cta;
   unsigned long long wait_ns;
+  // Layout variants: FWHT block size (64, 128 or 256), log2 of the scale
+  // group over 128 (0 or 1), and the number of 128-groups of K that meet
+  // rotated activations (K / 128 without a residual pass; with one, K counts
+  // the codes of both passes and groups from g_rot on meet x unrotated).
+  int blk;
+  int lgs;
+  int64_t g_rot;
 };
 // ---------------------------------------------------------------- PTX helpers
 
@@ -352,7 +359,8 @@ __device__ __forceinline__ uint16_t ldg_nc_u16(const uint16_t* p) {
 // h = 16, 32, 64 pair lanes l ^ 4, l ^ 8, l ^ 16.  The stages run in the
 // order h = 1, 2, 4, ..., 64 with the lower index keeping a + b, then * c,
 // so the result equals the staged fp32 definition bit for bit.
-__device__ __forceinline__ void fwht128_strided(float v[4], int lane) {
+template <bool kH64 = true>
+__device__ __forceinline__ void fwht128_strided_stages(float v[4], int lane) {
   auto shfl_stage = [&](int m) {
     const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
@@ -372,9 +380,36 @@ __device__ __forceinline__ void fwht128_strided(float v[4], int lane) {
   }
   shfl_stage(4);
   shfl_stage(8);
-  shfl_stage(16);
+  if constexpr (kH64) shfl_stage(16);
+}
+
+__device__ __forceinline__ void fwht128_strided(float v[4], int lane) {
+  fwht128_strided_stages(v, lane);
 #pragma unroll
   for (int b = 0; b < 4; ++b) v[b] = __fmul_rn(v[b], kInvSqrt128);
+}
+
+// The layout variants on the same lane layout (fp32, staged order, bit for
+// bit the definition): 64-blocks stop before the stage h = 64 (lanes l ^ 16)
+// and multiply by 1/8; a 256-block also rotates the other 128-group of its
+// block (partner, same lanes), then runs the stage h = 128 between the two
+// (the lower group keeps a + b) and multiplies by 1/16.
+__device__ __forceinline__ void rotate_group(float v[4], int lane, int blk, const uint16_t* partner, bool upper) {
+  if (blk == 128) {
+    fwht128_strided(v, lane);
+  } else if (blk == 64) {
+    fwht128_strided_stages<false>(v, lane);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) v[b] = __fmul_rn(v[b], 0.125f);
+  } else {
+    float o[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) o[b] = __uint_as_float((uint32_t)ldg_nc_u16(partner + 4 * b) << 16);
+    fwht128_strided_stages(v, lane);
+    fwht128_strided_stages(o, lane);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) v[b] = __fmul_rn(upper ? __fsub_rn(o[b], v[b]) : __fadd_rn(v[b], o[b]), 0.0625f);
+  }
 }
 
 // The five base-3 digits of the four code bytes of w (byte b = sum_i d_i 3^i,
@@ -556,11 +591,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   for (int it = pwarp; it < ng * M && warp != kTmaWarp; it += kThreads / 32 - 1) {
     const int gl = it / M, m = it - gl * M;
     const int i8 = lane >> 2, jc = lane & 3;
-    const uint16_t* xg = p.x + m * p.ldx + (g0 + gl) * 128 + 16 * i8 + jc;
+    // a residual layout's second half of the codes meets x itself
+    const int64_t gg = g0 + gl;
+    const bool rot = gg < p.g_rot;
+    const int64_t xc = rot ? gg : gg - p.g_rot;
+    const uint16_t* xrow = p.x + m * p.ldx + 16 * i8 + jc;
+    const uint16_t* xg = xrow + xc * 128;
     float v[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ldg_nc_u16(xg + 4 * b) << 16);
-    fwht128_strided(v, lane);
+    if (rot) rotate_group(v, lane, p.blk, xrow + (xc ^ 1) * 128, (xc & 1) != 0);
     float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
@@ -783,10 +823,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       for (int h = 0; h < kGS; ++h) sc[h] = 0u;
       const int64_t n = (t0 + tl) * 128 + r;
       if (tl >= ntiles || n >= p.N) return;
-      const uint16_t* q = p.scales + n * p.lds + g0 + kGS * c;
+      const uint16_t* q = p.scales + n * p.lds;
+      const int64_t gc = g0 + kGS * c;  // a scale per 2^lgs groups of 128
 #pragma unroll
       for (int h = 0; h < kGS; ++h)
-        if (kGS * c + h < ng) sc[h] = __ldg(q + h);
+        if (kGS * c + h < ng) sc[h] = __ldg(q + ((gc + h) >> p.lgs));
     };
     // The scales are loaded kAhead stages before they are used (a DRAM miss
     // takes longer than a stage).  The stage loop is unrolled by kAhead so
@@ -1106,7 +1147,7 @@ int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt) {
 
 cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds,
                            int64_t N, int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
-                           bool prefetch, cudaStream_t s, bool test_stall) {
+                           bool prefetch, cudaStream_t s, bool test_stall, const GemvLayout* lay) {
   if (N == 0) return cudaSuccess;
   const bool b3 = fmt == TQ_PACK_BASE3;
   const int64_t G = K / 128, T = (N + 127) / 128;
@@ -1119,7 +1160,7 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
     for (int i = 0; i < l; ++i) {
       const int64_t mi = (M - m0) / (l - i);
       cudaError_t e = launch_gemv_tc(codes, ldc, fmt, scales, lds, N, K, static_cast<const uint16_t*>(x) + m0 * ldx,
-                                     ldx, mi, y + m0 * ldy, ldy, prefetch, s, test_stall && i == 0);
+                                     ldx, mi, y + m0 * ldy, ldy, prefetch, s, test_stall && i == 0, lay);
       if (e != cudaSuccess) return e;
       m0 += mi;
     }
@@ -1157,6 +1198,9 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
   p.prefetch = prefetch ? 1 : 0;
   p.stall_cta = test_stall ? 0 : -1;
   p.wait_ns = test_stall ? kTestWaitLimitNs : kWaitLimitNs;
+  p.blk = lay != nullptr ? lay->block : 128;
+  p.lgs = (lay != nullptr && lay->group == 256) ? 1 : 0;
+  p.g_rot = (lay != nullptr && lay->residual) ? G / 2 : G;
   const int64_t smem_max = device_max_smem_optin();
   // More than half an SM's shared memory, so no two CTAs share an SM whatever
   // the register count: each allocates all of tensor memory, and a second

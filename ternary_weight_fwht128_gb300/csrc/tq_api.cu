@@ -200,6 +200,159 @@ tq_status tq_gemm_check_range(const void* workspace, tq_stream stream) {
   return (flag & 1u) ? TQ_ERR_RANGE : TQ_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// A checked layout: returns TQ_OK and fills the fields, or the status a call
+// with it returns.
+struct Lay {
+  int block = 128, group = 128, residual = 0;
+  bool plain() const { return block == 128 && group == 128 && residual == 0; }
+  int64_t keff(int64_t K) const { return residual ? 2 * K : K; }
+  int64_t geff(int64_t K) const { return (residual ? 2 : 1) * (K / group); }
+};
+
+tq_status read_layout(const tq_layout* lay, Lay* out) {
+  Lay L;
+  if (lay != nullptr) {
+    if (lay->block != 64 && lay->block != 128 && lay->block != 256) return TQ_ERR_INVALID_ARG;
+    if (lay->group != 128 && lay->group != 256) return TQ_ERR_INVALID_ARG;
+    if (lay->flags & ~(uint32_t)TQ_LAYOUT_RESIDUAL) return TQ_ERR_INVALID_ARG;
+    L.block = lay->block;
+    L.group = lay->group;
+    L.residual = (lay->flags & TQ_LAYOUT_RESIDUAL) ? 1 : 0;
+  }
+  *out = L;
+  return TQ_OK;
+}
+
+bool k_fits(int64_t K, const Lay& L) { return k_ok(K) && K % L.block == 0 && K % L.group == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int64_t tq_layout_codes_ld(int64_t K, int fmt, const tq_layout* lay) {
+  Lay L;
+  if (read_layout(lay, &L) != TQ_OK || !k_fits(K, L)) return -1;
+  return tq_packed_ld(L.keff(K), fmt);
+}
+
+int64_t tq_layout_scales_ld(int64_t K, const tq_layout* lay) {
+  Lay L;
+  if (read_layout(lay, &L) != TQ_OK || !k_fits(K, L)) return -1;
+  return L.geff(K);
+}
+
+tq_status tq_fwht(const void* x, int xt, int64_t ldx, void* y, int yt, int64_t ldy, int64_t rows, int64_t K,
+                  int block, tq_stream stream) {
+  if (block != 64 && block != 128 && block != 256) return TQ_ERR_INVALID_ARG;
+  if (block == 128) return tq_fwht128(x, xt, ldx, y, yt, ldy, rows, K, stream);
+  if (xt != TQ_F32 && xt != TQ_BF16) return TQ_ERR_INVALID_ARG;
+  if (yt != TQ_F32 && yt != TQ_BF16 && yt != TQ_F16) return TQ_ERR_INVALID_ARG;
+  if (rows < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_ok(K) || K % block) return TQ_ERR_SHAPE;
+  if (rows == 0) return TQ_OK;
+  if (x == nullptr || y == nullptr) return TQ_ERR_INVALID_ARG;
+  if (ldx < K || ldy < K) return TQ_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(y) || (ldx * dtype_size(xt)) % 16 || (ldy * dtype_size(yt)) % 16)
+    return TQ_ERR_ALIGN;
+  if (x == y && (xt != yt || ldx != ldy)) return TQ_ERR_INVALID_ARG;
+  return from_cuda(launch_fwht(x, xt, ldx, y, yt, ldy, rows, K, block, false, nullptr, (cudaStream_t)stream));
+}
+
+tq_status tq_quantize_pack_layout(const void* W, int wt, int64_t N, int64_t K, int64_t ldw, int fmt,
+                                  uint8_t* codes2, int64_t ld2, uint8_t* codes3, int64_t ld3, uint16_t* scales,
+                                  int64_t lds, const tq_layout* lay, tq_stream stream) {
+  Lay L;
+  const tq_status st = read_layout(lay, &L);
+  if (st != TQ_OK) return st;
+  if (L.plain()) return tq_quantize_pack(W, wt, N, K, ldw, fmt, codes2, ld2, codes3, ld3, scales, lds, stream);
+  if (wt != TQ_F32 && wt != TQ_BF16) return TQ_ERR_INVALID_ARG;
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3 && fmt != TQ_PACK_BOTH) return TQ_ERR_INVALID_ARG;
+  if (N < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_fits(K, L)) return TQ_ERR_SHAPE;
+  if (N == 0) return TQ_OK;
+  const bool do2 = (fmt & TQ_PACK_2BIT) != 0, do3 = (fmt & TQ_PACK_BASE3) != 0;
+  if (W == nullptr || scales == nullptr || (do2 && codes2 == nullptr) || (do3 && codes3 == nullptr))
+    return TQ_ERR_INVALID_ARG;
+  const int64_t Ke = L.keff(K);
+  if (ldw < K || lds < L.geff(K) || (do2 && ld2 < Ke / 4) || (do3 && ld3 < ld3_min(Ke))) return TQ_ERR_SHAPE;
+  if (!aligned16(W) || (ldw * dtype_size(wt)) % 16 || !aligned2(scales)) return TQ_ERR_ALIGN;
+  return from_cuda(launch_quantize_layout(W, wt, N, K, ldw, L.block, L.group, L.residual, do2 ? codes2 : nullptr,
+                                          ld2, do3 ? codes3 : nullptr, ld3, scales, lds, (cudaStream_t)stream));
+}
+
+tq_status tq_gemv_layout(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
+                         int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
+                         const tq_layout* lay, unsigned int flags, tq_stream stream) {
+  Lay L;
+  const tq_status st = read_layout(lay, &L);
+  if (st != TQ_OK) return st;
+  if (L.plain()) return tq_gemv_ex(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy, flags, stream);
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return TQ_ERR_INVALID_ARG;
+  if (flags & ~(unsigned int)(TQ_GEMV_WEIGHTS_READY | TQ_GEMV_TEST_STALL)) return TQ_ERR_INVALID_ARG;
+  if (N < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_fits(K, L) || M < 1 || M > 16) return TQ_ERR_SHAPE;
+  if (N == 0) return TQ_OK;
+  if (codes == nullptr || scales == nullptr || x == nullptr || y == nullptr) return TQ_ERR_INVALID_ARG;
+  const int64_t Ke = L.keff(K);
+  if (ldc < tq_packed_ld(Ke, fmt) || lds < L.geff(K) || ldx < K || ldy < N) return TQ_ERR_SHAPE;
+  if (!aligned16(codes) || ldc % 16 || !aligned2(scales) || !aligned16(x) || (ldx * 2) % 16 ||
+      (reinterpret_cast<uintptr_t>(y) & 3u))
+    return TQ_ERR_ALIGN;
+  if (tq::gemv_tc_launches(N, Ke, M, fmt) == 0) return TQ_ERR_UNSUPPORTED;
+  const GemvLayout gl{L.block, L.group, L.residual};
+  return from_cuda(launch_gemv_tc(codes, ldc, fmt, scales, lds, N, Ke, x, ldx, M, y, ldy,
+                                  (flags & TQ_GEMV_WEIGHTS_READY) != 0, (cudaStream_t)stream,
+                                  (flags & TQ_GEMV_TEST_STALL) != 0, &gl));
+}
+
+size_t tq_gemm_workspace_bytes_layout(int64_t M, int64_t K, const tq_layout* lay) {
+  Lay L;
+  if (read_layout(lay, &L) != TQ_OK || M < 0 || K < 0) return 0;
+  return tq_gemm_workspace_bytes(M, L.keff(K));
+}
+
+tq_status tq_gemm_layout(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
+                         int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, void* workspace,
+                         size_t ws_bytes, const tq_layout* lay, unsigned int flags, tq_stream stream) {
+  Lay L;
+  const tq_status st = read_layout(lay, &L);
+  if (st != TQ_OK) return st;
+  if (L.plain())
+    return tq_gemm_ex(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy, workspace, ws_bytes, flags, stream);
+  if (flags & ~(unsigned int)(TQ_GEMM_REUSE_ROTATED | TQ_GEMM_TEST_STALL)) return TQ_ERR_INVALID_ARG;
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return TQ_ERR_INVALID_ARG;
+  if (N < 0 || M < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_fits(K, L)) return TQ_ERR_SHAPE;
+  if (N == 0 || M == 0) return TQ_OK;
+  if (fmt != TQ_PACK_2BIT) return TQ_ERR_UNSUPPORTED;
+  if (codes == nullptr || scales == nullptr || x == nullptr || y == nullptr || workspace == nullptr)
+    return TQ_ERR_INVALID_ARG;
+  const int64_t Ke = L.keff(K);
+  if (ldc < Ke / 4 || lds < L.geff(K) || ldx < K || ldy < N) return TQ_ERR_SHAPE;
+  if (ws_bytes < tq_gemm_workspace_bytes(M, Ke)) return TQ_ERR_SHAPE;
+  if (!aligned16(codes) || ldc % 16 || !aligned2(scales) || !aligned16(x) || (ldx * 2) % 16 ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(y) & 3u))
+    return TQ_ERR_ALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t* flag = static_cast<uint32_t*>(workspace);
+  uint16_t* xrot = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(workspace) + 256);
+  if (!(flags & TQ_GEMM_REUSE_ROTATED)) {
+    cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return TQ_ERR_CUDA;
+    e = launch_fwht(x, TQ_BF16, ldx, xrot, TQ_F16, Ke, M, K, L.block, true, flag, s);
+    // the residual pass meets x itself: converted and laid out the same way
+    if (e == cudaSuccess && L.residual) e = launch_fwht(x, TQ_BF16, ldx, xrot + K, TQ_F16, Ke, M, K, 0, true, flag, s);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  unsigned char* split = static_cast<unsigned char*>(workspace) + gemm_split_offset(M, Ke);
+  return from_cuda(launch_gemm(codes, ldc, scales, lds, N, Ke, xrot, M, y, ldy, flag, split,
+                               ws_bytes - gemm_split_offset(M, Ke), s, (flags & TQ_GEMM_TEST_STALL) != 0, L.group));
+}
+
 tq_status tq_device_fault(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
   const unsigned int f = take_fault_gemv() | take_fault_quant() | take_fault_noalloc();

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/tq.h"
 #include "tq_device.cuh"
 
@@ -20,9 +22,24 @@ int device_max_smem_optin();
 cudaError_t launch_fwht128(const void* x, int xt, int64_t ldx, void* y, int yt, int64_t ldy, int64_t rows,
                            int64_t K, bool perm16, uint32_t* flag, cudaStream_t s);
 
+// Block FWHT of size `block` (64, 128 or 256; K a multiple of it), same
+// forms as launch_fwht128.  block == 0: no rotation, the GEMM pre-pass form
+// only (bf16 -> fp16 permuted, overflow flagged) -- the residual half of the
+// activations of a residual layout.
+cudaError_t launch_fwht(const void* x, int xt, int64_t ldx, void* y, int yt, int64_t ldy, int64_t rows, int64_t K,
+                        int block, bool perm16, uint32_t* flag, cudaStream_t s);
+
 cudaError_t launch_quantize_pack(const void* W, int wt, int64_t N, int64_t K, int64_t ldw, int fmt,
                                  uint8_t* codes2, int64_t ld2, uint8_t* codes3, int64_t ld3, uint16_t* scales,
                                  int64_t lds, cudaStream_t s);
+
+// Quantise + pack under a layout variant (block 64/128/256, group 128/256,
+// residual pass): one CTA per row, the row's trits (K, or 2K with the
+// residual pass) in shared memory; cudaErrorNotSupported when they do not fit.
+size_t quantize_layout_smem(int64_t K, int residual);
+cudaError_t launch_quantize_layout(const void* W, int wt, int64_t N, int64_t K, int64_t ldw, int block, int group,
+                                   int residual, uint8_t* codes2, int64_t ld2, uint8_t* codes3, int64_t ld3,
+                                   uint16_t* scales, int64_t lds, cudaStream_t s);
 
 // prefetch: codes and scales may be read before the preceding kernel on the
 // stream has finished (they were complete before it started).
@@ -37,11 +54,21 @@ cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16
 // rows each, 0 when the shape does not suit it.
 bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl, int* clusters);
 int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt);
+// A layout variant of the method (block size, scale group, residual pass);
+// nullptr means block 128, group 128, no residual pass.
+struct GemvLayout {
+  int block;     // 64, 128 or 256
+  int group;     // 128 or 256
+  int residual;  // codes and scales hold a residual pass after the first
+};
+
 // test_stall: failure-path test (CTA 0 withholds a copy; waits bounded by
-// milliseconds), see TQ_GEMV_TEST_STALL.
+// milliseconds), see TQ_GEMV_TEST_STALL.  lay: K counts the codes of both
+// passes of a residual layout (twice the activations' K).
 cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds,
                            int64_t N, int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
-                           bool prefetch, cudaStream_t s, bool test_stall = false);
+                           bool prefetch, cudaStream_t s, bool test_stall = false,
+                           const GemvLayout* lay = nullptr);
 
 // Returns cudaErrorNotSupported when the shape needs more shared memory than
 // one CTA can have.
@@ -50,10 +77,11 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
 constexpr int64_t kMaxSplitUnits = 160;  // one segment per SM on up to 160 SMs
 constexpr size_t kGemmSplitBytes = (size_t)kMaxSplitUnits * 256 * 256 * sizeof(float);  // 40 MiB
 // test_stall: failure-path test (CTA 0 withholds a copy; waits bounded by
-// milliseconds), see TQ_GEMM_TEST_STALL.
+// milliseconds), see TQ_GEMM_TEST_STALL.  group: weights per scale (128 or
+// 256).  K counts every code column (both passes of a residual layout).
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
                         const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, void* split_ws,
-                        size_t split_bytes, cudaStream_t s, bool test_stall = false);
+                        size_t split_bytes, cudaStream_t s, bool test_stall = false, int group = 128);
 
 // Reads and clears the device status word of the GEMV kernels (non-zero:
 // a bounded wait ran out).

@@ -224,3 +224,50 @@ def test_gemm_noalloc_validation(L):
     # M * K above the fixed scratch array (2^24 rotated activations)
     assert call(M=2048, K=27648, ldx=27648, ldc=6912, lds=216) == tq.TQ_ERR_SHAPE
     assert call(M=(1 << 24) // 256 + 1) == tq.TQ_ERR_SHAPE
+
+
+def test_layout_validation(L):
+    """Layout entry points reject bad layouts and shapes on the host."""
+    lay = tq.layout(256, 256, True)
+    assert tq.layout_codes_ld(5120, tq.TQ_PACK_2BIT, lay) == 2560
+    assert tq.layout_codes_ld(5120, tq.TQ_PACK_BASE3, lay) == 2048
+    assert tq.layout_scales_ld(5120, lay) == 40
+    assert tq.layout_scales_ld(5120, None) == 40
+    assert tq.layout_codes_ld(5120 + 128, tq.TQ_PACK_2BIT, lay) == -1  # not a multiple of 256
+    assert tq.layout_codes_ld(5120, tq.TQ_PACK_2BIT, tq.layout(96, 128, False)) == -1
+    assert tq.gemm_workspace_bytes_layout(4, 256, lay) == tq.gemm_workspace_bytes(4, 512)
+    ctypes = __import__("ctypes")
+    bad = [tq.Layout(32, 128, 0), tq.Layout(128, 64, 0), tq.Layout(128, 128, 6)]
+    for b in bad:
+        assert L.tq_gemv_layout(A, 64, tq.TQ_PACK_2BIT, B, 2, 8, 256, B, 256, 1, B, 8, ctypes.byref(b), 0,
+                                None) == tq.TQ_ERR_INVALID_ARG
+        assert L.tq_quantize_pack_layout(A, tq.TQ_BF16, 8, 256, 256, tq.TQ_PACK_2BIT, B, 64, None, 0, B, 2,
+                                         ctypes.byref(b), None) == tq.TQ_ERR_INVALID_ARG
+    lp = ctypes.byref(lay)
+    # K = 384 is not a multiple of 256
+    assert L.tq_gemv_layout(A, 256, tq.TQ_PACK_2BIT, B, 8, 8, 384, B, 384, 1, B, 8, lp, 0, None) == tq.TQ_ERR_SHAPE
+    # codes must hold both passes: ld >= 2K/4
+    assert L.tq_gemv_layout(A, 64, tq.TQ_PACK_2BIT, B, 4, 8, 256, B, 256, 1, B, 8, lp, 0, None) == tq.TQ_ERR_SHAPE
+    # scales must hold both passes: 2 x 256 / 256
+    assert L.tq_gemv_layout(A, 128, tq.TQ_PACK_2BIT, B, 1, 8, 256, B, 256, 1, B, 8, lp, 0, None) == tq.TQ_ERR_SHAPE
+    assert L.tq_gemv_layout(A, 128, tq.TQ_PACK_2BIT, B, 4, 0, 256, B, 256, 1, B, 8, lp, 0, None) == tq.TQ_OK
+    assert L.tq_gemv_layout(A, 128, tq.TQ_PACK_2BIT, B, 4, 8, 256, B, 256, 17, B, 8, lp, 0, None) == tq.TQ_ERR_SHAPE
+    assert L.tq_gemv_layout(A, 128, tq.TQ_PACK_2BIT, B, 4, 8, 256, MIS, 256, 1, B, 8, lp, 0, None) == tq.TQ_ERR_ALIGN
+    assert L.tq_gemv_layout(A, 128, tq.TQ_PACK_2BIT, B, 4, 8, 256, B, 256, 1, B, 8, lp, 4, None) == \
+        tq.TQ_ERR_INVALID_ARG
+    assert L.tq_quantize_pack_layout(A, tq.TQ_BF16, 0, 256, 256, tq.TQ_PACK_2BIT, B, 128, None, 0, B, 4, lp,
+                                     None) == tq.TQ_OK
+    assert L.tq_quantize_pack_layout(A, tq.TQ_BF16, 8, 256, 256, tq.TQ_PACK_2BIT, B, 64, None, 0, B, 4, lp,
+                                     None) == tq.TQ_ERR_SHAPE
+    assert L.tq_quantize_pack_layout(A, tq.TQ_BF16, 8, 256, 256, tq.TQ_PACK_2BIT, B, 128, None, 0, B, 1, lp,
+                                     None) == tq.TQ_ERR_SHAPE
+    assert L.tq_quantize_pack_layout(A, tq.TQ_BF16, 8, 256, 256, tq.TQ_PACK_BASE3, None, 0, B, 96, B, 4, lp,
+                                     None) == tq.TQ_ERR_SHAPE  # ld3 >= roundup16(ceil(512 / 5)) = 112
+    ws = tq.gemm_workspace_bytes_layout(4, 256, lay)
+    assert L.tq_gemm_layout(A, 128, tq.TQ_PACK_2BIT, B, 4, 8, 256, B, 256, 4, B, 8, B + 65536, ws - 1, lp, 0,
+                            None) == tq.TQ_ERR_SHAPE
+    assert L.tq_gemm_layout(A, 128, tq.TQ_PACK_BASE3, B, 4, 8, 256, B, 256, 4, B, 8, B + 65536, ws, lp, 0,
+                            None) == tq.TQ_ERR_UNSUPPORTED
+    assert L.tq_fwht(A, tq.TQ_F32, 256, B, tq.TQ_F32, 256, 2, 256, 32, None) == tq.TQ_ERR_INVALID_ARG
+    assert L.tq_fwht(A, tq.TQ_F32, 384, B, tq.TQ_F32, 384, 2, 384, 256, None) == tq.TQ_ERR_SHAPE
+    assert L.tq_fwht(A, tq.TQ_F32, 256, B, tq.TQ_F32, 256, 0, 256, 64, None) == tq.TQ_OK
