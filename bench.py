@@ -502,6 +502,36 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
                         "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4)})
     except tq.TQError as e:
         prefill.append({"shape": f"2x{N}x{K} (gate, up: one x' pre-pass)", "M": M, "unavailable": str(e)})
+    # a layer whose input is the previous layer's output: the first GEMM writes
+    # the second's x' in its epilogue (tq_gemm_rotate_next) and the second
+    # skips its pre-pass; against two plain calls, each with its pre-pass
+    N = K = HIDDEN
+    M = 2048
+    x = activations(torch, dev, K, M, seed=13 + K)
+    ws1 = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+    ws2 = torch.empty(tq.gemm_workspace_bytes(M, N), dtype=torch.uint8, device=dev)
+    ya, yb = torch.empty(M, N, device=dev), torch.empty(M, N, device=dev)
+    xz = torch.zeros(M, N, dtype=torch.bfloat16, device=dev)
+
+    def chained():
+        tq.gemm_rotate_next(mats["h2h_a"][3], mats["h2h_a"][4], x, K, ws2, workspace=ws1, out=ya)
+        tq.gemm(mats["h2h_b"][3], mats["h2h_b"][4], xz, N, tq.TQ_PACK_2BIT, workspace=ws2, out=yb,
+                reuse_rotated=True)
+
+    def two_plain():
+        tq.gemm(mats["h2h_a"][3], mats["h2h_a"][4], x, K, tq.TQ_PACK_2BIT, workspace=ws1, out=ya)
+        tq.gemm(mats["h2h_b"][3], mats["h2h_b"][4], x, N, tq.TQ_PACK_2BIT, workspace=ws2, out=yb)
+
+    try:
+        ms_c = time_events(chained, 10, torch)
+        ms_p = time_events(two_plain, 10, torch)
+        for label, ms in (("chained: x' of the second written by the first's epilogue", ms_c),
+                          ("two plain calls, each with its pre-pass", ms_p)):
+            tf = 2 * 2 * M * N * K / (ms * 1e-3) / 1e12
+            prefill.append({"shape": f"2x{N}x{K} ({label})", "M": M, "us": round(ms * 1e3, 1),
+                            "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4)})
+    except tq.TQError as e:
+        prefill.append({"shape": f"2x{N}x{K} chained", "M": M, "unavailable": str(e)})
     out["prefill"] = prefill
     # --- offline quantise + pack of one layer group, weights resident (bf16)
     sweep = []

@@ -215,6 +215,25 @@ TQ_API tq_status tq_gemm_ex(const uint8_t *codes, int64_t ldc, int fmt, const ui
                   int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
                   void *workspace, size_t ws_bytes, unsigned int flags, tq_stream stream);
 
+/* tq_gemm_ex that also hands its output to the next layer already rotated
+ * (the activation transform fused into the producer of x: dpshk.com/news/
+ * 5289456 sec. 4.2, mhpq.cn/news/1159370 sec. 3.3).  Besides y it writes
+ * FWHT-128(y), computed in fp32 from the accumulators in the staged order and
+ * rounded once to fp16, into next_ws -- the rotated activations of a
+ * following tq_gemm_ex(..., TQ_GEMM_REUSE_ROTATED) on next_ws whose x is this
+ * call's y (M rows, K_next = N), which then skips its pre-pass -- and records
+ * their fp16 overflow in next_ws's status word (cleared first; read with
+ * tq_gemm_check_range(next_ws)).  The fp16 x' comes from the fp32 y, not from
+ * y rounded to bf16 as the plain chain would give it.  N must be a multiple
+ * of 128 and next_ws_bytes >= tq_gemm_workspace_bytes(M, N); the output
+ * tiles are then whole 128-column groups and the K split of a short last wave
+ * is not used.  next_ws must not overlap workspace.  Flags and everything
+ * else as tq_gemm_ex. */
+TQ_API tq_status tq_gemm_rotate_next(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales,
+                                     int64_t lds, int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M,
+                                     float *y, int64_t ldy, void *workspace, size_t ws_bytes, unsigned int flags,
+                                     void *next_ws, size_t next_ws_bytes, tq_stream stream);
+
 /* Synchronises `stream`, then reads the status word the last tq_gemm left in
  * `workspace`: TQ_ERR_RANGE if a rotated activation overflowed fp16 (the
  * output is then not meaningful), else TQ_OK. */

@@ -32,7 +32,8 @@ TQ_PACK_2BIT, TQ_PACK_BASE3, TQ_PACK_BOTH = 1, 2, 3
 EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_quantize_pack", "tq_gemv",
             "tq_gemv_ex", "tq_gemv_path", "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_ex", "tq_gemm_check_range",
             "tq_device_fault", "tq_gemm_noalloc", "tq_layout_codes_ld", "tq_layout_scales_ld", "tq_fwht",
-            "tq_quantize_pack_layout", "tq_gemv_layout", "tq_gemm_workspace_bytes_layout", "tq_gemm_layout")
+            "tq_quantize_pack_layout", "tq_gemv_layout", "tq_gemm_workspace_bytes_layout", "tq_gemm_layout",
+            "tq_gemm_rotate_next")
 TQ_GEMV_TENSOR_MEMORY, TQ_GEMV_MMA_SYNC = 1, 2
 TQ_GEMV_WEIGHTS_READY = 1
 TQ_GEMM_REUSE_ROTATED = 1
@@ -99,6 +100,9 @@ def lib() -> ctypes.CDLL:
         L.tq_device_fault.argtypes = []
         L.tq_gemm_noalloc.restype = _int
         L.tq_gemm_noalloc.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp]
+        L.tq_gemm_rotate_next.restype = _int
+        L.tq_gemm_rotate_next.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
+                                          ctypes.c_size_t, ctypes.c_uint, _vp, ctypes.c_size_t, _vp]
         lp = ctypes.POINTER(Layout)
         L.tq_layout_codes_ld.restype = _i64
         L.tq_layout_codes_ld.argtypes = [_i64, _int, lp]
@@ -353,4 +357,26 @@ def gemm_layout(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: i
                               x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), workspace.data_ptr(),
                               workspace.numel() * workspace.element_size(), _lp(lay), flags, _stream(stream))
     _check(st, "tq_gemm_layout")
+    return out
+
+
+def gemm_rotate_next(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, next_ws: torch.Tensor,
+                     workspace: torch.Tensor | None = None, out: torch.Tensor | None = None, stream=None,
+                     flags: int = 0) -> torch.Tensor:
+    """gemm that also writes FWHT-128(y) into next_ws as the x' of a following
+    gemm(..., workspace=next_ws, reuse_rotated=True) whose x is this y."""
+    _cuda2d(codes, "codes")
+    _cuda2d(scales, "scales")
+    _cuda2d(x, "x")
+    N = codes.shape[0]
+    M = x.shape[0]
+    if workspace is None:
+        workspace = torch.empty(gemm_workspace_bytes(M, K), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    st = lib().tq_gemm_rotate_next(codes.data_ptr(), codes.stride(0), TQ_PACK_2BIT, scales.data_ptr(),
+                                   scales.stride(0), N, K, x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0),
+                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(), flags,
+                                   next_ws.data_ptr(), next_ws.numel() * next_ws.element_size(), _stream(stream))
+    _check(st, "tq_gemm_rotate_next")
     return out

@@ -195,6 +195,13 @@ struct Params {
   int stall_cta;
   unsigned long long wait_ns;
   int lgs;  // one scale per 128 << lgs weights (layout variants: groups of 256)
+  // Fused producer of the next layer's x': when xnext is set (whole tiles of
+  // whole 128-column groups, no K split), the epilogue also writes
+  // FWHT-128(y) rounded to fp16, in the GEMM's k order inside each 16-chunk,
+  // to xnext ([M][ldxn]) and ORs fp16 overflow into *flag_next.
+  uint16_t* xnext;
+  int64_t ldxn;
+  uint32_t* flag_next;
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SmemCtl* ctl, uint32_t* flag) {
@@ -203,6 +210,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sm
   return false;
 }
 
+// EXT: the layout variants' scale groups (lgs) and the fused producer of the
+// next layer's x' (xnext) are compiled in; without it the kernel is the
+// method's plain GEMM.
+template <bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
               const __grid_constant__ CUtensorMap pmap, const Params p) {
@@ -308,7 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return (in_tile && st < nk) ? ldg_nc_u4(crow + (s0 + st) * (BK / 4)) : make_uint4(0, 0, 0, 0);
     };
     auto ld_scale = [&](int st) {
-      return (row_ok && st < nk) ? __ldg(srow + (((s0 + st) * BK) >> (7 + p.lgs))) : (uint16_t)0;
+      const int lgs = EXT ? p.lgs : 0;
+      return (row_ok && st < nk) ? __ldg(srow + (((s0 + st) * BK) >> (7 + lgs))) : (uint16_t)0;
     };
     uint4 cur = ld_codes(0), nx1 = ld_codes(1);
     uint16_t scur = ld_scale(0), snx1 = ld_scale(1);
@@ -396,6 +408,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i)  // constant indices keep v in registers
             if (c0 + i < ncols) yrow[c0 + i] = v[i];
+        }
+      }
+    }
+    // ---- the next layer's rotated activations: FWHT-128 of each 128-column
+    // group of this thread's row of y, all in registers (the row of a
+    // tensor-memory lane is one thread's), in the staged order of the
+    // definition (h = 1 .. 64, lower element a + b, then * c), fp16 RN
+    if (EXT && p.xnext != nullptr && unit < 0) {
+      const bool row_ok = m < p.M;
+#pragma unroll 1
+      for (int j = 0; j < bn / 128 && n0 + 128 * j < p.N; ++j) {  // warp-uniform bounds
+        float w[128];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          __syncwarp();
+          tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * BN + 128 * j + 32 * q), w + 32 * q);
+        }
+        if (__any_sync(0xffffffffu, ctl->abort != 0)) break;
+#pragma unroll
+        for (int h = 1; h < 128; h *= 2) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            if ((i & h) == 0) {
+              const float a = w[i], b = w[i + h];
+              w[i] = __fadd_rn(a, b);
+              w[i + h] = __fsub_rn(a, b);
+            }
+          }
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          w[i] = __fmul_rn(w[i], kInvSqrt128);
+          amax = fmaxf(amax, fabsf(w[i]));
+        }
+        if (!row_ok) continue;
+        // |v| >= 65520 rounds to an fp16 infinity (round to nearest even)
+        if (amax >= 65520.0f) atomicOr(p.flag_next, 1u);
+        uint16_t* dst = p.xnext + m * p.ldxn + n0 + 128 * j;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16-chunk c: slots hold elements 0, 8, 1, 9, ..., 7, 15
+          uint32_t o[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[i] = pack_half2(w[16 * c + i], w[16 * c + 8 + i]);
+          reinterpret_cast<uint4*>(dst + 16 * c)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          reinterpret_cast<uint4*>(dst + 16 * c)[1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
       }
     }
@@ -498,12 +556,14 @@ struct GemmPlan {
 
 constexpr int64_t kFillStages = 4;
 
-static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes) {
+static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes, bool whole_groups = false) {
   const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 1;
   const int64_t tm = (M + BM - 1) / BM, nk = K / BK;
   GemmPlan best{BN, 0, 0, 0};
   int64_t best_cost = -1;
-  for (int bn = BN; bn >= 64; bn -= 16) {
+  // whole_groups: tiles of whole 128-column groups (bn 256 or 128), no K split
+  if (whole_groups) split_bytes = 0;
+  for (int bn = BN; bn >= 64; bn -= whole_groups ? 128 : 16) {
     const int64_t tiles = tm * ((N + bn - 1) / bn), w = bn + 96, c = (nk + kFillStages) * w;
     const int64_t full = tiles / sms, L = tiles - full * sms;
     int64_t cost = (full + (L > 0 ? 1 : 0)) * c, n_main = tiles, S = 0;
@@ -531,7 +591,8 @@ static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes) {
 
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
                         const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, void* split_ws,
-                        size_t split_bytes, cudaStream_t s, bool test_stall, int group) {
+                        size_t split_bytes, cudaStream_t s, bool test_stall, int group, uint16_t* xnext,
+                        uint32_t* flag_next) {
   if (N == 0 || M == 0) return cudaSuccess;
   if ((int64_t)device_max_smem_optin() < (int64_t)kGemmSmem) return cudaErrorNotSupported;
   EncodeTiledFn enc = encode_fn();
@@ -560,7 +621,11 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   p.wait_ns = test_stall ? kTestWaitLimitNs : kWaitLimitNs;
   p.lgs = group == 256 ? 1 : 0;
   p.n_tiles_m = (int)((M + BM - 1) / BM);
-  const GemmPlan g = gemm_plan(N, M, K, split_ws != nullptr ? split_bytes : 0);
+  const GemmPlan g = gemm_plan(N, M, K, split_ws != nullptr ? split_bytes : 0, xnext != nullptr);
+  if (xnext != nullptr && (N % 128 != 0 || g.bn % 128 != 0)) return cudaErrorNotSupported;
+  p.xnext = xnext;
+  p.ldxn = N;
+  p.flag_next = flag_next;
   p.bn = g.bn;
   p.idesc = idesc_f16(p.bn);
   p.vec_store = ((reinterpret_cast<uintptr_t>(y) & 15u) == 0 && ldy % 4 == 0) ? 1 : 0;
@@ -586,7 +651,9 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!smem_set[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return e;
     smem_set[dev].store(true, std::memory_order_release);
   }
@@ -600,7 +667,9 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, map, ymap, pmap, p);
+  const bool ext = p.lgs != 0 || p.xnext != nullptr;
+  cudaError_t e = ext ? cudaLaunchKernelEx(&cfg, k_gemm_tc<true>, map, ymap, pmap, p)
+                      : cudaLaunchKernelEx(&cfg, k_gemm_tc<false>, map, ymap, pmap, p);
   if (e != cudaSuccess || n_split_tiles == 0) return e;
   // y of the split tiles: the partials added in segment order
   const int64_t work = n_split_tiles * BM * (p.bn / 4);

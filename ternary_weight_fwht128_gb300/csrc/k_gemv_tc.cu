@@ -466,7 +466,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ct
 
 // Shared memory (1024-aligned): [code ring][B: groups_cap x kGroupB][zeros kZeroBytes]
 // [ztab: groups_cap x kZs x {pw Zt, pw}][partial sums: tiles_cap x kcl x M x 128 / kcl][Ctl]
-template <int V, bool B3>
+// LAYOUT: the layout variants' parameters (blk, lgs, g_rot) are read; without
+// it the kernel is compiled for the method's own layout only.
+template <int V, bool B3, bool LAYOUT>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__ CUtensorMap cmap, const Params p) {
   using Gm = Geo<V, B3>;
   using Fg = FmtGeo<B3>;
@@ -591,16 +593,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   for (int it = pwarp; it < ng * M && warp != kTmaWarp; it += kThreads / 32 - 1) {
     const int gl = it / M, m = it - gl * M;
     const int i8 = lane >> 2, jc = lane & 3;
-    // a residual layout's second half of the codes meets x itself
-    const int64_t gg = g0 + gl;
-    const bool rot = gg < p.g_rot;
-    const int64_t xc = rot ? gg : gg - p.g_rot;
-    const uint16_t* xrow = p.x + m * p.ldx + 16 * i8 + jc;
-    const uint16_t* xg = xrow + xc * 128;
     float v[4];
+    if constexpr (LAYOUT) {
+      // a residual layout's second half of the codes meets x itself
+      const int64_t gg = g0 + gl;
+      const bool rot = gg < p.g_rot;
+      const int64_t xc = rot ? gg : gg - p.g_rot;
+      const uint16_t* xrow = p.x + m * p.ldx + 16 * i8 + jc;
+      const uint16_t* xg = xrow + xc * 128;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ldg_nc_u16(xg + 4 * b) << 16);
-    if (rot) rotate_group(v, lane, p.blk, xrow + (xc ^ 1) * 128, (xc & 1) != 0);
+      for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ldg_nc_u16(xg + 4 * b) << 16);
+      if (rot) rotate_group(v, lane, p.blk, xrow + (xc ^ 1) * 128, (xc & 1) != 0);
+    } else {
+      const uint16_t* xg = p.x + m * p.ldx + (g0 + gl) * 128 + 16 * i8 + jc;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ldg_nc_u16(xg + 4 * b) << 16);
+      fwht128_strided(v, lane);
+    }
     float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
@@ -823,11 +832,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       for (int h = 0; h < kGS; ++h) sc[h] = 0u;
       const int64_t n = (t0 + tl) * 128 + r;
       if (tl >= ntiles || n >= p.N) return;
-      const uint16_t* q = p.scales + n * p.lds;
-      const int64_t gc = g0 + kGS * c;  // a scale per 2^lgs groups of 128
+      if constexpr (LAYOUT) {
+        const uint16_t* q = p.scales + n * p.lds;
+        const int64_t gc = g0 + kGS * c;  // a scale per 2^lgs groups of 128
 #pragma unroll
-      for (int h = 0; h < kGS; ++h)
-        if (kGS * c + h < ng) sc[h] = __ldg(q + ((gc + h) >> p.lgs));
+        for (int h = 0; h < kGS; ++h)
+          if (kGS * c + h < ng) sc[h] = __ldg(q + ((gc + h) >> p.lgs));
+      } else {
+        const uint16_t* q = p.scales + n * p.lds + g0 + kGS * c;
+#pragma unroll
+        for (int h = 0; h < kGS; ++h)
+          if (kGS * c + h < ng) sc[h] = __ldg(q + h);
+      }
     };
     // The scales are loaded kAhead stages before they are used (a DRAM miss
     // takes longer than a stage).  The stage loop is unrolled by kAhead so
@@ -1023,7 +1039,8 @@ int max_active_clusters(int kcl) {
   int v = cache[dev][slot].load(std::memory_order_acquire);
   if (v > 0) return v;
   const int smem = device_max_smem_optin();
-  if (cudaFuncSetAttribute(k_gemv_tc<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(k_gemv_tc<1, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(device_sm_count() * kcl));
@@ -1036,7 +1053,7 @@ int max_active_clusters(int kcl) {
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaOccupancyMaxActiveClusters(&v, k_gemv_tc<1, false>, &cfg) != cudaSuccess || v < 1) {
+  if (cudaOccupancyMaxActiveClusters(&v, k_gemv_tc<1, false, false>, &cfg) != cudaSuccess || v < 1) {
     (void)cudaGetLastError();
     return 0;
   }
@@ -1044,14 +1061,15 @@ int max_active_clusters(int kcl) {
   return v;
 }
 
-template <int V, bool B3>
+template <int V, bool B3, bool LAYOUT>
 cudaError_t launch_v(const CUtensorMap& map, const Params& p, size_t smem, cudaStream_t s) {
   // raise the kernel's shared-memory limit only when a launch needs more
   static std::atomic<int> smem_set[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem_set[dev].load(std::memory_order_acquire) < (int)smem) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemv_tc<V, B3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_gemv_tc<V, B3, LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int cur = smem_set[dev].load(std::memory_order_acquire);
     while (cur < (int)smem && !smem_set[dev].compare_exchange_weak(cur, (int)smem)) {
@@ -1071,7 +1089,7 @@ cudaError_t launch_v(const CUtensorMap& map, const Params& p, size_t smem, cudaS
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemv_tc<V, B3>, map, p);
+  return cudaLaunchKernelEx(&cfg, k_gemv_tc<V, B3, LAYOUT>, map, p);
 }
 
 // Cost model of the busiest CTA, in units of 1/24 stage: a stage streams
@@ -1206,20 +1224,18 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
   // the register count: each allocates all of tensor memory, and a second
   // one would block in tcgen05.alloc while its cluster peers wait for it.
   const size_t smem = std::max(smem_bytes(b3, p.groups_cap, p.tiles_cap, M), (size_t)(smem_max / 2 + 1024));
-  if (b3) {
-    switch (variant_of(M)) {
-      case 1: return launch_v<1, true>(map, p, smem, s);
-      case 2: return launch_v<2, true>(map, p, smem, s);
-      case 3: return launch_v<3, true>(map, p, smem, s);
-      default: return launch_v<4, true>(map, p, smem, s);
-    }
+  const bool lv = lay != nullptr && (lay->block != 128 || lay->group != 128 || lay->residual);
+  const int v = variant_of(M);
+  if (lv) {
+    if (b3) return v == 1 ? launch_v<1, true, true>(map, p, smem, s) : v == 2 ? launch_v<2, true, true>(map, p, smem, s)
+                 : v == 3 ? launch_v<3, true, true>(map, p, smem, s) : launch_v<4, true, true>(map, p, smem, s);
+    return v == 1 ? launch_v<1, false, true>(map, p, smem, s) : v == 2 ? launch_v<2, false, true>(map, p, smem, s)
+           : v == 3 ? launch_v<3, false, true>(map, p, smem, s) : launch_v<4, false, true>(map, p, smem, s);
   }
-  switch (variant_of(M)) {
-    case 1: return launch_v<1, false>(map, p, smem, s);
-    case 2: return launch_v<2, false>(map, p, smem, s);
-    case 3: return launch_v<3, false>(map, p, smem, s);
-    default: return launch_v<4, false>(map, p, smem, s);
-  }
+  if (b3) return v == 1 ? launch_v<1, true, false>(map, p, smem, s) : v == 2 ? launch_v<2, true, false>(map, p, smem, s)
+               : v == 3 ? launch_v<3, true, false>(map, p, smem, s) : launch_v<4, true, false>(map, p, smem, s);
+  return v == 1 ? launch_v<1, false, false>(map, p, smem, s) : v == 2 ? launch_v<2, false, false>(map, p, smem, s)
+         : v == 3 ? launch_v<3, false, false>(map, p, smem, s) : launch_v<4, false, false>(map, p, smem, s);
 }
 
 }  // namespace tq

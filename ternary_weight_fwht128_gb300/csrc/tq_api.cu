@@ -190,6 +190,43 @@ tq_status tq_gemm_ex(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t*
                                ws_bytes - gemm_split_offset(M, K), s, (flags & TQ_GEMM_TEST_STALL) != 0));
 }
 
+tq_status tq_gemm_rotate_next(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds,
+                              int64_t N, int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
+                              void* workspace, size_t ws_bytes, unsigned int flags, void* next_ws,
+                              size_t next_ws_bytes, tq_stream stream) {
+  if (flags & ~(unsigned int)(TQ_GEMM_REUSE_ROTATED | TQ_GEMM_TEST_STALL)) return TQ_ERR_INVALID_ARG;
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return TQ_ERR_INVALID_ARG;
+  if (N < 0 || M < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_ok(K) || N % 128 != 0) return TQ_ERR_SHAPE;
+  if (N == 0 || M == 0) return TQ_OK;
+  if (fmt != TQ_PACK_2BIT) return TQ_ERR_UNSUPPORTED;
+  if (codes == nullptr || scales == nullptr || x == nullptr || y == nullptr || workspace == nullptr ||
+      next_ws == nullptr)
+    return TQ_ERR_INVALID_ARG;
+  if (ldc < K / 4 || lds < K / 128 || ldx < K || ldy < N) return TQ_ERR_SHAPE;
+  if (ws_bytes < tq_gemm_workspace_bytes(M, K) || next_ws_bytes < tq_gemm_workspace_bytes(M, N)) return TQ_ERR_SHAPE;
+  if (!aligned16(codes) || ldc % 16 || !aligned2(scales) || !aligned16(x) || (ldx * 2) % 16 ||
+      !aligned16(workspace) || !aligned16(next_ws) || (reinterpret_cast<uintptr_t>(y) & 3u))
+    return TQ_ERR_ALIGN;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(workspace), b0 = reinterpret_cast<uintptr_t>(next_ws);
+  if (a0 < b0 + next_ws_bytes && b0 < a0 + ws_bytes) return TQ_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t* flag = static_cast<uint32_t*>(workspace);
+  uint16_t* xrot = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(workspace) + 256);
+  uint32_t* flag_next = static_cast<uint32_t*>(next_ws);
+  uint16_t* xnext = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(next_ws) + 256);
+  cudaError_t e = cudaMemsetAsync(flag_next, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return TQ_ERR_CUDA;
+  if (!(flags & TQ_GEMM_REUSE_ROTATED)) {
+    e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return TQ_ERR_CUDA;
+    e = launch_fwht128(x, TQ_BF16, ldx, xrot, TQ_F16, K, M, K, true, flag, s);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return from_cuda(launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, nullptr, 0, s,
+                               (flags & TQ_GEMM_TEST_STALL) != 0, 128, xnext, flag_next));
+}
+
 tq_status tq_gemm_check_range(const void* workspace, tq_stream stream) {
   if (workspace == nullptr) return TQ_ERR_INVALID_ARG;
   if (!aligned16(workspace)) return TQ_ERR_ALIGN;

@@ -271,3 +271,26 @@ def test_layout_validation(L):
     assert L.tq_fwht(A, tq.TQ_F32, 256, B, tq.TQ_F32, 256, 2, 256, 32, None) == tq.TQ_ERR_INVALID_ARG
     assert L.tq_fwht(A, tq.TQ_F32, 384, B, tq.TQ_F32, 384, 2, 384, 256, None) == tq.TQ_ERR_SHAPE
     assert L.tq_fwht(A, tq.TQ_F32, 256, B, tq.TQ_F32, 256, 0, 256, 64, None) == tq.TQ_OK
+
+
+def test_gemm_rotate_next_validation(L):
+    f = L.tq_gemm_rotate_next
+    ws = tq.gemm_workspace_bytes(4, 256)
+    wsn = tq.gemm_workspace_bytes(4, 128)
+    W1, W2 = B + 65536, B + 65536 + (1 << 27)
+    ok = dict(c=A, ldc=64, fmt=tq.TQ_PACK_2BIT, s=B, lds=2, N=128, K=256, x=B + 4096, ldx=256, M=4, y=B + 8192,
+              ldy=128, w=W1, wsb=ws, fl=0, nw=W2, nwb=wsn)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["c"], a["ldc"], a["fmt"], a["s"], a["lds"], a["N"], a["K"], a["x"], a["ldx"], a["M"], a["y"],
+                 a["ldy"], a["w"], a["wsb"], a["fl"], a["nw"], a["nwb"], None)
+
+    assert call(M=0) == tq.TQ_OK
+    assert call(N=192, ldy=192) == tq.TQ_ERR_SHAPE        # N not a multiple of 128
+    assert call(nwb=wsn - 1) == tq.TQ_ERR_SHAPE
+    assert call(nw=None) == tq.TQ_ERR_INVALID_ARG
+    assert call(nw=W1 + 4096) == tq.TQ_ERR_INVALID_ARG      # overlaps the workspace
+    assert call(nw=W2 + 8) == tq.TQ_ERR_ALIGN
+    assert call(fl=4) == tq.TQ_ERR_INVALID_ARG
+    assert call(fmt=tq.TQ_PACK_BASE3) == tq.TQ_ERR_UNSUPPORTED

@@ -560,3 +560,60 @@ def test_gemm_range_flag():
     x[3].zero_()
     tq.gemm(c2, s, x, K, workspace=ws)
     tq.gemm_check_range(ws)  # cleared on the next call
+
+
+# ------------------------------------------- the rotation fused into the producer
+
+def _unpermute16(xp: np.ndarray) -> np.ndarray:
+    """Inverse of the GEMM k order inside each 16-chunk (slots 0, 8, 1, 9, ...)."""
+    M, K = xp.shape
+    v = xp.reshape(M, K // 16, 8, 2)
+    return np.concatenate([v[:, :, :, 0], v[:, :, :, 1]], axis=2).reshape(M, K)
+
+
+@pytest.mark.parametrize("N1,K1,N2,M", [(1280, 640, 512, 300), (5120, 5120, 1024, 2048), (384, 256, 256, 257)])
+def test_gemm_rotate_next_chain(orc, N1, K1, N2, M):
+    """The first GEMM writes FWHT-128 of its output as the second's fp16 x':
+    bit for bit the rounded staged fp32 transform of y1, and the second GEMM
+    (pre-pass skipped) matches the oracle applied to y1."""
+    W1 = synth.weights(N1, K1, 61, dtype="bf16")
+    W2 = synth.weights(N2, N1, 62, dtype="bf16")
+    c1, _, s1 = tq.quantize_pack(to_dev_bf16(W1), tq.TQ_PACK_2BIT)
+    c2, _, s2 = tq.quantize_pack(to_dev_bf16(W2), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(synth.activations(M, K1, 63))
+    ws2 = torch.empty(tq.gemm_workspace_bytes(M, N1), dtype=torch.uint8, device="cuda")
+    y1 = tq.gemm_rotate_next(c1, s1, x, K1, ws2)
+    torch.cuda.synchronize()
+    tq.gemm_check_range(ws2)
+    y1n = y1.cpu().numpy()
+    xr = ws2[256:256 + 2 * M * N1].view(torch.float16).view(M, N1).cpu().numpy()
+    ref_xr = orc.fwht128_f32(y1n).astype(np.float16)
+    assert np.array_equal(_unpermute16(xr).view(np.uint16), ref_xr.view(np.uint16))
+    y2 = tq.gemm(c2, s2, torch.zeros(M, N1, dtype=torch.bfloat16, device="cuda"), N1, workspace=ws2,
+                 reuse_rotated=True)
+    torch.cuda.synchronize()
+    rows = np.arange(0, N2, max(1, N2 // 64))
+    T2, S2 = orc.quantize(W2, rows)
+    mrows = np.arange(0, M, max(1, M // 48))
+    check_y(y2.cpu().numpy()[np.ix_(mrows, rows)], orc.gemv(T2, S2, y1n[mrows]), "chained y2")
+    T1, S1 = orc.quantize(W1, rows[rows < N1])
+    check_y(y1n[np.ix_(mrows, rows[rows < N1])], orc.gemv(T1, S1, synth.bf16_bits_to_f32(
+        synth.activations(M, K1, 63))[mrows]), "y1")
+
+
+def test_gemm_rotate_next_reports_overflow():
+    """An output whose rotation overflows fp16 is reported on the next workspace."""
+    N1, K1, M = 256, 256, 128
+    # weights ~N(0, 2000): fp16 scales near 1600, outputs of a few 10^4 whose
+    # rotation exceeds 65504; the activations' own rotation stays in range
+    W1 = synth.weights(N1, K1, 64, dtype="f32", std=2000.0)
+    c1, _, s1 = tq.quantize_pack(to_dev_f32(W1), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(synth.activations(M, K1, 65))
+    ws2 = torch.empty(tq.gemm_workspace_bytes(M, N1), dtype=torch.uint8, device="cuda")
+    ws1 = torch.empty(tq.gemm_workspace_bytes(M, K1), dtype=torch.uint8, device="cuda")
+    y1 = tq.gemm_rotate_next(c1, s1, x, K1, ws2, workspace=ws1)
+    tq.gemm_check_range(ws1)
+    assert torch.isfinite(y1).all()
+    with pytest.raises(tq.TQError) as e:
+        tq.gemm_check_range(ws2)
+    assert e.value.status == tq.TQ_ERR_RANGE
