@@ -4,8 +4,10 @@
 Headline (the `value` of the JSON line): decode GEMV throughput on packed
 weight bytes (codes + fp16 scales), GB/s, for one decode step = one token
 (M = 1) through the linear layers of a 64-layer stack of 27B-class shapes
-(per layer 5120x5120 x2, 27648x5120 x2, 5120x27648; 2-bit codes): 320 GEMV
-launches and 8.1 GB of packed weights per step, far larger than L2, so every
+(per layer 5120x5120 x2, 27648x5120 x2, 5120x27648; 2-bit codes; gate and up
+read the same x, so their rows are stored as one 55296x5120 matrix and run as
+one GEMV): 256 GEMV launches and 8.1 GB of packed weights per step, far larger
+than L2, so every
 step streams its weights from HBM.  The activation FWHT-128 runs inside every
 GEMV launch.  Extra keys report the other hot-path rows: skinny M = 2..16
 (2-bit and base-3), the tensor-core prefill GEMM (M = 2048), and the offline
@@ -32,8 +34,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HIDDEN, FFN, LAYERS = 5120, 27648, 64
-# (name, N, K, count per layer): two 5120x5120, two 27648x5120, one 5120x27648
-LAYER_SHAPES = [("h2h_a", HIDDEN, HIDDEN), ("h2h_b", HIDDEN, HIDDEN), ("gate", FFN, HIDDEN), ("up", FFN, HIDDEN),
+# (name, N, K) per layer: two 5120x5120, gate and up (two 27648x5120 that read
+# the same x, stored as one matrix of 2 x 27648 rows), one 5120x27648
+LAYER_SHAPES = [("h2h_a", HIDDEN, HIDDEN), ("h2h_b", HIDDEN, HIDDEN), ("gate_up", 2 * FFN, HIDDEN),
                 ("down", HIDDEN, FFN)]
 METRIC = "ternary GEMV packed-weight HBM GB/s (% of peak); prefill GEMM TFLOP/s"
 # DRAM bytes per algorithmic byte of k_gemv_tc, from an ncu capture of one
@@ -41,7 +44,8 @@ METRIC = "ternary GEMV packed-weight HBM GB/s (% of peak); prefill GEMM TFLOP/s"
 # 37,668,096 + 256 for 37,601,280 packed bytes (every weight byte read once).
 GEMV_TC_TRAFFIC_RATIO = (37668096 + 256) / 37601280
 WORKLOAD = ("decode GEMV M=1, 2-bit codes, 64-layer stack of 27B-class shapes "
-            "{5120x5120 x2, 27648x5120 x2, 5120x27648} per layer (320 launches, FWHT-128 fused)")
+            "{5120x5120 x2, 27648x5120 x2, 5120x27648} per layer; gate and up (the two 27648x5120, same x) "
+            "stored as one 55296x5120 matrix and run as one GEMV (256 launches, FWHT-128 fused)")
 
 
 def packed_bytes(N: int, K: int, fmt: str = "2bit") -> int:
@@ -181,7 +185,7 @@ def build_stack(tq, torch, dev, seed: int, keep_weights: bool = False):
         for name, N, K in LAYER_SHAPES:
             Wb = synth_weight(torch, gen, dev, N, K)
             # base-3 codes as well for the shapes the skinny comparison uses
-            fmt = tq.TQ_PACK_BOTH if name in ("gate", "down") else tq.TQ_PACK_2BIT
+            fmt = tq.TQ_PACK_BOTH if name in ("gate_up", "down") else tq.TQ_PACK_2BIT
             c2, c3, s = tq.quantize_pack(Wb, fmt)
             mats.append((name, N, K, c2, s, c3))
             if keep_weights:
@@ -264,7 +268,7 @@ def gpu_arm(args, world, rank, local):
 
     stack, sweep_w = build_stack(tq, torch, dev, seed=1000 + rank, keep_weights=not args.quick)
     xs = {K: activations(torch, dev, K, 1, seed=K) for K in (HIDDEN, FFN)}
-    ys = {N: torch.empty(1, N, device=dev) for N in (HIDDEN, FFN)}
+    ys = {N: torch.empty(1, N, device=dev) for N in sorted({N for _, N, _ in LAYER_SHAPES})}
     launches_per_step = LAYERS * len(LAYER_SHAPES)
 
     # the weights are written once, before any timing: every GEMV may start
@@ -281,7 +285,7 @@ def gpu_arm(args, world, rank, local):
             fn()
 
     # eager steps first: one-time set-up (attributes, occupancy queries) runs
-    # before the capture; then the step's 320 launches become one CUDA graph
+    # before the capture; then the step's 256 launches become one CUDA graph
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -330,7 +334,7 @@ def gpu_arm(args, world, rank, local):
 
     # ---- end to end through the public API with host buffers: every step
     # copies its activations in from pinned host memory (one token row per
-    # input width), replays the step's 320 GEMVs, and reads its outputs back.
+    # input width), replays the step's 256 GEMVs, and reads its outputs back.
     hx = {K: xs[K].cpu().pin_memory() for K in xs}
     hy = {N: torch.empty(1, N, dtype=torch.float32).pin_memory() for N in ys}
     dx = {K: torch.empty_like(xs[K]) for K in xs}
@@ -395,7 +399,7 @@ def gpu_arm(args, world, rank, local):
         "data": "synthetic (seeded; weights N(0,0.02)+0.1% x20 outliers, x N(0,1)+4 channels x30)",
         "config": {"workload": WORKLOAD, "M": 1, "layers": LAYERS, "packed_bytes_per_step": bytes_step,
                    "launches_per_step": launches_per_step,
-                   "launch": "one CUDA graph per step (320 launches, programmatic dependent launch edges; "
+                   "launch": "one CUDA graph per step (256 launches, programmatic dependent launch edges; "
                              "tq_gemv_ex with TQ_GEMV_WEIGHTS_READY: weights stream while the previous GEMV ends)",
                    "l2": "inputs larger than L2 (8.1 GB of packed weights streamed per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -445,8 +449,13 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
     skinny = []
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
-    for (name, N, K) in (("gate", FFN, HIDDEN), ("down", HIDDEN, FFN)):
-        mats = [[m for m in layer if m[0] == name][0] for layer in stack]
+    def rows_of(m, n):
+        # (name, N, K, c2, s, c3) restricted to the first n rows (gate of gate_up)
+        nm, _, K, c2, s, c3 = m
+        return (nm, n, K, c2[:n], s[:n], c3[:n] if c3 is not None else None)
+
+    for (name, N, K) in (("gate_up", FFN, HIDDEN), ("down", HIDDEN, FFN)):
+        mats = [rows_of([m for m in layer if m[0] == name][0], N) for layer in stack]
         for fmt_name, fmt in (("2bit", tq.TQ_PACK_2BIT), ("base3", tq.TQ_PACK_BASE3)):
             for M in (1, 2, 4, 8, 16):
                 x = activations(torch, dev, K, M, seed=K + M)
@@ -469,8 +478,8 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
     out["skinny"] = skinny
     # --- prefill GEMM, M = 2048 on the three shapes
     prefill = []
-    for name, N, K in (("h2h_a", HIDDEN, HIDDEN), ("gate", FFN, HIDDEN), ("down", HIDDEN, FFN)):
-        _, _, _, c2, s, _ = [m for m in stack[0] if m[0] == name][0]
+    for name, N, K in (("h2h_a", HIDDEN, HIDDEN), ("gate_up", FFN, HIDDEN), ("down", HIDDEN, FFN)):
+        _, _, _, c2, s, _ = rows_of([m for m in stack[0] if m[0] == name][0], N)
         M = 2048
         x = activations(torch, dev, K, M, seed=11 + K)
         ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
@@ -492,8 +501,9 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
     yg, yu = torch.empty(M, N, device=dev), torch.empty(M, N, device=dev)
 
     def pair():
-        tq.gemm(mats["gate"][3], mats["gate"][4], x, K, tq.TQ_PACK_2BIT, workspace=ws, out=yg)
-        tq.gemm(mats["up"][3], mats["up"][4], x, K, tq.TQ_PACK_2BIT, workspace=ws, out=yu, reuse_rotated=True)
+        gu = mats["gate_up"]
+        tq.gemm(gu[3][:FFN], gu[4][:FFN], x, K, tq.TQ_PACK_2BIT, workspace=ws, out=yg)
+        tq.gemm(gu[3][FFN:], gu[4][FFN:], x, K, tq.TQ_PACK_2BIT, workspace=ws, out=yu, reuse_rotated=True)
 
     try:
         ms = time_events(pair, 10, torch)
