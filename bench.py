@@ -800,7 +800,15 @@ def only_arm(args):
     W = (torch.randn(N, K, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
     fmt = tq.TQ_PACK_BASE3 if args.fmt == "base3" else tq.TQ_PACK_2BIT
     x = activations(torch, dev, K, M, seed=K + M)
-    if args.only == "quantize":
+    lay = None
+    if args.layout:
+        b, g, r = (int(v) for v in args.layout.split(","))
+        lay = tq.layout(b, g, bool(r))
+    if args.only == "quantize" and lay is not None:
+        c2, c3, s = tq.quantize_pack_layout(W, lay, tq.TQ_PACK_BOTH)
+        run = lambda: tq.quantize_pack_layout(W, lay, tq.TQ_PACK_BOTH)
+        work, unit = N * K * 2 + c2.numel() + c3.numel() + s.numel() * 2, "GB/s"
+    elif args.only == "quantize":
         run = lambda: tq.quantize_pack(W, tq.TQ_PACK_BOTH)
         work, unit = N * K * 2 + N * (K // 4) + N * tq.packed_ld(K, tq.TQ_PACK_BASE3) + N * (K // 128) * 2, "GB/s"
     elif args.only == "fwht":
@@ -815,6 +823,21 @@ def only_arm(args):
             y = torch.empty(M, N, device=dev)
             run = lambda: tq.gemv(codes, s, x, K, fmt, out=y)
             work, unit = packed_bytes(N, K, "base3" if fmt == tq.TQ_PACK_BASE3 else "2bit"), "GB/s"
+        elif args.only == "gemm_chain":
+            # layer a (N x K) writes layer b's x' in its epilogue; b (N x N) skips its pre-pass
+            Wb = (torch.randn(N, N, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+            cb, _, sb = tq.quantize_pack(Wb, tq.TQ_PACK_2BIT)
+            del Wb
+            ws1 = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+            ws2 = torch.empty(tq.gemm_workspace_bytes(M, N), dtype=torch.uint8, device=dev)
+            ya, yb = torch.empty(M, N, device=dev), torch.empty(M, N, device=dev)
+            xz = torch.zeros(M, N, dtype=torch.bfloat16, device=dev)
+
+            def run():
+                tq.gemm_rotate_next(codes, s, x, K, ws2, workspace=ws1, out=ya)
+                tq.gemm(cb, sb, xz, N, workspace=ws2, out=yb, reuse_rotated=True)
+
+            work, unit = 2 * M * N * (K + N), "TFLOP/s"
         else:
             ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
             y = torch.empty(M, N, device=dev)
@@ -838,7 +861,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=4.0)
-    ap.add_argument("--only", choices=["gemv", "gemm", "quantize", "fwht"],
+    ap.add_argument("--layout", default="", help="block,group,residual for --only quantize (layout variants)")
+    ap.add_argument("--only", choices=["gemv", "gemm", "gemm_chain", "quantize", "fwht"],
                     help="time one operation on one shape (for profiler captures)")
     ap.add_argument("--shape", default="27648x5120", help="NxK for --only")
     ap.add_argument("--M", type=int, default=1, help="activation rows for --only")

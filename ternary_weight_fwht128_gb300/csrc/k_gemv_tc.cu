@@ -507,12 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   };
   const int64_t T = (p.N + 127) / 128;
   int64_t t0, t1;
-  if (T * p.clusters <= 0xffffffffll) {
-    t0 = (uint32_t)(T * cluster) / (uint32_t)p.clusters;
-    t1 = (uint32_t)(T * (cluster + 1)) / (uint32_t)p.clusters;
-  } else {
-    t0 = T * cluster / p.clusters;
-    t1 = T * (cluster + 1) / p.clusters;
+  {
+    // the first T % clusters clusters take one tile more: CTAs of a GEMV
+    // launched behind another start in index order as SMs free up, so the
+    // last to start (on the SMs the previous GEMV held longest) get less work
+    const int64_t base = T / p.clusters, extra = T - base * p.clusters;
+    t0 = cluster * base + (cluster < extra ? cluster : extra);
+    t1 = t0 + base + (cluster < extra ? 1 : 0);
   }
   const int ntiles = (int)(t1 - t0);
   const int S = ntiles * nch;  // stages (ring loads) of this CTA
