@@ -69,7 +69,7 @@ typedef enum {
   TQ_ERR_ALIGN = 3,       /* pointer or row not 16-byte aligned            */
   TQ_ERR_UNSUPPORTED = 4, /* dtype/format combination not provided         */
   TQ_ERR_CUDA = 5,        /* a CUDA launch or query failed                 */
-  TQ_ERR_RANGE = 6,       /* fp16 overflow recorded by tq_gemm             */
+  TQ_ERR_RANGE = 6,       /* activations out of the representable range   */
   TQ_ERR_TIMEOUT = 7      /* a kernel gave up a bounded wait (see below)   */
 } tq_status;
 
@@ -348,7 +348,11 @@ TQ_API tq_status tq_gemm_layout(const uint8_t *codes, int64_t ldc, int fmt, cons
  * and exits, so the CUDA context stays usable; its outputs are then not
  * meaningful.  This call synchronises the device, returns TQ_ERR_TIMEOUT if
  * any kernel recorded such an event since the previous call (and clears the
- * record), else TQ_OK; TQ_ERR_CUDA if the device could not be queried. */
+ * record); else TQ_ERR_RANGE if a tensor-memory GEMV met a group of rotated
+ * activations outside what its fp8 pieces represent (max |x'| of the group
+ * at least 2^108 or infinite, or positive but below 2^-93: those groups'
+ * products saturate or flush, and y is not meaningful); else TQ_OK;
+ * TQ_ERR_CUDA if the device could not be queried. */
 TQ_API tq_status tq_device_fault(void);
 
 #ifdef __cplusplus

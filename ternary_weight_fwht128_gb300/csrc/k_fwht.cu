@@ -169,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_fwht128(const void* __restrict_
       if constexpr (XT == TQ_F32) raw[u].w[1] = raw[u].w[0];
       if (ok[u]) {
         const unsigned char* src = static_cast<const unsigned char*>(x) + (xo + 8 * p) * esize;
-        raw[u].w[0] = ldg_nc_u4(src);
-        if constexpr (XT == TQ_F32) raw[u].w[1] = ldg_nc_u4(src + 16);
+        raw[u].w[0] = ld_in_u4(src);
+        if constexpr (XT == TQ_F32) raw[u].w[1] = ld_in_u4(src + 16);
       }
       g += dg;
       r += dr;

@@ -316,11 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // codes and scales run two stages ahead of the decode, so their latency
     // hides behind two stages of MMA
     auto ld_codes = [&](int st) {
-      return (in_tile && st < nk) ? ldg_nc_u4(crow + (s0 + st) * (BK / 4)) : make_uint4(0, 0, 0, 0);
+      return (in_tile && st < nk) ? ld_in_u4(crow + (s0 + st) * (BK / 4)) : make_uint4(0, 0, 0, 0);
     };
     auto ld_scale = [&](int st) {
       const int lgs = EXT ? p.lgs : 0;
-      return (row_ok && st < nk) ? __ldg(srow + (((s0 + st) * BK) >> (7 + lgs))) : (uint16_t)0;
+      return (row_ok && st < nk) ? ld_in_u16(srow + (((s0 + st) * BK) >> (7 + lgs))) : (uint16_t)0;
     };
     uint4 cur = ld_codes(0), nx1 = ld_codes(1);
     uint16_t scur = ld_scale(0), snx1 = ld_scale(1);

@@ -333,13 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
         const int64_t k0 = (cg0 + 2 * lp + q) * 128 + 32 * tq;
         const int64_t a8 = (k0 / 5) & ~(int64_t)7;
         const bool has = q == 0 || two, hi = a8 + 16 <= p.ldc;
-        d.w[4 * q + 0] = has ? ldg_stream_u2(pa + a8) : make_uint2(0, 0);
-        d.w[4 * q + 1] = (has && hi) ? ldg_stream_u2(pa + a8 + 8) : make_uint2(0, 0);
-        d.w[4 * q + 2] = has ? ldg_stream_u2(pb + a8) : make_uint2(0, 0);
-        d.w[4 * q + 3] = (has && hi) ? ldg_stream_u2(pb + a8 + 8) : make_uint2(0, 0);
+        d.w[4 * q + 0] = has ? ld_in_u2(pa + a8) : make_uint2(0, 0);
+        d.w[4 * q + 1] = (has && hi) ? ld_in_u2(pa + a8 + 8) : make_uint2(0, 0);
+        d.w[4 * q + 2] = has ? ld_in_u2(pb + a8) : make_uint2(0, 0);
+        d.w[4 * q + 3] = (has && hi) ? ld_in_u2(pb + a8 + 8) : make_uint2(0, 0);
       }
-      d.sa = (uint32_t)__ldg(qa + 2 * lp) | (two ? ((uint32_t)__ldg(qa + 2 * lp + 1) << 16) : 0u);
-      d.sb = (uint32_t)__ldg(qb + 2 * lp) | (two ? ((uint32_t)__ldg(qb + 2 * lp + 1) << 16) : 0u);
+      d.sa = (uint32_t)ld_in_u16(qa + 2 * lp) | (two ? ((uint32_t)ld_in_u16(qa + 2 * lp + 1) << 16) : 0u);
+      d.sb = (uint32_t)ld_in_u16(qb + 2 * lp) | (two ? ((uint32_t)ld_in_u16(qb + 2 * lp + 1) << 16) : 0u);
       if (++lp == npairs) {
         lp = 0;
         ++lt;
@@ -349,17 +349,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
     auto load_unit = [&](Unit& d) {
       const bool two = 2 * lp + 1 < ng;  // the unit's second group exists
       const int o = lp * 64;
-      d.a0 = ldg_stream_u2(pa + o);
-      d.b0 = ldg_stream_u2(pb + o);
+      d.a0 = ld_in_u2(pa + o);
+      d.b0 = ld_in_u2(pb + o);
       if (two) {
-        d.a1 = ldg_stream_u2(pa + o + 32);
-        d.b1 = ldg_stream_u2(pb + o + 32);
+        d.a1 = ld_in_u2(pa + o + 32);
+        d.b1 = ld_in_u2(pb + o + 32);
       } else {
         d.a1 = make_uint2(0, 0);
         d.b1 = d.a1;
       }
-      d.sa = (uint32_t)__ldg(qa + 2 * lp) | (two ? ((uint32_t)__ldg(qa + 2 * lp + 1) << 16) : 0u);
-      d.sb = (uint32_t)__ldg(qb + 2 * lp) | (two ? ((uint32_t)__ldg(qb + 2 * lp + 1) << 16) : 0u);
+      d.sa = (uint32_t)ld_in_u16(qa + 2 * lp) | (two ? ((uint32_t)ld_in_u16(qa + 2 * lp + 1) << 16) : 0u);
+      d.sb = (uint32_t)ld_in_u16(qb + 2 * lp) | (two ? ((uint32_t)ld_in_u16(qb + 2 * lp + 1) << 16) : 0u);
       if (++lp == npairs) {
         lp = 0;
         ++lt;
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv(const Params p) {
     for (int b = warp; b < ng * M; b += kWarps) {
       const int m = b / ng, gl = b - m * ng;
       float v[4];
-      bf16x4_to_f32(ldg_nc_u2(p.x + (int64_t)m * p.ldx + (cg0 + gl) * 128 + 4 * lane), v);
+      bf16x4_to_f32(ld_in_u2(p.x + (int64_t)m * p.ldx + (cg0 + gl) * 128 + 4 * lane), v);
       fwht128_lane(v, lane);
       float hsum = 0.0f;
 #pragma unroll

@@ -86,7 +86,7 @@
 
 namespace tq {
 
-__device__ unsigned int g_gemv_fault;  // bit 1: a bounded wait ran out
+__device__ unsigned int g_gemv_fault;  // bit 1: a bounded wait ran out; bit 2: activations out of range
 
 namespace {
 
@@ -105,6 +105,7 @@ constexpr int kZeroBytes = 288;               // B rows 8..15 of the 8-row layou
 constexpr int kTmemCols = 512;                // one CTA per SM
 constexpr int kAbufMax = 3;
 constexpr uint32_t kFaultTimeout = 2u;
+constexpr uint32_t kFaultRange = 4u;  // a group's rotated activations outside what the e4m3 pieces represent
 
 // Per code format: groups per stage (kGS), weight (A) buffers in tensor
 // memory (kAbuf, one stage each), A columns per stage (kACols) and K steps
@@ -348,11 +349,6 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint
                : "memory");
 }
 
-__device__ __forceinline__ uint16_t ldg_nc_u16(const uint16_t* p) {
-  uint16_t r;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
-  return r;
-}
 
 // FWHT-128 with lane 4i + j holding elements 16i + j + 4b (b = 0..3): stages
 // h = 1, 2 pair lanes l ^ 1, l ^ 2; h = 4, 8 stay in the lane (b ^ 1, b ^ 2);
@@ -404,7 +400,7 @@ __device__ __forceinline__ void rotate_group(float v[4], int lane, int blk, cons
   } else {
     float o[4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) o[b] = __uint_as_float((uint32_t)ldg_nc_u16(partner + 4 * b) << 16);
+    for (int b = 0; b < 4; ++b) o[b] = __uint_as_float((uint32_t)ld_in_u16(partner + 4 * b) << 16);
     fwht128_strided_stages(v, lane);
     fwht128_strided_stages(o, lane);
 #pragma unroll
@@ -603,19 +599,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       const uint16_t* xrow = p.x + m * p.ldx + 16 * i8 + jc;
       const uint16_t* xg = xrow + xc * 128;
 #pragma unroll
-      for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ldg_nc_u16(xg + 4 * b) << 16);
+      for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ld_in_u16(xg + 4 * b) << 16);
       if (rot) rotate_group(v, lane, p.blk, xrow + (xc ^ 1) * 128, (xc & 1) != 0);
     } else {
       const uint16_t* xg = p.x + m * p.ldx + (g0 + gl) * 128 + 16 * i8 + jc;
 #pragma unroll
-      for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ldg_nc_u16(xg + 4 * b) << 16);
+      for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ld_in_u16(xg + 4 * b) << 16);
       fwht128_strided(v, lane);
     }
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    // the group's max |x'| in one warp reduction: non-negative fp32 values
+    // order like their bit patterns
+    const float amax = __uint_as_float(__reduce_max_sync(
+        kFull, __float_as_uint(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))))));
     int E = amax > 0.0f ? 134 - (int)((__float_as_uint(amax) >> 23) & 0xffu) : 0;  // max |x' 2^E| in [128, 256)
-    E = E < -100 ? -100 : (E > 100 ? 100 : E);
+    // |x'| >= 2^108 (or infinite) or 0 < max |x'| < 2^-93 in a group: the
+    // pieces under the clamped scale would saturate or flush -- recorded
+    if (E < -100 || E > 100) {
+      if (lane == 0) atomicOr(&g_gemv_fault, kFaultRange);
+      E = E < -100 ? -100 : 100;
+    }
     const float up = __uint_as_float((uint32_t)(127 + E) << 23);
     const float pw = __uint_as_float((uint32_t)(127 + 9 - E) << 23);
     // 2-bit: odd classes j meet the 4c weights, so their values are stored
@@ -711,8 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       uint4 c[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) c[q] = ok ? lds_u4(ring_u32 + slot * kSlotBytes + off[q]) : make_uint4(0, 0, 0, 0);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->empty[slot]);
+      // The slot is released only after the tensor-memory stores below have
+      // consumed c: the refill is a TMA (async-proxy) write, which is not
+      // ordered after shared-memory loads whose values have not returned yet,
+      // so an earlier release let the next stage's codes reach some lanes.
       if (s >= kAbuf) ok = wait_or_abort(&ctl->a_free[ab][team], ((s - kAbuf) / kAPeriod) & 1, ctl) && ok;
       if (!__all_sync(kFull, ok)) break;  // the tensor-memory stores below are warp-collective
       // order the stores below after the MMAs that read this buffer (observed
@@ -752,7 +756,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->a_full[ab][team]);
+      if (lane == 0) {
+        mbar_arrive(&ctl->empty[slot]);
+        mbar_arrive(&ctl->a_full[ab][team]);
+      }
       slot += 2;
       if (slot >= kRing) { slot -= kRing; ++use; }
     }
@@ -838,12 +845,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
         const int64_t gc = g0 + kGS * c;  // a scale per 2^lgs groups of 128
 #pragma unroll
         for (int h = 0; h < kGS; ++h)
-          if (kGS * c + h < ng) sc[h] = __ldg(q + ((gc + h) >> p.lgs));
+          if (kGS * c + h < ng) sc[h] = ld_in_u16(q + ((gc + h) >> p.lgs));
       } else {
         const uint16_t* q = p.scales + n * p.lds + g0 + kGS * c;
 #pragma unroll
         for (int h = 0; h < kGS; ++h)
-          if (kGS * c + h < ng) sc[h] = __ldg(q + h);
+          if (kGS * c + h < ng) sc[h] = ld_in_u16(q + h);
       }
     };
     // The scales are loaded kAhead stages before they are used (a DRAM miss
@@ -961,6 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   bool ok = true;
   if (p.kcl > 1) {
     ok = mbar_wait(&ctl->red_bar, 0, ctl->wait_ns);
+    if (ok) mbar_acquire_cluster(&ctl->red_bar, 0);
     if (!ok && threadIdx.x == 0) atomicOr(&g_gemv_fault, kFaultTimeout);
   }
   if (ok && !ctl->abort) {

@@ -393,7 +393,8 @@ tq_status tq_gemm_layout(const uint8_t* codes, int64_t ldc, int fmt, const uint1
 tq_status tq_device_fault(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
   const unsigned int f = take_fault_gemv() | take_fault_quant() | take_fault_noalloc();
-  return f ? TQ_ERR_TIMEOUT : TQ_OK;
+  if (f & 2u) return TQ_ERR_TIMEOUT;
+  return (f & 4u) ? TQ_ERR_RANGE : TQ_OK;
 }
 
 }  // extern "C"

@@ -140,28 +140,18 @@ __device__ __forceinline__ void bf16x4_to_f32(uint2 w, float v[4]) {
   v[3] = __uint_as_float(w.y & 0xffff0000u);
 }
 
-__device__ __forceinline__ uint2 ldg_nc_u2(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ uint4 ldg_nc_u4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-// Streaming load that is not kept in L1 (packed weights are read once).
-__device__ __forceinline__ uint2 ldg_stream_u2(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-               : "=r"(r.x), "=r"(r.y)
-               : "l"(p));
-  return r;
-}
+// Loads of kernel inputs.  Every kernel here may start before the kernel that
+// precedes it on the stream has finished (programmatic dependent launch) and
+// waits for it with griddepcontrol.wait before it reads anything that kernel
+// may have written.  Ordinary loads after that wait see those writes.  The
+// non-coherent path (ld.global.nc) is not used: it assumes the data is
+// read-only for the whole lifetime of the kernel, which a kernel that starts
+// early cannot promise.  These are plain C++ loads rather than volatile inline
+// assembly, so that the compiler may batch and schedule them, yet it cannot
+// move them above the wait (an asm statement with a memory clobber).
+__device__ __forceinline__ uint16_t ld_in_u16(const void* p) { return *reinterpret_cast<const uint16_t*>(p); }
+__device__ __forceinline__ uint2 ld_in_u2(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ uint4 ld_in_u4(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -263,6 +253,18 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t pari
     }
   }
   return true;
+}
+
+// A completed phase observed again with cluster-scope acquire: data that other
+// CTAs of the cluster wrote with st.async (signalling this barrier) is then
+// ordered before this thread's later reads.  Only for a phase already seen
+// complete (it returns at once).
+__device__ __forceinline__ void mbar_acquire_cluster(uint64_t* bar, uint32_t parity) {
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%0], %1;\n}\n" ::"r"(
+          smem_u32(bar)),
+      "r"(parity)
+      : "memory");
 }
 
 // Bounded-wait limit of a launch that tests the failure path (a stalled copy

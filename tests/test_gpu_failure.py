@@ -86,3 +86,23 @@ def test_gemm_stall_reports_timeout_then_recovers(N, K, M):
     y2 = tq.gemm(c2, s, x, K, workspace=ws)
     tq.gemm_check_range(ws)
     assert torch.equal(y2, ref)
+
+
+@pytest.mark.parametrize("scale_exp", [110, -110])
+def test_gemv_reports_activations_out_of_range(scale_exp):
+    """A group of x whose rotation lies beyond what the e4m3 pieces represent
+    (|x'| >= 2^108, or a positive max below 2^-93) is recorded, and
+    tq_device_fault reports TQ_ERR_RANGE once; the next clean call is clean."""
+    N, K, M = 27648, 5120, 1
+    assert tq.gemv_path(N, K, M) == tq.TQ_GEMV_TENSOR_MEMORY
+    W = synth.weights(N, K, 81, dtype="bf16")
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    xb = synth.activations(M, K, 82)
+    x = to_dev_bf16(xb).float()
+    x[:, 256:384] *= 2.0 ** scale_exp
+    x = x.to(torch.bfloat16)
+    tq.device_fault()
+    tq.gemv(c2, s, x, K)
+    assert tq.lib().tq_device_fault() == tq.TQ_ERR_RANGE
+    tq.gemv(c2, s, to_dev_bf16(xb), K)
+    assert tq.lib().tq_device_fault() == tq.TQ_OK
