@@ -19,6 +19,11 @@ Parity status of each function (what pins it, see ``tests/test_oracle.py``):
                       byte range, bit accounting
   gemv_f64            pinned: dense dequantised fp64 matmul with a scipy-built
                       block rotation, rotation invariance, delta activations
+  Sparse24Oracle      2:4 pattern (two largest |w'| per quad), absmean over the
+                      kept 64, joint 6-bit codes: pinned by a brute-force pattern
+                      search, every one of the 54 codes by hand, closed-form
+                      scales, order-sensitive sums over 64, the bit budget, and
+                      a dense fp64 GEMV of the expanded trits
   LayoutOracle        block sizes 64/128/256, groups 128/256, residual pass:
                       pinned by scipy's H_n, the n = 128 functions above (bit
                       for bit), exact normalisation constants, order-sensitive
@@ -104,6 +109,14 @@ class Oracle:
                                                ctypes.c_int, _vp, _vp]
         L.tqo_gemv_layout_f64.argtypes = [_vp, _vp, _i64, _vp, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           _vp]
+        L.tqo_quantize_group_24.restype = ctypes.c_uint16
+        L.tqo_quantize_group_24.argtypes = [_vp, _vp, _vp]
+        L.tqo_quantize_rows_24.argtypes = [_vp, ctypes.c_int, _i64, _i64, _vp, _i64, _vp, _vp, _vp]
+        L.tqo_ld24.restype = _i64
+        L.tqo_ld24.argtypes = [_i64]
+        L.tqo_pack24.argtypes = [_vp, _vp, _i64, _i64, _vp, _i64]
+        L.tqo_unpack24.restype = _i64
+        L.tqo_unpack24.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp]
 
     # -- Hadamard -------------------------------------------------------
     def hadamard_entry(self, i: int, j: int) -> int:
@@ -289,6 +302,70 @@ class LayoutOracle:
         y = np.zeros((M, R), dtype=np.float64)
         self._L.tqo_gemv_layout_f64(_p(T), _p(S), K, _p(x), M, R, block, group, 1 if residual else 0, _p(y))
         return y
+
+
+class Sparse24Oracle:
+    """The 2:4-sparse ternary format of the oracle (tqo_quantize_group_24 and
+    the functions after it in tq_oracle.c), on a loaded Oracle."""
+
+    def __init__(self, orc: Oracle):
+        self._orc = orc
+        self._L = orc._L
+
+    def quantize_group(self, wrot: np.ndarray) -> tuple[int, np.ndarray, np.ndarray]:
+        """(fp16 scale bits, t int8[128], keep uint8[128]) of one rotated group."""
+        w = np.ascontiguousarray(wrot, dtype=np.float32)
+        assert w.shape == (128,)
+        t = np.zeros(128, dtype=np.int8)
+        keep = np.zeros(128, dtype=np.uint8)
+        s = self._L.tqo_quantize_group_24(_p(w), _p(t), _p(keep))
+        return int(s), t, keep
+
+    def quantize(self, W: np.ndarray, rows: np.ndarray | None = None
+                 ) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+        """(T int8 [R][K], KEEP uint8 [R][K], S uint16 [R][K/128]) of W (fp32 or bf16 bits)."""
+        W = np.ascontiguousarray(W)
+        if W.dtype not in (np.float32, np.uint16):
+            raise TypeError("W must be float32 or uint16 (bf16 bits)")
+        wt = 0 if W.dtype == np.float32 else 1
+        N, K = W.shape
+        if K % 128:
+            raise ValueError("K must be a multiple of 128")
+        rp = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        R = N if rp is None else rp.shape[0]
+        T = np.zeros((R, K), dtype=np.int8)
+        KEEP = np.zeros((R, K), dtype=np.uint8)
+        S = np.zeros((R, K // 128), dtype=np.uint16)
+        self._L.tqo_quantize_rows_24(_p(W), wt, K, K, _p(rp), R, _p(T), _p(KEEP), _p(S))
+        return T, KEEP, S
+
+    def ld(self, K: int) -> int:
+        return int(self._L.tqo_ld24(K))
+
+    def pack(self, T: np.ndarray, KEEP: np.ndarray, ld: int | None = None) -> np.ndarray:
+        T = np.ascontiguousarray(T, dtype=np.int8)
+        KEEP = np.ascontiguousarray(KEEP, dtype=np.uint8)
+        N, K = T.shape
+        ld = self.ld(K) if ld is None else ld
+        codes = np.zeros((N, ld), dtype=np.uint8)
+        self._L.tqo_pack24(_p(T), _p(KEEP), N, K, _p(codes), ld)
+        return codes
+
+    def unpack(self, codes: np.ndarray, K: int) -> tuple[np.ndarray, np.ndarray, int]:
+        """(T, KEEP, number of invalid codes) of a packed tensor."""
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        N, ld = codes.shape
+        T = np.zeros((N, K), dtype=np.int8)
+        KEEP = np.zeros((N, K), dtype=np.uint8)
+        bad = self._L.tqo_unpack24(_p(codes), ld, N, K, _p(T), _p(KEEP))
+        return T, KEEP, int(bad)
+
+    def gemv(self, codes: np.ndarray, S: np.ndarray, x: np.ndarray, K: int) -> np.ndarray:
+        """fp64 y [M][N] of the packed weights: the dense GEMV of the unpacked trits."""
+        T, _, bad = self.unpack(codes, K)
+        if bad:
+            raise ValueError("invalid 2:4 codes")
+        return self._orc.gemv(T, S, x)
 
 
 def load(path: str | None = None) -> Oracle:

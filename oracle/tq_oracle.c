@@ -403,3 +403,107 @@ void tqo_gemv_layout_f64(const int8_t *T, const uint16_t *S, int64_t K, const fl
   free(xr);
   free(xrr);
 }
+
+/* ------------------------------------------------------------ 2:4 sparse */
+
+/* kept positions (i0, i1) of pattern p, in the order (0,1) (0,2) (0,3)
+ * (1,2) (1,3) (2,3) */
+static const int kPat24[6][2] = {{0, 1}, {0, 2}, {0, 3}, {1, 2}, {1, 3}, {2, 3}};
+
+/* [mhpq] sec. 1.2 (structured 2:4 sparsity, then ternarisation of what is
+ * kept) with the absmean rule of sec. 1.1 on the kept weights. */
+uint16_t tqo_quantize_group_24(const float *wrot, int8_t *t, uint8_t *keep) {
+  float kept[64];
+  int nk = 0;
+  for (int j = 0; j < 32; ++j) {
+    /* the two largest magnitudes of the quad; a tie goes to the lower index:
+     * position i is kept when fewer than two others beat it */
+    for (int i = 0; i < 4; ++i) {
+      float a = fabsf(wrot[4 * j + i]);
+      int beaten = 0;
+      for (int o = 0; o < 4; ++o) {
+        if (o == i) continue;
+        float b = fabsf(wrot[4 * j + o]);
+        if (b > a || (b == a && o < i)) ++beaten;
+      }
+      keep[4 * j + i] = (uint8_t)(beaten < 2);
+      if (beaten < 2) kept[nk++] = fabsf(wrot[4 * j + i]);
+    }
+  }
+  /* nk == 64: each quad keeps exactly two (a strict total order) */
+  for (int h = 32; h >= 1; h /= 2)
+    for (int i = 0; i < h; ++i) kept[i] = kept[i] + kept[i + h];
+  float mean = kept[0] * 0.015625f; /* * 2^-6 */
+  uint16_t sbits = tqo_f32_to_f16(mean);
+  float sc = tqo_f16_to_f32(sbits);
+  for (int i = 0; i < 128; ++i) {
+    if (!keep[i] || sc == 0.0f) { t[i] = 0; continue; }
+    float q = wrot[i] / sc;
+    float r = nearbyintf(q);
+    t[i] = (int8_t)(r > 1.0f ? 1 : (r < -1.0f ? -1 : (int)r));
+  }
+  return sbits;
+}
+
+void tqo_quantize_rows_24(const void *W, int wt, int64_t K, int64_t ldw, const int64_t *rows,
+                          int64_t nrows, int8_t *T, uint8_t *KEEP, uint16_t *S) {
+  int64_t G = K / 128;
+  float grp[128], rot[128];
+  for (int64_t r = 0; r < nrows; ++r) {
+    int64_t n = rows ? rows[r] : r;
+    for (int64_t g = 0; g < G; ++g) {
+      load_group(W, wt, n, ldw, g * 128, grp);
+      tqo_fwht128_f32(grp, rot);
+      S[r * G + g] = tqo_quantize_group_24(rot, T + r * K + g * 128, KEEP + r * K + g * 128);
+    }
+  }
+}
+
+int64_t tqo_ld24(int64_t K) { return K / 128 * 24; }
+
+void tqo_pack24(const int8_t *T, const uint8_t *KEEP, int64_t N, int64_t K, uint8_t *codes,
+                int64_t ld) {
+  int64_t G = K / 128;
+  for (int64_t n = 0; n < N; ++n) {
+    uint8_t *row = codes + n * ld;
+    for (int64_t b = 0; b < ld; ++b) row[b] = 0;
+    for (int64_t g = 0; g < G; ++g) {
+      uint8_t *grp = row + 24 * g;
+      for (int j = 0; j < 32; ++j) {
+        const int8_t *t = T + n * K + 128 * g + 4 * j;
+        const uint8_t *kp = KEEP + n * K + 128 * g + 4 * j;
+        int p = -1;
+        for (int q = 0; q < 6; ++q)
+          if (kp[kPat24[q][0]] && kp[kPat24[q][1]] &&
+              kp[0] + kp[1] + kp[2] + kp[3] == 2)
+            p = q;
+        if (p < 0) p = 0; /* not a 2:4 quad: cannot be stored (callers pass valid masks) */
+        unsigned c = (unsigned)(9 * p + 3 * (t[kPat24[p][0]] + 1) + (t[kPat24[p][1]] + 1));
+        grp[j / 2] = (uint8_t)(grp[j / 2] | ((c & 15u) << (4 * (j % 2))));
+        grp[16 + j / 4] = (uint8_t)(grp[16 + j / 4] | ((c >> 4) << (2 * (j % 4))));
+      }
+    }
+  }
+}
+
+int64_t tqo_unpack24(const uint8_t *codes, int64_t ld, int64_t N, int64_t K, int8_t *T,
+                     uint8_t *KEEP) {
+  int64_t G = K / 128, bad = 0;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t g = 0; g < G; ++g) {
+      const uint8_t *grp = codes + n * ld + 24 * g;
+      for (int j = 0; j < 32; ++j) {
+        unsigned c = ((grp[j / 2] >> (4 * (j % 2))) & 15u) | (((grp[16 + j / 4] >> (2 * (j % 4))) & 3u) << 4);
+        int8_t *t = T + n * K + 128 * g + 4 * j;
+        uint8_t *kp = KEEP + n * K + 128 * g + 4 * j;
+        for (int i = 0; i < 4; ++i) { t[i] = 0; kp[i] = 0; }
+        if (c >= 54) { ++bad; continue; }
+        int p = (int)(c / 9), v = (int)(c % 9);
+        kp[kPat24[p][0]] = 1;
+        kp[kPat24[p][1]] = 1;
+        t[kPat24[p][0]] = (int8_t)(v / 3 - 1);
+        t[kPat24[p][1]] = (int8_t)(v % 3 - 1);
+      }
+    }
+  return bad;
+}

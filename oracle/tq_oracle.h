@@ -106,6 +106,47 @@ void tqo_quantize_layout_rows(const void *W, int wt, int64_t K, int64_t ldw, con
 void tqo_gemv_layout_f64(const int8_t *T, const uint16_t *S, int64_t K, const float *x, int64_t M,
                          int64_t nrows, int block, int group, int residual, double *y);
 
+/* ---- 2:4-sparse ternary weights ([mhpq] sec. 1.2: structured 2:4
+ * sparsity -- two of every four weights kept, at regular positions -- and
+ * the kept weights ternarised).
+ *
+ * Readings where the page leaves a step open (the plainest ones):
+ *   - the pattern is chosen on the rotated weights w' (the matrix the
+ *     ternary codes multiply), per quad of four consecutive k of a group;
+ *   - the kept pair of a quad is its two largest |w'|, a tie going to the
+ *     lower index;
+ *   - "ternarise the remaining weights" is the absmean rule of [mhpq]
+ *     sec. 1.1 applied to the 64 kept weights of the group: the scale is
+ *     fp16_RN(mean |w'| over them), their sum taken by the halving tree over
+ *     the kept values in k order (s[i] += s[i + h], h = 32 .. 1, fp32), then
+ *     t = clamp(rint(w' / scale), -1, 1) as in tqo_quantize_group; a kept
+ *     weight may round to 0; a pruned weight is 0.
+ *
+ * Storage (one tensor holding mask and trits together, as the page
+ * describes, 24 bytes per group of 128):  quad j (k = 4j .. 4j + 3) of a
+ * group has pattern p (its kept positions i0 < i1 in the order (0,1),
+ * (0,2), (0,3), (1,2), (1,3), (2,3)) and code c = 9 p + 3 (t[i0] + 1) +
+ * (t[i1] + 1), 0 <= c < 54.  The low four bits of c are nibble (j % 2) of
+ * byte j / 2 of the group (bytes 0..15), its two high bits are bits
+ * 2 (j % 4) .. of byte 16 + j / 4 (bytes 16..23).  A row holds its groups in
+ * order: ld = 24 K / 128 bytes.  1.5 bits per weight plus 0.125 of scale.
+ *
+ * tqo_quantize_group_24: one rotated group -> dense t[128] (pruned = 0),
+ * keep[128] (1 at kept positions), returns the fp16 scale bits.
+ * tqo_quantize_rows_24: rows of W (fp32, wt = 0, or bf16 bits, wt = 1),
+ * FWHT-128 per group (tqo_fwht128_f32), then the above; T, KEEP [nrows][K],
+ * S [nrows][K/128].  tqo_pack24 / tqo_unpack24 convert (T, KEEP) to and
+ * from the codes; tqo_unpack24 returns the number of codes >= 54 seen
+ * (0 for a valid tensor; such quads decode as all zero). */
+uint16_t tqo_quantize_group_24(const float *wrot, int8_t *t, uint8_t *keep);
+void tqo_quantize_rows_24(const void *W, int wt, int64_t K, int64_t ldw, const int64_t *rows,
+                          int64_t nrows, int8_t *T, uint8_t *KEEP, uint16_t *S);
+int64_t tqo_ld24(int64_t K);
+void tqo_pack24(const int8_t *T, const uint8_t *KEEP, int64_t N, int64_t K, uint8_t *codes,
+                int64_t ld);
+int64_t tqo_unpack24(const uint8_t *codes, int64_t ld, int64_t N, int64_t K, int8_t *T,
+                     uint8_t *KEEP);
+
 #ifdef __cplusplus
 }
 #endif

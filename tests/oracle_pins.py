@@ -710,6 +710,278 @@ def check_group256_bit_accounting(orc):
     assert (T.shape[1] * 2 + S.shape[1] * 16) / 512 == 4.25
 
 
+# ------------------------------------------------------- 2:4 sparse format
+# [mhpq] sec. 1.2: two of every four weights kept at regular positions, the
+# kept ones ternarised.  Readings (documented in tq_oracle.h): the pattern is
+# chosen on the rotated weights, per quad of consecutive k; the kept pair is
+# the two largest |w'| (ties to the lower index); the absmean scale is taken
+# over the 64 kept weights (halving tree over them in k order, times 2^-6).
+
+_PAT24 = [(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)]
+
+
+def _sp(orc):
+    import oracle
+    return oracle.Sparse24Oracle(orc)
+
+
+def _keep_bruteforce(w: np.ndarray) -> np.ndarray:
+    """Per quad: order the four positions by (-|w|, index) and keep the first two."""
+    keep = np.zeros(w.size, dtype=np.uint8)
+    for j in range(w.size // 4):
+        q = np.abs(w[4 * j:4 * j + 4].astype(np.float64))
+        order = sorted(range(4), key=lambda i: (-q[i], i))
+        keep[4 * j + order[0]] = keep[4 * j + order[1]] = 1
+    return keep
+
+
+def check_sparse24_pattern_bruteforce(orc):
+    """Exactly two kept per quad, and they are the two largest magnitudes
+    (ties to the lower index), on random groups and on integer-valued groups
+    with many ties (including all-equal quads and signed ties)."""
+    sp = _sp(orc)
+    rng = np.random.default_rng(61)
+    for it in range(120):
+        if it % 3 == 0:
+            w = rng.integers(-2, 3, size=128).astype(np.float32)
+        elif it % 3 == 1:
+            w = (rng.standard_normal(128) * 0.02).astype(np.float32)
+        else:
+            w = rng.choice(np.array([-1.5, -0.5, 0.5, 1.5], dtype=np.float32), size=128)
+        _, t, keep = sp.quantize_group(w)
+        assert np.array_equal(keep, _keep_bruteforce(w)), it
+        assert np.all(keep.reshape(32, 4).sum(1) == 2)
+        assert not np.any(t[keep == 0]), "a pruned weight kept a trit"
+
+
+def _code24(p: int, a: int, b: int) -> int:
+    return 9 * p + 3 * (a + 1) + (b + 1)
+
+
+def check_sparse24_codes_by_hand(orc):
+    """Every one of the 54 (pattern, trit, trit) combinations, stored in quad
+    j of a group, packs to code 9 p + 3 (t0 + 1) + (t1 + 1) with its low
+    nibble in byte j // 2 (nibble j % 2) and its two high bits at bits
+    2 (j % 4) of byte 16 + j // 4; unpacking gives the quad back.  Two
+    whole-group byte images worked by hand: pattern (0,1) with trits (1, -1)
+    everywhere is code 6 (bytes 0x66 x 16, then 0x00 x 8); pattern (2,3) with
+    trits (1, 1) is code 53 = 0b110101 (bytes 0x55 x 16, then 0xFF x 8)."""
+    sp = _sp(orc)
+    combos = [(p, a, b) for p in range(6) for a in (-1, 0, 1) for b in (-1, 0, 1)]
+    assert len(combos) == 54
+    for start in range(0, 54, 32):
+        T = np.zeros((1, 128), dtype=np.int8)
+        KEEP = np.zeros((1, 128), dtype=np.uint8)
+        expect = np.zeros(24, dtype=np.uint8)
+        for j in range(32):
+            p, a, b = combos[(start + j) % 54]
+            i0, i1 = _PAT24[p]
+            KEEP[0, 4 * j + i0] = KEEP[0, 4 * j + i1] = 1
+            T[0, 4 * j + i0], T[0, 4 * j + i1] = a, b
+            c = _code24(p, a, b)
+            expect[j // 2] |= (c & 15) << (4 * (j % 2))
+            expect[16 + j // 4] |= (c >> 4) << (2 * (j % 4))
+        codes = sp.pack(T, KEEP)
+        assert np.array_equal(codes[0], expect), (start, codes[0], expect)
+        T2, K2, bad = sp.unpack(codes, 128)
+        assert bad == 0 and np.array_equal(T2, T) and np.array_equal(K2, KEEP)
+    for (p, a, b, img) in ((0, 1, -1, [0x66] * 16 + [0x00] * 8), (5, 1, 1, [0x55] * 16 + [0xFF] * 8)):
+        i0, i1 = _PAT24[p]
+        T = np.zeros((1, 128), dtype=np.int8)
+        KEEP = np.zeros((1, 128), dtype=np.uint8)
+        T[0, i0::4], T[0, i1::4] = a, b
+        KEEP[0, i0::4] = KEEP[0, i1::4] = 1
+        assert list(sp.pack(T, KEEP)[0]) == img
+    # codes 54..63 are not valid: they unpack to zeros and are counted
+    bad_codes = np.zeros((1, 24), dtype=np.uint8)
+    bad_codes[0, 0] = 0x0F  # quad 0: low nibble 15 ...
+    bad_codes[0, 16] = 0x03  # ... high bits 3: code 63
+    T, KEEP, bad = sp.unpack(bad_codes, 128)
+    assert bad == 1 and not T[0, :4].any() and not KEEP[0, :4].any()
+
+
+def check_sparse24_scale_closed_forms(orc):
+    """Kept magnitudes all equal to a (the pruned two of each quad smaller):
+    the mean over the kept is a, the scale fp16(a), each kept weight maps to
+    its sign.  An all-zero group keeps positions 0 and 1 of every quad (ties
+    to the lower index), with scale 0 and all trits 0.  A group whose pruned
+    weights are large would change a mean over all 128 but not this one."""
+    sp = _sp(orc)
+    rng = np.random.default_rng(62)
+    for a in (0.02, 1.0, 3.7e-3, 1234.5):
+        w = np.zeros(128, dtype=np.float32)
+        keep = np.zeros(128, dtype=np.uint8)
+        sign = np.where(rng.random(128) < 0.5, -1.0, 1.0).astype(np.float32)
+        for j in range(32):
+            i0, i1 = _PAT24[rng.integers(6)]
+            small = np.float32(a) * np.float32(rng.uniform(0.0, 0.9, size=4))
+            w[4 * j:4 * j + 4] = small * sign[4 * j:4 * j + 4]
+            for i in (i0, i1):
+                w[4 * j + i] = sign[4 * j + i] * np.float32(a)
+                keep[4 * j + i] = 1
+        s, t, kp = sp.quantize_group(w)
+        assert s == _fp16(np.float32(a)), (a, hex(s))
+        assert np.array_equal(kp, keep)
+        assert np.array_equal(t[keep == 1], sign[keep == 1].astype(np.int8))
+        assert not t[keep == 0].any()
+    s, t, kp = sp.quantize_group(np.zeros(128, dtype=np.float32))
+    assert s == 0 and not t.any()
+    assert np.array_equal(kp, np.tile(np.array([1, 1, 0, 0], dtype=np.uint8), 32))
+
+
+def _sum_halving_tree64_f32(a: np.ndarray) -> np.float32:
+    s = a.astype(np.float32).copy()
+    h = 32
+    while h >= 1:
+        s[:h] = s[:h] + s[h:2 * h]
+        h //= 2
+    return s[0]
+
+
+def check_sparse24_sum_order(orc):
+    """The kept weights' sum is the halving tree over the 64 kept values in
+    k order.  Groups are built with two large kept values and two tiny pruned
+    ones per quad, the kept magnitudes chosen so that their exact sum sits on
+    an fp16 rounding midpoint of 64 * scale; kept only where the halving tree
+    gives a different scale from a left-to-right sum and from a mean over all
+    128 weights."""
+    sp = _sp(orc)
+    found = 0
+    for seed in range(4000):
+        rng = np.random.default_rng(7000 + seed)
+        mag = np.exp(rng.uniform(-5.0, 3.0, size=64)).astype(np.float32)
+        others = sum(Fraction(float(v)) for v in mag[:-1])
+        guess = np.float16(float(others + Fraction(float(mag[-1]))) / 64)
+        lo = Fraction(float(guess))
+        hi = Fraction(float(np.nextafter(guess, np.float16(np.inf))))
+        need = 64 * (lo + hi) / 2 - others
+        if need <= 0:
+            continue
+        mag[-1] = np.float32(float(need))
+        if float(mag.min()) < 1e-3:
+            continue
+        w = np.zeros(128, dtype=np.float32)
+        pats = rng.integers(6, size=32)
+        tiny = np.float32(1e-6)
+        kept_pos = []
+        for j in range(32):
+            i0, i1 = _PAT24[pats[j]]
+            w[4 * j:4 * j + 4] = tiny
+            w[4 * j + i0] = mag[2 * j]
+            w[4 * j + i1] = -mag[2 * j + 1]
+            kept_pos += [4 * j + i0, 4 * j + i1]
+        kept = np.abs(w[kept_pos])  # k order
+        tree = _fp16(np.float32(_sum_halving_tree64_f32(kept) * np.float32(0.015625)))
+        seq = _fp16(np.float32(_sum_sequential_f32(kept) * np.float32(0.015625)))
+        all128 = _fp16(np.float32(_sum_halving_tree_f32(np.abs(w)) * np.float32(0.0078125)))
+        if tree == seq or tree == all128:
+            continue
+        s, _, kp = sp.quantize_group(w)
+        assert np.array_equal(np.nonzero(kp)[0], np.array(sorted(kept_pos)))
+        assert s == tree, (hex(s), hex(tree))
+        found += 1
+        if found == 4:
+            break
+    assert found == 4, "too few order-sensitive sparse groups"
+
+
+def check_sparse24_ties(orc):
+    """Round half to even on the kept weights, against the stored scale:
+    kept values at +-0.5 s, +-1.5 s, +-2.5 s and the fp32 neighbours of s/2
+    (each kept beside a filler, the other two of its quad zero), the fillers
+    making the mean of the 64 kept magnitudes s * 1.0003, which rounds to s
+    in fp16.  Expected trits as in check_quantize_ties."""
+    sp = _sp(orc)
+    for s0 in (1.0, 0.01171875, 6.103515625e-05):
+        s0 = np.float32(s0)
+        probes = np.array([0.5, -0.5, 1.5, -1.5, 2.5, -2.5], dtype=np.float32) * s0
+        up = np.nextafter(np.float32(0.5) * s0, np.float32(np.inf))
+        dn = np.nextafter(np.float32(0.5) * s0, np.float32(0))
+        probes = np.concatenate([probes, [up, dn, -up, -dn]]).astype(np.float32)
+        expect = np.array([0, 0, 1, -1, 1, -1, 1, 0, -1, 0], dtype=np.int8)
+        nfill = 64 - probes.size
+        fill_total = 64 * float(s0) * 1.0003 - float(np.sum(np.abs(probes.astype(np.float64))))
+        fill = np.float32(fill_total / nfill)  # (the other two of each quad are 0: both are kept)
+        w = np.zeros(128, dtype=np.float32)
+        for j in range(32):
+            if j < probes.size:
+                w[4 * j + 1], w[4 * j + 3] = probes[j], fill
+            else:
+                w[4 * j], w[4 * j + 2] = fill, -fill
+        s, t, keep = sp.quantize_group(w)
+        assert s == _fp16(s0), (s0, hex(s))
+        assert np.array_equal(t[1:4 * probes.size:4], expect), (s0, t[1:4 * probes.size:4])
+
+
+def check_sparse24_rule(orc):
+    """Kept weights: clamp(rint(w / s), -1, 1) with the stored fp16 scale
+    (numpy IEEE fp32 division and rint as the independent side); pruned: 0."""
+    sp = _sp(orc)
+    rng = np.random.default_rng(63)
+    for _ in range(150):
+        w = (rng.standard_normal(128) * rng.uniform(1e-4, 10)).astype(np.float32)
+        s, t, keep = sp.quantize_group(w)
+        sv = _fp16_val(s)
+        ref = np.clip(np.rint(w / sv), -1, 1).astype(np.int8)
+        ref[keep == 0] = 0
+        assert np.array_equal(t, ref)
+
+
+def check_sparse24_rows(orc):
+    """Whole rows (fp32 and bf16 input) are the FWHT-128 of each group
+    followed by the group rule: the rotation is checked against scipy's H
+    (fp32 rounding aside, every group's pattern and trits agree with the
+    group rule applied to the oracle's pinned fp32 rotation)."""
+    sp = _sp(orc)
+    rng = np.random.default_rng(64)
+    W = (rng.standard_normal((5, 384)) * 0.02).astype(np.float32)
+    T, KEEP, S = sp.quantize(W)
+    Wb = W.view(np.uint32)
+    Wb16 = ((Wb + 0x7FFF + ((Wb >> 16) & 1)) >> 16).astype(np.uint16)
+    Tb, KEEPb, Sb = sp.quantize(Wb16)
+    Wb32 = (Wb16.astype(np.uint32) << 16).view(np.float32)
+    for (Wx, Tx, Kx, Sx) in ((W, T, KEEP, S), (Wb32, Tb, KEEPb, Sb)):
+        for n in range(Wx.shape[0]):
+            for g in range(3):
+                rot = orc.fwht128_f32(Wx[n, 128 * g:128 * g + 128])
+                ref = _block_h(128) @ Wx[n, 128 * g:128 * g + 128].astype(np.float64)
+                assert np.max(np.abs(rot - ref)) <= 1e-5 * max(1.0, np.max(np.abs(ref)))
+                s, t, kp = sp.quantize_group(rot)
+                assert s == Sx[n, g] and np.array_equal(t, Tx[n, 128 * g:128 * g + 128])
+                assert np.array_equal(kp, Kx[n, 128 * g:128 * g + 128])
+
+
+def check_sparse24_gemv_dense(orc):
+    """y of the packed 2:4 weights equals the dense fp64 product of the
+    expanded, dequantised trits (t * s) with the block-rotated activations
+    (scipy H); the pruned weights contribute nothing."""
+    sp = _sp(orc)
+    rng = np.random.default_rng(65)
+    for (N, K, M) in ((9, 128, 1), (21, 384, 3)):
+        W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+        T, KEEP, S = sp.quantize(W)
+        codes = sp.pack(T, KEEP)
+        x = rng.standard_normal((M, K)).astype(np.float32)
+        ref = (x.astype(np.float64) @ _block_h(K).T) @ _dequant(T, S).T
+        got = sp.gemv(codes, S, x, K)
+        assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+        assert np.count_nonzero(T) <= N * K // 2
+
+
+def check_sparse24_bit_accounting(orc):
+    """24 bytes of codes per 128 weights (1.5 bit) plus a 2-byte scale
+    (0.125 bit): 1.625 bits per weight.  The entropy bound of the stored
+    information is log2(6 * 9) / 4 + 0.125 = 1.5637 bits: [mhpq] sec. 1.2's
+    "about 1.29" is below what a mask that can name all six patterns and two
+    free trits can reach (its accounting is not reproducible)."""
+    sp = _sp(orc)
+    for K in (128, 5120, 27648):
+        assert sp.ld(K) == 24 * K // 128
+        bits = (sp.ld(K) + 2 * (K // 128)) * 8 / K
+        assert bits == 1.625
+    assert abs(math.log2(54) / 4 + 0.125 - 1.5637) < 1e-4
+
+
 ALL_CHECKS = [
     check_hadamard_definitions,
     check_hadamard_orthogonal,
@@ -743,4 +1015,13 @@ ALL_CHECKS = [
     check_residual_reduces_error,
     check_layout_gemv_dense,
     check_group256_bit_accounting,
+    check_sparse24_pattern_bruteforce,
+    check_sparse24_codes_by_hand,
+    check_sparse24_scale_closed_forms,
+    check_sparse24_sum_order,
+    check_sparse24_ties,
+    check_sparse24_rule,
+    check_sparse24_rows,
+    check_sparse24_gemv_dense,
+    check_sparse24_bit_accounting,
 ]

@@ -57,17 +57,41 @@ MUTANTS = [
      "for (int i = 0; i < block; ++i) xrr[k0 + i] = xr[k0 + i];"),
     ("layout_group_stride", "const int8_t *t = T + q * Keff + pass * K + g * group;",
      "const int8_t *t = T + q * Keff + pass * K + g * 128;"),
+    # 2:4 sparse format
+    ("sp24_tie_to_higher", "if (b > a || (b == a && o < i)) ++beaten;", "if (b > a || (b == a && o > i)) ++beaten;"),
+    ("sp24_keep_three", "keep[4 * j + i] = (uint8_t)(beaten < 2);\n      if (beaten < 2)",
+     "keep[4 * j + i] = (uint8_t)(beaten < 3);\n      if (beaten < 3 && nk < 64)"),
+    ("sp24_signed_select", "float a = fabsf(wrot[4 * j + i]);", "float a = wrot[4 * j + i];"),
+    ("sp24_mean_over_128", "float mean = kept[0] * 0.015625f;", "float mean = kept[0] * 0.0078125f;"),
+    ("sp24_sequential_sum", "for (int h = 32; h >= 1; h /= 2)\n    for (int i = 0; i < h; ++i) kept[i] = kept[i] + kept[i + h];",
+     "for (int i = 1; i < 64; ++i) kept[0] = kept[0] + kept[i];"),
+    ("sp24_pruned_not_zeroed", "if (!keep[i] || sc == 0.0f) { t[i] = 0; continue; }", "if (sc == 0.0f) { t[i] = 0; continue; }"),
+    ("sp24_pattern_order", "{{0, 1}, {0, 2}, {0, 3}, {1, 2}, {1, 3}, {2, 3}}", "{{0, 1}, {0, 2}, {1, 2}, {0, 3}, {1, 3}, {2, 3}}"),
+    ("sp24_trit_order", "unsigned c = (unsigned)(9 * p + 3 * (t[kPat24[p][0]] + 1) + (t[kPat24[p][1]] + 1));",
+     "unsigned c = (unsigned)(9 * p + (t[kPat24[p][0]] + 1) + 3 * (t[kPat24[p][1]] + 1));"),
+    ("sp24_nibble_order", "grp[j / 2] = (uint8_t)(grp[j / 2] | ((c & 15u) << (4 * (j % 2))));",
+     "grp[j / 2] = (uint8_t)(grp[j / 2] | ((c & 15u) << (4 - 4 * (j % 2))));"),
+    ("sp24_high_plane_offset", "grp[16 + j / 4] = (uint8_t)(grp[16 + j / 4] | ((c >> 4) << (2 * (j % 4))));",
+     "grp[16 + j / 4] = (uint8_t)(grp[16 + j / 4] | ((c >> 4) << (2 * (3 - j % 4))));"),
+    ("sp24_unpack_digit_swap", "t[kPat24[p][0]] = (int8_t)(v / 3 - 1);\n        t[kPat24[p][1]] = (int8_t)(v % 3 - 1);",
+     "t[kPat24[p][0]] = (int8_t)(v % 3 - 1);\n        t[kPat24[p][1]] = (int8_t)(v / 3 - 1);"),
+    ("sp24_unpack_uncounted_bad", "if (c >= 54) { ++bad; continue; }", "if (c >= 54) { continue; }"),
 ]
 
 
 # sites that occur more than once: (name, text, replacement, which occurrence)
 # (the layout variants of the transform and the quantiser repeat lines of
-# the 128-point functions: occurrence 0 is the 128-point function, 1 the
-# variant)
+# the 128-point functions, and the 2:4 quantiser repeats the trit rule and the
+# row rotation: occurrence 0 is the 128-point function, 1 the layout variant,
+# 2 the 2:4 form)
 _REPEATED = ("butterfly_sign", "no_normalisation", "signed_sum", "divide_by_mean", "round_half_away", "no_clamp")
+_REPEATED3 = ("divide_by_mean", "round_half_away", "no_clamp")
 MUTANTS_NTH = [(*m, 0) for m in MUTANTS if m[0] in _REPEATED] + \
-    [("n_" + m[0], m[1], m[2], 1) for m in MUTANTS if m[0] in _REPEATED]
-MUTANTS = [m for m in MUTANTS if m[0] not in _REPEATED]
+    [("n_" + m[0], m[1], m[2], 1) for m in MUTANTS if m[0] in _REPEATED] + \
+    [("sp24_" + m[0], m[1], m[2], 2) for m in MUTANTS if m[0] in _REPEATED3] + \
+    [(*m, 0) for m in MUTANTS if m[0] == "skip_weight_rotation"] + \
+    [("sp24_" + m[0], m[1], m[2], 1) for m in MUTANTS if m[0] == "skip_weight_rotation"]
+MUTANTS = [m for m in MUTANTS if m[0] not in _REPEATED and m[0] != "skip_weight_rotation"]
 ALL_MUTANTS = [(*m, None) for m in MUTANTS] + MUTANTS_NTH
 
 
@@ -93,6 +117,6 @@ def test_mutant_is_caught(tmp_path, name, old, new, nth):
     for check in oracle_pins.ALL_CHECKS:
         try:
             check(orc)
-        except AssertionError:
+        except (AssertionError, ValueError):  # a pin that rejects the mutant's output catches it too
             failed.append(check.__name__)
     assert failed, f"mutant {name} passed every pin"
