@@ -555,6 +555,7 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
         del W
     out["quantize_pack"] = sweep
     out["layouts"] = layout_bench(tq, torch, dev, pk, gen)
+    out["sparse24"] = sparse24_bench(tq, torch, dev, pk, gen)
     return out
 
 
@@ -613,6 +614,51 @@ def layout_bench(tq, torch, dev, pk, gen) -> list:
             r["unavailable"] = str(e)
         rows.append(r)
     return rows
+
+
+def sparse24_bench(tq, torch, dev, pk, gen) -> dict:
+    """The 2:4-sparse ternary format: quantise + pack (bf16 in), and the
+    zero-skipping GEMV on the decode shapes (M = 1 and 16), cycling over 8
+    copies of the codes so each launch streams from HBM.  GB/s counts the
+    sparse codes and scales (26 bytes per 128 weights) of one launch."""
+    out = {"bits_per_weight": 1.625}
+    try:
+        W = (torch.randn(HIDDEN, HIDDEN, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+        ms = time_events(lambda: tq.quantize_pack_sparse24(W), 5, torch)
+        N = K = HIDDEN
+        qbytes = N * K * 2 + N * tq.sparse24_ld(K) + N * (K // 128) * 2
+        out["quantize_pack_5120x5120"] = {"us": round(ms * 1e3, 1), "Gparams/s": round(N * K / (ms * 1e-3) / 1e9, 1),
+                                          "GB/s": round(qbytes / (ms * 1e-3) / 1e9, 1),
+                                          "frac_of_peak": round(qbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+        del W
+        for (N, K) in ((FFN, HIDDEN), (HIDDEN, FFN)):
+            W = (torch.randn(N, K, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+            c, sc = tq.quantize_pack_sparse24(W)
+            del W
+            copies = [(c.clone(), sc.clone()) for _ in range(8)]
+            del c, sc
+            nbytes = copies[0][0].numel() + copies[0][1].numel() * 2
+            for M in (1, 16):
+                x = activations(torch, dev, K, M, seed=K + M)
+                y = torch.empty(M, N, device=dev)
+                ws = torch.empty(tq.gemv_sparse24_workspace_bytes(N, K, M), dtype=torch.uint8, device=dev)
+                it = [0]
+
+                def run():
+                    cc, ss = copies[it[0] % len(copies)]
+                    it[0] += 1
+                    tq.gemv_sparse24(cc, ss, x, K, out=y, workspace=ws)
+
+                for _ in range(len(copies)):
+                    run()
+                ms = time_events(run, 3 * len(copies), torch)
+                gb = nbytes / (ms * 1e-3) / 1e9
+                out[f"gemv_M{M}_{N}x{K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gb, 1),
+                                             "frac_of_peak": round(gb / pk["hbm_gbs"], 4), "bytes": nbytes}
+            del copies
+    except tq.TQError as e:
+        out["unavailable"] = str(e)
+    return out
 
 
 def sweep_bench(tq, torch, weights, pk, world: int) -> dict:
@@ -811,6 +857,16 @@ def only_arm(args):
     elif args.only == "quantize":
         run = lambda: tq.quantize_pack(W, tq.TQ_PACK_BOTH)
         work, unit = N * K * 2 + N * (K // 4) + N * tq.packed_ld(K, tq.TQ_PACK_BASE3) + N * (K // 128) * 2, "GB/s"
+    elif args.only == "sparse24_quantize":
+        run = lambda: tq.quantize_pack_sparse24(W)
+        work, unit = N * K * 2 + N * tq.sparse24_ld(K) + N * (K // 128) * 2, "GB/s"
+    elif args.only == "sparse24_gemv":
+        c24, s24 = tq.quantize_pack_sparse24(W)
+        del W
+        y = torch.empty(M, N, device=dev)
+        ws = torch.empty(tq.gemv_sparse24_workspace_bytes(N, K, M), dtype=torch.uint8, device=dev)
+        run = lambda: tq.gemv_sparse24(c24, s24, x, K, out=y, workspace=ws)
+        work, unit = c24.numel() + s24.numel() * 2, "GB/s"
     elif args.only == "fwht":
         out = torch.empty(M, K, device=dev, dtype=torch.float16)
         run = lambda: tq.fwht128(x, out=out)
@@ -862,7 +918,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-budget", type=float, default=4.0)
     ap.add_argument("--layout", default="", help="block,group,residual for --only quantize (layout variants)")
-    ap.add_argument("--only", choices=["gemv", "gemm", "gemm_chain", "quantize", "fwht"],
+    ap.add_argument("--only", choices=["gemv", "gemm", "gemm_chain", "quantize", "fwht", "sparse24_gemv",
+                                       "sparse24_quantize"],
                     help="time one operation on one shape (for profiler captures)")
     ap.add_argument("--shape", default="27648x5120", help="NxK for --only")
     ap.add_argument("--M", type=int, default=1, help="activation rows for --only")

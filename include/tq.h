@@ -341,6 +341,52 @@ TQ_API tq_status tq_gemm_layout(const uint8_t *codes, int64_t ldc, int fmt, cons
                                 void *workspace, size_t ws_bytes, const tq_layout *lay, unsigned int flags,
                                 tq_stream stream);
 
+/* ---- 2:4-sparse ternary weights (mhpq.cn/news/1159370 sec. 1.2: two of
+ * every four weights kept at regular positions, the kept ones ternarised;
+ * sec. 1.1: the absmean rule).  Per quad of four consecutive k of a rotated
+ * group w' = FWHT-128(w), the two largest |w'| are kept (a tie goes to the
+ * lower index); the group's fp16 scale is the round-to-nearest mean |w'| of
+ * its 64 kept weights (halving-tree sum in k order, times 2^-6); a kept
+ * weight's trit is clamp(rint(w' / scale), -1, 1), a pruned one's is 0.
+ *
+ * Codes, one tensor holding mask and trits (row-major, ldc bytes per row,
+ * 24 per group of 128: 1.5 bits per weight, plus 0.125 of scale): quad j of
+ * a group has pattern p in 0..5 (its kept positions i0 < i1 in the order
+ * (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)) and code c = 9 p + 3 (t[i0] + 1) +
+ * (t[i1] + 1) < 54; the low nibble of c is nibble j % 2 of byte j / 2 of the
+ * group, its two high bits are bits 2 (j % 4) of byte 16 + j / 4.  Scales
+ * fp16 [N][K/128], row stride lds elements. */
+
+/* Bytes of codes per row: 24 K / 128; -1 unless K is a positive multiple of 128. */
+TQ_API int64_t tq_sparse24_ld(int64_t K);
+
+/* Quantise + pack W (wt TQ_F32 or TQ_BF16, [N][K], ldw elements, 16-byte
+ * aligned rows) into the 2:4 codes and scales.  Codes and scales are
+ * bit-exact with the definition above (fp32 staged FWHT-128, IEEE division).
+ * Requires K % 128 == 0, ldc >= tq_sparse24_ld(K), ldc % 4 == 0 and a 4-byte
+ * aligned codes pointer (the codes are written as 32-bit words),
+ * lds >= K/128, 2-byte aligned scales.  One launch; no allocation. */
+TQ_API tq_status tq_quantize_pack_sparse24(const void *W, int wt, int64_t N, int64_t K, int64_t ldw,
+                                           uint8_t *codes, int64_t ldc, uint16_t *scales, int64_t lds,
+                                           tq_stream stream);
+
+/* Workspace of tq_gemv_sparse24: the fp32 FWHT-128 of x ([M][K]) and, when
+ * the K groups are split into several slices (M x K x 4 bytes above 96 KiB),
+ * fp32 partial sums [slices][M][N].  0 for bad arguments. */
+TQ_API size_t tq_gemv_sparse24_workspace_bytes(int64_t N, int64_t K, int64_t M);
+
+/* y [M][N] fp32 = sum_g s[n][g] sum_{k in g} t[n][k] x'[m][k] over the 2:4
+ * codes, x bf16 [M][K] (16-byte aligned rows), M = 1..16: a pre-pass writes
+ * x' = FWHT-128(x) in fp32 to the workspace, then a decode kernel adds only
+ * the kept weights (sign-select adds, fp32 accumulation, each group's sum
+ * scaled by its fp16 scale), and, when K is split, a third kernel adds the
+ * slices in order.  Results are identical from call to call.  ws_bytes >=
+ * tq_gemv_sparse24_workspace_bytes(N, K, M); the workspace must not overlap
+ * the other arguments.  Codes outside 0..53 are read as a quad of zeros. */
+TQ_API tq_status tq_gemv_sparse24(const uint8_t *codes, int64_t ldc, const uint16_t *scales, int64_t lds,
+                                  int64_t N, int64_t K, const uint16_t *x, int64_t ldx, int64_t M, float *y,
+                                  int64_t ldy, void *workspace, size_t ws_bytes, tq_stream stream);
+
 /* Failure detection.  Every wait inside a kernel (pipeline barriers between
  * the warps that copy weights and the warps that compute) is bounded by a
  * wall-clock limit of about 2 s.  A kernel whose wait runs out stops early,

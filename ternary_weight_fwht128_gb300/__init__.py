@@ -33,7 +33,8 @@ EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_
             "tq_gemv_ex", "tq_gemv_path", "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_ex", "tq_gemm_check_range",
             "tq_device_fault", "tq_gemm_noalloc", "tq_layout_codes_ld", "tq_layout_scales_ld", "tq_fwht",
             "tq_quantize_pack_layout", "tq_gemv_layout", "tq_gemm_workspace_bytes_layout", "tq_gemm_layout",
-            "tq_gemm_rotate_next")
+            "tq_gemm_rotate_next", "tq_sparse24_ld", "tq_quantize_pack_sparse24",
+            "tq_gemv_sparse24_workspace_bytes", "tq_gemv_sparse24")
 TQ_GEMV_TENSOR_MEMORY, TQ_GEMV_MMA_SYNC = 1, 2
 TQ_GEMV_WEIGHTS_READY = 1
 TQ_GEMM_REUSE_ROTATED = 1
@@ -121,6 +122,15 @@ def lib() -> ctypes.CDLL:
         L.tq_gemm_layout.restype = _int
         L.tq_gemm_layout.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
                                      ctypes.c_size_t, lp, ctypes.c_uint, _vp]
+        L.tq_sparse24_ld.restype = _i64
+        L.tq_sparse24_ld.argtypes = [_i64]
+        L.tq_quantize_pack_sparse24.restype = _int
+        L.tq_quantize_pack_sparse24.argtypes = [_vp, _int, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
+        L.tq_gemv_sparse24_workspace_bytes.restype = ctypes.c_size_t
+        L.tq_gemv_sparse24_workspace_bytes.argtypes = [_i64, _i64, _i64]
+        L.tq_gemv_sparse24.restype = _int
+        L.tq_gemv_sparse24.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
+                                       ctypes.c_size_t, _vp]
         _lib = L
     return _lib
 
@@ -379,4 +389,57 @@ def gemm_rotate_next(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor,
                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(), flags,
                                    next_ws.data_ptr(), next_ws.numel() * next_ws.element_size(), _stream(stream))
     _check(st, "tq_gemm_rotate_next")
+    return out
+
+
+# ---- 2:4-sparse ternary weights (tq_quantize_pack_sparse24, tq_gemv_sparse24)
+
+def sparse24_ld(K: int) -> int:
+    """Bytes of 2:4 codes per row (24 per group of 128)."""
+    r = int(lib().tq_sparse24_ld(K))
+    if r < 0:
+        raise TQError(TQ_ERR_SHAPE, "tq_sparse24_ld")
+    return r
+
+
+def quantize_pack_sparse24(W: torch.Tensor, out=None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """(codes uint8 [N][24 K/128], scales int16 [N][K/128] with fp16 bits) of
+    W (fp32 or bf16 [N][K]) in the 2:4-sparse ternary format."""
+    _cuda2d(W, "W")
+    N, K = W.shape
+    if out is None:
+        codes = torch.empty((N, 24 * (K // 128)), dtype=torch.uint8, device=W.device)
+        scales = torch.empty((N, K // 128), dtype=torch.int16, device=W.device)
+    else:
+        codes, scales = out
+        _cuda2d(codes, "codes")
+        _cuda2d(scales, "scales")
+    st = lib().tq_quantize_pack_sparse24(W.data_ptr(), _dt(W), N, K, W.stride(0), codes.data_ptr(),
+                                         codes.stride(0), scales.data_ptr(), scales.stride(0), _stream(stream))
+    _check(st, "tq_quantize_pack_sparse24")
+    return codes, scales
+
+
+def gemv_sparse24_workspace_bytes(N: int, K: int, M: int) -> int:
+    return int(lib().tq_gemv_sparse24_workspace_bytes(N, K, M))
+
+
+def gemv_sparse24(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int,
+                  out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """y [M][N] fp32 of the 2:4 codes and bf16 x [M][K] (M <= 16)."""
+    _cuda2d(codes, "codes")
+    _cuda2d(scales, "scales")
+    _cuda2d(x, "x")
+    N = codes.shape[0]
+    M = x.shape[0]
+    if workspace is None:
+        workspace = torch.empty(max(gemv_sparse24_workspace_bytes(N, K, M), 16), dtype=torch.uint8,
+                                device=x.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    st = lib().tq_gemv_sparse24(codes.data_ptr(), codes.stride(0), scales.data_ptr(), scales.stride(0), N, K,
+                                x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "tq_gemv_sparse24")
     return out

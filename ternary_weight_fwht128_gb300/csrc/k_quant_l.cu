@@ -44,21 +44,6 @@ struct LParams {
   int64_t lds;
 };
 
-// Staged transform of n values in shared memory by one warp.
-__device__ __forceinline__ void fwht_warp(float* v, int n, float c, int lane) {
-  for (int h = 1; h < n; h <<= 1) {
-    for (int q = lane; q < n / 2; q += 32) {
-      const int i = (q / h) * 2 * h + (q % h);  // lower index of pair q
-      const float a = v[i], b = v[i + h];
-      v[i] = __fadd_rn(a, b);
-      v[i + h] = __fsub_rn(a, b);
-    }
-    __syncwarp();
-  }
-  for (int i = lane; i < n; i += 32) v[i] = __fmul_rn(v[i], c);
-  __syncwarp();
-}
-
 // fp16 scale of g values: halving-tree sum of |v| in fp32, times 1/g (exact).
 __device__ __forceinline__ uint16_t group_scale(const float* v, float* s, int g, int lane) {
   for (int i = lane; i < g; i += 32) s[i] = fabsf(v[i]);
@@ -70,12 +55,6 @@ __device__ __forceinline__ uint16_t group_scale(const float* v, float* s, int g,
   const float mean = __fmul_rn(s[0], 1.0f / (float)g);
   __syncwarp();
   return __half_as_ushort(__float2half_rn(mean));
-}
-
-__device__ __forceinline__ int ternarise(float w, float sc) {
-  if (sc == 0.0f) return 0;
-  const float q = rintf(__fdiv_rn(w, sc));  // round half to even
-  return q > 1.0f ? 1 : (q < -1.0f ? -1 : (int)q);
 }
 
 __global__ void __launch_bounds__(kThreads) k_quantize_layout(const LParams p) {

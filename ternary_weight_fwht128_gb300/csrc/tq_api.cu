@@ -390,6 +390,44 @@ tq_status tq_gemm_layout(const uint8_t* codes, int64_t ldc, int fmt, const uint1
                                ws_bytes - gemm_split_offset(M, Ke), s, (flags & TQ_GEMM_TEST_STALL) != 0, L.group));
 }
 
+int64_t tq_sparse24_ld(int64_t K) { return k_ok(K) ? 24 * (K / 128) : -1; }
+
+tq_status tq_quantize_pack_sparse24(const void* W, int wt, int64_t N, int64_t K, int64_t ldw, uint8_t* codes,
+                                    int64_t ldc, uint16_t* scales, int64_t lds, tq_stream stream) {
+  if (wt != TQ_F32 && wt != TQ_BF16) return TQ_ERR_INVALID_ARG;
+  if (N < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_ok(K)) return TQ_ERR_SHAPE;
+  if (N == 0) return TQ_OK;
+  if (W == nullptr || codes == nullptr || scales == nullptr) return TQ_ERR_INVALID_ARG;
+  if (ldw < K || ldc < tq_sparse24_ld(K) || lds < K / 128) return TQ_ERR_SHAPE;
+  if (!aligned16(W) || (ldw * dtype_size(wt)) % 16 || (reinterpret_cast<uintptr_t>(codes) & 3u) || ldc % 4 ||
+      !aligned2(scales))
+    return TQ_ERR_ALIGN;
+  return from_cuda(launch_quantize_sparse24(W, wt, N, K, ldw, codes, ldc, scales, lds, (cudaStream_t)stream));
+}
+
+size_t tq_gemv_sparse24_workspace_bytes(int64_t N, int64_t K, int64_t M) {
+  if (N < 0 || !k_ok(K) || M < 1 || M > 16) return 0;
+  return sparse24_gemv_workspace(N, K, M);
+}
+
+tq_status tq_gemv_sparse24(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,
+                           int64_t K, const uint16_t* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
+                           void* workspace, size_t ws_bytes, tq_stream stream) {
+  if (N < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_ok(K) || M < 1 || M > 16) return TQ_ERR_SHAPE;
+  if (N == 0) return TQ_OK;
+  if (codes == nullptr || scales == nullptr || x == nullptr || y == nullptr || workspace == nullptr)
+    return TQ_ERR_INVALID_ARG;
+  if (ldc < tq_sparse24_ld(K) || lds < K / 128 || ldx < K || ldy < N) return TQ_ERR_SHAPE;
+  if (ws_bytes < sparse24_gemv_workspace(N, K, M)) return TQ_ERR_SHAPE;
+  if (!aligned16(x) || (ldx * 2) % 16 || !aligned2(scales) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(y) & 3u))
+    return TQ_ERR_ALIGN;
+  return from_cuda(launch_gemv_sparse24(codes, ldc, scales, lds, N, K, x, ldx, M, y, ldy, workspace,
+                                        (cudaStream_t)stream));
+}
+
 tq_status tq_device_fault(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
   const unsigned int f = take_fault_gemv() | take_fault_quant() | take_fault_noalloc();

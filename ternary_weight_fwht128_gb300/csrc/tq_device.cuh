@@ -149,9 +149,36 @@ __device__ __forceinline__ void bf16x4_to_f32(uint2 w, float v[4]) {
 // early cannot promise.  These are plain C++ loads rather than volatile inline
 // assembly, so that the compiler may batch and schedule them, yet it cannot
 // move them above the wait (an asm statement with a memory clobber).
+__device__ __forceinline__ uint8_t ld_in_u8(const void* p) { return *reinterpret_cast<const uint8_t*>(p); }
 __device__ __forceinline__ uint16_t ld_in_u16(const void* p) { return *reinterpret_cast<const uint16_t*>(p); }
 __device__ __forceinline__ uint2 ld_in_u2(const void* p) { return *reinterpret_cast<const uint2*>(p); }
 __device__ __forceinline__ uint4 ld_in_u4(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// Staged transform of n values in shared memory by one warp: butterfly
+// stages h = 1, 2, .., n / 2 (the lower index of a pair keeps a + b), then one
+// multiply by c -- the order of the definition, so the result is bit-exact
+// with it.
+__device__ __forceinline__ void fwht_warp(float* v, int n, float c, int lane) {
+  for (int h = 1; h < n; h <<= 1) {
+    for (int q = lane; q < n / 2; q += 32) {
+      const int i = (q / h) * 2 * h + (q % h);  // lower index of pair q
+      const float a = v[i], b = v[i + h];
+      v[i] = __fadd_rn(a, b);
+      v[i + h] = __fsub_rn(a, b);
+    }
+    __syncwarp();
+  }
+  for (int i = lane; i < n; i += 32) v[i] = __fmul_rn(v[i], c);
+  __syncwarp();
+}
+
+// t = clamp(rint(w / sc), -1, 1) with IEEE division and round half to even;
+// 0 when the scale is 0.
+__device__ __forceinline__ int ternarise(float w, float sc) {
+  if (sc == 0.0f) return 0;
+  const float q = rintf(__fdiv_rn(w, sc));  // round half to even
+  return q > 1.0f ? 1 : (q < -1.0f ? -1 : (int)q);
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);

@@ -294,3 +294,59 @@ def test_gemm_rotate_next_validation(L):
     assert call(nw=W2 + 8) == tq.TQ_ERR_ALIGN
     assert call(fl=4) == tq.TQ_ERR_INVALID_ARG
     assert call(fmt=tq.TQ_PACK_BASE3) == tq.TQ_ERR_UNSUPPORTED
+
+
+def test_sparse24_validation(L):
+    assert L.tq_sparse24_ld(5120) == 960 and L.tq_sparse24_ld(27648) == 5184
+    assert L.tq_sparse24_ld(100) == -1 and L.tq_sparse24_ld(0) == -1
+    # x' fp32 (rounded to 256 B), then partial sums when K is split into slices
+    assert L.tq_gemv_sparse24_workspace_bytes(5120, 5120, 1) == 5120 * 4
+    assert L.tq_gemv_sparse24_workspace_bytes(5120, 27648, 1) == 27648 * 4 + 2 * 5120 * 4
+    assert L.tq_gemv_sparse24_workspace_bytes(5120, 100, 1) == 0
+    assert L.tq_gemv_sparse24_workspace_bytes(5120, 256, 17) == 0
+    q = L.tq_quantize_pack_sparse24
+    okq = dict(W=A, wt=tq.TQ_BF16, N=4, K=256, ldw=256, c=B, ldc=48, s=B + 4096, lds=2)
+
+    def callq(**kw):
+        a = dict(okq, **kw)
+        return q(a["W"], a["wt"], a["N"], a["K"], a["ldw"], a["c"], a["ldc"], a["s"], a["lds"], None)
+
+    assert callq(N=0) == tq.TQ_OK
+    assert callq(wt=tq.TQ_F16) == tq.TQ_ERR_INVALID_ARG
+    assert callq(N=-1) == tq.TQ_ERR_INVALID_ARG
+    assert callq(K=200) == tq.TQ_ERR_SHAPE
+    assert callq(c=None) == tq.TQ_ERR_INVALID_ARG
+    assert callq(s=None) == tq.TQ_ERR_INVALID_ARG
+    assert callq(ldc=47) == tq.TQ_ERR_SHAPE
+    assert callq(lds=1) == tq.TQ_ERR_SHAPE
+    assert callq(ldw=255) == tq.TQ_ERR_SHAPE
+    assert callq(W=MIS) == tq.TQ_ERR_ALIGN
+    assert callq(c=B + 2) == tq.TQ_ERR_ALIGN        # codes are written as 32-bit words
+    assert callq(ldc=50) == tq.TQ_ERR_ALIGN
+    assert callq(s=B + 4097) == tq.TQ_ERR_ALIGN
+    g = L.tq_gemv_sparse24
+    ws = L.tq_gemv_sparse24_workspace_bytes(64, 256, 2)
+    okg = dict(c=B, ldc=48, s=B + 4096, lds=2, N=64, K=256, x=A, ldx=256, M=2, y=B + 8192, ldy=64, w=B + 65536,
+               wb=ws)
+
+    def callg(**kw):
+        a = dict(okg, **kw)
+        return g(a["c"], a["ldc"], a["s"], a["lds"], a["N"], a["K"], a["x"], a["ldx"], a["M"], a["y"], a["ldy"],
+                 a["w"], a["wb"], None)
+
+    assert callg(N=0) == tq.TQ_OK
+    assert callg(N=-1) == tq.TQ_ERR_INVALID_ARG
+    assert callg(K=100) == tq.TQ_ERR_SHAPE
+    assert callg(M=0) == tq.TQ_ERR_SHAPE and callg(M=17) == tq.TQ_ERR_SHAPE
+    for k in ("c", "s", "x", "y", "w"):
+        assert callg(**{k: None}) == tq.TQ_ERR_INVALID_ARG, k
+    assert callg(ldc=47) == tq.TQ_ERR_SHAPE
+    assert callg(lds=1) == tq.TQ_ERR_SHAPE
+    assert callg(ldx=255) == tq.TQ_ERR_SHAPE
+    assert callg(ldy=63) == tq.TQ_ERR_SHAPE
+    assert callg(wb=ws - 1) == tq.TQ_ERR_SHAPE
+    assert callg(x=MIS) == tq.TQ_ERR_ALIGN
+    assert callg(ldx=260) == tq.TQ_ERR_ALIGN        # bf16 rows of x: 16-byte multiples
+    assert callg(s=B + 4097) == tq.TQ_ERR_ALIGN
+    assert callg(w=B + 65536 + 8) == tq.TQ_ERR_ALIGN
+    assert callg(y=B + 8194) == tq.TQ_ERR_ALIGN
