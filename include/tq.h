@@ -370,9 +370,13 @@ TQ_API tq_status tq_quantize_pack_sparse24(const void *W, int wt, int64_t N, int
                                            uint8_t *codes, int64_t ldc, uint16_t *scales, int64_t lds,
                                            tq_stream stream);
 
-/* Workspace of tq_gemv_sparse24: the fp32 FWHT-128 of x ([M][K]) and, when
- * the K groups are split into several slices (M x K x 4 bytes above 96 KiB),
- * fp32 partial sums [slices][M][N].  0 for bad arguments. */
+/* Workspace of tq_gemv_sparse24: the fp32 FWHT-128 of x ([M][K], rounded up
+ * to 256 bytes) and, when the K groups are split into several slices, fp32
+ * partial sums [slices][M][N].  The split depends on the shape only: enough
+ * slices that M x (slice groups) x 516 bytes fit 96 KiB, and, for a short N,
+ * up to ceil(512 / ceil(N / 32)) slices of at least 8 groups, the groups per
+ * slice rounded up to a multiple of 8 where that still fits.  0 for bad
+ * arguments. */
 TQ_API size_t tq_gemv_sparse24_workspace_bytes(int64_t N, int64_t K, int64_t M);
 
 /* y [M][N] fp32 = sum_g s[n][g] sum_{k in g} t[n][k] x'[m][k] over the 2:4
@@ -382,7 +386,9 @@ TQ_API size_t tq_gemv_sparse24_workspace_bytes(int64_t N, int64_t K, int64_t M);
  * scaled by its fp16 scale), and, when K is split, a third kernel adds the
  * slices in order.  Results are identical from call to call.  ws_bytes >=
  * tq_gemv_sparse24_workspace_bytes(N, K, M); the workspace must not overlap
- * the other arguments.  Codes outside 0..53 are read as a quad of zeros. */
+ * the other arguments.  The codes are read as 32-bit words: 4-byte aligned
+ * codes pointer and ldc % 4 == 0.  Codes outside 0..53 are read as a quad of
+ * zeros. */
 TQ_API tq_status tq_gemv_sparse24(const uint8_t *codes, int64_t ldc, const uint16_t *scales, int64_t lds,
                                   int64_t N, int64_t K, const uint16_t *x, int64_t ldx, int64_t M, float *y,
                                   int64_t ldy, void *workspace, size_t ws_bytes, tq_stream stream);

@@ -22,14 +22,21 @@
 // it.  Lane l owns quad l; the code bytes are assembled with OR shuffles.
 //
 // k_gemv_sparse24: decode with the pruned weights skipped.  A pre-pass
-// rotates x into an fp32 workspace; a CTA owns 32 rows and one slice of the
-// K groups, with the slice of x' staged in shared memory transposed as
-// [m][group][position in quad][quad], so that lane l (quad l of every group)
-// reads its two kept activations without bank conflicts whatever the
-// pattern.  Each kept weight is a sign-select add (t in {-1, 0, 1}); a lane
-// scales its quad's sum by the group's fp16 scale and accumulates in fp32;
-// the lanes are added by a fixed xor tree and the K slices by a second kernel
-// in slice order, so results do not change from call to call.
+// rotates x into an fp32 workspace; a CTA owns one slice of the K groups and
+// a share of the 32-row blocks (as many CTAs as fit on the SMs at once), with
+// the slice of x' staged in shared memory transposed as [m][group][position
+// in quad][quad] (groups padded to 129 floats).  A warp
+// takes eight groups of a row at a time, four lanes per group: lane (g, q)
+// reads one 32-bit word of low nibbles and one 16-bit word of high bits (its
+// eight codes) and the group's scale, and looks each code up in a 64-entry
+// table of (activation offsets, trit masks); the eight groups then fall on
+// different banks, so the two kept activations of each quad are read without
+// conflicts whatever the pattern.  Each kept weight is one FMA with its trit
+// as an fp32 -1, 0 or 1 (exact products); a lane scales its eight quads' sum
+// by the group's fp16 scale and accumulates in fp32; the lanes are added by a
+// fixed xor tree and
+// the K slices by a second kernel in slice order, so results do not change
+// from call to call.
 #include <algorithm>
 
 #include "tq_internal.h"
@@ -139,63 +146,86 @@ struct SGParams {
   float* part;  // [nsl][M][N] when nsl > 1
 };
 
-// code -> i0 | i1 << 2 | (t0 + 1) << 4 | (t1 + 1) << 6; 54..63 -> a quad of zeros
+// x' of one group in shared memory: [position in quad i][quad j] (i * 32 + j),
+// groups kXStride floats apart (one float of padding: the eight groups a warp
+// reads at once then fall on different banks)
+constexpr int kXStride = 129;
+
+// code -> 32 i0 | (32 i1) << 8 | keep0 << 16 | neg0 << 17 | keep1 << 18 |
+// neg1 << 19 (keep: the trit is not 0; neg: it is -1); 54..63 -> all zero
 __device__ __forceinline__ uint32_t code_entry(uint32_t c) {
-  if (c >= 54) return 0u | (1u << 2) | (1u << 4) | (1u << 6);
-  const uint32_t pt = c / 9, v = c - 9 * pt;
+  if (c >= 54) return 0u;
+  const uint32_t pt = c / 9, v = c - 9 * pt, f0 = v / 3, f1 = v % 3;
   const uint32_t i0 = pt < 3 ? 0u : (pt < 5 ? 1u : 2u);
   const uint32_t i1 = pt < 3 ? pt + 1 : (pt < 5 ? pt - 1 : 3u);
-  return i0 | (i1 << 2) | ((v / 3) << 4) | ((v % 3) << 6);
+  return (32u * i0) | ((32u * i1) << 8) | ((f0 != 1u) << 16) | ((f0 == 0u) << 17) | ((f1 != 1u) << 18) |
+         ((f1 == 0u) << 19);
 }
 
-// t * x for a trit stored as f = t + 1: sign flip for -1, zero for 0
-__device__ __forceinline__ float trit_times(uint32_t f, float x) {
-  const uint32_t keep = f == 1u ? 0u : 0xffffffffu, neg = f == 0u ? 0x80000000u : 0u;
-  return __uint_as_float((__float_as_uint(x) ^ neg) & keep);
+// the trit described by bits B (not 0) and B + 1 (-1) of e, as an fp32 -1, 0 or 1
+template <int B>
+__device__ __forceinline__ float trit_f32(uint32_t e) {
+  const uint32_t keep = 0u - ((e >> B) & 1u), neg = (e << (30 - B)) & 0x80000000u;
+  return __uint_as_float((0x3f800000u | neg) & keep);
 }
 
 template <int MB>
 __global__ void __launch_bounds__(32 * kGWarps) k_gemv_sparse24(const SGParams p) {
-  extern __shared__ float xs[];  // [M][gs][4][32]
-  __shared__ uint8_t tab[64];
+  extern __shared__ float xs[];  // [M][gs][kXStride]
+  __shared__ uint32_t tab[64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = p.K / 128, g0 = (int64_t)blockIdx.y * p.gs;
   const int gn = (int)((G - g0) < p.gs ? (G - g0) : p.gs);
   const int M = p.M;
-  if (threadIdx.x < 64) tab[threadIdx.x] = (uint8_t)code_entry(threadIdx.x);
+  if (threadIdx.x < 64) tab[threadIdx.x] = code_entry(threadIdx.x);
   pdl_wait();
-  // the slice of x', transposed: xs[((m gs + gl) 4 + i) 32 + j] = x'[m][128 (g0 + gl) + 4 j + i]
+  // the slice of x': xs[(m gs + gl) kXStride + 32 i + j] = x'[m][128 (g0 + gl) + 4 j + i]
   const int nx = M * gn * 128;
   for (int idx = threadIdx.x; idx < nx; idx += 32 * kGWarps) {
     const int m = idx / (gn * 128), r = idx - m * gn * 128, gl = r >> 7, k = r & 127;
-    xs[((m * p.gs + gl) * 4 + (k & 3)) * 32 + (k >> 2)] = p.xr[(int64_t)m * p.K + 128 * (g0 + gl) + k];
+    xs[(m * p.gs + gl) * kXStride + (k & 3) * 32 + (k >> 2)] = p.xr[(int64_t)m * p.K + 128 * (g0 + gl) + k];
   }
   __syncthreads();
-  for (int rr = 0; rr < kGRowsPerWarp; ++rr) {
-    const int64_t n = (int64_t)blockIdx.x * kGRows + warp * kGRowsPerWarp + rr;
+  // lane (gq, q) = (lane / 4, lane % 4) takes quads 8q .. 8q + 7 of group gb + gq
+  const int gq = lane >> 2, q = lane & 3;
+  // the CTA keeps its slice of x' and takes row blocks blockIdx.x, + gridDim.x, ..
+  const int64_t nrb = (p.N + kGRows - 1) / kGRows;
+  for (int64_t rb = blockIdx.x; rb < nrb; rb += gridDim.x) {
+    for (int rr = 0; rr < kGRowsPerWarp; ++rr) {
+    const int64_t n = rb * kGRows + warp * kGRowsPerWarp + rr;
     if (n >= p.N) break;
     const uint8_t* crow = p.codes + n * p.ldc + 24 * g0;
     const uint16_t* srow = p.scales + n * p.lds + g0;
     float acc[MB];
 #pragma unroll
     for (int m = 0; m < MB; ++m) acc[m] = 0.0f;
-#pragma unroll 4
-    for (int gl = 0; gl < gn; ++gl) {
-      const uint8_t* gp = crow + 24 * gl;
-      const uint32_t c = ((uint32_t)(ld_in_u8(gp + (lane >> 1)) >> (4 * (lane & 1))) & 15u) |
-                         ((((uint32_t)ld_in_u8(gp + 16 + (lane >> 2)) >> (2 * (lane & 3))) & 3u) << 4);
-      const uint32_t e = tab[c];
-      const float sc = __half2float(__ushort_as_half(ld_in_u16(srow + gl)));
-      const uint32_t i0 = e & 3u, i1 = (e >> 2) & 3u, f0 = (e >> 4) & 3u, f1 = e >> 6;
-      const float* xg = xs + gl * 128 + lane;
+    for (int gb = 0; gb < gn; gb += 8) {
+      const int gl = gb + gq;
+      const bool on = gl < gn;
+      const int gc = on ? gl : gn - 1;  // a lane past the slice reads group gn - 1 and adds zeros
+      const uint8_t* gp = crow + 24 * gc;
+      const uint32_t lo = ld_in_u32(gp + 4 * q), hi = ld_in_u16(gp + 16 + 2 * q);
+      const float sc = __half2float(__ushort_as_half(ld_in_u16(srow + gc)));
+      float part[MB];
 #pragma unroll
-      for (int m = 0; m < MB; ++m) {
-        if (m < M) {
-          const float* xm = xg + m * p.gs * 128;
-          const float part = trit_times(f0, xm[i0 * 32]) + trit_times(f1, xm[i1 * 32]);
-          acc[m] = fmaf(sc, part, acc[m]);
+      for (int m = 0; m < MB; ++m) part[m] = 0.0f;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const uint32_t c = ((lo >> (4 * jj)) & 15u) | (((hi >> (2 * jj)) & 3u) << 4);
+        const uint32_t e = on ? tab[c] : 0u;
+        const float* xq = xs + gc * kXStride + 8 * q + jj;
+        const uint32_t o0 = e & 0xffu, o1 = (e >> 8) & 0xffu;
+        const float t0 = trit_f32<16>(e), t1 = trit_f32<18>(e);
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+          if (m < M) {
+            const float* xm = xq + m * p.gs * kXStride;
+            part[m] = fmaf(t1, xm[o1], fmaf(t0, xm[o0], part[m]));
+          }
         }
       }
+#pragma unroll
+      for (int m = 0; m < MB; ++m) acc[m] = fmaf(sc, part[m], acc[m]);
     }
 #pragma unroll
     for (int m = 0; m < MB; ++m) {
@@ -212,6 +242,7 @@ __global__ void __launch_bounds__(32 * kGWarps) k_gemv_sparse24(const SGParams p
             p.part[((int64_t)blockIdx.y * M + m) * p.N + n] = acc[m];
         }
       }
+    }
     }
   }
   pdl_launch_dependents();
@@ -263,26 +294,41 @@ cudaError_t set_smem_once(int bytes) {
 
 template <int MB>
 cudaError_t launch_gemv_mb(const SGParams& p, int64_t row_blocks, cudaStream_t s) {
-  const int smem = p.M * p.gs * 128 * (int)sizeof(float);
+  const int smem = p.M * p.gs * kXStride * (int)sizeof(float);
   cudaError_t e = set_smem_once<MB>(smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_gemv_sparse24<MB>, dim3((unsigned)row_blocks, (unsigned)p.nsl), dim3(32 * kGWarps),
+  // as many CTAs as fit on the SMs at once (over all slices), each taking
+  // row blocks in turn after staging its slice of x' once
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_gemv_sparse24<MB>, 32 * kGWarps, (size_t)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t per_slice = std::max<int64_t>(1, (int64_t)std::max(occ, 1) * device_sm_count() / p.nsl);
+  const int64_t grid_x = std::min<int64_t>(row_blocks, per_slice);
+  return launch_pdl(k_gemv_sparse24<MB>, dim3((unsigned)grid_x, (unsigned)p.nsl), dim3(32 * kGWarps),
                     (size_t)smem, s, p);
 }
 
 }  // namespace
 
-void sparse24_plan(int64_t K, int64_t M, int* gs, int* nsl) {
-  const int64_t G = K / 128;
-  const int64_t cap = kSliceBytes / (M * 128 * (int64_t)sizeof(float));  // groups of x' per slice
-  const int64_t ns = (G + cap - 1) / cap;
-  *nsl = (int)ns;
-  *gs = (int)((G + ns - 1) / ns);
+// K slices: at least enough for each slice of x' to fit kSliceBytes, and,
+// for a short N, enough that the grid has about 512 CTAs (keeping at least
+// 8 groups per slice); a slice holds a multiple of 8 groups when it fits
+// (a warp takes 8 groups at a time).  The same on every device.
+void sparse24_plan(int64_t N, int64_t K, int64_t M, int* gs, int* nsl) {
+  const int64_t G = K / 128, row_blocks = (N + kGRows - 1) / kGRows;
+  const int64_t cap = kSliceBytes / (M * kXStride * (int64_t)sizeof(float));  // groups of x' per slice
+  int64_t ns = (G + cap - 1) / cap;
+  const int64_t want = std::min<int64_t>((512 + row_blocks - 1) / std::max<int64_t>(row_blocks, 1), G / 8);
+  ns = std::max<int64_t>(std::max<int64_t>(ns, want), 1);
+  int64_t g = (G + ns - 1) / ns;
+  if ((g + 7) / 8 * 8 <= cap) g = (g + 7) / 8 * 8;
+  *gs = (int)g;
+  *nsl = (int)((G + g - 1) / g);
 }
 
 size_t sparse24_gemv_workspace(int64_t N, int64_t K, int64_t M) {
   int gs = 0, nsl = 0;
-  sparse24_plan(K, M, &gs, &nsl);
+  sparse24_plan(N, K, M, &gs, &nsl);
   const size_t xr = (size_t)M * (size_t)K * sizeof(float);
   const size_t part = nsl > 1 ? (size_t)nsl * (size_t)M * (size_t)N * sizeof(float) : 0;
   return (xr + 255) / 256 * 256 + part;
@@ -301,7 +347,7 @@ cudaError_t launch_gemv_sparse24(const uint8_t* codes, int64_t ldc, const uint16
                                  void* ws, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   int gs = 0, nsl = 0;
-  sparse24_plan(K, M, &gs, &nsl);
+  sparse24_plan(N, K, M, &gs, &nsl);
   const int64_t row_blocks = (N + kGRows - 1) / kGRows;
   if (row_blocks > 0x7fffffffll || nsl > 65535) return cudaErrorNotSupported;
   float* xr = static_cast<float*>(ws);

@@ -422,7 +422,7 @@ tq_status tq_gemv_sparse24(const uint8_t* codes, int64_t ldc, const uint16_t* sc
   if (ldc < tq_sparse24_ld(K) || lds < K / 128 || ldx < K || ldy < N) return TQ_ERR_SHAPE;
   if (ws_bytes < sparse24_gemv_workspace(N, K, M)) return TQ_ERR_SHAPE;
   if (!aligned16(x) || (ldx * 2) % 16 || !aligned2(scales) || !aligned16(workspace) ||
-      (reinterpret_cast<uintptr_t>(y) & 3u))
+      (reinterpret_cast<uintptr_t>(y) & 3u) || (reinterpret_cast<uintptr_t>(codes) & 3u) || ldc % 4)
     return TQ_ERR_ALIGN;
   return from_cuda(launch_gemv_sparse24(codes, ldc, scales, lds, N, K, x, ldx, M, y, ldy, workspace,
                                         (cudaStream_t)stream));

@@ -151,6 +151,7 @@ __device__ __forceinline__ void bf16x4_to_f32(uint2 w, float v[4]) {
 // move them above the wait (an asm statement with a memory clobber).
 __device__ __forceinline__ uint8_t ld_in_u8(const void* p) { return *reinterpret_cast<const uint8_t*>(p); }
 __device__ __forceinline__ uint16_t ld_in_u16(const void* p) { return *reinterpret_cast<const uint16_t*>(p); }
+__device__ __forceinline__ uint32_t ld_in_u32(const void* p) { return *reinterpret_cast<const uint32_t*>(p); }
 __device__ __forceinline__ uint2 ld_in_u2(const void* p) { return *reinterpret_cast<const uint2*>(p); }
 __device__ __forceinline__ uint4 ld_in_u4(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 

@@ -90,7 +90,7 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
 // 2:4-sparse ternary format (24 code bytes per group of 128).  The GEMV takes
 // a workspace of sparse24_gemv_workspace(N, K, M) bytes: the fp32 rotated x,
 // then (when K is split into several slices) the slices' partial sums.
-void sparse24_plan(int64_t K, int64_t M, int* groups_per_slice, int* slices);
+void sparse24_plan(int64_t N, int64_t K, int64_t M, int* groups_per_slice, int* slices);
 size_t sparse24_gemv_workspace(int64_t N, int64_t K, int64_t M);
 cudaError_t launch_quantize_sparse24(const void* W, int wt, int64_t N, int64_t K, int64_t ldw, uint8_t* codes,
                                      int64_t ldc, uint16_t* scales, int64_t lds, cudaStream_t s);

@@ -299,9 +299,14 @@ def test_gemm_rotate_next_validation(L):
 def test_sparse24_validation(L):
     assert L.tq_sparse24_ld(5120) == 960 and L.tq_sparse24_ld(27648) == 5184
     assert L.tq_sparse24_ld(100) == -1 and L.tq_sparse24_ld(0) == -1
-    # x' fp32 (rounded to 256 B), then partial sums when K is split into slices
-    assert L.tq_gemv_sparse24_workspace_bytes(5120, 5120, 1) == 5120 * 4
-    assert L.tq_gemv_sparse24_workspace_bytes(5120, 27648, 1) == 27648 * 4 + 2 * 5120 * 4
+    # x' fp32 (rounded to 256 B), then partial sums when K is split into slices:
+    # 55296x5120 needs one slice; 5120x5120 (160 row blocks, aiming at ~512
+    # CTAs) is cut into 3 slices of 16 groups; 5120x27648 into 4 of 56
+    assert L.tq_gemv_sparse24_workspace_bytes(55296, 5120, 1) == 5120 * 4
+    assert L.tq_gemv_sparse24_workspace_bytes(5120, 5120, 1) == 5120 * 4 + 3 * 5120 * 4
+    assert L.tq_gemv_sparse24_workspace_bytes(5120, 27648, 1) == 27648 * 4 + 4 * 5120 * 4
+    # M = 16: 11 groups of x' per 96 KiB slice -> 20 slices over 216 groups
+    assert L.tq_gemv_sparse24_workspace_bytes(5120, 27648, 16) == 16 * 27648 * 4 + 20 * 16 * 5120 * 4
     assert L.tq_gemv_sparse24_workspace_bytes(5120, 100, 1) == 0
     assert L.tq_gemv_sparse24_workspace_bytes(5120, 256, 17) == 0
     q = L.tq_quantize_pack_sparse24
@@ -350,3 +355,5 @@ def test_sparse24_validation(L):
     assert callg(s=B + 4097) == tq.TQ_ERR_ALIGN
     assert callg(w=B + 65536 + 8) == tq.TQ_ERR_ALIGN
     assert callg(y=B + 8194) == tq.TQ_ERR_ALIGN
+    assert callg(c=B + 2) == tq.TQ_ERR_ALIGN        # codes are read as 32-bit words
+    assert callg(ldc=50) == tq.TQ_ERR_ALIGN
