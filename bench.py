@@ -656,6 +656,20 @@ def sparse24_bench(tq, torch, dev, pk, gen) -> dict:
                 out[f"gemv_M{M}_{N}x{K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gb, 1),
                                              "frac_of_peak": round(gb / pk["hbm_gbs"], 4), "bytes": nbytes}
             del copies
+        # prefill M = 2048: dense fp16 MMAs on the expanded tiles (2 M N K flops)
+        M = 2048
+        for (N, K) in ((HIDDEN, HIDDEN), (FFN, HIDDEN)):
+            W = (torch.randn(N, K, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+            c, sc = tq.quantize_pack_sparse24(W)
+            del W
+            xg = activations(torch, dev, K, M, seed=K + 7)
+            ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+            yg = torch.empty(M, N, device=dev)
+            ms = time_events(lambda: tq.gemm_sparse24(c, sc, xg, K, workspace=ws, out=yg), 10, torch)
+            tf = 2 * M * N * K / (ms * 1e-3) / 1e12
+            out[f"gemm_M{M}_{N}x{K}"] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                                         "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4)}
+            del c, sc, ws, yg
     except tq.TQError as e:
         out["unavailable"] = str(e)
     return out
@@ -867,6 +881,13 @@ def only_arm(args):
         ws = torch.empty(tq.gemv_sparse24_workspace_bytes(N, K, M), dtype=torch.uint8, device=dev)
         run = lambda: tq.gemv_sparse24(c24, s24, x, K, out=y, workspace=ws)
         work, unit = c24.numel() + s24.numel() * 2, "GB/s"
+    elif args.only == "sparse24_gemm":
+        c24, s24 = tq.quantize_pack_sparse24(W)
+        del W
+        y = torch.empty(M, N, device=dev)
+        ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device=dev)
+        run = lambda: tq.gemm_sparse24(c24, s24, x, K, workspace=ws, out=y)
+        work, unit = 2 * M * N * K, "TFLOP/s"
     elif args.only == "fwht":
         out = torch.empty(M, K, device=dev, dtype=torch.float16)
         run = lambda: tq.fwht128(x, out=out)
@@ -919,7 +940,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=4.0)
     ap.add_argument("--layout", default="", help="block,group,residual for --only quantize (layout variants)")
     ap.add_argument("--only", choices=["gemv", "gemm", "gemm_chain", "quantize", "fwht", "sparse24_gemv",
-                                       "sparse24_quantize"],
+                                       "sparse24_quantize", "sparse24_gemm"],
                     help="time one operation on one shape (for profiler captures)")
     ap.add_argument("--shape", default="27648x5120", help="NxK for --only")
     ap.add_argument("--M", type=int, default=1, help="activation rows for --only")

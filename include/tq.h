@@ -393,6 +393,18 @@ TQ_API tq_status tq_gemv_sparse24(const uint8_t *codes, int64_t ldc, const uint1
                                   int64_t N, int64_t K, const uint16_t *x, int64_t ldx, int64_t M, float *y,
                                   int64_t ldy, void *workspace, size_t ws_bytes, tq_stream stream);
 
+/* Prefill GEMM of the 2:4 codes: tq_gemm on the tcgen05 tensor cores with
+ * the 2:4 codes, M >= 1 rows of bf16 x.  The pruned weights are expanded
+ * into the dense fp16 weight tiles in shared memory (dense kind::f16 MMAs;
+ * the 2:4 sparse MMA form is not used), so the time is that of tq_gemm plus
+ * the code expansion.  Same workspace (tq_gemm_workspace_bytes(M, K)), the
+ * same fp16 x' overflow report through tq_gemm_check_range, the same
+ * accuracy and repeatability.  The codes are read as 8-byte words: 8-byte
+ * aligned codes pointer and ldc % 8 == 0. */
+TQ_API tq_status tq_gemm_sparse24(const uint8_t *codes, int64_t ldc, const uint16_t *scales, int64_t lds,
+                                  int64_t N, int64_t K, const uint16_t *x, int64_t ldx, int64_t M, float *y,
+                                  int64_t ldy, void *workspace, size_t ws_bytes, tq_stream stream);
+
 /* Failure detection.  Every wait inside a kernel (pipeline barriers between
  * the warps that copy weights and the warps that compute) is bounded by a
  * wall-clock limit of about 2 s.  A kernel whose wait runs out stops early,

@@ -34,7 +34,7 @@ EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_
             "tq_device_fault", "tq_gemm_noalloc", "tq_layout_codes_ld", "tq_layout_scales_ld", "tq_fwht",
             "tq_quantize_pack_layout", "tq_gemv_layout", "tq_gemm_workspace_bytes_layout", "tq_gemm_layout",
             "tq_gemm_rotate_next", "tq_sparse24_ld", "tq_quantize_pack_sparse24",
-            "tq_gemv_sparse24_workspace_bytes", "tq_gemv_sparse24")
+            "tq_gemv_sparse24_workspace_bytes", "tq_gemv_sparse24", "tq_gemm_sparse24")
 TQ_GEMV_TENSOR_MEMORY, TQ_GEMV_MMA_SYNC = 1, 2
 TQ_GEMV_WEIGHTS_READY = 1
 TQ_GEMM_REUSE_ROTATED = 1
@@ -128,6 +128,9 @@ def lib() -> ctypes.CDLL:
         L.tq_quantize_pack_sparse24.argtypes = [_vp, _int, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
         L.tq_gemv_sparse24_workspace_bytes.restype = ctypes.c_size_t
         L.tq_gemv_sparse24_workspace_bytes.argtypes = [_i64, _i64, _i64]
+        L.tq_gemm_sparse24.restype = _int
+        L.tq_gemm_sparse24.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
+                                       ctypes.c_size_t, _vp]
         L.tq_gemv_sparse24.restype = _int
         L.tq_gemv_sparse24.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
                                        ctypes.c_size_t, _vp]
@@ -442,4 +445,24 @@ def gemv_sparse24(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K:
                                 x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "tq_gemv_sparse24")
+    return out
+
+
+def gemm_sparse24(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int,
+                  workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """Prefill y [M][N] fp32 of the 2:4 codes and bf16 x [M][K] on the tensor cores."""
+    _cuda2d(codes, "codes")
+    _cuda2d(scales, "scales")
+    _cuda2d(x, "x")
+    N = codes.shape[0]
+    M = x.shape[0]
+    if workspace is None:
+        workspace = torch.empty(gemm_workspace_bytes(M, K), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    st = lib().tq_gemm_sparse24(codes.data_ptr(), codes.stride(0), scales.data_ptr(), scales.stride(0), N, K,
+                                x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "tq_gemm_sparse24")
     return out

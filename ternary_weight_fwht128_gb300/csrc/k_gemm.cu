@@ -71,6 +71,7 @@ struct SmemCtl {
   unsigned long long wait_ns;  // limit of every bounded wait of this launch
   uint32_t tmem_base;
   int abort;
+  uint8_t sp_tab[64];  // 2:4 codes: code -> the 2-bit code byte of its quad
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -210,10 +211,28 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sm
   return false;
 }
 
+// The 2-bit code byte of a quad of the 2:4 format's code c (9 p + 3 (t0 + 1)
+// + (t1 + 1), kept positions of pattern p in the order (0,1) (0,2) (0,3)
+// (1,2) (1,3) (2,3)): t + 1 at bits 2i for every position i, 1 (t = 0) at
+// the pruned ones; codes 54..63 give a quad of zeros.
+__device__ __forceinline__ uint32_t sp24_code_byte(uint32_t c) {
+  if (c >= 54) return 0x55u;
+  const uint32_t pt = c / 9, v = c - 9 * pt;
+  const uint32_t i0 = pt < 3 ? 0u : (pt < 5 ? 1u : 2u);
+  const uint32_t i1 = pt < 3 ? pt + 1 : (pt < 5 ? pt - 1 : 3u);
+  uint32_t b = 0x55u;
+  b = (b & ~(3u << (2 * i0))) | ((v / 3) << (2 * i0));
+  b = (b & ~(3u << (2 * i1))) | ((v % 3) << (2 * i1));
+  return b;
+}
+
 // EXT: the layout variants' scale groups (lgs) and the fused producer of the
 // next layer's x' (xnext) are compiled in; without it the kernel is the
-// method's plain GEMM.
-template <bool EXT>
+// method's plain GEMM.  SP: the weights are 2:4-sparse codes (24 bytes per
+// group of 128: low nibbles, then high bit pairs); a stage's 16 codes are
+// turned into the four 2-bit code words of its 64 weights through a 64-entry
+// table and then decoded as usual.
+template <bool EXT, bool SP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
               const __grid_constant__ CUtensorMap pmap, const Params p) {
@@ -248,6 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->done, 1);
     ctl->abort = 0;
+    if constexpr (SP) {
+      for (int c = 0; c < 64; ++c) ctl->sp_tab[c] = (uint8_t)sp24_code_byte((uint32_t)c);
+    }
     ctl->wait_ns = p.wait_ns;
     fence_mbar_init();
   }
@@ -316,7 +338,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // codes and scales run two stages ahead of the decode, so their latency
     // hides behind two stages of MMA
     auto ld_codes = [&](int st) {
-      return (in_tile && st < nk) ? ld_in_u4(crow + (s0 + st) * (BK / 4)) : make_uint4(0, 0, 0, 0);
+      if (!(in_tile && st < nk)) return make_uint4(0, 0, 0, 0);
+      if constexpr (SP) {
+        // stage half hf of group g: low nibbles at bytes 8 hf .., high bits at 16 + 4 hf ..
+        const int64_t kk = (int64_t)(s0 + st) * BK;
+        const uint8_t* gp = crow + 24 * (kk >> 7);
+        const int hf = (int)((kk >> 6) & 1);
+        const uint2 lo = ld_in_u2(gp + 8 * hf);
+        return make_uint4(lo.x, lo.y, ld_in_u32(gp + 16 + 4 * hf), 0u);
+      } else {
+        return ld_in_u4(crow + (s0 + st) * (BK / 4));
+      }
     };
     auto ld_scale = [&](int st) {
       const int lgs = EXT ? p.lgs : 0;
@@ -332,7 +364,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (use > 0 && !wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl, p.flag)) break;
       const uint32_t s2 = (uint32_t)sbits | ((uint32_t)sbits << 16);
       unsigned char* dst = b_ring + slot * kBStage + row_off;
-      const uint32_t w[4] = {cur.x, cur.y, cur.z, cur.w};
+      uint32_t w[4] = {cur.x, cur.y, cur.z, cur.w};
+      if constexpr (SP) {
+        // quad j of the stage (j = 0..15): low nibble j of (x, y), high bits j of z
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t b = 0;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * q + jj;
+            const uint32_t c = (((j < 8 ? cur.x : cur.y) >> (4 * (j & 7))) & 15u) | (((cur.z >> (2 * j)) & 3u) << 4);
+            b |= (uint32_t)ctl->sp_tab[c] << (8 * jj);
+          }
+          w[q] = b;
+        }
+      }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {  // 16 codes -> two 16-byte chunks (rows past the tile: none)
         if (!in_tile) break;
@@ -592,7 +638,7 @@ static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes, b
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
                         const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, void* split_ws,
                         size_t split_bytes, cudaStream_t s, bool test_stall, int group, uint16_t* xnext,
-                        uint32_t* flag_next) {
+                        uint32_t* flag_next, bool sparse24) {
   if (N == 0 || M == 0) return cudaSuccess;
   if ((int64_t)device_max_smem_optin() < (int64_t)kGemmSmem) return cudaErrorNotSupported;
   EncodeTiledFn enc = encode_fn();
@@ -654,6 +700,8 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_gemm_tc<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return e;
     smem_set[dev].store(true, std::memory_order_release);
   }
@@ -668,8 +716,10 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   cfg.attrs = at;
   cfg.numAttrs = 1;
   const bool ext = p.lgs != 0 || p.xnext != nullptr;
-  cudaError_t e = ext ? cudaLaunchKernelEx(&cfg, k_gemm_tc<true>, map, ymap, pmap, p)
-                      : cudaLaunchKernelEx(&cfg, k_gemm_tc<false>, map, ymap, pmap, p);
+  if (sparse24 && ext) return cudaErrorNotSupported;
+  cudaError_t e = sparse24 ? cudaLaunchKernelEx(&cfg, k_gemm_tc<false, true>, map, ymap, pmap, p)
+                  : ext    ? cudaLaunchKernelEx(&cfg, k_gemm_tc<true>, map, ymap, pmap, p)
+                           : cudaLaunchKernelEx(&cfg, k_gemm_tc<false>, map, ymap, pmap, p);
   if (e != cudaSuccess || n_split_tiles == 0) return e;
   // y of the split tiles: the partials added in segment order
   const int64_t work = n_split_tiles * BM * (p.bn / 4);

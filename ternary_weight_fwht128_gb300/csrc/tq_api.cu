@@ -428,6 +428,31 @@ tq_status tq_gemv_sparse24(const uint8_t* codes, int64_t ldc, const uint16_t* sc
                                         (cudaStream_t)stream));
 }
 
+tq_status tq_gemm_sparse24(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,
+                           int64_t K, const uint16_t* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
+                           void* workspace, size_t ws_bytes, tq_stream stream) {
+  if (N < 0 || M < 0) return TQ_ERR_INVALID_ARG;
+  if (!k_ok(K)) return TQ_ERR_SHAPE;
+  if (N == 0 || M == 0) return TQ_OK;
+  if (codes == nullptr || scales == nullptr || x == nullptr || y == nullptr || workspace == nullptr)
+    return TQ_ERR_INVALID_ARG;
+  if (ldc < tq_sparse24_ld(K) || lds < K / 128 || ldx < K || ldy < N) return TQ_ERR_SHAPE;
+  if (ws_bytes < tq_gemm_workspace_bytes(M, K)) return TQ_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(codes) & 7u) || ldc % 8 || !aligned2(scales) || !aligned16(x) || (ldx * 2) % 16 ||
+      !aligned16(workspace) || (reinterpret_cast<uintptr_t>(y) & 3u))
+    return TQ_ERR_ALIGN;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t* flag = static_cast<uint32_t*>(workspace);
+  uint16_t* xrot = reinterpret_cast<uint16_t*>(static_cast<unsigned char*>(workspace) + 256);
+  cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return TQ_ERR_CUDA;
+  e = launch_fwht128(x, TQ_BF16, ldx, xrot, TQ_F16, K, M, K, true, flag, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  unsigned char* split = static_cast<unsigned char*>(workspace) + gemm_split_offset(M, K);
+  return from_cuda(launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, split,
+                               ws_bytes - gemm_split_offset(M, K), s, false, 128, nullptr, nullptr, true));
+}
+
 tq_status tq_device_fault(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TQ_ERR_CUDA;
   const unsigned int f = take_fault_gemv() | take_fault_quant() | take_fault_noalloc();

@@ -81,11 +81,12 @@ constexpr size_t kGemmSplitBytes = (size_t)kMaxSplitUnits * 256 * 256 * sizeof(f
 // 256).  K counts every code column (both passes of a residual layout).
 // xnext: also write FWHT-128(y) as the next GEMM's fp16 x' ([M][N], N a
 // multiple of 128) and OR its fp16 overflow into *flag_next (the K split of a
-// short last wave is then not used).
+// short last wave is then not used).  sparse24: codes are the 2:4-sparse
+// format (24 bytes per group of 128; group 128, no xnext).
 cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N, int64_t K,
                         const uint16_t* xrot, int64_t M, float* y, int64_t ldy, uint32_t* flag, void* split_ws,
                         size_t split_bytes, cudaStream_t s, bool test_stall = false, int group = 128,
-                        uint16_t* xnext = nullptr, uint32_t* flag_next = nullptr);
+                        uint16_t* xnext = nullptr, uint32_t* flag_next = nullptr, bool sparse24 = false);
 
 // 2:4-sparse ternary format (24 code bytes per group of 128).  The GEMV takes
 // a workspace of sparse24_gemv_workspace(N, K, M) bytes: the fp32 rotated x,

@@ -357,3 +357,30 @@ def test_sparse24_validation(L):
     assert callg(y=B + 8194) == tq.TQ_ERR_ALIGN
     assert callg(c=B + 2) == tq.TQ_ERR_ALIGN        # codes are read as 32-bit words
     assert callg(ldc=50) == tq.TQ_ERR_ALIGN
+
+
+def test_gemm_sparse24_validation(L):
+    f = L.tq_gemm_sparse24
+    ws = tq.gemm_workspace_bytes(8, 256)
+    ok = dict(c=B, ldc=48, s=B + 4096, lds=2, N=64, K=256, x=A, ldx=256, M=8, y=B + 8192, ldy=64, w=B + 65536, wb=ws)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["c"], a["ldc"], a["s"], a["lds"], a["N"], a["K"], a["x"], a["ldx"], a["M"], a["y"], a["ldy"],
+                 a["w"], a["wb"], None)
+
+    assert call(N=0) == tq.TQ_OK and call(M=0) == tq.TQ_OK
+    assert call(N=-1) == tq.TQ_ERR_INVALID_ARG and call(M=-1) == tq.TQ_ERR_INVALID_ARG
+    assert call(K=100) == tq.TQ_ERR_SHAPE
+    for k in ("c", "s", "x", "y", "w"):
+        assert call(**{k: None}) == tq.TQ_ERR_INVALID_ARG, k
+    assert call(ldc=40) == tq.TQ_ERR_SHAPE
+    assert call(lds=1) == tq.TQ_ERR_SHAPE
+    assert call(ldx=255) == tq.TQ_ERR_SHAPE
+    assert call(ldy=63) == tq.TQ_ERR_SHAPE
+    assert call(wb=ws - 1) == tq.TQ_ERR_SHAPE
+    assert call(c=B + 4) == tq.TQ_ERR_ALIGN          # codes are read as 8-byte words
+    assert call(ldc=52) == tq.TQ_ERR_ALIGN
+    assert call(x=MIS) == tq.TQ_ERR_ALIGN
+    assert call(s=B + 4097) == tq.TQ_ERR_ALIGN
+    assert call(y=B + 8194) == tq.TQ_ERR_ALIGN

@@ -166,3 +166,50 @@ def test_gemv_sparse24_empty():
     x = to_dev_bf16(synth.activations(1, K, 1))
     y = tq.gemv_sparse24(codes, scales, x, K)
     assert y.shape == (1, 0)
+
+
+def _gemm_case(sp, N, K, M, seed, rows=None):
+    W = synth.weights(N, K, seed, dtype="bf16")
+    xb = synth.activations(M, K, seed + 1)
+    codes, scales = tq.quantize_pack_sparse24(_dev(W))
+    out, check = guarded((M, N), torch.float32)
+    ws = torch.empty(tq.gemm_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    tq.gemm_sparse24(codes, scales, to_dev_bf16(xb), K, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    check()
+    tq.gemm_check_range(ws)
+    c = codes.cpu().numpy()
+    S = u16(scales)
+    if rows is not None:
+        c, S = c[rows], S[rows]
+    ref = sp.gemv(c, S, synth.bf16_bits_to_f32(xb), K)
+    got = out.cpu().numpy() if rows is None else out.cpu().numpy()[:, rows]
+    check_y(got, ref)
+    return codes, scales
+
+
+@pytest.mark.parametrize("N,K,M", [(256, 256, 1), (300, 1280, 200), (513, 2560, 300), (64, 128, 1000)])
+def test_gemm_sparse24(sp, N, K, M):
+    _gemm_case(sp, N, K, M, seed=N + K + M + 1)
+
+
+@pytest.mark.parametrize("N,K", [(5120, 5120), (27648, 5120), (5120, 27648)])
+def test_gemm_sparse24_full_size_sampled(sp, N, K):
+    """Prefill M = 2048 on the bench shapes; the oracle checks 24 sampled
+    weight rows (last included) for all 2048 tokens."""
+    rows = np.sort(np.random.default_rng(N + K).choice(N, size=24, replace=False))
+    rows[-1] = N - 1
+    _gemm_case(sp, N, K, 2048, seed=N + K + 13, rows=rows)
+
+
+def test_gemm_sparse24_repeatable_and_matches_gemv():
+    N, K, M = 1000, 2560, 8
+    W = synth.weights(N, K, 31, dtype="bf16")
+    codes, scales = tq.quantize_pack_sparse24(_dev(W))
+    x = to_dev_bf16(synth.activations(M, K, 32))
+    ys = [tq.gemm_sparse24(codes, scales, x, K) for _ in range(5)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+    # the GEMM (fp16 x') and the GEMV (fp32 x') agree within the tolerance
+    check_y(ys[0].cpu().numpy(), tq.gemv_sparse24(codes, scales, x, K).cpu().numpy().astype(np.float64))
