@@ -226,9 +226,11 @@ TQ_API tq_status tq_gemm_ex(const uint8_t *codes, int64_t ldc, int fmt, const ui
  * tq_gemm_check_range(next_ws)).  The fp16 x' comes from the fp32 y, not from
  * y rounded to bf16 as the plain chain would give it.  N must be a multiple
  * of 128 and next_ws_bytes >= tq_gemm_workspace_bytes(M, N); the output
- * tiles are then whole 128-column groups and the K split of a short last wave
- * is not used.  next_ws must not overlap workspace.  Flags and everything
- * else as tq_gemm_ex. */
+ * tiles are then whole 128-column groups.  When a short last wave is split
+ * along K (y 16-byte aligned, ldy % 4 == 0), the x' of those tiles is
+ * computed after the fix-up from the finished fp32 y by the same staged
+ * transform (bit-identical); otherwise the last wave is not split.  next_ws
+ * must not overlap workspace.  Flags and everything else as tq_gemm_ex. */
 TQ_API tq_status tq_gemm_rotate_next(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales,
                                      int64_t lds, int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M,
                                      float *y, int64_t ldy, void *workspace, size_t ws_bytes, unsigned int flags,

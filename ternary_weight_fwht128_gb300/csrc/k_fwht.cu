@@ -226,7 +226,9 @@ cudaError_t launch_fwht128(const void* x, int xt, int64_t ldx, void* y, int yt, 
                            int64_t K, bool perm16, uint32_t* flag, cudaStream_t s) {
   const int64_t G = K / 128;
   if (rows == 0 || G == 0) return cudaSuccess;
-  if (perm16) return launch_t<TQ_BF16, TQ_F16, true>(x, ldx, y, ldy, rows, G, flag, s);
+  if (perm16)  // the GEMM pre-pass form: from bf16 x, or from an fp32 y (x' of a split tile's output)
+    return xt == TQ_F32 ? launch_t<TQ_F32, TQ_F16, true>(x, ldx, y, ldy, rows, G, flag, s)
+                        : launch_t<TQ_BF16, TQ_F16, true>(x, ldx, y, ldy, rows, G, flag, s);
   flag = nullptr;  // overflow is recorded by the pre-pass form only
   if (xt == TQ_F32) {
     if (yt == TQ_F32) return launch_t<TQ_F32, TQ_F32, false>(x, ldx, y, ldy, rows, G, flag, s);

@@ -40,6 +40,7 @@
 // word of codes without shuffling, and the pre-pass stores x' in that order.
 #include <cuda.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "tq_internal.h"
@@ -607,8 +608,7 @@ static GemmPlan gemm_plan(int64_t N, int64_t M, int64_t K, size_t split_bytes, b
   const int64_t tm = (M + BM - 1) / BM, nk = K / BK;
   GemmPlan best{BN, 0, 0, 0};
   int64_t best_cost = -1;
-  // whole_groups: tiles of whole 128-column groups (bn 256 or 128), no K split
-  if (whole_groups) split_bytes = 0;
+  // whole_groups: tiles of whole 128-column groups (bn 256 or 128)
   for (int bn = BN; bn >= 64; bn -= whole_groups ? 128 : 16) {
     const int64_t tiles = tm * ((N + bn - 1) / bn), w = bn + 96, c = (nk + kFillStages) * w;
     const int64_t full = tiles / sms, L = tiles - full * sms;
@@ -667,7 +667,12 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   p.wait_ns = test_stall ? kTestWaitLimitNs : kWaitLimitNs;
   p.lgs = group == 256 ? 1 : 0;
   p.n_tiles_m = (int)((M + BM - 1) / BM);
-  const GemmPlan g = gemm_plan(N, M, K, split_ws != nullptr ? split_bytes : 0, xnext != nullptr);
+  // With xnext, split tiles get their x' from the finished y (a pre-pass form
+  // of the transform over their columns after the fix-up), which reads y with
+  // 16-byte loads: no K split unless y allows them.
+  const bool y_vec16 = (reinterpret_cast<uintptr_t>(y) & 15u) == 0 && ldy % 4 == 0;
+  const size_t split_ok = (split_ws != nullptr && (xnext == nullptr || y_vec16)) ? split_bytes : 0;
+  const GemmPlan g = gemm_plan(N, M, K, split_ok, xnext != nullptr);
   if (xnext != nullptr && (N % 128 != 0 || g.bn % 128 != 0)) return cudaErrorNotSupported;
   p.xnext = xnext;
   p.ldxn = N;
@@ -732,8 +737,25 @@ cudaError_t launch_gemm(const uint8_t* codes, int64_t ldc, const uint16_t* scale
   fc.stream = s;
   fc.attrs = at;
   fc.numAttrs = 1;  // programmatic serialisation: waits for the GEMM in pdl_wait
-  return cudaLaunchKernelEx(&fc, k_gemm_fixup, static_cast<const float*>(split_ws), g.n_main, (int)n_split_tiles,
-                            g.splits, p.n_tiles_m, p.bn, M, N, y, ldy);
+  e = cudaLaunchKernelEx(&fc, k_gemm_fixup, static_cast<const float*>(split_ws), g.n_main, (int)n_split_tiles,
+                         g.splits, p.n_tiles_m, p.bn, M, N, y, ldy);
+  if (e != cudaSuccess || xnext == nullptr) return e;
+  // x' of the split tiles: FWHT-128 of their finished y, in the GEMM pre-pass
+  // form (fp16, 16-chunk order, overflow into *flag_next) -- one launch per
+  // run of split tiles that share a column block (tile = tile_m + tile_n * n_tiles_m)
+  for (int64_t t = g.n_main; t < g.tiles;) {
+    const int64_t tn = t / p.n_tiles_m, tm0 = t % p.n_tiles_m;
+    int64_t t1 = t;
+    while (t1 < g.tiles && t1 / p.n_tiles_m == tn) ++t1;
+    const int64_t tm1 = (t1 - 1) % p.n_tiles_m;
+    const int64_t m0 = tm0 * BM, m1 = std::min<int64_t>(M, (tm1 + 1) * BM);
+    const int64_t nc0 = tn * p.bn, ncols = std::min<int64_t>(N - nc0, p.bn);
+    e = launch_fwht128(y + m0 * ldy + nc0, TQ_F32, ldy, xnext + m0 * N + nc0, TQ_F16, N, m1 - m0, ncols, true,
+                       flag_next, s);
+    if (e != cudaSuccess) return e;
+    t = t1;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace tq

@@ -223,8 +223,10 @@ tq_status tq_gemm_rotate_next(const uint8_t* codes, int64_t ldc, int fmt, const 
     e = launch_fwht128(x, TQ_BF16, ldx, xrot, TQ_F16, K, M, K, true, flag, s);
     if (e != cudaSuccess) return from_cuda(e);
   }
-  return from_cuda(launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, nullptr, 0, s,
-                               (flags & TQ_GEMM_TEST_STALL) != 0, 128, xnext, flag_next));
+  unsigned char* split = static_cast<unsigned char*>(workspace) + gemm_split_offset(M, K);
+  return from_cuda(launch_gemm(codes, ldc, scales, lds, N, K, xrot, M, y, ldy, flag, split,
+                               ws_bytes - gemm_split_offset(M, K), s, (flags & TQ_GEMM_TEST_STALL) != 0, 128,
+                               xnext, flag_next));
 }
 
 tq_status tq_gemm_check_range(const void* workspace, tq_stream stream) {
