@@ -901,6 +901,26 @@ def only_arm(args):
             y = torch.empty(M, N, device=dev)
             run = lambda: tq.gemv(codes, s, x, K, fmt, out=y)
             work, unit = packed_bytes(N, K, "base3" if fmt == tq.TQ_PACK_BASE3 else "2bit"), "GB/s"
+        elif args.only in ("gemv_chain", "gemv_pair"):
+            # layer a (N x K) then layer b (K x N), as up and down: chained, a
+            # writes b's rotated x; as a pair, b takes a bf16 x of its own
+            Wb = (torch.randn(K, N, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+            cb, cb3, sb = tq.quantize_pack(Wb, fmt | tq.TQ_PACK_2BIT)
+            cb = cb3 if fmt == tq.TQ_PACK_BASE3 else cb
+            del Wb
+            ya, yb = torch.empty(M, N, device=dev), torch.empty(M, K, device=dev)
+            xn = torch.empty(M, N, device=dev)
+            xb = activations(torch, dev, N, M, seed=N + M)
+            if args.only == "gemv_chain":
+                def run():
+                    tq.gemv_rotate_next(codes, s, x, K, fmt, xnext=xn, out=ya, weights_ready=True)
+                    tq.gemv(cb, sb, xn, N, fmt, out=yb, weights_ready=True, x_rotated=True)
+            else:
+                def run():
+                    tq.gemv(codes, s, x, K, fmt, out=ya, weights_ready=True)
+                    tq.gemv(cb, sb, xb, N, fmt, out=yb, weights_ready=True)
+            fk = "base3" if fmt == tq.TQ_PACK_BASE3 else "2bit"
+            work, unit = packed_bytes(N, K, fk) + packed_bytes(K, N, fk), "GB/s"
         elif args.only == "gemm_chain":
             # layer a (N x K) writes layer b's x' in its epilogue; b (N x N) skips its pre-pass
             Wb = (torch.randn(N, N, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
@@ -941,7 +961,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=4.0)
     ap.add_argument("--layout", default="", help="block,group,residual for --only quantize (layout variants)")
     ap.add_argument("--only", choices=["gemv", "gemm", "gemm_chain", "quantize", "fwht", "sparse24_gemv",
-                                       "sparse24_quantize", "sparse24_gemm"],
+                                       "sparse24_quantize", "sparse24_gemm", "gemv_chain", "gemv_pair"],
                     help="time one operation on one shape (for profiler captures)")
     ap.add_argument("--shape", default="27648x5120", help="NxK for --only")
     ap.add_argument("--M", type=int, default=1, help="activation rows for --only")

@@ -147,11 +147,32 @@ TQ_API tq_status tq_gemv(const uint8_t *codes, int64_t ldc, int fmt, const uint1
  *       TQ_ERR_TIMEOUT and the rows of y of the stalled CTA's cluster are not
  *       written.  TQ_ERR_UNSUPPORTED when the shape takes the mma.sync
  *       kernel (which has no waits).
+ *   TQ_GEMV_X_ROTATED  x is already rotated: fp32 x' = FWHT-128(x), M rows
+ *       of ldx floats (4-byte aligned), as tq_gemv_rotate_next writes it for
+ *       the next layer; it is read instead of bf16 x and not rotated again.
+ *       Tensor-memory kernel only (TQ_ERR_UNSUPPORTED otherwise).
  * Unknown flag bits: TQ_ERR_INVALID_ARG.  Everything else as tq_gemv. */
-enum { TQ_GEMV_WEIGHTS_READY = 1, TQ_GEMV_TEST_STALL = 0x100 };
+enum { TQ_GEMV_WEIGHTS_READY = 1, TQ_GEMV_X_ROTATED = 2, TQ_GEMV_TEST_STALL = 0x100 };
 TQ_API tq_status tq_gemv_ex(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales, int64_t lds,
                             int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M, float *y, int64_t ldy,
                             unsigned int flags, tq_stream stream);
+
+/* tq_gemv_ex that also hands its output to the next layer already rotated
+ * (the activation transform fused into the producer of x, dpshk.com/news/
+ * 5289456 sec. 4.2, mhpq.cn/news/1159370 sec. 3.3, for decode): besides y it
+ * writes x'_next = FWHT-128(y) in fp32 into xnext (M rows of ldxn >= N
+ * floats, 4-byte aligned), computed from the fp32 y in the staged order --
+ * the x of a following tq_gemv_ex(..., TQ_GEMV_X_ROTATED) whose x is this
+ * call's y (K_next = N).  N must be a multiple of 128.  In the cluster
+ * reduction rank 0 then adds the partial sums of all rows of its tiles (it
+ * needs whole groups), so the call may plan a different K split than
+ * tq_gemv_ex.  flags: TQ_GEMV_WEIGHTS_READY, TQ_GEMV_X_ROTATED (x is itself
+ * a previous call's xnext), TQ_GEMV_TEST_STALL.  Tensor-memory kernel only
+ * (TQ_ERR_UNSUPPORTED otherwise).  xnext must not overlap x or y. */
+TQ_API tq_status tq_gemv_rotate_next(const uint8_t *codes, int64_t ldc, int fmt, const uint16_t *scales,
+                                     int64_t lds, int64_t N, int64_t K, const void *x, int64_t ldx, int64_t M,
+                                     float *y, int64_t ldy, unsigned int flags, float *xnext, int64_t ldxn,
+                                     tq_stream stream);
 
 /* Which kernel tq_gemv runs for a shape (introspection; launches nothing):
  *   TQ_GEMV_TENSOR_MEMORY  2-bit or base-3 codes, any M, when one CTA's share

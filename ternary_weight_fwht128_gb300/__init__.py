@@ -34,9 +34,10 @@ EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_
             "tq_device_fault", "tq_gemm_noalloc", "tq_layout_codes_ld", "tq_layout_scales_ld", "tq_fwht",
             "tq_quantize_pack_layout", "tq_gemv_layout", "tq_gemm_workspace_bytes_layout", "tq_gemm_layout",
             "tq_gemm_rotate_next", "tq_sparse24_ld", "tq_quantize_pack_sparse24",
-            "tq_gemv_sparse24_workspace_bytes", "tq_gemv_sparse24", "tq_gemm_sparse24")
+            "tq_gemv_sparse24_workspace_bytes", "tq_gemv_sparse24", "tq_gemm_sparse24", "tq_gemv_rotate_next")
 TQ_GEMV_TENSOR_MEMORY, TQ_GEMV_MMA_SYNC = 1, 2
 TQ_GEMV_WEIGHTS_READY = 1
+TQ_GEMV_X_ROTATED = 2
 TQ_GEMM_REUSE_ROTATED = 1
 TQ_GEMV_TEST_STALL = 0x100
 TQ_GEMM_TEST_STALL = 0x100
@@ -128,6 +129,9 @@ def lib() -> ctypes.CDLL:
         L.tq_quantize_pack_sparse24.argtypes = [_vp, _int, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp]
         L.tq_gemv_sparse24_workspace_bytes.restype = ctypes.c_size_t
         L.tq_gemv_sparse24_workspace_bytes.argtypes = [_i64, _i64, _i64]
+        L.tq_gemv_rotate_next.restype = _int
+        L.tq_gemv_rotate_next.argtypes = [_vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64,
+                                          ctypes.c_uint, _vp, _i64, _vp]
         L.tq_gemm_sparse24.restype = _int
         L.tq_gemm_sparse24.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
                                        ctypes.c_size_t, _vp]
@@ -217,10 +221,13 @@ def quantize_pack(W: torch.Tensor, fmt: int = TQ_PACK_BOTH, stream=None, out=Non
 
 
 def gemv(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, fmt: int = TQ_PACK_2BIT,
-         out: torch.Tensor | None = None, stream=None, weights_ready: bool = False) -> torch.Tensor:
+         out: torch.Tensor | None = None, stream=None, weights_ready: bool = False,
+         x_rotated: bool = False) -> torch.Tensor:
     """y [M][N] fp32 = ternary GEMV/skinny GEMM of bf16 x [M][K] (M <= 16).
     weights_ready: codes and scales were complete before the work preceding
-    this call on the stream started (tq_gemv_ex, TQ_GEMV_WEIGHTS_READY)."""
+    this call on the stream started (tq_gemv_ex, TQ_GEMV_WEIGHTS_READY).
+    x_rotated: x is the fp32 FWHT-128 of the activations, as gemv_rotate_next
+    writes it (TQ_GEMV_X_ROTATED)."""
     _cuda2d(codes, "codes")
     _cuda2d(scales, "scales")
     _cuda2d(x, "x")
@@ -228,7 +235,7 @@ def gemv(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int, fmt
     M = x.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    flags = TQ_GEMV_WEIGHTS_READY if weights_ready else 0
+    flags = (TQ_GEMV_WEIGHTS_READY if weights_ready else 0) | (TQ_GEMV_X_ROTATED if x_rotated else 0)
     st = lib().tq_gemv_ex(codes.data_ptr(), codes.stride(0), fmt, scales.data_ptr(), scales.stride(0), N, K,
                           x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), flags, _stream(stream))
     _check(st, "tq_gemv_ex")
@@ -466,3 +473,26 @@ def gemm_sparse24(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K:
                                 workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "tq_gemm_sparse24")
     return out
+
+
+def gemv_rotate_next(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor, K: int,
+                     fmt: int = TQ_PACK_2BIT, xnext: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                     stream=None, weights_ready: bool = False, x_rotated: bool = False,
+                     flags: int = 0) -> tuple[torch.Tensor, torch.Tensor]:
+    """(y, xnext): gemv that also writes FWHT-128(y) in fp32 as the x of a
+    following gemv(..., x_rotated=True) (tq_gemv_rotate_next)."""
+    _cuda2d(codes, "codes")
+    _cuda2d(scales, "scales")
+    _cuda2d(x, "x")
+    N = codes.shape[0]
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if xnext is None:
+        xnext = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    flags |= (TQ_GEMV_WEIGHTS_READY if weights_ready else 0) | (TQ_GEMV_X_ROTATED if x_rotated else 0)
+    st = lib().tq_gemv_rotate_next(codes.data_ptr(), codes.stride(0), fmt, scales.data_ptr(), scales.stride(0), N, K,
+                                   x.data_ptr(), x.stride(0), M, out.data_ptr(), out.stride(0), flags,
+                                   xnext.data_ptr(), xnext.stride(0), _stream(stream))
+    _check(st, "tq_gemv_rotate_next")
+    return out, xnext

@@ -232,6 +232,16 @@ struct Params {
   int blk;
   int lgs;
   int64_t g_rot;
+  // Chained decode (compiled into the LAYOUT instance only).  xr: x already
+  // rotated (fp32 x' of M rows of ldxr), read instead of x and not rotated
+  // again.  xnext: also write FWHT-128(y) in fp32 (M rows of ldxn; N a
+  // multiple of 128) -- rank 0 of each cluster then reduces all 128 rows of
+  // its tiles, so that it holds whole groups.
+  const float* xr;
+  int64_t ldxr;
+  float* xnext;
+  int64_t ldxn;
+  int64_t ypart_floats;  // partial sums in shared memory (floats)
 };
 // ---------------------------------------------------------------- PTX helpers
 
@@ -462,8 +472,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ct
 
 // Shared memory (1024-aligned): [code ring][B: groups_cap x kGroupB][zeros kZeroBytes]
 // [ztab: groups_cap x kZs x {pw Zt, pw}][partial sums: tiles_cap x kcl x M x 128 / kcl][Ctl]
-// LAYOUT: the layout variants' parameters (blk, lgs, g_rot) are read; without
-// it the kernel is compiled for the method's own layout only.
+// LAYOUT: the layout variants' parameters (blk, lgs, g_rot) and the chained
+// decode (xr, xnext) are read; without it the kernel is compiled for the
+// method's own layout only.
 template <int V, bool B3, bool LAYOUT>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__ CUtensorMap cmap, const Params p) {
   using Gm = Geo<V, B3>;
@@ -476,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   unsigned char* zero = bsm + p.groups_cap * Gm::kGroupB;
   float2* ztab = reinterpret_cast<float2*>(zero + kZeroBytes);
   float* ypart = reinterpret_cast<float*>(ztab + p.groups_cap * Gm::kZs);
-  Ctl* ctl = reinterpret_cast<Ctl*>(ypart + p.tiles_cap * 128 * p.M);
+  Ctl* ctl = reinterpret_cast<Ctl*>(ypart + p.ypart_floats);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -514,8 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   const int ntiles = (int)(t1 - t0);
   const int S = ntiles * nch;  // stages (ring loads) of this CTA
   const int M = p.M;
-  // rank q reduces rows R q .. R q + R - 1 of every tile
-  const int lgR = 7 - lgk, R = 1 << lgR;
+  // rank q reduces rows R q .. R q + R - 1 of every tile; with xnext rank 0
+  // reduces all of them (R = 128: the other ranks own none)
+  const bool all_rows = LAYOUT && p.xnext != nullptr;
+  const int lgR = all_rows ? 7 : 7 - lgk, R = 1 << lgR;
 
   int issued_loads = 0;
   auto fill_ring = [&]() {
@@ -543,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     }
     mbar_init(&ctl->red_bar, 1);
     // every other rank sends its partial sums of this rank's rows: ntiles x M x R floats each
-    if (p.kcl > 1) mbar_arrive_expect_tx(&ctl->red_bar, (uint32_t)((p.kcl - 1) * ntiles * M * R * 4));
+    if (p.kcl > 1)
+      mbar_arrive_expect_tx(&ctl->red_bar, (all_rows && rank != 0) ? 0u : (uint32_t)((p.kcl - 1) * ntiles * M * R * 4));
     ctl->abort = 0;
     ctl->wait_ns = p.wait_ns;
     fence_mbar_init();
@@ -592,6 +606,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     const int i8 = lane >> 2, jc = lane & 3;
     float v[4];
     if constexpr (LAYOUT) {
+      if (p.xr != nullptr) {  // x' given (the method's layout only): read, no rotation
+        const float* xg = p.xr + m * p.ldxr + (g0 + gl) * 128 + 16 * i8 + jc;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) v[b] = ld_in_f32(xg + 4 * b);
+      } else {
       // a residual layout's second half of the codes meets x itself
       const int64_t gg = g0 + gl;
       const bool rot = gg < p.g_rot;
@@ -601,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
 #pragma unroll
       for (int b = 0; b < 4; ++b) v[b] = __uint_as_float((uint32_t)ld_in_u16(xg + 4 * b) << 16);
       if (rot) rotate_group(v, lane, p.blk, xrow + (xc ^ 1) * 128, (xc & 1) != 0);
+      }
     } else {
       const uint16_t* xg = p.x + m * p.ldx + (g0 + gl) * 128 + 16 * i8 + jc;
 #pragma unroll
@@ -971,7 +991,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     if (ok) mbar_acquire_cluster(&ctl->red_bar, 0);
     if (!ok && threadIdx.x == 0) atomicOr(&g_gemv_fault, kFaultTimeout);
   }
-  if (ok && !ctl->abort) {
+  if (ok && !ctl->abort && all_rows) {
+    // rank 0: y of every row, then FWHT-128 of each (tile, row of x) group as
+    // the next layer's x'; warp w takes groups w, w + 23, ..  Lane 4i + j
+    // holds rows 16i + j + 4b of the tile (the transform's lane layout).
+    if (rank == 0) {
+      for (int it = warp; it < ntiles * M; it += kThreads / 32) {
+        const int tl = it / M, m = it - tl * M;
+        const int64_t n0 = (t0 + tl) * 128;
+        float v[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int rr = 16 * (lane >> 2) + (lane & 3) + 4 * b;
+          const float* src = ypart + (tl * p.kcl * M + m) * 128 + rr;
+          float sum = src[0];
+          for (int q = 1; q < p.kcl; ++q) sum += src[q * M * 128];
+          p.y[m * p.ldy + n0 + rr] = sum;
+          v[b] = sum;
+        }
+        fwht128_strided(v, lane);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) p.xnext[m * p.ldxn + n0 + 16 * (lane >> 2) + (lane & 3) + 4 * b] = v[b];
+      }
+    }
+  } else if (ok && !ctl->abort) {
     const int total = ntiles * M * R;
     for (int i = threadIdx.x; i < total; i += kThreads) {
       const int rr = i & (R - 1), j = i >> lgR, tl = j / M, m = j - tl * M;
@@ -1008,25 +1051,27 @@ EncodeTiledFn encode_fn() {
   return f;
 }
 
+// ypart_mult: 1, or kcl when rank 0 reduces every row (chained decode)
 template <int V, bool B3>
-size_t smem_bytes_v(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
+size_t smem_bytes_v(int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ypart_mult) {
   return 1024 + (size_t)kRing * kSlotBytes + (size_t)groups_cap * Geo<V, B3>::kGroupB + kZeroBytes +
-         (size_t)groups_cap * Geo<V, B3>::kZs * sizeof(float2) + (size_t)tiles_cap * 128 * M * sizeof(float) +
-         sizeof(Ctl);
+         (size_t)groups_cap * Geo<V, B3>::kZs * sizeof(float2) +
+         (size_t)tiles_cap * 128 * M * ypart_mult * sizeof(float) + sizeof(Ctl);
 }
 
 template <bool B3>
-size_t smem_bytes_f(int64_t groups_cap, int64_t tiles_cap, int64_t M) {
+size_t smem_bytes_f(int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ypart_mult) {
   switch (variant_of(M)) {
-    case 1: return smem_bytes_v<1, B3>(groups_cap, tiles_cap, M);
-    case 2: return smem_bytes_v<2, B3>(groups_cap, tiles_cap, M);
-    case 3: return smem_bytes_v<3, B3>(groups_cap, tiles_cap, M);
-    default: return smem_bytes_v<4, B3>(groups_cap, tiles_cap, M);
+    case 1: return smem_bytes_v<1, B3>(groups_cap, tiles_cap, M, ypart_mult);
+    case 2: return smem_bytes_v<2, B3>(groups_cap, tiles_cap, M, ypart_mult);
+    case 3: return smem_bytes_v<3, B3>(groups_cap, tiles_cap, M, ypart_mult);
+    default: return smem_bytes_v<4, B3>(groups_cap, tiles_cap, M, ypart_mult);
   }
 }
 
-size_t smem_bytes(bool b3, int64_t groups_cap, int64_t tiles_cap, int64_t M) {
-  return b3 ? smem_bytes_f<true>(groups_cap, tiles_cap, M) : smem_bytes_f<false>(groups_cap, tiles_cap, M);
+size_t smem_bytes(bool b3, int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ypart_mult = 1) {
+  return b3 ? smem_bytes_f<true>(groups_cap, tiles_cap, M, ypart_mult)
+            : smem_bytes_f<false>(groups_cap, tiles_cap, M, ypart_mult);
 }
 
 // Groups per CTA the shared layout holds: the largest K slice a rank gets,
@@ -1124,7 +1169,7 @@ unsigned int take_fault_gemv() {
 // busiest CTA (its stages -- 128 code bytes of one 128-row tile -- and its
 // prologue items); ties go to fewer CTAs.  Returns false when no split fits
 // in shared memory.
-bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* clusters_out) {
+bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* clusters_out, bool all_rows) {
   if (N <= 0 || K <= 0 || K % 128 != 0 || M < 1 || M > 16) return false;
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return false;
   const bool b3 = fmt == TQ_PACK_BASE3;
@@ -1143,7 +1188,7 @@ bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* c
     const int64_t gcap = groups_cap_of(b3, G, kcl);
     const int64_t gslice = b3 ? std::min(gcap, G) : (G + kcl - 1) / kcl;
     const int64_t tcap = (T + c - 1) / c;
-    if ((int64_t)smem_bytes(b3, gcap, tcap, M) > smem_max) continue;
+    if ((int64_t)smem_bytes(b3, gcap, tcap, M, all_rows ? kcl : 1) > smem_max) continue;
     const int64_t cost = tcap * (gcap / gs) * kItemsPerStage + gslice * M;
     if (best_kcl == 0 || cost < best || (cost == best && c * kcl < best_c * best_kcl)) {
       best = cost;
@@ -1162,10 +1207,10 @@ bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* c
 // shared-memory layout holds (the B layout grows with M), at most
 // kMaxLaunches launches; 0 when the shape does not suit the kernel.
 constexpr int kMaxLaunches = 4;
-int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt) {
+int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt, bool all_rows) {
   int kcl = 0, c = 0;
   for (int64_t m = M; m >= 1; --m) {
-    if (!plan_gemv_tc(N, K, m, fmt, &kcl, &c)) continue;
+    if (!plan_gemv_tc(N, K, m, fmt, &kcl, &c, all_rows)) continue;
     const int64_t l = (M + m - 1) / m;
     return l <= kMaxLaunches ? (int)l : 0;
   }
@@ -1174,20 +1219,31 @@ int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt) {
 
 cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds,
                            int64_t N, int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
-                           bool prefetch, cudaStream_t s, bool test_stall, const GemvLayout* lay) {
+                           bool prefetch, cudaStream_t s, bool test_stall, const GemvLayout* lay,
+                           const GemvChain* chain) {
   if (N == 0) return cudaSuccess;
   const bool b3 = fmt == TQ_PACK_BASE3;
   const int64_t G = K / 128, T = (N + 127) / 128;
+  const bool all_rows = chain != nullptr && chain->xnext != nullptr;
+  if (all_rows && N % 128 != 0) return cudaErrorNotSupported;
   int kcl = 0, clusters = 0;
-  if (!plan_gemv_tc(N, K, M, fmt, &kcl, &clusters)) {
+  if (!plan_gemv_tc(N, K, M, fmt, &kcl, &clusters, all_rows)) {
     // several launches, the rows of x split as evenly as possible
-    const int l = gemv_tc_launches(N, K, M, fmt);
+    const int l = gemv_tc_launches(N, K, M, fmt, all_rows);
     if (l < 2) return cudaErrorNotSupported;
     int64_t m0 = 0;
     for (int i = 0; i < l; ++i) {
       const int64_t mi = (M - m0) / (l - i);
-      cudaError_t e = launch_gemv_tc(codes, ldc, fmt, scales, lds, N, K, static_cast<const uint16_t*>(x) + m0 * ldx,
-                                     ldx, mi, y + m0 * ldy, ldy, prefetch, s, test_stall && i == 0, lay);
+      GemvChain ci{};
+      if (chain != nullptr) {
+        ci = *chain;
+        if (ci.xr != nullptr) ci.xr += m0 * ci.ldxr;
+        if (ci.xnext != nullptr) ci.xnext += m0 * ci.ldxn;
+      }
+      const uint16_t* xi = chain != nullptr && chain->xr != nullptr ? static_cast<const uint16_t*>(x)
+                                                                     : static_cast<const uint16_t*>(x) + m0 * ldx;
+      cudaError_t e = launch_gemv_tc(codes, ldc, fmt, scales, lds, N, K, xi, ldx, mi, y + m0 * ldy, ldy, prefetch, s,
+                                     test_stall && i == 0, lay, chain != nullptr ? &ci : nullptr);
       if (e != cudaSuccess) return e;
       m0 += mi;
     }
@@ -1228,12 +1284,21 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
   p.blk = lay != nullptr ? lay->block : 128;
   p.lgs = (lay != nullptr && lay->group == 256) ? 1 : 0;
   p.g_rot = (lay != nullptr && lay->residual) ? G / 2 : G;
+  if (chain != nullptr) {
+    p.xr = chain->xr;
+    p.ldxr = chain->ldxr;
+    p.xnext = chain->xnext;
+    p.ldxn = chain->ldxn;
+  }
+  p.ypart_floats = (int64_t)p.tiles_cap * 128 * M * (all_rows ? kcl : 1);
   const int64_t smem_max = device_max_smem_optin();
   // More than half an SM's shared memory, so no two CTAs share an SM whatever
   // the register count: each allocates all of tensor memory, and a second
   // one would block in tcgen05.alloc while its cluster peers wait for it.
-  const size_t smem = std::max(smem_bytes(b3, p.groups_cap, p.tiles_cap, M), (size_t)(smem_max / 2 + 1024));
-  const bool lv = lay != nullptr && (lay->block != 128 || lay->group != 128 || lay->residual);
+  const size_t smem =
+      std::max(smem_bytes(b3, p.groups_cap, p.tiles_cap, M, all_rows ? kcl : 1), (size_t)(smem_max / 2 + 1024));
+  const bool lv = (lay != nullptr && (lay->block != 128 || lay->group != 128 || lay->residual)) ||
+                  (chain != nullptr && (chain->xr != nullptr || chain->xnext != nullptr));
   const int v = variant_of(M);
   if (lv) {
     if (b3) return v == 1 ? launch_v<1, true, true>(map, p, smem, s) : v == 2 ? launch_v<2, true, true>(map, p, smem, s)

@@ -108,19 +108,39 @@ tq_status tq_quantize_pack(const void* W, int wt, int64_t N, int64_t K, int64_t 
                                         ld3, scales, lds, (cudaStream_t)stream));
 }
 
-tq_status tq_gemv_ex(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
-                     int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, unsigned int flags,
-                     tq_stream stream) {
+namespace {
+// Validation shared by tq_gemv_ex and tq_gemv_rotate_next (x is bf16, or the
+// fp32 rotated x with TQ_GEMV_X_ROTATED).
+tq_status gemv_check(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
+                     int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, unsigned int flags) {
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return TQ_ERR_INVALID_ARG;
-  if (flags & ~(unsigned int)(TQ_GEMV_WEIGHTS_READY | TQ_GEMV_TEST_STALL)) return TQ_ERR_INVALID_ARG;
+  if (flags & ~(unsigned int)(TQ_GEMV_WEIGHTS_READY | TQ_GEMV_X_ROTATED | TQ_GEMV_TEST_STALL))
+    return TQ_ERR_INVALID_ARG;
   if (N < 0) return TQ_ERR_INVALID_ARG;
   if (!k_ok(K) || M < 1 || M > 16) return TQ_ERR_SHAPE;
   if (N == 0) return TQ_OK;
   if (codes == nullptr || scales == nullptr || x == nullptr || y == nullptr) return TQ_ERR_INVALID_ARG;
   if (ldc < tq_packed_ld(K, fmt) || lds < K / 128 || ldx < K || ldy < N) return TQ_ERR_SHAPE;
-  if (!aligned16(codes) || ldc % 16 || !aligned2(scales) || !aligned16(x) || (ldx * 2) % 16 ||
-      (reinterpret_cast<uintptr_t>(y) & 3u))
+  const bool xrot = (flags & TQ_GEMV_X_ROTATED) != 0;
+  const bool x_ok = xrot ? (reinterpret_cast<uintptr_t>(x) & 3u) == 0 : (aligned16(x) && (ldx * 2) % 16 == 0);
+  if (!aligned16(codes) || ldc % 16 || !aligned2(scales) || !x_ok || (reinterpret_cast<uintptr_t>(y) & 3u))
     return TQ_ERR_ALIGN;
+  return TQ_OK;
+}
+}  // namespace
+
+tq_status tq_gemv_ex(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,
+                     int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy, unsigned int flags,
+                     tq_stream stream) {
+  const tq_status st = gemv_check(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy, flags);
+  if (st != TQ_OK || N == 0) return st;
+  if (flags & TQ_GEMV_X_ROTATED) {  // the tensor-memory kernel reads the fp32 x'
+    if (tq::gemv_tc_launches(N, K, M, fmt) == 0) return TQ_ERR_UNSUPPORTED;
+    const GemvChain ch{static_cast<const float*>(x), ldx, nullptr, 0};
+    return from_cuda(launch_gemv_tc(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy,
+                                    (flags & TQ_GEMV_WEIGHTS_READY) != 0, (cudaStream_t)stream,
+                                    (flags & TQ_GEMV_TEST_STALL) != 0, nullptr, &ch));
+  }
   if (flags & TQ_GEMV_TEST_STALL) {  // only the tensor-memory kernel has waits to stall
     if (tq::gemv_tc_launches(N, K, M, fmt) == 0) return TQ_ERR_UNSUPPORTED;
     return from_cuda(launch_gemv_tc(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy,
@@ -128,6 +148,28 @@ tq_status tq_gemv_ex(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t*
   }
   return from_cuda(launch_gemv(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy,
                                (flags & TQ_GEMV_WEIGHTS_READY) != 0, (cudaStream_t)stream));
+}
+
+tq_status tq_gemv_rotate_next(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds,
+                              int64_t N, int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
+                              unsigned int flags, float* xnext, int64_t ldxn, tq_stream stream) {
+  const tq_status st = gemv_check(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy, flags);
+  if (st != TQ_OK) return st;
+  if (N % 128 != 0) return TQ_ERR_SHAPE;
+  if (N == 0) return TQ_OK;
+  if (xnext == nullptr) return TQ_ERR_INVALID_ARG;
+  if (ldxn < N) return TQ_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(xnext) & 3u) return TQ_ERR_ALIGN;
+  const bool xrot = (flags & TQ_GEMV_X_ROTATED) != 0;
+  const uintptr_t xn0 = reinterpret_cast<uintptr_t>(xnext), xn1 = xn0 + (uintptr_t)((M - 1) * ldxn + N) * 4;
+  const uintptr_t y0 = reinterpret_cast<uintptr_t>(y), y1 = y0 + (uintptr_t)((M - 1) * ldy + N) * 4;
+  const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), x1 = x0 + (uintptr_t)((M - 1) * ldx + K) * (xrot ? 4 : 2);
+  if ((xn0 < y1 && y0 < xn1) || (xn0 < x1 && x0 < xn1)) return TQ_ERR_INVALID_ARG;
+  if (tq::gemv_tc_launches(N, K, M, fmt, true) == 0) return TQ_ERR_UNSUPPORTED;
+  const GemvChain ch{xrot ? static_cast<const float*>(x) : nullptr, ldx, xnext, ldxn};
+  return from_cuda(launch_gemv_tc(codes, ldc, fmt, scales, lds, N, K, x, ldx, M, y, ldy,
+                                  (flags & TQ_GEMV_WEIGHTS_READY) != 0, (cudaStream_t)stream,
+                                  (flags & TQ_GEMV_TEST_STALL) != 0, nullptr, &ch));
 }
 
 tq_status tq_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds, int64_t N,

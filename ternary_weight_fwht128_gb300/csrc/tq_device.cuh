@@ -152,6 +152,7 @@ __device__ __forceinline__ void bf16x4_to_f32(uint2 w, float v[4]) {
 __device__ __forceinline__ uint8_t ld_in_u8(const void* p) { return *reinterpret_cast<const uint8_t*>(p); }
 __device__ __forceinline__ uint16_t ld_in_u16(const void* p) { return *reinterpret_cast<const uint16_t*>(p); }
 __device__ __forceinline__ uint32_t ld_in_u32(const void* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ float ld_in_f32(const void* p) { return *reinterpret_cast<const float*>(p); }
 __device__ __forceinline__ uint2 ld_in_u2(const void* p) { return *reinterpret_cast<const uint2*>(p); }
 __device__ __forceinline__ uint4 ld_in_u4(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 

@@ -52,8 +52,10 @@ cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16
 // caller then uses launch_gemv's mma.sync kernel).  gemv_tc_launches: 1 when
 // one launch takes all M rows of x, 2 when it takes two launches of half the
 // rows each, 0 when the shape does not suit it.
-bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl, int* clusters);
-int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt);
+// all_rows: the chained form (GemvChain::xnext), where rank 0 of each cluster
+// holds the partial sums of every row of its tiles.
+bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl, int* clusters, bool all_rows = false);
+int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt, bool all_rows = false);
 // A layout variant of the method (block size, scale group, residual pass);
 // nullptr means block 128, group 128, no residual pass.
 struct GemvLayout {
@@ -62,13 +64,23 @@ struct GemvLayout {
   int residual;  // codes and scales hold a residual pass after the first
 };
 
+// Chained decode: xr (if set) is x already rotated, fp32 [M][ldxr], read
+// instead of x; xnext (if set) receives FWHT-128(y) in fp32 [M][ldxn] (N a
+// multiple of 128).  Method's layout only.
+struct GemvChain {
+  const float* xr;
+  int64_t ldxr;
+  float* xnext;
+  int64_t ldxn;
+};
+
 // test_stall: failure-path test (CTA 0 withholds a copy; waits bounded by
 // milliseconds), see TQ_GEMV_TEST_STALL.  lay: K counts the codes of both
 // passes of a residual layout (twice the activations' K).
 cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uint16_t* scales, int64_t lds,
                            int64_t N, int64_t K, const void* x, int64_t ldx, int64_t M, float* y, int64_t ldy,
                            bool prefetch, cudaStream_t s, bool test_stall = false,
-                           const GemvLayout* lay = nullptr);
+                           const GemvLayout* lay = nullptr, const GemvChain* chain = nullptr);
 
 // Returns cudaErrorNotSupported when the shape needs more shared memory than
 // one CTA can have.

@@ -110,7 +110,7 @@ def test_quantize_validation(L):
 def test_gemv_ex_validation(L):
     f = L.tq_gemv_ex
     args = (A, 64, tq.TQ_PACK_2BIT, B, 2, 8, 256, B + 4096, 256, 1, B + 8192, 8)
-    assert f(*args, 2, None) == tq.TQ_ERR_INVALID_ARG            # unknown flag bit
+    assert f(*args, 0x40, None) == tq.TQ_ERR_INVALID_ARG         # unknown flag bit
     assert f(*args[:5], 0, *args[6:], tq.TQ_GEMV_WEIGHTS_READY, None) == tq.TQ_OK   # N == 0
     assert f(*args[:9], 0, *args[10:], tq.TQ_GEMV_WEIGHTS_READY, None) == tq.TQ_ERR_SHAPE  # M == 0
 
@@ -384,3 +384,31 @@ def test_gemm_sparse24_validation(L):
     assert call(x=MIS) == tq.TQ_ERR_ALIGN
     assert call(s=B + 4097) == tq.TQ_ERR_ALIGN
     assert call(y=B + 8194) == tq.TQ_ERR_ALIGN
+
+
+def test_gemv_rotate_next_validation(L):
+    f = L.tq_gemv_rotate_next
+    ok = dict(c=B, ldc=64, fmt=tq.TQ_PACK_2BIT, s=B + 4096, lds=2, N=256, K=256, x=A, ldx=256, M=2, y=B + 8192,
+              ldy=256, fl=0, xn=B + 65536, ldxn=256)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["c"], a["ldc"], a["fmt"], a["s"], a["lds"], a["N"], a["K"], a["x"], a["ldx"], a["M"], a["y"],
+                 a["ldy"], a["fl"], a["xn"], a["ldxn"], None)
+
+    assert call(N=0) == tq.TQ_OK
+    assert call(fmt=7) == tq.TQ_ERR_INVALID_ARG
+    assert call(fl=0x40) == tq.TQ_ERR_INVALID_ARG
+    assert call(N=200, ldy=256, ldxn=256) == tq.TQ_ERR_SHAPE      # N a multiple of 128
+    assert call(M=0) == tq.TQ_ERR_SHAPE and call(M=17) == tq.TQ_ERR_SHAPE
+    assert call(xn=None) == tq.TQ_ERR_INVALID_ARG
+    assert call(ldxn=255) == tq.TQ_ERR_SHAPE
+    assert call(xn=B + 65538) == tq.TQ_ERR_ALIGN
+    assert call(xn=B + 8192 + 512) == tq.TQ_ERR_INVALID_ARG      # overlaps y
+    assert call(x=MIS) == tq.TQ_ERR_ALIGN                         # bf16 x: 16-byte rows
+    # rotated fp32 x needs 4-byte alignment only
+    g = L.tq_gemv_ex
+    assert g(B, 64, tq.TQ_PACK_2BIT, B + 4096, 2, 0, 256, MIS, 256, 1, B + 8192, 256, tq.TQ_GEMV_X_ROTATED,
+             None) == tq.TQ_OK
+    assert g(B, 64, tq.TQ_PACK_2BIT, B + 4096, 2, 4, 256, A + 2, 256, 1, B + 8192, 256, tq.TQ_GEMV_X_ROTATED,
+             None) == tq.TQ_ERR_ALIGN

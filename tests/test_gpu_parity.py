@@ -621,3 +621,46 @@ def test_gemm_rotate_next_reports_overflow():
     with pytest.raises(tq.TQError) as e:
         tq.gemm_check_range(ws2)
     assert e.value.status == tq.TQ_ERR_RANGE
+
+
+@pytest.mark.parametrize("fmt", [tq.TQ_PACK_2BIT, tq.TQ_PACK_BASE3], ids=["2bit", "base3"])
+@pytest.mark.parametrize("N1,K1,N2,M", [(5120, 5120, 1024, 1), (27648, 5120, 640, 1), (5120, 27648, 2048, 2),
+                                         (1280, 640, 384, 4), (640, 1280, 256, 16)])
+def test_gemv_rotate_next_chain(orc, fmt, N1, K1, N2, M):
+    """Decode chain: the first GEMV writes FWHT-128 of its fp32 output as the
+    next x' (bit for bit the oracle's staged fp32 transform of y1), and the
+    second GEMV reads it (TQ_GEMV_X_ROTATED) and matches the oracle applied to
+    y1.  The shapes reach every K split (5120x27648 uses clusters of 8, where
+    rank 0 then adds all 128 rows of each tile)."""
+    W1 = synth.weights(N1, K1, 71, dtype="bf16")
+    W2 = synth.weights(N2, N1, 72, dtype="bf16")
+    c1a, c1b, s1 = tq.quantize_pack(to_dev_bf16(W1), fmt)
+    c2a, c2b, s2 = tq.quantize_pack(to_dev_bf16(W2), fmt)
+    c1 = c1a if fmt == tq.TQ_PACK_2BIT else c1b
+    c2 = c2a if fmt == tq.TQ_PACK_2BIT else c2b
+    xb = synth.activations(M, K1, 73)
+    y1, xn = tq.gemv_rotate_next(c1, s1, to_dev_bf16(xb), K1, fmt)
+    y2 = tq.gemv(c2, s2, xn, N1, fmt, x_rotated=True)
+    torch.cuda.synchronize()
+    tq.device_fault()
+    y1n = y1.cpu().numpy()
+    assert np.array_equal(xn.cpu().numpy().view(np.uint32), orc.fwht128_f32(y1n).view(np.uint32))
+    # y1 equals the plain call's y within the tolerance (the reduction order of a different K split may differ)
+    check_y(y1n, tq.gemv(c1, s1, to_dev_bf16(xb), K1, fmt).cpu().numpy().astype(np.float64), "y1 vs plain")
+    rows = np.arange(0, N2, max(1, N2 // 48))
+    T2, S2 = orc.quantize(W2, rows)
+    check_y(y2.cpu().numpy()[:, rows], orc.gemv(T2, S2, y1n), "chained y2")
+    rows1 = np.arange(0, N1, max(1, N1 // 48))
+    T1, S1 = orc.quantize(W1, rows1)
+    check_y(y1n[:, rows1], orc.gemv(T1, S1, synth.bf16_bits_to_f32(xb)), "y1")
+
+
+def test_gemv_rotate_next_repeatable():
+    N1, K1, M = 5120, 27648, 1
+    W1 = synth.weights(N1, K1, 74, dtype="bf16")
+    c1, _, s1 = tq.quantize_pack(to_dev_bf16(W1), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(synth.activations(M, K1, 75))
+    outs = [tq.gemv_rotate_next(c1, s1, x, K1) for _ in range(30)]
+    torch.cuda.synchronize()
+    for y, xn in outs[1:]:
+        assert torch.equal(y, outs[0][0]) and torch.equal(xn, outs[0][1])
