@@ -1,11 +1,15 @@
 // k_fwht.cu -- block FWHT of activation rows (tq_fwht128 / tq_fwht, and the
 // rotation pre-pass of tq_gemm), block sizes 64, 128 and 256.
 //
-// A half-warp rotates one 128-block (row r, group g): lane p holds elements
-// 8p .. 8p+7, loaded with one 16-byte load (bf16) or two (fp32), so a warp
-// moves two blocks per load instruction.  Each warp keeps kUnroll block pairs
-// in flight before it computes; with four CTAs of eight warps per SM that is
-// 64-128 KB in flight per SM, which is what this bandwidth-bound pass needs.
+// Block 128 (k_fwht128_x16): an 8-lane group rotates one 128-block, lane p
+// holding elements 16p .. 16p+15 (two 16-byte loads for bf16), so four of the
+// seven butterfly stages stay in registers and three cross lanes.  Blocks 64
+// and 256 and the copy form (k_fwht128): a half-warp per 128-block, lane p
+// holding elements 8p .. 8p+7, loaded with one 16-byte load (bf16) or two
+// (fp32), so a warp moves two blocks per load instruction.  Each warp keeps
+// enough loads in flight before it computes that, with four CTAs of eight
+// warps per SM, 64-128 KB are in flight per SM, which is what this
+// bandwidth-bound pass needs.
 #include "tq_internal.h"
 
 namespace tq {
@@ -199,6 +203,185 @@ __global__ void __launch_bounds__(kThreads, 4) k_fwht128(const void* __restrict_
   pdl_launch_dependents();
 }
 
+// ---------------------------------------------------------------------------
+// Block size 128 with 16 elements per lane: an 8-lane group rotates one
+// 128-block (lane p = lane % 8 holds elements 16p .. 16p + 15; a warp holds four
+// blocks).  Stages h = 1, 2, 4, 8 run in the lane's registers (h = 1 on single
+// values, then packed f32x2 pairs), h = 16, 32, 64 across lanes l ^ 1, 2, 4 --
+// three shuffle stages instead of four, on half as many lanes per block -- then
+// one multiply by c; every operation as in the staged definition, so the result
+// is bit-identical to it.  A lane also holds a whole 16-element chunk, so the
+// GEMM pre-pass order (0,8,1,9,...,7,15) is a permutation of its own registers.
+template <int XT>
+struct Raw16 {
+  uint4 w[XT == TQ_F32 ? 4 : 2];
+};
+
+__device__ __forceinline__ void fwht128_x16(float v[16], int lane) {
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {  // h = 1
+    const float a = v[j], b = v[j + 1];
+    v[j] = a + b;
+    v[j + 1] = a - b;
+  }
+  uint64_t q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) q[i] = f2_pack(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int hp = 1; hp < 8; hp <<= 1) {  // h = 2, 4, 8 on pairs
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & hp) == 0) {
+        const uint64_t a = q[i], b = q[i + hp];
+        q[i] = f2_add(a, b);
+        q[i + hp] = f2_sub(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {  // h = 16, 32, 64: lower lane a + b, upper lane a - b
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
+    const uint64_t sg = f2_pack(sgn, sgn);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float lo, hi;
+      f2_unpack(q[i], lo, hi);
+      const float olo = __shfl_xor_sync(kFull, lo, m), ohi = __shfl_xor_sync(kFull, hi, m);
+      q[i] = f2_fma(sg, q[i], f2_pack(olo, ohi));
+    }
+  }
+  const uint64_t sc = f2_pack(kInvSqrt128, kInvSqrt128);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) f2_unpack(f2_mul(q[i], sc), v[2 * i], v[2 * i + 1]);
+}
+
+template <int YT, bool PERM16>
+__device__ __forceinline__ void store16(void* y, int64_t off, const float v[16], uint32_t* flag, bool valid) {
+  if (!valid) return;
+  if constexpr (YT == TQ_F32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(y) + off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else if constexpr (YT == TQ_BF16) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + off);
+    dst[0] = make_uint4(pack_bf162(v[0], v[1]), pack_bf162(v[2], v[3]), pack_bf162(v[4], v[5]), pack_bf162(v[6], v[7]));
+    dst[1] = make_uint4(pack_bf162(v[8], v[9]), pack_bf162(v[10], v[11]), pack_bf162(v[12], v[13]),
+                        pack_bf162(v[14], v[15]));
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + off);
+    if constexpr (PERM16) {
+      if (flag != nullptr) {  // fp16 infinity exactly from |v| >= 65520 (round to nearest even)
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        if (amax >= 65520.0f) atomicOr(flag, 1u);
+      }
+      // slots 2i, 2i + 1 hold elements i and 8 + i
+      dst[0] = make_uint4(pack_half2(v[0], v[8]), pack_half2(v[1], v[9]), pack_half2(v[2], v[10]),
+                          pack_half2(v[3], v[11]));
+      dst[1] = make_uint4(pack_half2(v[4], v[12]), pack_half2(v[5], v[13]), pack_half2(v[6], v[14]),
+                          pack_half2(v[7], v[15]));
+    } else {
+      dst[0] = make_uint4(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]), pack_half2(v[6], v[7]));
+      dst[1] = make_uint4(pack_half2(v[8], v[9]), pack_half2(v[10], v[11]), pack_half2(v[12], v[13]),
+                          pack_half2(v[14], v[15]));
+    }
+  }
+}
+
+// Loads in flight per lane: 32 bytes each (bf16) -- two keep as many bytes in
+// flight per SM as four of the 8-element form; one for fp32 (64 bytes).
+template <int XT>
+constexpr int kUnroll16 = XT == TQ_F32 ? 1 : 2;
+
+template <int XT, int YT, bool PERM16>
+__global__ void __launch_bounds__(kThreads, 4) k_fwht128_x16(const void* __restrict__ x, int64_t ldx, void* y,
+                                                             int64_t ldy, int64_t rows, int64_t G, uint32_t* flag) {
+  constexpr int esize = XT == TQ_F32 ? 4 : 2;
+  const int lane = threadIdx.x & 31, p = lane & 7, grp = lane >> 3;
+  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int64_t nblk = rows * G;
+  pdl_wait();
+  // Warp-iteration u covers blocks 4 (warp + u nwarps) + {0 .. 3}; each lane
+  // walks its block sequence with a constant stride of 4 nwarps blocks,
+  // advancing (row, group) and the offsets incrementally (no division).
+  const int64_t step = 4 * nwarps, dr = step / G, dg = step - (step / G) * G;
+  const int64_t b_first = 4 * warp + grp;
+  int64_t g = b_first % G, r = b_first / G;
+  int64_t xo = r * ldx + g * 128 + 16 * p, yo = r * ldy + g * 128 + 16 * p;
+  const int64_t xadv = dr * ldx + dg * 128, yadv = dr * ldy + dg * 128;
+  const int64_t xwrap = ldx - G * 128, ywrap = ldy - G * 128;
+  for (int64_t b0 = warp; 4 * b0 < nblk; b0 += nwarps * kUnroll16<XT>) {
+    Raw16<XT> raw[kUnroll16<XT>];
+    int64_t yof[kUnroll16<XT>];
+    bool ok[kUnroll16<XT>];
+#pragma unroll
+    for (int u = 0; u < kUnroll16<XT>; ++u) {
+      ok[u] = r < rows;
+      yof[u] = yo;
+#pragma unroll
+      for (int i = 0; i < (XT == TQ_F32 ? 4 : 2); ++i) raw[u].w[i] = make_uint4(0, 0, 0, 0);
+      if (ok[u]) {
+        const unsigned char* src = static_cast<const unsigned char*>(x) + xo * esize;
+#pragma unroll
+        for (int i = 0; i < (XT == TQ_F32 ? 4 : 2); ++i) raw[u].w[i] = ld_in_u4(src + 16 * i);
+      }
+      g += dg;
+      r += dr;
+      xo += xadv;
+      yo += yadv;
+      if (g >= G) {
+        g -= G;
+        r += 1;
+        xo += xwrap;
+        yo += ywrap;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll16<XT>; ++u) {
+      if (4 * (b0 + (int64_t)u * nwarps) >= nblk) break;  // warp-uniform
+      float v[16];
+      if constexpr (XT == TQ_F32) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[4 * i] = __uint_as_float(raw[u].w[i].x);
+          v[4 * i + 1] = __uint_as_float(raw[u].w[i].y);
+          v[4 * i + 2] = __uint_as_float(raw[u].w[i].z);
+          v[4 * i + 3] = __uint_as_float(raw[u].w[i].w);
+        }
+      } else {
+        bf16x8_to_f32(raw[u].w[0], v);
+        bf16x8_to_f32(raw[u].w[1], v + 8);
+      }
+      fwht128_x16(v, lane);
+      store16<YT, PERM16>(y, yof[u], v, flag, ok[u]);
+    }
+  }
+  pdl_launch_dependents();
+}
+
+template <int XT, int YT, bool PERM16>
+cudaError_t launch_x16(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t rows, int64_t G, uint32_t* flag,
+                       cudaStream_t s) {
+  const int64_t nblk = rows * G;
+  const int sms = device_sm_count();
+  const int64_t want = (nblk + 4 * (kThreads / 32) - 1) / (4 * (kThreads / 32));
+  const int64_t cap = (int64_t)sms * 4;  // 4 resident CTAs of 256 threads per SM
+  int64_t grid = want < cap ? want : cap;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_fwht128_x16<XT, YT, PERM16>, x, ldx, y, ldy, rows, G, flag);
+}
+
 template <int XT, int YT, bool PERM16, int BLK = 128>
 cudaError_t launch_t(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t rows, int64_t G, uint32_t* flag,
                      cudaStream_t s) {
@@ -227,17 +410,17 @@ cudaError_t launch_fwht128(const void* x, int xt, int64_t ldx, void* y, int yt, 
   const int64_t G = K / 128;
   if (rows == 0 || G == 0) return cudaSuccess;
   if (perm16)  // the GEMM pre-pass form: from bf16 x, or from an fp32 y (x' of a split tile's output)
-    return xt == TQ_F32 ? launch_t<TQ_F32, TQ_F16, true>(x, ldx, y, ldy, rows, G, flag, s)
-                        : launch_t<TQ_BF16, TQ_F16, true>(x, ldx, y, ldy, rows, G, flag, s);
+    return xt == TQ_F32 ? launch_x16<TQ_F32, TQ_F16, true>(x, ldx, y, ldy, rows, G, flag, s)
+                        : launch_x16<TQ_BF16, TQ_F16, true>(x, ldx, y, ldy, rows, G, flag, s);
   flag = nullptr;  // overflow is recorded by the pre-pass form only
   if (xt == TQ_F32) {
-    if (yt == TQ_F32) return launch_t<TQ_F32, TQ_F32, false>(x, ldx, y, ldy, rows, G, flag, s);
-    if (yt == TQ_BF16) return launch_t<TQ_F32, TQ_BF16, false>(x, ldx, y, ldy, rows, G, flag, s);
-    return launch_t<TQ_F32, TQ_F16, false>(x, ldx, y, ldy, rows, G, flag, s);
+    if (yt == TQ_F32) return launch_x16<TQ_F32, TQ_F32, false>(x, ldx, y, ldy, rows, G, flag, s);
+    if (yt == TQ_BF16) return launch_x16<TQ_F32, TQ_BF16, false>(x, ldx, y, ldy, rows, G, flag, s);
+    return launch_x16<TQ_F32, TQ_F16, false>(x, ldx, y, ldy, rows, G, flag, s);
   }
-  if (yt == TQ_F32) return launch_t<TQ_BF16, TQ_F32, false>(x, ldx, y, ldy, rows, G, flag, s);
-  if (yt == TQ_BF16) return launch_t<TQ_BF16, TQ_BF16, false>(x, ldx, y, ldy, rows, G, flag, s);
-  return launch_t<TQ_BF16, TQ_F16, false>(x, ldx, y, ldy, rows, G, flag, s);
+  if (yt == TQ_F32) return launch_x16<TQ_BF16, TQ_F32, false>(x, ldx, y, ldy, rows, G, flag, s);
+  if (yt == TQ_BF16) return launch_x16<TQ_BF16, TQ_BF16, false>(x, ldx, y, ldy, rows, G, flag, s);
+  return launch_x16<TQ_BF16, TQ_F16, false>(x, ldx, y, ldy, rows, G, flag, s);
 }
 
 namespace {
