@@ -25,18 +25,17 @@
 // rotates x into an fp32 workspace; a CTA owns one slice of the K groups and
 // a share of the 32-row blocks (as many CTAs as fit on the SMs at once), with
 // the slice of x' staged in shared memory transposed as [m][group][position
-// in quad][quad] (groups padded to 129 floats).  A warp
-// takes eight groups of a row at a time, four lanes per group: lane (g, q)
-// reads one 32-bit word of low nibbles and one 16-bit word of high bits (its
-// eight codes) and the group's scale, and looks each code up in a 64-entry
-// table of (activation offsets, trit masks); the eight groups then fall on
-// different banks, so the two kept activations of each quad are read without
-// conflicts whatever the pattern.  Each kept weight is one FMA with its trit
-// as an fp32 -1, 0 or 1 (exact products); a lane scales its eight quads' sum
-// by the group's fp16 scale and accumulates in fp32; the lanes are added by a
-// fixed xor tree and
-// the K slices by a second kernel in slice order, so results do not change
-// from call to call.
+// in quad][quad] (groups padded to 129 floats).  A warp takes eight groups of
+// a row at a time, four lanes per group: lane (g, q) reads one 32-bit word of
+// low nibbles and one 16-bit word of high bits (its eight codes) and the
+// group's scale, and looks each code up in two 64-entry tables (the two
+// activation offsets; the two trits as fp32 high halves).  The eight groups
+// fall on different banks, so the two kept activations of each quad are read
+// without conflicts whatever the pattern.  Each kept weight is one FMA with
+// its trit as an fp32 -1, 0 or 1 (exact products); a lane scales its eight
+// quads' sum by the group's fp16 scale and accumulates in fp32; the lanes are
+// added by a fixed xor tree and the K slices by a second kernel in slice
+// order, so results do not change from call to call.
 #include <algorithm>
 
 #include "tq_internal.h"
@@ -151,33 +150,35 @@ struct SGParams {
 // reads at once then fall on different banks)
 constexpr int kXStride = 129;
 
-// code -> 32 i0 | (32 i1) << 8 | keep0 << 16 | neg0 << 17 | keep1 << 18 |
-// neg1 << 19 (keep: the trit is not 0; neg: it is -1); 54..63 -> all zero
-__device__ __forceinline__ uint32_t code_entry(uint32_t c) {
-  if (c >= 54) return 0u;
+// The two tables of a code c < 54 (pattern p = c / 9, trits t0, t1 at the
+// kept positions i0 < i1): offsets 32 i0 | (32 i1) << 16 of the two
+// activations (x' is stored [position][quad]); and the high halves of t0 and
+// t1 as fp32 (0xbf80 for -1, 0 for 0, 0x3f80 for 1; the low halves of these
+// values are zero), t0's in bits 16..31 and t1's in bits 0..15.  Codes 54..63
+// give trits 0 (offsets 0).
+__device__ __forceinline__ void code_tables(uint32_t c, uint32_t& off, uint32_t& tr) {
+  if (c >= 54) {
+    off = 0u;
+    tr = 0u;
+    return;
+  }
   const uint32_t pt = c / 9, v = c - 9 * pt, f0 = v / 3, f1 = v % 3;
   const uint32_t i0 = pt < 3 ? 0u : (pt < 5 ? 1u : 2u);
   const uint32_t i1 = pt < 3 ? pt + 1 : (pt < 5 ? pt - 1 : 3u);
-  return (32u * i0) | ((32u * i1) << 8) | ((f0 != 1u) << 16) | ((f0 == 0u) << 17) | ((f1 != 1u) << 18) |
-         ((f1 == 0u) << 19);
-}
-
-// the trit described by bits B (not 0) and B + 1 (-1) of e, as an fp32 -1, 0 or 1
-template <int B>
-__device__ __forceinline__ float trit_f32(uint32_t e) {
-  const uint32_t keep = 0u - ((e >> B) & 1u), neg = (e << (30 - B)) & 0x80000000u;
-  return __uint_as_float((0x3f800000u | neg) & keep);
+  auto hi16 = [](uint32_t f) { return f == 0u ? 0xbf80u : (f == 1u ? 0u : 0x3f80u); };
+  off = (32u * i0) | ((32u * i1) << 16);
+  tr = (hi16(f0) << 16) | hi16(f1);
 }
 
 template <int MB>
 __global__ void __launch_bounds__(32 * kGWarps) k_gemv_sparse24(const SGParams p) {
   extern __shared__ float xs[];  // [M][gs][kXStride]
-  __shared__ uint32_t tab[64];
+  __shared__ uint32_t tab_off[64], tab_tr[64];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = p.K / 128, g0 = (int64_t)blockIdx.y * p.gs;
   const int gn = (int)((G - g0) < p.gs ? (G - g0) : p.gs);
   const int M = p.M;
-  if (threadIdx.x < 64) tab[threadIdx.x] = code_entry(threadIdx.x);
+  if (threadIdx.x < 64) code_tables(threadIdx.x, tab_off[threadIdx.x], tab_tr[threadIdx.x]);
   pdl_wait();
   // the slice of x': xs[(m gs + gl) kXStride + 32 i + j] = x'[m][128 (g0 + gl) + 4 j + i]
   const int nx = M * gn * 128;
@@ -204,7 +205,8 @@ __global__ void __launch_bounds__(32 * kGWarps) k_gemv_sparse24(const SGParams p
       const bool on = gl < gn;
       const int gc = on ? gl : gn - 1;  // a lane past the slice reads group gn - 1 and adds zeros
       const uint8_t* gp = crow + 24 * gc;
-      const uint32_t lo = ld_in_u32(gp + 4 * q), hi = ld_in_u16(gp + 16 + 2 * q);
+      // past the slice: all codes 63, whose table entries are zero
+      const uint32_t lo = on ? ld_in_u32(gp + 4 * q) : 0xffffffffu, hi = on ? ld_in_u16(gp + 16 + 2 * q) : 0xffffu;
       const float sc = __half2float(__ushort_as_half(ld_in_u16(srow + gc)));
       float part[MB];
 #pragma unroll
@@ -212,10 +214,10 @@ __global__ void __launch_bounds__(32 * kGWarps) k_gemv_sparse24(const SGParams p
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const uint32_t c = ((lo >> (4 * jj)) & 15u) | (((hi >> (2 * jj)) & 3u) << 4);
-        const uint32_t e = on ? tab[c] : 0u;
+        const uint32_t off = tab_off[c], tr = tab_tr[c];
         const float* xq = xs + gc * kXStride + 8 * q + jj;
-        const uint32_t o0 = e & 0xffu, o1 = (e >> 8) & 0xffu;
-        const float t0 = trit_f32<16>(e), t1 = trit_f32<18>(e);
+        const uint32_t o0 = off & 0xffffu, o1 = off >> 16;
+        const float t0 = __uint_as_float(tr & 0xffff0000u), t1 = __uint_as_float(tr << 16);
 #pragma unroll
         for (int m = 0; m < MB; ++m) {
           if (m < M) {
