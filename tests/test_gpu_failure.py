@@ -106,3 +106,22 @@ def test_gemv_reports_activations_out_of_range(scale_exp):
     assert tq.lib().tq_device_fault() == tq.TQ_ERR_RANGE
     tq.gemv(c2, s, to_dev_bf16(xb), K)
     assert tq.lib().tq_device_fault() == tq.TQ_OK
+
+
+@pytest.mark.parametrize("N,K,M", [(5120, 27648, 1), (27648, 5120, 2)])
+def test_gemv_rotate_next_stall_reports_timeout_then_recovers(N, K, M):
+    """The chained form (rank 0 of each cluster reduces every row): the
+    stalled CTA is rank 0 of the first cluster, which its peers push all
+    their rows into; the launch still winds down, reports TQ_ERR_TIMEOUT, and
+    the next clean call reproduces y and x' bit for bit."""
+    W = synth.weights(N, K, 91, dtype="bf16")
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(synth.activations(M, K, 92))
+    ref_y, ref_xn = tq.gemv_rotate_next(c2, s, x, K)
+    tq.device_fault()
+    y, xn = tq.gemv_rotate_next(c2, s, x, K, flags=TQ_GEMV_TEST_STALL)
+    torch.cuda.synchronize()
+    assert tq.lib().tq_device_fault() == tq.TQ_ERR_TIMEOUT
+    y2, xn2 = tq.gemv_rotate_next(c2, s, x, K)
+    tq.device_fault()
+    assert torch.equal(y2, ref_y) and torch.equal(xn2, ref_xn)
