@@ -217,44 +217,6 @@ struct Raw16 {
   uint4 w[XT == TQ_F32 ? 4 : 2];
 };
 
-__device__ __forceinline__ void fwht128_x16(float v[16], int lane) {
-#pragma unroll
-  for (int j = 0; j < 16; j += 2) {  // h = 1
-    const float a = v[j], b = v[j + 1];
-    v[j] = a + b;
-    v[j + 1] = a - b;
-  }
-  uint64_t q[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = f2_pack(v[2 * i], v[2 * i + 1]);
-#pragma unroll
-  for (int hp = 1; hp < 8; hp <<= 1) {  // h = 2, 4, 8 on pairs
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if ((i & hp) == 0) {
-        const uint64_t a = q[i], b = q[i + hp];
-        q[i] = f2_add(a, b);
-        q[i + hp] = f2_sub(a, b);
-      }
-    }
-  }
-#pragma unroll
-  for (int m = 1; m < 8; m <<= 1) {  // h = 16, 32, 64: lower lane a + b, upper lane a - b
-    const float sgn = (lane & m) ? -1.0f : 1.0f;
-    const uint64_t sg = f2_pack(sgn, sgn);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float lo, hi;
-      f2_unpack(q[i], lo, hi);
-      const float olo = __shfl_xor_sync(kFull, lo, m), ohi = __shfl_xor_sync(kFull, hi, m);
-      q[i] = f2_fma(sg, q[i], f2_pack(olo, ohi));
-    }
-  }
-  const uint64_t sc = f2_pack(kInvSqrt128, kInvSqrt128);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) f2_unpack(f2_mul(q[i], sc), v[2 * i], v[2 * i + 1]);
-}
-
 template <int YT, bool PERM16>
 __device__ __forceinline__ void store16(void* y, int64_t off, const float v[16], uint32_t* flag, bool valid) {
   if (!valid) return;

@@ -16,10 +16,11 @@
 // 2 (j % 4) of byte 16 + j / 4 (bytes 16..23).  Codes 54..63 are not written
 // by the quantiser; the GEMV reads them as a quad of zeros.
 //
-// k_quantize_sparse24: one CTA per row, a warp per group at a time; the
-// staged FWHT-128, the selection, the 64-value halving tree and the division
-// follow the definition step by step, so codes and scales are bit-exact with
-// it.  Lane l owns quad l; the code bytes are assembled with OR shuffles.
+// k_quantize_sparse24: an 8-lane group per 128-weight group, lane q holding
+// weights 16q .. 16q + 15 (quads 4q .. 4q + 3) in registers: the staged
+// FWHT-128 (stages h = 1 .. 8 in the lane, h = 16 .. 64 as shuffles), the
+// selection, the 64-value halving tree and the ternarisation give codes and
+// scales bit-exact with the definition.
 //
 // k_gemv_sparse24: decode with the pruned weights skipped.  A pre-pass
 // rotates x into an fp32 workspace; a CTA owns one slice of the K groups and
@@ -37,6 +38,7 @@
 // added by a fixed xor tree and the K slices by a second kernel in slice
 // order, so results do not change from call to call.
 #include <algorithm>
+#include <atomic>
 
 #include "tq_internal.h"
 
@@ -57,71 +59,102 @@ struct SQParams {
   int64_t lds;
 };
 
-// pattern index of the kept positions i0 < i1
-__device__ __forceinline__ int pattern24(int i0, int i1) { return i0 == 0 ? i1 - 1 : (i0 == 1 ? i1 + 1 : 5); }
+// One quad: the two positions of largest |w'| (a tie to the lower index),
+// its pattern index (kept positions (0,1) (0,2) (0,3) (1,2) (1,3) (2,3) ->
+// 0..5) and the kept values in position order.  Position o beats i > o when
+// |w_o| >= |w_i|; that is a strict total order, so the positions that beat at
+// least two others are exactly the two largest.
+__device__ __forceinline__ int select24(const float* w, float& k0, float& k1) {
+  const float a0 = fabsf(w[0]), a1 = fabsf(w[1]), a2 = fabsf(w[2]), a3 = fabsf(w[3]);
+  const int g01 = a0 >= a1, g02 = a0 >= a2, g03 = a0 >= a3;
+  const int g12 = a1 >= a2, g13 = a1 >= a3, g23 = a2 >= a3;
+  const bool keep0 = g01 + g02 + g03 >= 2, keep1 = (1 - g01) + g12 + g13 >= 2;
+  const bool keep2 = (2 - g02 - g12) + g23 >= 2, keep3 = 3 - g03 - g13 - g23 >= 2;
+  const int i0 = keep0 ? 0 : (keep1 ? 1 : 2);
+  const int i1 = keep3 ? 3 : (keep2 ? 2 : 1);
+  k0 = keep0 ? w[0] : (keep1 ? w[1] : w[2]);
+  k1 = keep3 ? w[3] : (keep2 ? w[2] : w[1]);
+  return i0 == 0 ? i1 - 1 : (i0 == 1 ? i1 + 1 : 5);
+}
 
-// o beats i: larger magnitude, or equal magnitude and lower index
-__device__ __forceinline__ bool beats(const float* a, int o, int i) { return a[o] > a[i] || (a[o] == a[i] && o < i); }
-
-__global__ void __launch_bounds__(32 * kQWarps) k_quantize_sparse24(const SQParams p) {
-  __shared__ float sv[kQWarps][128];
-  __shared__ float ss[kQWarps][64];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t n = blockIdx.x, G = p.K / 128;
-  float* v = sv[warp];
-  float* s = ss[warp];
+__global__ void __launch_bounds__(32 * kQWarps, 4) k_quantize_sparse24(const SQParams p) {
+  const int lane = threadIdx.x & 31, q = lane & 7;
+  const int64_t G = p.K / 128, units = p.N * G;
+  const int64_t wid = ((int64_t)blockIdx.x * (32 * kQWarps) + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * (32 * kQWarps)) >> 5;
   pdl_wait();
-  for (int64_t g = warp; g < G; g += kQWarps) {
+  // a warp takes four consecutive units (row-major groups) at a time; the
+  // 8-lane group j = lane / 8 takes unit 4 i + j, lane q of it holding
+  // weights 16q .. 16q + 15 (quads 4q .. 4q + 3)
+  for (int64_t u0 = 4 * wid; u0 < units; u0 += 4 * nw) {
+    const int64_t u = u0 + (lane >> 3);
+    const bool live = u < units;
+    const int64_t n = live ? u / G : 0, g = live ? u - n * G : 0;
+    float v[16];
     if (p.wt == TQ_F32) {
-      const float* w = static_cast<const float*>(p.W) + n * p.ldw + 128 * g;
-      for (int i = lane; i < 128; i += 32) v[i] = w[i];
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.W) + n * p.ldw + 128 * g + 16 * q);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 f = live ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+      }
     } else {
-      const uint16_t* w = static_cast<const uint16_t*>(p.W) + n * p.ldw + 128 * g;
-      for (int i = lane; i < 128; i += 32) v[i] = __uint_as_float((uint32_t)w[i] << 16);
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.W) + n * p.ldw + 128 * g + 16 * q);
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      bf16x8_to_f32(live ? src[0] : z, v);
+      bf16x8_to_f32(live ? src[1] : z, v + 8);
     }
-    __syncwarp();
-    fwht_warp(v, 128, kInvSqrt128, lane);
-    // quad `lane`: the best position under "beats", then the best of the rest
-    float w[4], a[4];
+    fwht128_x16(v, lane);  // the staged FWHT-128 and the normalisation
+    float k[8];
+    int pat[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      w[i] = v[4 * lane + i];
-      a[i] = fabsf(w[i]);
+    for (int r = 0; r < 4; ++r) pat[r] = select24(v + 4 * r, k[2 * r], k[2 * r + 1]);
+    // the 64 kept magnitudes in k order (lane q: kept[8q .. 8q + 7]) by the
+    // halving tree s[i] += s[i + h], h = 32 .. 1: h = 32, 16, 8 pair lane q
+    // with q + 4, q + 2, q + 1 (both lanes form the same IEEE sums), h = 4, 2,
+    // 1 stay in the lane
+    uint64_t t[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) t[i] = f2_pack(fabsf(k[2 * i]), fabsf(k[2 * i + 1]));
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float lo, hi;
+        f2_unpack(t[i], lo, hi);
+        t[i] = f2_add(t[i], f2_pack(__shfl_xor_sync(kFull, lo, m), __shfl_xor_sync(kFull, hi, m)));
+      }
     }
-    int b0 = 0;
-#pragma unroll
-    for (int i = 1; i < 4; ++i)
-      if (beats(a, i, b0)) b0 = i;
-    int b1 = b0 == 0 ? 1 : 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (i != b0 && i != b1 && beats(a, i, b1)) b1 = i;
-    const int i0 = b0 < b1 ? b0 : b1, i1 = b0 < b1 ? b1 : b0;
-    // the 64 kept magnitudes in k order: quad l holds kept[2l], kept[2l + 1]
-    s[2 * lane] = a[i0];
-    s[2 * lane + 1] = a[i1];
-    __syncwarp();
-    for (int h = 32; h >= 1; h >>= 1) {
-      if (lane < h) s[lane] = __fadd_rn(s[lane], s[lane + h]);
-      __syncwarp();
-    }
-    const uint16_t sb = __half_as_ushort(__float2half_rn(__fmul_rn(s[0], 0.015625f)));
+    t[0] = f2_add(t[0], t[2]);  // h = 4
+    t[1] = f2_add(t[1], t[3]);
+    t[0] = f2_add(t[0], t[1]);  // h = 2
+    float s0, s1;
+    f2_unpack(t[0], s0, s1);
+    const float ssum = __shfl_sync(kFull, __fadd_rn(s0, s1), lane & 24);  // h = 1, from lane q = 0
+    const uint16_t sb = __half_as_ushort(__float2half_rn(__fmul_rn(ssum, 0.015625f)));
     const float sc = __half2float(__ushort_as_half(sb));
-    const int t0 = ternarise(w[i0], sc), t1 = ternarise(w[i1], sc);
-    const uint32_t c = (uint32_t)(9 * pattern24(i0, i1) + 3 * (t0 + 1) + (t1 + 1));
-    // low nibbles: word q (bytes 4q ..) holds codes 8q .. 8q + 7; high bits:
-    // word q (bytes 16 + 4q ..) holds codes 16q .. 16q + 15
-    uint32_t lo = (c & 15u) << (4 * (lane & 7));
-    uint32_t hi = (c >> 4) << (2 * (lane & 15));
+    // t = sign(w') [|w'| > s/2] for a finite s > 0, 0 for s = 0, inf or NaN:
+    // the same values as clamp(rint(w' / s), -1, 1) with IEEE division and
+    // ties to even (the quotient rounds above 1/2 exactly when |w'| > s/2)
+    const float thr = (sc != 0.0f) ? __fmul_rn(sc, 0.5f) : __int_as_float(0x7f800000);
+    uint32_t lo = 0u, hi = 0u;
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) lo |= __shfl_xor_sync(0xffffffffu, lo, o);
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) hi |= __shfl_xor_sync(0xffffffffu, hi, o);
-    uint8_t* gp = p.codes + n * p.ldc + 24 * g;
-    if ((lane & 7) == 0) *reinterpret_cast<uint32_t*>(gp + (lane >> 1)) = lo;
-    if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(gp + 16 + (lane >> 2)) = hi;
-    if (lane == 0) p.scales[n * p.lds + g] = sb;
-    __syncwarp();  // v and s are refilled for the next group
+    for (int r = 0; r < 4; ++r) {
+      const int t0 = (int)(k[2 * r] > thr) - (int)(k[2 * r] < -thr);
+      const int t1 = (int)(k[2 * r + 1] > thr) - (int)(k[2 * r + 1] < -thr);
+      const uint32_t c = (uint32_t)(9 * pat[r] + 3 * (t0 + 1) + (t1 + 1));
+      lo |= (c & 15u) << (4 * r);  // codes 4q .. 4q + 3: low nibbles in bytes 2q, 2q + 1
+      hi |= (c >> 4) << (2 * r);   // high bits in byte 16 + q
+    }
+    if (live) {
+      uint8_t* gp = p.codes + n * p.ldc + 24 * g;
+      *reinterpret_cast<uint16_t*>(gp + 2 * q) = (uint16_t)lo;
+      gp[16 + q] = (uint8_t)hi;
+      if (q == 0) p.scales[n * p.lds + g] = sb;
+    }
   }
   pdl_launch_dependents();
 }
@@ -294,6 +327,28 @@ cudaError_t set_smem_once(int bytes) {
   return cudaSuccess;
 }
 
+// CTAs of k_gemv_sparse24<MB> resident per SM with `kb` KB of dynamic shared
+// memory, queried once per device and size (a host query, kept off the
+// per-call path)
+template <int MB>
+cudaError_t occupancy_of(int kb, int* occ) {
+  constexpr int kMaxKb = kSliceBytes / 1024 + 1;
+  static std::atomic<int> cache[64][kMaxKb + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || kb < 0 || kb > kMaxKb)
+    return cudaErrorInvalidValue;
+  int v = cache[dev][kb].load(std::memory_order_relaxed);
+  if (v == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_gemv_sparse24<MB>, 32 * kGWarps,
+                                                                  (size_t)kb * 1024);
+    if (e != cudaSuccess) return e;
+    if (v < 1) v = 1;
+    cache[dev][kb].store(v, std::memory_order_relaxed);
+  }
+  *occ = v;
+  return cudaSuccess;
+}
+
 template <int MB>
 cudaError_t launch_gemv_mb(const SGParams& p, int64_t row_blocks, cudaStream_t s) {
   const int smem = p.M * p.gs * kXStride * (int)sizeof(float);
@@ -302,7 +357,7 @@ cudaError_t launch_gemv_mb(const SGParams& p, int64_t row_blocks, cudaStream_t s
   // as many CTAs as fit on the SMs at once (over all slices), each taking
   // row blocks in turn after staging its slice of x' once
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_gemv_sparse24<MB>, 32 * kGWarps, (size_t)smem);
+  e = occupancy_of<MB>((smem + 1023) / 1024, &occ);
   if (e != cudaSuccess) return e;
   const int64_t per_slice = std::max<int64_t>(1, (int64_t)std::max(occ, 1) * device_sm_count() / p.nsl);
   const int64_t grid_x = std::min<int64_t>(row_blocks, per_slice);
@@ -341,7 +396,10 @@ cudaError_t launch_quantize_sparse24(const void* W, int wt, int64_t N, int64_t K
   if (N == 0) return cudaSuccess;
   if (N > 0x7fffffffll) return cudaErrorNotSupported;
   SQParams p{W, wt, N, K, ldw, codes, ldc, scales, lds};
-  return launch_pdl(k_quantize_sparse24, dim3((unsigned)N), dim3(32 * kQWarps), 0, s, p);
+  // four groups per warp at a time; four CTAs of eight warps per SM
+  const int64_t units = N * (K / 128);
+  const int64_t grid = std::min<int64_t>((units + 4 * kQWarps - 1) / (4 * kQWarps), (int64_t)device_sm_count() * 4);
+  return launch_pdl(k_quantize_sparse24, dim3((unsigned)grid), dim3(32 * kQWarps), 0, s, p);
 }
 
 cudaError_t launch_gemv_sparse24(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,

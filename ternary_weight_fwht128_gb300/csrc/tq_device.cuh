@@ -120,6 +120,47 @@ __device__ __forceinline__ void fwht128_x8(float v[8], int lane) {
   for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(q[i], sc), v[2 * i], v[2 * i + 1]);
 }
 
+// FWHT-128 on an 8-lane group: lane p (= lane & 7) holds elements
+// 16p .. 16p+15 of the block; stages h = 1 .. 8 in registers (2 .. 8 on
+// f32x2 pairs), h = 16, 32, 64 across lanes, then the normalisation.
+__device__ __forceinline__ void fwht128_x16(float v[16], int lane) {
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {  // h = 1
+    const float a = v[j], b = v[j + 1];
+    v[j] = a + b;
+    v[j + 1] = a - b;
+  }
+  uint64_t q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) q[i] = f2_pack(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int hp = 1; hp < 8; hp <<= 1) {  // h = 2, 4, 8 on pairs
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & hp) == 0) {
+        const uint64_t a = q[i], b = q[i + hp];
+        q[i] = f2_add(a, b);
+        q[i + hp] = f2_sub(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {  // h = 16, 32, 64: lower lane a + b, upper lane a - b
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
+    const uint64_t sg = f2_pack(sgn, sgn);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float lo, hi;
+      f2_unpack(q[i], lo, hi);
+      const float olo = __shfl_xor_sync(kFull, lo, m), ohi = __shfl_xor_sync(kFull, hi, m);
+      q[i] = f2_fma(sg, q[i], f2_pack(olo, ohi));
+    }
+  }
+  const uint64_t sc = f2_pack(kInvSqrt128, kInvSqrt128);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) f2_unpack(f2_mul(q[i], sc), v[2 * i], v[2 * i + 1]);
+}
+
 // Eight consecutive bf16 (as a 128-bit word) -> fp32.
 __device__ __forceinline__ void bf16x8_to_f32(uint4 w, float v[8]) {
   v[0] = __uint_as_float(w.x << 16);
