@@ -81,11 +81,22 @@ def test_quantize_sparse24_special_rows(sp):
 
 
 def test_quantize_sparse24_codes_valid(sp):
+    """The codes equal the oracle's, whose masks keep two of every four."""
     W = synth.weights(64, 1280, 11, dtype="bf16")
     codes, _ = tq.quantize_pack_sparse24(_dev(W))
-    T, KEEP, bad = sp.unpack(codes.cpu().numpy(), 1280)
-    assert bad == 0
+    T, KEEP, _ = sp.quantize(W)
     assert np.all(KEEP.reshape(-1, 4).sum(1) == 2)
+    assert np.array_equal(codes.cpu().numpy(), sp.pack(T, KEEP))
+
+
+def _oracle_codes(sp, W, rows, codes, scales):
+    """The oracle's codes and scales of W (rows: a sample); the GPU's, which
+    the kernels under test read, must equal them bit for bit."""
+    T, KEEP, S = sp.quantize(W, rows)
+    c = sp.pack(T, KEEP)
+    sel = slice(None) if rows is None else torch.as_tensor(rows, device="cuda")
+    assert np.array_equal(codes[sel].cpu().numpy(), c) and np.array_equal(u16(scales[sel]), S)
+    return c, S
 
 
 def _gemv_case(sp, N, K, M, seed, rows=None):
@@ -96,10 +107,7 @@ def _gemv_case(sp, N, K, M, seed, rows=None):
     y = tq.gemv_sparse24(codes, scales, to_dev_bf16(xb), K, out=out)
     torch.cuda.synchronize()
     check()
-    c = codes.cpu().numpy()
-    S = u16(scales)
-    if rows is not None:
-        c, S = c[rows], S[rows]
+    c, S = _oracle_codes(sp, W, rows, codes, scales)
     ref = sp.gemv(c, S, synth.bf16_bits_to_f32(xb), K)
     got = out.cpu().numpy() if rows is None else out.cpu().numpy()[:, rows]
     check_y(got, ref)
@@ -133,18 +141,20 @@ def test_gemv_sparse24_repeatable():
 
 
 def test_gemv_sparse24_invalid_codes_read_as_zero(sp):
-    """Quads whose code is 54..63 contribute nothing (documented behaviour)."""
+    """Quads whose code is 54..63 contribute nothing (documented behaviour):
+    the oracle's codes with one quad set to code 63, on both sides."""
     N, K, M = 64, 256, 2
     W = synth.weights(N, K, 21, dtype="bf16")
-    codes, scales = tq.quantize_pack_sparse24(_dev(W))
-    c = codes.cpu().numpy().copy()
+    T0, KEEP0, S = sp.quantize(W)
+    c = sp.pack(T0, KEEP0).copy()
     c[5, 0] |= 0x0F   # quad 0 of row 5: low nibble 15 ...
     c[5, 16] |= 0x03  # ... and high bits 3: code 63
     xb = synth.activations(M, K, 22)
+    scales = torch.from_numpy(S.view(np.int16)).cuda()
     y = tq.gemv_sparse24(torch.from_numpy(c).cuda(), scales, to_dev_bf16(xb), K)
     T, KEEP, bad = sp.unpack(c, K)
     assert bad == 1
-    ref = oracle.load().gemv(T, u16(scales), synth.bf16_bits_to_f32(xb))
+    ref = oracle.load().gemv(T, S, synth.bf16_bits_to_f32(xb))
     check_y(y.cpu().numpy(), ref)
 
 
@@ -178,10 +188,7 @@ def _gemm_case(sp, N, K, M, seed, rows=None):
     torch.cuda.synchronize()
     check()
     tq.gemm_check_range(ws)
-    c = codes.cpu().numpy()
-    S = u16(scales)
-    if rows is not None:
-        c, S = c[rows], S[rows]
+    c, S = _oracle_codes(sp, W, rows, codes, scales)
     ref = sp.gemv(c, S, synth.bf16_bits_to_f32(xb), K)
     got = out.cpu().numpy() if rows is None else out.cpu().numpy()[:, rows]
     check_y(got, ref)
@@ -202,14 +209,21 @@ def test_gemm_sparse24_full_size_sampled(sp, N, K):
     _gemm_case(sp, N, K, 2048, seed=N + K + 13, rows=rows)
 
 
-def test_gemm_sparse24_repeatable_and_matches_gemv():
+def test_gemm_sparse24_repeatable_and_gemv_agree(sp):
+    """Repeated prefill calls give identical bits; the GEMM (fp16 x') and the
+    GEMV (fp32 x') on the same skinny input are both within the tolerance of
+    the oracle."""
     N, K, M = 1000, 2560, 8
     W = synth.weights(N, K, 31, dtype="bf16")
+    xb = synth.activations(M, K, 32)
     codes, scales = tq.quantize_pack_sparse24(_dev(W))
-    x = to_dev_bf16(synth.activations(M, K, 32))
+    x = to_dev_bf16(xb)
     ys = [tq.gemm_sparse24(codes, scales, x, K) for _ in range(5)]
+    yv = tq.gemv_sparse24(codes, scales, x, K)
     torch.cuda.synchronize()
     for y in ys[1:]:
         assert torch.equal(y, ys[0])
-    # the GEMM (fp16 x') and the GEMV (fp32 x') agree within the tolerance
-    check_y(ys[0].cpu().numpy(), tq.gemv_sparse24(codes, scales, x, K).cpu().numpy().astype(np.float64))
+    c, S = _oracle_codes(sp, W, None, codes, scales)
+    ref = sp.gemv(c, S, synth.bf16_bits_to_f32(xb), K)
+    check_y(ys[0].cpu().numpy(), ref, "gemm")
+    check_y(yv.cpu().numpy(), ref, "gemv")
