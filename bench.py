@@ -619,9 +619,10 @@ def layout_bench(tq, torch, dev, pk, gen) -> list:
 
 def sparse24_bench(tq, torch, dev, pk, gen) -> dict:
     """The 2:4-sparse ternary format: quantise + pack (bf16 in), and the
-    zero-skipping GEMV on the decode shapes (M = 1 and 16), cycling over 8
-    copies of the codes so each launch streams from HBM.  GB/s counts the
-    sparse codes and scales (26 bytes per 128 weights) of one launch."""
+    GEMV on the decode shapes (M = 1 and 16; the tensor-memory kernel, the
+    codes expanded through a table), cycling over 8 copies of the codes so
+    each launch streams from HBM.  GB/s counts the sparse codes and scales
+    (26 bytes per 128 weights) of one launch."""
     out = {"bits_per_weight": 1.625}
     try:
         W = (torch.randn(HIDDEN, HIDDEN, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
@@ -654,8 +655,11 @@ def sparse24_bench(tq, torch, dev, pk, gen) -> dict:
                     run()
                 ms = time_events(run, 3 * len(copies), torch)
                 gb = nbytes / (ms * 1e-3) / 1e9
+                path = tq.gemv_sparse24_path(N, K, M)
                 out[f"gemv_M{M}_{N}x{K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gb, 1),
-                                             "frac_of_peak": round(gb / pk["hbm_gbs"], 4), "bytes": nbytes}
+                                             "frac_of_peak": round(gb / pk["hbm_gbs"], 4), "bytes": nbytes,
+                                             "kernel": "k_gemv_tc (2:4 codes)" if path == tq.TQ_GEMV_TENSOR_MEMORY
+                                             else "k_gemv_sparse24 (CUDA cores)"}
             del copies
         # prefill M = 2048: dense fp16 MMAs on the expanded tiles (2 M N K flops)
         M = 2048

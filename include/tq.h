@@ -189,7 +189,7 @@ TQ_API tq_status tq_gemv_rotate_next(const uint8_t *codes, int64_t ldc, int fmt,
  * Queries device properties of the current device on first use.  Returns
  * -TQ_ERR_INVALID_ARG / -TQ_ERR_SHAPE for arguments tq_gemv would reject
  * with those codes. */
-enum { TQ_GEMV_TENSOR_MEMORY = 1, TQ_GEMV_MMA_SYNC = 2 };
+enum { TQ_GEMV_TENSOR_MEMORY = 1, TQ_GEMV_MMA_SYNC = 2, TQ_GEMV_CUDA_CORES = 3 };
 TQ_API int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt);
 
 /* Bytes of caller-provided workspace tq_gemm needs for M x K activations:
@@ -403,18 +403,34 @@ TQ_API tq_status tq_quantize_pack_sparse24(const void *W, int wt, int64_t N, int
 TQ_API size_t tq_gemv_sparse24_workspace_bytes(int64_t N, int64_t K, int64_t M);
 
 /* y [M][N] fp32 = sum_g s[n][g] sum_{k in g} t[n][k] x'[m][k] over the 2:4
- * codes, x bf16 [M][K] (16-byte aligned rows), M = 1..16: a pre-pass writes
- * x' = FWHT-128(x) in fp32 to the workspace, then a decode kernel adds only
- * the kept weights (sign-select adds, fp32 accumulation, each group's sum
- * scaled by its fp16 scale), and, when K is split, a third kernel adds the
- * slices in order.  Results are identical from call to call.  ws_bytes >=
- * tq_gemv_sparse24_workspace_bytes(N, K, M); the workspace must not overlap
- * the other arguments.  The codes are read as 32-bit words: 4-byte aligned
- * codes pointer and ldc % 4 == 0.  Codes outside 0..53 are read as a quad of
- * zeros. */
+ * codes, x bf16 [M][K] (16-byte aligned rows), M = 1..16.  Two kernels:
+ *   - the tensor-memory GEMV of tq_gemv (TQ_GEMV_TENSOR_MEMORY, see
+ *     tq_gemv_sparse24_path) when the codes are 16-byte aligned with
+ *     ldc % 16 == 0 and K / 128 is even and at least 4: each quad's code
+ *     expands through a table into its four weights as fp8 bytes in tensor
+ *     memory (the pruned ones as zeros), x' is carried as the three e4m3
+ *     pieces of tq_gemv, and one launch does the rest (the workspace is not
+ *     used);
+ *   - otherwise (TQ_GEMV_CUDA_CORES) a pre-pass writes x' = FWHT-128(x) in
+ *     fp32 to the workspace, a decode kernel adds only the kept weights
+ *     (sign-select adds, fp32 accumulation, each group's sum scaled by its
+ *     fp16 scale), and, when K is split, a third kernel adds the slices in
+ *     order.
+ * Results are identical from call to call.  ws_bytes >=
+ * tq_gemv_sparse24_workspace_bytes(N, K, M) in both cases; the workspace must
+ * not overlap the other arguments.  The codes are read as 32-bit words at
+ * least: 4-byte aligned codes pointer and ldc % 4 == 0.  Codes outside 0..53
+ * are read as a quad of zeros. */
 TQ_API tq_status tq_gemv_sparse24(const uint8_t *codes, int64_t ldc, const uint16_t *scales, int64_t lds,
                                   int64_t N, int64_t K, const uint16_t *x, int64_t ldx, int64_t M, float *y,
                                   int64_t ldy, void *workspace, size_t ws_bytes, tq_stream stream);
+
+/* Which kernel tq_gemv_sparse24 runs for a shape whose codes are 16-byte
+ * aligned with ldc % 16 == 0 (introspection; launches nothing; queries the
+ * current device on first use): TQ_GEMV_TENSOR_MEMORY or TQ_GEMV_CUDA_CORES.
+ * -TQ_ERR_INVALID_ARG / -TQ_ERR_SHAPE for arguments tq_gemv_sparse24 would
+ * reject with those codes. */
+TQ_API int tq_gemv_sparse24_path(int64_t N, int64_t K, int64_t M);
 
 /* Prefill GEMM of the 2:4 codes: tq_gemm on the tcgen05 tensor cores with
  * the 2:4 codes, M >= 1 rows of bf16 x.  The pruned weights are expanded

@@ -34,8 +34,9 @@ EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_
             "tq_device_fault", "tq_gemm_noalloc", "tq_layout_codes_ld", "tq_layout_scales_ld", "tq_fwht",
             "tq_quantize_pack_layout", "tq_gemv_layout", "tq_gemm_workspace_bytes_layout", "tq_gemm_layout",
             "tq_gemm_rotate_next", "tq_sparse24_ld", "tq_quantize_pack_sparse24",
-            "tq_gemv_sparse24_workspace_bytes", "tq_gemv_sparse24", "tq_gemm_sparse24", "tq_gemv_rotate_next")
-TQ_GEMV_TENSOR_MEMORY, TQ_GEMV_MMA_SYNC = 1, 2
+            "tq_gemv_sparse24_workspace_bytes", "tq_gemv_sparse24", "tq_gemm_sparse24", "tq_gemv_rotate_next",
+            "tq_gemv_sparse24_path")
+TQ_GEMV_TENSOR_MEMORY, TQ_GEMV_MMA_SYNC, TQ_GEMV_CUDA_CORES = 1, 2, 3
 TQ_GEMV_WEIGHTS_READY = 1
 TQ_GEMV_X_ROTATED = 2
 TQ_GEMM_REUSE_ROTATED = 1
@@ -138,6 +139,8 @@ def lib() -> ctypes.CDLL:
         L.tq_gemv_sparse24.restype = _int
         L.tq_gemv_sparse24.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp,
                                        ctypes.c_size_t, _vp]
+        L.tq_gemv_sparse24_path.restype = _int
+        L.tq_gemv_sparse24_path.argtypes = [_i64, _i64, _i64]
         _lib = L
     return _lib
 
@@ -496,3 +499,8 @@ def gemv_rotate_next(codes: torch.Tensor, scales: torch.Tensor, x: torch.Tensor,
                                    xnext.data_ptr(), xnext.stride(0), _stream(stream))
     _check(st, "tq_gemv_rotate_next")
     return out, xnext
+
+
+def gemv_sparse24_path(N: int, K: int, M: int = 1) -> int:
+    """TQ_GEMV_TENSOR_MEMORY or TQ_GEMV_CUDA_CORES (tq_gemv_sparse24_path)."""
+    return lib().tq_gemv_sparse24_path(N, K, M)

@@ -56,6 +56,9 @@
 // add nothing.  Digits are e4m3 bytes d * 2^-9 (no 4c class), and
 // sum_k t x = sum_k d x - sum_k x as before.
 //
+// The 2:4-sparse codes (tq_gemv_sparse24) take the 2-bit pipeline with a
+// table-driven unpack into natural-order columns (see the SP instance below).
+//
 // Work split: a cluster of kcl CTAs owns a range of 128-row tiles; CTA rank r
 // owns the r-th slice of the K groups and rotates only that slice of x.  A
 // CTA walks (tile, four-group) stages with four warp roles that hand buffers
@@ -470,13 +473,44 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ct
   return false;
 }
 
+// The 2:4-sparse codes (SP): a group of 128 weights is 24 code bytes (16
+// bytes of low nibbles, 8 of high bit pairs; one 6-bit code per quad of four
+// consecutive k: pattern and two trits), a stage of four groups 96 bytes per
+// row, copied without swizzle.  Each code becomes one 32-bit tensor-memory
+// column -- the quad's four weights as e4m3 bytes c * 2^-9, c = t + 1 (1 for
+// the pruned positions and for the codes 54..63 the quantiser never writes)
+// -- through a 64-entry table replicated for every lane (lane l reads copy l,
+// so the 32 lookups of a warp fall on 32 banks).  The columns then hold k in
+// natural order, and the prologue writes x' bytes in natural order too (no
+// odd-class scaling).
+constexpr int kSpTabBytes = 64 * 32 * 4;
+
+__host__ __device__ constexpr uint32_t sp24_word(uint32_t c) {
+  if (c >= 54) return 0x01010101u;
+  const uint32_t p = c / 9, r = c % 9;
+  const uint32_t i0 = p < 3 ? 0u : (p < 5 ? 1u : 2u);
+  const uint32_t i1 = p == 0 ? 1u : (p == 1 ? 2u : (p == 2 ? 3u : (p == 3 ? 2u : 3u)));
+  uint32_t w = 0x01010101u;
+  w = (w & ~(0xffu << (8 * i0))) | ((r / 3) << (8 * i0));
+  w = (w & ~(0xffu << (8 * i1))) | ((r % 3) << (8 * i1));
+  return w;
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
 // Shared memory (1024-aligned): [code ring][B: groups_cap x kGroupB][zeros kZeroBytes]
-// [ztab: groups_cap x kZs x {pw Zt, pw}][partial sums: tiles_cap x kcl x M x 128 / kcl][Ctl]
+// [ztab: groups_cap x kZs x {pw Zt, pw}][partial sums: tiles_cap x kcl x M x 128 / kcl]
+// [SP: code table, kSpTabBytes][Ctl]
 // LAYOUT: the layout variants' parameters (blk, lgs, g_rot) and the chained
 // decode (xr, xnext) are read; without it the kernel is compiled for the
 // method's own layout only.
-template <int V, bool B3, bool LAYOUT>
+template <int V, bool B3, bool LAYOUT, bool SP = false>
 __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__ CUtensorMap cmap, const Params p) {
+  static_assert(!SP || (!B3 && !LAYOUT), "2:4 codes: the method's own layout only");
   using Gm = Geo<V, B3>;
   using Fg = FmtGeo<B3>;
   constexpr int kGS = Fg::kGS, kAbuf = Fg::kAbuf, kAPeriod = Fg::kAPeriod;
@@ -487,7 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   unsigned char* zero = bsm + p.groups_cap * Gm::kGroupB;
   float2* ztab = reinterpret_cast<float2*>(zero + kZeroBytes);
   float* ypart = reinterpret_cast<float*>(ztab + p.groups_cap * Gm::kZs);
-  Ctl* ctl = reinterpret_cast<Ctl*>(ypart + p.ypart_floats);
+  uint32_t* sptab = reinterpret_cast<uint32_t*>(ypart + p.ypart_floats);
+  Ctl* ctl = reinterpret_cast<Ctl*>(reinterpret_cast<unsigned char*>(sptab) + (SP ? kSpTabBytes : 0));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -503,14 +538,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     const int64_t nst = (G + 4) / 5;
     g0 = 5 * ((nst * rank) >> lgk);
     g1 = std::min<int64_t>(5 * ((nst * (rank + 1)) >> lgk), G);
+  } else if constexpr (SP) {
+    // slices of whole group pairs (G is even): a stage then starts at a
+    // multiple of 48 code bytes, which the copy engine needs (16)
+    g0 = 2 * (((G / 2) * rank) >> lgk);
+    g1 = 2 * (((G / 2) * (rank + 1)) >> lgk);
   } else {
     g0 = (G * rank) >> lgk;
     g1 = (G * (rank + 1)) >> lgk;
   }
   const int ng = (int)(g1 - g0), nch = (ng + kGS - 1) / kGS;
+  // bytes one stage's copy delivers: 128 rows x 128 code bytes (96 for 2:4 codes)
+  constexpr uint32_t kStageTx = SP ? 128u * 96u : (uint32_t)kSlotBytes;
   // TMA x (bytes) of stage lc of the slice
   auto stage_x = [&](int lc) -> int {
-    return B3 ? (int)((g0 / 5 + lc) * 128) : (int)((g0 + 4 * lc) * 32);
+    return B3 ? (int)((g0 / 5 + lc) * 128) : (int)((g0 + 4 * lc) * (SP ? 24 : 32));
   };
   const int64_t T = (p.N + 127) / 128;
   int64_t t0, t1;
@@ -535,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     for (; issued_loads < S && issued_loads < kRing; ++issued_loads) {
       const int l = issued_loads, tile = l / nch, lc = l - tile * nch;
       if (l == 0 && (int)blockIdx.x == p.stall_cta) continue;  // failure-path test: never arrives
-      mbar_arrive_expect_tx(&ctl->full[l], kSlotBytes);
+      mbar_arrive_expect_tx(&ctl->full[l], kStageTx);
       tma_load_2d(smem_u32(ring + l * kSlotBytes), &cmap, stage_x(lc), (int)((t0 + tile) * 128), &ctl->full[l]);
     }
   };
@@ -574,6 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     const int n16 = (p.groups_cap * Gm::kGroupB + kZeroBytes) / 16;
     for (int i = threadIdx.x; i < n16; i += kThreads) z4[i] = make_uint4(0, 0, 0, 0);
     for (int i = threadIdx.x; i < p.groups_cap * Gm::kZs; i += kThreads) ztab[i] = make_float2(0.0f, 0.0f);
+    if constexpr (SP)
+      for (int i = threadIdx.x; i < kSpTabBytes / 4; i += kThreads) sptab[i] = sp24_word((uint32_t)(i >> 5));
   }
   tc_fence_before();
   __syncwarp();  // a warp reaches the block barrier whole (lanes may have diverged)
@@ -642,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     const float pw = __uint_as_float((uint32_t)(127 + 9 - E) << 23);
     // 2-bit: odd classes j meet the 4c weights, so their values are stored
     // divided by 4; base-3 digits are all plain d * 2^-9
-    const float cls = (!B3 && (jc & 1)) ? 0.25f : 1.0f, acls = (!B3 && (jc & 1)) ? 4.0f : 1.0f;
+    const float cls = (!B3 && !SP && (jc & 1)) ? 0.25f : 1.0f, acls = (!B3 && !SP && (jc & 1)) ? 4.0f : 1.0f;
     float u[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) u[b] = v[b] * up * cls;
@@ -654,7 +698,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     // code byte j = trit / 5 (digit trit % 5), which sits in byte j % 4 of
     // A column 5 (j / 4) + digit; its place in the group's window of K steps
     // is kappa = 4 (column - window start) + j % 4.
-    unsigned char* gdst = gbase + (i8 >> 1) * Gm::kUnit + (i8 & 1) * Gm::kLbo + 4 * jc;
+    // 2:4 codes: natural order, k'' = 16 (i % 2) + j + 4 b
+    unsigned char* gdst = gbase + (i8 >> 1) * Gm::kUnit + (i8 & 1) * Gm::kLbo + (SP ? jc : 4 * jc);
     int boff[4];
     if constexpr (B3) {
       const int h = (int)((g0 + gl) % 5);
@@ -677,6 +722,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
         unsigned char* rdst = gbase + pass * Gm::kSteps * Gm::kUnit + (row >> 3) * 128 + (row & 7) * 16;
 #pragma unroll
         for (int b = 0; b < 4; ++b) rdst[boff[b]] = (unsigned char)(word >> (8 * b));
+      } else if constexpr (SP) {
+        unsigned char* rdst = gdst + pass * 4 * Gm::kUnit + (row >> 3) * 128 + (row & 7) * 16;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) rdst[4 * b] = (unsigned char)(word >> (8 * b));
       } else {
         *reinterpret_cast<uint32_t*>(gdst + pass * 4 * Gm::kUnit + (row >> 3) * 128 + (row & 7) * 16) = word;
       }
@@ -699,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       int l = issued_loads, slot = l % kRing, use = l / kRing, tile = l / (nch > 0 ? nch : 1), lc = l - tile * nch;
       for (; l < S; ++l) {
         if (!wait_or_abort(&ctl->empty[slot], (use - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(&ctl->full[slot], kSlotBytes);
+        mbar_arrive_expect_tx(&ctl->full[slot], kStageTx);
         tma_load_2d(smem_u32(ring + slot * kSlotBytes), &cmap, stage_x(lc), (int)((t0 + tile) * 128),
                     &ctl->full[slot]);
         if (++slot == kRing) { slot = 0; ++use; }
@@ -724,6 +773,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     uint32_t off[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) off[q] = rbase + ((((uint32_t)(4 * gh + q)) ^ rx) << 4);
+    if constexpr (SP) {  // rows of 96 bytes, no swizzle: this half's two groups are bytes 48 gh .. + 47
+#pragma unroll
+      for (int q = 0; q < 4; ++q) off[q] = (uint32_t)(r * 96 + 48 * gh + 16 * (q < 3 ? q : 2));
+    }
+    const uint32_t tab_lane = smem_u32(sptab) + 4u * (uint32_t)lane;  // this lane's copy of the code table
     int slot = team, use = 0;  // ring slot of stage s and its use count (s % kRing, s / kRing)
     for (int s = team; s < S; s += 2) {
       // A buffer ab last held stage s - kAbuf, whose MMAs are the
@@ -732,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       bool ok = wait_or_abort(&ctl->full[slot], use & 1, ctl);
       uint4 c[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) c[q] = ok ? lds_u4(ring_u32 + slot * kSlotBytes + off[q]) : make_uint4(0, 0, 0, 0);
+      for (int q = 0; q < (SP ? 3 : 4); ++q) c[q] = ok ? lds_u4(ring_u32 + slot * kSlotBytes + off[q]) : make_uint4(0, 0, 0, 0);
       // The slot is released only after the tensor-memory stores below have
       // consumed c: the refill is a TMA (async-proxy) write, which is not
       // ordered after shared-memory loads whose values have not returned yet,
@@ -755,6 +809,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
           const uint32_t col = acol + (uint32_t)(80 * gh + 40 * h);
           tmem_st32(col, a);
           tmem_st8(col + 32, a + 32);
+        }
+      } else if constexpr (SP) {
+        // group h of this half: low-nibble words nw (8 codes each) and
+        // high-bit words hw (16 codes each); code j -> column 32 (2 gh + h) + j
+        const uint32_t nw[2][4] = {{c[0].x, c[0].y, c[0].z, c[0].w}, {c[1].z, c[1].w, c[2].x, c[2].y}};
+        const uint32_t hw[2][2] = {{c[1].x, c[1].y}, {c[2].z, c[2].w}};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t code = ((nw[h][j >> 3] >> (4 * (j & 7))) & 15u) | (((hw[h][j >> 4] >> (2 * (j & 15))) & 3u) << 4);
+            a[j] = lds_u32(tab_lane + (code << 7));
+          }
+          tmem_st32(acol + (uint32_t)((2 * gh + h) * 32), a);
         }
       } else {
 #pragma unroll
@@ -1069,16 +1138,18 @@ size_t smem_bytes_f(int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t yp
   }
 }
 
-size_t smem_bytes(bool b3, int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ypart_mult = 1) {
-  return b3 ? smem_bytes_f<true>(groups_cap, tiles_cap, M, ypart_mult)
-            : smem_bytes_f<false>(groups_cap, tiles_cap, M, ypart_mult);
+size_t smem_bytes(bool b3, int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ypart_mult = 1, bool sp = false) {
+  return (b3 ? smem_bytes_f<true>(groups_cap, tiles_cap, M, ypart_mult)
+             : smem_bytes_f<false>(groups_cap, tiles_cap, M, ypart_mult)) +
+         (sp ? (size_t)kSpTabBytes : 0);
 }
 
 // Groups per CTA the shared layout holds: the largest K slice a rank gets,
 // in whole stages (2-bit: slices of whole groups; base-3: of five-group
 // stages).
-int64_t groups_cap_of(bool b3, int64_t G, int64_t kcl) {
+int64_t groups_cap_of(bool b3, int64_t G, int64_t kcl, bool sp = false) {
   if (b3) return 5 * (((G + 4) / 5 + kcl - 1) / kcl);
+  if (sp) return 4 * ((2 * ((G / 2 + kcl - 1) / kcl) + 3) / 4);  // slices of group pairs
   return 4 * (((G + kcl - 1) / kcl + 3) / 4);
 }
 
@@ -1115,7 +1186,7 @@ int max_active_clusters(int kcl) {
   return v;
 }
 
-template <int V, bool B3, bool LAYOUT>
+template <int V, bool B3, bool LAYOUT, bool SP = false>
 cudaError_t launch_v(const CUtensorMap& map, const Params& p, size_t smem, cudaStream_t s) {
   // raise the kernel's shared-memory limit only when a launch needs more
   static std::atomic<int> smem_set[64];
@@ -1123,7 +1194,7 @@ cudaError_t launch_v(const CUtensorMap& map, const Params& p, size_t smem, cudaS
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem_set[dev].load(std::memory_order_acquire) < (int)smem) {
     cudaError_t e =
-        cudaFuncSetAttribute(k_gemv_tc<V, B3, LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(k_gemv_tc<V, B3, LAYOUT, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int cur = smem_set[dev].load(std::memory_order_acquire);
     while (cur < (int)smem && !smem_set[dev].compare_exchange_weak(cur, (int)smem)) {
@@ -1143,7 +1214,7 @@ cudaError_t launch_v(const CUtensorMap& map, const Params& p, size_t smem, cudaS
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_gemv_tc<V, B3, LAYOUT>, map, p);
+  return cudaLaunchKernelEx(&cfg, k_gemv_tc<V, B3, LAYOUT, SP>, map, p);
 }
 
 // Cost model of the busiest CTA, in units of 1/24 stage: a stage streams
@@ -1171,24 +1242,25 @@ unsigned int take_fault_gemv() {
 // in shared memory.
 bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* clusters_out, bool all_rows) {
   if (N <= 0 || K <= 0 || K % 128 != 0 || M < 1 || M > 16) return false;
-  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3) return false;
-  const bool b3 = fmt == TQ_PACK_BASE3;
+  if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3 && fmt != kFmtSparse24) return false;
+  const bool b3 = fmt == TQ_PACK_BASE3, sp = fmt == kFmtSparse24;
   const int64_t G = K / 128, T = (N + 127) / 128;
+  if (sp && (G % 2 != 0 || G < 4)) return false;  // 2:4 rows: whole 16-byte pitches, at least one full stage
   const int64_t gs = b3 ? 5 : 4;
   const int sms = device_sm_count();
   if (sms <= 0) return false;
   const int64_t smem_max = device_max_smem_optin();
   int64_t best = 0, best_kcl = 0, best_c = 0;
   for (int64_t kcl = 1; kcl <= 8; kcl *= 2) {
-    if (kcl > (b3 ? (G + gs - 1) / gs : G)) break;  // at least one group (2-bit) / stage (base-3) per rank
+    if (kcl > (b3 ? (G + gs - 1) / gs : (sp ? G / 2 : G))) break;  // a group (2-bit), pair (2:4) or stage (base-3) per rank
     int64_t c = max_active_clusters((int)kcl);
     if (c > sms / kcl) c = sms / kcl;
     if (c > T) c = T;
     if (c < 1) continue;
-    const int64_t gcap = groups_cap_of(b3, G, kcl);
+    const int64_t gcap = groups_cap_of(b3, G, kcl, sp);
     const int64_t gslice = b3 ? std::min(gcap, G) : (G + kcl - 1) / kcl;
     const int64_t tcap = (T + c - 1) / c;
-    if ((int64_t)smem_bytes(b3, gcap, tcap, M, all_rows ? kcl : 1) > smem_max) continue;
+    if ((int64_t)smem_bytes(b3, gcap, tcap, M, all_rows ? kcl : 1, sp) > smem_max) continue;
     const int64_t cost = tcap * (gcap / gs) * kItemsPerStage + gslice * M;
     if (best_kcl == 0 || cost < best || (cost == best && c * kcl < best_c * best_kcl)) {
       best = cost;
@@ -1222,7 +1294,8 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
                            bool prefetch, cudaStream_t s, bool test_stall, const GemvLayout* lay,
                            const GemvChain* chain) {
   if (N == 0) return cudaSuccess;
-  const bool b3 = fmt == TQ_PACK_BASE3;
+  const bool b3 = fmt == TQ_PACK_BASE3, sp = fmt == kFmtSparse24;
+  if (sp && (lay != nullptr || chain != nullptr || test_stall)) return cudaErrorNotSupported;
   const int64_t G = K / 128, T = (N + 127) / 128;
   const bool all_rows = chain != nullptr && chain->xnext != nullptr;
   if (all_rows && N % 128 != 0) return cudaErrorNotSupported;
@@ -1253,16 +1326,17 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
   if (enc == nullptr) return cudaErrorNotSupported;
   CUtensorMap map;
   // 2-bit rows hold K / 4 code bytes; base-3 rows ceil(K / 5) rounded up to
-  // 16 (zero padding).  Boxes of 128 bytes past that read zeros, which meet
-  // zero activations.
-  const int64_t row_bytes = b3 ? ((K + 4) / 5 + 15) / 16 * 16 : K / 4;
+  // 16 (zero padding); 2:4 rows 24 bytes per group, copied 96 bytes (a
+  // stage) per row without swizzle.  Boxes past the row read zeros, which
+  // meet zero activations.
+  const int64_t row_bytes = b3 ? ((K + 4) / 5 + 15) / 16 * 16 : (sp ? 24 * G : K / 4);
   const cuuint64_t gdim[2] = {(cuuint64_t)row_bytes, (cuuint64_t)N};
   const cuuint64_t gstride[1] = {(cuuint64_t)ldc};
-  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t box[2] = {sp ? 96u : 128u, 128};
   const cuuint32_t estride[2] = {1, 1};
   if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), gdim, gstride, box, estride,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+          CU_TENSOR_MAP_INTERLEAVE_NONE, sp ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   Params p{};
   p.scales = scales;
@@ -1276,7 +1350,7 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
   p.M = (int)M;
   p.kcl = kcl;
   p.clusters = clusters;
-  p.groups_cap = (int)groups_cap_of(b3, G, kcl);
+  p.groups_cap = (int)groups_cap_of(b3, G, kcl, sp);
   p.tiles_cap = (int)((T + clusters - 1) / clusters);
   p.prefetch = prefetch ? 1 : 0;
   p.stall_cta = test_stall ? 0 : -1;
@@ -1296,10 +1370,14 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
   // the register count: each allocates all of tensor memory, and a second
   // one would block in tcgen05.alloc while its cluster peers wait for it.
   const size_t smem =
-      std::max(smem_bytes(b3, p.groups_cap, p.tiles_cap, M, all_rows ? kcl : 1), (size_t)(smem_max / 2 + 1024));
+      std::max(smem_bytes(b3, p.groups_cap, p.tiles_cap, M, all_rows ? kcl : 1, sp), (size_t)(smem_max / 2 + 1024));
   const bool lv = (lay != nullptr && (lay->block != 128 || lay->group != 128 || lay->residual)) ||
                   (chain != nullptr && (chain->xr != nullptr || chain->xnext != nullptr));
   const int v = variant_of(M);
+  if (sp)
+    return v == 1 ? launch_v<1, false, false, true>(map, p, smem, s)
+           : v == 2 ? launch_v<2, false, false, true>(map, p, smem, s)
+           : v == 3 ? launch_v<3, false, false, true>(map, p, smem, s) : launch_v<4, false, false, true>(map, p, smem, s);
   if (lv) {
     if (b3) return v == 1 ? launch_v<1, true, true>(map, p, smem, s) : v == 2 ? launch_v<2, true, true>(map, p, smem, s)
                  : v == 3 ? launch_v<3, true, true>(map, p, smem, s) : launch_v<4, true, true>(map, p, smem, s);

@@ -22,7 +22,9 @@
 // selection, the 64-value halving tree and the ternarisation give codes and
 // scales bit-exact with the definition.
 //
-// k_gemv_sparse24: decode with the pruned weights skipped.  A pre-pass
+// k_gemv_sparse24: decode with the pruned weights skipped, on the CUDA cores
+// (the shapes and code layouts the tensor-memory kernel does not take: an
+// odd number of groups per row, fewer than four, unaligned codes).  A pre-pass
 // rotates x into an fp32 workspace; a CTA owns one slice of the K groups and
 // a share of the 32-row blocks (as many CTAs as fit on the SMs at once), with
 // the slice of x' staged in shared memory transposed as [m][group][position

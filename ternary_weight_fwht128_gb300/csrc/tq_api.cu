@@ -468,8 +468,20 @@ tq_status tq_gemv_sparse24(const uint8_t* codes, int64_t ldc, const uint16_t* sc
   if (!aligned16(x) || (ldx * 2) % 16 || !aligned2(scales) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(y) & 3u) || (reinterpret_cast<uintptr_t>(codes) & 3u) || ldc % 4)
     return TQ_ERR_ALIGN;
+  // the tensor-memory kernel when the codes suit its copies (16-byte aligned
+  // rows; an even number of groups per row, at least four), else the
+  // zero-skipping kernel on the CUDA cores
+  if (aligned16(codes) && ldc % 16 == 0 && tq_gemv_sparse24_path(N, K, M) == TQ_GEMV_TENSOR_MEMORY)
+    return from_cuda(launch_gemv_tc(codes, ldc, kFmtSparse24, scales, lds, N, K, x, ldx, M, y, ldy, false,
+                                    (cudaStream_t)stream));
   return from_cuda(launch_gemv_sparse24(codes, ldc, scales, lds, N, K, x, ldx, M, y, ldy, workspace,
                                         (cudaStream_t)stream));
+}
+
+int tq_gemv_sparse24_path(int64_t N, int64_t K, int64_t M) {
+  if (N < 0) return -TQ_ERR_INVALID_ARG;
+  if (!k_ok(K) || M < 1 || M > 16) return -TQ_ERR_SHAPE;
+  return tq::gemv_tc_launches(N, K, M, kFmtSparse24) > 0 ? TQ_GEMV_TENSOR_MEMORY : TQ_GEMV_CUDA_CORES;
 }
 
 tq_status tq_gemm_sparse24(const uint8_t* codes, int64_t ldc, const uint16_t* scales, int64_t lds, int64_t N,

@@ -54,6 +54,10 @@ cudaError_t launch_gemv(const uint8_t* codes, int64_t ldc, int fmt, const uint16
 // rows each, 0 when the shape does not suit it.
 // all_rows: the chained form (GemvChain::xnext), where rank 0 of each cluster
 // holds the partial sums of every row of its tiles.
+// fmt: TQ_PACK_2BIT, TQ_PACK_BASE3, or kFmtSparse24 (the 2:4-sparse codes:
+// 24 bytes per group; K / 128 even and at least 4, codes 16-byte aligned,
+// ldc a multiple of 16; method's layout only, no chain, no stall test).
+constexpr int kFmtSparse24 = 0x24;
 bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl, int* clusters, bool all_rows = false);
 int gemv_tc_launches(int64_t N, int64_t K, int64_t M, int fmt, bool all_rows = false);
 // A layout variant of the method (block size, scale group, residual pass);

@@ -299,6 +299,9 @@ def test_gemm_rotate_next_validation(L):
 def test_sparse24_validation(L):
     assert L.tq_sparse24_ld(5120) == 960 and L.tq_sparse24_ld(27648) == 5184
     assert L.tq_sparse24_ld(100) == -1 and L.tq_sparse24_ld(0) == -1
+    assert L.tq_gemv_sparse24_path(5120, 100, 1) == -tq.TQ_ERR_SHAPE
+    assert L.tq_gemv_sparse24_path(5120, 5120, 17) == -tq.TQ_ERR_SHAPE
+    assert L.tq_gemv_sparse24_path(-1, 5120, 1) == -tq.TQ_ERR_INVALID_ARG
     # x' fp32 (rounded to 256 B), then partial sums when K is split into slices:
     # 55296x5120 needs one slice; 5120x5120 (160 row blocks, aiming at ~512
     # CTAs) is cut into 3 slices of 16 groups; 5120x27648 into 4 of 56

@@ -129,6 +129,54 @@ def test_gemv_sparse24_full_size_sampled(sp, N, K, M):
     _gemv_case(sp, N, K, M, seed=N + K + M + 5, rows=rows)
 
 
+def test_gemv_sparse24_path():
+    """The tensor-memory kernel takes the shapes whose rows hold an even number
+    (at least four) of groups; the others go to the CUDA-core kernel."""
+    TM, CC = tq.TQ_GEMV_TENSOR_MEMORY, tq.TQ_GEMV_CUDA_CORES
+    for N, K, M in [(27648, 5120, 1), (5120, 27648, 1), (5120, 27648, 16), (27648, 5120, 8), (300, 1280, 1),
+                    (200, 768, 16), (1, 512, 1)]:
+        assert tq.gemv_sparse24_path(N, K, M) == TM, (N, K, M)
+    for N, K, M in [(256, 256, 1), (33, 384, 3), (1, 128, 2), (513, 2560 - 128, 1)]:
+        assert tq.gemv_sparse24_path(N, K, M) == CC, (N, K, M)
+
+
+@pytest.mark.parametrize("N,K,M", [(1000, 2560, 1), (4096, 5120, 2), (300, 6912, 7), (129, 512, 16)])
+def test_gemv_sparse24_both_kernels(sp, N, K, M):
+    """The same shape through both kernels: codes at the packed pitch (the
+    tensor-memory kernel) and at a pitch 4 bytes longer (not a multiple of 16:
+    the CUDA-core kernel); both within the tolerance of the oracle."""
+    W = synth.weights(N, K, N + K + M + 9, dtype="bf16")
+    xb = synth.activations(M, K, N + K + M + 10)
+    ld = tq.sparse24_ld(K)
+    wide = torch.zeros((N, ld + 4), dtype=torch.uint8, device="cuda")
+    codes_a, scales = tq.quantize_pack_sparse24(_dev(W))
+    codes_b = wide[:, :ld]
+    scales_b = torch.empty_like(scales)
+    tq.quantize_pack_sparse24(_dev(W), out=(codes_b, scales_b))
+    assert tq.gemv_sparse24_path(N, K, M) == tq.TQ_GEMV_TENSOR_MEMORY
+    c, S = _oracle_codes(sp, W, None, codes_a, scales)
+    assert np.array_equal(codes_b.cpu().numpy(), c)
+    ref = sp.gemv(c, S, synth.bf16_bits_to_f32(xb), K)
+    x = to_dev_bf16(xb)
+    ya = tq.gemv_sparse24(codes_a, scales, x, K)
+    yb = tq.gemv_sparse24(codes_b, scales_b, x, K)
+    torch.cuda.synchronize()
+    check_y(ya.cpu().numpy(), ref, "tensor-memory kernel")
+    check_y(yb.cpu().numpy(), ref, "CUDA-core kernel")
+
+
+def test_gemv_sparse24_tensor_memory_repeatable():
+    N, K, M = 27648, 5120, 1
+    W = synth.weights(N, K, 19, dtype="bf16")
+    codes, scales = tq.quantize_pack_sparse24(_dev(W))
+    x = to_dev_bf16(synth.activations(M, K, 20))
+    assert tq.gemv_sparse24_path(N, K, M) == tq.TQ_GEMV_TENSOR_MEMORY
+    ys = [tq.gemv_sparse24(codes, scales, x, K) for _ in range(20)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+
+
 def test_gemv_sparse24_repeatable():
     N, K, M = 5120, 27648, 4
     W = synth.weights(N, K, 17, dtype="bf16")
