@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
     uint32_t cwd[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int j = 0; j < 64; ++j) {
-      const uint32_t c = (uint32_t)(v[j] > thr) + (uint32_t)!(v[j] < -thr);
-      cwd[j >> 4] |= c << (2 * (j & 15));
+      // c 4^j as two conditional adds of 4^j (the fields never carry: c <= 2)
+      const uint32_t bit = 1u << (2 * (j & 15));
+      cwd[j >> 4] += (v[j] > thr ? bit : 0u) + (!(v[j] < -thr) ? bit : 0u);
     }
     if (ok) {
       if constexpr (DO2) {
