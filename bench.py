@@ -504,7 +504,9 @@ def gpu_extras(args, tq, torch, dev, stack, pk) -> dict:
             continue
         tf = 2 * M * N * K / (ms * 1e-3) / 1e12
         prefill.append({"shape": f"{N}x{K}", "M": M, "us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
-                        "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4)})
+                        "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4),
+                        "l2": "one layer's weights, repeated: its codes (6.6-35 MB) stay in L2; the GEMM is "
+                              "tensor-bound, x' (21-113 MB) and y stream"})
     # gate and up of one layer read the same x: the second call reuses the
     # rotated x' in the workspace (TQ_GEMM_REUSE_ROTATED), one pre-pass per pair
     mats = {m[0]: m for m in stack[0]}
