@@ -539,8 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     g0 = 5 * ((nst * rank) >> lgk);
     g1 = std::min<int64_t>(5 * ((nst * (rank + 1)) >> lgk), G);
   } else if constexpr (SP) {
-    // slices of whole group pairs (G is even): a stage then starts at a
-    // multiple of 48 code bytes, which the copy engine needs (16)
+    // slices of whole group pairs (G is even), so that every stage's copy
+    // starts on a multiple of 48 code bytes (the copy engine needs 16); a
+    // short last stage reads the next slice's codes, which meet zero x'
+    // pieces and zero scales
     g0 = 2 * (((G / 2) * rank) >> lgk);
     g1 = 2 * (((G / 2) * (rank + 1)) >> lgk);
   } else {
