@@ -192,6 +192,21 @@ TQ_API tq_status tq_gemv_rotate_next(const uint8_t *codes, int64_t ldc, int fmt,
 enum { TQ_GEMV_TENSOR_MEMORY = 1, TQ_GEMV_MMA_SYNC = 2, TQ_GEMV_CUDA_CORES = 3 };
 TQ_API int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt);
 
+/* The tensor-memory kernel's work split for a shape (introspection; launches
+ * nothing).  *ctas_per_cluster (1 .. 8): the CTAs of a thread-block cluster
+ * that split the K groups of its tiles and add their partial sums in
+ * distributed shared memory; *clusters: the clusters of a launch, each
+ * owning a range of 128-row tiles; *launches (1 .. 4): the launches the rows
+ * of x are split over (the split reported is the first launch's, which takes
+ * M / launches rows, rounded down).  chained != 0 plans tq_gemv_rotate_next
+ * (N a multiple of 128).  fmt: TQ_PACK_2BIT or TQ_PACK_BASE3.  Returns TQ_OK;
+ * TQ_ERR_UNSUPPORTED when the shape takes another kernel (tq_gemv_path);
+ * TQ_ERR_INVALID_ARG for a null output or bad format; TQ_ERR_SHAPE as
+ * tq_gemv_path, or a chained N that is not a multiple of 128.  Queries the
+ * current device as tq_gemv_path does. */
+TQ_API tq_status tq_gemv_plan(int64_t N, int64_t K, int64_t M, int fmt, int chained, int *ctas_per_cluster,
+                              int *clusters, int *launches);
+
 /* Bytes of caller-provided workspace tq_gemm needs for M x K activations:
  * a status word and the rotated activations in fp16 (256 + 2 M K bytes,
  * rounded up to 256), then 40 MiB for the fp32 partial tiles of a last wave

@@ -30,7 +30,7 @@ TQ_F32, TQ_BF16, TQ_F16 = 0, 1, 2
 TQ_PACK_2BIT, TQ_PACK_BASE3, TQ_PACK_BOTH = 1, 2, 3
 
 EXPORTED = ("tq_status_string", "tq_version", "tq_packed_ld", "tq_fwht128", "tq_quantize_pack", "tq_gemv",
-            "tq_gemv_ex", "tq_gemv_path", "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_ex", "tq_gemm_check_range",
+            "tq_gemv_ex", "tq_gemv_path", "tq_gemv_plan", "tq_gemm_workspace_bytes", "tq_gemm", "tq_gemm_ex", "tq_gemm_check_range",
             "tq_device_fault", "tq_gemm_noalloc", "tq_layout_codes_ld", "tq_layout_scales_ld", "tq_fwht",
             "tq_quantize_pack_layout", "tq_gemv_layout", "tq_gemm_workspace_bytes_layout", "tq_gemm_layout",
             "tq_gemm_rotate_next", "tq_sparse24_ld", "tq_quantize_pack_sparse24",
@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
                                  _vp]
         L.tq_gemv_path.restype = _int
         L.tq_gemv_path.argtypes = [_i64, _i64, _i64, _int]
+        L.tq_gemv_plan.restype = _int
+        L.tq_gemv_plan.argtypes = [_i64, _i64, _i64, _int, _int, _vp, _vp, _vp]
         L.tq_gemm_workspace_bytes.restype = ctypes.c_size_t
         L.tq_gemm_workspace_bytes.argtypes = [_i64, _i64]
         L.tq_gemm.restype = _int
@@ -252,6 +254,16 @@ def gemv_path(N: int, K: int, M: int = 1, fmt: int = TQ_PACK_2BIT) -> int:
     if r < 0:
         raise TQError(-r, "tq_gemv_path")
     return r
+
+
+def gemv_plan(N: int, K: int, M: int = 1, fmt: int = TQ_PACK_2BIT, chained: bool = False) -> tuple[int, int, int]:
+    """The tensor-memory kernel's split for the shape (tq_gemv_plan):
+    (CTAs per cluster, clusters, launches)."""
+    v = (ctypes.c_int * 3)()
+    base = ctypes.addressof(v)
+    st = lib().tq_gemv_plan(N, K, M, fmt, 1 if chained else 0, base, base + 4, base + 8)
+    _check(st, "tq_gemv_plan")
+    return int(v[0]), int(v[1]), int(v[2])
 
 
 def gemm_workspace_bytes(M: int, K: int) -> int:

@@ -73,7 +73,8 @@
 //                MMAs of each stage of team t into accumulator buffer t;
 //   warps 19-22  read the accumulators of their 32 rows and apply the scales.
 // The partial sums of the K slices are reduced across the cluster by rows:
-// rank q owns rows 128 q / kcl .. of every tile, the others push their
+// rank q owns rows R q .. R q + R - 1 of every tile (R = ceil(128 / kcl); the
+// last rank owns what is left), the others push their
 // partial sums of those rows into its shared memory (st.async, counted on an
 // mbarrier there), and rank q adds the kcl partials in rank order and writes
 // y.  Every wait is bounded in time; a wait that runs out sets the library's
@@ -186,6 +187,12 @@ __device__ __forceinline__ void piece_slot(int m, int q, int& pass, int& row) {
 }
 
 int variant_of(int64_t M) { return M <= 2 ? 1 : M <= 5 ? 2 : M <= 8 ? 3 : 4; }
+
+// Largest cluster (K split) the planner uses: the portable limit
+constexpr int kMaxCluster = 8;
+
+// Rows of a 128-row tile each cluster rank reduces (the last rank: the rest)
+__host__ __device__ constexpr int rows_per_rank(int kcl) { return (128 + kcl - 1) / kcl; }
 
 // A buffer b holds the stages s with s % kAbuf == b, so its stages alternate
 // between the teams (and MMA warps).  Its barriers are kept per team, which
@@ -503,7 +510,7 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
 }
 
 // Shared memory (1024-aligned): [code ring][B: groups_cap x kGroupB][zeros kZeroBytes]
-// [ztab: groups_cap x kZs x {pw Zt, pw}][partial sums: tiles_cap x kcl x M x 128 / kcl]
+// [ztab: groups_cap x kZs x {pw Zt, pw}][partial sums: tiles_cap x kcl x M x R]
 // [SP: code table, kSpTabBytes][Ctl]
 // LAYOUT: the layout variants' parameters (blk, lgs, g_rot) and the chained
 // decode (xr, xnext) are read; without it the kernel is compiled for the
@@ -526,28 +533,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
-  // kcl is a power of two; the tile ranges use 32-bit division when it cannot
-  // overflow (64-bit division is a long instruction sequence)
-  const int lgk = __ffs(p.kcl) - 1;
-  const int64_t cluster = blockIdx.x >> lgk;
+  // kcl is 1 .. 8; the slices use 32-bit division (the host keeps G kcl
+  // below 2^31; 64-bit division is a long instruction sequence)
+  const uint32_t kcl = (uint32_t)p.kcl;
+  const int64_t cluster = blockIdx.x / kcl;
   const int64_t G = p.K / 128;
   // K slice of this rank: whole groups (2-bit), whole five-group stages (base-3,
   // so that a slice starts on a code byte); nch stages per tile
   int64_t g0, g1;
   if constexpr (B3) {
     const int64_t nst = (G + 4) / 5;
-    g0 = 5 * ((nst * rank) >> lgk);
-    g1 = std::min<int64_t>(5 * ((nst * (rank + 1)) >> lgk), G);
+    g0 = 5 * (int64_t)((uint32_t)nst * rank / kcl);
+    g1 = std::min<int64_t>(5 * (int64_t)((uint32_t)nst * (rank + 1) / kcl), G);
   } else if constexpr (SP) {
     // slices of whole group pairs (G is even), so that every stage's copy
     // starts on a multiple of 48 code bytes (the copy engine needs 16); a
     // short last stage reads the next slice's codes, which meet zero x'
     // pieces and zero scales
-    g0 = 2 * (((G / 2) * rank) >> lgk);
-    g1 = 2 * (((G / 2) * (rank + 1)) >> lgk);
+    g0 = 2 * (int64_t)((uint32_t)(G / 2) * rank / kcl);
+    g1 = 2 * (int64_t)((uint32_t)(G / 2) * (rank + 1) / kcl);
   } else {
-    g0 = (G * rank) >> lgk;
-    g1 = (G * (rank + 1)) >> lgk;
+    g0 = (int64_t)((uint32_t)G * rank / kcl);
+    g1 = (int64_t)((uint32_t)G * (rank + 1) / kcl);
   }
   const int ng = (int)(g1 - g0), nch = (ng + kGS - 1) / kGS;
   // bytes one stage's copy delivers: 128 rows x 128 code bytes (96 for 2:4 codes)
@@ -569,10 +576,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
   const int ntiles = (int)(t1 - t0);
   const int S = ntiles * nch;  // stages (ring loads) of this CTA
   const int M = p.M;
-  // rank q reduces rows R q .. R q + R - 1 of every tile; with xnext rank 0
-  // reduces all of them (R = 128: the other ranks own none)
+  // rank q reduces rows R q .. R q + Rq - 1 of every tile (R = ceil(128 /
+  // kcl), Rq = R but for the last rank, which takes what is left); with xnext
+  // rank 0 reduces all of them (R = 128: the other ranks own none).  R is
+  // also the stride of the partial sums in shared memory.
   const bool all_rows = LAYOUT && p.xnext != nullptr;
-  const int lgR = all_rows ? 7 : 7 - lgk, R = 1 << lgR;
+  const int R = all_rows ? 128 : rows_per_rank(p.kcl);
+  const int Rq = all_rows ? (rank == 0 ? 128 : 0) : min(R, 128 - (int)rank * R);
 
   int issued_loads = 0;
   auto fill_ring = [&]() {
@@ -601,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     mbar_init(&ctl->red_bar, 1);
     // every other rank sends its partial sums of this rank's rows: ntiles x M x R floats each
     if (p.kcl > 1)
-      mbar_arrive_expect_tx(&ctl->red_bar, (all_rows && rank != 0) ? 0u : (uint32_t)((p.kcl - 1) * ntiles * M * R * 4));
+      mbar_arrive_expect_tx(&ctl->red_bar, (uint32_t)((p.kcl - 1) * ntiles * M * Rq * 4));
     ctl->abort = 0;
     ctl->wait_ns = p.wait_ns;
     fence_mbar_init();
@@ -959,8 +969,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     }
     cluster_wait();
     // this row's partial sums go to the rank that reduces it
-    const uint32_t owner = (uint32_t)(r >> lgR);
-    const int rr = r & (R - 1);
+    const uint32_t owner = (uint32_t)(r / R);
+    const int rr = r - (int)owner * R;
     const bool local = owner == rank;
     const uint32_t push_base = local ? 0u : map_rank(ypart, owner);
     const uint32_t push_bar = local ? 0u : map_rank(&ctl->red_bar, owner);
@@ -1086,9 +1096,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
       }
     }
   } else if (ok && !ctl->abort) {
-    const int total = ntiles * M * R;
+    const int total = ntiles * M * Rq;
     for (int i = threadIdx.x; i < total; i += kThreads) {
-      const int rr = i & (R - 1), j = i >> lgR, tl = j / M, m = j - tl * M;
+      const int j = i / Rq, rr = i - j * Rq, tl = j / M, m = j - tl * M;
       const int64_t n = (t0 + tl) * 128 + (int64_t)rank * R + rr;
       if (n >= p.N) continue;
       const float* src = ypart + (tl * p.kcl * M + m) * R + rr;
@@ -1122,27 +1132,34 @@ EncodeTiledFn encode_fn() {
   return f;
 }
 
-// ypart_mult: 1, or kcl when rank 0 reduces every row (chained decode)
+// Partial-sum floats per (tile, row of x) in a rank's shared memory: the kcl
+// ranks' sums of its R rows, or of all 128 when rank 0 reduces every row
+// (chained decode)
+int64_t ypart_cols(int64_t kcl, bool all_rows) { return kcl * (all_rows ? 128 : rows_per_rank((int)kcl)); }
+// The partial-sum area in floats, whole 128-byte blocks (what follows it, the
+// control block's mbarriers and the 2:4 code table, stays aligned)
+int64_t ypart_floats_of(int64_t tiles_cap, int64_t M, int64_t ycols) { return (tiles_cap * M * ycols + 31) / 32 * 32; }
+
 template <int V, bool B3>
-size_t smem_bytes_v(int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ypart_mult) {
+size_t smem_bytes_v(int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ycols) {
   return 1024 + (size_t)kRing * kSlotBytes + (size_t)groups_cap * Geo<V, B3>::kGroupB + kZeroBytes +
          (size_t)groups_cap * Geo<V, B3>::kZs * sizeof(float2) +
-         (size_t)tiles_cap * 128 * M * ypart_mult * sizeof(float) + sizeof(Ctl);
+         (size_t)ypart_floats_of(tiles_cap, M, ycols) * sizeof(float) + sizeof(Ctl);
 }
 
 template <bool B3>
-size_t smem_bytes_f(int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ypart_mult) {
+size_t smem_bytes_f(int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ycols) {
   switch (variant_of(M)) {
-    case 1: return smem_bytes_v<1, B3>(groups_cap, tiles_cap, M, ypart_mult);
-    case 2: return smem_bytes_v<2, B3>(groups_cap, tiles_cap, M, ypart_mult);
-    case 3: return smem_bytes_v<3, B3>(groups_cap, tiles_cap, M, ypart_mult);
-    default: return smem_bytes_v<4, B3>(groups_cap, tiles_cap, M, ypart_mult);
+    case 1: return smem_bytes_v<1, B3>(groups_cap, tiles_cap, M, ycols);
+    case 2: return smem_bytes_v<2, B3>(groups_cap, tiles_cap, M, ycols);
+    case 3: return smem_bytes_v<3, B3>(groups_cap, tiles_cap, M, ycols);
+    default: return smem_bytes_v<4, B3>(groups_cap, tiles_cap, M, ycols);
   }
 }
 
-size_t smem_bytes(bool b3, int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ypart_mult = 1, bool sp = false) {
-  return (b3 ? smem_bytes_f<true>(groups_cap, tiles_cap, M, ypart_mult)
-             : smem_bytes_f<false>(groups_cap, tiles_cap, M, ypart_mult)) +
+size_t smem_bytes(bool b3, int64_t groups_cap, int64_t tiles_cap, int64_t M, int64_t ycols, bool sp = false) {
+  return (b3 ? smem_bytes_f<true>(groups_cap, tiles_cap, M, ycols)
+             : smem_bytes_f<false>(groups_cap, tiles_cap, M, ycols)) +
          (sp ? (size_t)kSpTabBytes : 0);
 }
 
@@ -1159,10 +1176,10 @@ int64_t groups_cap_of(bool b3, int64_t G, int64_t kcl, bool sp = false) {
 // GPC, so large clusters do not tile all SMs); queried once per device.  The
 // layouts share block size and shared-memory limit, so one query serves all.
 int max_active_clusters(int kcl) {
-  static std::atomic<int> cache[64][4];
+  static std::atomic<int> cache[64][kMaxCluster + 1];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  const int slot = kcl == 1 ? 0 : kcl == 2 ? 1 : kcl == 4 ? 2 : 3;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || kcl < 1 || kcl > kMaxCluster) return 0;
+  const int slot = kcl;
   int v = cache[dev][slot].load(std::memory_order_acquire);
   if (v > 0) return v;
   const int smem = device_max_smem_optin();
@@ -1236,12 +1253,19 @@ unsigned int take_fault_gemv() {
   return f;
 }
 
-// Work split for M rows of x: kcl in {1, 2, 4, 8} CTAs per cluster share a
+// Work split for M rows of x: kcl in 1 .. 8 CTAs per cluster share a
 // tile range and split its K groups; at most as many clusters as can be
 // resident at once (one wave).  The choice minimises the cost model of the
 // busiest CTA (its stages -- 128 code bytes of one 128-row tile -- and its
-// prologue items); ties go to fewer CTAs.  Returns false when no split fits
-// in shared memory.
+// prologue items) over kcl = 1, 2, 4, 8, ties going to fewer CTAs.  A
+// cluster of 3, 5, 6 or 7 (46, 28, 23, 15 resident on 152 SMs) replaces that
+// choice only when it costs at least 10 % less and gives the busiest CTA at
+// most one tile more, since the model leaves out what these cost beyond
+// their stages.  Measured: 5120x5120 (M = 1 .. 4) and 5120x27648 (M = 1)
+// gain from clusters of 6; 2048x2048 at M = 1 lost with them at a 4 % lower
+// cost, and 27648x5120 at M = 2 .. 16 with clusters of 5 (eight tiles a CTA
+// instead of three or six).  Returns false when no split fits in shared
+// memory.
 bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* clusters_out, bool all_rows) {
   if (N <= 0 || K <= 0 || K % 128 != 0 || M < 1 || M > 16) return false;
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3 && fmt != kFmtSparse24) return false;
@@ -1252,9 +1276,15 @@ bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* c
   const int sms = device_sm_count();
   if (sms <= 0) return false;
   const int64_t smem_max = device_max_smem_optin();
-  int64_t best = 0, best_kcl = 0, best_c = 0;
-  for (int64_t kcl = 1; kcl <= 8; kcl *= 2) {
-    if (kcl > (b3 ? (G + gs - 1) / gs : (sp ? G / 2 : G))) break;  // a group (2-bit), pair (2:4) or stage (base-3) per rank
+  int64_t best = 0, best_kcl = 0, best_c = 0, best_t = 0, best_p = 0;
+  if (G * kMaxCluster >= (int64_t(1) << 31)) return false;  // the kernel's 32-bit slice arithmetic
+  const int64_t most = b3 ? (G + gs - 1) / gs : (sp ? G / 2 : G);  // a group (2-bit), pair (2:4) or stage (base-3) per rank
+  static constexpr int kOrder[kMaxCluster] = {1, 2, 4, 8, 3, 5, 6, 7};
+  for (int i = 0; i < kMaxCluster; ++i) {
+    const int64_t kcl = kOrder[i];
+    const bool pow2 = i < 4;
+    if (kcl > most) continue;
+    if (!pow2 && best_kcl == 0) break;  // the other sizes only refine a plan of the first four
     int64_t c = max_active_clusters((int)kcl);
     if (c > sms / kcl) c = sms / kcl;
     if (c > T) c = T;
@@ -1262,12 +1292,17 @@ bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* c
     const int64_t gcap = groups_cap_of(b3, G, kcl, sp);
     const int64_t gslice = b3 ? std::min(gcap, G) : (G + kcl - 1) / kcl;
     const int64_t tcap = (T + c - 1) / c;
-    if ((int64_t)smem_bytes(b3, gcap, tcap, M, all_rows ? kcl : 1, sp) > smem_max) continue;
+    if ((int64_t)smem_bytes(b3, gcap, tcap, M, ypart_cols(kcl, all_rows), sp) > smem_max) continue;
     const int64_t cost = tcap * (gcap / gs) * kItemsPerStage + gslice * M;
-    if (best_kcl == 0 || cost < best || (cost == best && c * kcl < best_c * best_kcl)) {
+    const bool better = best_kcl == 0 || cost < best || (cost == best && c * kcl < best_c * best_kcl);
+    if (better && (pow2 || (10 * cost <= 9 * best_p && tcap <= best_t + 1))) {
       best = cost;
       best_kcl = kcl;
       best_c = c;
+      if (pow2) {  // the refinement is measured against the first four's plan
+        best_t = tcap;
+        best_p = cost;
+      }
     }
   }
   if (best_kcl == 0) return false;
@@ -1366,13 +1401,13 @@ cudaError_t launch_gemv_tc(const uint8_t* codes, int64_t ldc, int fmt, const uin
     p.xnext = chain->xnext;
     p.ldxn = chain->ldxn;
   }
-  p.ypart_floats = (int64_t)p.tiles_cap * 128 * M * (all_rows ? kcl : 1);
+  p.ypart_floats = ypart_floats_of(p.tiles_cap, M, ypart_cols(kcl, all_rows));
   const int64_t smem_max = device_max_smem_optin();
   // More than half an SM's shared memory, so no two CTAs share an SM whatever
   // the register count: each allocates all of tensor memory, and a second
   // one would block in tcgen05.alloc while its cluster peers wait for it.
   const size_t smem =
-      std::max(smem_bytes(b3, p.groups_cap, p.tiles_cap, M, all_rows ? kcl : 1, sp), (size_t)(smem_max / 2 + 1024));
+      std::max(smem_bytes(b3, p.groups_cap, p.tiles_cap, M, ypart_cols(kcl, all_rows), sp), (size_t)(smem_max / 2 + 1024));
   const bool lv = (lay != nullptr && (lay->block != 128 || lay->group != 128 || lay->residual)) ||
                   (chain != nullptr && (chain->xr != nullptr || chain->xnext != nullptr));
   const int v = variant_of(M);

@@ -185,6 +185,19 @@ int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt) {
   return TQ_GEMV_MMA_SYNC;
 }
 
+tq_status tq_gemv_plan(int64_t N, int64_t K, int64_t M, int fmt, int chained, int* ctas_per_cluster, int* clusters,
+                       int* launches) {
+  if (ctas_per_cluster == nullptr || clusters == nullptr || launches == nullptr) return TQ_ERR_INVALID_ARG;
+  const int path = tq_gemv_path(N, K, M, fmt);
+  if (path < 0) return (tq_status)(-path);
+  if (chained && N % 128 != 0) return TQ_ERR_SHAPE;
+  const int l = tq::gemv_tc_launches(N, K, M, fmt, chained != 0);
+  if (l < 1) return TQ_ERR_UNSUPPORTED;
+  if (!tq::plan_gemv_tc(N, K, M / l, fmt, ctas_per_cluster, clusters, chained != 0)) return TQ_ERR_UNSUPPORTED;
+  *launches = l;
+  return TQ_OK;
+}
+
 namespace {
 // start of the split-partial area of a tq_gemm workspace (256-byte aligned)
 size_t gemm_split_offset(int64_t M, int64_t K) { return (256 + (size_t)M * (size_t)K * 2 + 255) / 256 * 256; }

@@ -5,10 +5,12 @@ Every call below fails host-side validation (or is an empty no-op), so the
 fake device pointers are never dereferenced and no CUDA work is issued."""
 from __future__ import annotations
 
+import ctypes
 import os
 import re
 
 import pytest
+import torch
 
 import ternary_weight_fwht128_gb300 as tq
 from ternary_weight_fwht128_gb300 import build as tqbuild
@@ -125,6 +127,21 @@ def test_gemv_path_validation(L):
     # base-3 codes always take the mma.sync kernel (no device query needed)
     assert f(27648, 5120, 1, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
     assert f(5120, 27648, 16, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
+
+
+def test_gemv_plan_validation(L):
+    f = L.tq_gemv_plan
+    v = (ctypes.c_int * 3)()
+    a = ctypes.addressof(v)
+    assert f(8, 256, 1, tq.TQ_PACK_2BIT, 0, None, a + 4, a + 8) == tq.TQ_ERR_INVALID_ARG
+    assert f(8, 256, 1, tq.TQ_PACK_2BIT, 0, a, None, a + 8) == tq.TQ_ERR_INVALID_ARG
+    assert f(8, 256, 1, tq.TQ_PACK_2BIT, 0, a, a + 4, None) == tq.TQ_ERR_INVALID_ARG
+    assert f(8, 256, 1, 3, 0, a, a + 4, a + 8) == tq.TQ_ERR_INVALID_ARG
+    assert f(8, 200, 1, tq.TQ_PACK_2BIT, 0, a, a + 4, a + 8) == tq.TQ_ERR_SHAPE
+    assert f(8, 256, 17, tq.TQ_PACK_2BIT, 0, a, a + 4, a + 8) == tq.TQ_ERR_SHAPE
+    # without a device every shape takes the other kernel (nothing to plan)
+    if not torch.cuda.is_available():
+        assert f(5120, 5120, 1, tq.TQ_PACK_2BIT, 0, a, a + 4, a + 8) == tq.TQ_ERR_UNSUPPORTED
 
 
 def test_gemv_validation(L):

@@ -263,6 +263,61 @@ def test_gemv_tc_skinny(orc, N, K, M):
     _gemv_case(orc, N, K, M, seed=N * 5 + K + M, rows=rows)
 
 
+# One shape per K split the planner can choose (1 .. 8 CTAs per cluster at
+# M = 3): 5120x128 has one group, 3000x2048 and 123x896 ragged tiles.
+CLUSTER_SHAPES = [(5120, 128), (27648, 5120), (5120, 1536), (3000, 2048), (2560, 2560), (2048, 3072), (123, 896),
+                  (1024, 27648)]
+
+
+def test_gemv_tc_plans_every_cluster_size():
+    """At M = 3 the shapes of the next test reach every cluster size the
+    planner has (the plan is queried through tq_gemv_plan, not assumed)."""
+    sizes = [tq.gemv_plan(N, K, 3)[0] for N, K in CLUSTER_SHAPES]
+    assert sizes == list(range(1, 9)), sizes
+
+
+@pytest.mark.parametrize("N,K", CLUSTER_SHAPES)
+@pytest.mark.parametrize("M", [1, 3])
+def test_gemv_tc_cluster_sizes(orc, N, K, M):
+    """Each K split, including clusters of 3, 5, 6 and 7 whose ranks own
+    ceil(128 / kcl) rows of a tile (the last rank the rest) and floor-divided
+    K slices: sampled rows and the tail against the oracle, and 20 repeats
+    bit-identical to the first."""
+    kcl, clusters, launches = tq.gemv_plan(N, K, M)
+    assert 1 <= kcl <= 8 and clusters >= 1 and launches == 1
+    rng = np.random.default_rng(N + K + M + 5)
+    rows = np.unique(np.concatenate([rng.choice(N, size=min(N, 40), replace=False), np.arange(max(0, N - 130), N)]))
+    _gemv_case(orc, N, K, M, seed=N * 11 + K + M, rows=rows)
+    W = synth.weights(N, K, 91, dtype="bf16")
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    x = to_dev_bf16(synth.activations(M, K, 92))
+    outs = [tq.gemv(c2, s, x, K, weights_ready=True) for _ in range(20)]
+    torch.cuda.synchronize()
+    tq.device_fault()
+    for y in outs[1:]:
+        assert torch.equal(y, outs[0])
+
+
+@pytest.mark.parametrize("N,K", [(5120, 5120), (5120, 1536), (2560, 2560), (2048, 3072)])
+def test_gemv_rotate_next_cluster_sizes(orc, N, K):
+    """The chained form (rank 0 adds the partial sums of all 128 rows of
+    its tiles) on shapes whose plan is not a power-of-two cluster: y against
+    the oracle, x'_next bit for bit the staged transform of y."""
+    kcl, _, _ = tq.gemv_plan(N, K, 1, chained=True)
+    assert kcl in (3, 5, 6, 7)
+    W = synth.weights(N, K, 93, dtype="bf16")
+    c2, _, s = tq.quantize_pack(to_dev_bf16(W), tq.TQ_PACK_2BIT)
+    xb = synth.activations(1, K, 94)
+    y, xn = tq.gemv_rotate_next(c2, s, to_dev_bf16(xb), K)
+    torch.cuda.synchronize()
+    tq.device_fault()
+    yn = y.cpu().numpy()
+    assert np.array_equal(xn.cpu().numpy().view(np.uint32), _staged_fwht128(yn).view(np.uint32))
+    rows = np.arange(0, N, max(1, N // 64))
+    T, S = orc.quantize(W, rows)
+    check_y(yn[:, rows], orc.gemv(T, S, synth.bf16_bits_to_f32(xb)), f"chained y (clusters of {kcl})")
+
+
 @pytest.mark.parametrize("N,K,M", [
     (27648, 5120, 1), (19457, 2560, 3), (20000, 2944, 5), (27648, 5120, 6), (4999, 27648, 8),
     (19500, 4480, 11), (5120, 27648, 13), (2049, 1152, 16), (300, 640, 1), (129, 768, 2), (1000, 27648, 16),
