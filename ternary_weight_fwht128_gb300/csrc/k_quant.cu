@@ -91,15 +91,17 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
   }
   pdl_wait();
 
-  // rows and units-in-row of the three units of triple `it` (one division)
+  // rows and units-in-row of the three units of triple `it`: one 32-bit
+  // division (the host keeps the unit count below 2^31), done once per
+  // triple -- the loop hands the triple it loads on to its processing
   struct Tri {
-    int64_t n[3], u[3];
+    uint32_t n[3], u[3];
   };
   auto triple = [&](int64_t it) {
     Tri t;
-    const int64_t U0 = 3 * it;
-    t.n[0] = U0 / nu;
-    t.u[0] = U0 - t.n[0] * nu;
+    const uint32_t U0 = (uint32_t)(3 * it), row = U0 / (uint32_t)nu;
+    t.n[0] = row;
+    t.u[0] = U0 - row * (uint32_t)nu;
 #pragma unroll
     for (int q = 1; q < 3; ++q) {
       t.n[q] = t.n[q - 1];
@@ -114,14 +116,16 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
   // group of this lane in triple `it`: row n, group g (valid: inside the matrix)
   auto locate = [&](int64_t it, const Tri& t, int64_t& n, int64_t& g) -> bool {
     const int q = ul < 3 ? ul : 0;
-    n = q == 0 ? t.n[0] : (q == 1 ? t.n[1] : t.n[2]);
-    g = 5 * (q == 0 ? t.u[0] : (q == 1 ? t.u[1] : t.u[2])) + kq;
-    return ul < 3 && 3 * it + ul < nunits && g < G;
+    const uint32_t n32 = q == 0 ? t.n[0] : (q == 1 ? t.n[1] : t.n[2]);
+    const uint32_t g32 = 5u * (q == 0 ? t.u[0] : (q == 1 ? t.u[1] : t.u[2])) + (uint32_t)kq;
+    n = n32;
+    g = g32;
+    return ul < 3 && (uint32_t)(3 * it) + (uint32_t)ul < (uint32_t)nunits && g32 < (uint32_t)G;
   };
   // starts the copy of triple `it`'s weights into staging buffer `buf`
-  auto load = [&](int buf, int64_t it) {
+  auto load = [&](int buf, int64_t it, const Tri& tri) {
     int64_t n, g;
-    if (it < niters && locate(it, triple(it), n, g)) {
+    if (it < niters && locate(it, tri, n, g)) {
       const unsigned char* src = static_cast<const unsigned char*>(W) + (n * ldw + g * 128 + 64 * h) * esize;
       const uint32_t dst = smem_u32(stage_at(buf) + lane * kLaneStage<WT>);
 #pragma unroll
@@ -135,9 +139,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
     for (int i = 0; i < (WT == TQ_F32 ? 16 : 8); ++i) r.w[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
   };
 
-  auto process = [&](int buf, int64_t it) {
+  auto process = [&](int buf, int64_t it, const Tri& tri) {
     int64_t n, g;
-    const Tri tri = triple(it);
     const bool ok = locate(it, tri, n, g);
     Raw<WT> r;
     fetch(r, buf, ok);
@@ -256,28 +259,28 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
       // 12 lane .. 12 lane + 11): a word never straddles two units (128 bytes
       // each), and its four bytes take their 10-bit windows from three
       // consecutive code words.
-      const int64_t U0 = 3 * it;
+      const uint32_t U0 = (uint32_t)(3 * it);
 #pragma unroll
       for (int m4 = 0; m4 < 3; ++m4) {
         const int B = 12 * lane + 4 * m4;  // first byte of the word, of the triple's 384
         const int q = B >> 7, b = B & 127;
-        if (U0 + q >= nunits) continue;
-        const int64_t un = q == 0 ? tri.n[0] : (q == 1 ? tri.n[1] : tri.n[2]);
-        const int64_t uu = q == 0 ? tri.u[0] : (q == 1 ? tri.u[1] : tri.u[2]);
-        const int64_t pos = uu * 128 + b;  // byte of the row (a multiple of 4)
-        if (pos >= ld3min) continue;        // past the row's zero padding (ld3min % 16 == 0)
+        if (U0 + (uint32_t)q >= (uint32_t)nunits) continue;
+        const uint32_t un = q == 0 ? tri.n[0] : (q == 1 ? tri.n[1] : tri.n[2]);
+        const uint32_t uu = q == 0 ? tri.u[0] : (q == 1 ? tri.u[1] : tri.u[2]);
+        const uint32_t pos = uu * 128u + (uint32_t)b;  // byte of the row (a multiple of 4)
+        if (pos >= (uint32_t)ld3min) continue;          // past the row's zero padding (ld3min % 16 == 0)
         const int bit0 = 1280 * q + 10 * b;
         const uint32_t w0 = wbuf[bit0 >> 5], w1 = wbuf[(bit0 >> 5) + 1], w2 = wbuf[(bit0 >> 5) + 2];
         uint32_t word = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          if (pos + k < nbytes3) {
+          if (pos + k < (uint32_t)nbytes3) {
             const int sh = (bit0 & 31) + 10 * k;  // 0 .. 61
             const uint32_t win = sh < 32 ? __funnelshift_r(w0, w1, sh) : __funnelshift_r(w1, w2, sh - 32);
             word |= (uint32_t)b3[win & 0x3ffu] << (8 * k);
           }
         }
-        uint8_t* dst = codes3 + un * ld3 + pos;
+        uint8_t* dst = codes3 + (int64_t)un * ld3 + pos;
         if (vec3) {
           *reinterpret_cast<uint32_t*>(dst) = word;
         } else {
@@ -290,13 +293,16 @@ __global__ void __launch_bounds__(kThreads, 3) k_quantize_pack(const void* __res
 
   int64_t it = (int64_t)blockIdx.x * kWarps + warp;
   int buf = 0;
-  load(buf, it);
+  Tri cur = triple(it);
+  load(buf, it, cur);
   for (; it < niters; it += stride) {
-    load(buf ^ 1, it + stride);  // the next triple streams in meanwhile
-    cp_async_wait<1>();          // this lane's copies of triple `it` have landed
-    process(buf, it);
-    __syncwarp();                // every lane has read `buf` before it is refilled
+    const Tri next = triple(it + stride);
+    load(buf ^ 1, it + stride, next);  // the next triple streams in meanwhile
+    cp_async_wait<1>();                // this lane's copies of triple `it` have landed
+    process(buf, it, cur);
+    __syncwarp();                      // every lane has read `buf` before it is refilled
     buf ^= 1;
+    cur = next;
   }
   cp_async_wait<0>();
   pdl_launch_dependents();
@@ -307,6 +313,8 @@ cudaError_t launch_t(const void* W, int64_t N, int64_t K, int64_t ldw, uint8_t* 
                      int64_t ld3, uint16_t* sc, int64_t lds, cudaStream_t s) {
   const int64_t G = K / 128;
   const int64_t niters = (N * ((G + 4) / 5) + 2) / 3;  // unit triples, one per warp iteration
+  // the kernel's unit index is 32-bit (about 2.8 TB of bf16 weights; never reached in memory)
+  if (3 * niters >= (int64_t(1) << 31) - (int64_t(1) << 24)) return cudaErrorInvalidValue;
   // exactly the resident CTAs: triples are dealt out statically, so a CTA
   // waiting for a second wave would leave the tail to few SMs
   const size_t smem = (size_t)2 * kWarps * 32 * kLaneStage<WT>;

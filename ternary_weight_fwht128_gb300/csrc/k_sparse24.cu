@@ -88,10 +88,12 @@ __global__ void __launch_bounds__(32 * kQWarps, 4) k_quantize_sparse24(const SQP
   // a warp takes four consecutive units (row-major groups) at a time; the
   // 8-lane group j = lane / 8 takes unit 4 i + j, lane q of it holding
   // weights 16q .. 16q + 15 (quads 4q .. 4q + 3)
+  // (the host keeps the unit count below 2^31: 32-bit row / group split)
   for (int64_t u0 = 4 * wid; u0 < units; u0 += 4 * nw) {
     const int64_t u = u0 + (lane >> 3);
     const bool live = u < units;
-    const int64_t n = live ? u / G : 0, g = live ? u - n * G : 0;
+    const uint32_t n32 = live ? (uint32_t)u / (uint32_t)G : 0u;
+    const int64_t n = n32, g = live ? (int64_t)((uint32_t)u - n32 * (uint32_t)G) : 0;
     float v[16];
     if (p.wt == TQ_F32) {
       const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.W) + n * p.ldw + 128 * g + 16 * q);
@@ -397,6 +399,9 @@ cudaError_t launch_quantize_sparse24(const void* W, int wt, int64_t N, int64_t K
                                      int64_t ldc, uint16_t* scales, int64_t lds, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   if (N > 0x7fffffffll) return cudaErrorNotSupported;
+  // the kernel splits its unit index into row and group in 32 bits
+  if (N * (K / 128) + 4 * 32 * kQWarps * (int64_t)device_sm_count() * 4 >= (int64_t(1) << 31))
+    return cudaErrorNotSupported;
   SQParams p{W, wt, N, K, ldw, codes, ldc, scales, lds};
   // four groups per warp at a time; four CTAs of eight warps per SM
   const int64_t units = N * (K / 128);
