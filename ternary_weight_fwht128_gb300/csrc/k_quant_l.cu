@@ -6,20 +6,27 @@
 // the residual r = w' - s1 t1 is rotated once more by the same block
 // transform and ternarised with a scale of its own.
 //
-// One CTA per weight row, eight warps.  A warp takes a unit of
-// u = max(block, group) weights at a time, staged in its own shared memory:
-// every butterfly stage of the transform runs in parallel over the unit's
-// pairs (h = 1, 2, ..., block / 2, lower index keeps a + b, then one multiply
-// by RN_fp32(1/sqrt(block))), the absmean sum is the halving tree
-// s[i] += s[i + h] for h = group / 2 .. 1, the scale is fp16 round-to-nearest,
-// and t = clamp(rint(w' / s)) with IEEE division -- each step in the order of
-// the definition, so codes and scales are bit-exact with it.  The trits of the
-// whole row (both passes: Keff = K or 2K) are kept in shared memory; once the
-// row is done, its 2-bit bytes (code t + 1 at bits 2 (k % 4)) and base-3 bytes
-// (five digits t + 1 per byte, lowest k least significant, digit 1 past Keff,
-// zero bytes up to the 16-byte padded length) are written from there.  This
-// is the general path; the method's own layout (128, 128, no residual) keeps
-// the fused lane-pair kernel of k_quant.cu.
+// One CTA per weight row, eight warps.  A warp takes 256 consecutive weights
+// of its row at a time, lane l holding weights 8 l .. 8 l + 7 in registers
+// (blocks and groups of 128 and 256 weights both tile the span; at block and
+// group <= 128 each half-warp holds one 128-weight unit).  The transform runs
+// stages h = 1, 2, 4 inside the lane and h = 8 .. block / 2 as shuffles with
+// lane l ^ (h / 8) (the lower index of a pair keeps a + b), then one multiply
+// by RN_fp32(1/sqrt(block)); the absmean sum is the halving tree
+// s[i] += s[i + h] for h = group / 2 .. 1 -- levels h >= 8 between lanes,
+// where both lanes of a pair form the sum (an IEEE sum does not depend on the
+// order of its operands, so they hold the same bits), levels 4, 2, 1 inside
+// the lane; the scale is fp16 round-to-nearest; and t = sign(w') [|w'| > s/2]
+// for a finite s > 0, else 0 -- the same trits as clamp(rint(w' / s), -1, 1)
+// with IEEE division and ties to even (the rule of the method-layout kernel in
+// k_quant.cu).  Each step follows the definition's order, so codes and scales
+// are bit-exact with it.  The trits of the whole row (both passes: Keff = K or
+// 2K) are kept in shared memory; once the row is done, its 2-bit bytes (code
+// t + 1 at bits 2 (k % 4)) and base-3 bytes (five digits t + 1 per byte,
+// lowest k least significant, digit 1 past Keff, zero bytes up to the 16-byte
+// padded length) are written from there.  This is the general path; the
+// method's own layout (128, 128, no residual) keeps the fused lane-pair
+// kernel of k_quant.cu.
 #include "tq_internal.h"
 
 namespace tq {
@@ -28,8 +35,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnitMax = 256;
-constexpr int kWarpFloats = 3 * kUnitMax;  // w', r and the sum tree
+constexpr int kSpan = 256;  // weights a warp takes at a time (8 per lane)
 
 struct LParams {
   const void* W;
@@ -44,65 +50,108 @@ struct LParams {
   int64_t lds;
 };
 
-// fp16 scale of g values: halving-tree sum of |v| in fp32, times 1/g (exact).
-__device__ __forceinline__ uint16_t group_scale(const float* v, float* s, int g, int lane) {
-  for (int i = lane; i < g; i += 32) s[i] = fabsf(v[i]);
-  __syncwarp();
-  for (int h = g / 2; h >= 1; h >>= 1) {
-    for (int i = lane; i < h; i += 32) s[i] = __fadd_rn(s[i], s[i + h]);
-    __syncwarp();
+// Block transform of the lane's 8 weights (elements 8 lane .. 8 lane + 7 of
+// the span): stages h = 1, 2, 4 in the lane, h = 8 .. block / 2 with lane
+// l ^ (h / 8), then * c.
+__device__ __forceinline__ void fwht_lanes(float v[8], int block, float c, int lane) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j & h) continue;
+      const float a = v[j], b = v[j + h];
+      v[j] = __fadd_rn(a, b);
+      v[j + h] = __fsub_rn(a, b);
+    }
   }
+  for (int m = 1; 8 * m < block; m <<= 1) {
+    const bool up = (lane & m) != 0;  // this lane holds the upper elements i + h
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float o = __shfl_xor_sync(kFull, v[j], m);
+      v[j] = up ? __fsub_rn(o, v[j]) : __fadd_rn(v[j], o);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], c);
+}
+
+// fp16 scale of the group of g values this lane's 8 belong to: halving-tree
+// sum of |v| in fp32 (levels h = g / 2 .. 8 with lane l ^ (h / 8), both lanes
+// forming the sum; levels 4, 2, 1 in the lane), times 1/g (exact).  Every
+// lane of the group returns it.
+__device__ __forceinline__ uint16_t group_scale_lanes(const float v[8], int g) {
+  float s[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s[j] = fabsf(v[j]);
+  for (int m = g / 16; m >= 1; m >>= 1) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], __shfl_xor_sync(kFull, s[j], m));
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) s[j] = __fadd_rn(s[j], s[j + 4]);
+  s[0] = __fadd_rn(s[0], s[2]);
+  s[1] = __fadd_rn(s[1], s[3]);
+  s[0] = __fadd_rn(s[0], s[1]);
   const float mean = __fmul_rn(s[0], 1.0f / (float)g);
-  __syncwarp();
   return __half_as_ushort(__float2half_rn(mean));
+}
+
+// Trits of the lane's 8 values under scale bits sb: t = [w > s/2] - [w < -s/2]
+// for a finite s > 0, else 0 (see the file comment); packed as int8 bytes.
+__device__ __forceinline__ uint2 ternarise8(const float v[8], uint16_t sb, int t[8]) {
+  const float sc = __half2float(__ushort_as_half(sb));
+  const float thr = (sc != 0.0f) ? sc * 0.5f : __int_as_float(0x7f800000);  // sc * 0.5 is exact
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    t[j] = (v[j] > thr ? 1 : 0) - (v[j] < -thr ? 1 : 0);
+    w[j >> 2] |= (uint32_t)(uint8_t)(int8_t)t[j] << (8 * (j & 3));
+  }
+  return make_uint2(w[0], w[1]);
 }
 
 __global__ void __launch_bounds__(kThreads) k_quantize_layout(const LParams p) {
   extern __shared__ __align__(16) unsigned char sm[];
   const int64_t Keff = p.residual ? 2 * p.K : p.K;
-  const int64_t tbytes = (Keff + 15) / 16 * 16;
   int8_t* trits = reinterpret_cast<int8_t*>(sm);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* v = reinterpret_cast<float*>(sm + tbytes) + warp * kWarpFloats;
-  float* r = v + kUnitMax;
-  float* s = r + kUnitMax;
-  const int u = p.block > p.group ? p.block : p.group;
   const int64_t n = blockIdx.x;
   const int64_t G = p.K / p.group;
   const float cb = p.block == 64 ? 0.125f : (p.block == 256 ? 0.0625f : kInvSqrt128);
   pdl_wait();
-  for (int64_t k0 = (int64_t)warp * u; k0 < p.K; k0 += (int64_t)kWarps * u) {
+  for (int64_t k0 = (int64_t)warp * kSpan; k0 < p.K; k0 += (int64_t)kWarps * kSpan) {
+    // K is a multiple of 128: a half-warp is wholly inside the row or past it
+    // (then it computes on zeros and stores nothing; the shuffles need it)
+    const int64_t kl = k0 + 8 * lane;
+    const bool live = kl < p.K;
+    float v[8];
     if (p.wt == TQ_F32) {
-      const float* w = static_cast<const float*>(p.W) + n * p.ldw + k0;
-      for (int i = lane; i < u; i += 32) v[i] = w[i];
+      const float* w = static_cast<const float*>(p.W) + n * p.ldw + kl;
+      const uint4 a = live ? ld_in_u4(w) : make_uint4(0, 0, 0, 0), b = live ? ld_in_u4(w + 4) : make_uint4(0, 0, 0, 0);
+      v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+      v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
     } else {
-      const uint16_t* w = static_cast<const uint16_t*>(p.W) + n * p.ldw + k0;
-      for (int i = lane; i < u; i += 32) v[i] = __uint_as_float((uint32_t)w[i] << 16);
+      const uint16_t* w = static_cast<const uint16_t*>(p.W) + n * p.ldw + kl;
+      bf16x8_to_f32(live ? ld_in_u4(w) : make_uint4(0, 0, 0, 0), v);
     }
-    __syncwarp();
-    for (int b = 0; b < u; b += p.block) fwht_warp(v + b, p.block, cb, lane);
-    for (int g = 0; g < u; g += p.group) {
-      const uint16_t sb = group_scale(v + g, s, p.group, lane);
-      if (lane == 0) p.scales[n * p.lds + (k0 + g) / p.group] = sb;
-      const float sc = __half2float(__ushort_as_half(sb));
-      for (int i = lane; i < p.group; i += 32) {
-        const float w = v[g + i];
-        const int t = ternarise(w, sc);
-        trits[k0 + g + i] = (int8_t)t;
-        // a zero trit dequantises to 0 whatever the scale (which may be inf)
-        r[g + i] = t == 0 ? w : __fsub_rn(w, __fmul_rn(sc, (float)t));
-      }
-      __syncwarp();
-    }
+    const bool first = live && (kl % p.group) == 0;  // the lane that stores its group's scale
+    fwht_lanes(v, p.block, cb, lane);
+    const uint16_t sb = group_scale_lanes(v, p.group);
+    if (first) p.scales[n * p.lds + kl / p.group] = sb;
+    int t[8];
+    const uint2 tw = ternarise8(v, sb, t);
+    if (live) *reinterpret_cast<uint2*>(trits + kl) = tw;
     if (!p.residual) continue;
-    for (int b = 0; b < u; b += p.block) fwht_warp(r + b, p.block, cb, lane);
-    for (int g = 0; g < u; g += p.group) {
-      const uint16_t sb = group_scale(r + g, s, p.group, lane);
-      if (lane == 0) p.scales[n * p.lds + G + (k0 + g) / p.group] = sb;
-      const float sc = __half2float(__ushort_as_half(sb));
-      for (int i = lane; i < p.group; i += 32) trits[p.K + k0 + g + i] = (int8_t)ternarise(r[g + i], sc);
-      __syncwarp();
-    }
+    // residual r = w' - s t (a zero trit leaves w' itself, whatever the scale)
+    const float sc = __half2float(__ushort_as_half(sb));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = t[j] == 0 ? v[j] : __fsub_rn(v[j], __fmul_rn(sc, (float)t[j]));
+    fwht_lanes(v, p.block, cb, lane);
+    const uint16_t sb2 = group_scale_lanes(v, p.group);
+    if (first) p.scales[n * p.lds + G + kl / p.group] = sb2;
+    const uint2 tw2 = ternarise8(v, sb2, t);
+    if (live) *reinterpret_cast<uint2*>(trits + p.K + kl) = tw2;
   }
   __syncthreads();
   if (p.codes2 != nullptr) {
@@ -138,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize_layout(const LParams p) {
 
 size_t quantize_layout_smem(int64_t K, int residual) {
   const int64_t Keff = residual ? 2 * K : K;
-  return (size_t)((Keff + 15) / 16 * 16) + (size_t)kWarps * kWarpFloats * sizeof(float);
+  return (size_t)((Keff + 15) / 16 * 16);  // the row's trits
 }
 
 cudaError_t launch_quantize_layout(const void* W, int wt, int64_t N, int64_t K, int64_t ldw, int block, int group,
