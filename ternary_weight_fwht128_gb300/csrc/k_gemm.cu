@@ -524,14 +524,15 @@ __global__ void __launch_bounds__(256) k_gemm_fixup(const float* __restrict__ pa
                                                    int splits, int n_tiles_m, int bn, int64_t M, int64_t N,
                                                    float* __restrict__ y, int64_t ldy) {
   pdl_wait();
-  const int c4 = bn / 4;
-  const int64_t total = (int64_t)n_split_tiles * BM * c4;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int lt = (int)(i / ((int64_t)BM * c4));
-    const int rem = (int)(i - (int64_t)lt * BM * c4);
-    const int row = rem / c4, c = 4 * (rem - row * c4);
-    const int tile = n_main + lt;
-    const int64_t m = (int64_t)(tile % n_tiles_m) * BM + row, n = (int64_t)(tile / n_tiles_m) * bn + c;
+  // 32-bit index arithmetic: the split tiles are at most one wave (a few
+  // million outputs of 4 columns)
+  const uint32_t c4 = (uint32_t)bn / 4, per_tile = (uint32_t)BM * c4;
+  const uint32_t total = (uint32_t)n_split_tiles * per_tile;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const uint32_t lt = i / per_tile, rem = i - lt * per_tile;
+    const uint32_t row = rem / c4, c = 4 * (rem - row * c4);
+    const uint32_t tile = (uint32_t)n_main + lt, tn = tile / (uint32_t)n_tiles_m;
+    const int64_t m = (int64_t)(tile - tn * (uint32_t)n_tiles_m) * BM + row, n = (int64_t)tn * bn + c;
     if (m >= M || n >= N) continue;
     const float* src = part + ((int64_t)lt * splits * BM + row) * bn + c;
     const int64_t seg = (int64_t)BM * bn;

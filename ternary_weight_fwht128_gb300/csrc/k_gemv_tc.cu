@@ -569,7 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemv_tc(const __grid_constant__
     // the first T % clusters clusters take one tile more: CTAs of a GEMV
     // launched behind another start in index order as SMs free up, so the
     // last to start (on the SMs the previous GEMV held longest) get less work
-    const int64_t base = T / p.clusters, extra = T - base * p.clusters;
+    // (32-bit: the planner keeps T below 2^31)
+    const int64_t base = (uint32_t)T / (uint32_t)p.clusters, extra = T - base * p.clusters;
     t0 = cluster * base + (cluster < extra ? cluster : extra);
     t1 = t0 + base + (cluster < extra ? 1 : 0);
   }
@@ -1277,7 +1278,7 @@ bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* c
   if (sms <= 0) return false;
   const int64_t smem_max = device_max_smem_optin();
   int64_t best = 0, best_kcl = 0, best_c = 0, best_t = 0, best_p = 0;
-  if (G * kMaxCluster >= (int64_t(1) << 31)) return false;  // the kernel's 32-bit slice arithmetic
+  if (G * kMaxCluster >= (int64_t(1) << 31) || T >= (int64_t(1) << 31)) return false;  // the kernel's 32-bit slice and tile arithmetic
   const int64_t most = b3 ? (G + gs - 1) / gs : (sp ? G / 2 : G);  // a group (2-bit), pair (2:4) or stage (base-3) per rank
   static constexpr int kOrder[kMaxCluster] = {1, 2, 4, 8, 3, 5, 6, 7};
   for (int i = 0; i < kMaxCluster; ++i) {

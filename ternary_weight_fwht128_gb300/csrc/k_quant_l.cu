@@ -36,6 +36,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSpan = 256;  // weights a warp takes at a time (8 per lane)
+constexpr int kTritTail = 32;  // zero bytes after the row's trits (word reads of the base-3 packing)
 
 struct LParams {
   const void* W;
@@ -116,6 +117,8 @@ __global__ void __launch_bounds__(kThreads) k_quantize_layout(const LParams p) {
   const int64_t Keff = p.residual ? 2 * p.K : p.K;
   int8_t* trits = reinterpret_cast<int8_t*>(sm);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the tail past the row's trits reads as t = 0 in the base-3 packing
+  if (threadIdx.x < kTritTail) trits[Keff + threadIdx.x] = 0;
   const int64_t n = blockIdx.x;
   const int64_t G = p.K / p.group;
   const float cb = p.block == 64 ? 0.125f : (p.block == 256 ? 0.0625f : kInvSqrt128);
@@ -155,29 +158,61 @@ __global__ void __launch_bounds__(kThreads) k_quantize_layout(const LParams p) {
   }
   __syncthreads();
   if (p.codes2 != nullptr) {
+    // 16 trits a thread: one 16-byte read, t + 1 per byte (no carries), and
+    // the four 2-bit fields of each byte word gathered by two shift-ors
     uint8_t* row = p.codes2 + n * p.ld2;
-    for (int64_t j = threadIdx.x; j < Keff / 4; j += kThreads) {
-      uint32_t b = 0;
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.codes2) | (uintptr_t)p.ld2) & 3u) == 0;
+    const int nw = (int)(Keff / 16);
+    for (int j = threadIdx.x; j < nw; j += kThreads) {
+      const uint4 tb = *reinterpret_cast<const uint4*>(trits + 16 * j);
+      const uint32_t q[4] = {tb.x, tb.y, tb.z, tb.w};
+      uint32_t w = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) b |= (uint32_t)(trits[4 * j + i] + 1) << (2 * i);
-      row[j] = (uint8_t)b;
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t c = __vadd4(q[i], 0x01010101u);  // codes 0..2, one per byte
+        const uint32_t y = c | (c >> 6);                 // codes 0, 1 at bits 0..3; 2, 3 at 16..19
+        w |= ((y & 0xfu) | ((y >> 12) & 0xf0u)) << (8 * i);
+      }
+      if (vec) {
+        *reinterpret_cast<uint32_t*>(row + 4 * j) = w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) row[4 * j + i] = (uint8_t)(w >> (8 * i));
+      }
     }
   }
   if (p.codes3 != nullptr) {
+    // four bytes a thread: 20 trits in five word reads (past Keff the zeroed
+    // tail reads as t = 0, digit 1), each byte sum (t + 1) 3^i by Horner's rule;
+    // bytes past ceil(Keff / 5) up to the padded length are zero
     uint8_t* row = p.codes3 + n * p.ld3;
-    const int64_t nb = (Keff + 4) / 5, padded = (nb + 15) / 16 * 16;
-    for (int64_t j = threadIdx.x; j < padded; j += kThreads) {
-      uint32_t b = 0;
-      if (j < nb) {
-        uint32_t pw = 1;
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.codes3) | (uintptr_t)p.ld3) & 3u) == 0;
+    const int nb = (int)((Keff + 4) / 5), padded = (nb + 15) / 16 * 16;
+    for (int j = threadIdx.x; j < padded / 4; j += kThreads) {
+      uint32_t w = 0;
+      if (4 * j < nb) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(trits + 20 * j);
+        uint32_t c[5];
 #pragma unroll
-        for (int i = 0; i < 5; ++i) {
-          const int64_t k = 5 * j + i;
-          b += (k < Keff ? (uint32_t)(trits[k] + 1) : 1u) * pw;
-          pw *= 3;
+        for (int i = 0; i < 5; ++i) c[i] = __vadd4(src[i], 0x01010101u);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          if (4 * j + b >= nb) continue;
+          uint32_t v = 0;
+#pragma unroll
+          for (int i = 4; i >= 0; --i) {
+            const int e = 5 * b + i;  // code e of the 20
+            v = 3u * v + ((c[e >> 2] >> (8 * (e & 3))) & 0xffu);
+          }
+          w |= v << (8 * b);
         }
       }
-      row[j] = (uint8_t)b;
+      if (vec) {
+        *reinterpret_cast<uint32_t*>(row + 4 * j) = w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) row[4 * j + i] = (uint8_t)(w >> (8 * i));
+      }
     }
   }
   pdl_launch_dependents();
@@ -187,7 +222,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize_layout(const LParams p) {
 
 size_t quantize_layout_smem(int64_t K, int residual) {
   const int64_t Keff = residual ? 2 * K : K;
-  return (size_t)((Keff + 15) / 16 * 16);  // the row's trits
+  return (size_t)((Keff + kTritTail + 15) / 16 * 16);  // the row's trits and a zero tail
 }
 
 cudaError_t launch_quantize_layout(const void* W, int wt, int64_t N, int64_t K, int64_t ldw, int block, int group,
