@@ -53,28 +53,44 @@ struct LParams {
 
 // Block transform of the lane's 8 weights (elements 8 lane .. 8 lane + 7 of
 // the span): stages h = 1, 2, 4 in the lane, h = 8 .. block / 2 with lane
-// l ^ (h / 8), then * c.
+// l ^ (h / 8), then * c; from h = 2 on in f32x2 pairs (elements 2i, 2i + 1),
+// each half rounded as the scalar operation.  A cross-lane step is
+// fma(+-1, own, other): other + own in the lower lane, other - own in the
+// upper, one rounding each as the add or subtract it stands for.
 __device__ __forceinline__ void fwht_lanes(float v[8], int block, float c, int lane) {
 #pragma unroll
-  for (int h = 1; h < 8; h <<= 1) {
+  for (int j = 0; j < 8; j += 2) {  // h = 1
+    const float a = v[j], b = v[j + 1];
+    v[j] = __fadd_rn(a, b);
+    v[j + 1] = __fsub_rn(a, b);
+  }
+  uint64_t q[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j & h) continue;
-      const float a = v[j], b = v[j + h];
-      v[j] = __fadd_rn(a, b);
-      v[j + h] = __fsub_rn(a, b);
+  for (int i = 0; i < 4; ++i) q[i] = f2_pack(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int hp = 1; hp < 4; hp <<= 1) {  // h = 2, 4 on pairs
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (i & hp) continue;
+      const uint64_t a = q[i], b = q[i + hp];
+      q[i] = f2_add(a, b);
+      q[i + hp] = f2_sub(a, b);
     }
   }
   for (int m = 1; 8 * m < block; m <<= 1) {
-    const bool up = (lane & m) != 0;  // this lane holds the upper elements i + h
+    const float sgn = (lane & m) ? -1.0f : 1.0f;  // the upper lane holds elements i + h
+    const uint64_t sg = f2_pack(sgn, sgn);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float o = __shfl_xor_sync(kFull, v[j], m);
-      v[j] = up ? __fsub_rn(o, v[j]) : __fadd_rn(v[j], o);
+    for (int i = 0; i < 4; ++i) {
+      float lo, hi;
+      f2_unpack(q[i], lo, hi);
+      const float olo = __shfl_xor_sync(kFull, lo, m), ohi = __shfl_xor_sync(kFull, hi, m);
+      q[i] = f2_fma(sg, q[i], f2_pack(olo, ohi));
     }
   }
+  const uint64_t c2 = f2_pack(c, c);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], c);
+  for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(q[i], c2), v[2 * i], v[2 * i + 1]);
 }
 
 // fp16 scale of the group of g values this lane's 8 belong to: halving-tree
@@ -82,18 +98,23 @@ __device__ __forceinline__ void fwht_lanes(float v[8], int block, float c, int l
 // forming the sum; levels 4, 2, 1 in the lane), times 1/g (exact).  Every
 // lane of the group returns it.
 __device__ __forceinline__ uint16_t group_scale_lanes(const float v[8], int g) {
-  float s[8];
+  uint64_t s2[4];  // |v| of elements 2i, 2i + 1 as f32x2 pairs
 #pragma unroll
-  for (int j = 0; j < 8; ++j) s[j] = fabsf(v[j]);
+  for (int i = 0; i < 4; ++i) s2[i] = f2_pack(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
   for (int m = g / 16; m >= 1; m >>= 1) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s[j] = __fadd_rn(s[j], __shfl_xor_sync(kFull, s[j], m));
+    for (int i = 0; i < 4; ++i) {
+      float lo, hi;
+      f2_unpack(s2[i], lo, hi);
+      s2[i] = f2_add(s2[i], f2_pack(__shfl_xor_sync(kFull, lo, m), __shfl_xor_sync(kFull, hi, m)));
+    }
   }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) s[j] = __fadd_rn(s[j], s[j + 4]);
-  s[0] = __fadd_rn(s[0], s[2]);
-  s[1] = __fadd_rn(s[1], s[3]);
-  s[0] = __fadd_rn(s[0], s[1]);
+  s2[0] = f2_add(s2[0], s2[2]);  // level 4: sums 0, 1 and (below) 2, 3
+  s2[1] = f2_add(s2[1], s2[3]);
+  s2[0] = f2_add(s2[0], s2[1]);  // level 2: sums 0, 1
+  float s0, s1;
+  f2_unpack(s2[0], s0, s1);
+  float s[1] = {__fadd_rn(s0, s1)};  // level 1
   const float mean = __fmul_rn(s[0], 1.0f / (float)g);
   return __half_as_ushort(__float2half_rn(mean));
 }
@@ -120,7 +141,8 @@ __global__ void __launch_bounds__(kThreads) k_quantize_layout(const LParams p) {
   // the tail past the row's trits reads as t = 0 in the base-3 packing
   if (threadIdx.x < kTritTail) trits[Keff + threadIdx.x] = 0;
   const int64_t n = blockIdx.x;
-  const int64_t G = p.K / p.group;
+  const int lgg = p.group == 256 ? 8 : 7;  // group 128 or 256: shifts, not 64-bit divisions
+  const int64_t G = p.K >> lgg;
   const float cb = p.block == 64 ? 0.125f : (p.block == 256 ? 0.0625f : kInvSqrt128);
   pdl_wait();
   for (int64_t k0 = (int64_t)warp * kSpan; k0 < p.K; k0 += (int64_t)kWarps * kSpan) {
@@ -138,10 +160,10 @@ __global__ void __launch_bounds__(kThreads) k_quantize_layout(const LParams p) {
       const uint16_t* w = static_cast<const uint16_t*>(p.W) + n * p.ldw + kl;
       bf16x8_to_f32(live ? ld_in_u4(w) : make_uint4(0, 0, 0, 0), v);
     }
-    const bool first = live && (kl % p.group) == 0;  // the lane that stores its group's scale
+    const bool first = live && (kl & (p.group - 1)) == 0;  // the lane that stores its group's scale
     fwht_lanes(v, p.block, cb, lane);
     const uint16_t sb = group_scale_lanes(v, p.group);
-    if (first) p.scales[n * p.lds + kl / p.group] = sb;
+    if (first) p.scales[n * p.lds + (kl >> lgg)] = sb;
     int t[8];
     const uint2 tw = ternarise8(v, sb, t);
     if (live) *reinterpret_cast<uint2*>(trits + kl) = tw;
@@ -152,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize_layout(const LParams p) {
     for (int j = 0; j < 8; ++j) v[j] = t[j] == 0 ? v[j] : __fsub_rn(v[j], __fmul_rn(sc, (float)t[j]));
     fwht_lanes(v, p.block, cb, lane);
     const uint16_t sb2 = group_scale_lanes(v, p.group);
-    if (first) p.scales[n * p.lds + G + kl / p.group] = sb2;
+    if (first) p.scales[n * p.lds + G + (kl >> lgg)] = sb2;
     const uint2 tw2 = ternarise8(v, sb2, t);
     if (live) *reinterpret_cast<uint2*>(trits + p.K + kl) = tw2;
   }
