@@ -1259,14 +1259,15 @@ unsigned int take_fault_gemv() {
 // resident at once (one wave).  The choice minimises the cost model of the
 // busiest CTA (its stages -- 128 code bytes of one 128-row tile -- and its
 // prologue items) over kcl = 1, 2, 4, 8, ties going to fewer CTAs.  A
-// cluster of 3, 5, 6 or 7 (46, 28, 23, 15 resident on 152 SMs) replaces that
-// choice only when it costs at least 10 % less and gives the busiest CTA at
-// most one tile more, since the model leaves out what these cost beyond
-// their stages.  Measured: 5120x5120 (M = 1 .. 4) and 5120x27648 (M = 1)
-// gain from clusters of 6; 2048x2048 at M = 1 lost with them at a 4 % lower
-// cost, and 27648x5120 at M = 2 .. 16 with clusters of 5 (eight tiles a CTA
-// instead of three or six).  Returns false when no split fits in shared
-// memory.
+// cluster of 3, 6 or 7 (46, 23, 15 resident on 152 SMs) replaces that choice
+// only when it costs at least 10 % less and gives the busiest CTA at most one
+// tile more, since the model leaves out what these cost beyond their stages.
+// Measured: 5120x5120 (M = 1 .. 4) and 5120x27648 (M = 1) gain from clusters
+// of 6 (5120x5120 also from 3, less); 2048x2048 at M = 1 lost with 6 at a
+// 4 % lower modelled cost.  Clusters of 5 are left out: they lost wherever
+// measured (5120x5120 in the decode step, 27648x5120 at M = 2 .. 16), below
+// the power-of-two plans they replaced.  Returns false when no split fits in
+// shared memory.
 bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* clusters_out, bool all_rows) {
   if (N <= 0 || K <= 0 || K % 128 != 0 || M < 1 || M > 16) return false;
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3 && fmt != kFmtSparse24) return false;
@@ -1280,8 +1281,8 @@ bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* c
   int64_t best = 0, best_kcl = 0, best_c = 0, best_t = 0, best_p = 0;
   if (G * kMaxCluster >= (int64_t(1) << 31) || T >= (int64_t(1) << 31)) return false;  // the kernel's 32-bit slice and tile arithmetic
   const int64_t most = b3 ? (G + gs - 1) / gs : (sp ? G / 2 : G);  // a group (2-bit), pair (2:4) or stage (base-3) per rank
-  static constexpr int kOrder[kMaxCluster] = {1, 2, 4, 8, 3, 5, 6, 7};
-  for (int i = 0; i < kMaxCluster; ++i) {
+  static constexpr int kOrder[] = {1, 2, 4, 8, 3, 6, 7};
+  for (int i = 0; i < (int)(sizeof(kOrder) / sizeof(kOrder[0])); ++i) {
     const int64_t kcl = kOrder[i];
     const bool pow2 = i < 4;
     if (kcl > most) continue;
