@@ -177,7 +177,8 @@ TQ_API tq_status tq_gemv_rotate_next(const uint8_t *codes, int64_t ldc, int fmt,
 /* Which kernel tq_gemv runs for a shape (introspection; launches nothing):
  *   TQ_GEMV_TENSOR_MEMORY  2-bit or base-3 codes, any M, when one CTA's share
  *                          of the rotated activations fits in shared memory
- *                          (2-bit: K up to about 140 thousand at M <= 2, 35
+ *                          (a K slice of up to 16 CTAs of a cluster; 2-bit:
+ *                          K up to about 280 thousand at M <= 2, 150
  *                          thousand at M = 16; base-3 about two thirds of
  *                          that; when the rows of x do not fit one launch
  *                          they are split evenly over up to four launches):

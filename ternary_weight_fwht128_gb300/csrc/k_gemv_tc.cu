@@ -188,8 +188,10 @@ __device__ __forceinline__ void piece_slot(int m, int q, int& pass, int& row) {
 
 int variant_of(int64_t M) { return M <= 2 ? 1 : M <= 5 ? 2 : M <= 8 ? 3 : 4; }
 
-// Largest cluster (K split) the planner uses: the portable limit
-constexpr int kMaxCluster = 8;
+// Largest cluster (K split) the planner uses: 16, a non-portable size (the
+// kernels opt in before such a launch), taken only when no cluster of at most
+// 8 -- the portable limit -- fits the activations of one launch
+constexpr int kMaxPortable = 8, kMaxCluster = 16;
 
 // Rows of a 128-row tile each cluster rank reduces (the last rank: the rest)
 __host__ __device__ constexpr int rows_per_rank(int kcl) { return (128 + kcl - 1) / kcl; }
@@ -1187,6 +1189,11 @@ int max_active_clusters(int kcl) {
   if (cudaFuncSetAttribute(k_gemv_tc<1, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return 0;
+  if (kcl > kMaxPortable &&
+      cudaFuncSetAttribute(k_gemv_tc<1, false, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(device_sm_count() * kcl));
   cfg.blockDim = dim3(kThreads);
@@ -1218,6 +1225,14 @@ cudaError_t launch_v(const CUtensorMap& map, const Params& p, size_t smem, cudaS
     if (e != cudaSuccess) return e;
     int cur = smem_set[dev].load(std::memory_order_acquire);
     while (cur < (int)smem && !smem_set[dev].compare_exchange_weak(cur, (int)smem)) {
+    }
+  }
+  if (p.kcl > kMaxPortable) {  // a non-portable cluster size: opt in once per device
+    static std::atomic<bool> np_set[64];
+    if (!np_set[dev].load(std::memory_order_acquire)) {
+      cudaError_t e = cudaFuncSetAttribute(k_gemv_tc<V, B3, LAYOUT, SP>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      np_set[dev].store(true, std::memory_order_release);
     }
   }
   cudaLaunchConfig_t cfg = {};
@@ -1266,8 +1281,11 @@ unsigned int take_fault_gemv() {
 // of 6 (5120x5120 also from 3, less); 2048x2048 at M = 1 lost with 6 at a
 // 4 % lower modelled cost.  Clusters of 5 are left out: they lost wherever
 // measured (5120x5120 in the decode step, 27648x5120 at M = 2 .. 16), below
-// the power-of-two plans they replaced.  Returns false when no split fits in
-// shared memory.
+// the power-of-two plans they replaced.  When no cluster of at most 8 fits the
+// activations in shared memory, a cluster of 16 (non-portable; 7 resident)
+// gives each CTA a sixteenth of K, so that one launch still takes all rows of
+// x (5120x27648 at M = 16 instead of two launches).  Returns false when no
+// split fits in shared memory.
 bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* clusters_out, bool all_rows) {
   if (N <= 0 || K <= 0 || K % 128 != 0 || M < 1 || M > 16) return false;
   if (fmt != TQ_PACK_2BIT && fmt != TQ_PACK_BASE3 && fmt != kFmtSparse24) return false;
@@ -1281,12 +1299,15 @@ bool plan_gemv_tc(int64_t N, int64_t K, int64_t M, int fmt, int* kcl_out, int* c
   int64_t best = 0, best_kcl = 0, best_c = 0, best_t = 0, best_p = 0;
   if (G * kMaxCluster >= (int64_t(1) << 31) || T >= (int64_t(1) << 31)) return false;  // the kernel's 32-bit slice and tile arithmetic
   const int64_t most = b3 ? (G + gs - 1) / gs : (sp ? G / 2 : G);  // a group (2-bit), pair (2:4) or stage (base-3) per rank
-  static constexpr int kOrder[] = {1, 2, 4, 8, 3, 6, 7};
-  for (int i = 0; i < (int)(sizeof(kOrder) / sizeof(kOrder[0])); ++i) {
+  // the last entry, 16, is tried only when none of the others fits
+  static constexpr int kOrder[] = {1, 2, 4, 8, 3, 6, 7, 16};
+  constexpr int kOrders = (int)(sizeof(kOrder) / sizeof(kOrder[0]));
+  for (int i = 0; i < kOrders; ++i) {
     const int64_t kcl = kOrder[i];
-    const bool pow2 = i < 4;
+    const bool pow2 = i < 4 || i == kOrders - 1;
     if (kcl > most) continue;
-    if (!pow2 && best_kcl == 0) break;  // the other sizes only refine a plan of the first four
+    // 3, 6 and 7 refine a plan of the first four; 16 is the last resort
+    if (i == kOrders - 1 ? best_kcl != 0 : (!pow2 && best_kcl == 0)) continue;
     int64_t c = max_active_clusters((int)kcl);
     if (c > sms / kcl) c = sms / kcl;
     if (c > T) c = T;

@@ -58,7 +58,7 @@ def test_gemv_stall_reports_timeout_then_recovers(N, K, M, fmt):
 
 def test_gemv_stall_needs_the_tensor_memory_kernel():
     """The mma.sync kernel has no waits to stall: the flag is refused there."""
-    N, K, M = 96, 131072, 16
+    N, K, M = 96, 262144, 16
     assert tq.gemv_path(N, K, M) == tq.TQ_GEMV_MMA_SYNC
     dummy = torch.empty(16, dtype=torch.uint8, device="cuda")
     p = dummy.data_ptr()

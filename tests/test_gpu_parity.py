@@ -298,6 +298,31 @@ def test_gemv_tc_cluster_sizes(orc, N, K, M):
         assert torch.equal(y, outs[0])
 
 
+@pytest.mark.parametrize("fmt", [tq.TQ_PACK_2BIT, tq.TQ_PACK_BASE3], ids=["2bit", "base3"])
+def test_gemv_tc_cluster_of_16(orc, fmt):
+    """5120x27648 at M = 16: no cluster of at most 8 CTAs fits the
+    activations of all rows in shared memory, so the 2-bit plan is one launch
+    on clusters of 16 (a non-portable size; 8 rows a rank); both formats
+    against the oracle on sampled rows and the tail, and 10 repeats
+    bit-identical to the first."""
+    N, K, M = 5120, 27648, 16
+    kcl, _, launches = tq.gemv_plan(N, K, M, fmt)
+    if fmt == tq.TQ_PACK_2BIT:
+        assert (kcl, launches) == (16, 1)
+    rng = np.random.default_rng(97)
+    rows = np.unique(np.concatenate([rng.choice(N, size=32, replace=False), np.arange(N - 130, N)]))
+    _gemv_case(orc, N, K, M, seed=98, fmt=fmt, rows=rows)
+    W = synth.weights(N, K, 99, dtype="bf16")
+    c2, c3, s = tq.quantize_pack(to_dev_bf16(W), fmt)
+    codes = c2 if fmt == tq.TQ_PACK_2BIT else c3
+    x = to_dev_bf16(synth.activations(M, K, 100))
+    outs = [tq.gemv(codes, s, x, K, fmt, weights_ready=True) for _ in range(10)]
+    torch.cuda.synchronize()
+    tq.device_fault()
+    for y in outs[1:]:
+        assert torch.equal(y, outs[0])
+
+
 @pytest.mark.parametrize("N,K", [(5120, 5120), (5120, 1536), (2560, 2560), (2048, 3072)])
 def test_gemv_rotate_next_cluster_sizes(orc, N, K):
     """The chained form (rank 0 adds the partial sums of all 128 rows of
@@ -339,7 +364,7 @@ def test_gemv_tc_base3(orc, N, K, M):
 def test_gemv_mma_sync_fallback_base3(orc):
     """Base-3 codes whose K slice of B does not fit shared memory even for
     a quarter of the rows of x take the mma.sync kernel."""
-    N, K, M = 96, 131072, 16
+    N, K, M = 96, 262144, 16
     assert tq.gemv_path(N, K, M, tq.TQ_PACK_BASE3) == tq.TQ_GEMV_MMA_SYNC
     _gemv_case(orc, N, K, M, seed=78, fmt=tq.TQ_PACK_BASE3)
 
@@ -391,7 +416,7 @@ def test_gemv_tc_reads_no_stale_shared_memory(N, K, M):
 def test_gemv_mma_sync_fallback_2bit(orc):
     """2-bit codes whose K slice of B does not fit shared memory even for a
     quarter of the rows of x take the mma.sync kernel."""
-    N, K, M = 96, 131072, 16
+    N, K, M = 96, 262144, 16
     assert tq.gemv_path(N, K, M) == tq.TQ_GEMV_MMA_SYNC
     _gemv_case(orc, N, K, M, seed=77)
 
