@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(256) k_gemm_fixup(const float* __restrict__ pa
   pdl_launch_dependents();
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once (no link to libcuda).
+// cuTensorMapEncodeTiled from the CUDA driver, looked up once (no link to libcuda).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
