@@ -41,9 +41,9 @@ LAYER_SHAPES = [("h2h_a", HIDDEN, HIDDEN), ("h2h_b", HIDDEN, HIDDEN), ("gate_up"
 METRIC = "ternary GEMV packed-weight HBM GB/s (% of peak); prefill GEMM TFLOP/s"
 # DRAM bytes per algorithmic byte of k_gemv_tc, from an ncu capture of one
 # 27648x5120 launch of the current kernel: dram__bytes_read.sum +
-# dram__bytes_write.sum = 37,668,352 + 0 for 37,601,280 packed bytes
+# dram__bytes_write.sum = 37,666,560 + 0 for 37,601,280 packed bytes
 # (every weight byte read once).
-GEMV_TC_TRAFFIC_RATIO = 37668352 / 37601280
+GEMV_TC_TRAFFIC_RATIO = 37666560 / 37601280
 WORKLOAD = ("decode GEMV M=1, 2-bit codes, 64-layer stack of 27B-class shapes "
             "{5120x5120 x2, 27648x5120 x2, 5120x27648} per layer; gate and up (the two 27648x5120, same x) "
             "stored as one 55296x5120 matrix and run as one GEMV (256 launches, FWHT-128 fused)")
