@@ -194,9 +194,10 @@ enum { TQ_GEMV_TENSOR_MEMORY = 1, TQ_GEMV_MMA_SYNC = 2, TQ_GEMV_CUDA_CORES = 3 }
 TQ_API int tq_gemv_path(int64_t N, int64_t K, int64_t M, int fmt);
 
 /* The tensor-memory kernel's work split for a shape (introspection; launches
- * nothing).  *ctas_per_cluster (1 .. 8): the CTAs of a thread-block cluster
- * that split the K groups of its tiles and add their partial sums in
- * distributed shared memory; *clusters: the clusters of a launch, each
+ * nothing).  *ctas_per_cluster (1, 2, 3, 4, 6, 7, 8, or 16 where no smaller
+ * cluster fits the activations): the CTAs of a thread-block cluster that
+ * split the K groups of its tiles and add their partial sums in distributed
+ * shared memory; *clusters: the clusters of a launch, each
  * owning a range of 128-row tiles; *launches (1 .. 4): the launches the rows
  * of x are split over (the split reported is the first launch's, which takes
  * M / launches rows, rounded down).  chained != 0 plans tq_gemv_rotate_next
